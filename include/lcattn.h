@@ -1,0 +1,183 @@
+/*
+ * lcattn -- fused masked scaled-dot-product attention for GB300 (sm_103a).
+ *
+ * C ABI of the library liblcattn.so.  The operator is the one every kernel on
+ * the pages benchmarks ("Long-Context Attention Benchmark: From Kernel
+ * Efficiency to Distributed Context Parallelism", xllm-io blog review, sections
+ * "密集注意力内核" and "稀疏注意力内核"): softmax attention under a mask, forward
+ * and backward, bf16 inputs, head dim 128, MHA and GQA (section "实验设置").
+ *
+ *   S = scale * Q K^T,  P = row softmax over the allowed keys,  O = P V,
+ *   LSE_i = ln sum_{j allowed} exp(S_ij)   (-inf for a row that allows nothing)
+ *
+ * The mask reaches the kernels as one of two descriptors:
+ *   - column bounds (the column-wise representation the pages credit to
+ *     FlashMask, section "掩码支持"): for every key column j, the allowed query
+ *     rows are the union of two half-open intervals [a0,b0) and [a1,b1).  All
+ *     twelve static mask families of the pages (section "注意力掩码模式") fit it.
+ *   - block map (the dynamic Uniform Block / Variable Block masks, same
+ *     section): a keep byte per (query block, key block) and query head, with
+ *     arbitrary block boundaries.
+ *
+ * Conventions for every call:
+ *   - Pointers marked "device" point to GPU memory, owned by the caller.  The
+ *     library allocates nothing, frees nothing and keeps no state between calls
+ *     besides cached kernel attributes.
+ *   - Calls are asynchronous on `stream` (NULL = the legacy default stream); the
+ *     library never synchronises except in lcattn_read_status.
+ *   - Arguments are validated on the host before anything is launched; an
+ *     invalid call returns a negative status and launches nothing.
+ *   - Tensors are bf16 (except LSE / D / accumulators, fp32) with the last
+ *     dimension (head dim, 128 elements) contiguous; the (batch, sequence,
+ *     head) strides are given in elements and must be multiples of 8 (16
+ *     bytes), and base pointers must be 16-byte aligned.
+ *   - Query head h reads KV head h / (Hq / Hkv) (contiguous GQA groups).
+ */
+#ifndef LCATTN_H_
+#define LCATTN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* lcattn_stream_t; /* same handle as cudaStream_t */
+
+/* ---- status codes ------------------------------------------------------ */
+#define LCATTN_OK 0
+#define LCATTN_ERR_INVALID_ARG (-1)   /* null pointer, bad size, bad stride      */
+#define LCATTN_ERR_UNSUPPORTED (-2)   /* head dim != 128, Hq % Hkv != 0, alignment */
+#define LCATTN_ERR_WORKSPACE (-3)     /* buffer smaller than the size query says  */
+#define LCATTN_ERR_CUDA (-4)          /* a CUDA call or launch failed             */
+#define LCATTN_ERR_DEVICE_TIMEOUT (-5)/* a kernel gave up waiting (bounded wait)  */
+#define LCATTN_ERR_DEVICE_MASK (-6)   /* block offsets not increasing from 0 to S */
+
+/* ---- problem shape ------------------------------------------------------ */
+typedef struct lcattn_shape {
+  int64_t B;    /* batch                                                    */
+  int64_t Sq;   /* query length                                             */
+  int64_t Sk;   /* key length                                               */
+  int64_t Hq;   /* query heads                                              */
+  int64_t Hkv;  /* key/value heads; Hq % Hkv == 0                          */
+  int64_t D;    /* head dim; must be 128                                    */
+  /* element strides of (batch, sequence, head); the head dim is contiguous.
+   * dO and dQ use q_stride's layout rules with o_stride / q_stride:
+   *   O and dO share o_stride, Q and dQ share q_stride,
+   *   K and dK share k_stride, V and dV share v_stride.                    */
+  int64_t q_stride[3];
+  int64_t k_stride[3];
+  int64_t v_stride[3];
+  int64_t o_stride[3];
+} lcattn_shape;
+
+/* ---- mask descriptor ----------------------------------------------------- */
+#define LCATTN_MASK_COLBOUNDS 1
+#define LCATTN_MASK_BLOCKMAP 2
+
+typedef struct lcattn_mask_desc {
+  int32_t kind;
+  /* kind 1 (device) int32 [B][Sk][4] = {a0, b0, a1, b1}: query row i may attend
+   * key column j iff a0 <= i < b0 or a1 <= i < b1.  Any int32 values are
+   * allowed; intervals are clipped to [0, Sq).                              */
+  const int32_t* col_bounds;
+  /* kind 2 (device) uint8 [B][Hq][nQb][nKb]: nonzero = keep the block.       */
+  const uint8_t* block_map;
+  /* kind 2 (device) int32 [nQb+1] / [nKb+1]: block boundaries, nondecreasing,
+   * first 0, last Sq (resp. Sk); checked on the device by the mask compiler. */
+  const int32_t* q_block_offs;
+  const int32_t* k_block_offs;
+  int32_t nQb;
+  int32_t nKb;
+} lcattn_mask_desc;
+
+/* Tile classes written by the mask compiler (one byte per 128x128 tile). */
+#define LCATTN_TILE_EMPTY 0
+#define LCATTN_TILE_FULL 1
+#define LCATTN_TILE_PARTIAL 2
+
+/* Tile geometry: 128 query rows x 128 key columns. */
+#define LCATTN_BLOCK_M 128
+#define LCATTN_BLOCK_N 128
+
+/* ---- tile metadata -------------------------------------------------------
+ * The mask compiler turns a descriptor into per-tile classes and compacted
+ * tile lists (section "掩码支持": FlashMask's column-wise representation exists to
+ * skip masked-out work; here the skip decision is made once per 128x128 tile).
+ * Layout of the buffer (all offsets from lcattn_tile_meta_layout):
+ *   status  int32[4]                     device status words (0 = OK)
+ *   class   uint8 [B][nH][nQt][nKt]      LCATTN_TILE_* per tile
+ *   fwd_cnt int32 [B][nH][nQt]           non-empty key tiles per query tile
+ *   fwd_lst int32 [B][nH][nQt][nKt]      (kt << 1) | partial, kt increasing
+ *   fwd_ord int32 [B][nH][nQt]           query tiles by fwd_cnt descending
+ *   bwd_cnt int32 [B][nH][nKt]           non-empty query tiles per key tile
+ *   bwd_lst int32 [B][nH][nKt][nQt]      (qt << 1) | partial, qt increasing
+ *   bwd_ord int32 [B][nH][nKt]           key tiles by bwd_cnt descending
+ * where nH = 1 for column bounds (the mask is the same for every head) and
+ * nH = Hq for block maps.                                                    */
+typedef struct lcattn_tile_meta_layout {
+  int64_t nQt, nKt, nH, B;
+  int64_t off_status, off_class, off_fwd_cnt, off_fwd_lst, off_fwd_ord;
+  int64_t off_bwd_cnt, off_bwd_lst, off_bwd_ord;
+  int64_t total_bytes;
+} lcattn_tile_meta_layout;
+
+/* Fills *out for this shape and descriptor.  Returns a status. */
+int lcattn_tile_meta_layout_of(const lcattn_shape* shape, const lcattn_mask_desc* mask,
+                               lcattn_tile_meta_layout* out);
+
+/* Bytes of device memory lcattn_mask_compile needs for `tile_meta`. */
+size_t lcattn_tile_meta_size(const lcattn_shape* shape, const lcattn_mask_desc* mask);
+
+/* Mask compiler.  Classifies every (query tile, key tile) pair as EMPTY, FULL
+ * or PARTIAL, builds the forward (per query tile) and backward (per key tile)
+ * lists of non-empty tiles and the longest-first orders.  `tile_meta` (device,
+ * `bytes` >= lcattn_tile_meta_size) is overwritten.  The result depends only
+ * on the shape's sizes and the descriptor, so one compile serves any number of
+ * forward and backward calls with the same mask.                           */
+int lcattn_mask_compile(const lcattn_shape* shape, const lcattn_mask_desc* mask,
+                        void* tile_meta, size_t bytes, lcattn_stream_t stream);
+
+/* Forward.  q [B][Sq][Hq][128], k/v [B][Sk][Hkv][128] bf16 (device) ->
+ * o [B][Sq][Hq][128] bf16 and lse [B][Hq][Sq] fp32 (natural log; -inf for a
+ * row with no allowed key, whose O row is 0).  `tile_meta` must come from
+ * lcattn_mask_compile with the same shape sizes and descriptor, and `mask`
+ * is needed again because partial tiles evaluate the mask per element.     */
+int lcattn_fwd(const lcattn_shape* shape, const void* q, const void* k, const void* v,
+               const void* tile_meta, const lcattn_mask_desc* mask, float scale, void* o,
+               float* lse, lcattn_stream_t stream);
+
+/* Workspace (device bytes) lcattn_bwd needs: D = rowsum(dO * O) fp32
+ * [B][Hq][Sq] and the fp32 dQ accumulator [B][Sq][Hq][128].                */
+size_t lcattn_bwd_workspace_size(const lcattn_shape* shape);
+
+/* Backward of L = sum(O * dO).  Inputs as for lcattn_fwd plus o, d_o (bf16,
+ * o_stride) and lse from the forward.  Outputs dq (bf16, q_stride), dk
+ * (k_stride) and dv (v_stride); dk/dv hold the sum over each GQA group.  The
+ * three steps run in order on `stream`: D pre-pass (also zeroes the dQ
+ * accumulator), one pass per key tile for dK/dV that adds dQ partials into the
+ * accumulator, and the dQ conversion to bf16.                              */
+int lcattn_bwd(const lcattn_shape* shape, const void* q, const void* k, const void* v,
+               const void* o, const void* d_o, const float* lse, const void* tile_meta,
+               const lcattn_mask_desc* mask, float scale, void* dq, void* dk, void* dv,
+               void* workspace, size_t workspace_bytes, lcattn_stream_t stream);
+
+/* Synchronises `stream`, then returns the first nonzero device status word of
+ * `tile_meta` (LCATTN_ERR_DEVICE_*), or LCATTN_OK.  Clears nothing.          */
+int lcattn_read_status(const void* tile_meta, lcattn_stream_t stream);
+
+/* Zeroes the device status words of `tile_meta` (asynchronously). */
+int lcattn_clear_status(void* tile_meta, lcattn_stream_t stream);
+
+/* Static string for a status code. */
+const char* lcattn_status_string(int status);
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+int lcattn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LCATTN_H_ */

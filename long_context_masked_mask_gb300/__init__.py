@@ -1,0 +1,296 @@
+"""GB300-native fused masked attention (forward and backward), bf16, head dim 128.
+
+Python binding of the C-ABI library ``liblcattn.so`` (declared in
+``include/lcattn.h``).  This module only marshals arguments: every step of the
+attention path (mask compilation, forward, backward) runs in the library's CUDA
+kernels.  PyTorch provides device memory and the current stream.
+
+The functions carry the C names:
+
+* :func:`lcattn_mask_compile` -- descriptor -> tile classes and tile lists
+* :func:`lcattn_fwd` -- O and LSE
+* :func:`lcattn_bwd` -- dQ, dK, dV
+* :func:`lcattn_read_status` -- device status words (bounded-wait expiry etc.)
+
+plus :class:`DeviceMask`, which uploads a host-built mask descriptor
+(see :mod:`.masks`).
+
+There is no fallback: importing this module fails when the library is missing,
+and every call fails when there is no CUDA device.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+from typing import Optional, Tuple
+
+import numpy as np
+import torch
+
+from . import masks
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "liblcattn.so")
+
+LCATTN_OK = 0
+LCATTN_ERR_INVALID_ARG = -1
+LCATTN_ERR_UNSUPPORTED = -2
+LCATTN_ERR_WORKSPACE = -3
+LCATTN_ERR_CUDA = -4
+LCATTN_ERR_DEVICE_TIMEOUT = -5
+LCATTN_ERR_DEVICE_MASK = -6
+LCATTN_MASK_COLBOUNDS = 1
+LCATTN_MASK_BLOCKMAP = 2
+LCATTN_TILE_EMPTY, LCATTN_TILE_FULL, LCATTN_TILE_PARTIAL = 0, 1, 2
+BLOCK_M = BLOCK_N = 128
+
+# Every entry point include/lcattn.h declares.
+EXPORTED = (
+    "lcattn_tile_meta_layout_of", "lcattn_tile_meta_size", "lcattn_mask_compile", "lcattn_fwd",
+    "lcattn_bwd_workspace_size", "lcattn_bwd", "lcattn_read_status", "lcattn_clear_status",
+    "lcattn_status_string", "lcattn_version",
+)
+
+
+class lcattn_shape(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int64), ("Sq", ctypes.c_int64), ("Sk", ctypes.c_int64),
+                ("Hq", ctypes.c_int64), ("Hkv", ctypes.c_int64), ("D", ctypes.c_int64),
+                ("q_stride", ctypes.c_int64 * 3), ("k_stride", ctypes.c_int64 * 3),
+                ("v_stride", ctypes.c_int64 * 3), ("o_stride", ctypes.c_int64 * 3)]
+
+
+class lcattn_mask_desc(ctypes.Structure):
+    _fields_ = [("kind", ctypes.c_int32), ("col_bounds", ctypes.c_void_p),
+                ("block_map", ctypes.c_void_p), ("q_block_offs", ctypes.c_void_p),
+                ("k_block_offs", ctypes.c_void_p), ("nQb", ctypes.c_int32), ("nKb", ctypes.c_int32)]
+
+
+class lcattn_tile_meta_layout(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int64) for n in (
+        "nQt", "nKt", "nH", "B", "off_status", "off_class", "off_fwd_cnt", "off_fwd_lst",
+        "off_fwd_ord", "off_bwd_cnt", "off_bwd_lst", "off_bwd_ord", "total_bytes")]
+
+
+class LcattnError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: {status_string(status)} ({status})")
+        self.status = status
+
+
+def _load():
+    if not os.path.exists(_LIB_PATH):
+        raise ImportError(
+            f"{_LIB_PATH} is missing; build it with "
+            "`python -m long_context_masked_mask_gb300.build` (needs nvcc for sm_103a)")
+    lib = ctypes.CDLL(_LIB_PATH)
+    P = ctypes.c_void_p
+    S = ctypes.POINTER(lcattn_shape)
+    M = ctypes.POINTER(lcattn_mask_desc)
+    sig = {
+        "lcattn_tile_meta_layout_of": (ctypes.c_int, [S, M, ctypes.POINTER(lcattn_tile_meta_layout)]),
+        "lcattn_tile_meta_size": (ctypes.c_size_t, [S, M]),
+        "lcattn_mask_compile": (ctypes.c_int, [S, M, P, ctypes.c_size_t, P]),
+        "lcattn_fwd": (ctypes.c_int, [S, P, P, P, P, M, ctypes.c_float, P, P, P]),
+        "lcattn_bwd_workspace_size": (ctypes.c_size_t, [S]),
+        "lcattn_bwd": (ctypes.c_int, [S, P, P, P, P, P, P, P, M, ctypes.c_float, P, P, P, P,
+                                      ctypes.c_size_t, P]),
+        "lcattn_read_status": (ctypes.c_int, [P, P]),
+        "lcattn_clear_status": (ctypes.c_int, [P, P]),
+        "lcattn_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+        "lcattn_version": (ctypes.c_int, []),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    return lib
+
+
+_lib = _load()
+
+
+def library():
+    """The loaded ctypes library."""
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return _lib.lcattn_status_string(int(status)).decode()
+
+
+def _check(status: int, what: str):
+    if status != LCATTN_OK:
+        raise LcattnError(status, what)
+
+
+def _stream_ptr(stream: Optional[torch.cuda.Stream]) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return int(s.cuda_stream)
+
+
+def _bshd_strides(t: torch.Tensor):
+    if t.dim() != 4 or t.stride(3) != 1:
+        raise ValueError("expected a [B, S, H, 128] tensor with a contiguous last dim")
+    return (t.stride(0), t.stride(1), t.stride(2))
+
+
+def make_shape(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
+               o: Optional[torch.Tensor] = None) -> lcattn_shape:
+    """lcattn_shape from [B, S, H, D] tensors (o defaults to q's layout)."""
+    B, Sq, Hq, D = q.shape
+    s = lcattn_shape()
+    s.B, s.Sq, s.Sk, s.Hq, s.Hkv, s.D = B, Sq, k.shape[1], Hq, k.shape[2], D
+    s.q_stride[:] = _bshd_strides(q)
+    s.k_stride[:] = _bshd_strides(k)
+    s.v_stride[:] = _bshd_strides(v)
+    s.o_stride[:] = _bshd_strides(o if o is not None else q)
+    return s
+
+
+class DeviceMask:
+    """A mask descriptor uploaded to the device, plus the host-side facts the
+    benchmark needs (allowed pair count).  Built from a mask spec with the
+    host builders of :mod:`.masks`; the same descriptor serves every batch
+    entry (it is replicated ``B`` times)."""
+
+    def __init__(self, spec, N: int, Hq: int, B: int = 1, device: str = "cuda"):
+        self.spec = spec
+        self.N, self.Hq, self.B = N, Hq, B
+        self.desc = lcattn_mask_desc()
+        if spec.kind in ("UNIFORM_BLOCK", "VARIABLE_BLOCK"):
+            keep, q_offs, k_offs = masks.block_map(spec, N, Hq)
+            self.pairs_per_batch = masks.allowed_pairs_from_blocks(keep, q_offs, k_offs)
+            self.block_map = torch.from_numpy(np.broadcast_to(keep, (B,) + keep.shape).copy()).to(device)
+            self.q_offs = torch.from_numpy(q_offs).to(device)
+            self.k_offs = torch.from_numpy(k_offs).to(device)
+            self.desc.kind = LCATTN_MASK_BLOCKMAP
+            self.desc.block_map = self.block_map.data_ptr()
+            self.desc.q_block_offs = self.q_offs.data_ptr()
+            self.desc.k_block_offs = self.k_offs.data_ptr()
+            self.desc.nQb = keep.shape[1]
+            self.desc.nKb = keep.shape[2]
+        else:
+            cb = masks.col_bounds(spec, N)
+            self.pairs_per_batch = Hq * masks.allowed_pairs_from_bounds(cb, N)
+            self.col_bounds = torch.from_numpy(np.broadcast_to(cb, (B,) + cb.shape).copy()).to(device)
+            self.desc.kind = LCATTN_MASK_COLBOUNDS
+            self.desc.col_bounds = self.col_bounds.data_ptr()
+
+    @property
+    def allowed_pairs(self) -> int:
+        """Allowed (query, key) pairs summed over batch and query heads."""
+        return self.B * self.pairs_per_batch
+
+
+def tile_meta_layout(shape: lcattn_shape, mask: DeviceMask) -> lcattn_tile_meta_layout:
+    L = lcattn_tile_meta_layout()
+    _check(_lib.lcattn_tile_meta_layout_of(ctypes.byref(shape), ctypes.byref(mask.desc),
+                                           ctypes.byref(L)), "lcattn_tile_meta_layout_of")
+    return L
+
+
+def lcattn_mask_compile(shape: lcattn_shape, mask: DeviceMask, tile_meta: Optional[torch.Tensor] = None,
+                        stream=None, device="cuda") -> torch.Tensor:
+    """Runs the mask compiler; returns the (uint8) tile-meta buffer."""
+    nbytes = _lib.lcattn_tile_meta_size(ctypes.byref(shape), ctypes.byref(mask.desc))
+    if nbytes == 0:
+        tile_meta_layout(shape, mask)  # raises with the reason
+    if tile_meta is None:
+        tile_meta = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    _check(_lib.lcattn_mask_compile(ctypes.byref(shape), ctypes.byref(mask.desc), tile_meta.data_ptr(),
+                                    tile_meta.numel(), _stream_ptr(stream)), "lcattn_mask_compile")
+    return tile_meta
+
+
+def lcattn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, mask: DeviceMask,
+               tile_meta: torch.Tensor, scale: Optional[float] = None,
+               o: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+               stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Forward: returns (O [B,Sq,Hq,128] bf16, LSE [B,Hq,Sq] fp32)."""
+    B, Sq, Hq, D = q.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty(B, Hq, Sq, dtype=torch.float32, device=q.device)
+    for t in (q, k, v, o):
+        if t.dtype != torch.bfloat16:
+            raise TypeError("q, k, v and o must be bf16")
+    shape = make_shape(q, k, v, o)
+    _check(_lib.lcattn_fwd(ctypes.byref(shape), q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                           tile_meta.data_ptr(), ctypes.byref(mask.desc), float(scale), o.data_ptr(),
+                           lse.data_ptr(), _stream_ptr(stream)), "lcattn_fwd")
+    return o, lse
+
+
+def lcattn_bwd_workspace_size(shape: lcattn_shape) -> int:
+    return int(_lib.lcattn_bwd_workspace_size(ctypes.byref(shape)))
+
+
+def lcattn_bwd(q, k, v, o, d_o, lse, mask: DeviceMask, tile_meta, scale: Optional[float] = None,
+               dq=None, dk=None, dv=None, workspace=None, stream=None):
+    """Backward: returns (dQ, dK, dV), bf16, laid out like q, k, v."""
+    D = q.shape[3]
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if d_o.stride() != o.stride():
+        raise ValueError("dO must have O's strides")
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    if dq.stride() != q.stride() or dk.stride() != k.stride() or dv.stride() != v.stride():
+        raise ValueError("gradients must have their inputs' strides")
+    shape = make_shape(q, k, v, o)
+    ws_bytes = lcattn_bwd_workspace_size(shape)
+    if workspace is None:
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device)
+    _check(_lib.lcattn_bwd(ctypes.byref(shape), q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                           d_o.data_ptr(), lse.data_ptr(), tile_meta.data_ptr(), ctypes.byref(mask.desc),
+                           float(scale), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
+                           workspace.data_ptr(), workspace.numel(), _stream_ptr(stream)), "lcattn_bwd")
+    return dq, dk, dv
+
+
+def lcattn_read_status(tile_meta: torch.Tensor, stream=None) -> int:
+    """Synchronises the stream and returns the first nonzero device status word."""
+    return int(_lib.lcattn_read_status(tile_meta.data_ptr(), _stream_ptr(stream)))
+
+
+def lcattn_clear_status(tile_meta: torch.Tensor, stream=None) -> None:
+    _check(_lib.lcattn_clear_status(tile_meta.data_ptr(), _stream_ptr(stream)), "lcattn_clear_status")
+
+
+def tile_classes(tile_meta: torch.Tensor, shape: lcattn_shape, mask: DeviceMask) -> torch.Tensor:
+    """View of the class bytes [B, nH, nQt, nKt] inside a compiled tile-meta buffer."""
+    L = tile_meta_layout(shape, mask)
+    n = L.B * L.nH * L.nQt * L.nKt
+    return tile_meta[L.off_class:L.off_class + n].view(L.B, L.nH, L.nQt, L.nKt)
+
+
+def tile_lists(tile_meta: torch.Tensor, shape: lcattn_shape, mask: DeviceMask):
+    """Views (fwd_cnt, fwd_lst, fwd_ord, bwd_cnt, bwd_lst, bwd_ord) of a tile-meta buffer."""
+    L = tile_meta_layout(shape, mask)
+    bh = L.B * L.nH
+
+    def view(off, *dims):
+        n = int(np.prod(dims)) * 4
+        return tile_meta[off:off + n].view(torch.int32).view(*dims)
+
+    return (view(L.off_fwd_cnt, bh, L.nQt), view(L.off_fwd_lst, bh, L.nQt, L.nKt),
+            view(L.off_fwd_ord, bh, L.nQt), view(L.off_bwd_cnt, bh, L.nKt),
+            view(L.off_bwd_lst, bh, L.nKt, L.nQt), view(L.off_bwd_ord, bh, L.nKt))
+
+
+def attention(q, k, v, spec, scale=None, d_o=None, stream=None):
+    """Convenience composition of the C calls: compile the mask, run the
+    forward, and (when ``d_o`` is given) the backward.  Returns a dict."""
+    B, N, Hq, _ = q.shape
+    mask = DeviceMask(spec, N, Hq, B, device=q.device)
+    shape = make_shape(q, k, v)
+    meta = lcattn_mask_compile(shape, mask, stream=stream, device=q.device)
+    o, lse = lcattn_fwd(q, k, v, mask, meta, scale, stream=stream)
+    out = {"o": o, "lse": lse, "mask": mask, "tile_meta": meta}
+    if d_o is not None:
+        out["dq"], out["dk"], out["dv"] = lcattn_bwd(q, k, v, o, d_o, lse, mask, meta, scale, stream=stream)
+    return out

@@ -1,0 +1,279 @@
+// Host layer of the C ABI declared in include/lcattn.h: argument validation,
+// TMA descriptor encoding, tile-metadata layout, and the launches of the mask
+// compiler, forward and backward kernels.  Allocates nothing.
+#include <cudaTypedefs.h>
+
+#include <cstring>
+
+#include "lcattn_internal.cuh"
+
+using namespace lcattn;
+
+namespace {
+
+constexpr int64_t kMaxSeq = int64_t(1) << 20;  // tile lists and orders use int32 / smem sorts
+
+int64_t align_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int validate_shape(const lcattn_shape* s) {
+  if (!s) return LCATTN_ERR_INVALID_ARG;
+  if (s->B < 1 || s->Sq < 1 || s->Sk < 1 || s->Hq < 1 || s->Hkv < 1) return LCATTN_ERR_INVALID_ARG;
+  if (s->Sq > kMaxSeq || s->Sk > kMaxSeq || s->B > 65535 || s->Hq > 65535)
+    return LCATTN_ERR_UNSUPPORTED;
+  if (s->D != kD) return LCATTN_ERR_UNSUPPORTED;
+  if (s->Hq % s->Hkv != 0) return LCATTN_ERR_UNSUPPORTED;
+  const int64_t* st[4] = {s->q_stride, s->k_stride, s->v_stride, s->o_stride};
+  for (auto x : st)
+    for (int i = 0; i < 3; ++i) {
+      if (x[i] < 0) return LCATTN_ERR_INVALID_ARG;
+      if (x[i] % 8 != 0) return LCATTN_ERR_UNSUPPORTED;  // 16-byte rows for TMA and vector I/O
+    }
+  // The head and sequence strides must at least separate rows.
+  for (auto x : st)
+    if (x[2] < kD || x[1] < kD) return LCATTN_ERR_INVALID_ARG;
+  return LCATTN_OK;
+}
+
+int validate_mask(const lcattn_shape* s, const lcattn_mask_desc* m) {
+  if (!m) return LCATTN_ERR_INVALID_ARG;
+  if (m->kind == LCATTN_MASK_COLBOUNDS) {
+    if (!m->col_bounds || !aligned16(m->col_bounds)) return LCATTN_ERR_INVALID_ARG;
+    return LCATTN_OK;
+  }
+  if (m->kind == LCATTN_MASK_BLOCKMAP) {
+    if (!m->block_map || !m->q_block_offs || !m->k_block_offs) return LCATTN_ERR_INVALID_ARG;
+    if (m->nQb < 1 || m->nKb < 1 || m->nQb > s->Sq || m->nKb > s->Sk) return LCATTN_ERR_INVALID_ARG;
+    return LCATTN_OK;
+  }
+  return LCATTN_ERR_INVALID_ARG;
+}
+
+int layout_of(const lcattn_shape* s, const lcattn_mask_desc* m, lcattn_tile_meta_layout* L) {
+  int st = validate_shape(s);
+  if (st) return st;
+  if ((st = validate_mask(s, m))) return st;
+  std::memset(L, 0, sizeof(*L));
+  L->B = s->B;
+  L->nQt = (s->Sq + kBM - 1) / kBM;
+  L->nKt = (s->Sk + kBN - 1) / kBN;
+  L->nH = m->kind == LCATTN_MASK_BLOCKMAP ? s->Hq : 1;
+  const int64_t bh = L->B * L->nH;
+  int64_t off = 0;
+  L->off_status = off; off = align_up(off + 16, 256);
+  L->off_class = off;   off = align_up(off + bh * L->nQt * L->nKt, 256);
+  L->off_fwd_cnt = off; off = align_up(off + 4 * bh * L->nQt, 256);
+  L->off_fwd_lst = off; off = align_up(off + 4 * bh * L->nQt * L->nKt, 256);
+  L->off_fwd_ord = off; off = align_up(off + 4 * bh * L->nQt, 256);
+  L->off_bwd_cnt = off; off = align_up(off + 4 * bh * L->nKt, 256);
+  L->off_bwd_lst = off; off = align_up(off + 4 * bh * L->nKt * L->nQt, 256);
+  L->off_bwd_ord = off; off = align_up(off + 4 * bh * L->nKt, 256);
+  L->total_bytes = off;
+  return LCATTN_OK;
+}
+
+ProblemDev problem_of(const lcattn_shape* s) {
+  ProblemDev p;
+  p.B = (int)s->B; p.Sq = (int)s->Sq; p.Sk = (int)s->Sk;
+  p.Hq = (int)s->Hq; p.Hkv = (int)s->Hkv; p.G = (int)(s->Hq / s->Hkv);
+  return p;
+}
+
+MaskDev mask_of(const lcattn_mask_desc* m) {
+  MaskDev d;
+  d.kind = m->kind;
+  d.col_bounds = reinterpret_cast<const int4*>(m->col_bounds);
+  d.block_map = m->block_map;
+  d.q_offs = m->q_block_offs;
+  d.k_offs = m->k_block_offs;
+  d.nQb = m->nQb;
+  d.nKb = m->nKb;
+  return d;
+}
+
+TileMetaDev meta_of(const lcattn_tile_meta_layout& L, const void* base) {
+  uint8_t* p = static_cast<uint8_t*>(const_cast<void*>(base));
+  TileMetaDev t;
+  t.status = reinterpret_cast<int32_t*>(p + L.off_status);
+  t.cls = p + L.off_class;
+  t.fwd_cnt = reinterpret_cast<int32_t*>(p + L.off_fwd_cnt);
+  t.fwd_lst = reinterpret_cast<int32_t*>(p + L.off_fwd_lst);
+  t.fwd_ord = reinterpret_cast<int32_t*>(p + L.off_fwd_ord);
+  t.bwd_cnt = reinterpret_cast<int32_t*>(p + L.off_bwd_cnt);
+  t.bwd_lst = reinterpret_cast<int32_t*>(p + L.off_bwd_lst);
+  t.bwd_ord = reinterpret_cast<int32_t*>(p + L.off_bwd_ord);
+  t.nQt = (int)L.nQt; t.nKt = (int)L.nKt; t.nH = (int)L.nH; t.B = (int)L.B;
+  return t;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// [B][S][H][128] bf16 with element strides (b, s, h): 4-D map with a
+// 64-element x 1 head x 128 row box and 128-byte swizzle (one K-major half
+// tile per copy).
+int encode_bshd(CUtensorMap* m, const void* ptr, int64_t B, int64_t S, int64_t H,
+                const int64_t st[3]) {
+  auto fn = encode_fn();
+  if (!fn) return LCATTN_ERR_CUDA;
+  cuuint64_t dims[4] = {(cuuint64_t)kD, (cuuint64_t)H, (cuuint64_t)S, (cuuint64_t)B};
+  cuuint64_t strides[3] = {(cuuint64_t)st[2] * 2, (cuuint64_t)st[1] * 2,
+                           (cuuint64_t)(st[0] > 0 ? st[0] : S * st[1]) * 2};
+  cuuint32_t box[4] = {64, 1, 128, 1};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims, strides,
+                  box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? LCATTN_OK : LCATTN_ERR_UNSUPPORTED;
+}
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? LCATTN_OK : LCATTN_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+int lcattn_tile_meta_layout_of(const lcattn_shape* shape, const lcattn_mask_desc* mask,
+                               lcattn_tile_meta_layout* out) {
+  if (!out) return LCATTN_ERR_INVALID_ARG;
+  return layout_of(shape, mask, out);
+}
+
+size_t lcattn_tile_meta_size(const lcattn_shape* shape, const lcattn_mask_desc* mask) {
+  lcattn_tile_meta_layout L;
+  if (layout_of(shape, mask, &L) != LCATTN_OK) return 0;
+  return (size_t)L.total_bytes;
+}
+
+int lcattn_mask_compile(const lcattn_shape* shape, const lcattn_mask_desc* mask, void* tile_meta,
+                        size_t bytes, lcattn_stream_t stream) {
+  lcattn_tile_meta_layout L;
+  int st = layout_of(shape, mask, &L);
+  if (st) return st;
+  if (!tile_meta || !aligned16(tile_meta)) return LCATTN_ERR_INVALID_ARG;
+  if (bytes < (size_t)L.total_bytes) return LCATTN_ERR_WORKSPACE;
+  return cuda_status(launch_mask_compile(problem_of(shape), mask_of(mask), meta_of(L, tile_meta),
+                                         reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int lcattn_fwd(const lcattn_shape* shape, const void* q, const void* k, const void* v,
+               const void* tile_meta, const lcattn_mask_desc* mask, float scale, void* o,
+               float* lse, lcattn_stream_t stream) {
+  lcattn_tile_meta_layout L;
+  int st = layout_of(shape, mask, &L);
+  if (st) return st;
+  if (!q || !k || !v || !o || !lse || !tile_meta) return LCATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(tile_meta))
+    return LCATTN_ERR_UNSUPPORTED;
+  if (!(scale > 0.f) || !(scale < 1e30f)) return LCATTN_ERR_INVALID_ARG;
+  CUtensorMap tq, tk, tv;
+  if ((st = encode_bshd(&tq, q, shape->B, shape->Sq, shape->Hq, shape->q_stride))) return st;
+  if ((st = encode_bshd(&tk, k, shape->B, shape->Sk, shape->Hkv, shape->k_stride))) return st;
+  if ((st = encode_bshd(&tv, v, shape->B, shape->Sk, shape->Hkv, shape->v_stride))) return st;
+  FwdArgs a;
+  a.pr = problem_of(shape);
+  a.mask = mask_of(mask);
+  a.meta = meta_of(L, tile_meta);
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.o = o;
+  a.o_sb = shape->o_stride[0]; a.o_ss = shape->o_stride[1]; a.o_sh = shape->o_stride[2];
+  a.lse = lse;
+  return cuda_status(launch_fwd(tq, tk, tv, a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+size_t lcattn_bwd_workspace_size(const lcattn_shape* shape) {
+  if (validate_shape(shape) != LCATTN_OK) return 0;
+  const int64_t d_bytes = align_up(4 * shape->B * shape->Hq * shape->Sq, 256);
+  const int64_t acc_bytes = 4 * shape->B * shape->Sq * shape->Hq * kD;
+  return (size_t)(d_bytes + acc_bytes);
+}
+
+int lcattn_bwd(const lcattn_shape* shape, const void* q, const void* k, const void* v,
+               const void* o, const void* d_o, const float* lse, const void* tile_meta,
+               const lcattn_mask_desc* mask, float scale, void* dq, void* dk, void* dv,
+               void* workspace, size_t workspace_bytes, lcattn_stream_t stream) {
+  lcattn_tile_meta_layout L;
+  int st = layout_of(shape, mask, &L);
+  if (st) return st;
+  if (!q || !k || !v || !o || !d_o || !lse || !tile_meta || !dq || !dk || !dv || !workspace)
+    return LCATTN_ERR_INVALID_ARG;
+  const void* ptrs[] = {q, k, v, o, d_o, dq, dk, dv, workspace, tile_meta};
+  for (auto p : ptrs)
+    if (!aligned16(p)) return LCATTN_ERR_UNSUPPORTED;
+  if (!(scale > 0.f) || !(scale < 1e30f)) return LCATTN_ERR_INVALID_ARG;
+  if (workspace_bytes < lcattn_bwd_workspace_size(shape)) return LCATTN_ERR_WORKSPACE;
+  CUtensorMap tq, tk, tv, tdo;
+  if ((st = encode_bshd(&tq, q, shape->B, shape->Sq, shape->Hq, shape->q_stride))) return st;
+  if ((st = encode_bshd(&tk, k, shape->B, shape->Sk, shape->Hkv, shape->k_stride))) return st;
+  if ((st = encode_bshd(&tv, v, shape->B, shape->Sk, shape->Hkv, shape->v_stride))) return st;
+  if ((st = encode_bshd(&tdo, d_o, shape->B, shape->Sq, shape->Hq, shape->o_stride))) return st;
+  BwdArgs a;
+  a.pr = problem_of(shape);
+  a.mask = mask_of(mask);
+  a.meta = meta_of(L, tile_meta);
+  a.scale = scale;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.o = o;
+  a.d_o = d_o;
+  a.o_sb = shape->o_stride[0]; a.o_ss = shape->o_stride[1]; a.o_sh = shape->o_stride[2];
+  a.lse = lse;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  a.dvec = reinterpret_cast<float*>(ws);
+  a.dq_acc = reinterpret_cast<float*>(ws + align_up(4 * shape->B * shape->Hq * shape->Sq, 256));
+  a.dq = dq;
+  a.q_sb = shape->q_stride[0]; a.q_ss = shape->q_stride[1]; a.q_sh = shape->q_stride[2];
+  a.dk = dk;
+  a.k_sb = shape->k_stride[0]; a.k_ss = shape->k_stride[1]; a.k_sh = shape->k_stride[2];
+  a.dv = dv;
+  a.v_sb = shape->v_stride[0]; a.v_ss = shape->v_stride[1]; a.v_sh = shape->v_stride[2];
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_bwd_prepass(a, s);
+  if (e == cudaSuccess) e = launch_bwd_dkdv(tq, tk, tv, tdo, a, s);
+  if (e == cudaSuccess) e = launch_bwd_dq_convert(a, s);
+  return cuda_status(e);
+}
+
+int lcattn_read_status(const void* tile_meta, lcattn_stream_t stream) {
+  if (!tile_meta) return LCATTN_ERR_INVALID_ARG;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return LCATTN_ERR_CUDA;
+  int32_t w[4] = {0, 0, 0, 0};
+  if (cudaMemcpy(w, tile_meta, sizeof(w), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return LCATTN_ERR_CUDA;
+  for (int i = 0; i < 4; ++i)
+    if (w[i] != 0) return w[i];
+  return LCATTN_OK;
+}
+
+int lcattn_clear_status(void* tile_meta, lcattn_stream_t stream) {
+  if (!tile_meta) return LCATTN_ERR_INVALID_ARG;
+  return cuda_status(cudaMemsetAsync(tile_meta, 0, 16, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+const char* lcattn_status_string(int status) {
+  switch (status) {
+    case LCATTN_OK: return "ok";
+    case LCATTN_ERR_INVALID_ARG: return "invalid argument";
+    case LCATTN_ERR_UNSUPPORTED: return "unsupported shape, stride, alignment or head dim";
+    case LCATTN_ERR_WORKSPACE: return "buffer smaller than required";
+    case LCATTN_ERR_CUDA: return "CUDA error";
+    case LCATTN_ERR_DEVICE_TIMEOUT: return "a kernel gave up waiting (bounded device wait expired)";
+    case LCATTN_ERR_DEVICE_MASK: return "block offsets are not nondecreasing from 0 to the sequence length";
+    default: return "unknown status";
+  }
+}
+
+int lcattn_version(void) { return 100; }
+
+}  // extern "C"

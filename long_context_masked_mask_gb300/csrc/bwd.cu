@@ -1,0 +1,565 @@
+// Backward masked attention for sm_103a, in three launches:
+//   1. pre-pass: D_i = <dO_i, O_i> (fp32) and zero the fp32 dQ accumulator;
+//   2. dK/dV: one CTA per (key tile, KV head, batch).  For every query head of
+//      the GQA group and every non-empty query tile of its list it recomputes
+//      S^T = K Q^T and P^T = exp(S^T - LSE), forms dP^T = V dO^T and
+//      dS^T = scale * P^T (dP^T - D), accumulates dV += P^T dO and
+//      dK += dS^T Q in TMEM, and adds the partial dQ = dS K into the fp32
+//      accumulator with vector reductions;
+//   3. dQ conversion to bf16.
+// The pages single the backward out as the main bottleneck of masked and
+// sparse attention ("Long-Context Attention Benchmark", xllm-io blog review,
+// sections "稀疏内核性能" and "核心发现总结"); the gradients are the textbook ones
+// for L = <O, dO>.
+//
+// dK/dV kernel roles (320 threads):
+//   warps 0-3  elementwise: thread = key row (TMEM lane) of the tile; builds
+//              P^T and dS^T, writes both to TMEM (bf16) and dS^T to shared
+//              memory for the dQ product; at the end stores dK and dV.
+//   warps 4-7  dQ drain: thread = query row; TMEM -> red.global.add.v4.f32.
+//   warp  8    producer: K, V once; Q_i, dO_i by TMA and LSE_i, D_i by plain
+//              loads into a 2-deep ring.
+//   warp  9    TMEM owner and MMA issuer.
+// TMEM: [0,128) S^T then P^T | [128,256) dP^T then dS^T, then dQ |
+//       [256,384) dV | [384,512) dK.
+#include <cuda_bf16.h>
+
+#include "lcattn_internal.cuh"
+#include "sm103_primitives.cuh"
+
+namespace lcattn {
+namespace {
+
+using namespace dev;
+
+constexpr int kTileBytes = 32768;
+constexpr int kHalfBytes = 16384;
+constexpr int kThreads = 320;
+constexpr float kLog2e = 1.4426950408889634f;
+
+// ---------------------------------------------------------------------------
+// 1. D pre-pass
+// ---------------------------------------------------------------------------
+__global__ void prepass_kernel(BwdArgs a) {
+  const int lane = threadIdx.x & 31;
+  const int64_t nrows = (int64_t)a.pr.B * a.pr.Sq * a.pr.Hq;
+  const int64_t wstride = (int64_t)gridDim.x * (blockDim.x >> 5);
+  for (int64_t w = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); w < nrows;
+       w += wstride) {
+    const int h = (int)(w % a.pr.Hq);
+    const int i = (int)((w / a.pr.Hq) % a.pr.Sq);
+    const int b = (int)(w / ((int64_t)a.pr.Hq * a.pr.Sq));
+    const int64_t off = (int64_t)b * a.o_sb + (int64_t)i * a.o_ss + (int64_t)h * a.o_sh;
+    const uint2 ov = __ldg(reinterpret_cast<const uint2*>(
+        reinterpret_cast<const __nv_bfloat16*>(a.o) + off) + lane);
+    const uint2 dv = __ldg(reinterpret_cast<const uint2*>(
+        reinterpret_cast<const __nv_bfloat16*>(a.d_o) + off) + lane);
+    const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(&ov);
+    const __nv_bfloat162* d2 = reinterpret_cast<const __nv_bfloat162*>(&dv);
+    float acc = 0.f;
+    #pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const float2 of = __bfloat1622float2(o2[k]);
+      const float2 df = __bfloat1622float2(d2[k]);
+      acc = fmaf(of.x, df.x, acc);
+      acc = fmaf(of.y, df.y, acc);
+    }
+    #pragma unroll
+    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    if (lane == 0) a.dvec[((int64_t)b * a.pr.Hq + h) * a.pr.Sq + i] = acc;
+    float4* dq = reinterpret_cast<float4*>(a.dq_acc + (((int64_t)b * a.pr.Sq + i) * a.pr.Hq + h) * kD);
+    dq[lane] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// 3. dQ conversion
+// ---------------------------------------------------------------------------
+__global__ void dq_convert_kernel(BwdArgs a) {
+  const int64_t nvec = (int64_t)a.pr.B * a.pr.Sq * a.pr.Hq * (kD / 8);
+  for (int64_t v = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; v < nvec;
+       v += (int64_t)gridDim.x * blockDim.x) {
+    const int c = (int)(v % (kD / 8));
+    const int64_t row = v / (kD / 8);  // (b, i, h)
+    const int h = (int)(row % a.pr.Hq);
+    const int i = (int)((row / a.pr.Hq) % a.pr.Sq);
+    const int b = (int)(row / ((int64_t)a.pr.Hq * a.pr.Sq));
+    const float4* src = reinterpret_cast<const float4*>(a.dq_acc + row * kD + c * 8);
+    const float4 x = src[0], y = src[1];
+    uint4 out;
+    out.x = pack_bf16x2(x.x, x.y);
+    out.y = pack_bf16x2(x.z, x.w);
+    out.z = pack_bf16x2(y.x, y.y);
+    out.w = pack_bf16x2(y.z, y.w);
+    __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(a.dq) + (int64_t)b * a.q_sb +
+                         (int64_t)i * a.q_ss + (int64_t)h * a.q_sh + c * 8;
+    *reinterpret_cast<uint4*>(dst) = out;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// 2. dK / dV
+// ---------------------------------------------------------------------------
+struct BwdSmem {
+  alignas(1024) uint8_t k[kTileBytes];
+  alignas(1024) uint8_t v[kTileBytes];
+  alignas(1024) uint8_t q[2][kTileBytes];
+  alignas(1024) uint8_t dO[2][kTileBytes];
+  alignas(1024) uint8_t ds[kTileBytes];
+  float lse2[2][128];  // LSE * log2(e); +inf where P must be 0
+  float dvec[2][128];
+  uint64_t kv_full;
+  uint64_t q_full[2];
+  uint64_t q_empty[2];
+  uint64_t s_full, dp_full, ds_ready, dq_full, dq_free, done;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+struct BwdKernelArgs {
+  BwdArgs a;
+};
+
+__device__ __forceinline__ int block_of(const int32_t* offs, int n, int x) {
+  int lo = 0, hi = n - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (__ldg(offs + mid) <= x) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+// Iterates the (query head in group, list index) pairs of one CTA in order.
+struct ItemIter {
+  const int32_t* cnt_base;  // bwd_cnt for (b, list head 0), stride nKt per list head
+  const int32_t* lst_base;
+  int nH, nKt, nQt, kt, G, g;
+  int hi, idx, cnt;
+  __device__ void init(const TileMetaDev& t, int b, int kt_, int G_, int g_) {
+    nH = t.nH; nKt = t.nKt; nQt = t.nQt; kt = kt_; G = G_; g = g_;
+    cnt_base = t.bwd_cnt + (int64_t)b * t.nH * t.nKt;
+    lst_base = t.bwd_lst + (int64_t)b * t.nH * t.nKt * t.nQt;
+    hi = 0; idx = 0;
+    cnt = count_of(0);
+    skip_empty();
+  }
+  __device__ int list_head(int hh) const { return nH == 1 ? 0 : g * G + hh; }
+  __device__ int count_of(int hh) const { return __ldg(cnt_base + (int64_t)list_head(hh) * nKt + kt); }
+  __device__ void skip_empty() {
+    while (hi < G && idx >= cnt) { ++hi; idx = 0; if (hi < G) cnt = count_of(hi); }
+  }
+  __device__ bool valid() const { return hi < G; }
+  __device__ int entry() const {
+    return __ldg(lst_base + ((int64_t)list_head(hi) * nKt + kt) * nQt + idx);
+  }
+  __device__ int head() const { return g * G + hi; }
+  __device__ void next() { ++idx; skip_empty(); }
+};
+
+__global__ void __launch_bounds__(kThreads, 1)
+dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+            const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
+            const __grid_constant__ BwdKernelArgs ka) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  const BwdArgs& a = ka.a;
+  const ProblemDev& pr = a.pr;
+  int32_t* gstatus = a.meta.status;
+  if ((smem_u32(smem_raw) & 1023u) != 0u) {  // layout relies on 1 KB alignment
+    if (threadIdx.x == 0) atomicCAS(gstatus, 0, LCATTN_ERR_CUDA);
+    return;
+  }
+  BwdSmem& sm = *reinterpret_cast<BwdSmem*>(smem_raw);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  const int b = blockIdx.z;
+  const int g = blockIdx.y;
+  // Longest key tiles first.  With per-head lists the order of the group's
+  // first head is used.
+  const int lh0 = a.meta.nH == 1 ? 0 : g * pr.G;
+  const int kt = __ldg(a.meta.bwd_ord + ((int64_t)b * a.meta.nH + lh0) * a.meta.nKt + blockIdx.x);
+
+  if (tid == 0) {
+    mbar_init(&sm.kv_full, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&sm.q_full[s], 33);
+      mbar_init(&sm.q_empty[s], 1);
+    }
+    mbar_init(&sm.s_full, 1);
+    mbar_init(&sm.dp_full, 1);
+    mbar_init(&sm.ds_ready, 128);
+    mbar_init(&sm.dq_full, 1);
+    mbar_init(&sm.dq_free, 128);
+    mbar_init(&sm.done, 1);
+    sm.abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 9) tmem_alloc(&sm.tmem_base, 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sm.tmem_base;
+  volatile int* abort_flag = &sm.abort_flag;
+  const int TO = LCATTN_ERR_DEVICE_TIMEOUT;
+
+  if (warp == 8) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      tma_prefetch_desc(&tmdO);
+      mbar_expect_tx(&sm.kv_full, 2 * kTileBytes);
+      tma_load_4d(sm.k, &tmK, &sm.kv_full, 0, g, kt * kBN, b);
+      tma_load_4d(sm.k + kHalfBytes, &tmK, &sm.kv_full, 64, g, kt * kBN, b);
+      tma_load_4d(sm.v, &tmV, &sm.kv_full, 0, g, kt * kBN, b);
+      tma_load_4d(sm.v + kHalfBytes, &tmV, &sm.kv_full, 64, g, kt * kBN, b);
+    }
+    ItemIter it;
+    it.init(a.meta, b, kt, pr.G, g);
+    int i = 0, issued = 0;
+    for (; it.valid(); it.next(), ++i) {
+      const int st = i & 1, use = i >> 1;
+      if (use > 0) {
+        bool ok = mbar_wait(&sm.q_empty[st], (use - 1) & 1, abort_flag, gstatus, TO);
+        if (!__all_sync(0xffffffffu, ok)) break;
+      }
+      const int qt = it.entry() >> 1;
+      const int h = it.head();
+      if (lane == 0) {
+        mbar_expect_tx(&sm.q_full[st], 2 * kTileBytes);
+        tma_load_4d(sm.q[st], &tmQ, &sm.q_full[st], 0, h, qt * kBM, b);
+        tma_load_4d(sm.q[st] + kHalfBytes, &tmQ, &sm.q_full[st], 64, h, qt * kBM, b);
+        tma_load_4d(sm.dO[st], &tmdO, &sm.q_full[st], 0, h, qt * kBM, b);
+        tma_load_4d(sm.dO[st] + kHalfBytes, &tmdO, &sm.q_full[st], 64, h, qt * kBM, b);
+      }
+      const float* lse = a.lse + ((int64_t)b * pr.Hq + h) * pr.Sq;
+      const float* dv = a.dvec + ((int64_t)b * pr.Hq + h) * pr.Sq;
+      #pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int c = lane * 4 + k;
+        const int q = qt * kBM + c;
+        float l2 = INFINITY, d = 0.f;
+        if (q < pr.Sq) {
+          const float l = __ldg(lse + q);
+          l2 = (l == -INFINITY) ? INFINITY : l * kLog2e;  // fully masked row: P = 0
+          d = __ldg(dv + q);
+        }
+        sm.lse2[st][c] = l2;
+        sm.dvec[st][c] = d;
+      }
+      mbar_arrive(&sm.q_full[st]);
+      issued = i + 1;
+    }
+    if (lane == 0) {
+      int dummy = 0;
+      for (int t = max(0, issued - 2); t < issued; ++t)
+        mbar_wait(&sm.q_full[t & 1], (t >> 1) & 1, &dummy, gstatus, TO);
+      mbar_wait(&sm.kv_full, 0, &dummy, gstatus, TO);
+    }
+  } else if (warp == 9) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t id_kmaj = idesc_bf16_f32(128, 128, false, false);
+      const uint32_t id_ts = idesc_bf16_f32(128, 128, false, true);
+      const uint32_t id_mn = idesc_bf16_f32(128, 128, true, true);
+      const uint32_t tS = tmem, tP = tmem + 128, tdV = tmem + 256, tdK = tmem + 384;
+      const uint32_t k_s = smem_u32(sm.k), v_s = smem_u32(sm.v), ds_s = smem_u32(sm.ds);
+      bool ok = mbar_wait(&sm.kv_full, 0, abort_flag, gstatus, TO);
+      ItemIter it;
+      it.init(a.meta, b, kt, pr.G, g);
+      int i = 0;
+      for (; ok && it.valid(); it.next(), ++i) {
+        const int st = i & 1;
+        if (!(ok = mbar_wait(&sm.q_full[st], (i >> 1) & 1, abort_flag, gstatus, TO))) break;
+        tc_fence_after();
+        const uint32_t q_s = smem_u32(sm.q[st]), do_s = smem_u32(sm.dO[st]);
+        // S^T = K Q^T
+        #pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
+          mma_ss(tS, sdesc_sw128(k_s + off, 16, 1024), sdesc_sw128(q_s + off, 16, 1024), id_kmaj,
+                 kk > 0 ? 1u : 0u);
+        }
+        tc_commit(&sm.s_full);
+        // dP^T = V dO^T, into columns the previous dQ used: wait for its drain.
+        if (i > 0) {
+          if (!(ok = mbar_wait(&sm.dq_free, (i - 1) & 1, abort_flag, gstatus, TO))) break;
+          tc_fence_after();
+        }
+        #pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
+          mma_ss(tP, sdesc_sw128(v_s + off, 16, 1024), sdesc_sw128(do_s + off, 16, 1024), id_kmaj,
+                 kk > 0 ? 1u : 0u);
+        }
+        tc_commit(&sm.dp_full);
+        if (!(ok = mbar_wait(&sm.ds_ready, i & 1, abort_flag, gstatus, TO))) break;
+        tc_fence_after();
+        // dV += P^T dO ; dK += dS^T Q   (A from TMEM, B MN-major from smem)
+        #pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          mma_ts(tdV, tS + kk * 8, sdesc_sw128(do_s + kk * 2048, kHalfBytes, 1024), id_ts,
+                 (i > 0 || kk > 0) ? 1u : 0u);
+        #pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          mma_ts(tdK, tP + kk * 8, sdesc_sw128(q_s + kk * 2048, kHalfBytes, 1024), id_ts,
+                 (i > 0 || kk > 0) ? 1u : 0u);
+        tc_commit(&sm.q_empty[st]);
+        // dQ = dS K  (A = dS^T in smem read MN-major, B = K MN-major)
+        #pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          mma_ss(tP, sdesc_sw128(ds_s + kk * 2048, kHalfBytes, 1024),
+                 sdesc_sw128(k_s + kk * 2048, kHalfBytes, 1024), id_mn, kk > 0 ? 1u : 0u);
+        tc_commit(&sm.dq_full);
+      }
+      tc_commit(&sm.done);
+      int dummy = 0;
+      mbar_wait(&sm.done, 0, &dummy, gstatus, TO);
+    }
+  } else if (warp < 4) {
+    // ------------------------------------------------------------ elementwise
+    const int r = tid;  // key row within the tile == TMEM lane
+    const int key = kt * kBN + r;
+    const bool key_ok = key < pr.Sk;
+    const uint32_t lane_off = static_cast<uint32_t>(32 * warp) << 16;
+    const uint32_t tS = tmem + lane_off, tP = tmem + lane_off + 128;
+    const float sl2 = a.scale_log2, scale = a.scale;
+    int4 cb = make_int4(0, 0, 0, 0);
+    int kb = 0;
+    if (key_ok) {
+      if (a.mask.kind == LCATTN_MASK_COLBOUNDS) cb = __ldg(a.mask.col_bounds + (int64_t)b * pr.Sk + key);
+      else kb = block_of(a.mask.k_offs, a.mask.nKb, key);
+    }
+    const bool ragged_q = (pr.Sq % kBM) != 0;
+    const int last_qt = (pr.Sq - 1) / kBM;
+    ItemIter it;
+    it.init(a.meta, b, kt, pr.G, g);
+    int i = 0;
+    bool ok = true;
+    for (; it.valid(); it.next(), ++i) {
+      const int st = i & 1;
+      const int e = it.entry();
+      const int qt = e >> 1;
+      const int q0 = qt * kBM;
+      const bool partial = (e & 1) != 0;
+      // Allowed-query bits of this key for the tile (bit c = query q0 + c).
+      uint32_t mw[4] = {0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu};
+      if (!key_ok) {
+        mw[0] = mw[1] = mw[2] = mw[3] = 0u;
+      } else if (partial) {
+        if (a.mask.kind == LCATTN_MASK_COLBOUNDS) {
+          #pragma unroll
+          for (int w = 0; w < 4; ++w) {
+            uint32_t bits = 0u;
+            #pragma unroll
+            for (int c = 0; c < 32; ++c) {
+              const int q = q0 + 32 * w + c;
+              const bool okq = (cb.x <= q && q < cb.y) || (cb.z <= q && q < cb.w);
+              bits |= (okq ? 1u : 0u) << c;
+            }
+            mw[w] = bits;
+          }
+        } else {
+          mw[0] = mw[1] = mw[2] = mw[3] = 0u;
+          const uint8_t* map = a.mask.block_map +
+                               ((int64_t)b * pr.Hq + it.head()) * a.mask.nQb * (int64_t)a.mask.nKb + kb;
+          const int q1 = min(q0 + kBM, pr.Sq);
+          for (int qb = block_of(a.mask.q_offs, a.mask.nQb, q0); qb < a.mask.nQb; ++qb) {
+            const int lo = max(__ldg(a.mask.q_offs + qb), q0);
+            if (lo >= q1) break;
+            const int hi = min(__ldg(a.mask.q_offs + qb + 1), q1);
+            if (hi > lo && __ldg(map + (int64_t)qb * a.mask.nKb)) {
+              #pragma unroll
+              for (int w = 0; w < 4; ++w) {
+                const int x0 = max(lo - q0, 32 * w), x1 = min(hi - q0, 32 * w + 32);
+                if (x1 > x0) {
+                  const int nb = x1 - x0;
+                  mw[w] |= (nb == 32) ? 0xffffffffu : (((1u << nb) - 1u) << (x0 - 32 * w));
+                }
+              }
+            }
+          }
+        }
+      }
+      (void)ragged_q; (void)last_qt;  // rows past Sq carry LSE = +inf, so P = 0 there
+      ok = mbar_wait(&sm.q_full[st], (i >> 1) & 1, abort_flag, gstatus, TO) &&
+           mbar_wait(&sm.s_full, i & 1, abort_flag, gstatus, TO) &&
+           mbar_wait(&sm.dp_full, i & 1, abort_flag, gstatus, TO);
+      if (i > 0 && ok) ok = mbar_wait(&sm.dq_full, (i - 1) & 1, abort_flag, gstatus, TO);
+      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+      tc_fence_after();
+      const float* lse2 = sm.lse2[st];
+      const float* dvec = sm.dvec[st];
+      uint8_t* ds_row = sm.ds + r * 128;
+      #pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t sr[32], pr32[32];
+        tmem_ld32(tS + c * 32, sr);
+        tmem_ld32(tP + c * 32, pr32);
+        tmem_ld_wait();
+        uint32_t pp[16], dd[16];
+        #pragma unroll
+        for (int k = 0; k < 16; ++k) {
+          float pv[2], dsv[2];
+          #pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const int col = c * 32 + 2 * k + u;
+            const bool allowed = (mw[col >> 5] >> (col & 31)) & 1u;
+            float p = fast_exp2(fmaf(__uint_as_float(sr[2 * k + u]), sl2, -lse2[col]));
+            p = allowed ? p : 0.f;
+            pv[u] = p;
+            dsv[u] = scale * p * (__uint_as_float(pr32[2 * k + u]) - dvec[col]);
+          }
+          pp[k] = pack_bf16x2(pv[0], pv[1]);
+          dd[k] = pack_bf16x2(dsv[0], dsv[1]);
+        }
+        // P^T and dS^T (bf16 pairs) over the first halves of their regions.
+        asm volatile(
+            "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+            "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
+            :: "r"(tS + c * 16), "r"(pp[0]), "r"(pp[1]), "r"(pp[2]), "r"(pp[3]), "r"(pp[4]),
+               "r"(pp[5]), "r"(pp[6]), "r"(pp[7]), "r"(pp[8]), "r"(pp[9]), "r"(pp[10]),
+               "r"(pp[11]), "r"(pp[12]), "r"(pp[13]), "r"(pp[14]), "r"(pp[15]) : "memory");
+        asm volatile(
+            "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+            "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
+            :: "r"(tP + c * 16), "r"(dd[0]), "r"(dd[1]), "r"(dd[2]), "r"(dd[3]), "r"(dd[4]),
+               "r"(dd[5]), "r"(dd[6]), "r"(dd[7]), "r"(dd[8]), "r"(dd[9]), "r"(dd[10]),
+               "r"(dd[11]), "r"(dd[12]), "r"(dd[13]), "r"(dd[14]), "r"(dd[15]) : "memory");
+        // dS^T row r, queries c*32 .. c*32+31 -> 4 swizzled 16-byte chunks.
+        #pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int chunk = c * 4 + u;          // 8 queries per chunk
+          const int grp = chunk >> 3, cc = chunk & 7;
+          *reinterpret_cast<uint4*>(ds_row + grp * kHalfBytes + ((cc ^ (r & 7)) << 4)) =
+              make_uint4(dd[4 * u], dd[4 * u + 1], dd[4 * u + 2], dd[4 * u + 3]);
+        }
+      }
+      tmem_st_wait();
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(&sm.ds_ready);
+    }
+    // ---- dK, dV out (bf16); zero when no query tile touched this key tile
+    if (ok) {
+      bool have = i > 0;
+      if (have) {
+        have = mbar_wait(&sm.done, 0, abort_flag, gstatus, TO);
+        have = __all_sync(0xffffffffu, have);
+        tc_fence_after();
+      }
+      for (int which = 0; which < 2; ++which) {
+        const uint32_t tacc = tmem + lane_off + (which == 0 ? 256 : 384);
+        __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(which == 0 ? a.dv : a.dk) +
+                             (int64_t)b * (which == 0 ? a.v_sb : a.k_sb) +
+                             (int64_t)key * (which == 0 ? a.v_ss : a.k_ss) +
+                             (int64_t)g * (which == 0 ? a.v_sh : a.k_sh);
+        #pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t x[32];
+          if (have) {
+            tmem_ld32(tacc + c * 32, x);
+            tmem_ld_wait();
+          } else {
+            #pragma unroll
+            for (int k = 0; k < 32; ++k) x[k] = 0u;
+          }
+          if (key_ok) {
+            uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
+            #pragma unroll
+            for (int u = 0; u < 4; ++u)
+              d4[u] = make_uint4(pack_bf16x2(__uint_as_float(x[8 * u]), __uint_as_float(x[8 * u + 1])),
+                                 pack_bf16x2(__uint_as_float(x[8 * u + 2]), __uint_as_float(x[8 * u + 3])),
+                                 pack_bf16x2(__uint_as_float(x[8 * u + 4]), __uint_as_float(x[8 * u + 5])),
+                                 pack_bf16x2(__uint_as_float(x[8 * u + 6]), __uint_as_float(x[8 * u + 7])));
+          }
+        }
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ dQ drain
+    const int r = tid - 128;  // query row within the tile
+    const uint32_t lane_off = static_cast<uint32_t>(32 * (warp & 3)) << 16;
+    const uint32_t tQ = tmem + lane_off + 128;
+    ItemIter it;
+    it.init(a.meta, b, kt, pr.G, g);
+    int i = 0;
+    for (; it.valid(); it.next(), ++i) {
+      const int qt = it.entry() >> 1;
+      const int h = it.head();
+      const int q = qt * kBM + r;
+      bool ok = mbar_wait(&sm.dq_full, i & 1, abort_flag, gstatus, TO);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      tc_fence_after();
+      float* dst = a.dq_acc + (((int64_t)b * pr.Sq + q) * pr.Hq + h) * kD;
+      #pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t x[32];
+        tmem_ld32(tQ + c * 32, x);
+        tmem_ld_wait();
+        if (q < pr.Sq) {
+          #pragma unroll
+          for (int u = 0; u < 8; ++u)
+            asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};"
+                         :: "l"(dst + c * 32 + 4 * u), "f"(__uint_as_float(x[4 * u])),
+                            "f"(__uint_as_float(x[4 * u + 1])), "f"(__uint_as_float(x[4 * u + 2])),
+                            "f"(__uint_as_float(x[4 * u + 3]))
+                         : "memory");
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&sm.dq_free);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 9) {
+    __syncwarp();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_prepass(const BwdArgs& a, cudaStream_t st) {
+  int dev = 0, nsm = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
+  const int64_t rows = (int64_t)a.pr.B * a.pr.Sq * a.pr.Hq;
+  int64_t blocks = (rows + 7) / 8;
+  if (blocks > (int64_t)nsm * 32) blocks = (int64_t)nsm * 32;
+  prepass_kernel<<<(unsigned)blocks, 256, 0, st>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_dkdv(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                            const CUtensorMap& tdo, const BwdArgs& a, cudaStream_t st) {
+  static bool attr_done = false;
+  const size_t smem = sizeof(BwdSmem);
+  if (!attr_done) {
+    cudaError_t e =
+        cudaFuncSetAttribute(dkdv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    attr_done = true;
+  }
+  BwdKernelArgs ka;
+  ka.a = a;
+  dim3 grid(a.meta.nKt, a.pr.Hkv, a.pr.B);
+  dkdv_kernel<<<grid, kThreads, smem, st>>>(tq, tk, tv, tdo, ka);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_dq_convert(const BwdArgs& a, cudaStream_t st) {
+  int dev = 0, nsm = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
+  const int64_t nvec = (int64_t)a.pr.B * a.pr.Sq * a.pr.Hq * (kD / 8);
+  int64_t blocks = (nvec + 255) / 256;
+  if (blocks > (int64_t)nsm * 32) blocks = (int64_t)nsm * 32;
+  dq_convert_kernel<<<(unsigned)blocks, 256, 0, st>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace lcattn

@@ -1,0 +1,411 @@
+// Forward masked attention for sm_103a.
+//
+// Computes O = softmax(scale * Q K^T restricted to the allowed keys) V and the
+// natural-log LSE per query row -- the forward operator benchmarked on the
+// pages ("Long-Context Attention Benchmark", xllm-io blog review, sections
+// "密集注意力内核" and "密集内核性能": bf16, head dim 128, GQA 64:8 and MHA 64:64).
+//
+// One CTA owns up to two 128-row query tiles ("slots") that share one list of
+// key tiles: two query heads of the same GQA group (the mask is head
+// independent for column bounds), or a single tile otherwise.  Roles:
+//   warps 0-3  softmax for slot 0 (thread = query row = TMEM lane)
+//   warps 4-7  softmax for slot 1
+//   warp  8    TMA producer: Q tiles once, then K_j, V_j into a 4-deep ring
+//   warp  9    TMEM owner and single-thread tcgen05.mma issuer
+// TMEM (512 columns): S0 | S1 | O0 | O1, 128 fp32 columns each.  The softmax
+// writes P (bf16 pairs) over the first 64 columns of its S, and the PV product
+// reads P from TMEM (A operand) and V from shared memory (B operand).
+// Issue order per key tile j: PV0(j-1), S0(j), PV1(j-1), S1(j), so each slot's
+// softmax overlaps the other slot's two GEMMs.
+// The running max is kept in the log2 domain and only moved when a row max grows
+// by more than 8 (a factor 256 of headroom in fp32 / bf16), so O is rescaled in
+// TMEM rarely; the final O is divided by the row sum in the epilogue.
+#include <cuda_bf16.h>
+
+#include "lcattn_internal.cuh"
+#include "sm103_primitives.cuh"
+
+namespace lcattn {
+namespace {
+
+using namespace dev;
+
+constexpr int kStages = 4;          // K/V ring depth (K and V tiles alternate)
+constexpr int kTileBytes = 32768;   // 128 rows x 128 bf16
+constexpr int kHalfBytes = 16384;   // one 64-column TMA box
+constexpr int kThreads = 320;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
+
+struct FwdSmem {
+  alignas(1024) uint8_t q[2][kTileBytes];
+  alignas(1024) uint8_t kv[kStages][kTileBytes];
+  uint64_t q_full[2];
+  uint64_t kv_full[kStages];
+  uint64_t kv_empty[kStages];
+  uint64_t s_full[2];
+  uint64_t p_full[2];
+  uint64_t o_full[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+struct FwdKernelArgs {
+  FwdArgs a;
+  int heads_per_cta;
+};
+
+__device__ __forceinline__ void set_bits(uint32_t (&mw)[4], int lo, int hi) {
+  #pragma unroll
+  for (int w = 0; w < 4; ++w) {
+    const int a = max(lo, 32 * w), b = min(hi, 32 * w + 32);
+    if (b > a) {
+      const int n = b - a;
+      const uint32_t bits = (n == 32) ? 0xffffffffu : (((1u << n) - 1u) << (a - 32 * w));
+      mw[w] |= bits;
+    }
+  }
+}
+
+__device__ __forceinline__ int block_of(const int32_t* offs, int n, int x) {
+  int lo = 0, hi = n - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (__ldg(offs + mid) <= x) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+// Allowed-key bits of query row `row` for key tile kt (bit c = key kt*128+c).
+__device__ __forceinline__ void tile_mask_bits(const MaskDev& m, const ProblemDev& pr, int b,
+                                               int h, int row, int qb_row, int kt,
+                                               bool evaluate_mask, uint32_t (&mw)[4]) {
+  const int j0 = kt * kBN;
+  const int nvalid = min(kBN, pr.Sk - j0);
+  mw[0] = mw[1] = mw[2] = mw[3] = 0u;
+  if (!evaluate_mask) {  // full tile cut by the end of the key sequence
+    set_bits(mw, 0, nvalid);
+    return;
+  }
+  if (m.kind == LCATTN_MASK_COLBOUNDS) {
+    const int4* cb = m.col_bounds + (int64_t)b * pr.Sk + j0;
+    #pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      uint32_t bits = 0u;
+      #pragma unroll
+      for (int c = 0; c < 32; ++c) {
+        const int key = 32 * w + c;
+        if (key < nvalid) {
+          const int4 v = __ldg(cb + key);
+          const bool ok = (v.x <= row && row < v.y) || (v.z <= row && row < v.w);
+          bits |= (ok ? 1u : 0u) << c;
+        }
+      }
+      mw[w] = bits;
+    }
+  } else {
+    const int j1 = j0 + nvalid;
+    const uint8_t* map =
+        m.block_map + (((int64_t)b * pr.Hq + h) * m.nQb + qb_row) * (int64_t)m.nKb;
+    for (int kb = block_of(m.k_offs, m.nKb, j0); kb < m.nKb; ++kb) {
+      const int lo = max(__ldg(m.k_offs + kb), j0);
+      if (lo >= j1) break;
+      const int hi = min(__ldg(m.k_offs + kb + 1), j1);
+      if (hi > lo && __ldg(map + kb)) set_bits(mw, lo - j0, hi - j0);
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+           const __grid_constant__ CUtensorMap tmV, const __grid_constant__ FwdKernelArgs ka) {
+  extern __shared__ uint8_t smem_raw[];
+  FwdSmem& sm = *reinterpret_cast<FwdSmem*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const FwdArgs& a = ka.a;
+  const ProblemDev& pr = a.pr;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int hpc = ka.heads_per_cta;
+
+  // ---- work item -----------------------------------------------------------
+  const int b = blockIdx.z;
+  const int rank = blockIdx.y;
+  const int h0 = blockIdx.x * hpc;
+  const int lh = a.meta.nH == 1 ? 0 : h0;
+  const int64_t lbase = ((int64_t)b * a.meta.nH + lh) * a.meta.nQt;
+  const int qt = __ldg(a.meta.fwd_ord + lbase + rank);
+  const int n = __ldg(a.meta.fwd_cnt + lbase + qt);
+  const int32_t* list = a.meta.fwd_lst + (lbase + qt) * a.meta.nKt;
+  const int g = h0 / pr.G;
+  int32_t* gstatus = a.meta.status;
+
+  if (tid == 0) {
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&sm.q_full[s], 1);
+      mbar_init(&sm.s_full[s], 1);
+      mbar_init(&sm.p_full[s], 128);
+      mbar_init(&sm.o_full[s], 1);
+    }
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(&sm.kv_full[i], 1);
+      mbar_init(&sm.kv_empty[i], 1);
+    }
+    mbar_init(&sm.drain, 1);
+    sm.abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 9) tmem_alloc(&sm.tmem_base, 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sm.tmem_base;
+  volatile int* abort_flag = &sm.abort_flag;
+
+  if (warp == 8) {
+    // ---------------------------------------------------------------- producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      for (int s = 0; s < hpc; ++s) {
+        mbar_expect_tx(&sm.q_full[s], kTileBytes);
+        tma_load_4d(sm.q[s], &tmQ, &sm.q_full[s], 0, h0 + s, qt * kBM, b);
+        tma_load_4d(sm.q[s] + kHalfBytes, &tmQ, &sm.q_full[s], 64, h0 + s, qt * kBM, b);
+      }
+      int issued = 0;
+      for (int t = 0; t < 2 * n; ++t) {
+        const int stage = t % kStages, use = t / kStages;
+        if (use > 0 && !mbar_wait(&sm.kv_empty[stage], (use - 1) & 1, abort_flag, gstatus,
+                                  LCATTN_ERR_DEVICE_TIMEOUT))
+          break;
+        const int kt = __ldg(list + (t >> 1)) >> 1;
+        const CUtensorMap* tm = (t & 1) ? &tmV : &tmK;
+        mbar_expect_tx(&sm.kv_full[stage], kTileBytes);
+        tma_load_4d(sm.kv[stage], tm, &sm.kv_full[stage], 0, g, kt * kBN, b);
+        tma_load_4d(sm.kv[stage] + kHalfBytes, tm, &sm.kv_full[stage], 64, g, kt * kBN, b);
+        issued = t + 1;
+      }
+      // Never leave copies in flight: wait (bounded, ignoring the abort word)
+      // for the last load issued on each stage.
+      for (int t = max(0, issued - kStages); t < issued; ++t) {
+        int dummy = 0;
+        mbar_wait(&sm.kv_full[t % kStages], (t / kStages) & 1, &dummy, gstatus,
+                  LCATTN_ERR_DEVICE_TIMEOUT);
+      }
+      for (int s = 0; s < hpc; ++s) {
+        int dummy = 0;
+        mbar_wait(&sm.q_full[s], 0, &dummy, gstatus, LCATTN_ERR_DEVICE_TIMEOUT);
+      }
+    }
+  } else if (warp == 9) {
+    // ---------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc_qk = idesc_bf16_f32(128, 128, false, false);
+      const uint32_t idesc_pv = idesc_bf16_f32(128, 128, false, true);
+      bool ok = true;
+      for (int s = 0; s < hpc && ok; ++s)
+        ok = mbar_wait(&sm.q_full[s], 0, abort_flag, gstatus, LCATTN_ERR_DEVICE_TIMEOUT);
+      for (int j = 0; ok && j <= n; ++j) {
+        const int tk = 2 * j, tv = 2 * j - 1;
+        if (j < n)
+          ok = mbar_wait(&sm.kv_full[tk % kStages], (tk / kStages) & 1, abort_flag, gstatus,
+                         LCATTN_ERR_DEVICE_TIMEOUT);
+        if (ok && j > 0)
+          ok = mbar_wait(&sm.kv_full[tv % kStages], (tv / kStages) & 1, abort_flag, gstatus,
+                         LCATTN_ERR_DEVICE_TIMEOUT);
+        if (!ok) break;
+        tc_fence_after();
+        for (int s = 0; s < hpc; ++s) {
+          const uint32_t tS = tmem + s * 128, tO = tmem + 256 + s * 128;
+          if (j > 0) {
+            if (!(ok = mbar_wait(&sm.p_full[s], (j - 1) & 1, abort_flag, gstatus,
+                                 LCATTN_ERR_DEVICE_TIMEOUT)))
+              break;
+            tc_fence_after();
+            const uint32_t vb = smem_u32(sm.kv[tv % kStages]);
+            #pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+              mma_ts(tO, tS + kk * 8, sdesc_sw128(vb + kk * 2048, kHalfBytes, 1024), idesc_pv,
+                     (j > 1 || kk > 0) ? 1u : 0u);
+            tc_commit(&sm.o_full[s]);
+          }
+          if (j < n) {
+            const uint32_t qb = smem_u32(sm.q[s]), kb = smem_u32(sm.kv[tk % kStages]);
+            #pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+              const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
+              mma_ss(tS, sdesc_sw128(qb + off, 16, 1024), sdesc_sw128(kb + off, 16, 1024),
+                     idesc_qk, kk > 0 ? 1u : 0u);
+            }
+            tc_commit(&sm.s_full[s]);
+          }
+        }
+        if (!ok) break;
+        if (j < n) tc_commit(&sm.kv_empty[tk % kStages]);
+        if (j > 0) tc_commit(&sm.kv_empty[tv % kStages]);
+      }
+      // Drain: every MMA issued above has completed once this barrier flips.
+      tc_commit(&sm.drain);
+      int dummy = 0;
+      mbar_wait(&sm.drain, 0, &dummy, gstatus, LCATTN_ERR_DEVICE_TIMEOUT);
+    }
+  } else {
+    // ---------------------------------------------------------------- softmax
+    const int s = warp >> 2;
+    const int r = tid & 127;  // == 32 * (warp % 4) + lane: this thread's TMEM lane
+    if (s < hpc) {
+      const int h = h0 + s;
+      const int row = qt * kBM + r;
+      const uint32_t lane_off = static_cast<uint32_t>(32 * (warp & 3)) << 16;
+      const uint32_t tS = tmem + lane_off + s * 128;
+      const uint32_t tO = tmem + lane_off + 256 + s * 128;
+      const float sl2 = a.scale_log2;
+      const int last_kt = (pr.Sk - 1) / kBN;
+      const bool ragged_k = (pr.Sk % kBN) != 0;
+      int qb_row = 0;
+      if (a.mask.kind == LCATTN_MASK_BLOCKMAP)
+        qb_row = block_of(a.mask.q_offs, a.mask.nQb, min(row, pr.Sq - 1));
+      float m_run = -INFINITY, l_run = 0.f;
+      bool ok = true;
+      for (int j = 0; j < n; ++j) {
+        const int e = __ldg(list + j);
+        const int kt = e >> 1;
+        const bool partial = (e & 1) != 0;
+        const bool masked = partial || (ragged_k && kt == last_kt);
+        uint32_t mw[4];
+        if (masked) tile_mask_bits(a.mask, pr, b, h, row, qb_row, kt, partial, mw);
+        ok = mbar_wait(&sm.s_full[s], j & 1, abort_flag, gstatus, LCATTN_ERR_DEVICE_TIMEOUT);
+        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+        tc_fence_after();
+        uint32_t xr[128];
+        tmem_ld32(tS + 0, xr + 0);
+        tmem_ld32(tS + 32, xr + 32);
+        tmem_ld32(tS + 64, xr + 64);
+        tmem_ld32(tS + 96, xr + 96);
+        tmem_ld_wait();
+        float x[128];
+        #pragma unroll
+        for (int c = 0; c < 128; ++c) x[c] = __uint_as_float(xr[c]);
+        if (masked) {
+          #pragma unroll
+          for (int c = 0; c < 128; ++c)
+            if (!((mw[c >> 5] >> (c & 31)) & 1u)) x[c] = -INFINITY;
+        }
+        float mx = x[0];
+        #pragma unroll
+        for (int c = 1; c < 128; ++c) mx = fmaxf(mx, x[c]);
+        const float m_tile = mx * sl2;  // -inf stays -inf
+        const bool need = m_tile > m_run + kRescaleThreshold;
+        const bool warp_rescale = __any_sync(0xffffffffu, need) && j > 0;
+        const float m_new = need ? m_tile : m_run;
+        const float alpha = need ? fast_exp2(m_run - m_new) : 1.f;  // exp2(-inf) = 0
+        m_run = m_new;
+        const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
+        float sum = 0.f;
+        #pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          uint32_t pk[32];
+          #pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const float p0 = fast_exp2(fmaf(x[c * 64 + 2 * i], sl2, -m_use));
+            const float p1 = fast_exp2(fmaf(x[c * 64 + 2 * i + 1], sl2, -m_use));
+            sum += p0 + p1;
+            pk[i] = pack_bf16x2(p0, p1);
+          }
+          tmem_st32(tS + c * 32, pk);
+        }
+        l_run = l_run * alpha + sum;
+        if (warp_rescale) {
+          // O holds PV up to tile j-1: wait for it, then scale it in place
+          // before PV(j) is issued (which needs p_full below).
+          ok = mbar_wait(&sm.o_full[s], (j - 1) & 1, abort_flag, gstatus,
+                         LCATTN_ERR_DEVICE_TIMEOUT);
+          if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+          tc_fence_after();
+          #pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            uint32_t o32[32];
+            tmem_ld32(tO + c * 32, o32);
+            tmem_ld_wait();
+            #pragma unroll
+            for (int i = 0; i < 32; ++i) o32[i] = __float_as_uint(__uint_as_float(o32[i]) * alpha);
+            tmem_st32(tO + c * 32, o32);
+          }
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&sm.p_full[s]);
+      }
+      // ---- epilogue: O / l and LSE
+      bool have_o = ok && n > 0;
+      if (have_o) {
+        have_o = mbar_wait(&sm.o_full[s], (n - 1) & 1, abort_flag, gstatus,
+                           LCATTN_ERR_DEVICE_TIMEOUT);
+        have_o = __all_sync(0xffffffffu, have_o);
+        tc_fence_after();
+      }
+      if (ok) {
+        const bool live = l_run > 0.f;
+        const float inv = live ? 1.f / l_run : 0.f;
+        __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(a.o) + (int64_t)b * a.o_sb +
+                              (int64_t)row * a.o_ss + (int64_t)h * a.o_sh;
+        #pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t o32[32];
+          if (have_o) {
+            tmem_ld32(tO + c * 32, o32);
+            tmem_ld_wait();
+          } else {
+            #pragma unroll
+            for (int i = 0; i < 32; ++i) o32[i] = 0u;
+          }
+          uint32_t pk[16];
+          #pragma unroll
+          for (int i = 0; i < 16; ++i)
+            pk[i] = pack_bf16x2(__uint_as_float(o32[2 * i]) * inv,
+                                __uint_as_float(o32[2 * i + 1]) * inv);
+          if (row < pr.Sq) {
+            uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+            #pragma unroll
+            for (int i = 0; i < 4; ++i)
+              dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+          }
+        }
+        if (row < pr.Sq)
+          a.lse[((int64_t)b * pr.Hq + h) * pr.Sq + row] =
+              live ? (m_run + __log2f(l_run)) * 0.69314718055994531f : -INFINITY;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 9) {
+    __syncwarp();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                       const FwdArgs& a, cudaStream_t st) {
+  static bool attr_done = false;
+  const size_t smem = sizeof(FwdSmem) + 1024;
+  if (!attr_done) {
+    cudaError_t e =
+        cudaFuncSetAttribute(fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    attr_done = true;
+  }
+  FwdKernelArgs ka;
+  ka.a = a;
+  // Two query heads per CTA when they share the key tiles and the tile list.
+  ka.heads_per_cta = (a.meta.nH == 1 && a.pr.G % 2 == 0) ? 2 : 1;
+  dim3 grid(a.pr.Hq / ka.heads_per_cta, a.meta.nQt, a.pr.B);
+  fwd_kernel<<<grid, kThreads, smem, st>>>(tq, tk, tv, ka);
+  return cudaGetLastError();
+}
+
+}  // namespace lcattn

@@ -1,0 +1,84 @@
+// Internal declarations shared by the host layer (api.cu) and the kernel
+// translation units.  Nothing here is part of the public ABI.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "../../include/lcattn.h"
+
+namespace lcattn {
+
+constexpr int kBM = LCATTN_BLOCK_M;  // query rows per tile
+constexpr int kBN = LCATTN_BLOCK_N;  // key columns per tile
+constexpr int kD = 128;              // head dim
+
+// Mask descriptor as the kernels see it.
+struct MaskDev {
+  int kind;                  // LCATTN_MASK_COLBOUNDS / LCATTN_MASK_BLOCKMAP
+  const int4* col_bounds;    // [B][Sk] {a0,b0,a1,b1}
+  const uint8_t* block_map;  // [B][Hq][nQb][nKb]
+  const int32_t* q_offs;     // [nQb+1]
+  const int32_t* k_offs;     // [nKb+1]
+  int nQb, nKb;
+};
+
+// Pointers into a tile-meta buffer.
+struct TileMetaDev {
+  int32_t* status;
+  uint8_t* cls;
+  int32_t* fwd_cnt;
+  int32_t* fwd_lst;
+  int32_t* fwd_ord;
+  int32_t* bwd_cnt;
+  int32_t* bwd_lst;
+  int32_t* bwd_ord;
+  int nQt, nKt, nH, B;
+};
+
+struct ProblemDev {
+  int B, Sq, Sk, Hq, Hkv, G;
+};
+
+// ---- launchers (defined in the kernel translation units) -----------------
+cudaError_t launch_mask_compile(const ProblemDev& pr, const MaskDev& m, const TileMetaDev& t,
+                                cudaStream_t st);
+
+struct FwdArgs {
+  ProblemDev pr;
+  MaskDev mask;
+  TileMetaDev meta;
+  float scale_log2;
+  void* o;
+  int64_t o_sb, o_ss, o_sh;
+  float* lse;
+};
+cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                       const FwdArgs& a, cudaStream_t st);
+
+struct BwdArgs {
+  ProblemDev pr;
+  MaskDev mask;
+  TileMetaDev meta;
+  float scale;
+  float scale_log2;
+  const void* o;
+  const void* d_o;
+  int64_t o_sb, o_ss, o_sh;
+  const float* lse;
+  float* dvec;   // D [B][Hq][Sq]
+  float* dq_acc; // [B][Sq][Hq][128] fp32
+  void* dq;
+  int64_t q_sb, q_ss, q_sh;
+  void* dk;
+  int64_t k_sb, k_ss, k_sh;
+  void* dv;
+  int64_t v_sb, v_ss, v_sh;
+};
+cudaError_t launch_bwd_prepass(const BwdArgs& a, cudaStream_t st);
+cudaError_t launch_bwd_dkdv(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                            const CUtensorMap& tdo, const BwdArgs& a, cudaStream_t st);
+cudaError_t launch_bwd_dq_convert(const BwdArgs& a, cudaStream_t st);
+
+}  // namespace lcattn

@@ -1,0 +1,176 @@
+// Mask compiler: tile classification, compacted tile lists and longest-first
+// orders (the step that lets the attention kernels skip masked-out tiles and
+// run full tiles without any per-element mask).
+//
+// The pages credit FlashMask's column-wise mask representation with making
+// heterogeneous masks efficient ("Long-Context Attention Benchmark", xllm-io
+// blog review, sections "掩码支持" and "关键洞察"); the descriptor here carries the
+// allowed query rows of every key column as two intervals, and this compiler
+// reduces it once per 128x128 tile to EMPTY / FULL / PARTIAL.
+#include "lcattn_internal.cuh"
+
+namespace lcattn {
+namespace {
+
+__device__ __forceinline__ int ilen(int a, int b, int r0, int r1) {
+  const int lo = max(a, r0), hi = min(b, r1);
+  return hi > lo ? hi - lo : 0;
+}
+
+// Largest idx in [0, n) with offs[idx] <= x (offs nondecreasing, offs[0] <= x).
+__device__ __forceinline__ int block_of(const int32_t* offs, int n, int x) {
+  int lo = 0, hi = n - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (__ldg(offs + mid) <= x) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+// Checks that block offsets run nondecreasing from 0 to S.
+__global__ void validate_offsets_kernel(MaskDev m, int Sq, int Sk, int32_t* status) {
+  if (threadIdx.x != 0 || blockIdx.x != 0) return;
+  bool ok = m.nQb > 0 && m.nKb > 0 && m.q_offs[0] == 0 && m.k_offs[0] == 0 &&
+            m.q_offs[m.nQb] == Sq && m.k_offs[m.nKb] == Sk;
+  for (int i = 0; ok && i < m.nQb; ++i) ok = m.q_offs[i] <= m.q_offs[i + 1];
+  for (int i = 0; ok && i < m.nKb; ++i) ok = m.k_offs[i] <= m.k_offs[i + 1];
+  if (!ok) atomicCAS(status, 0, LCATTN_ERR_DEVICE_MASK);
+}
+
+// One warp per tile.  Column bounds: count the allowed rows of each column
+// inside the tile's row range (union of the two intervals) and compare the sum
+// with the tile's in-range area.  Block map: look at every (query block, key
+// block) pair that overlaps the tile.
+__global__ void classify_kernel(ProblemDev pr, MaskDev m, TileMetaDev t) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warps_total = (int64_t)gridDim.x * (blockDim.x >> 5);
+  const int64_t total = (int64_t)t.B * t.nH * t.nQt * t.nKt;
+  for (int64_t w = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); w < total;
+       w += warps_total) {
+    const int kt = (int)(w % t.nKt);
+    const int qt = (int)((w / t.nKt) % t.nQt);
+    const int h = (int)((w / ((int64_t)t.nKt * t.nQt)) % t.nH);
+    const int b = (int)(w / ((int64_t)t.nKt * t.nQt * t.nH));
+    const int r0 = qt * kBM, r1 = min(pr.Sq, r0 + kBM);
+    const int c0 = kt * kBN, c1 = min(pr.Sk, c0 + kBN);
+    uint8_t cls;
+    if (m.kind == LCATTN_MASK_COLBOUNDS) {
+      int cnt = 0;
+      const int4* cb = m.col_bounds + (int64_t)b * pr.Sk;
+      for (int j = c0 + lane; j < c1; j += 32) {
+        const int4 v = __ldg(cb + j);
+        cnt += ilen(v.x, v.y, r0, r1) + ilen(v.z, v.w, r0, r1) -
+               ilen(max(v.x, v.z), min(v.y, v.w), r0, r1);
+      }
+      #pragma unroll
+      for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
+      const int area = (r1 - r0) * (c1 - c0);
+      cls = cnt == 0 ? LCATTN_TILE_EMPTY : (cnt == area ? LCATTN_TILE_FULL : LCATTN_TILE_PARTIAL);
+    } else {
+      const int qb0 = block_of(m.q_offs, m.nQb, r0), qb1 = block_of(m.q_offs, m.nQb, r1 - 1);
+      const int kb0 = block_of(m.k_offs, m.nKb, c0), kb1 = block_of(m.k_offs, m.nKb, c1 - 1);
+      const int nk = kb1 - kb0 + 1;
+      const int64_t npairs = (int64_t)(qb1 - qb0 + 1) * nk;
+      const uint8_t* map = m.block_map + (((int64_t)b * pr.Hq + h) * m.nQb) * m.nKb;
+      bool any_keep = false, any_drop = false;
+      for (int64_t p = lane; p < npairs; p += 32) {
+        const int qb = qb0 + (int)(p / nk), kb = kb0 + (int)(p % nk);
+        const int qlen = min(__ldg(m.q_offs + qb + 1), r1) - max(__ldg(m.q_offs + qb), r0);
+        const int klen = min(__ldg(m.k_offs + kb + 1), c1) - max(__ldg(m.k_offs + kb), c0);
+        if (qlen <= 0 || klen <= 0) continue;
+        if (__ldg(map + (int64_t)qb * m.nKb + kb)) any_keep = true; else any_drop = true;
+      }
+      any_keep = __any_sync(0xffffffffu, any_keep);
+      any_drop = __any_sync(0xffffffffu, any_drop);
+      cls = !any_keep ? LCATTN_TILE_EMPTY : (any_drop ? LCATTN_TILE_PARTIAL : LCATTN_TILE_FULL);
+    }
+    if (lane == 0) t.cls[w] = cls;
+  }
+}
+
+// One warp per row of tiles (forward: fixed query tile) or column of tiles
+// (backward: fixed key tile); non-empty entries are compacted in order with a
+// ballot prefix.
+template <bool kByQuery>
+__global__ void list_kernel(TileMetaDev t) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warps_total = (int64_t)gridDim.x * (blockDim.x >> 5);
+  const int nOuter = kByQuery ? t.nQt : t.nKt;
+  const int nInner = kByQuery ? t.nKt : t.nQt;
+  const int64_t total = (int64_t)t.B * t.nH * nOuter;
+  for (int64_t w = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); w < total;
+       w += warps_total) {
+    const int outer = (int)(w % nOuter);
+    const int64_t bh = w / nOuter;
+    const uint8_t* cls = t.cls + bh * t.nQt * t.nKt;
+    int32_t* lst = (kByQuery ? t.fwd_lst : t.bwd_lst) + w * nInner;
+    int n = 0;
+    for (int i0 = 0; i0 < nInner; i0 += 32) {
+      const int i = i0 + lane;
+      uint8_t c = LCATTN_TILE_EMPTY;
+      if (i < nInner) c = kByQuery ? cls[(int64_t)outer * t.nKt + i] : cls[(int64_t)i * t.nKt + outer];
+      const unsigned bal = __ballot_sync(0xffffffffu, c != LCATTN_TILE_EMPTY);
+      if (c != LCATTN_TILE_EMPTY)
+        lst[n + __popc(bal & ((1u << lane) - 1u))] = (i << 1) | (c == LCATTN_TILE_PARTIAL ? 1 : 0);
+      n += __popc(bal);
+    }
+    if (lane == 0) (kByQuery ? t.fwd_cnt : t.bwd_cnt)[w] = n;
+  }
+}
+
+// Longest-first order of the tiles of one (batch, list head): item i goes to
+// rank #{j : cnt[j] > cnt[i]} + #{j < i : cnt[j] == cnt[i]} (stable).
+template <bool kByQuery>
+__global__ void order_kernel(TileMetaDev t) {
+  extern __shared__ int32_t cnt_s[];
+  const int n = kByQuery ? t.nQt : t.nKt;
+  const int64_t bh = blockIdx.x;
+  const int32_t* cnt = (kByQuery ? t.fwd_cnt : t.bwd_cnt) + bh * n;
+  int32_t* ord = (kByQuery ? t.fwd_ord : t.bwd_ord) + bh * n;
+  for (int i = threadIdx.x; i < n; i += blockDim.x) cnt_s[i] = cnt[i];
+  __syncthreads();
+  for (int i = threadIdx.x; i < n; i += blockDim.x) {
+    const int ci = cnt_s[i];
+    int r = 0;
+    for (int j = 0; j < n; ++j) {
+      const int cj = cnt_s[j];
+      r += (cj > ci) || (cj == ci && j < i);
+    }
+    ord[r] = i;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_mask_compile(const ProblemDev& pr, const MaskDev& m, const TileMetaDev& t,
+                                cudaStream_t st) {
+  cudaError_t e = cudaMemsetAsync(t.status, 0, 16, st);
+  if (e != cudaSuccess) return e;
+  if (m.kind == LCATTN_MASK_BLOCKMAP) {
+    validate_offsets_kernel<<<1, 32, 0, st>>>(m, pr.Sq, pr.Sk, t.status);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  int dev = 0, nsm = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
+  const int threads = 256;
+  const int64_t tiles = (int64_t)t.B * t.nH * t.nQt * t.nKt;
+  int64_t blocks = (tiles + 7) / 8;
+  const int64_t cap = (int64_t)nsm * 16;
+  if (blocks > cap) blocks = cap;
+  classify_kernel<<<(unsigned)blocks, threads, 0, st>>>(pr, m, t);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  int64_t rows = (int64_t)t.B * t.nH * t.nQt;
+  list_kernel<true><<<(unsigned)((rows + 7) / 8), threads, 0, st>>>(t);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  int64_t cols = (int64_t)t.B * t.nH * t.nKt;
+  list_kernel<false><<<(unsigned)((cols + 7) / 8), threads, 0, st>>>(t);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  const unsigned nbh = (unsigned)(t.B * t.nH);
+  order_kernel<true><<<nbh, 1024, t.nQt * sizeof(int32_t), st>>>(t);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  order_kernel<false><<<nbh, 1024, t.nKt * sizeof(int32_t), st>>>(t);
+  return cudaGetLastError();
+}
+
+}  // namespace lcattn

@@ -1,0 +1,114 @@
+"""The C-ABI library loads, exports every declared entry point, and validates
+arguments on the host before launching anything (CPU only: no call here
+reaches the GPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+lc = pytest.importorskip("long_context_masked_mask_gb300")
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "lcattn.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(lcattn_\w+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported():
+    names = declared_functions()
+    assert "lcattn_fwd" in names and "lcattn_bwd" in names and "lcattn_mask_compile" in names
+    lib = ctypes.CDLL(lc._LIB_PATH)
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) == set(lc.EXPORTED)
+
+
+def _shape(B=1, S=256, Hq=4, Hkv=2, D=128):
+    s = lc.lcattn_shape()
+    s.B, s.Sq, s.Sk, s.Hq, s.Hkv, s.D = B, S, S, Hq, Hkv, D
+    for name, H in (("q_stride", Hq), ("k_stride", Hkv), ("v_stride", Hkv), ("o_stride", Hq)):
+        getattr(s, name)[:] = (S * H * 128, H * 128, 128)
+    return s
+
+
+def _colbounds_desc(ptr=0x1000):
+    d = lc.lcattn_mask_desc()
+    d.kind = lc.LCATTN_MASK_COLBOUNDS
+    d.col_bounds = ptr
+    return d
+
+
+def _layout(shape, desc):
+    L = lc.lcattn_tile_meta_layout()
+    st = lc.library().lcattn_tile_meta_layout_of(ctypes.byref(shape), ctypes.byref(desc), ctypes.byref(L))
+    return st, L
+
+
+def test_layout_sizes_and_alignment():
+    st, L = _layout(_shape(S=300), _colbounds_desc())
+    assert st == 0
+    assert (L.nQt, L.nKt, L.nH, L.B) == (3, 3, 1, 1)
+    offs = [L.off_status, L.off_class, L.off_fwd_cnt, L.off_fwd_lst, L.off_fwd_ord,
+            L.off_bwd_cnt, L.off_bwd_lst, L.off_bwd_ord, L.total_bytes]
+    assert all(o % 256 == 0 for o in offs) and offs == sorted(offs)
+    assert L.off_fwd_lst - L.off_fwd_cnt >= 4 * 3
+    assert L.off_fwd_ord - L.off_fwd_lst >= 4 * 9
+    # block maps carry one list per query head
+    d = lc.lcattn_mask_desc()
+    d.kind, d.block_map, d.q_block_offs, d.k_block_offs, d.nQb, d.nKb = 2, 0x1000, 0x2000, 0x3000, 3, 3
+    st, L = _layout(_shape(S=300, Hq=4), d)
+    assert st == 0 and L.nH == 4
+
+
+@pytest.mark.parametrize("field,value,status", [
+    ("D", 64, lc.LCATTN_ERR_UNSUPPORTED),
+    ("Hkv", 3, lc.LCATTN_ERR_UNSUPPORTED),
+    ("Sq", 0, lc.LCATTN_ERR_INVALID_ARG),
+    ("B", 0, lc.LCATTN_ERR_INVALID_ARG),
+])
+def test_shape_validation(field, value, status):
+    s = _shape()
+    setattr(s, field, value)
+    st, _ = _layout(s, _colbounds_desc())
+    assert st == status
+    assert lc.library().lcattn_tile_meta_size(ctypes.byref(s), ctypes.byref(_colbounds_desc())) == 0
+
+
+def test_stride_and_descriptor_validation():
+    s = _shape()
+    s.q_stride[2] = 130  # not a multiple of 8 elements
+    assert _layout(s, _colbounds_desc())[0] == lc.LCATTN_ERR_UNSUPPORTED
+    assert _layout(_shape(), _colbounds_desc(ptr=0))[0] == lc.LCATTN_ERR_INVALID_ARG
+    d = lc.lcattn_mask_desc()
+    d.kind = 7
+    assert _layout(_shape(), d)[0] == lc.LCATTN_ERR_INVALID_ARG
+    d.kind = lc.LCATTN_MASK_BLOCKMAP  # null block map
+    assert _layout(_shape(), d)[0] == lc.LCATTN_ERR_INVALID_ARG
+
+
+def test_calls_reject_bad_pointers_before_launch():
+    lib = lc.library()
+    s, d = _shape(), _colbounds_desc()
+    st = lib.lcattn_fwd(ctypes.byref(s), None, 0x1000, 0x1000, 0x1000, ctypes.byref(d), 0.1, 0x1000, 0x1000, None)
+    assert st == lc.LCATTN_ERR_INVALID_ARG
+    st = lib.lcattn_fwd(ctypes.byref(s), 0x1008, 0x1000, 0x1000, 0x1000, ctypes.byref(d), 0.1, 0x1000, 0x1000, None)
+    assert st == lc.LCATTN_ERR_UNSUPPORTED  # misaligned q
+    st = lib.lcattn_fwd(ctypes.byref(s), 0x1000, 0x1000, 0x1000, 0x1000, ctypes.byref(d), -1.0, 0x1000, 0x1000, None)
+    assert st == lc.LCATTN_ERR_INVALID_ARG  # bad scale
+    st = lib.lcattn_mask_compile(ctypes.byref(s), ctypes.byref(d), 0x1000, 16, None)
+    assert st == lc.LCATTN_ERR_WORKSPACE
+    ws = lib.lcattn_bwd_workspace_size(ctypes.byref(s))
+    assert ws == 4 * 4 * 256 + 4 * 256 * 4 * 128
+    st = lib.lcattn_bwd(ctypes.byref(s), *([0x1000] * 7), ctypes.byref(d), 0.1, 0x1000, 0x1000, 0x1000,
+                        0x1000, ws - 1, None)
+    assert st == lc.LCATTN_ERR_WORKSPACE
+
+
+def test_status_strings():
+    for code in range(-6, 1):
+        assert lc.status_string(code) not in ("", "unknown status")
+    assert lc.status_string(-99) == "unknown status"
+    assert lc.library().lcattn_version() >= 100

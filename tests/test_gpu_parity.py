@@ -1,0 +1,201 @@
+"""GPU parity at sizes the oracle finishes in seconds (spanning several tiles and
+a ragged tail): every mask family, MHA and GQA, both descriptor kinds.  All
+calls go through the C ABI.  Bars: O max-abs <= 2e-2 and relative Frobenius
+<= 1e-2; dQ/dK/dV relative Frobenius <= 3e-2; LSE max-abs <= 5e-3 with -inf
+at exactly the oracle's -inf rows; tile classes bit-exact."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from synthetic import MaskSpec, block_keep, qkv, segment_lengths
+
+pytestmark = pytest.mark.gpu
+
+lc = pytest.importorskip("long_context_masked_mask_gb300")
+
+O_MAXABS, O_RELF, G_RELF, LSE_MAXABS = 2e-2, 1e-2, 3e-2, 5e-3
+
+
+def relf(g, r):
+    nr = np.linalg.norm(r)
+    return float(np.linalg.norm(g - r) / nr) if nr > 0 else float(np.linalg.norm(g))
+
+
+def spec_for(kind, N, Hq, seed=0):
+    docs = segment_lengths(N, max(1, N // 6), max(2, N // 2), seed)
+    if kind == "FULL":
+        return MaskSpec("FULL")
+    if kind == "CAUSAL":
+        return MaskSpec("CAUSAL")
+    if kind == "FULL_DOCUMENT":
+        return MaskSpec("FULL_DOCUMENT", {"doc_lens": docs})
+    if kind == "CAUSAL_DOCUMENT":
+        return MaskSpec("CAUSAL_DOCUMENT", {"doc_lens": docs})
+    if kind == "FULL_SLIDING_WINDOW":
+        return MaskSpec("FULL_SLIDING_WINDOW", {"window": max(1, N // 5)})
+    if kind == "CAUSAL_SLIDING_WINDOW":
+        return MaskSpec("CAUSAL_SLIDING_WINDOW", {"window": max(1, N // 4)})
+    if kind == "SHARED_QUESTION":
+        q = N // 4
+        return MaskSpec("SHARED_QUESTION", {"question_len": q,
+                                            "answer_lens": segment_lengths(N - q, 20, N // 3, seed + 1)})
+    if kind == "GLOBAL_SLIDING":
+        return MaskSpec("GLOBAL_SLIDING", {"global_tokens": max(1, N // 16), "window": max(1, N // 8)})
+    if kind == "CAUSAL_BLOCKWISE":
+        return MaskSpec("CAUSAL_BLOCKWISE", {"block": max(1, N // 5)})
+    if kind == "PREFIX_LM_CAUSAL":
+        return MaskSpec("PREFIX_LM_CAUSAL", {"prefix": N // 3})
+    if kind == "PREFIX_LM_DOCUMENT":
+        return MaskSpec("PREFIX_LM_DOCUMENT", {"doc_lens": docs, "prefix_lens": [L // 2 for L in docs]})
+    if kind == "BLOCK_CAUSAL_DOCUMENT":
+        blocks = [segment_lengths(L, 16, 96, seed + 5 + i) for i, L in enumerate(docs)]
+        return MaskSpec("BLOCK_CAUSAL_DOCUMENT", {"doc_lens": docs, "block_lens": blocks})
+    if kind == "UNIFORM_BLOCK":
+        bs = 64
+        nb = -(-N // bs)
+        return MaskSpec("UNIFORM_BLOCK", {"block": bs, "keep": block_keep(Hq, nb, nb, 0.5, seed)})
+    if kind == "UNIFORM_BLOCK_128":
+        nb = -(-N // 128)
+        return MaskSpec("UNIFORM_BLOCK", {"block": 128, "keep": block_keep(Hq, nb, nb, 0.5, seed)})
+    if kind == "VARIABLE_BLOCK":
+        ql = segment_lengths(N, 32, 200, seed + 2)
+        kl = segment_lengths(N, 32, 200, seed + 3)
+        return MaskSpec("VARIABLE_BLOCK", {"q_block_lens": ql, "k_block_lens": kl,
+                                           "keep": block_keep(Hq, len(ql), len(kl), 0.5, seed, force_diagonal=False)})
+    raise KeyError(kind)
+
+
+KINDS = ["FULL", "CAUSAL", "FULL_DOCUMENT", "CAUSAL_DOCUMENT", "FULL_SLIDING_WINDOW",
+         "CAUSAL_SLIDING_WINDOW", "SHARED_QUESTION", "GLOBAL_SLIDING", "CAUSAL_BLOCKWISE",
+         "PREFIX_LM_CAUSAL", "PREFIX_LM_DOCUMENT", "BLOCK_CAUSAL_DOCUMENT", "UNIFORM_BLOCK",
+         "UNIFORM_BLOCK_128", "VARIABLE_BLOCK"]
+
+
+def run_and_compare(spec, B, N, Hq, Hkv, seed=0, check_classes=True):
+    D = 128
+    x = qkv(B, N, Hq, Hkv, D, seed=seed)
+    dev = {k: t.cuda() for k, t in x.items()}
+    out = lc.attention(dev["q"], dev["k"], dev["v"], spec, d_o=dev["do"])
+    torch.cuda.synchronize()
+    assert lc.lcattn_read_status(out["tile_meta"]) == 0
+    f64 = {k: t.double().numpy() for k, t in x.items()}
+    scale = 1.0 / math.sqrt(D)
+    dQ, dK, dV, O, LSE = oracle.attention_bwd(f64["q"], f64["k"], f64["v"], f64["do"], spec, scale)
+    o = out["o"].double().cpu().numpy()
+    lse = out["lse"].double().cpu().numpy()
+    assert np.abs(o - O).max() <= O_MAXABS, np.abs(o - O).max()
+    assert relf(o, O) <= O_RELF, relf(o, O)
+    inf_ref = np.isneginf(LSE)
+    np.testing.assert_array_equal(np.isneginf(lse), inf_ref)
+    if (~inf_ref).any():
+        assert np.abs(lse[~inf_ref] - LSE[~inf_ref]).max() <= LSE_MAXABS
+    for name, ref in (("dq", dQ), ("dk", dK), ("dv", dV)):
+        g = out[name].double().cpu().numpy()
+        assert np.isfinite(g).all(), name
+        assert relf(g, ref) <= G_RELF, (name, relf(g, ref))
+    if check_classes:
+        shape = lc.make_shape(dev["q"], dev["k"], dev["v"])
+        cls = lc.tile_classes(out["tile_meta"], shape, out["mask"]).cpu().numpy()
+        heads = range(Hq) if spec.per_head else [0]
+        for b in range(B):
+            for hi, h in enumerate(heads):
+                np.testing.assert_array_equal(cls[b, hi], oracle.classify_tiles(spec, N, 128, 128, head=h))
+    return out, (dQ, dK, dV, O, LSE)
+
+
+@pytest.mark.parametrize("kind", KINDS)
+def test_mask_family_gqa_ragged(kind):
+    N, Hq, Hkv = 392, 4, 2
+    run_and_compare(spec_for(kind, N, Hq), 1, N, Hq, Hkv)
+
+
+@pytest.mark.parametrize("kind", ["CAUSAL", "GLOBAL_SLIDING", "SHARED_QUESTION", "UNIFORM_BLOCK"])
+def test_mha_and_batch(kind):
+    N, Hq = 512, 2
+    run_and_compare(spec_for(kind, N, Hq, seed=3), 2, N, Hq, Hq, seed=1)
+
+
+@pytest.mark.parametrize("Hq,Hkv", [(6, 2), (8, 1)])
+def test_odd_and_wide_groups(Hq, Hkv):
+    run_and_compare(spec_for("CAUSAL_DOCUMENT", 300, Hq), 1, 300, Hq, Hkv, seed=2)
+
+
+@pytest.mark.parametrize("N", [1, 2, 127, 128, 129])
+def test_tiny_and_boundary_lengths(N):
+    run_and_compare(MaskSpec("CAUSAL"), 1, N, 2, 1, seed=4)
+    run_and_compare(MaskSpec("FULL"), 1, N, 2, 2, seed=5)
+
+
+def test_fully_masked_rows():
+    """Query blocks whose keep row is all zero: O = 0, LSE = -inf, dQ = 0."""
+    N, Hq, bs = 384, 2, 64
+    nb = N // bs
+    keep = np.ones((Hq, nb, nb), dtype=bool)
+    keep[:, 2, :] = False      # rows 128..191: nothing allowed (inside a partial tile row)
+    keep[0, 4:6, :] = False    # head 0, rows 256..383: an entire query tile with no key
+    spec = MaskSpec("UNIFORM_BLOCK", {"block": bs, "keep": keep})
+    out, (dQ, dK, dV, O, LSE) = run_and_compare(spec, 1, N, Hq, 1, seed=6)
+    o = out["o"].float().cpu().numpy()
+    dq = out["dq"].float().cpu().numpy()
+    assert (o[0, 128:192] == 0).all() and (dq[0, 128:192] == 0).all()
+    assert (o[0, 256:, 0] == 0).all() and (dq[0, 256:, 0] == 0).all()
+    assert np.isneginf(out["lse"].cpu().numpy()[0, 0, 256:]).all()
+
+
+def test_key_tile_seen_by_no_query():
+    """A key tile no query attends gets dK = dV = 0 (written, not left stale)."""
+    N, Hq = 384, 2
+    nb = 3
+    keep = np.ones((Hq, nb, nb), dtype=bool)
+    keep[:, :, 1] = False
+    spec = MaskSpec("UNIFORM_BLOCK", {"block": 128, "keep": keep})
+    x = qkv(1, N, Hq, 1, 128, seed=8)
+    dev = {k: t.cuda() for k, t in x.items()}
+    mask = lc.DeviceMask(spec, N, Hq)
+    shape = lc.make_shape(dev["q"], dev["k"], dev["v"])
+    meta = lc.lcattn_mask_compile(shape, mask)
+    o, lse = lc.lcattn_fwd(dev["q"], dev["k"], dev["v"], mask, meta)
+    dk = torch.full_like(dev["k"], 7.0)
+    dv = torch.full_like(dev["v"], 7.0)
+    lc.lcattn_bwd(dev["q"], dev["k"], dev["v"], o, dev["do"], lse, mask, meta, dk=dk, dv=dv)
+    torch.cuda.synchronize()
+    assert (dk[0, 128:256] == 0).all() and (dv[0, 128:256] == 0).all()
+
+
+def test_tile_lists_consistent_with_classes():
+    N, Hq = 1000, 2
+    spec = spec_for("GLOBAL_SLIDING", N, Hq)
+    x = qkv(1, N, Hq, 1, 128, seed=0, with_do=False)
+    dev = {k: t.cuda() for k, t in x.items()}
+    mask = lc.DeviceMask(spec, N, Hq)
+    shape = lc.make_shape(dev["q"], dev["k"], dev["v"])
+    meta = lc.lcattn_mask_compile(shape, mask)
+    cls = lc.tile_classes(meta, shape, mask).cpu().numpy()[0, 0]
+    fc, fl, fo, bc, bl, bo = (t.cpu().numpy() for t in lc.tile_lists(meta, shape, mask))
+    nq, nk = cls.shape
+    for qt in range(nq):
+        want = [(kt << 1) | int(cls[qt, kt] == 2) for kt in range(nk) if cls[qt, kt] != 0]
+        assert fc[0, qt] == len(want) and list(fl[0, qt, :len(want)]) == want
+    for kt in range(nk):
+        want = [(qt << 1) | int(cls[qt, kt] == 2) for qt in range(nq) if cls[qt, kt] != 0]
+        assert bc[0, kt] == len(want) and list(bl[0, kt, :len(want)]) == want
+    assert sorted(fo[0]) == list(range(nq)) and sorted(bo[0]) == list(range(nk))
+    assert all(fc[0, fo[0, i]] >= fc[0, fo[0, i + 1]] for i in range(nq - 1))
+    assert all(bc[0, bo[0, i]] >= bc[0, bo[0, i + 1]] for i in range(nk - 1))
+
+
+def test_bad_block_offsets_reported_on_device():
+    N, Hq = 256, 1
+    spec = MaskSpec("VARIABLE_BLOCK", {"q_block_lens": [100, 156], "k_block_lens": [128, 128],
+                                       "keep": np.ones((1, 2, 2), bool)})
+    mask = lc.DeviceMask(spec, N, Hq)
+    mask.q_offs.copy_(torch.tensor([0, 200, 100], dtype=torch.int32))  # not nondecreasing, wrong end
+    q = torch.zeros(1, N, Hq, 128, dtype=torch.bfloat16, device="cuda")
+    shape = lc.make_shape(q, q, q)
+    meta = lc.lcattn_mask_compile(shape, mask)
+    assert lc.lcattn_read_status(meta) == lc.LCATTN_ERR_DEVICE_MASK
+    lc.lcattn_clear_status(meta)
+    assert lc.lcattn_read_status(meta) == 0
