@@ -1,0 +1,444 @@
+#!/usr/bin/env python
+"""Benchmark: effective attention TFLOP/s (forward + backward, unmasked FLOPs).
+
+One step is the whole hot path over one synthetic batch, for every mask of the
+workload: mask compile -> forward -> backward (D pre-pass, dK/dV, dQ).  The
+default workload is dense attention at 8K: B=1, N=8192, GQA 64:8, head dim
+128, bf16, FULL and CAUSAL masks.
+
+Effective FLOPs count only allowed (query, key) pairs: forward 4*D per pair
+and query head, backward 2.5x the forward (five GEMMs against two).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+    python bench.py --impl reference ...   # the fp64 CPU oracle, same metric
+
+Under torchrun every rank runs its own copy of the workload on its own GPU
+(weak scaling, no collective on the data path); rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "effective attention TFLOP/s fwd/bwd (unmasked FLOPs) and % of GB300 bf16 peak"
+UNIT = "TFLOP/s"
+L2_FLUSH_BYTES = 512 << 20  # > 129 MB of L2, written before every timed step
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="lcattn", choices=["lcattn", "reference"])
+    ap.add_argument("--workload", default="dense_8k")
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--breakdown-reps", type=int, default=5)
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--out", default=None, help="also write the JSON line to this file")
+    return ap.parse_args()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return {"burst": float(p["bf16_tflops"]), "sustained": float(p["bf16_tflops_sustained"]),
+                "hbm_gbs": float(p["hbm_gbs"]), "source": "measured"}
+    return {"burst": 1900.0, "sustained": 1700.0, "hbm_gbs": 6800.0, "source": "fallback"}
+
+
+def workload_desc(wl):
+    return (f"{wl.name}: B={wl.B}, N={wl.N}, Hq:Hkv={wl.Hq}:{wl.Hkv}, hd={wl.D}, bf16, masks "
+            + "+".join(s.label() for s in wl.masks))
+
+
+# ----------------------------------------------------------------------------
+# oracle timing (CPU): the bounded sample shared by cpu_baseline and --impl reference
+# ----------------------------------------------------------------------------
+
+def oracle_sample(wl, seed):
+    """Inputs for the oracle sample: query head 0 with its KV head over the full
+    sequence, every mask of the workload."""
+    import numpy as np
+    from synthetic import qkv
+    x = qkv(1, wl.N, 1, 1, wl.D, seed=seed)
+    return {k: t.double().numpy() for k, t in x.items()}
+
+
+def oracle_step(wl, sample):
+    """One oracle pass over the sample; returns effective FLOPs of the sample."""
+    import oracle
+    flops = 0.0
+    scale = 1.0 / math.sqrt(wl.D)
+    for spec in wl.masks:
+        oracle.attention_bwd(sample["q"], sample["k"], sample["v"], sample["do"], spec, scale)
+        pairs = oracle.allowed_pairs(spec, wl.N, head=0)
+        flops += 4.0 * wl.D * pairs * 3.5
+    return flops
+
+
+def cpu_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads") for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n and n[0]:
+            return int(n[0])
+    except Exception:
+        pass
+    return os.cpu_count()
+
+
+def cpu_baseline(wl, seed):
+    sample = oracle_sample(wl, seed)
+    t0 = time.perf_counter()
+    flops = oracle_step(wl, sample)
+    dt = time.perf_counter() - t0
+    return {"value": flops / dt / 1e12, "unit": UNIT, "cores": cpu_threads(), "kind": "oracle",
+            "seconds": round(dt, 3),
+            "sample": f"fp64 NumPy oracle fwd+bwd, query head 0 / KV head 0 of {wl.name} over the full "
+                      f"N={wl.N}, masks {'+'.join(s.label() for s in wl.masks)}; effective FLOPs of that head"}
+
+
+def run_reference(args, rank, world):
+    from synthetic import workload
+    wl = workload(args.workload, args.seed)
+    if rank != 0:
+        return
+    sample = oracle_sample(wl, args.seed)
+    for _ in range(args.warmup):
+        oracle_step(wl, sample)
+    times, flops = [], 0.0
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        flops = oracle_step(wl, sample)
+        times.append(time.perf_counter() - t0)
+    ms = 1e3 * statistics.mean(times)
+    value = flops / (ms / 1e3) / 1e12
+    sample_desc = (f"query head 0 / KV head 0 of {wl.name} over the full N={wl.N}, "
+                   f"masks {'+'.join(s.label() for s in wl.masks)}")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": workload_desc(wl), "sample": sample_desc},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_threads(), "kind": "oracle",
+                             "sample": sample_desc},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    emit(line, args)
+
+
+def emit(line, args):
+    text = json.dumps(line)
+    print(text, flush=True)
+    if args.out:
+        with open(args.out, "w") as f:
+            f.write(text + "\n")
+
+
+# ----------------------------------------------------------------------------
+# clocks
+# ----------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,utilization.gpu,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.path = tempfile.mktemp(prefix="clocks_", suffix=".csv")
+        self.proc = None
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200", "-i", str(gpu_index)], stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 10:
+                    continue
+                try:
+                    rows.append({"sm": float(parts[1]), "max": float(parts[2]), "util": float(parts[4]),
+                                 "hw": parts[6], "hw_th": parts[7], "sw_th": parts[8], "pcap": parts[9]})
+                except ValueError:
+                    continue
+        os.unlink(self.path)
+        if not rows:
+            return None
+        load = [r for r in rows if r["util"] >= 50] or rows
+        reasons = set()
+        for r in load:
+            for key, name in (("hw", "hw_slowdown"), ("hw_th", "hw_thermal_slowdown"),
+                              ("sw_th", "sw_thermal_slowdown"), ("pcap", "sw_power_cap")):
+                if r[key].lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in load), "sm_max_mhz": max(r["max"] for r in rows),
+                "reasons": sorted(reasons), "samples": len(load)}
+
+
+# ----------------------------------------------------------------------------
+# GPU arm
+# ----------------------------------------------------------------------------
+
+def traffic_lookup(kernel):
+    """DRAM bytes per launch recorded from an ncu capture, if the kernel's source
+    has not changed since (profiles/traffic.json)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        rec = json.load(f).get(kernel)
+    if not rec:
+        return None
+    src = os.path.join(ROOT, "long_context_masked_mask_gb300", "csrc", rec["source"])
+    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
+    return rec["dram_bytes_per_launch"] if sha == rec["source_sha256"] else None
+
+
+def run_gpu(args, rank, world, dist):
+    import torch
+    import long_context_masked_mask_gb300 as lc
+    from synthetic import qkv, qkv_device, workload
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    wl = workload(args.workload, args.seed)
+    B, N, Hq, Hkv, D = wl.B, wl.N, wl.Hq, wl.Hkv, wl.D
+    seed = args.seed + 1000 * rank
+    if wl.device_inputs:
+        x = qkv_device(B, N, Hq, Hkv, D, seed=seed, device=str(dev))
+    else:
+        x = {k: t.to(dev) for k, t in qkv(B, N, Hq, Hkv, D, seed=seed).items()}
+    q, k, v, d_o = x["q"], x["k"], x["v"], x["do"]
+    shape = lc.make_shape(q, k, v)
+    ws = torch.empty(lc.lcattn_bwd_workspace_size(shape), dtype=torch.uint8, device=dev)
+    runs = []
+    for spec in wl.masks:
+        m = lc.DeviceMask(spec, N, Hq, B, device=dev)
+        meta = lc.lcattn_mask_compile(shape, m, device=dev)
+        fwd_flops = 4.0 * D * m.allowed_pairs
+        runs.append({"spec": spec, "mask": m, "meta": meta, "o": torch.empty_like(q),
+                     "lse": torch.empty(B, Hq, N, dtype=torch.float32, device=dev),
+                     "dq": torch.empty_like(q), "dk": torch.empty_like(k), "dv": torch.empty_like(v),
+                     "fwd_flops": fwd_flops, "bwd_flops": 2.5 * fwd_flops,
+                     "launches": (6 if spec.per_head else 5) + 1 + 3})
+    step_flops = sum(r["fwd_flops"] + r["bwd_flops"] for r in runs)
+    launches_per_step = sum(r["launches"] for r in runs)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(qq=q, kk=k, vv=v, dd=d_o):
+        for r in runs:
+            lc.lcattn_mask_compile(shape, r["mask"], r["meta"])
+            lc.lcattn_fwd(qq, kk, vv, r["mask"], r["meta"], o=r["o"], lse=r["lse"])
+            lc.lcattn_bwd(qq, kk, vv, r["o"], dd, r["lse"], r["mask"], r["meta"],
+                          dq=r["dq"], dk=r["dk"], dv=r["dv"], workspace=ws)
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    for r in runs:
+        st = lc.lcattn_read_status(r["meta"])
+        if st != 0:
+            raise RuntimeError(f"device status {st}: {lc.status_string(st)}")
+
+    # ---- timed region -------------------------------------------------------
+    try:
+        gpu_sel = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        gpu_sel = str(local)
+    sampler = ClockSampler(gpu_sel)
+    time.sleep(0.3)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    barrier()
+    torch.cuda.synchronize()
+    for e0, e1 in evs:
+        flush.zero_()
+        e0.record(stream)
+        step()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    clocks = sampler.stop()
+    ms_steps = [e0.elapsed_time(e1) for e0, e1 in evs]
+    ms = statistics.mean(ms_steps)
+    if dist is not None:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    value = world * step_flops / (ms / 1e3) / 1e12
+
+    # ---- per-kernel breakdown (CUDA events on the launching stream) ---------
+    pk = peaks()
+    kernels = {"mask_compile": [0.0, 0.0, 0], "fwd_kernel": [0.0, 0.0, 0],
+               "bwd_prepass": [0.0, 0.0, 0], "dkdv_kernel": [0.0, 0.0, 0], "dq_convert": [0.0, 0.0, 0]}
+    per_mask = []
+    reps = args.breakdown_reps
+
+    def timed(fn):
+        tot = 0.0
+        for _ in range(reps):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            tot += e0.elapsed_time(e1)
+        return tot / reps
+
+    for r in runs:
+        m, meta = r["mask"], r["meta"]
+        t_c = timed(lambda: lc.lcattn_mask_compile(shape, m, meta))
+        t_f = timed(lambda: lc.lcattn_fwd(q, k, v, m, meta, o=r["o"], lse=r["lse"]))
+        tb = []
+        for stage in (1, 2, 3):
+            tb.append(timed(lambda: lc.lcattn_bwd(q, k, v, r["o"], d_o, r["lse"], m, meta, dq=r["dq"],
+                                                  dk=r["dk"], dv=r["dv"], workspace=ws, stage=stage)))
+        for name, t, fl in (("mask_compile", t_c, 0.0), ("fwd_kernel", t_f, r["fwd_flops"]),
+                            ("bwd_prepass", tb[0], 0.0), ("dkdv_kernel", tb[1], r["bwd_flops"]),
+                            ("dq_convert", tb[2], 0.0)):
+            kernels[name][0] += t
+            kernels[name][1] += fl
+            kernels[name][2] += 1
+        fwd_tf = r["fwd_flops"] / (t_f / 1e3) / 1e12
+        bwd_tf = r["bwd_flops"] / (sum(tb) / 1e3) / 1e12
+        per_mask.append({"mask": r["spec"].label(), "allowed_pairs": r["mask"].allowed_pairs,
+                         "density": r["mask"].allowed_pairs / (B * Hq * N * N),
+                         "fwd_ms": round(t_f, 4), "bwd_ms": round(sum(tb), 4),
+                         "bwd_stage_ms": [round(t, 4) for t in tb], "mask_compile_ms": round(t_c, 4),
+                         "fwd_tflops": round(fwd_tf, 1), "bwd_tflops": round(bwd_tf, 1),
+                         "fwd_frac_of_peak": round(fwd_tf / pk["sustained"], 4),
+                         "bwd_frac_of_peak": round(bwd_tf / pk["sustained"], 4)})
+    dom = max(kernels, key=lambda n: kernels[n][0])
+    t_dom, fl_dom, n_dom = kernels[dom]
+    if fl_dom > 0:
+        achieved = fl_dom / (t_dom / 1e3) / 1e12
+        roof = {"kernel": dom, "bound": "tensor", "achieved": round(achieved, 1), "peak": pk["sustained"],
+                "unit": "TFLOP/s", "frac": round(achieved / pk["sustained"], 4),
+                "peak_kind": f"bf16 dense, {pk['source']} sustained"}
+    else:  # a memory-bound kernel dominating would be reported against HBM
+        roof = {"kernel": dom, "bound": "hbm", "achieved": None, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                "frac": None, "peak_kind": f"{pk['source']} copy bandwidth"}
+    tr = traffic_lookup(dom)
+    roof["traffic"] = tr
+
+    # ---- end to end through the C ABI with host buffers ----------------------
+    host = {n: t.cpu().pin_memory() for n, t in (("q", q), ("k", k), ("v", v), ("do", d_o))}
+    dq_, dk_, dv_, do_ = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v), torch.empty_like(d_o)
+    q_, k_, v_ = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    outs = [{n: torch.empty(r[n].shape, dtype=r[n].dtype, pin_memory=True) for n in ("o", "lse", "dq", "dk", "dv")}
+            for r in runs]
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = sum(t.numel() * t.element_size() for o in outs for t in o.values())
+    e2e_ms = []
+    for i in range(args.warmup + args.e2e_steps):
+        flush.zero_()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        q_.copy_(host["q"], non_blocking=True)
+        k_.copy_(host["k"], non_blocking=True)
+        v_.copy_(host["v"], non_blocking=True)
+        do_.copy_(host["do"], non_blocking=True)
+        step(q_, k_, v_, do_)
+        for r, o in zip(runs, outs):
+            for n in o:
+                o[n].copy_(r[n], non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        if i >= args.warmup:
+            e2e_ms.append(e0.elapsed_time(e1))
+    e2e_t = statistics.mean(e2e_ms)
+    if dist is not None:
+        t = torch.tensor([e2e_t], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_t = float(t.item())
+    e2e = {"value": world * step_flops / (e2e_t / 1e3) / 1e12, "unit": UNIT, "ms_per_step": e2e_t,
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+    for r in runs:
+        st = lc.lcattn_read_status(r["meta"])
+        if st != 0:
+            raise RuntimeError(f"device status {st}: {lc.status_string(st)}")
+
+    if rank != 0:
+        return
+    line = {"metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": workload_desc(wl), "seq_len": N, "global_batch": B * world,
+                       "heads": f"{Hq}:{Hkv}", "head_dim": D,
+                       "parallelism": f"replicas x{world} (independent batches, no collective)",
+                       "l2": f"flushed by a {L2_FLUSH_BYTES >> 20} MiB write before every timed step"},
+            "frac_of_peak": round(value / pk["sustained"], 4),
+            "peak_tflops": {"sustained": pk["sustained"], "burst": pk["burst"], "source": pk["source"]},
+            "per_mask": per_mask,
+            "kernel_ms": {n: round(v[0], 4) for n, v in kernels.items()},
+            "roofline": roof, "e2e": e2e, "gpu_launches": launches_per_step * args.steps,
+            "clocks": clocks}
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(wl, args.seed)
+    emit(line, args)
+
+
+def main():
+    args = parse()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist_mod
+        dist = dist_mod
+        if args.impl == "reference":
+            run_reference(args, rank, world)
+            return
+        import torch
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+        dist.init_process_group("nccl")
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    try:
+        run_gpu(args, rank, world, dist)
+    finally:
+        if dist is not None:
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

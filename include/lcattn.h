@@ -163,6 +163,17 @@ int lcattn_bwd(const lcattn_shape* shape, const void* q, const void* k, const vo
                const lcattn_mask_desc* mask, float scale, void* dq, void* dk, void* dv,
                void* workspace, size_t workspace_bytes, lcattn_stream_t stream);
 
+/* One stage of lcattn_bwd, same arguments: stage 1 = D pre-pass (and zeroing
+ * of the dQ accumulator), 2 = dK/dV with dQ partials, 3 = dQ conversion.
+ * Running stages 1, 2, 3 in order on one stream is exactly lcattn_bwd; the
+ * stages exist so that each kernel can be scheduled or timed on its own.
+ * Any other stage value returns LCATTN_ERR_INVALID_ARG.                   */
+int lcattn_bwd_stage(int stage, const lcattn_shape* shape, const void* q, const void* k,
+                     const void* v, const void* o, const void* d_o, const float* lse,
+                     const void* tile_meta, const lcattn_mask_desc* mask, float scale, void* dq,
+                     void* dk, void* dv, void* workspace, size_t workspace_bytes,
+                     lcattn_stream_t stream);
+
 /* Synchronises `stream`, then returns the first nonzero device status word of
  * `tile_meta` (LCATTN_ERR_DEVICE_*), or LCATTN_OK.  Clears nothing.          */
 int lcattn_read_status(const void* tile_meta, lcattn_stream_t stream);

@@ -47,7 +47,7 @@ BLOCK_M = BLOCK_N = 128
 # Every entry point include/lcattn.h declares.
 EXPORTED = (
     "lcattn_tile_meta_layout_of", "lcattn_tile_meta_size", "lcattn_mask_compile", "lcattn_fwd",
-    "lcattn_bwd_workspace_size", "lcattn_bwd", "lcattn_read_status", "lcattn_clear_status",
+    "lcattn_bwd_workspace_size", "lcattn_bwd", "lcattn_bwd_stage", "lcattn_read_status", "lcattn_clear_status",
     "lcattn_status_string", "lcattn_version",
 )
 
@@ -81,7 +81,7 @@ def _load():
     if not os.path.exists(_LIB_PATH):
         raise ImportError(
             f"{_LIB_PATH} is missing; build it with "
-            "`python -m long_context_masked_mask_gb300.build` (needs nvcc for sm_103a)")
+            "`python long_context_masked_mask_gb300/build.py` (needs nvcc for sm_103a)")
     lib = ctypes.CDLL(_LIB_PATH)
     P = ctypes.c_void_p
     S = ctypes.POINTER(lcattn_shape)
@@ -94,6 +94,8 @@ def _load():
         "lcattn_bwd_workspace_size": (ctypes.c_size_t, [S]),
         "lcattn_bwd": (ctypes.c_int, [S, P, P, P, P, P, P, P, M, ctypes.c_float, P, P, P, P,
                                       ctypes.c_size_t, P]),
+        "lcattn_bwd_stage": (ctypes.c_int, [ctypes.c_int, S, P, P, P, P, P, P, P, M, ctypes.c_float,
+                                            P, P, P, P, ctypes.c_size_t, P]),
         "lcattn_read_status": (ctypes.c_int, [P, P]),
         "lcattn_clear_status": (ctypes.c_int, [P, P]),
         "lcattn_status_string": (ctypes.c_char_p, [ctypes.c_int]),
@@ -229,8 +231,9 @@ def lcattn_bwd_workspace_size(shape: lcattn_shape) -> int:
 
 
 def lcattn_bwd(q, k, v, o, d_o, lse, mask: DeviceMask, tile_meta, scale: Optional[float] = None,
-               dq=None, dk=None, dv=None, workspace=None, stream=None):
-    """Backward: returns (dQ, dK, dV), bf16, laid out like q, k, v."""
+               dq=None, dk=None, dv=None, workspace=None, stream=None, stage: Optional[int] = None):
+    """Backward: returns (dQ, dK, dV), bf16, laid out like q, k, v.  With
+    ``stage`` in (1, 2, 3), runs only that stage (lcattn_bwd_stage)."""
     D = q.shape[3]
     if scale is None:
         scale = 1.0 / math.sqrt(D)
@@ -245,10 +248,14 @@ def lcattn_bwd(q, k, v, o, d_o, lse, mask: DeviceMask, tile_meta, scale: Optiona
     ws_bytes = lcattn_bwd_workspace_size(shape)
     if workspace is None:
         workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device)
-    _check(_lib.lcattn_bwd(ctypes.byref(shape), q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
-                           d_o.data_ptr(), lse.data_ptr(), tile_meta.data_ptr(), ctypes.byref(mask.desc),
-                           float(scale), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
-                           workspace.data_ptr(), workspace.numel(), _stream_ptr(stream)), "lcattn_bwd")
+    args = (ctypes.byref(shape), q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+            d_o.data_ptr(), lse.data_ptr(), tile_meta.data_ptr(), ctypes.byref(mask.desc),
+            float(scale), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
+            workspace.data_ptr(), workspace.numel(), _stream_ptr(stream))
+    if stage is None:
+        _check(_lib.lcattn_bwd(*args), "lcattn_bwd")
+    else:
+        _check(_lib.lcattn_bwd_stage(int(stage), *args), f"lcattn_bwd_stage({stage})")
     return dq, dk, dv
 
 

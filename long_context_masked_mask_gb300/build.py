@@ -2,11 +2,12 @@
 
 Each CUDA translation unit under ``csrc/`` is compiled by its own nvcc process
 (in parallel), then linked into ``liblcattn.so`` next to this file.  Run as
-``python -m long_context_masked_mask_gb300.build``.
+``python long_context_masked_mask_gb300/build.py`` (or ``__graft_entry__.build()``).
 """
 from __future__ import annotations
 
 import os
+import platform
 import shutil
 import subprocess
 import sys
@@ -37,6 +38,11 @@ def _stale(out: str, deps) -> bool:
 
 def build(verbose: bool = False, force: bool = False, extra_flags=()) -> str:
     os.makedirs(BUILD, exist_ok=True)
+    # Objects from another host architecture (or other flags) are never reused.
+    stamp = os.path.join(BUILD, "stamp.txt")
+    key = f"{platform.machine()} {' '.join(CFLAGS + list(extra_flags))}"
+    if not os.path.exists(stamp) or open(stamp).read() != key or not os.path.exists(LIB):
+        force = True
     headers = [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".cuh", ".h"))]
     headers.append(os.path.join(os.path.dirname(PKG), "include", "lcattn.h"))
     procs = []
@@ -65,6 +71,8 @@ def build(verbose: bool = False, force: bool = False, extra_flags=()) -> str:
         r = subprocess.run(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT)
         if r.returncode != 0:
             raise RuntimeError("link failed:\n" + r.stdout.decode(errors="replace"))
+    with open(stamp, "w") as f:
+        f.write(key)
     return LIB
 
 

@@ -199,10 +199,15 @@ size_t lcattn_bwd_workspace_size(const lcattn_shape* shape) {
   return (size_t)(d_bytes + acc_bytes);
 }
 
-int lcattn_bwd(const lcattn_shape* shape, const void* q, const void* k, const void* v,
-               const void* o, const void* d_o, const float* lse, const void* tile_meta,
-               const lcattn_mask_desc* mask, float scale, void* dq, void* dk, void* dv,
-               void* workspace, size_t workspace_bytes, lcattn_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// Stages: bit 0 = pre-pass, bit 1 = dK/dV, bit 2 = dQ conversion.
+int bwd_run(unsigned stages, const lcattn_shape* shape, const void* q, const void* k,
+            const void* v, const void* o, const void* d_o, const float* lse,
+            const void* tile_meta, const lcattn_mask_desc* mask, float scale, void* dq, void* dk,
+            void* dv, void* workspace, size_t workspace_bytes, lcattn_stream_t stream) {
   lcattn_tile_meta_layout L;
   int st = layout_of(shape, mask, &L);
   if (st) return st;
@@ -238,10 +243,33 @@ int lcattn_bwd(const lcattn_shape* shape, const void* q, const void* k, const vo
   a.dv = dv;
   a.v_sb = shape->v_stride[0]; a.v_ss = shape->v_stride[1]; a.v_sh = shape->v_stride[2];
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  cudaError_t e = launch_bwd_prepass(a, s);
-  if (e == cudaSuccess) e = launch_bwd_dkdv(tq, tk, tv, tdo, a, s);
-  if (e == cudaSuccess) e = launch_bwd_dq_convert(a, s);
+  cudaError_t e = cudaSuccess;
+  if (stages & 1u) e = launch_bwd_prepass(a, s);
+  if (e == cudaSuccess && (stages & 2u)) e = launch_bwd_dkdv(tq, tk, tv, tdo, a, s);
+  if (e == cudaSuccess && (stages & 4u)) e = launch_bwd_dq_convert(a, s);
   return cuda_status(e);
+}
+
+}  // namespace
+
+extern "C" {
+
+int lcattn_bwd(const lcattn_shape* shape, const void* q, const void* k, const void* v,
+               const void* o, const void* d_o, const float* lse, const void* tile_meta,
+               const lcattn_mask_desc* mask, float scale, void* dq, void* dk, void* dv,
+               void* workspace, size_t workspace_bytes, lcattn_stream_t stream) {
+  return bwd_run(7u, shape, q, k, v, o, d_o, lse, tile_meta, mask, scale, dq, dk, dv, workspace,
+                 workspace_bytes, stream);
+}
+
+int lcattn_bwd_stage(int stage, const lcattn_shape* shape, const void* q, const void* k,
+                     const void* v, const void* o, const void* d_o, const float* lse,
+                     const void* tile_meta, const lcattn_mask_desc* mask, float scale, void* dq,
+                     void* dk, void* dv, void* workspace, size_t workspace_bytes,
+                     lcattn_stream_t stream) {
+  if (stage < 1 || stage > 3) return LCATTN_ERR_INVALID_ARG;
+  return bwd_run(1u << (stage - 1), shape, q, k, v, o, d_o, lse, tile_meta, mask, scale, dq, dk,
+                 dv, workspace, workspace_bytes, stream);
 }
 
 int lcattn_read_status(const void* tile_meta, lcattn_stream_t stream) {
