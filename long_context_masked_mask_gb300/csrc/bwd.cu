@@ -5,7 +5,7 @@
 //      S^T = K Q^T and P^T = exp(S^T - LSE), forms dP^T = V dO^T and
 //      dS^T = scale * P^T (dP^T - D), accumulates dV += P^T dO and
 //      dK += dS^T Q in TMEM, and adds the partial dQ = dS K into the fp32
-//      accumulator with vector reductions;
+//      accumulator with bulk tensor reduce-adds;
 //   3. dQ conversion to bf16.
 // The pages single the backward out as the main bottleneck of masked and
 // sparse attention ("Long-Context Attention Benchmark", xllm-io blog review,
@@ -16,7 +16,9 @@
 //   warps 0-3  elementwise: thread = key row (TMEM lane) of the tile; builds
 //              P^T and dS^T, writes both to TMEM (bf16) and dS^T to shared
 //              memory for the dQ product; at the end stores dK and dV.
-//   warps 4-7  dQ drain: thread = query row; TMEM -> red.global.add.v4.f32.
+//   warps 4-7  dQ drain: thread = query row; TMEM -> 16 KB swizzled chunks in
+//              the dS buffer (free once the dQ product has read it) -> bulk
+//              tensor reduce-add into the fp32 accumulator (one elected thread).
 //   warp  8    producer: K, V once; Q_i, dO_i by TMA and LSE_i, D_i by plain
 //              loads into a 2-deep ring.
 //   warp  9    TMEM owner and MMA issuer.
@@ -112,6 +114,7 @@ struct BwdSmem {
   uint64_t q_full[2];
   uint64_t q_empty[2];
   uint64_t s_full, dp_full, ds_ready, dq_full, dq_free, done;
+  uint64_t stg_full[2], stg_free[2], ds_idle;
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -134,7 +137,7 @@ struct ItemIter {
   const int32_t* cnt_base;  // bwd_cnt for (b, list head 0), stride nKt per list head
   const int32_t* lst_base;
   int nH, nKt, nQt, kt, G, g;
-  int hi, idx, cnt;
+  int hi, idx, cnt, cur;
   __device__ void init(const TileMetaDev& t, int b, int kt_, int G_, int g_) {
     nH = t.nH; nKt = t.nKt; nQt = t.nQt; kt = kt_; G = G_; g = g_;
     cnt_base = t.bwd_cnt + (int64_t)b * t.nH * t.nKt;
@@ -145,13 +148,14 @@ struct ItemIter {
   }
   __device__ int list_head(int hh) const { return nH == 1 ? 0 : g * G + hh; }
   __device__ int count_of(int hh) const { return __ldg(cnt_base + (int64_t)list_head(hh) * nKt + kt); }
+  // Advances past empty lists and loads the entry at the new position early,
+  // so the load overlaps the rest of the current iteration.
   __device__ void skip_empty() {
     while (hi < G && idx >= cnt) { ++hi; idx = 0; if (hi < G) cnt = count_of(hi); }
+    if (hi < G) cur = __ldg(lst_base + ((int64_t)list_head(hi) * nKt + kt) * nQt + idx);
   }
   __device__ bool valid() const { return hi < G; }
-  __device__ int entry() const {
-    return __ldg(lst_base + ((int64_t)list_head(hi) * nKt + kt) * nQt + idx);
-  }
+  __device__ int entry() const { return cur; }
   __device__ int head() const { return g * G + hi; }
   __device__ void next() { ++idx; skip_empty(); }
 };
@@ -159,7 +163,7 @@ struct ItemIter {
 __global__ void __launch_bounds__(kThreads, 1)
 dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
             const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
-            const __grid_constant__ BwdKernelArgs ka) {
+            const __grid_constant__ CUtensorMap tmdQacc, const __grid_constant__ BwdKernelArgs ka) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const BwdArgs& a = ka.a;
   const ProblemDev& pr = a.pr;
@@ -190,6 +194,11 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
     mbar_init(&sm.dq_full, 1);
     mbar_init(&sm.dq_free, 128);
     mbar_init(&sm.done, 1);
+    for (int s2 = 0; s2 < 2; ++s2) {
+      mbar_init(&sm.stg_full[s2], 128);
+      mbar_init(&sm.stg_free[s2], 1);
+    }
+    mbar_init(&sm.ds_idle, 1);
     sm.abort_flag = 0;
     fence_barrier_init();
   }
@@ -330,8 +339,6 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
       if (a.mask.kind == LCATTN_MASK_COLBOUNDS) cb = __ldg(a.mask.col_bounds + (int64_t)b * pr.Sk + key);
       else kb = block_of(a.mask.k_offs, a.mask.nKb, key);
     }
-    const bool ragged_q = (pr.Sq % kBM) != 0;
-    const int last_qt = (pr.Sq - 1) / kBM;
     ItemIter it;
     it.init(a.meta, b, kt, pr.G, g);
     int i = 0;
@@ -381,11 +388,12 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
           }
         }
       }
-      (void)ragged_q; (void)last_qt;  // rows past Sq carry LSE = +inf, so P = 0 there
+      // Rows past Sq carry LSE = +inf (set by the producer), so P = 0 there.
       ok = mbar_wait(&sm.q_full[st], (i >> 1) & 1, abort_flag, gstatus, TO) &&
            mbar_wait(&sm.s_full, i & 1, abort_flag, gstatus, TO) &&
            mbar_wait(&sm.dp_full, i & 1, abort_flag, gstatus, TO);
-      if (i > 0 && ok) ok = mbar_wait(&sm.dq_full, (i - 1) & 1, abort_flag, gstatus, TO);
+      // dS(i) goes into the buffer that carried dQ(i-1) to the reduce-adds.
+      if (i > 0 && ok) ok = mbar_wait(&sm.ds_idle, (i - 1) & 1, abort_flag, gstatus, TO);
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       tc_fence_after();
       const float* lse2 = sm.lse2[st];
@@ -479,37 +487,59 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
   } else {
     // ------------------------------------------------------------ dQ drain
     const int r = tid - 128;  // query row within the tile
+    const bool elected = (r == 0);
     const uint32_t lane_off = static_cast<uint32_t>(32 * (warp & 3)) << 16;
     const uint32_t tQ = tmem + lane_off + 128;
     ItemIter it;
     it.init(a.meta, b, kt, pr.G, g);
-    int i = 0;
-    for (; it.valid(); it.next(), ++i) {
+    int i = 0, n = 0;  // n counts 32-column chunks; chunk n uses staging half n & 1
+    bool ok = true;
+    for (; ok && it.valid(); it.next(), ++i) {
       const int qt = it.entry() >> 1;
       const int h = it.head();
-      const int q = qt * kBM + r;
-      bool ok = mbar_wait(&sm.dq_full, i & 1, abort_flag, gstatus, TO);
-      if (!__all_sync(0xffffffffu, ok)) break;
+      ok = mbar_wait(&sm.dq_full, i & 1, abort_flag, gstatus, TO);
+      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       tc_fence_after();
-      float* dst = a.dq_acc + (((int64_t)b * pr.Sq + q) * pr.Hq + h) * kD;
-      #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      #pragma unroll 1
+      for (int c = 0; c < 4; ++c, ++n) {
+        const int st = n & 1, use = n >> 1;
+        if (use > 0) {
+          ok = mbar_wait(&sm.stg_free[st], (use - 1) & 1, abort_flag, gstatus, TO);
+          if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+        }
         uint32_t x[32];
         tmem_ld32(tQ + c * 32, x);
         tmem_ld_wait();
-        if (q < pr.Sq) {
-          #pragma unroll
-          for (int u = 0; u < 8; ++u)
-            asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};"
-                         :: "l"(dst + c * 32 + 4 * u), "f"(__uint_as_float(x[4 * u])),
-                            "f"(__uint_as_float(x[4 * u + 1])), "f"(__uint_as_float(x[4 * u + 2])),
-                            "f"(__uint_as_float(x[4 * u + 3]))
-                         : "memory");
+        if (c == 3) {  // every TMEM read of dQ(i) is done: its columns may be reused
+          tc_fence_before();
+          mbar_arrive(&sm.dq_free);
+        }
+        uint8_t* stg = sm.ds + st * kHalfBytes + r * 128;
+        #pragma unroll
+        for (int u = 0; u < 8; ++u)
+          *reinterpret_cast<uint4*>(stg + ((u ^ (r & 7)) << 4)) =
+              make_uint4(x[4 * u], x[4 * u + 1], x[4 * u + 2], x[4 * u + 3]);
+        fence_proxy_async_smem();
+        mbar_arrive(&sm.stg_full[st]);
+        if (elected) {
+          int dummy = 0;
+          if (mbar_wait(&sm.stg_full[st], use & 1, &dummy, gstatus, TO)) {
+            tma_reduce_add_4d(&tmdQacc, sm.ds + st * kHalfBytes, c * 32, h, qt * kBM, b);
+            bulk_commit_group();
+          }
+          // The previous chunk's source has been read: free its half.
+          bulk_wait_group_read<1>();
+          if (c > 0) mbar_arrive(&sm.stg_free[(n - 1) & 1]);
         }
       }
-      tc_fence_before();
-      mbar_arrive(&sm.dq_free);
+      if (!ok) break;
+      if (elected) {
+        bulk_wait_group_read<0>();
+        mbar_arrive(&sm.stg_free[(n - 1) & 1]);
+        mbar_arrive(&sm.ds_idle);  // the dS buffer is free for dS(i+1)
+      }
     }
+    if (elected) bulk_wait_group<0>();  // reduce-adds complete before the CTA exits
   }
 
   tc_fence_before();
@@ -535,7 +565,8 @@ cudaError_t launch_bwd_prepass(const BwdArgs& a, cudaStream_t st) {
 }
 
 cudaError_t launch_bwd_dkdv(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                            const CUtensorMap& tdo, const BwdArgs& a, cudaStream_t st) {
+                            const CUtensorMap& tdo, const CUtensorMap& tdq_acc, const BwdArgs& a,
+                            cudaStream_t st) {
   static bool attr_done = false;
   const size_t smem = sizeof(BwdSmem);
   if (!attr_done) {
@@ -547,7 +578,7 @@ cudaError_t launch_bwd_dkdv(const CUtensorMap& tq, const CUtensorMap& tk, const 
   BwdKernelArgs ka;
   ka.a = a;
   dim3 grid(a.meta.nKt, a.pr.Hkv, a.pr.B);
-  dkdv_kernel<<<grid, kThreads, smem, st>>>(tq, tk, tv, tdo, ka);
+  dkdv_kernel<<<grid, kThreads, smem, st>>>(tq, tk, tv, tdo, tdq_acc, ka);
   return cudaGetLastError();
 }
 

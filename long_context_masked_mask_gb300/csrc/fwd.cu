@@ -12,6 +12,7 @@
 //   warps 4-7  softmax for slot 1
 //   warp  8    TMA producer: Q tiles once, then K_j, V_j into a 4-deep ring
 //   warp  9    TMEM owner and single-thread tcgen05.mma issuer
+//   warps 10-11 idle (they complete the third warpgroup for setmaxnreg)
 // TMEM (512 columns): S0 | S1 | O0 | O1, 128 fp32 columns each.  The softmax
 // writes P (bf16 pairs) over the first 64 columns of its S, and the PV product
 // reads P from TMEM (A operand) and V from shared memory (B operand).
@@ -33,7 +34,12 @@ using namespace dev;
 constexpr int kStages = 4;          // K/V ring depth (K and V tiles alternate)
 constexpr int kTileBytes = 32768;   // 128 rows x 128 bf16
 constexpr int kHalfBytes = 16384;   // one 64-column TMA box
-constexpr int kThreads = 320;
+constexpr int kThreads = 384;        // 3 warpgroups
+// Register split (launch: 384 threads x 168): softmax warpgroups 224 each,
+// producer/MMA warpgroup 56.  128 * (224 + 224 + 56) = 384 * 168.
+constexpr int kRegsSoftmax = 224;
+constexpr int kRegsOther = 56;
+static_assert(128 * (2 * kRegsSoftmax + kRegsOther) <= kThreads * 168, "register split");
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
 struct FwdSmem {
@@ -55,16 +61,12 @@ struct FwdKernelArgs {
   int heads_per_cta;
 };
 
-__device__ __forceinline__ void set_bits(uint32_t (&mw)[4], int lo, int hi) {
-  #pragma unroll
-  for (int w = 0; w < 4; ++w) {
-    const int a = max(lo, 32 * w), b = min(hi, 32 * w + 32);
-    if (b > a) {
-      const int n = b - a;
-      const uint32_t bits = (n == 32) ? 0xffffffffu : (((1u << n) - 1u) << (a - 32 * w));
-      mw[w] |= bits;
-    }
-  }
+// Bits [lo, hi) of a 128-bit row mask that fall into the 32-bit word starting at `base`.
+__device__ __forceinline__ uint32_t range_bits(int lo, int hi, int base) {
+  const int a = max(lo, base), b = min(hi, base + 32);
+  if (b <= a) return 0u;
+  const int n = b - a;
+  return (n == 32) ? 0xffffffffu : (((1u << n) - 1u) << (a - base));
 }
 
 __device__ __forceinline__ int block_of(const int32_t* offs, int n, int x) {
@@ -84,7 +86,10 @@ __device__ __forceinline__ void tile_mask_bits(const MaskDev& m, const ProblemDe
   const int nvalid = min(kBN, pr.Sk - j0);
   mw[0] = mw[1] = mw[2] = mw[3] = 0u;
   if (!evaluate_mask) {  // full tile cut by the end of the key sequence
-    set_bits(mw, 0, nvalid);
+    mw[0] = range_bits(0, nvalid, 0);
+    mw[1] = range_bits(0, nvalid, 32);
+    mw[2] = range_bits(0, nvalid, 64);
+    mw[3] = range_bits(0, nvalid, 96);
     return;
   }
   if (m.kind == LCATTN_MASK_COLBOUNDS) {
@@ -107,12 +112,19 @@ __device__ __forceinline__ void tile_mask_bits(const MaskDev& m, const ProblemDe
     const int j1 = j0 + nvalid;
     const uint8_t* map =
         m.block_map + (((int64_t)b * pr.Hq + h) * m.nQb + qb_row) * (int64_t)m.nKb;
+    uint32_t b0 = 0u, b1 = 0u, b2 = 0u, b3 = 0u;
     for (int kb = block_of(m.k_offs, m.nKb, j0); kb < m.nKb; ++kb) {
       const int lo = max(__ldg(m.k_offs + kb), j0);
       if (lo >= j1) break;
       const int hi = min(__ldg(m.k_offs + kb + 1), j1);
-      if (hi > lo && __ldg(map + kb)) set_bits(mw, lo - j0, hi - j0);
+      if (hi > lo && __ldg(map + kb)) {
+        b0 |= range_bits(lo - j0, hi - j0, 0);
+        b1 |= range_bits(lo - j0, hi - j0, 32);
+        b2 |= range_bits(lo - j0, hi - j0, 64);
+        b3 |= range_bits(lo - j0, hi - j0, 96);
+      }
     }
+    mw[0] = b0; mw[1] = b1; mw[2] = b2; mw[3] = b3;
   }
 }
 
@@ -160,8 +172,9 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
   tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
   volatile int* abort_flag = &sm.abort_flag;
-
-  if (warp == 8) {
+  if (warp >= 8) {
+    regs_dec<kRegsOther>();
+    if (warp == 8) {
     // ---------------------------------------------------------------- producer
     if (lane == 0) {
       tma_prefetch_desc(&tmQ);
@@ -197,7 +210,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
         mbar_wait(&sm.q_full[s], 0, &dummy, gstatus, LCATTN_ERR_DEVICE_TIMEOUT);
       }
     }
-  } else if (warp == 9) {
+    } else if (warp == 9) {
     // ---------------------------------------------------------------- MMA issuer
     if (lane == 0) {
       const uint32_t idesc_qk = idesc_bf16_f32(128, 128, false, false);
@@ -249,7 +262,9 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
       int dummy = 0;
       mbar_wait(&sm.drain, 0, &dummy, gstatus, LCATTN_ERR_DEVICE_TIMEOUT);
     }
+    }
   } else {
+    regs_inc<kRegsSoftmax>();
     // ---------------------------------------------------------------- softmax
     const int s = warp >> 2;
     const int r = tid & 127;  // == 32 * (warp % 4) + lane: this thread's TMEM lane
@@ -267,8 +282,10 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
         qb_row = block_of(a.mask.q_offs, a.mask.nQb, min(row, pr.Sq - 1));
       float m_run = -INFINITY, l_run = 0.f;
       bool ok = true;
+      int e_next = n > 0 ? __ldg(list) : 0;
       for (int j = 0; j < n; ++j) {
-        const int e = __ldg(list + j);
+        const int e = e_next;
+        if (j + 1 < n) e_next = __ldg(list + j + 1);  // prefetch the next entry
         const int kt = e >> 1;
         const bool partial = (e & 1) != 0;
         const bool masked = partial || (ragged_k && kt == last_kt);
@@ -287,21 +304,31 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
         #pragma unroll
         for (int c = 0; c < 128; ++c) x[c] = __uint_as_float(xr[c]);
         if (masked) {
+          const uint32_t w0 = mw[0], w1 = mw[1], w2 = mw[2], w3 = mw[3];
           #pragma unroll
-          for (int c = 0; c < 128; ++c)
-            if (!((mw[c >> 5] >> (c & 31)) & 1u)) x[c] = -INFINITY;
+          for (int c = 0; c < 128; ++c) {
+            const uint32_t w = c < 32 ? w0 : (c < 64 ? w1 : (c < 96 ? w2 : w3));
+            if (!((w >> (c & 31)) & 1u)) x[c] = -INFINITY;
+          }
         }
-        float mx = x[0];
+        // Row max as 8 independent chains (a single 128-long chain is latency bound).
+        float m8[8];
         #pragma unroll
-        for (int c = 1; c < 128; ++c) mx = fmaxf(mx, x[c]);
-        const float m_tile = mx * sl2;  // -inf stays -inf
+        for (int c = 0; c < 8; ++c) m8[c] = x[c];
+        #pragma unroll
+        for (int c = 8; c < 128; ++c) m8[c & 7] = fmaxf(m8[c & 7], x[c]);
+        #pragma unroll
+        for (int w = 4; w > 0; w >>= 1)
+          #pragma unroll
+          for (int c = 0; c < w; ++c) m8[c] = fmaxf(m8[c], m8[c + w]);
+        const float m_tile = m8[0] * sl2;  // -inf stays -inf
         const bool need = m_tile > m_run + kRescaleThreshold;
         const bool warp_rescale = __any_sync(0xffffffffu, need) && j > 0;
         const float m_new = need ? m_tile : m_run;
         const float alpha = need ? fast_exp2(m_run - m_new) : 1.f;  // exp2(-inf) = 0
         m_run = m_new;
         const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
-        float sum = 0.f;
+        float s8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
         #pragma unroll
         for (int c = 0; c < 2; ++c) {
           uint32_t pk[32];
@@ -309,12 +336,16 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
           for (int i = 0; i < 32; ++i) {
             const float p0 = fast_exp2(fmaf(x[c * 64 + 2 * i], sl2, -m_use));
             const float p1 = fast_exp2(fmaf(x[c * 64 + 2 * i + 1], sl2, -m_use));
-            sum += p0 + p1;
+            s8[i & 7] += p0 + p1;
             pk[i] = pack_bf16x2(p0, p1);
           }
           tmem_st32(tS + c * 32, pk);
         }
-        l_run = l_run * alpha + sum;
+        #pragma unroll
+        for (int w = 4; w > 0; w >>= 1)
+          #pragma unroll
+          for (int c = 0; c < w; ++c) s8[c] += s8[c + w];
+        l_run = l_run * alpha + s8[0];
         if (warp_rescale) {
           // O holds PV up to tile j-1: wait for it, then scale it in place
           // before PV(j) is issued (which needs p_full below).

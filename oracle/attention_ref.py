@@ -140,14 +140,13 @@ def attention_bwd_sampled(q, k, v, do, spec, scale, b: int, g: int, q_rows, k_co
         dS = P * (dP - Dr[:, None])
         dQ[hi] = scale * (dS @ kk)
         # dK/dV columns: find every row that attends at least one sampled key.
-        for r0 in range(0, N, 1024):
-            rows = np.arange(r0, min(N, r0 + 1024))
-            Mc = allowed(spec, N, rows, head=h)
-            need = Mc[:, k_cols].any(axis=1)
+        for r0 in range(0, N, 8192):
+            rows = np.arange(r0, min(N, r0 + 8192))
+            need = allowed(spec, N, rows, head=h, cols=k_cols).any(axis=1)
             if not need.any():
                 continue
             rr = rows[need]
-            Mr = Mc[need]
+            Mr = allowed(spec, N, rr, head=h)
             o, lse, P = _rows_fwd(q[b, rr, h], kk, vv, Mr, scale)
             dOr = do[b, rr, h]
             Pc = P[:, k_cols]
@@ -159,22 +158,25 @@ def attention_bwd_sampled(q, k, v, do, spec, scale, b: int, g: int, q_rows, k_co
     return dQ, dK, dV
 
 
-def classify_tiles(spec, N: int, BM: int = 128, BN: int = 128, head: int = 0) -> np.ndarray:
+def classify_tiles(spec, N: int, BM: int = 128, BN: int = 128, head: int = 0,
+                   q_tiles=None) -> np.ndarray:
     """Class of every (query tile, key tile) pair: EMPTY when no in-range pair of
     the tile is allowed, FULL when all are, PARTIAL otherwise.  Rows and columns
-    past N (a ragged last tile) are not part of the tile."""
+    past N (a ragged last tile) are not part of the tile.  With ``q_tiles``,
+    only those rows of tiles are classified (output row r = q_tiles[r])."""
     nQt = (N + BM - 1) // BM
     nKt = (N + BN - 1) // BN
-    out = np.zeros((nQt, nKt), dtype=np.uint8)
-    for qt in range(nQt):
+    tiles = range(nQt) if q_tiles is None else list(q_tiles)
+    out = np.zeros((len(tiles), nKt), dtype=np.uint8)
+    for r, qt in enumerate(tiles):
         rows = np.arange(qt * BM, min(N, (qt + 1) * BM))
         M = allowed(spec, N, rows, head=head)
         for kt in range(nKt):
             blk = M[:, kt * BN:min(N, (kt + 1) * BN)]
             if not blk.any():
-                out[qt, kt] = EMPTY
+                out[r, kt] = EMPTY
             elif blk.all():
-                out[qt, kt] = FULL
+                out[r, kt] = FULL
             else:
-                out[qt, kt] = PARTIAL
+                out[r, kt] = PARTIAL
     return out

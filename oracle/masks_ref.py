@@ -43,17 +43,18 @@ def _segment_start(seg: np.ndarray, lens) -> np.ndarray:
     return starts[seg]
 
 
-def allowed(spec, N: int, rows=None, head: int = 0) -> np.ndarray:
-    """Boolean mask rows: ``out[r, j]`` is True when query ``rows[r]`` may attend
-    key ``j`` (0 <= j < N) under ``spec`` for query head ``head``."""
+def allowed(spec, N: int, rows=None, head: int = 0, cols=None) -> np.ndarray:
+    """Boolean mask rows: ``out[r, c]`` is True when query ``rows[r]`` may attend
+    key ``cols[c]`` (all keys 0..N-1 by default) under ``spec`` for query head
+    ``head``."""
     if rows is None:
         rows = np.arange(N)
     i = np.asarray(rows, dtype=np.int64)[:, None]
-    j = np.arange(N, dtype=np.int64)[None, :]
+    j = (np.arange(N, dtype=np.int64) if cols is None else np.asarray(cols, dtype=np.int64))[None, :]
     k = spec.kind
     p = spec.params
     if k == "FULL":
-        return np.ones((i.shape[0], N), dtype=bool)
+        return np.ones((i.shape[0], j.shape[1]), dtype=bool)
     if k == "CAUSAL":
         return j <= i
     if k in ("FULL_DOCUMENT", "CAUSAL_DOCUMENT"):
