@@ -53,6 +53,7 @@ typedef struct CUstream_st* lcattn_stream_t; /* same handle as cudaStream_t */
 #define LCATTN_ERR_CUDA (-4)          /* a CUDA call or launch failed             */
 #define LCATTN_ERR_DEVICE_TIMEOUT (-5)/* a kernel gave up waiting (bounded wait)  */
 #define LCATTN_ERR_DEVICE_MASK (-6)   /* block offsets not increasing from 0 to S */
+#define LCATTN_ERR_SCRATCH_LIMIT (-7) /* problem too large for lcattn_bwd_noalloc  */
 
 /* ---- problem shape ------------------------------------------------------ */
 typedef struct lcattn_shape {
@@ -173,6 +174,34 @@ int lcattn_bwd_stage(int stage, const lcattn_shape* shape, const void* q, const 
                      const void* tile_meta, const lcattn_mask_desc* mask, float scale, void* dq,
                      void* dk, void* dv, void* workspace, size_t workspace_bytes,
                      lcattn_stream_t stream);
+
+/* Backward that allocates nothing and takes no workspace.  The pages have no
+ * counterpart: this is an interface for callers that cannot hand the library
+ * device memory of their own -- for example a plugin inside a host runtime that
+ * owns every device allocation and forbids cudaMalloc (or offers no allocator
+ * to its plugins), or a latency-critical serving path where cudaMalloc, which
+ * may synchronise the device, is not allowed after start-up.
+ *
+ * Same arguments and results as lcattn_bwd without `workspace`.  The D vector
+ * and the fp32 dQ accumulator live instead in one fixed device array inside the
+ * library, LCATTN_NOALLOC_SCRATCH_BYTES (32 MiB) large; every GPU that loads
+ * the library holds it until the process exits.  A problem whose
+ * lcattn_bwd_workspace_size exceeds it returns LCATTN_ERR_SCRATCH_LIMIT and
+ * launches nothing (32 MiB covers B * Hq * Sq up to 65,027 query rows, e.g.
+ * 8 heads at 8K tokens).
+ *
+ * The first call on a device looks the array's device address up (with that
+ * device current) and caches it; make that first call before any stream
+ * capture.  Every call on a device shares the one array and finds the previous
+ * call's contents in it; the first stage of each call rewrites all of it that
+ * must start at zero (the dQ accumulator) and all of D.  Calls whose work
+ * overlaps on the GPU (different streams, different host threads) race on the
+ * array and corrupt each other's gradients: order them on one stream.      */
+#define LCATTN_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
+int lcattn_bwd_noalloc(const lcattn_shape* shape, const void* q, const void* k, const void* v,
+                       const void* o, const void* d_o, const float* lse, const void* tile_meta,
+                       const lcattn_mask_desc* mask, float scale, void* dq, void* dk, void* dv,
+                       lcattn_stream_t stream);
 
 /* Synchronises `stream`, then returns the first nonzero device status word of
  * `tile_meta` (LCATTN_ERR_DEVICE_*), or LCATTN_OK.  Clears nothing.          */

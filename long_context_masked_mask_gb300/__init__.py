@@ -39,6 +39,8 @@ LCATTN_ERR_WORKSPACE = -3
 LCATTN_ERR_CUDA = -4
 LCATTN_ERR_DEVICE_TIMEOUT = -5
 LCATTN_ERR_DEVICE_MASK = -6
+LCATTN_ERR_SCRATCH_LIMIT = -7
+LCATTN_NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024
 LCATTN_MASK_COLBOUNDS = 1
 LCATTN_MASK_BLOCKMAP = 2
 LCATTN_TILE_EMPTY, LCATTN_TILE_FULL, LCATTN_TILE_PARTIAL = 0, 1, 2
@@ -48,7 +50,7 @@ BLOCK_M = BLOCK_N = 128
 EXPORTED = (
     "lcattn_tile_meta_layout_of", "lcattn_tile_meta_size", "lcattn_mask_compile", "lcattn_fwd",
     "lcattn_bwd_workspace_size", "lcattn_bwd", "lcattn_bwd_stage", "lcattn_read_status", "lcattn_clear_status",
-    "lcattn_status_string", "lcattn_version",
+    "lcattn_status_string", "lcattn_version", "lcattn_bwd_noalloc",
 )
 
 
@@ -96,6 +98,7 @@ def _load():
                                       ctypes.c_size_t, P]),
         "lcattn_bwd_stage": (ctypes.c_int, [ctypes.c_int, S, P, P, P, P, P, P, P, M, ctypes.c_float,
                                             P, P, P, P, ctypes.c_size_t, P]),
+        "lcattn_bwd_noalloc": (ctypes.c_int, [S, P, P, P, P, P, P, P, M, ctypes.c_float, P, P, P, P]),
         "lcattn_read_status": (ctypes.c_int, [P, P]),
         "lcattn_clear_status": (ctypes.c_int, [P, P]),
         "lcattn_status_string": (ctypes.c_char_p, [ctypes.c_int]),
@@ -256,6 +259,25 @@ def lcattn_bwd(q, k, v, o, d_o, lse, mask: DeviceMask, tile_meta, scale: Optiona
         _check(_lib.lcattn_bwd(*args), "lcattn_bwd")
     else:
         _check(_lib.lcattn_bwd_stage(int(stage), *args), f"lcattn_bwd_stage({stage})")
+    return dq, dk, dv
+
+
+def lcattn_bwd_noalloc(q, k, v, o, d_o, lse, mask: DeviceMask, tile_meta, scale: Optional[float] = None,
+                       dq=None, dk=None, dv=None, stream=None):
+    """Backward through lcattn_bwd_noalloc: the library takes its scratch from a
+    fixed 32 MiB device array instead of a caller workspace.  Meant for callers
+    that may not allocate device memory; outputs given here are written in
+    place (this wrapper allocates them only when they are omitted)."""
+    if scale is None:
+        scale = 1.0 / math.sqrt(q.shape[3])
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    shape = make_shape(q, k, v, o)
+    _check(_lib.lcattn_bwd_noalloc(ctypes.byref(shape), q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                                   o.data_ptr(), d_o.data_ptr(), lse.data_ptr(), tile_meta.data_ptr(),
+                                   ctypes.byref(mask.desc), float(scale), dq.data_ptr(), dk.data_ptr(),
+                                   dv.data_ptr(), _stream_ptr(stream)), "lcattn_bwd_noalloc")
     return dq, dk, dv
 
 

@@ -4,6 +4,7 @@
 #include <cudaTypedefs.h>
 
 #include <cstring>
+#include <mutex>
 
 #include "lcattn_internal.cuh"
 
@@ -289,6 +290,53 @@ int lcattn_bwd_stage(int stage, const lcattn_shape* shape, const void* q, const 
                  dv, workspace, workspace_bytes, stream);
 }
 
+}  // extern "C"
+
+namespace {
+
+// Backward scratch (D vector + fp32 dQ accumulator) for lcattn_bwd_noalloc.
+// In host code this name is only a stand-in for the device array; kernels get
+// the device address that cudaGetSymbolAddress returns.
+static __device__ __align__(256) uint8_t g_noalloc_scratch[LCATTN_NOALLOC_SCRATCH_BYTES];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void* g_noalloc_addr[kMaxDevices] = {};
+
+// Device address of the scratch array on the current device, looked up once
+// per device with that device current.
+int noalloc_scratch(void** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return LCATTN_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return LCATTN_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (!g_noalloc_addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return LCATTN_ERR_CUDA;
+    g_noalloc_addr[dev] = p;
+  }
+  *out = g_noalloc_addr[dev];
+  return LCATTN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int lcattn_bwd_noalloc(const lcattn_shape* shape, const void* q, const void* k, const void* v,
+                       const void* o, const void* d_o, const float* lse, const void* tile_meta,
+                       const lcattn_mask_desc* mask, float scale, void* dq, void* dk, void* dv,
+                       lcattn_stream_t stream) {
+  int st = validate_shape(shape);
+  if (st) return st;
+  const size_t need = lcattn_bwd_workspace_size(shape);
+  if (need > (size_t)LCATTN_NOALLOC_SCRATCH_BYTES) return LCATTN_ERR_SCRATCH_LIMIT;
+  void* ws = nullptr;
+  if ((st = noalloc_scratch(&ws))) return st;
+  return bwd_run(7u, shape, q, k, v, o, d_o, lse, tile_meta, mask, scale, dq, dk, dv, ws,
+                 (size_t)LCATTN_NOALLOC_SCRATCH_BYTES, stream);
+}
+
 int lcattn_read_status(const void* tile_meta, lcattn_stream_t stream) {
   if (!tile_meta) return LCATTN_ERR_INVALID_ARG;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -315,6 +363,8 @@ const char* lcattn_status_string(int status) {
     case LCATTN_ERR_CUDA: return "CUDA error";
     case LCATTN_ERR_DEVICE_TIMEOUT: return "a kernel gave up waiting (bounded device wait expired)";
     case LCATTN_ERR_DEVICE_MASK: return "block offsets are not nondecreasing from 0 to the sequence length";
+    case LCATTN_ERR_SCRATCH_LIMIT:
+      return "problem needs more backward scratch than the fixed no-allocation array holds";
     default: return "unknown status";
   }
 }

@@ -108,7 +108,7 @@ def test_calls_reject_bad_pointers_before_launch():
 
 
 def test_status_strings():
-    for code in range(-6, 1):
+    for code in range(-7, 1):
         assert lc.status_string(code) not in ("", "unknown status")
     assert lc.status_string(-99) == "unknown status"
     assert lc.library().lcattn_version() >= 100
