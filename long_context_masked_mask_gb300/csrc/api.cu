@@ -139,21 +139,6 @@ int encode_bshd(CUtensorMap* m, const void* ptr, int64_t B, int64_t S, int64_t H
   return r == CUDA_SUCCESS ? LCATTN_OK : LCATTN_ERR_UNSUPPORTED;
 }
 
-// fp32 dQ accumulator [B][S][H][128] (contiguous): 32-float x 128-row boxes
-// with 128-byte swizzle, the target of the bulk reduce-add.
-int encode_acc_f32(CUtensorMap* m, void* ptr, int64_t B, int64_t S, int64_t H) {
-  auto fn = encode_fn();
-  if (!fn) return LCATTN_ERR_CUDA;
-  cuuint64_t dims[4] = {(cuuint64_t)kD, (cuuint64_t)H, (cuuint64_t)S, (cuuint64_t)B};
-  cuuint64_t strides[3] = {(cuuint64_t)kD * 4, (cuuint64_t)(H * kD * 4), (cuuint64_t)(S * H * kD * 4)};
-  cuuint32_t box[4] = {32, 1, 128, 1};
-  cuuint32_t es[4] = {1, 1, 1, 1};
-  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, ptr, dims, strides, box, es,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? LCATTN_OK : LCATTN_ERR_UNSUPPORTED;
-}
-
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? LCATTN_OK : LCATTN_ERR_CUDA; }
 
 }  // namespace
@@ -258,12 +243,10 @@ int bwd_run(unsigned stages, const lcattn_shape* shape, const void* q, const voi
   a.k_sb = shape->k_stride[0]; a.k_ss = shape->k_stride[1]; a.k_sh = shape->k_stride[2];
   a.dv = dv;
   a.v_sb = shape->v_stride[0]; a.v_ss = shape->v_stride[1]; a.v_sh = shape->v_stride[2];
-  CUtensorMap tacc;
-  if ((st = encode_acc_f32(&tacc, a.dq_acc, shape->B, shape->Sq, shape->Hq))) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e = cudaSuccess;
   if (stages & 1u) e = launch_bwd_prepass(a, s);
-  if (e == cudaSuccess && (stages & 2u)) e = launch_bwd_dkdv(tq, tk, tv, tdo, tacc, a, s);
+  if (e == cudaSuccess && (stages & 2u)) e = launch_bwd_dkdv(tq, tk, tv, tdo, a, s);
   if (e == cudaSuccess && (stages & 4u)) e = launch_bwd_dq_convert(a, s);
   return cuda_status(e);
 }

@@ -4,8 +4,8 @@
 //      the GQA group and every non-empty query tile of its list it recomputes
 //      S^T = K Q^T and P^T = exp(S^T - LSE), forms dP^T = V dO^T and
 //      dS^T = scale * P^T (dP^T - D), accumulates dV += P^T dO and
-//      dK += dS^T Q in TMEM, and adds the partial dQ = dS K into the fp32
-//      accumulator with bulk tensor reduce-adds;
+//      dK += dS^T Q in TMEM, and adds the partial dQ^T = K^T dS^T into the fp32
+//      accumulator;
 //   3. dQ conversion to bf16.
 // The pages single the backward out as the main bottleneck of masked and
 // sparse attention ("Long-Context Attention Benchmark", xllm-io blog review,
@@ -13,16 +13,18 @@
 // for L = <O, dO>.
 //
 // dK/dV kernel roles (320 threads):
-//   warps 0-3  elementwise: thread = key row (TMEM lane) of the tile; builds
-//              P^T and dS^T, writes both to TMEM (bf16) and dS^T to shared
-//              memory for the dQ product; at the end stores dK and dV.
-//   warps 4-7  dQ drain: thread = query row; TMEM -> 16 KB swizzled chunks in
-//              the dS buffer (free once the dQ product has read it) -> bulk
-//              tensor reduce-add into the fp32 accumulator (one elected thread).
+//   warps 0-3, 4-7  two warpgroups, one per half of the 128 query columns of a
+//              tile.  Thread r is key row r of S^T / dP^T (TMEM lane r): it
+//              builds its half of P^T and dS^T, writes both to TMEM (bf16, in
+//              columns only its own warpgroup reads) and dS^T to shared memory
+//              for the dQ product.  The same thread is head-dim row r of dQ^T
+//              and adds its half of dQ into the accumulator: a warp's 32 lanes
+//              cover 128 contiguous bytes of one query row, one L2 request per
+//              instruction.  At the end warpgroup 0 stores dV, warpgroup 1 dK.
 //   warp  8    producer: K, V once; Q_i, dO_i by TMA and LSE_i, D_i by plain
 //              loads into a 2-deep ring.
 //   warp  9    TMEM owner and MMA issuer.
-// TMEM: [0,128) S^T then P^T | [128,256) dP^T then dS^T, then dQ |
+// TMEM: [0,128) S^T then P^T | [128,256) dP^T then dS^T, then dQ^T |
 //       [256,384) dV | [384,512) dK.
 #include <cuda_bf16.h>
 
@@ -107,14 +109,13 @@ struct BwdSmem {
   alignas(1024) uint8_t v[kTileBytes];
   alignas(1024) uint8_t q[2][kTileBytes];
   alignas(1024) uint8_t dO[2][kTileBytes];
-  alignas(1024) uint8_t ds[kTileBytes];
+  alignas(1024) uint8_t ds[kTileBytes];  // dS^T, keys x queries, read MN-major by dQ^T
   float lse2[2][128];  // LSE * log2(e); +inf where P must be 0
   float dvec[2][128];
   uint64_t kv_full;
   uint64_t q_full[2];
   uint64_t q_empty[2];
   uint64_t s_full, dp_full, ds_ready, dq_full, dq_free, done;
-  uint64_t stg_full[2], stg_free[2], ds_idle;
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -160,10 +161,18 @@ struct ItemIter {
   __device__ void next() { ++idx; skip_empty(); }
 };
 
+// Bits [lo, hi) of a 64-bit column mask that fall into the word starting at `base`.
+__device__ __forceinline__ uint32_t range_bits(int lo, int hi, int base) {
+  const int a = max(lo, base), b = min(hi, base + 32);
+  if (b <= a) return 0u;
+  const int n = b - a;
+  return (n == 32) ? 0xffffffffu : (((1u << n) - 1u) << (a - base));
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
 dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
             const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
-            const __grid_constant__ CUtensorMap tmdQacc, const __grid_constant__ BwdKernelArgs ka) {
+            const __grid_constant__ BwdKernelArgs ka) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const BwdArgs& a = ka.a;
   const ProblemDev& pr = a.pr;
@@ -190,15 +199,10 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
     }
     mbar_init(&sm.s_full, 1);
     mbar_init(&sm.dp_full, 1);
-    mbar_init(&sm.ds_ready, 128);
+    mbar_init(&sm.ds_ready, 256);
     mbar_init(&sm.dq_full, 1);
-    mbar_init(&sm.dq_free, 128);
+    mbar_init(&sm.dq_free, 256);
     mbar_init(&sm.done, 1);
-    for (int s2 = 0; s2 < 2; ++s2) {
-      mbar_init(&sm.stg_full[s2], 128);
-      mbar_init(&sm.stg_free[s2], 1);
-    }
-    mbar_init(&sm.ds_idle, 1);
     sm.abort_flag = 0;
     fence_barrier_init();
   }
@@ -267,6 +271,8 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
     }
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
+    // Per item i: dP^T(i) | wait dS(i) | dV, dK | S^T(i+1) | dQ^T(i).  S^T(i+1)
+    // goes before dQ^T(i) so that P(i+1) is computed while dQ^T(i) runs.
     if (lane == 0) {
       const uint32_t id_kmaj = idesc_bf16_f32(128, 128, false, false);
       const uint32_t id_ts = idesc_bf16_f32(128, 128, false, true);
@@ -276,13 +282,8 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
       bool ok = mbar_wait(&sm.kv_full, 0, abort_flag, gstatus, TO);
       ItemIter it;
       it.init(a.meta, b, kt, pr.G, g);
-      int i = 0;
-      for (; ok && it.valid(); it.next(), ++i) {
-        const int st = i & 1;
-        if (!(ok = mbar_wait(&sm.q_full[st], (i >> 1) & 1, abort_flag, gstatus, TO))) break;
-        tc_fence_after();
-        const uint32_t q_s = smem_u32(sm.q[st]), do_s = smem_u32(sm.dO[st]);
-        // S^T = K Q^T
+      auto issue_s = [&](int st) {  // S^T = K Q^T into [0, 128)
+        const uint32_t q_s = smem_u32(sm.q[st]);
         #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
@@ -290,7 +291,19 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
                  kk > 0 ? 1u : 0u);
         }
         tc_commit(&sm.s_full);
-        // dP^T = V dO^T, into columns the previous dQ used: wait for its drain.
+      };
+      if (ok && it.valid()) {
+        ok = mbar_wait(&sm.q_full[0], 0, abort_flag, gstatus, TO);
+        if (ok) {
+          tc_fence_after();
+          issue_s(0);
+        }
+      }
+      int i = 0;
+      for (; ok && it.valid(); ++i) {
+        const int st = i & 1;
+        const uint32_t q_s = smem_u32(sm.q[st]), do_s = smem_u32(sm.dO[st]);
+        // dP^T = V dO^T, into the columns dQ^T(i-1) used: wait for its drain.
         if (i > 0) {
           if (!(ok = mbar_wait(&sm.dq_free, (i - 1) & 1, abort_flag, gstatus, TO))) break;
           tc_fence_after();
@@ -304,33 +317,46 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
         tc_commit(&sm.dp_full);
         if (!(ok = mbar_wait(&sm.ds_ready, i & 1, abort_flag, gstatus, TO))) break;
         tc_fence_after();
-        // dV += P^T dO ; dK += dS^T Q   (A from TMEM, B MN-major from smem)
+        // dV += P^T dO ; dK += dS^T Q.  A from TMEM: queries 0-63 sit in the
+        // first 32 columns of each half's region, queries 64-127 at +64.
         #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          mma_ts(tdV, tS + kk * 8, sdesc_sw128(do_s + kk * 2048, kHalfBytes, 1024), id_ts,
-                 (i > 0 || kk > 0) ? 1u : 0u);
+          mma_ts(tdV, tS + (kk >> 2) * 64 + (kk & 3) * 8,
+                 sdesc_sw128(do_s + kk * 2048, kHalfBytes, 1024), id_ts, (i > 0 || kk > 0) ? 1u : 0u);
         #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          mma_ts(tdK, tP + kk * 8, sdesc_sw128(q_s + kk * 2048, kHalfBytes, 1024), id_ts,
-                 (i > 0 || kk > 0) ? 1u : 0u);
+          mma_ts(tdK, tP + (kk >> 2) * 64 + (kk & 3) * 8,
+                 sdesc_sw128(q_s + kk * 2048, kHalfBytes, 1024), id_ts, (i > 0 || kk > 0) ? 1u : 0u);
         tc_commit(&sm.q_empty[st]);
-        // dQ = dS K  (A = dS^T in smem read MN-major, B = K MN-major)
+        it.next();
+        if (it.valid()) {
+          const int st2 = (i + 1) & 1;
+          if (!(ok = mbar_wait(&sm.q_full[st2], ((i + 1) >> 1) & 1, abort_flag, gstatus, TO))) break;
+          tc_fence_after();
+          issue_s(st2);
+        }
+        // dQ^T = K^T dS^T: A = K read MN-major (M = head dim), B = dS^T read
+        // MN-major (N = queries).  Lands in [128, 256): lane = head dim.
         #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          mma_ss(tP, sdesc_sw128(ds_s + kk * 2048, kHalfBytes, 1024),
-                 sdesc_sw128(k_s + kk * 2048, kHalfBytes, 1024), id_mn, kk > 0 ? 1u : 0u);
+          mma_ss(tP, sdesc_sw128(k_s + kk * 2048, kHalfBytes, 1024),
+                 sdesc_sw128(ds_s + kk * 2048, kHalfBytes, 1024), id_mn, kk > 0 ? 1u : 0u);
         tc_commit(&sm.dq_full);
       }
       tc_commit(&sm.done);
       int dummy = 0;
       mbar_wait(&sm.done, 0, &dummy, gstatus, TO);
     }
-  } else if (warp < 4) {
-    // ------------------------------------------------------------ elementwise
-    const int r = tid;  // key row within the tile == TMEM lane
+  } else {
+    // ------------------------------------------------- elementwise + dQ drain
+    // Warpgroup x takes query columns [64x, 64x+64) of every tile; thread r is
+    // key row r of S^T / dP^T and head-dim row r of dQ^T (the TMEM lane).
+    const int x = warp >> 2;
+    const int r = 32 * (warp & 3) + lane;
+    const int c0 = 64 * x;
     const int key = kt * kBN + r;
     const bool key_ok = key < pr.Sk;
-    const uint32_t lane_off = static_cast<uint32_t>(32 * warp) << 16;
+    const uint32_t lane_off = static_cast<uint32_t>(32 * (warp & 3)) << 16;
     const uint32_t tS = tmem + lane_off, tP = tmem + lane_off + 128;
     const float sl2 = a.scale_log2, scale = a.scale;
     int4 cb = make_int4(0, 0, 0, 0);
@@ -339,116 +365,136 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
       if (a.mask.kind == LCATTN_MASK_COLBOUNDS) cb = __ldg(a.mask.col_bounds + (int64_t)b * pr.Sk + key);
       else kb = block_of(a.mask.k_offs, a.mask.nKb, key);
     }
+    const int64_t dq_row_stride = (int64_t)pr.Hq * kD;
+    // Adds this warpgroup's half of dQ(item) (TMEM columns [128 + 64x, +64)).
+    auto drain = [&](int i_prev, int qt_prev, int h_prev, bool signal) -> bool {
+      bool okd = mbar_wait(&sm.dq_full, i_prev & 1, abort_flag, gstatus, TO);
+      if (!__all_sync(0xffffffffu, okd)) return false;
+      tc_fence_after();
+      uint32_t d0[32], d1[32];
+      tmem_ld32(tP + c0, d0);
+      tmem_ld32(tP + c0 + 32, d1);
+      tmem_ld_wait();
+      if (signal) {
+        tc_fence_before();
+        mbar_arrive(&sm.dq_free);
+      }
+      const int qbase = qt_prev * kBM + c0;
+      float* dst = a.dq_acc + (((int64_t)b * pr.Sq + qbase) * pr.Hq + h_prev) * kD + r;
+      const int nq = min(64, pr.Sq - qbase);
+      #pragma unroll
+      for (int c = 0; c < 32; ++c)
+        if (c < nq) atomicAdd(dst + c * dq_row_stride, __uint_as_float(d0[c]));
+      #pragma unroll
+      for (int c = 0; c < 32; ++c)
+        if (c + 32 < nq) atomicAdd(dst + (c + 32) * dq_row_stride, __uint_as_float(d1[c]));
+      return true;
+    };
     ItemIter it;
     it.init(a.meta, b, kt, pr.G, g);
-    int i = 0;
+    int i = 0, qt_prev = 0, h_prev = 0;
     bool ok = true;
     for (; it.valid(); it.next(), ++i) {
       const int st = i & 1;
       const int e = it.entry();
       const int qt = e >> 1;
-      const int q0 = qt * kBM;
+      const int h = it.head();
+      const int q0 = qt * kBM + c0;
       const bool partial = (e & 1) != 0;
-      // Allowed-query bits of this key for the tile (bit c = query q0 + c).
-      uint32_t mw[4] = {0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu};
+      // Allowed-query bits of this key for the 64 columns (bit c = query q0 + c).
+      uint32_t m0 = 0xffffffffu, m1 = 0xffffffffu;
       if (!key_ok) {
-        mw[0] = mw[1] = mw[2] = mw[3] = 0u;
+        m0 = m1 = 0u;
       } else if (partial) {
         if (a.mask.kind == LCATTN_MASK_COLBOUNDS) {
+          m0 = m1 = 0u;
           #pragma unroll
-          for (int w = 0; w < 4; ++w) {
-            uint32_t bits = 0u;
-            #pragma unroll
-            for (int c = 0; c < 32; ++c) {
-              const int q = q0 + 32 * w + c;
-              const bool okq = (cb.x <= q && q < cb.y) || (cb.z <= q && q < cb.w);
-              bits |= (okq ? 1u : 0u) << c;
-            }
-            mw[w] = bits;
+          for (int c = 0; c < 32; ++c) {
+            const int q = q0 + c, q2 = q0 + 32 + c;
+            m0 |= (((cb.x <= q && q < cb.y) || (cb.z <= q && q < cb.w)) ? 1u : 0u) << c;
+            m1 |= (((cb.x <= q2 && q2 < cb.y) || (cb.z <= q2 && q2 < cb.w)) ? 1u : 0u) << c;
           }
         } else {
-          mw[0] = mw[1] = mw[2] = mw[3] = 0u;
+          m0 = m1 = 0u;
           const uint8_t* map = a.mask.block_map +
-                               ((int64_t)b * pr.Hq + it.head()) * a.mask.nQb * (int64_t)a.mask.nKb + kb;
-          const int q1 = min(q0 + kBM, pr.Sq);
-          for (int qb = block_of(a.mask.q_offs, a.mask.nQb, q0); qb < a.mask.nQb; ++qb) {
+                               ((int64_t)b * pr.Hq + h) * a.mask.nQb * (int64_t)a.mask.nKb + kb;
+          const int q1 = min(q0 + 64, pr.Sq);
+          for (int qb = block_of(a.mask.q_offs, a.mask.nQb, min(q0, pr.Sq - 1)); qb < a.mask.nQb; ++qb) {
             const int lo = max(__ldg(a.mask.q_offs + qb), q0);
             if (lo >= q1) break;
             const int hi = min(__ldg(a.mask.q_offs + qb + 1), q1);
             if (hi > lo && __ldg(map + (int64_t)qb * a.mask.nKb)) {
-              #pragma unroll
-              for (int w = 0; w < 4; ++w) {
-                const int x0 = max(lo - q0, 32 * w), x1 = min(hi - q0, 32 * w + 32);
-                if (x1 > x0) {
-                  const int nb = x1 - x0;
-                  mw[w] |= (nb == 32) ? 0xffffffffu : (((1u << nb) - 1u) << (x0 - 32 * w));
-                }
-              }
+              m0 |= range_bits(lo - q0, hi - q0, 0);
+              m1 |= range_bits(lo - q0, hi - q0, 32);
             }
           }
         }
       }
       // Rows past Sq carry LSE = +inf (set by the producer), so P = 0 there.
       ok = mbar_wait(&sm.q_full[st], (i >> 1) & 1, abort_flag, gstatus, TO) &&
-           mbar_wait(&sm.s_full, i & 1, abort_flag, gstatus, TO) &&
-           mbar_wait(&sm.dp_full, i & 1, abort_flag, gstatus, TO);
-      // dS(i) goes into the buffer that carried dQ(i-1) to the reduce-adds.
-      if (i > 0 && ok) ok = mbar_wait(&sm.ds_idle, (i - 1) & 1, abort_flag, gstatus, TO);
+           mbar_wait(&sm.s_full, i & 1, abort_flag, gstatus, TO);
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       tc_fence_after();
-      const float* lse2 = sm.lse2[st];
-      const float* dvec = sm.dvec[st];
-      uint8_t* ds_row = sm.ds + r * 128;
-      #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t sr[32], pr32[32];
-        tmem_ld32(tS + c * 32, sr);
-        tmem_ld32(tP + c * 32, pr32);
+      const float* lse2 = sm.lse2[st] + c0;
+      const float* dvec = sm.dvec[st] + c0;
+      // ---- P^T for 64 queries (fp32 kept for dS), bf16 copy into TMEM
+      float p[64];
+      {
+        uint32_t s0[32], s1[32];
+        tmem_ld32(tS + c0, s0);
+        tmem_ld32(tS + c0 + 32, s1);
         tmem_ld_wait();
-        uint32_t pp[16], dd[16];
         #pragma unroll
-        for (int k = 0; k < 16; ++k) {
-          float pv[2], dsv[2];
-          #pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const int col = c * 32 + 2 * k + u;
-            const bool allowed = (mw[col >> 5] >> (col & 31)) & 1u;
-            float p = fast_exp2(fmaf(__uint_as_float(sr[2 * k + u]), sl2, -lse2[col]));
-            p = allowed ? p : 0.f;
-            pv[u] = p;
-            dsv[u] = scale * p * (__uint_as_float(pr32[2 * k + u]) - dvec[col]);
-          }
-          pp[k] = pack_bf16x2(pv[0], pv[1]);
-          dd[k] = pack_bf16x2(dsv[0], dsv[1]);
+        for (int c = 0; c < 32; ++c) {
+          const float e0 = fast_exp2(fmaf(__uint_as_float(s0[c]), sl2, -lse2[c]));
+          const float e1 = fast_exp2(fmaf(__uint_as_float(s1[c]), sl2, -lse2[c + 32]));
+          p[c] = ((m0 >> c) & 1u) ? e0 : 0.f;
+          p[c + 32] = ((m1 >> c) & 1u) ? e1 : 0.f;
         }
-        // P^T and dS^T (bf16 pairs) over the first halves of their regions.
-        asm volatile(
-            "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
-            "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
-            :: "r"(tS + c * 16), "r"(pp[0]), "r"(pp[1]), "r"(pp[2]), "r"(pp[3]), "r"(pp[4]),
-               "r"(pp[5]), "r"(pp[6]), "r"(pp[7]), "r"(pp[8]), "r"(pp[9]), "r"(pp[10]),
-               "r"(pp[11]), "r"(pp[12]), "r"(pp[13]), "r"(pp[14]), "r"(pp[15]) : "memory");
-        asm volatile(
-            "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
-            "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
-            :: "r"(tP + c * 16), "r"(dd[0]), "r"(dd[1]), "r"(dd[2]), "r"(dd[3]), "r"(dd[4]),
-               "r"(dd[5]), "r"(dd[6]), "r"(dd[7]), "r"(dd[8]), "r"(dd[9]), "r"(dd[10]),
-               "r"(dd[11]), "r"(dd[12]), "r"(dd[13]), "r"(dd[14]), "r"(dd[15]) : "memory");
-        // dS^T row r, queries c*32 .. c*32+31 -> 4 swizzled 16-byte chunks.
+        uint32_t pk[32];
         #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int chunk = c * 4 + u;          // 8 queries per chunk
-          const int grp = chunk >> 3, cc = chunk & 7;
-          *reinterpret_cast<uint4*>(ds_row + grp * kHalfBytes + ((cc ^ (r & 7)) << 4)) =
-              make_uint4(dd[4 * u], dd[4 * u + 1], dd[4 * u + 2], dd[4 * u + 3]);
+        for (int c = 0; c < 32; ++c) pk[c] = pack_bf16x2(p[2 * c], p[2 * c + 1]);
+        tmem_st32(tS + c0, pk);  // columns [64x, 64x + 32): only this warpgroup read them
+      }
+      // ---- drain dQ of the previous item; frees [128, 256) for dP^T(i)
+      if (i > 0 && !drain(i - 1, qt_prev, h_prev, true)) { ok = false; break; }
+      // ---- dS^T = scale * P^T (dP^T - D)
+      ok = mbar_wait(&sm.dp_full, i & 1, abort_flag, gstatus, TO);
+      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+      tc_fence_after();
+      {
+        uint32_t d0[32], d1[32];
+        tmem_ld32(tP + c0, d0);
+        tmem_ld32(tP + c0 + 32, d1);
+        tmem_ld_wait();
+        uint32_t dk[32];
+        #pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          const float a0 = scale * p[2 * c] * (__uint_as_float(d0[2 * c]) - dvec[2 * c]);
+          const float a1 = scale * p[2 * c + 1] * (__uint_as_float(d0[2 * c + 1]) - dvec[2 * c + 1]);
+          const float b0 = scale * p[32 + 2 * c] * (__uint_as_float(d1[2 * c]) - dvec[32 + 2 * c]);
+          const float b1 = scale * p[33 + 2 * c] * (__uint_as_float(d1[2 * c + 1]) - dvec[33 + 2 * c]);
+          dk[c] = pack_bf16x2(a0, a1);
+          dk[16 + c] = pack_bf16x2(b0, b1);
         }
+        tmem_st32(tP + c0, dk);
+        // dS^T row r, queries [64x, 64x+64) -> 8 swizzled 16-byte chunks of half x.
+        uint8_t* ds_row = sm.ds + x * kHalfBytes + r * 128;
+        #pragma unroll
+        for (int u = 0; u < 8; ++u)
+          *reinterpret_cast<uint4*>(ds_row + ((u ^ (r & 7)) << 4)) =
+              make_uint4(dk[4 * u], dk[4 * u + 1], dk[4 * u + 2], dk[4 * u + 3]);
       }
       tmem_st_wait();
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(&sm.ds_ready);
+      qt_prev = qt;
+      h_prev = h;
     }
-    // ---- dK, dV out (bf16); zero when no query tile touched this key tile
+    if (ok && i > 0) ok = drain(i - 1, qt_prev, h_prev, false);
+    // ---- dV (warpgroup 0) / dK (warpgroup 1) out, bf16; zero when no query
+    // tile touched this key tile.
     if (ok) {
       bool have = i > 0;
       if (have) {
@@ -456,90 +502,32 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
         have = __all_sync(0xffffffffu, have);
         tc_fence_after();
       }
-      for (int which = 0; which < 2; ++which) {
-        const uint32_t tacc = tmem + lane_off + (which == 0 ? 256 : 384);
-        __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(which == 0 ? a.dv : a.dk) +
-                             (int64_t)b * (which == 0 ? a.v_sb : a.k_sb) +
-                             (int64_t)key * (which == 0 ? a.v_ss : a.k_ss) +
-                             (int64_t)g * (which == 0 ? a.v_sh : a.k_sh);
-        #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t x[32];
-          if (have) {
-            tmem_ld32(tacc + c * 32, x);
-            tmem_ld_wait();
-          } else {
-            #pragma unroll
-            for (int k = 0; k < 32; ++k) x[k] = 0u;
-          }
-          if (key_ok) {
-            uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
-            #pragma unroll
-            for (int u = 0; u < 4; ++u)
-              d4[u] = make_uint4(pack_bf16x2(__uint_as_float(x[8 * u]), __uint_as_float(x[8 * u + 1])),
-                                 pack_bf16x2(__uint_as_float(x[8 * u + 2]), __uint_as_float(x[8 * u + 3])),
-                                 pack_bf16x2(__uint_as_float(x[8 * u + 4]), __uint_as_float(x[8 * u + 5])),
-                                 pack_bf16x2(__uint_as_float(x[8 * u + 6]), __uint_as_float(x[8 * u + 7])));
-          }
+      const uint32_t tacc = tmem + lane_off + (x == 0 ? 256 : 384);
+      __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(x == 0 ? a.dv : a.dk) +
+                           (int64_t)b * (x == 0 ? a.v_sb : a.k_sb) +
+                           (int64_t)key * (x == 0 ? a.v_ss : a.k_ss) +
+                           (int64_t)g * (x == 0 ? a.v_sh : a.k_sh);
+      #pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t xr[32];
+        if (have) {
+          tmem_ld32(tacc + c * 32, xr);
+          tmem_ld_wait();
+        } else {
+          #pragma unroll
+          for (int k = 0; k < 32; ++k) xr[k] = 0u;
+        }
+        if (key_ok) {
+          uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
+          #pragma unroll
+          for (int u = 0; u < 4; ++u)
+            d4[u] = make_uint4(pack_bf16x2(__uint_as_float(xr[8 * u]), __uint_as_float(xr[8 * u + 1])),
+                               pack_bf16x2(__uint_as_float(xr[8 * u + 2]), __uint_as_float(xr[8 * u + 3])),
+                               pack_bf16x2(__uint_as_float(xr[8 * u + 4]), __uint_as_float(xr[8 * u + 5])),
+                               pack_bf16x2(__uint_as_float(xr[8 * u + 6]), __uint_as_float(xr[8 * u + 7])));
         }
       }
     }
-  } else {
-    // ------------------------------------------------------------ dQ drain
-    const int r = tid - 128;  // query row within the tile
-    const bool elected = (r == 0);
-    const uint32_t lane_off = static_cast<uint32_t>(32 * (warp & 3)) << 16;
-    const uint32_t tQ = tmem + lane_off + 128;
-    ItemIter it;
-    it.init(a.meta, b, kt, pr.G, g);
-    int i = 0, n = 0;  // n counts 32-column chunks; chunk n uses staging half n & 1
-    bool ok = true;
-    for (; ok && it.valid(); it.next(), ++i) {
-      const int qt = it.entry() >> 1;
-      const int h = it.head();
-      ok = mbar_wait(&sm.dq_full, i & 1, abort_flag, gstatus, TO);
-      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-      tc_fence_after();
-      #pragma unroll 1
-      for (int c = 0; c < 4; ++c, ++n) {
-        const int st = n & 1, use = n >> 1;
-        if (use > 0) {
-          ok = mbar_wait(&sm.stg_free[st], (use - 1) & 1, abort_flag, gstatus, TO);
-          if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-        }
-        uint32_t x[32];
-        tmem_ld32(tQ + c * 32, x);
-        tmem_ld_wait();
-        if (c == 3) {  // every TMEM read of dQ(i) is done: its columns may be reused
-          tc_fence_before();
-          mbar_arrive(&sm.dq_free);
-        }
-        uint8_t* stg = sm.ds + st * kHalfBytes + r * 128;
-        #pragma unroll
-        for (int u = 0; u < 8; ++u)
-          *reinterpret_cast<uint4*>(stg + ((u ^ (r & 7)) << 4)) =
-              make_uint4(x[4 * u], x[4 * u + 1], x[4 * u + 2], x[4 * u + 3]);
-        fence_proxy_async_smem();
-        mbar_arrive(&sm.stg_full[st]);
-        if (elected) {
-          int dummy = 0;
-          if (mbar_wait(&sm.stg_full[st], use & 1, &dummy, gstatus, TO)) {
-            tma_reduce_add_4d(&tmdQacc, sm.ds + st * kHalfBytes, c * 32, h, qt * kBM, b);
-            bulk_commit_group();
-          }
-          // The previous chunk's source has been read: free its half.
-          bulk_wait_group_read<1>();
-          if (c > 0) mbar_arrive(&sm.stg_free[(n - 1) & 1]);
-        }
-      }
-      if (!ok) break;
-      if (elected) {
-        bulk_wait_group_read<0>();
-        mbar_arrive(&sm.stg_free[(n - 1) & 1]);
-        mbar_arrive(&sm.ds_idle);  // the dS buffer is free for dS(i+1)
-      }
-    }
-    if (elected) bulk_wait_group<0>();  // reduce-adds complete before the CTA exits
   }
 
   tc_fence_before();
@@ -565,8 +553,7 @@ cudaError_t launch_bwd_prepass(const BwdArgs& a, cudaStream_t st) {
 }
 
 cudaError_t launch_bwd_dkdv(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                            const CUtensorMap& tdo, const CUtensorMap& tdq_acc, const BwdArgs& a,
-                            cudaStream_t st) {
+                            const CUtensorMap& tdo, const BwdArgs& a, cudaStream_t st) {
   static bool attr_done = false;
   const size_t smem = sizeof(BwdSmem);
   if (!attr_done) {
@@ -578,7 +565,7 @@ cudaError_t launch_bwd_dkdv(const CUtensorMap& tq, const CUtensorMap& tk, const 
   BwdKernelArgs ka;
   ka.a = a;
   dim3 grid(a.meta.nKt, a.pr.Hkv, a.pr.B);
-  dkdv_kernel<<<grid, kThreads, smem, st>>>(tq, tk, tv, tdo, tdq_acc, ka);
+  dkdv_kernel<<<grid, kThreads, smem, st>>>(tq, tk, tv, tdo, ka);
   return cudaGetLastError();
 }
 

@@ -78,8 +78,7 @@ struct BwdArgs {
 };
 cudaError_t launch_bwd_prepass(const BwdArgs& a, cudaStream_t st);
 cudaError_t launch_bwd_dkdv(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                            const CUtensorMap& tdo, const CUtensorMap& tdq_acc, const BwdArgs& a,
-                            cudaStream_t st);
+                            const CUtensorMap& tdo, const BwdArgs& a, cudaStream_t st);
 cudaError_t launch_bwd_dq_convert(const BwdArgs& a, cudaStream_t st);
 
 }  // namespace lcattn

@@ -116,29 +116,6 @@ __device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* m, uin
       : "memory");
 }
 
-// Bulk tensor reduce-add shared -> global (fp32 add in L2), tracked by bulk groups.
-__device__ __forceinline__ void tma_reduce_add_4d(const CUtensorMap* m, const void* src, int32_t c0,
-                                                  int32_t c1, int32_t c2, int32_t c3) {
-  asm volatile(
-      "cp.reduce.async.bulk.tensor.4d.global.shared::cta.add.tile.bulk_group"
-      " [%0, {%2, %3, %4, %5}], [%1];"
-      :: "l"(reinterpret_cast<uint64_t>(m)), "r"(smem_u32(src)), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
-      : "memory");
-}
-__device__ __forceinline__ void bulk_commit_group() {
-  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-}
-// Wait until at most N bulk groups still read their shared-memory source.
-template <int N>
-__device__ __forceinline__ void bulk_wait_group_read() {
-  asm volatile("cp.async.bulk.wait_group.read %0;" :: "n"(N) : "memory");
-}
-// Wait until at most N bulk groups are still in flight (writes included).
-template <int N>
-__device__ __forceinline__ void bulk_wait_group() {
-  asm volatile("cp.async.bulk.wait_group %0;" :: "n"(N) : "memory");
-}
-
 // ---------------------------------------------------------------------------
 // tcgen05: tensor memory
 // ---------------------------------------------------------------------------
