@@ -12,18 +12,22 @@
 // sections "稀疏内核性能" and "核心发现总结"); the gradients are the textbook ones
 // for L = <O, dO>.
 //
-// dK/dV kernel roles (320 threads):
+// dK/dV kernel roles (512 threads, 4 warpgroups):
 //   warps 0-3, 4-7  two warpgroups, one per half of the 128 query columns of a
 //              tile.  Thread r is key row r of S^T / dP^T (TMEM lane r): it
-//              builds its half of P^T and dS^T, writes both to TMEM (bf16, in
-//              columns only its own warpgroup reads) and dS^T to shared memory
-//              for the dQ product.  The same thread is head-dim row r of dQ^T
-//              and adds its half of dQ into the accumulator: a warp's 32 lanes
-//              cover 128 contiguous bytes of one query row, one L2 request per
-//              instruction.  At the end warpgroup 0 stores dV, warpgroup 1 dK.
-//   warp  8    producer: K, V once; Q_i, dO_i by TMA and LSE_i, D_i by plain
+//              builds its half of P'^T = scale * P^T and dS^T, writes both to
+//              TMEM (bf16, in columns only its own warpgroup reads) and dS^T to
+//              shared memory for the dQ product.  At the end warpgroup 0 stores
+//              dV (= sum P'^T dO / scale), warpgroup 1 dK.
+//   warps 8-11 dQ drain.  Thread r is head-dim row r of dQ^T = K^T dS^T: it
+//              reads all 128 query columns out of TMEM (freeing them for the
+//              next dP^T at once), then adds them into the fp32 accumulator;
+//              a warp's 32 lanes cover 128 contiguous bytes of one query row,
+//              one L2 request per instruction, off the MMA's critical path.
+//   warp  12   producer: K, V once; Q_i, dO_i by TMA and LSE_i, D_i by plain
 //              loads into a 2-deep ring.
-//   warp  9    TMEM owner and MMA issuer.
+//   warp  13   TMEM owner and MMA issuer; warps 14-15 idle (they complete the
+//              warpgroup for setmaxnreg).
 // TMEM: [0,128) S^T then P^T | [128,256) dP^T then dS^T, then dQ^T |
 //       [256,384) dV | [384,512) dK.
 #include <cuda_bf16.h>
@@ -38,7 +42,12 @@ using namespace dev;
 
 constexpr int kTileBytes = 32768;
 constexpr int kHalfBytes = 16384;
-constexpr int kThreads = 320;
+constexpr int kThreadsDkdv = 512;      // 4 warpgroups
+// Register split for dK/dV (launch: 512 threads x 128): the two elementwise
+// warpgroups and the drain warpgroup 144 each, producer/MMA warpgroup 80.
+constexpr int kRegsWork = 144;
+constexpr int kRegsCtl = 80;
+static_assert(128 * (3 * kRegsWork + kRegsCtl) <= kThreadsDkdv * 128, "register split");
 constexpr float kLog2e = 1.4426950408889634f;
 
 // ---------------------------------------------------------------------------
@@ -110,8 +119,8 @@ struct BwdSmem {
   alignas(1024) uint8_t q[2][kTileBytes];
   alignas(1024) uint8_t dO[2][kTileBytes];
   alignas(1024) uint8_t ds[kTileBytes];  // dS^T, keys x queries, read MN-major by dQ^T
-  float lse2[2][128];  // LSE * log2(e); +inf where P must be 0
-  float dvec[2][128];
+  alignas(16) float lse2[2][128];  // LSE*log2(e) - log2(scale); +inf where P must be 0
+  alignas(16) float dvec_s[2][128];
   uint64_t kv_full;
   uint64_t q_full[2];
   uint64_t q_empty[2];
@@ -169,7 +178,7 @@ __device__ __forceinline__ uint32_t range_bits(int lo, int hi, int base) {
   return (n == 32) ? 0xffffffffu : (((1u << n) - 1u) << (a - base));
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreadsDkdv, 1)
 dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
             const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
             const __grid_constant__ BwdKernelArgs ka) {
@@ -201,12 +210,12 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
     mbar_init(&sm.dp_full, 1);
     mbar_init(&sm.ds_ready, 256);
     mbar_init(&sm.dq_full, 1);
-    mbar_init(&sm.dq_free, 256);
+    mbar_init(&sm.dq_free, 128);
     mbar_init(&sm.done, 1);
     sm.abort_flag = 0;
     fence_barrier_init();
   }
-  if (warp == 9) tmem_alloc(&sm.tmem_base, 512);
+  if (warp == 13) tmem_alloc(&sm.tmem_base, 512);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -214,7 +223,9 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
   volatile int* abort_flag = &sm.abort_flag;
   const int TO = LCATTN_ERR_DEVICE_TIMEOUT;
 
-  if (warp == 8) {
+  if (warp >= 12) {
+    regs_dec<kRegsCtl>();
+  if (warp == 12) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       tma_prefetch_desc(&tmQ);
@@ -245,6 +256,7 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
         tma_load_4d(sm.dO[st], &tmdO, &sm.q_full[st], 0, h, qt * kBM, b);
         tma_load_4d(sm.dO[st] + kHalfBytes, &tmdO, &sm.q_full[st], 64, h, qt * kBM, b);
       }
+      const float log2_scale = log2f(a.scale);
       const float* lse = a.lse + ((int64_t)b * pr.Hq + h) * pr.Sq;
       const float* dv = a.dvec + ((int64_t)b * pr.Hq + h) * pr.Sq;
       #pragma unroll
@@ -254,11 +266,11 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
         float l2 = INFINITY, d = 0.f;
         if (q < pr.Sq) {
           const float l = __ldg(lse + q);
-          l2 = (l == -INFINITY) ? INFINITY : l * kLog2e;  // fully masked row: P = 0
+          l2 = (l == -INFINITY) ? INFINITY : l * kLog2e - log2_scale;  // fully masked row: P = 0
           d = __ldg(dv + q);
         }
         sm.lse2[st][c] = l2;
-        sm.dvec[st][c] = d;
+        sm.dvec_s[st][c] = d;
       }
       mbar_arrive(&sm.q_full[st]);
       issued = i + 1;
@@ -269,7 +281,7 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
         mbar_wait(&sm.q_full[t & 1], (t >> 1) & 1, &dummy, gstatus, TO);
       mbar_wait(&sm.kv_full, 0, &dummy, gstatus, TO);
     }
-  } else if (warp == 9) {
+  } else if (warp == 13) {
     // ------------------------------------------------------------ MMA issuer
     // Per item i: dP^T(i) | wait dS(i) | dV, dK | S^T(i+1) | dQ^T(i).  S^T(i+1)
     // goes before dQ^T(i) so that P(i+1) is computed while dQ^T(i) runs.
@@ -347,10 +359,46 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
       int dummy = 0;
       mbar_wait(&sm.done, 0, &dummy, gstatus, TO);
     }
+  }
+  } else if (warp >= 8) {
+    regs_inc<kRegsWork>();
+    // ------------------------------------------------------------ dQ drain
+    const int r = 32 * (warp & 3) + lane;  // head-dim row of dQ^T (TMEM lane)
+    const uint32_t tQ = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16) + 128;
+    const int64_t dq_row_stride = (int64_t)pr.Hq * kD;
+    ItemIter it;
+    it.init(a.meta, b, kt, pr.G, g);
+    for (int i = 0; it.valid(); it.next(), ++i) {
+      const int qt = it.entry() >> 1;
+      const int h = it.head();
+      bool ok = mbar_wait(&sm.dq_full, i & 1, abort_flag, gstatus, TO);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      tc_fence_after();
+      uint32_t d[128];
+      tmem_ld32(tQ, d);
+      tmem_ld32(tQ + 32, d + 32);
+      tmem_ld32(tQ + 64, d + 64);
+      tmem_ld32(tQ + 96, d + 96);
+      tmem_ld_wait();
+      tc_fence_before();
+      mbar_arrive(&sm.dq_free);  // columns [128, 256) may take dP^T(i+1) now
+      const int q0 = qt * kBM;
+      const int nq = min(kBM, pr.Sq - q0);
+      float* dst = a.dq_acc + (((int64_t)b * pr.Sq + q0) * pr.Hq + h) * kD + r;
+      if (nq == kBM) {
+        #pragma unroll
+        for (int c = 0; c < 128; ++c) atomicAdd(dst + c * dq_row_stride, __uint_as_float(d[c]));
+      } else {
+        #pragma unroll
+        for (int c = 0; c < 128; ++c)
+          if (c < nq) atomicAdd(dst + c * dq_row_stride, __uint_as_float(d[c]));
+      }
+    }
   } else {
-    // ------------------------------------------------- elementwise + dQ drain
+    regs_inc<kRegsWork>();
+    // ------------------------------------------------------------ elementwise
     // Warpgroup x takes query columns [64x, 64x+64) of every tile; thread r is
-    // key row r of S^T / dP^T and head-dim row r of dQ^T (the TMEM lane).
+    // key row r of S^T / dP^T (the TMEM lane).
     const int x = warp >> 2;
     const int r = 32 * (warp & 3) + lane;
     const int c0 = 64 * x;
@@ -358,41 +406,16 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
     const bool key_ok = key < pr.Sk;
     const uint32_t lane_off = static_cast<uint32_t>(32 * (warp & 3)) << 16;
     const uint32_t tS = tmem + lane_off, tP = tmem + lane_off + 128;
-    const float sl2 = a.scale_log2, scale = a.scale;
+    const float sl2 = a.scale_log2;
     int4 cb = make_int4(0, 0, 0, 0);
     int kb = 0;
     if (key_ok) {
       if (a.mask.kind == LCATTN_MASK_COLBOUNDS) cb = __ldg(a.mask.col_bounds + (int64_t)b * pr.Sk + key);
       else kb = block_of(a.mask.k_offs, a.mask.nKb, key);
     }
-    const int64_t dq_row_stride = (int64_t)pr.Hq * kD;
-    // Adds this warpgroup's half of dQ(item) (TMEM columns [128 + 64x, +64)).
-    auto drain = [&](int i_prev, int qt_prev, int h_prev, bool signal) -> bool {
-      bool okd = mbar_wait(&sm.dq_full, i_prev & 1, abort_flag, gstatus, TO);
-      if (!__all_sync(0xffffffffu, okd)) return false;
-      tc_fence_after();
-      uint32_t d0[32], d1[32];
-      tmem_ld32(tP + c0, d0);
-      tmem_ld32(tP + c0 + 32, d1);
-      tmem_ld_wait();
-      if (signal) {
-        tc_fence_before();
-        mbar_arrive(&sm.dq_free);
-      }
-      const int qbase = qt_prev * kBM + c0;
-      float* dst = a.dq_acc + (((int64_t)b * pr.Sq + qbase) * pr.Hq + h_prev) * kD + r;
-      const int nq = min(64, pr.Sq - qbase);
-      #pragma unroll
-      for (int c = 0; c < 32; ++c)
-        if (c < nq) atomicAdd(dst + c * dq_row_stride, __uint_as_float(d0[c]));
-      #pragma unroll
-      for (int c = 0; c < 32; ++c)
-        if (c + 32 < nq) atomicAdd(dst + (c + 32) * dq_row_stride, __uint_as_float(d1[c]));
-      return true;
-    };
     ItemIter it;
     it.init(a.meta, b, kt, pr.G, g);
-    int i = 0, qt_prev = 0, h_prev = 0;
+    int i = 0;
     bool ok = true;
     for (; it.valid(); it.next(), ++i) {
       const int st = i & 1;
@@ -400,12 +423,13 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
       const int qt = e >> 1;
       const int h = it.head();
       const int q0 = qt * kBM + c0;
-      const bool partial = (e & 1) != 0;
-      // Allowed-query bits of this key for the 64 columns (bit c = query q0 + c).
+      // Per-element mask only for partial tiles and keys past Sk (warp-uniform
+      // except for the key test, which is per lane).
+      const bool masked = (e & 1) != 0 || !key_ok;
       uint32_t m0 = 0xffffffffu, m1 = 0xffffffffu;
       if (!key_ok) {
         m0 = m1 = 0u;
-      } else if (partial) {
+      } else if (masked) {
         if (a.mask.kind == LCATTN_MASK_COLBOUNDS) {
           m0 = m1 = 0u;
           #pragma unroll
@@ -435,30 +459,40 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
            mbar_wait(&sm.s_full, i & 1, abort_flag, gstatus, TO);
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       tc_fence_after();
-      const float* lse2 = sm.lse2[st] + c0;
-      const float* dvec = sm.dvec[st] + c0;
-      // ---- P^T for 64 queries (fp32 kept for dS), bf16 copy into TMEM
-      float p[64];
+      const float4* lse4 = reinterpret_cast<const float4*>(sm.lse2[st] + c0);
+      const float4* dv4 = reinterpret_cast<const float4*>(sm.dvec_s[st] + c0);
+      // ---- P'^T = scale * P^T for 64 queries, bf16 into TMEM (kept packed)
+      uint32_t pk[32];
       {
         uint32_t s0[32], s1[32];
         tmem_ld32(tS + c0, s0);
         tmem_ld32(tS + c0 + 32, s1);
         tmem_ld_wait();
         #pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          const float e0 = fast_exp2(fmaf(__uint_as_float(s0[c]), sl2, -lse2[c]));
-          const float e1 = fast_exp2(fmaf(__uint_as_float(s1[c]), sl2, -lse2[c + 32]));
-          p[c] = ((m0 >> c) & 1u) ? e0 : 0.f;
-          p[c + 32] = ((m1 >> c) & 1u) ? e1 : 0.f;
+        for (int c4 = 0; c4 < 8; ++c4) {
+          const float4 la = lse4[c4], lb = lse4[8 + c4];
+          const float l_a[4] = {la.x, la.y, la.z, la.w}, l_b[4] = {lb.x, lb.y, lb.z, lb.w};
+          float pa[4], pb[4];
+          #pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            pa[u] = fast_exp2(fmaf(__uint_as_float(s0[4 * c4 + u]), sl2, -l_a[u]));
+            pb[u] = fast_exp2(fmaf(__uint_as_float(s1[4 * c4 + u]), sl2, -l_b[u]));
+          }
+          if (masked) {
+            #pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              pa[u] = ((m0 >> (4 * c4 + u)) & 1u) ? pa[u] : 0.f;
+              pb[u] = ((m1 >> (4 * c4 + u)) & 1u) ? pb[u] : 0.f;
+            }
+          }
+          pk[2 * c4] = pack_bf16x2(pa[0], pa[1]);
+          pk[2 * c4 + 1] = pack_bf16x2(pa[2], pa[3]);
+          pk[16 + 2 * c4] = pack_bf16x2(pb[0], pb[1]);
+          pk[16 + 2 * c4 + 1] = pack_bf16x2(pb[2], pb[3]);
         }
-        uint32_t pk[32];
-        #pragma unroll
-        for (int c = 0; c < 32; ++c) pk[c] = pack_bf16x2(p[2 * c], p[2 * c + 1]);
         tmem_st32(tS + c0, pk);  // columns [64x, 64x + 32): only this warpgroup read them
       }
-      // ---- drain dQ of the previous item; frees [128, 256) for dP^T(i)
-      if (i > 0 && !drain(i - 1, qt_prev, h_prev, true)) { ok = false; break; }
-      // ---- dS^T = scale * P^T (dP^T - D)
+      // ---- dS^T = P'^T (dP^T - D) = scale * P^T (dP^T - D), from the bf16 P'
       ok = mbar_wait(&sm.dp_full, i & 1, abort_flag, gstatus, TO);
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       tc_fence_after();
@@ -469,13 +503,22 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
         tmem_ld_wait();
         uint32_t dk[32];
         #pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          const float a0 = scale * p[2 * c] * (__uint_as_float(d0[2 * c]) - dvec[2 * c]);
-          const float a1 = scale * p[2 * c + 1] * (__uint_as_float(d0[2 * c + 1]) - dvec[2 * c + 1]);
-          const float b0 = scale * p[32 + 2 * c] * (__uint_as_float(d1[2 * c]) - dvec[32 + 2 * c]);
-          const float b1 = scale * p[33 + 2 * c] * (__uint_as_float(d1[2 * c + 1]) - dvec[33 + 2 * c]);
-          dk[c] = pack_bf16x2(a0, a1);
-          dk[16 + c] = pack_bf16x2(b0, b1);
+        for (int c4 = 0; c4 < 8; ++c4) {
+          const float4 da = dv4[c4], db = dv4[8 + c4];
+          const float D_a[4] = {da.x, da.y, da.z, da.w}, D_b[4] = {db.x, db.y, db.z, db.w};
+          float sa[4], sb[4];
+          #pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const uint32_t wa = pk[2 * c4 + (u >> 1)], wb = pk[16 + 2 * c4 + (u >> 1)];
+            const float p_a = __uint_as_float((u & 1) ? (wa & 0xffff0000u) : (wa << 16));
+            const float p_b = __uint_as_float((u & 1) ? (wb & 0xffff0000u) : (wb << 16));
+            sa[u] = p_a * (__uint_as_float(d0[4 * c4 + u]) - D_a[u]);
+            sb[u] = p_b * (__uint_as_float(d1[4 * c4 + u]) - D_b[u]);
+          }
+          dk[2 * c4] = pack_bf16x2(sa[0], sa[1]);
+          dk[2 * c4 + 1] = pack_bf16x2(sa[2], sa[3]);
+          dk[16 + 2 * c4] = pack_bf16x2(sb[0], sb[1]);
+          dk[16 + 2 * c4 + 1] = pack_bf16x2(sb[2], sb[3]);
         }
         tmem_st32(tP + c0, dk);
         // dS^T row r, queries [64x, 64x+64) -> 8 swizzled 16-byte chunks of half x.
@@ -489,12 +532,9 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(&sm.ds_ready);
-      qt_prev = qt;
-      h_prev = h;
     }
-    if (ok && i > 0) ok = drain(i - 1, qt_prev, h_prev, false);
     // ---- dV (warpgroup 0) / dK (warpgroup 1) out, bf16; zero when no query
-    // tile touched this key tile.
+    // tile touched this key tile.  dV accumulated P' = scale * P: undo it.
     if (ok) {
       bool have = i > 0;
       if (have) {
@@ -502,6 +542,7 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
         have = __all_sync(0xffffffffu, have);
         tc_fence_after();
       }
+      const float mul = x == 0 ? 1.f / a.scale : 1.f;
       const uint32_t tacc = tmem + lane_off + (x == 0 ? 256 : 384);
       __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(x == 0 ? a.dv : a.dk) +
                            (int64_t)b * (x == 0 ? a.v_sb : a.k_sb) +
@@ -521,10 +562,11 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
           uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
           #pragma unroll
           for (int u = 0; u < 4; ++u)
-            d4[u] = make_uint4(pack_bf16x2(__uint_as_float(xr[8 * u]), __uint_as_float(xr[8 * u + 1])),
-                               pack_bf16x2(__uint_as_float(xr[8 * u + 2]), __uint_as_float(xr[8 * u + 3])),
-                               pack_bf16x2(__uint_as_float(xr[8 * u + 4]), __uint_as_float(xr[8 * u + 5])),
-                               pack_bf16x2(__uint_as_float(xr[8 * u + 6]), __uint_as_float(xr[8 * u + 7])));
+            d4[u] = make_uint4(
+                pack_bf16x2(__uint_as_float(xr[8 * u]) * mul, __uint_as_float(xr[8 * u + 1]) * mul),
+                pack_bf16x2(__uint_as_float(xr[8 * u + 2]) * mul, __uint_as_float(xr[8 * u + 3]) * mul),
+                pack_bf16x2(__uint_as_float(xr[8 * u + 4]) * mul, __uint_as_float(xr[8 * u + 5]) * mul),
+                pack_bf16x2(__uint_as_float(xr[8 * u + 6]) * mul, __uint_as_float(xr[8 * u + 7]) * mul));
         }
       }
     }
@@ -533,7 +575,7 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 9) {
+  if (warp == 13) {
     __syncwarp();
     tmem_dealloc(tmem, 512);
   }
@@ -565,7 +607,7 @@ cudaError_t launch_bwd_dkdv(const CUtensorMap& tq, const CUtensorMap& tk, const 
   BwdKernelArgs ka;
   ka.a = a;
   dim3 grid(a.meta.nKt, a.pr.Hkv, a.pr.B);
-  dkdv_kernel<<<grid, kThreads, smem, st>>>(tq, tk, tv, tdo, ka);
+  dkdv_kernel<<<grid, kThreadsDkdv, smem, st>>>(tq, tk, tv, tdo, ka);
   return cudaGetLastError();
 }
 
