@@ -44,9 +44,9 @@ constexpr int kTileBytes = 32768;
 constexpr int kHalfBytes = 16384;
 constexpr int kThreadsDkdv = 512;      // 4 warpgroups
 // Register split for dK/dV (launch: 512 threads x 128): the two elementwise
-// warpgroups and the drain warpgroup 144 each, producer/MMA warpgroup 80.
-constexpr int kRegsWork = 144;
-constexpr int kRegsCtl = 80;
+// warpgroups and the drain warpgroup 136 each, producer/MMA warpgroup 104.
+constexpr int kRegsWork = 136;
+constexpr int kRegsCtl = 104;
 static_assert(128 * (3 * kRegsWork + kRegsCtl) <= kThreadsDkdv * 128, "register split");
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -290,69 +290,76 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
       const uint32_t id_ts = idesc_bf16_f32(128, 128, false, true);
       const uint32_t id_mn = idesc_bf16_f32(128, 128, true, true);
       const uint32_t tS = tmem, tP = tmem + 128, tdV = tmem + 256, tdK = tmem + 384;
-      const uint32_t k_s = smem_u32(sm.k), v_s = smem_u32(sm.v), ds_s = smem_u32(sm.ds);
+      // Base descriptors (K-major and MN-major views); ring stage st is kTileBytes on.
+      const uint64_t dK_k = sdesc_sw128(smem_u32(sm.k), 16, 1024);
+      const uint64_t dK_mn = sdesc_sw128(smem_u32(sm.k), kHalfBytes, 1024);
+      const uint64_t dV_k = sdesc_sw128(smem_u32(sm.v), 16, 1024);
+      const uint64_t dQ_k = sdesc_sw128(smem_u32(sm.q[0]), 16, 1024);
+      const uint64_t dQ_mn = sdesc_sw128(smem_u32(sm.q[0]), kHalfBytes, 1024);
+      const uint64_t dO_k = sdesc_sw128(smem_u32(sm.dO[0]), 16, 1024);
+      const uint64_t dO_mn = sdesc_sw128(smem_u32(sm.dO[0]), kHalfBytes, 1024);
+      const uint64_t dS_mn = sdesc_sw128(smem_u32(sm.ds), kHalfBytes, 1024);
       bool ok = mbar_wait(&sm.kv_full, 0, abort_flag, gstatus, TO);
       ItemIter it;
       it.init(a.meta, b, kt, pr.G, g);
-      auto issue_s = [&](int st) {  // S^T = K Q^T into [0, 128)
-        const uint32_t q_s = smem_u32(sm.q[st]);
+      // Both operands K-major: 16-column steps inside a 64-column half, then the next half.
+      auto issue_kmaj = [&](uint32_t d, uint64_t a0, uint64_t b0) {
+        mma_ss_c<0>(d, a0, b0, id_kmaj);
         #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
+        for (int kk = 1; kk < 8; ++kk) {
           const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
-          mma_ss(tS, sdesc_sw128(k_s + off, 16, 1024), sdesc_sw128(q_s + off, 16, 1024), id_kmaj,
-                 kk > 0 ? 1u : 0u);
+          mma_ss_c<1>(d, sdesc_add(a0, off), sdesc_add(b0, off), id_kmaj);
         }
-        tc_commit(&sm.s_full);
       };
       if (ok && it.valid()) {
         ok = mbar_wait(&sm.q_full[0], 0, abort_flag, gstatus, TO);
         if (ok) {
           tc_fence_after();
-          issue_s(0);
+          issue_kmaj(tS, dK_k, dQ_k);  // S^T(0) = K Q_0^T
+          tc_commit(&sm.s_full);
         }
       }
       int i = 0;
       for (; ok && it.valid(); ++i) {
         const int st = i & 1;
-        const uint32_t q_s = smem_u32(sm.q[st]), do_s = smem_u32(sm.dO[st]);
+        const uint32_t qoff = st * kTileBytes;
         // dP^T = V dO^T, into the columns dQ^T(i-1) used: wait for its drain.
         if (i > 0) {
           if (!(ok = mbar_wait(&sm.dq_free, (i - 1) & 1, abort_flag, gstatus, TO))) break;
           tc_fence_after();
         }
-        #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
-          mma_ss(tP, sdesc_sw128(v_s + off, 16, 1024), sdesc_sw128(do_s + off, 16, 1024), id_kmaj,
-                 kk > 0 ? 1u : 0u);
-        }
+        issue_kmaj(tP, dV_k, sdesc_add(dO_k, qoff));
         tc_commit(&sm.dp_full);
         if (!(ok = mbar_wait(&sm.ds_ready, i & 1, abort_flag, gstatus, TO))) break;
         tc_fence_after();
-        // dV += P^T dO ; dK += dS^T Q.  A from TMEM: queries 0-63 sit in the
+        // dV += P'^T dO ; dK += dS^T Q.  A from TMEM: queries 0-63 sit in the
         // first 32 columns of each half's region, queries 64-127 at +64.
-        #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          mma_ts(tdV, tS + (kk >> 2) * 64 + (kk & 3) * 8,
-                 sdesc_sw128(do_s + kk * 2048, kHalfBytes, 1024), id_ts, (i > 0 || kk > 0) ? 1u : 0u);
-        #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          mma_ts(tdK, tP + (kk >> 2) * 64 + (kk & 3) * 8,
-                 sdesc_sw128(q_s + kk * 2048, kHalfBytes, 1024), id_ts, (i > 0 || kk > 0) ? 1u : 0u);
+        {
+          const uint64_t bo = sdesc_add(dO_mn, qoff), bq = sdesc_add(dQ_mn, qoff);
+          mma_ts(tdV, tS, bo, id_ts, i > 0 ? 1u : 0u);
+          #pragma unroll
+          for (int kk = 1; kk < 8; ++kk)
+            mma_ts_c<1>(tdV, tS + (kk >> 2) * 64 + (kk & 3) * 8, sdesc_add(bo, kk * 2048), id_ts);
+          mma_ts(tdK, tP, bq, id_ts, i > 0 ? 1u : 0u);
+          #pragma unroll
+          for (int kk = 1; kk < 8; ++kk)
+            mma_ts_c<1>(tdK, tP + (kk >> 2) * 64 + (kk & 3) * 8, sdesc_add(bq, kk * 2048), id_ts);
+        }
         tc_commit(&sm.q_empty[st]);
         it.next();
         if (it.valid()) {
           const int st2 = (i + 1) & 1;
           if (!(ok = mbar_wait(&sm.q_full[st2], ((i + 1) >> 1) & 1, abort_flag, gstatus, TO))) break;
           tc_fence_after();
-          issue_s(st2);
+          issue_kmaj(tS, dK_k, sdesc_add(dQ_k, st2 * kTileBytes));  // S^T(i+1)
+          tc_commit(&sm.s_full);
         }
         // dQ^T = K^T dS^T: A = K read MN-major (M = head dim), B = dS^T read
         // MN-major (N = queries).  Lands in [128, 256): lane = head dim.
+        mma_ss_c<0>(tP, dK_mn, dS_mn, id_mn);
         #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          mma_ss(tP, sdesc_sw128(k_s + kk * 2048, kHalfBytes, 1024),
-                 sdesc_sw128(ds_s + kk * 2048, kHalfBytes, 1024), id_mn, kk > 0 ? 1u : 0u);
+        for (int kk = 1; kk < 8; ++kk)
+          mma_ss_c<1>(tP, sdesc_add(dK_mn, kk * 2048), sdesc_add(dS_mn, kk * 2048), id_mn);
         tc_commit(&sm.dq_full);
       }
       tc_commit(&sm.done);

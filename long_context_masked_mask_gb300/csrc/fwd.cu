@@ -45,6 +45,8 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 units
 struct FwdSmem {
   alignas(1024) uint8_t q[2][kTileBytes];
   alignas(1024) uint8_t kv[kStages][kTileBytes];
+  int4 bnd[2][2][kBN];  // column bounds of a partial tile, per slot, double-buffered
+  uint64_t bnd_ready[2][2];
   uint64_t q_full[2];
   uint64_t kv_full[kStages];
   uint64_t kv_empty[kStages];
@@ -79,9 +81,11 @@ __device__ __forceinline__ int block_of(const int32_t* offs, int n, int x) {
 }
 
 // Allowed-key bits of query row `row` for key tile kt (bit c = key kt*128+c).
+// Column bounds are read from `bnd` (the tile's 128 bounds in shared memory).
 __device__ __forceinline__ void tile_mask_bits(const MaskDev& m, const ProblemDev& pr, int b,
                                                int h, int row, int qb_row, int kt,
-                                               bool evaluate_mask, uint32_t (&mw)[4]) {
+                                               bool evaluate_mask, const int4* bnd,
+                                               uint32_t (&mw)[4]) {
   const int j0 = kt * kBN;
   const int nvalid = min(kBN, pr.Sk - j0);
   mw[0] = mw[1] = mw[2] = mw[3] = 0u;
@@ -93,18 +97,16 @@ __device__ __forceinline__ void tile_mask_bits(const MaskDev& m, const ProblemDe
     return;
   }
   if (m.kind == LCATTN_MASK_COLBOUNDS) {
-    const int4* cb = m.col_bounds + (int64_t)b * pr.Sk + j0;
+    // Bounds come from shared memory (staged by the caller); keys past the end
+    // of the sequence were staged as empty intervals.
     #pragma unroll
     for (int w = 0; w < 4; ++w) {
       uint32_t bits = 0u;
       #pragma unroll
       for (int c = 0; c < 32; ++c) {
-        const int key = 32 * w + c;
-        if (key < nvalid) {
-          const int4 v = __ldg(cb + key);
-          const bool ok = (v.x <= row && row < v.y) || (v.z <= row && row < v.w);
-          bits |= (ok ? 1u : 0u) << c;
-        }
+        const int4 v = bnd[32 * w + c];
+        const bool ok = (v.x <= row && row < v.y) || (v.z <= row && row < v.w);
+        bits |= (ok ? 1u : 0u) << c;
       }
       mw[w] = bits;
     }
@@ -163,6 +165,8 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
       mbar_init(&sm.kv_empty[i], 1);
     }
     mbar_init(&sm.drain, 1);
+    for (int s = 0; s < 2; ++s)
+      for (int u = 0; u < 2; ++u) mbar_init(&sm.bnd_ready[s][u], 128);
     sm.abort_flag = 0;
     fence_barrier_init();
   }
@@ -215,6 +219,11 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
     if (lane == 0) {
       const uint32_t idesc_qk = idesc_bf16_f32(128, 128, false, false);
       const uint32_t idesc_pv = idesc_bf16_f32(128, 128, false, true);
+      // Base descriptors; stage s of the ring is kTileBytes further on.
+      const uint64_t dq0 = sdesc_sw128(smem_u32(sm.q[0]), 16, 1024);
+      const uint64_t dq1 = sdesc_sw128(smem_u32(sm.q[1]), 16, 1024);
+      const uint64_t dk0 = sdesc_sw128(smem_u32(sm.kv[0]), 16, 1024);          // K tile, K-major
+      const uint64_t dv0 = sdesc_sw128(smem_u32(sm.kv[0]), kHalfBytes, 1024);  // V tile, MN-major
       bool ok = true;
       for (int s = 0; s < hpc && ok; ++s)
         ok = mbar_wait(&sm.q_full[s], 0, abort_flag, gstatus, LCATTN_ERR_DEVICE_TIMEOUT);
@@ -228,6 +237,8 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
                          LCATTN_ERR_DEVICE_TIMEOUT);
         if (!ok) break;
         tc_fence_after();
+        const uint64_t kb = sdesc_add(dk0, (tk % kStages) * kTileBytes);
+        const uint64_t vb = sdesc_add(dv0, ((tv + kStages) % kStages) * kTileBytes);
         for (int s = 0; s < hpc; ++s) {
           const uint32_t tS = tmem + s * 128, tO = tmem + 256 + s * 128;
           if (j > 0) {
@@ -235,20 +246,21 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
                                  LCATTN_ERR_DEVICE_TIMEOUT)))
               break;
             tc_fence_after();
-            const uint32_t vb = smem_u32(sm.kv[tv % kStages]);
+            // O += P V: A = P (bf16 pairs in TMEM), B = V read MN-major.
+            mma_ts(tO, tS, vb, idesc_pv, j > 1 ? 1u : 0u);
             #pragma unroll
-            for (int kk = 0; kk < 8; ++kk)
-              mma_ts(tO, tS + kk * 8, sdesc_sw128(vb + kk * 2048, kHalfBytes, 1024), idesc_pv,
-                     (j > 1 || kk > 0) ? 1u : 0u);
+            for (int kk = 1; kk < 8; ++kk) mma_ts_c<1>(tO, tS + kk * 8, sdesc_add(vb, kk * 2048), idesc_pv);
             tc_commit(&sm.o_full[s]);
           }
           if (j < n) {
-            const uint32_t qb = smem_u32(sm.q[s]), kb = smem_u32(sm.kv[tk % kStages]);
+            // S = Q K^T, both K-major.
+            const uint64_t qd = s ? dq1 : dq0;
+            mma_ss_c<0>(tS, qd, kb, idesc_qk);
             #pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-              const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
-              mma_ss(tS, sdesc_sw128(qb + off, 16, 1024), sdesc_sw128(kb + off, 16, 1024),
-                     idesc_qk, kk > 0 ? 1u : 0u);
+            for (int kk = 1; kk < 8; ++kk) {
+              constexpr uint32_t kHalf = kHalfBytes;
+              const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
+              mma_ss_c<1>(tS, sdesc_add(qd, off), sdesc_add(kb, off), idesc_qk);
             }
             tc_commit(&sm.s_full[s]);
           }
@@ -282,6 +294,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
         qb_row = block_of(a.mask.q_offs, a.mask.nQb, min(row, pr.Sq - 1));
       float m_run = -INFINITY, l_run = 0.f;
       bool ok = true;
+      int n_partial = 0;  // partial column-bounds tiles staged so far (selects the buffer)
       int e_next = n > 0 ? __ldg(list) : 0;
       for (int j = 0; j < n; ++j) {
         const int e = e_next;
@@ -290,7 +303,24 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
         const bool partial = (e & 1) != 0;
         const bool masked = partial || (ragged_k && kt == last_kt);
         uint32_t mw[4];
-        if (masked) tile_mask_bits(a.mask, pr, b, h, row, qb_row, kt, partial, mw);
+        if (masked) {
+          const int4* bnd = nullptr;
+          if (partial && a.mask.kind == LCATTN_MASK_COLBOUNDS) {
+            // Stage the tile's 128 column bounds in shared memory: one coalesced
+            // load per thread instead of 128 dependent loads per thread.
+            const int u = n_partial & 1;
+            const int key = kt * kBN + r;
+            sm.bnd[s][u][r] = key < pr.Sk ? __ldg(a.mask.col_bounds + (int64_t)b * pr.Sk + key)
+                                          : make_int4(0, 0, 0, 0);
+            mbar_arrive(&sm.bnd_ready[s][u]);
+            ok = mbar_wait(&sm.bnd_ready[s][u], (n_partial >> 1) & 1, abort_flag, gstatus,
+                           LCATTN_ERR_DEVICE_TIMEOUT);
+            if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+            bnd = sm.bnd[s][u];
+            ++n_partial;
+          }
+          tile_mask_bits(a.mask, pr, b, h, row, qb_row, kt, partial, bnd, mw);
+        }
         ok = mbar_wait(&sm.s_full[s], j & 1, abort_flag, gstatus, LCATTN_ERR_DEVICE_TIMEOUT);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
         tc_fence_after();
