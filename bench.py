@@ -218,7 +218,9 @@ def traffic_lookup(kernel):
         return None
     src = os.path.join(ROOT, "long_context_masked_mask_gb300", "csrc", rec["source"])
     sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
-    return rec["dram_bytes_per_launch"] if sha == rec["source_sha256"] else None
+    if sha != rec["source_sha256"]:
+        return None
+    return {"bytes": rec["dram_bytes_per_launch"], "launch": rec["launch"]}
 
 
 def run_gpu(args, rank, world, dist):
@@ -354,7 +356,9 @@ def run_gpu(args, rank, world, dist):
         roof = {"kernel": dom, "bound": "hbm", "achieved": None, "peak": pk["hbm_gbs"], "unit": "GB/s",
                 "frac": None, "peak_kind": f"{pk['source']} copy bandwidth"}
     tr = traffic_lookup(dom)
-    roof["traffic"] = tr
+    roof["traffic"] = tr["bytes"] if tr else None
+    if tr:
+        roof["traffic_launch"] = tr["launch"]
 
     # ---- end to end through the C ABI with host buffers ----------------------
     host = {n: t.cpu().pin_memory() for n, t in (("q", q), ("k", k), ("v", v), ("do", d_o))}
