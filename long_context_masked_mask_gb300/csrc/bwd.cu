@@ -227,17 +227,19 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
     regs_dec<kRegsCtl>();
   if (warp == 12) {
     // ------------------------------------------------------------ producer
+    // The whole warp runs the loop; the elected lane issues the copies.
     if (lane == 0) {
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
       tma_prefetch_desc(&tmdO);
-      mbar_expect_tx(&sm.kv_full, 2 * kTileBytes);
-      tma_load_4d(sm.k, &tmK, &sm.kv_full, 0, g, kt * kBN, b);
-      tma_load_4d(sm.k + kHalfBytes, &tmK, &sm.kv_full, 64, g, kt * kBN, b);
-      tma_load_4d(sm.v, &tmV, &sm.kv_full, 0, g, kt * kBN, b);
-      tma_load_4d(sm.v + kHalfBytes, &tmV, &sm.kv_full, 64, g, kt * kBN, b);
     }
+    __syncwarp();
+    mbar_expect_tx_e(&sm.kv_full, 2 * kTileBytes);
+    tma_load_4d_e(sm.k, &tmK, &sm.kv_full, 0, g, kt * kBN, b);
+    tma_load_4d_e(sm.k + kHalfBytes, &tmK, &sm.kv_full, 64, g, kt * kBN, b);
+    tma_load_4d_e(sm.v, &tmV, &sm.kv_full, 0, g, kt * kBN, b);
+    tma_load_4d_e(sm.v + kHalfBytes, &tmV, &sm.kv_full, 64, g, kt * kBN, b);
     ItemIter it;
     it.init(a.meta, b, kt, pr.G, g);
     int i = 0, issued = 0;
@@ -249,13 +251,11 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
       }
       const int qt = it.entry() >> 1;
       const int h = it.head();
-      if (lane == 0) {
-        mbar_expect_tx(&sm.q_full[st], 2 * kTileBytes);
-        tma_load_4d(sm.q[st], &tmQ, &sm.q_full[st], 0, h, qt * kBM, b);
-        tma_load_4d(sm.q[st] + kHalfBytes, &tmQ, &sm.q_full[st], 64, h, qt * kBM, b);
-        tma_load_4d(sm.dO[st], &tmdO, &sm.q_full[st], 0, h, qt * kBM, b);
-        tma_load_4d(sm.dO[st] + kHalfBytes, &tmdO, &sm.q_full[st], 64, h, qt * kBM, b);
-      }
+      mbar_expect_tx_e(&sm.q_full[st], 2 * kTileBytes);
+      tma_load_4d_e(sm.q[st], &tmQ, &sm.q_full[st], 0, h, qt * kBM, b);
+      tma_load_4d_e(sm.q[st] + kHalfBytes, &tmQ, &sm.q_full[st], 64, h, qt * kBM, b);
+      tma_load_4d_e(sm.dO[st], &tmdO, &sm.q_full[st], 0, h, qt * kBM, b);
+      tma_load_4d_e(sm.dO[st] + kHalfBytes, &tmdO, &sm.q_full[st], 64, h, qt * kBM, b);
       const float log2_scale = log2f(a.scale);
       const float* lse = a.lse + ((int64_t)b * pr.Hq + h) * pr.Sq;
       const float* dv = a.dvec + ((int64_t)b * pr.Hq + h) * pr.Sq;
@@ -275,7 +275,7 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
       mbar_arrive(&sm.q_full[st]);
       issued = i + 1;
     }
-    if (lane == 0) {
+    {
       int dummy = 0;
       for (int t = max(0, issued - 2); t < issued; ++t)
         mbar_wait(&sm.q_full[t & 1], (t >> 1) & 1, &dummy, gstatus, TO);
@@ -284,8 +284,10 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
   } else if (warp == 13) {
     // ------------------------------------------------------------ MMA issuer
     // Per item i: dP^T(i) | wait dS(i) | dV, dK | S^T(i+1) | dQ^T(i).  S^T(i+1)
-    // goes before dQ^T(i) so that P(i+1) is computed while dQ^T(i) runs.
-    if (lane == 0) {
+    // goes before dQ^T(i) so that P(i+1) is computed while dQ^T(i) runs.  The
+    // whole warp runs the loop; each tcgen05.mma / commit is issued by one
+    // elected lane.
+    {
       const uint32_t id_kmaj = idesc_bf16_f32(128, 128, false, false);
       const uint32_t id_ts = idesc_bf16_f32(128, 128, false, true);
       const uint32_t id_mn = idesc_bf16_f32(128, 128, true, true);
@@ -299,24 +301,24 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
       const uint64_t dO_k = sdesc_sw128(smem_u32(sm.dO[0]), 16, 1024);
       const uint64_t dO_mn = sdesc_sw128(smem_u32(sm.dO[0]), kHalfBytes, 1024);
       const uint64_t dS_mn = sdesc_sw128(smem_u32(sm.ds), kHalfBytes, 1024);
-      bool ok = mbar_wait(&sm.kv_full, 0, abort_flag, gstatus, TO);
+      bool ok = __all_sync(0xffffffffu, mbar_wait(&sm.kv_full, 0, abort_flag, gstatus, TO));
       ItemIter it;
       it.init(a.meta, b, kt, pr.G, g);
       // Both operands K-major: 16-column steps inside a 64-column half, then the next half.
       auto issue_kmaj = [&](uint32_t d, uint64_t a0, uint64_t b0) {
-        mma_ss_c<0>(d, a0, b0, id_kmaj);
+        mma_ss_e<0>(d, a0, b0, id_kmaj);
         #pragma unroll
         for (int kk = 1; kk < 8; ++kk) {
           const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
-          mma_ss_c<1>(d, sdesc_add(a0, off), sdesc_add(b0, off), id_kmaj);
+          mma_ss_e<1>(d, sdesc_add(a0, off), sdesc_add(b0, off), id_kmaj);
         }
       };
       if (ok && it.valid()) {
-        ok = mbar_wait(&sm.q_full[0], 0, abort_flag, gstatus, TO);
+        ok = __all_sync(0xffffffffu, mbar_wait(&sm.q_full[0], 0, abort_flag, gstatus, TO));
         if (ok) {
           tc_fence_after();
           issue_kmaj(tS, dK_k, dQ_k);  // S^T(0) = K Q_0^T
-          tc_commit(&sm.s_full);
+          tc_commit_e(&sm.s_full);
         }
       }
       int i = 0;
@@ -325,44 +327,47 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
         const uint32_t qoff = st * kTileBytes;
         // dP^T = V dO^T, into the columns dQ^T(i-1) used: wait for its drain.
         if (i > 0) {
-          if (!(ok = mbar_wait(&sm.dq_free, (i - 1) & 1, abort_flag, gstatus, TO))) break;
+          ok = __all_sync(0xffffffffu, mbar_wait(&sm.dq_free, (i - 1) & 1, abort_flag, gstatus, TO));
+          if (!ok) break;
           tc_fence_after();
         }
         issue_kmaj(tP, dV_k, sdesc_add(dO_k, qoff));
-        tc_commit(&sm.dp_full);
-        if (!(ok = mbar_wait(&sm.ds_ready, i & 1, abort_flag, gstatus, TO))) break;
+        tc_commit_e(&sm.dp_full);
+        ok = __all_sync(0xffffffffu, mbar_wait(&sm.ds_ready, i & 1, abort_flag, gstatus, TO));
+        if (!ok) break;
         tc_fence_after();
         // dV += P'^T dO ; dK += dS^T Q.  A from TMEM: queries 0-63 sit in the
         // first 32 columns of each half's region, queries 64-127 at +64.
         {
           const uint64_t bo = sdesc_add(dO_mn, qoff), bq = sdesc_add(dQ_mn, qoff);
-          mma_ts(tdV, tS, bo, id_ts, i > 0 ? 1u : 0u);
+          mma_ts_er(tdV, tS, bo, id_ts, i > 0 ? 1u : 0u);
           #pragma unroll
           for (int kk = 1; kk < 8; ++kk)
-            mma_ts_c<1>(tdV, tS + (kk >> 2) * 64 + (kk & 3) * 8, sdesc_add(bo, kk * 2048), id_ts);
-          mma_ts(tdK, tP, bq, id_ts, i > 0 ? 1u : 0u);
+            mma_ts_e<1>(tdV, tS + (kk >> 2) * 64 + (kk & 3) * 8, sdesc_add(bo, kk * 2048), id_ts);
+          mma_ts_er(tdK, tP, bq, id_ts, i > 0 ? 1u : 0u);
           #pragma unroll
           for (int kk = 1; kk < 8; ++kk)
-            mma_ts_c<1>(tdK, tP + (kk >> 2) * 64 + (kk & 3) * 8, sdesc_add(bq, kk * 2048), id_ts);
+            mma_ts_e<1>(tdK, tP + (kk >> 2) * 64 + (kk & 3) * 8, sdesc_add(bq, kk * 2048), id_ts);
         }
-        tc_commit(&sm.q_empty[st]);
+        tc_commit_e(&sm.q_empty[st]);
         it.next();
         if (it.valid()) {
           const int st2 = (i + 1) & 1;
-          if (!(ok = mbar_wait(&sm.q_full[st2], ((i + 1) >> 1) & 1, abort_flag, gstatus, TO))) break;
+          ok = __all_sync(0xffffffffu, mbar_wait(&sm.q_full[st2], ((i + 1) >> 1) & 1, abort_flag, gstatus, TO));
+          if (!ok) break;
           tc_fence_after();
           issue_kmaj(tS, dK_k, sdesc_add(dQ_k, st2 * kTileBytes));  // S^T(i+1)
-          tc_commit(&sm.s_full);
+          tc_commit_e(&sm.s_full);
         }
         // dQ^T = K^T dS^T: A = K read MN-major (M = head dim), B = dS^T read
         // MN-major (N = queries).  Lands in [128, 256): lane = head dim.
-        mma_ss_c<0>(tP, dK_mn, dS_mn, id_mn);
+        mma_ss_e<0>(tP, dK_mn, dS_mn, id_mn);
         #pragma unroll
         for (int kk = 1; kk < 8; ++kk)
-          mma_ss_c<1>(tP, sdesc_add(dK_mn, kk * 2048), sdesc_add(dS_mn, kk * 2048), id_mn);
-        tc_commit(&sm.dq_full);
+          mma_ss_e<1>(tP, sdesc_add(dK_mn, kk * 2048), sdesc_add(dS_mn, kk * 2048), id_mn);
+        tc_commit_e(&sm.dq_full);
       }
-      tc_commit(&sm.done);
+      tc_commit_e(&sm.done);
       int dummy = 0;
       mbar_wait(&sm.done, 0, &dummy, gstatus, TO);
     }

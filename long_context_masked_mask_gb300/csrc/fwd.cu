@@ -180,43 +180,49 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
     regs_dec<kRegsOther>();
     if (warp == 8) {
     // ---------------------------------------------------------------- producer
+    // The whole warp runs the loop (waits included); the elected lane issues.
     if (lane == 0) {
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
-      for (int s = 0; s < hpc; ++s) {
-        mbar_expect_tx(&sm.q_full[s], kTileBytes);
-        tma_load_4d(sm.q[s], &tmQ, &sm.q_full[s], 0, h0 + s, qt * kBM, b);
-        tma_load_4d(sm.q[s] + kHalfBytes, &tmQ, &sm.q_full[s], 64, h0 + s, qt * kBM, b);
+    }
+    __syncwarp();
+    for (int s = 0; s < hpc; ++s) {
+      mbar_expect_tx_e(&sm.q_full[s], kTileBytes);
+      tma_load_4d_e(sm.q[s], &tmQ, &sm.q_full[s], 0, h0 + s, qt * kBM, b);
+      tma_load_4d_e(sm.q[s] + kHalfBytes, &tmQ, &sm.q_full[s], 64, h0 + s, qt * kBM, b);
+    }
+    int issued = 0;
+    for (int t = 0; t < 2 * n; ++t) {
+      const int stage = t % kStages, use = t / kStages;
+      if (use > 0) {
+        const bool okw = mbar_wait(&sm.kv_empty[stage], (use - 1) & 1, abort_flag, gstatus,
+                                   LCATTN_ERR_DEVICE_TIMEOUT);
+        if (!__all_sync(0xffffffffu, okw)) break;
       }
-      int issued = 0;
-      for (int t = 0; t < 2 * n; ++t) {
-        const int stage = t % kStages, use = t / kStages;
-        if (use > 0 && !mbar_wait(&sm.kv_empty[stage], (use - 1) & 1, abort_flag, gstatus,
-                                  LCATTN_ERR_DEVICE_TIMEOUT))
-          break;
-        const int kt = __ldg(list + (t >> 1)) >> 1;
-        const CUtensorMap* tm = (t & 1) ? &tmV : &tmK;
-        mbar_expect_tx(&sm.kv_full[stage], kTileBytes);
-        tma_load_4d(sm.kv[stage], tm, &sm.kv_full[stage], 0, g, kt * kBN, b);
-        tma_load_4d(sm.kv[stage] + kHalfBytes, tm, &sm.kv_full[stage], 64, g, kt * kBN, b);
-        issued = t + 1;
-      }
-      // Never leave copies in flight: wait (bounded, ignoring the abort word)
-      // for the last load issued on each stage.
-      for (int t = max(0, issued - kStages); t < issued; ++t) {
-        int dummy = 0;
-        mbar_wait(&sm.kv_full[t % kStages], (t / kStages) & 1, &dummy, gstatus,
-                  LCATTN_ERR_DEVICE_TIMEOUT);
-      }
-      for (int s = 0; s < hpc; ++s) {
-        int dummy = 0;
-        mbar_wait(&sm.q_full[s], 0, &dummy, gstatus, LCATTN_ERR_DEVICE_TIMEOUT);
-      }
+      const int kt = __ldg(list + (t >> 1)) >> 1;
+      const CUtensorMap* tm = (t & 1) ? &tmV : &tmK;
+      mbar_expect_tx_e(&sm.kv_full[stage], kTileBytes);
+      tma_load_4d_e(sm.kv[stage], tm, &sm.kv_full[stage], 0, g, kt * kBN, b);
+      tma_load_4d_e(sm.kv[stage] + kHalfBytes, tm, &sm.kv_full[stage], 64, g, kt * kBN, b);
+      issued = t + 1;
+    }
+    // Never leave copies in flight: wait (bounded, ignoring the abort word)
+    // for the last load issued on each stage.
+    for (int t = max(0, issued - kStages); t < issued; ++t) {
+      int dummy = 0;
+      mbar_wait(&sm.kv_full[t % kStages], (t / kStages) & 1, &dummy, gstatus,
+                LCATTN_ERR_DEVICE_TIMEOUT);
+    }
+    for (int s = 0; s < hpc; ++s) {
+      int dummy = 0;
+      mbar_wait(&sm.q_full[s], 0, &dummy, gstatus, LCATTN_ERR_DEVICE_TIMEOUT);
     }
     } else if (warp == 9) {
     // ---------------------------------------------------------------- MMA issuer
-    if (lane == 0) {
+    // The whole warp runs the loop; every tcgen05.mma / commit is issued by one
+    // elected lane (see the elected-lane forms in the primitives header).
+    {
       const uint32_t idesc_qk = idesc_bf16_f32(128, 128, false, false);
       const uint32_t idesc_pv = idesc_bf16_f32(128, 128, false, true);
       // Base descriptors; stage s of the ring is kTileBytes further on.
@@ -226,7 +232,8 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
       const uint64_t dv0 = sdesc_sw128(smem_u32(sm.kv[0]), kHalfBytes, 1024);  // V tile, MN-major
       bool ok = true;
       for (int s = 0; s < hpc && ok; ++s)
-        ok = mbar_wait(&sm.q_full[s], 0, abort_flag, gstatus, LCATTN_ERR_DEVICE_TIMEOUT);
+        ok = __all_sync(0xffffffffu, mbar_wait(&sm.q_full[s], 0, abort_flag, gstatus,
+                                               LCATTN_ERR_DEVICE_TIMEOUT));
       for (int j = 0; ok && j <= n; ++j) {
         const int tk = 2 * j, tv = 2 * j - 1;
         if (j < n)
@@ -235,42 +242,42 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
         if (ok && j > 0)
           ok = mbar_wait(&sm.kv_full[tv % kStages], (tv / kStages) & 1, abort_flag, gstatus,
                          LCATTN_ERR_DEVICE_TIMEOUT);
-        if (!ok) break;
+        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
         tc_fence_after();
         const uint64_t kb = sdesc_add(dk0, (tk % kStages) * kTileBytes);
         const uint64_t vb = sdesc_add(dv0, ((tv + kStages) % kStages) * kTileBytes);
         for (int s = 0; s < hpc; ++s) {
           const uint32_t tS = tmem + s * 128, tO = tmem + 256 + s * 128;
           if (j > 0) {
-            if (!(ok = mbar_wait(&sm.p_full[s], (j - 1) & 1, abort_flag, gstatus,
-                                 LCATTN_ERR_DEVICE_TIMEOUT)))
-              break;
+            ok = mbar_wait(&sm.p_full[s], (j - 1) & 1, abort_flag, gstatus,
+                           LCATTN_ERR_DEVICE_TIMEOUT);
+            if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
             tc_fence_after();
             // O += P V: A = P (bf16 pairs in TMEM), B = V read MN-major.
-            mma_ts(tO, tS, vb, idesc_pv, j > 1 ? 1u : 0u);
+            mma_ts_er(tO, tS, vb, idesc_pv, j > 1 ? 1u : 0u);
             #pragma unroll
-            for (int kk = 1; kk < 8; ++kk) mma_ts_c<1>(tO, tS + kk * 8, sdesc_add(vb, kk * 2048), idesc_pv);
-            tc_commit(&sm.o_full[s]);
+            for (int kk = 1; kk < 8; ++kk) mma_ts_e<1>(tO, tS + kk * 8, sdesc_add(vb, kk * 2048), idesc_pv);
+            tc_commit_e(&sm.o_full[s]);
           }
           if (j < n) {
             // S = Q K^T, both K-major.
             const uint64_t qd = s ? dq1 : dq0;
-            mma_ss_c<0>(tS, qd, kb, idesc_qk);
+            mma_ss_e<0>(tS, qd, kb, idesc_qk);
             #pragma unroll
             for (int kk = 1; kk < 8; ++kk) {
               constexpr uint32_t kHalf = kHalfBytes;
               const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
-              mma_ss_c<1>(tS, sdesc_add(qd, off), sdesc_add(kb, off), idesc_qk);
+              mma_ss_e<1>(tS, sdesc_add(qd, off), sdesc_add(kb, off), idesc_qk);
             }
-            tc_commit(&sm.s_full[s]);
+            tc_commit_e(&sm.s_full[s]);
           }
         }
         if (!ok) break;
-        if (j < n) tc_commit(&sm.kv_empty[tk % kStages]);
-        if (j > 0) tc_commit(&sm.kv_empty[tv % kStages]);
+        if (j < n) tc_commit_e(&sm.kv_empty[tk % kStages]);
+        if (j > 0) tc_commit_e(&sm.kv_empty[tv % kStages]);
       }
       // Drain: every MMA issued above has completed once this barrier flips.
-      tc_commit(&sm.drain);
+      tc_commit_e(&sm.drain);
       int dummy = 0;
       mbar_wait(&sm.drain, 0, &dummy, gstatus, LCATTN_ERR_DEVICE_TIMEOUT);
     }
