@@ -207,6 +207,16 @@ int lcattn_bwd_noalloc(const lcattn_shape* shape, const void* q, const void* k, 
  * `tile_meta` (LCATTN_ERR_DEVICE_*), or LCATTN_OK.  Clears nothing.          */
 int lcattn_read_status(const void* tile_meta, lcattn_stream_t stream);
 
+/* Diagnostic: launches one CTA whose bounded device wait, on a barrier that
+ * nothing completes, expires after about two seconds.  The kernel then records
+ * LCATTN_ERR_DEVICE_TIMEOUT in the status words of `tile_meta` (device, any
+ * buffer from lcattn_mask_compile) and returns, as every kernel of the library
+ * does when one of its waits expires; the context stays usable.  Lets a caller
+ * (or a test) exercise that path without faulting or hanging the GPU.  The
+ * status words are only written, not cleared: clear them afterwards with
+ * lcattn_clear_status.                                                      */
+int lcattn_selftest_wait_timeout(void* tile_meta, lcattn_stream_t stream);
+
 /* Zeroes the device status words of `tile_meta` (asynchronously). */
 int lcattn_clear_status(void* tile_meta, lcattn_stream_t stream);
 

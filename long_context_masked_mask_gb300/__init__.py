@@ -50,7 +50,7 @@ BLOCK_M = BLOCK_N = 128
 EXPORTED = (
     "lcattn_tile_meta_layout_of", "lcattn_tile_meta_size", "lcattn_mask_compile", "lcattn_fwd",
     "lcattn_bwd_workspace_size", "lcattn_bwd", "lcattn_bwd_stage", "lcattn_read_status", "lcattn_clear_status",
-    "lcattn_status_string", "lcattn_version", "lcattn_bwd_noalloc",
+    "lcattn_status_string", "lcattn_version", "lcattn_bwd_noalloc", "lcattn_selftest_wait_timeout",
 )
 
 
@@ -101,6 +101,7 @@ def _load():
         "lcattn_bwd_noalloc": (ctypes.c_int, [S, P, P, P, P, P, P, P, M, ctypes.c_float, P, P, P, P]),
         "lcattn_read_status": (ctypes.c_int, [P, P]),
         "lcattn_clear_status": (ctypes.c_int, [P, P]),
+        "lcattn_selftest_wait_timeout": (ctypes.c_int, [P, P]),
         "lcattn_status_string": (ctypes.c_char_p, [ctypes.c_int]),
         "lcattn_version": (ctypes.c_int, []),
     }
@@ -284,6 +285,13 @@ def lcattn_bwd_noalloc(q, k, v, o, d_o, lse, mask: DeviceMask, tile_meta, scale:
 def lcattn_read_status(tile_meta: torch.Tensor, stream=None) -> int:
     """Synchronises the stream and returns the first nonzero device status word."""
     return int(_lib.lcattn_read_status(tile_meta.data_ptr(), _stream_ptr(stream)))
+
+
+def lcattn_selftest_wait_timeout(tile_meta: torch.Tensor, stream=None) -> None:
+    """Launches the diagnostic kernel whose bounded wait expires (~2 s) and
+    records LCATTN_ERR_DEVICE_TIMEOUT in `tile_meta`'s status words."""
+    _check(_lib.lcattn_selftest_wait_timeout(tile_meta.data_ptr(), _stream_ptr(stream)),
+           "lcattn_selftest_wait_timeout")
 
 
 def lcattn_clear_status(tile_meta: torch.Tensor, stream=None) -> None:

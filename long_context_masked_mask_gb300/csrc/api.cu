@@ -332,6 +332,12 @@ int lcattn_read_status(const void* tile_meta, lcattn_stream_t stream) {
   return LCATTN_OK;
 }
 
+int lcattn_selftest_wait_timeout(void* tile_meta, lcattn_stream_t stream) {
+  if (!tile_meta || !aligned16(tile_meta)) return LCATTN_ERR_INVALID_ARG;
+  return cuda_status(launch_selftest_wait_timeout(static_cast<int32_t*>(tile_meta),
+                                                  reinterpret_cast<cudaStream_t>(stream)));
+}
+
 int lcattn_clear_status(void* tile_meta, lcattn_stream_t stream) {
   if (!tile_meta) return LCATTN_ERR_INVALID_ARG;
   return cuda_status(cudaMemsetAsync(tile_meta, 0, 16, reinterpret_cast<cudaStream_t>(stream)));

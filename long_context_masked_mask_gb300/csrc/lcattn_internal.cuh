@@ -80,5 +80,6 @@ cudaError_t launch_bwd_prepass(const BwdArgs& a, cudaStream_t st);
 cudaError_t launch_bwd_dkdv(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             const CUtensorMap& tdo, const BwdArgs& a, cudaStream_t st);
 cudaError_t launch_bwd_dq_convert(const BwdArgs& a, cudaStream_t st);
+cudaError_t launch_selftest_wait_timeout(int32_t* status, cudaStream_t st);
 
 }  // namespace lcattn

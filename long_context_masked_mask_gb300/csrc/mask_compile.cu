@@ -37,10 +37,9 @@ __global__ void validate_offsets_kernel(MaskDev m, int Sq, int Sk, int32_t* stat
   if (!ok) atomicCAS(status, 0, LCATTN_ERR_DEVICE_MASK);
 }
 
-// One warp per tile.  Column bounds: count the allowed rows of each column
+// Column bounds, one warp per tile: count the allowed rows of each column
 // inside the tile's row range (union of the two intervals) and compare the sum
-// with the tile's in-range area.  Block map: look at every (query block, key
-// block) pair that overlaps the tile.
+// with the tile's in-range area.
 __global__ void classify_kernel(ProblemDev pr, MaskDev m, TileMetaDev t) {
   const int lane = threadIdx.x & 31;
   const int64_t warps_total = (int64_t)gridDim.x * (blockDim.x >> 5);
@@ -53,39 +52,82 @@ __global__ void classify_kernel(ProblemDev pr, MaskDev m, TileMetaDev t) {
     const int b = (int)(w / ((int64_t)t.nKt * t.nQt * t.nH));
     const int r0 = qt * kBM, r1 = min(pr.Sq, r0 + kBM);
     const int c0 = kt * kBN, c1 = min(pr.Sk, c0 + kBN);
-    uint8_t cls;
-    if (m.kind == LCATTN_MASK_COLBOUNDS) {
-      int cnt = 0;
-      const int4* cb = m.col_bounds + (int64_t)b * pr.Sk;
-      for (int j = c0 + lane; j < c1; j += 32) {
-        const int4 v = __ldg(cb + j);
-        cnt += ilen(v.x, v.y, r0, r1) + ilen(v.z, v.w, r0, r1) -
-               ilen(max(v.x, v.z), min(v.y, v.w), r0, r1);
-      }
-      #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
-      const int area = (r1 - r0) * (c1 - c0);
-      cls = cnt == 0 ? LCATTN_TILE_EMPTY : (cnt == area ? LCATTN_TILE_FULL : LCATTN_TILE_PARTIAL);
-    } else {
-      const int qb0 = block_of(m.q_offs, m.nQb, r0), qb1 = block_of(m.q_offs, m.nQb, r1 - 1);
-      const int kb0 = block_of(m.k_offs, m.nKb, c0), kb1 = block_of(m.k_offs, m.nKb, c1 - 1);
-      const int nk = kb1 - kb0 + 1;
-      const int64_t npairs = (int64_t)(qb1 - qb0 + 1) * nk;
-      const uint8_t* map = m.block_map + (((int64_t)b * pr.Hq + h) * m.nQb) * m.nKb;
-      bool any_keep = false, any_drop = false;
-      for (int64_t p = lane; p < npairs; p += 32) {
-        const int qb = qb0 + (int)(p / nk), kb = kb0 + (int)(p % nk);
-        const int qlen = min(__ldg(m.q_offs + qb + 1), r1) - max(__ldg(m.q_offs + qb), r0);
-        const int klen = min(__ldg(m.k_offs + kb + 1), c1) - max(__ldg(m.k_offs + kb), c0);
-        if (qlen <= 0 || klen <= 0) continue;
-        if (__ldg(map + (int64_t)qb * m.nKb + kb)) any_keep = true; else any_drop = true;
-      }
-      any_keep = __any_sync(0xffffffffu, any_keep);
-      any_drop = __any_sync(0xffffffffu, any_drop);
-      cls = !any_keep ? LCATTN_TILE_EMPTY : (any_drop ? LCATTN_TILE_PARTIAL : LCATTN_TILE_FULL);
+    int cnt = 0;
+    const int4* cb = m.col_bounds + (int64_t)b * pr.Sk;
+    for (int j = c0 + lane; j < c1; j += 32) {
+      const int4 v = __ldg(cb + j);
+      cnt += ilen(v.x, v.y, r0, r1) + ilen(v.z, v.w, r0, r1) -
+             ilen(max(v.x, v.z), min(v.y, v.w), r0, r1);
     }
+    #pragma unroll
+    for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
+    const int area = (r1 - r0) * (c1 - c0);
+    const uint8_t cls =
+        cnt == 0 ? LCATTN_TILE_EMPTY : (cnt == area ? LCATTN_TILE_FULL : LCATTN_TILE_PARTIAL);
     if (lane == 0) t.cls[w] = cls;
   }
+}
+
+// Block maps: one warp per row of tiles (batch, head, query tile); lanes take
+// key tiles.  The query-block range is found once per row; each lane looks up
+// its tile's key-block range and scans the covered (query block, key block)
+// pairs.
+__global__ void classify_blockmap_kernel(ProblemDev pr, MaskDev m, TileMetaDev t) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warps_total = (int64_t)gridDim.x * (blockDim.x >> 5);
+  const int64_t rows = (int64_t)t.B * t.nH * t.nQt;
+  for (int64_t w = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); w < rows;
+       w += warps_total) {
+    const int qt = (int)(w % t.nQt);
+    const int h = (int)((w / t.nQt) % t.nH);
+    const int b = (int)(w / ((int64_t)t.nQt * t.nH));
+    const int r0 = qt * kBM, r1 = min(pr.Sq, r0 + kBM);
+    const int qb0 = block_of(m.q_offs, m.nQb, r0), qb1 = block_of(m.q_offs, m.nQb, r1 - 1);
+    const uint8_t* map = m.block_map + (((int64_t)b * pr.Hq + h) * m.nQb) * m.nKb;
+    uint8_t* out = t.cls + w * t.nKt;
+    for (int kt = lane; kt < t.nKt; kt += 32) {
+      const int c0 = kt * kBN, c1 = min(pr.Sk, c0 + kBN);
+      const int kb0 = block_of(m.k_offs, m.nKb, c0), kb1 = block_of(m.k_offs, m.nKb, c1 - 1);
+      bool any_keep = false, any_drop = false;
+      for (int qb = qb0; qb <= qb1; ++qb) {
+        const int qlen = min(__ldg(m.q_offs + qb + 1), r1) - max(__ldg(m.q_offs + qb), r0);
+        if (qlen <= 0) continue;
+        for (int kb = kb0; kb <= kb1; ++kb) {
+          const int klen = min(__ldg(m.k_offs + kb + 1), c1) - max(__ldg(m.k_offs + kb), c0);
+          if (klen <= 0) continue;
+          if (__ldg(map + (int64_t)qb * m.nKb + kb)) any_keep = true; else any_drop = true;
+        }
+      }
+      out[kt] = !any_keep ? LCATTN_TILE_EMPTY : (any_drop ? LCATTN_TILE_PARTIAL : LCATTN_TILE_FULL);
+    }
+  }
+}
+
+// Backward lists (fixed key tile) through a 32 x 32 shared-memory transpose of
+// the class bytes: the block reads 32 query-tile rows x 32 key tiles at a time
+// (row-contiguous), and warp c compacts key tile kt0 + c over those rows.
+__global__ void __launch_bounds__(1024) bwd_list_kernel(TileMetaDev t) {
+  __shared__ uint8_t tile[32][33];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nChunks = (t.nKt + 31) / 32;
+  const int64_t bh = blockIdx.x / nChunks;
+  const int kt0 = (int)(blockIdx.x % nChunks) * 32;
+  const uint8_t* cls = t.cls + bh * t.nQt * t.nKt;
+  const int kt = kt0 + warp;
+  int32_t* lst = t.bwd_lst + (bh * t.nKt + kt) * t.nQt;
+  int n = 0;
+  for (int qt0 = 0; qt0 < t.nQt; qt0 += 32) {
+    const int qr = qt0 + warp, kc = kt0 + lane;
+    tile[warp][lane] = (qr < t.nQt && kc < t.nKt) ? cls[(int64_t)qr * t.nKt + kc] : (uint8_t)LCATTN_TILE_EMPTY;
+    __syncthreads();
+    const uint8_t c = tile[lane][warp];  // row qt0 + lane, key tile kt
+    const unsigned bal = __ballot_sync(0xffffffffu, c != LCATTN_TILE_EMPTY);
+    if (kt < t.nKt && c != LCATTN_TILE_EMPTY)
+      lst[n + __popc(bal & ((1u << lane) - 1u))] = ((qt0 + lane) << 1) | (c == LCATTN_TILE_PARTIAL ? 1 : 0);
+    n += __popc(bal);
+    __syncthreads();
+  }
+  if (lane == 0 && kt < t.nKt) t.bwd_cnt[bh * t.nKt + kt] = n;
 }
 
 // One warp per row of tiles (forward: fixed query tile) or column of tiles
@@ -158,13 +200,20 @@ cudaError_t launch_mask_compile(const ProblemDev& pr, const MaskDev& m, const Ti
   int64_t blocks = (tiles + 7) / 8;
   const int64_t cap = (int64_t)nsm * 16;
   if (blocks > cap) blocks = cap;
-  classify_kernel<<<(unsigned)blocks, threads, 0, st>>>(pr, m, t);
+  if (m.kind == LCATTN_MASK_BLOCKMAP) {
+    const int64_t rows = (int64_t)t.B * t.nH * t.nQt;
+    int64_t rblocks = (rows + 7) / 8;
+    if (rblocks > cap) rblocks = cap;
+    classify_blockmap_kernel<<<(unsigned)rblocks, threads, 0, st>>>(pr, m, t);
+  } else {
+    classify_kernel<<<(unsigned)blocks, threads, 0, st>>>(pr, m, t);
+  }
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   int64_t rows = (int64_t)t.B * t.nH * t.nQt;
   list_kernel<true><<<(unsigned)((rows + 7) / 8), threads, 0, st>>>(t);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  int64_t cols = (int64_t)t.B * t.nH * t.nKt;
-  list_kernel<false><<<(unsigned)((cols + 7) / 8), threads, 0, st>>>(t);
+  const int64_t col_blocks = (int64_t)t.B * t.nH * ((t.nKt + 31) / 32);
+  bwd_list_kernel<<<(unsigned)col_blocks, 1024, 0, st>>>(t);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   const unsigned nbh = (unsigned)(t.B * t.nH);
   order_kernel<true><<<nbh, 1024, t.nQt * sizeof(int32_t), st>>>(t);
