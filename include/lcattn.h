@@ -108,6 +108,8 @@ typedef struct lcattn_mask_desc {
  * skip masked-out work; here the skip decision is made once per 128x128 tile).
  * Layout of the buffer (all offsets from lcattn_tile_meta_layout):
  *   status  int32[4]                     device status words (0 = OK)
+ *   sched   uint64[2]                    forward work counter and finished-CTA
+ *                                        count (zero between calls; see lcattn_fwd)
  *   class   uint8 [B][nH][nQt][nKt]      LCATTN_TILE_* per tile
  *   fwd_cnt int32 [B][nH][nQt]           non-empty key tiles per query tile
  *   fwd_lst int32 [B][nH][nQt][nKt]      (kt << 1) | partial, kt increasing
@@ -119,7 +121,7 @@ typedef struct lcattn_mask_desc {
  * nH = Hq for block maps.                                                    */
 typedef struct lcattn_tile_meta_layout {
   int64_t nQt, nKt, nH, B;
-  int64_t off_status, off_class, off_fwd_cnt, off_fwd_lst, off_fwd_ord;
+  int64_t off_status, off_sched, off_class, off_fwd_cnt, off_fwd_lst, off_fwd_ord;
   int64_t off_bwd_cnt, off_bwd_lst, off_bwd_ord;
   int64_t total_bytes;
 } lcattn_tile_meta_layout;
@@ -144,7 +146,13 @@ int lcattn_mask_compile(const lcattn_shape* shape, const lcattn_mask_desc* mask,
  * o [B][Sq][Hq][128] bf16 and lse [B][Hq][Sq] fp32 (natural log; -inf for a
  * row with no allowed key, whose O row is 0).  `tile_meta` must come from
  * lcattn_mask_compile with the same shape sizes and descriptor, and `mask`
- * is needed again because partial tiles evaluate the mask per element.     */
+ * is needed again because partial tiles evaluate the mask per element.
+ * The kernel is persistent: its CTAs take query tiles, longest list first,
+ * from a work counter in the scheduler words of `tile_meta`, and the last CTA
+ * to run out of work puts the counter back to zero.  So forward calls that
+ * share one `tile_meta` must not overlap in time (issue them on one stream);
+ * after a DEVICE_TIMEOUT status, lcattn_clear_status also resets the counter.
+ * The forward only reads the rest of `tile_meta`.                           */
 int lcattn_fwd(const lcattn_shape* shape, const void* q, const void* k, const void* v,
                const void* tile_meta, const lcattn_mask_desc* mask, float scale, void* o,
                float* lse, lcattn_stream_t stream);

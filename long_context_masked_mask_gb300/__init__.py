@@ -69,7 +69,7 @@ class lcattn_mask_desc(ctypes.Structure):
 
 class lcattn_tile_meta_layout(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int64) for n in (
-        "nQt", "nKt", "nH", "B", "off_status", "off_class", "off_fwd_cnt", "off_fwd_lst",
+        "nQt", "nKt", "nH", "B", "off_status", "off_sched", "off_class", "off_fwd_cnt", "off_fwd_lst",
         "off_fwd_ord", "off_bwd_cnt", "off_bwd_lst", "off_bwd_ord", "total_bytes")]
 
 

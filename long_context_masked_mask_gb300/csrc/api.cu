@@ -62,7 +62,8 @@ int layout_of(const lcattn_shape* s, const lcattn_mask_desc* m, lcattn_tile_meta
   L->nH = m->kind == LCATTN_MASK_BLOCKMAP ? s->Hq : 1;
   const int64_t bh = L->B * L->nH;
   int64_t off = 0;
-  L->off_status = off; off = align_up(off + 16, 256);
+  L->off_status = off;
+  L->off_sched = off + 16; off = align_up(off + 32, 256);
   L->off_class = off;   off = align_up(off + bh * L->nQt * L->nKt, 256);
   L->off_fwd_cnt = off; off = align_up(off + 4 * bh * L->nQt, 256);
   L->off_fwd_lst = off; off = align_up(off + 4 * bh * L->nQt * L->nKt, 256);
@@ -97,6 +98,7 @@ TileMetaDev meta_of(const lcattn_tile_meta_layout& L, const void* base) {
   uint8_t* p = static_cast<uint8_t*>(const_cast<void*>(base));
   TileMetaDev t;
   t.status = reinterpret_cast<int32_t*>(p + L.off_status);
+  t.sched = reinterpret_cast<unsigned long long*>(p + L.off_sched);
   t.cls = p + L.off_class;
   t.fwd_cnt = reinterpret_cast<int32_t*>(p + L.off_fwd_cnt);
   t.fwd_lst = reinterpret_cast<int32_t*>(p + L.off_fwd_lst);
@@ -340,7 +342,8 @@ int lcattn_selftest_wait_timeout(void* tile_meta, lcattn_stream_t stream) {
 
 int lcattn_clear_status(void* tile_meta, lcattn_stream_t stream) {
   if (!tile_meta) return LCATTN_ERR_INVALID_ARG;
-  return cuda_status(cudaMemsetAsync(tile_meta, 0, 16, reinterpret_cast<cudaStream_t>(stream)));
+  // Status words and the scheduler words behind them (offsets 0 and 16 for every layout).
+  return cuda_status(cudaMemsetAsync(tile_meta, 0, 32, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 const char* lcattn_status_string(int status) {

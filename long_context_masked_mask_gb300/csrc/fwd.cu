@@ -5,19 +5,22 @@
 // pages ("Long-Context Attention Benchmark", xllm-io blog review, sections
 // "密集注意力内核" and "密集内核性能": bf16, head dim 128, GQA 64:8 and MHA 64:64).
 //
-// One CTA owns up to two 128-row query tiles ("slots") that share one list of
-// key tiles: two query heads of the same GQA group (the mask is head
-// independent for column bounds), or a single tile otherwise.  Roles:
+// Persistent: one CTA per SM walks a sequence of work items.  An item is up to
+// two 128-row query tiles ("slots") that share one list of key tiles: two query
+// heads of the same GQA group (the mask is head independent for column
+// bounds), or a single tile otherwise.  Roles:
 //   warps 0-3  softmax for slot 0 (thread = query row = TMEM lane)
 //   warps 4-7  softmax for slot 1
-//   warp  8    TMA producer: Q tiles once, then K_j, V_j into a 4-deep ring
+//   warp  8    TMA producer: per item its Q tiles, then K_j, V_j into a 4-deep
+//              ring that runs on across items
 //   warp  9    TMEM owner and single-thread tcgen05.mma issuer
 //   warps 10-11 idle (they complete the third warpgroup for setmaxnreg)
 // TMEM (512 columns): S0 | S1 | O0 | O1, 128 fp32 columns each.  The softmax
 // writes P (bf16 pairs) over the first 64 columns of its S, and the PV product
 // reads P from TMEM (A operand) and V from shared memory (B operand).
 // Issue order per key tile j: PV0(j-1), S0(j), PV1(j-1), S1(j), so each slot's
-// softmax overlaps the other slot's two GEMMs.
+// softmax overlaps the other slot's two GEMMs; the order runs on across items,
+// so an item's tail (last PV, epilogue) overlaps the next item's first GEMMs.
 // The running max is kept in the log2 domain and only moved when a row max grows
 // by more than 8 (a factor 256 of headroom in fp32 / bf16), so O is rescaled in
 // TMEM rarely; the final O is divided by the row sum in the epilogue.
@@ -32,13 +35,14 @@ namespace {
 using namespace dev;
 
 constexpr int kStages = 4;          // K/V ring depth (K and V tiles alternate)
+constexpr int kItemQ = 4;           // depth of the work-item queue (producer -> other roles)
 constexpr int kTileBytes = 32768;   // 128 rows x 128 bf16
 constexpr int kHalfBytes = 16384;   // one 64-column TMA box
 constexpr int kThreads = 384;        // 3 warpgroups
-// Register split (launch: 384 threads x 168): softmax warpgroups 224 each,
-// producer/MMA warpgroup 56.  128 * (224 + 224 + 56) = 384 * 168.
-constexpr int kRegsSoftmax = 224;
-constexpr int kRegsOther = 56;
+// Register split (launch: 384 threads x 168): softmax warpgroups 216 each,
+// producer/MMA warpgroup 72.  128 * (216 + 216 + 72) = 384 * 168.
+constexpr int kRegsSoftmax = 216;
+constexpr int kRegsOther = 72;
 static_assert(128 * (2 * kRegsSoftmax + kRegsOther) <= kThreads * 168, "register split");
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
@@ -48,12 +52,16 @@ struct FwdSmem {
   int4 bnd[2][2][kBN];  // column bounds of a partial tile, per slot, double-buffered
   uint64_t bnd_ready[2][2];
   uint64_t q_full[2];
+  uint64_t q_empty[2];
   uint64_t kv_full[kStages];
   uint64_t kv_empty[kStages];
   uint64_t s_full[2];
   uint64_t p_full[2];
   uint64_t o_full[2];
   uint64_t drain;
+  int items[kItemQ];           // item indices handed from the producer to the other roles
+  uint64_t item_full[kItemQ];
+  uint64_t item_empty[kItemQ];
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -61,6 +69,7 @@ struct FwdSmem {
 struct FwdKernelArgs {
   FwdArgs a;
   int heads_per_cta;
+  int total_items;
 };
 
 // Bits [lo, hi) of a 128-bit row mask that fall into the 32-bit word starting at `base`.
@@ -130,6 +139,37 @@ __device__ __forceinline__ void tile_mask_bits(const MaskDev& m, const ProblemDe
   }
 }
 
+// ---- persistent schedule ----------------------------------------------------
+// An item is one query tile for `heads_per_cta` query heads.  Items are ordered
+// rank-major: rank r is the r-th longest key-tile list of its (batch, head)
+// list (the mask compiler's LPT order), so item costs fall along the sequence.
+// CTAs take items greedily from a device-wide counter (longest-processing-time
+// first): the producer warp fetches an index one item ahead (so it can warm L2
+// with that item's query rows) and hands the indices to the MMA and softmax
+// warps through a small queue in shared memory; -1 ends the sequence.
+
+struct FwdItem {
+  int b, h0, qt, n;
+  const int32_t* list;
+};
+
+// idx < total_items < 2^31 (the launcher checks), so 32-bit arithmetic suffices.
+__device__ __forceinline__ FwdItem fwd_item(const FwdArgs& a, int hpc, int idx) {
+  const int groups = a.pr.Hq / hpc;
+  const int per_rank = groups * a.pr.B;
+  const int rank = idx / per_rank;
+  const int rem = idx - rank * per_rank;
+  FwdItem it;
+  it.b = rem / groups;
+  it.h0 = (rem - it.b * groups) * hpc;
+  const int lh = a.meta.nH == 1 ? 0 : it.h0;
+  const int64_t lbase = ((int64_t)it.b * a.meta.nH + lh) * a.meta.nQt;
+  it.qt = __ldg(a.meta.fwd_ord + lbase + rank);
+  it.n = __ldg(a.meta.fwd_cnt + lbase + it.qt);
+  it.list = a.meta.fwd_lst + (lbase + it.qt) * a.meta.nKt;
+  return it;
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
 fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
            const __grid_constant__ CUtensorMap tmV, const __grid_constant__ FwdKernelArgs ka) {
@@ -140,22 +180,13 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
   const ProblemDev& pr = a.pr;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int hpc = ka.heads_per_cta;
-
-  // ---- work item -----------------------------------------------------------
-  const int b = blockIdx.z;
-  const int rank = blockIdx.y;
-  const int h0 = blockIdx.x * hpc;
-  const int lh = a.meta.nH == 1 ? 0 : h0;
-  const int64_t lbase = ((int64_t)b * a.meta.nH + lh) * a.meta.nQt;
-  const int qt = __ldg(a.meta.fwd_ord + lbase + rank);
-  const int n = __ldg(a.meta.fwd_cnt + lbase + qt);
-  const int32_t* list = a.meta.fwd_lst + (lbase + qt) * a.meta.nKt;
-  const int g = h0 / pr.G;
+  const int total = ka.total_items;
   int32_t* gstatus = a.meta.status;
 
   if (tid == 0) {
     for (int s = 0; s < 2; ++s) {
       mbar_init(&sm.q_full[s], 1);
+      mbar_init(&sm.q_empty[s], 1);
       mbar_init(&sm.s_full[s], 1);
       mbar_init(&sm.p_full[s], 128);
       mbar_init(&sm.o_full[s], 1);
@@ -167,6 +198,10 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
     mbar_init(&sm.drain, 1);
     for (int s = 0; s < 2; ++s)
       for (int u = 0; u < 2; ++u) mbar_init(&sm.bnd_ready[s][u], 128);
+    for (int e = 0; e < kItemQ; ++e) {
+      mbar_init(&sm.item_full[e], 1);
+      mbar_init(&sm.item_empty[e], 1 + 4 * hpc);  // the MMA warp and every active softmax warp
+    }
     sm.abort_flag = 0;
     fence_barrier_init();
   }
@@ -181,47 +216,123 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
     if (warp == 8) {
     // ---------------------------------------------------------------- producer
     // The whole warp runs the loop (waits included); the elected lane issues.
+    // Ring entry t (counted across items) holds K of tile t/2 for even t and V
+    // of tile t/2 for odd t.  An item's Q tiles go in after its first K tile,
+    // once the previous item's last S GEMM of that slot has released them.
     if (lane == 0) {
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
     }
     __syncwarp();
-    for (int s = 0; s < hpc; ++s) {
-      mbar_expect_tx_e(&sm.q_full[s], kTileBytes);
-      tma_load_4d_e(sm.q[s], &tmQ, &sm.q_full[s], 0, h0 + s, qt * kBM, b);
-      tma_load_4d_e(sm.q[s] + kHalfBytes, &tmQ, &sm.q_full[s], 64, h0 + s, qt * kBM, b);
-    }
-    int issued = 0;
-    for (int t = 0; t < 2 * n; ++t) {
-      const int stage = t % kStages, use = t / kStages;
-      if (use > 0) {
-        const bool okw = mbar_wait(&sm.kv_empty[stage], (use - 1) & 1, abort_flag, gstatus,
-                                   LCATTN_ERR_DEVICE_TIMEOUT);
-        if (!__all_sync(0xffffffffu, okw)) break;
+    int t = 0, nq = 0;       // ring entries issued; items whose Q tiles were issued
+    int q_issued[2] = {0, 0};  // Q loads issued per slot
+    bool ok = true;
+    unsigned long long* sched = a.meta.sched;
+    // Next item index from the device-wide counter, or -1.  The CTA that
+    // fetches the last "-1" of the launch puts the counters back to zero (no
+    // CTA touches them afterwards), ready for the next call.
+    auto fetch = [&]() -> int {
+      unsigned long long v = 0ull;
+      if (lane == 0) {
+        v = atomicAdd(&sched[0], 1ull);
+        if (v >= static_cast<unsigned long long>(total)) {
+          __threadfence();
+          if (atomicAdd(&sched[1], 1ull) == gridDim.x - 1ull) {
+            atomicExch(&sched[0], 0ull);
+            atomicExch(&sched[1], 0ull);
+          }
+        }
       }
-      const int kt = __ldg(list + (t >> 1)) >> 1;
-      const CUtensorMap* tm = (t & 1) ? &tmV : &tmK;
-      mbar_expect_tx_e(&sm.kv_full[stage], kTileBytes);
-      tma_load_4d_e(sm.kv[stage], tm, &sm.kv_full[stage], 0, g, kt * kBN, b);
-      tma_load_4d_e(sm.kv[stage] + kHalfBytes, tm, &sm.kv_full[stage], 64, g, kt * kBN, b);
-      issued = t + 1;
+      v = __shfl_sync(0xffffffffu, v, 0);
+      return v < static_cast<unsigned long long>(total) ? static_cast<int>(v) : -1;
+    };
+    int published = 0;
+    auto publish = [&](int idx) -> bool {
+      const int e = published % kItemQ;
+      if (published >= kItemQ) {
+        const bool okw = mbar_wait(&sm.item_empty[e], ((published / kItemQ) - 1) & 1, abort_flag,
+                                   gstatus, LCATTN_ERR_DEVICE_TIMEOUT);
+        if (!__all_sync(0xffffffffu, okw)) return false;
+      }
+      if (lane == 0) {
+        sm.items[e] = idx;
+        mbar_arrive(&sm.item_full[e]);  // release: the index is visible to whoever sees the phase
+      }
+      __syncwarp();
+      ++published;
+      return true;
+    };
+    int cur = fetch();
+    while (ok) {
+      if (!publish(cur)) { ok = false; break; }
+      if (cur < 0) break;
+      const int nxt = fetch();
+      const FwdItem it = fwd_item(a, hpc, cur);
+      cur = nxt;
+      if (nxt >= 0) {
+        // Warm L2 with the next item's query rows while this item runs.
+        const FwdItem nx = fwd_item(a, hpc, nxt);
+        if (nx.n > 0)
+          for (int s = 0; s < hpc; ++s) {
+            tma_prefetch_l2_4d_e(&tmQ, 0, nx.h0 + s, nx.qt * kBM, nx.b);
+            tma_prefetch_l2_4d_e(&tmQ, 64, nx.h0 + s, nx.qt * kBM, nx.b);
+          }
+      }
+      if (it.n == 0) continue;
+      const int g = it.h0 / pr.G;
+      for (int u = 0; u < 2 * it.n; ++u, ++t) {
+        const int stage = t % kStages, use = t / kStages;
+        if (use > 0) {
+          ok = mbar_wait(&sm.kv_empty[stage], (use - 1) & 1, abort_flag, gstatus,
+                         LCATTN_ERR_DEVICE_TIMEOUT);
+          if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+        }
+        const int kt = __ldg(it.list + (u >> 1)) >> 1;
+        const CUtensorMap* tm = (u & 1) ? &tmV : &tmK;
+        mbar_expect_tx_e(&sm.kv_full[stage], kTileBytes);
+        tma_load_4d_e(sm.kv[stage], tm, &sm.kv_full[stage], 0, g, kt * kBN, it.b);
+        tma_load_4d_e(sm.kv[stage] + kHalfBytes, tm, &sm.kv_full[stage], 64, g, kt * kBN, it.b);
+        if (u == 0) {
+          for (int s = 0; s < hpc && ok; ++s) {
+            if (nq > 0) {
+              ok = mbar_wait(&sm.q_empty[s], (nq - 1) & 1, abort_flag, gstatus,
+                             LCATTN_ERR_DEVICE_TIMEOUT);
+              if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+            }
+            mbar_expect_tx_e(&sm.q_full[s], kTileBytes);
+            tma_load_4d_e(sm.q[s], &tmQ, &sm.q_full[s], 0, it.h0 + s, it.qt * kBM, it.b);
+            tma_load_4d_e(sm.q[s] + kHalfBytes, &tmQ, &sm.q_full[s], 64, it.h0 + s,
+                          it.qt * kBM, it.b);
+            ++q_issued[s];
+          }
+          if (!ok) { ++t; break; }
+          ++nq;
+        }
+      }
     }
-    // Never leave copies in flight: wait (bounded, ignoring the abort word)
-    // for the last load issued on each stage.
-    for (int t = max(0, issued - kStages); t < issued; ++t) {
+    // Never leave copies in flight: wait (bounded, ignoring the abort word) for
+    // the last load issued on each ring stage and for the last Q tiles.
+    for (int u = max(0, t - kStages); u < t; ++u) {
       int dummy = 0;
-      mbar_wait(&sm.kv_full[t % kStages], (t / kStages) & 1, &dummy, gstatus,
+      mbar_wait(&sm.kv_full[u % kStages], (u / kStages) & 1, &dummy, gstatus,
                 LCATTN_ERR_DEVICE_TIMEOUT);
     }
-    for (int s = 0; s < hpc; ++s) {
+    for (int s = 0; s < 2; ++s) {
+      if (q_issued[s] == 0) continue;
       int dummy = 0;
-      mbar_wait(&sm.q_full[s], 0, &dummy, gstatus, LCATTN_ERR_DEVICE_TIMEOUT);
+      mbar_wait(&sm.q_full[s], (q_issued[s] - 1) & 1, &dummy, gstatus, LCATTN_ERR_DEVICE_TIMEOUT);
     }
     } else if (warp == 9) {
     // ---------------------------------------------------------------- MMA issuer
     // The whole warp runs the loop; every tcgen05.mma / commit is issued by one
     // elected lane (see the elected-lane forms in the primitives header).
+    // The issue stream is flat over this CTA's tiles (T counts them across
+    // items): step T issues PV(T-1) and S(T) per slot, so the first S of an
+    // item follows the previous item's last PV without a gap.  PV(T-1) starts
+    // a fresh accumulation when tile T-1 opened its item; by then the softmax
+    // has read the previous item's O (it does so before releasing the item's
+    // first P).
     {
       const uint32_t idesc_qk = idesc_bf16_f32(128, 128, false, false);
       const uint32_t idesc_pv = idesc_bf16_f32(128, 128, false, true);
@@ -231,36 +342,53 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
       const uint64_t dk0 = sdesc_sw128(smem_u32(sm.kv[0]), 16, 1024);          // K tile, K-major
       const uint64_t dv0 = sdesc_sw128(smem_u32(sm.kv[0]), kHalfBytes, 1024);  // V tile, MN-major
       bool ok = true;
-      for (int s = 0; s < hpc && ok; ++s)
-        ok = __all_sync(0xffffffffu, mbar_wait(&sm.q_full[s], 0, abort_flag, gstatus,
-                                               LCATTN_ERR_DEVICE_TIMEOUT));
-      for (int j = 0; ok && j <= n; ++j) {
-        const int tk = 2 * j, tv = 2 * j - 1;
-        if (j < n)
+      int T = 0, nq = 0;
+      uint32_t pv_acc = 0u;  // accumulate flag of the pending PV(T-1)
+      auto issue_pv = [&](int s) -> bool {
+        const uint32_t tS = tmem + s * 128, tO = tmem + 256 + s * 128;
+        const bool okw = mbar_wait(&sm.p_full[s], (T - 1) & 1, abort_flag, gstatus,
+                                   LCATTN_ERR_DEVICE_TIMEOUT);
+        if (!__all_sync(0xffffffffu, okw)) return false;
+        tc_fence_after();
+        const int tv = 2 * T - 1;
+        const uint64_t vb = sdesc_add(dv0, (tv % kStages) * kTileBytes);
+        // O += P V: A = P (bf16 pairs in TMEM), B = V read MN-major.
+        mma_ts_er(tO, tS, vb, idesc_pv, pv_acc);
+        #pragma unroll
+        for (int kk = 1; kk < 8; ++kk) mma_ts_e<1>(tO, tS + kk * 8, sdesc_add(vb, kk * 2048), idesc_pv);
+        tc_commit_e(&sm.o_full[s]);
+        return true;
+      };
+      for (int k = 0; ok; ++k) {
+        const int e = k % kItemQ;
+        ok = mbar_wait(&sm.item_full[e], (k / kItemQ) & 1, abort_flag, gstatus,
+                       LCATTN_ERR_DEVICE_TIMEOUT);
+        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+        const int idx = sm.items[e];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.item_empty[e]);
+        if (idx < 0) break;
+        const int n = fwd_item(a, hpc, idx).n;
+        if (n == 0) continue;
+        for (int j = 0; j < n; ++j, ++T) {
+          const int tk = 2 * T, tv = 2 * T - 1;
           ok = mbar_wait(&sm.kv_full[tk % kStages], (tk / kStages) & 1, abort_flag, gstatus,
                          LCATTN_ERR_DEVICE_TIMEOUT);
-        if (ok && j > 0)
-          ok = mbar_wait(&sm.kv_full[tv % kStages], (tv / kStages) & 1, abort_flag, gstatus,
-                         LCATTN_ERR_DEVICE_TIMEOUT);
-        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-        tc_fence_after();
-        const uint64_t kb = sdesc_add(dk0, (tk % kStages) * kTileBytes);
-        const uint64_t vb = sdesc_add(dv0, ((tv + kStages) % kStages) * kTileBytes);
-        for (int s = 0; s < hpc; ++s) {
-          const uint32_t tS = tmem + s * 128, tO = tmem + 256 + s * 128;
-          if (j > 0) {
-            ok = mbar_wait(&sm.p_full[s], (j - 1) & 1, abort_flag, gstatus,
+          if (ok && T > 0)
+            ok = mbar_wait(&sm.kv_full[tv % kStages], (tv / kStages) & 1, abort_flag, gstatus,
                            LCATTN_ERR_DEVICE_TIMEOUT);
-            if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-            tc_fence_after();
-            // O += P V: A = P (bf16 pairs in TMEM), B = V read MN-major.
-            mma_ts_er(tO, tS, vb, idesc_pv, j > 1 ? 1u : 0u);
-            #pragma unroll
-            for (int kk = 1; kk < 8; ++kk) mma_ts_e<1>(tO, tS + kk * 8, sdesc_add(vb, kk * 2048), idesc_pv);
-            tc_commit_e(&sm.o_full[s]);
-          }
-          if (j < n) {
+          if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+          tc_fence_after();
+          const uint64_t kb = sdesc_add(dk0, (tk % kStages) * kTileBytes);
+          for (int s = 0; s < hpc; ++s) {
+            if (T > 0 && !issue_pv(s)) { ok = false; break; }
+            if (j == 0) {
+              ok = mbar_wait(&sm.q_full[s], nq & 1, abort_flag, gstatus, LCATTN_ERR_DEVICE_TIMEOUT);
+              if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+              tc_fence_after();
+            }
             // S = Q K^T, both K-major.
+            const uint32_t tS = tmem + s * 128;
             const uint64_t qd = s ? dq1 : dq0;
             mma_ss_e<0>(tS, qd, kb, idesc_qk);
             #pragma unroll
@@ -270,11 +398,26 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
               mma_ss_e<1>(tS, sdesc_add(qd, off), sdesc_add(kb, off), idesc_qk);
             }
             tc_commit_e(&sm.s_full[s]);
+            if (j == n - 1) tc_commit_e(&sm.q_empty[s]);  // Q of this slot is read for good
           }
+          if (!ok) break;
+          tc_commit_e(&sm.kv_empty[tk % kStages]);
+          if (T > 0) tc_commit_e(&sm.kv_empty[tv % kStages]);
+          pv_acc = j > 0 ? 1u : 0u;
         }
-        if (!ok) break;
-        if (j < n) tc_commit_e(&sm.kv_empty[tk % kStages]);
-        if (j > 0) tc_commit_e(&sm.kv_empty[tv % kStages]);
+        if (ok) ++nq;
+      }
+      // The last PV of the sequence.
+      if (ok && T > 0) {
+        const int tv = 2 * T - 1;
+        ok = mbar_wait(&sm.kv_full[tv % kStages], (tv / kStages) & 1, abort_flag, gstatus,
+                       LCATTN_ERR_DEVICE_TIMEOUT);
+        if (__all_sync(0xffffffffu, ok)) {
+          tc_fence_after();
+          for (int s = 0; s < hpc; ++s)
+            if (!issue_pv(s)) break;
+          tc_commit_e(&sm.kv_empty[tv % kStages]);
+        }
       }
       // Drain: every MMA issued above has completed once this barrier flips.
       tc_commit_e(&sm.drain);
@@ -288,160 +431,177 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
     const int s = warp >> 2;
     const int r = tid & 127;  // == 32 * (warp % 4) + lane: this thread's TMEM lane
     if (s < hpc) {
-      const int h = h0 + s;
-      const int row = qt * kBM + r;
       const uint32_t lane_off = static_cast<uint32_t>(32 * (warp & 3)) << 16;
       const uint32_t tS = tmem + lane_off + s * 128;
       const uint32_t tO = tmem + lane_off + 256 + s * 128;
       const float sl2 = a.scale_log2;
       const int last_kt = (pr.Sk - 1) / kBN;
       const bool ragged_k = (pr.Sk % kBN) != 0;
-      int qb_row = 0;
-      if (a.mask.kind == LCATTN_MASK_BLOCKMAP)
-        qb_row = block_of(a.mask.q_offs, a.mask.nQb, min(row, pr.Sq - 1));
-      float m_run = -INFINITY, l_run = 0.f;
       bool ok = true;
+      int T = 0;          // tiles of this CTA processed before the current item
       int n_partial = 0;  // partial column-bounds tiles staged so far (selects the buffer)
-      int e_next = n > 0 ? __ldg(list) : 0;
-      for (int j = 0; j < n; ++j) {
-        const int e = e_next;
-        if (j + 1 < n) e_next = __ldg(list + j + 1);  // prefetch the next entry
-        const int kt = e >> 1;
-        const bool partial = (e & 1) != 0;
-        const bool masked = partial || (ragged_k && kt == last_kt);
-        uint32_t mw[4];
-        if (masked) {
-          const int4* bnd = nullptr;
-          if (partial && a.mask.kind == LCATTN_MASK_COLBOUNDS) {
-            // Stage the tile's 128 column bounds in shared memory: one coalesced
-            // load per thread instead of 128 dependent loads per thread.
-            const int u = n_partial & 1;
-            const int key = kt * kBN + r;
-            sm.bnd[s][u][r] = key < pr.Sk ? __ldg(a.mask.col_bounds + (int64_t)b * pr.Sk + key)
-                                          : make_int4(0, 0, 0, 0);
-            mbar_arrive(&sm.bnd_ready[s][u]);
-            ok = mbar_wait(&sm.bnd_ready[s][u], (n_partial >> 1) & 1, abort_flag, gstatus,
-                           LCATTN_ERR_DEVICE_TIMEOUT);
-            if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-            bnd = sm.bnd[s][u];
-            ++n_partial;
-          }
-          tile_mask_bits(a.mask, pr, b, h, row, qb_row, kt, partial, bnd, mw);
-        }
-        ok = mbar_wait(&sm.s_full[s], j & 1, abort_flag, gstatus, LCATTN_ERR_DEVICE_TIMEOUT);
+      for (int k = 0; ok; ++k) {
+        const int e = k % kItemQ;
+        ok = mbar_wait(&sm.item_full[e], (k / kItemQ) & 1, abort_flag, gstatus,
+                       LCATTN_ERR_DEVICE_TIMEOUT);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-        tc_fence_after();
-        uint32_t xr[128];
-        tmem_ld32(tS + 0, xr + 0);
-        tmem_ld32(tS + 32, xr + 32);
-        tmem_ld32(tS + 64, xr + 64);
-        tmem_ld32(tS + 96, xr + 96);
-        tmem_ld_wait();
-        float x[128];
-        #pragma unroll
-        for (int c = 0; c < 128; ++c) x[c] = __uint_as_float(xr[c]);
-        if (masked) {
-          const uint32_t w0 = mw[0], w1 = mw[1], w2 = mw[2], w3 = mw[3];
-          #pragma unroll
-          for (int c = 0; c < 128; ++c) {
-            const uint32_t w = c < 32 ? w0 : (c < 64 ? w1 : (c < 96 ? w2 : w3));
-            if (!((w >> (c & 31)) & 1u)) x[c] = -INFINITY;
+        const int idx = sm.items[e];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.item_empty[e]);
+        if (idx < 0) break;
+        const FwdItem it = fwd_item(a, hpc, idx);
+        const int n = it.n, b = it.b;
+        const int h = it.h0 + s;
+        const int row = it.qt * kBM + r;
+        int qb_row = 0;
+        if (a.mask.kind == LCATTN_MASK_BLOCKMAP)
+          qb_row = block_of(a.mask.q_offs, a.mask.nQb, min(row, pr.Sq - 1));
+        float m_run = -INFINITY, l_run = 0.f;
+        int e_next = n > 0 ? __ldg(it.list) : 0;
+        for (int j = 0; j < n; ++j) {
+          const int e = e_next;
+          if (j + 1 < n) e_next = __ldg(it.list + j + 1);  // prefetch the next entry
+          const int kt = e >> 1;
+          const bool partial = (e & 1) != 0;
+          const bool masked = partial || (ragged_k && kt == last_kt);
+          uint32_t mw[4];
+          if (masked) {
+            const int4* bnd = nullptr;
+            if (partial && a.mask.kind == LCATTN_MASK_COLBOUNDS) {
+              // Stage the tile's 128 column bounds in shared memory: one coalesced
+              // load per thread instead of 128 dependent loads per thread.
+              const int u = n_partial & 1;
+              const int key = kt * kBN + r;
+              sm.bnd[s][u][r] = key < pr.Sk ? __ldg(a.mask.col_bounds + (int64_t)b * pr.Sk + key)
+                                            : make_int4(0, 0, 0, 0);
+              mbar_arrive(&sm.bnd_ready[s][u]);
+              ok = mbar_wait(&sm.bnd_ready[s][u], (n_partial >> 1) & 1, abort_flag, gstatus,
+                             LCATTN_ERR_DEVICE_TIMEOUT);
+              if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+              bnd = sm.bnd[s][u];
+              ++n_partial;
+            }
+            tile_mask_bits(a.mask, pr, b, h, row, qb_row, kt, partial, bnd, mw);
           }
-        }
-        // Row max as 8 independent chains (a single 128-long chain is latency bound).
-        float m8[8];
-        #pragma unroll
-        for (int c = 0; c < 8; ++c) m8[c] = x[c];
-        #pragma unroll
-        for (int c = 8; c < 128; ++c) m8[c & 7] = fmaxf(m8[c & 7], x[c]);
-        #pragma unroll
-        for (int w = 4; w > 0; w >>= 1)
-          #pragma unroll
-          for (int c = 0; c < w; ++c) m8[c] = fmaxf(m8[c], m8[c + w]);
-        const float m_tile = m8[0] * sl2;  // -inf stays -inf
-        const bool need = m_tile > m_run + kRescaleThreshold;
-        const bool warp_rescale = __any_sync(0xffffffffu, need) && j > 0;
-        const float m_new = need ? m_tile : m_run;
-        const float alpha = need ? fast_exp2(m_run - m_new) : 1.f;  // exp2(-inf) = 0
-        m_run = m_new;
-        const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
-        float s8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-        #pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          uint32_t pk[32];
-          #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const float p0 = fast_exp2(fmaf(x[c * 64 + 2 * i], sl2, -m_use));
-            const float p1 = fast_exp2(fmaf(x[c * 64 + 2 * i + 1], sl2, -m_use));
-            s8[i & 7] += p0 + p1;
-            pk[i] = pack_bf16x2(p0, p1);
-          }
-          tmem_st32(tS + c * 32, pk);
-        }
-        #pragma unroll
-        for (int w = 4; w > 0; w >>= 1)
-          #pragma unroll
-          for (int c = 0; c < w; ++c) s8[c] += s8[c + w];
-        l_run = l_run * alpha + s8[0];
-        if (warp_rescale) {
-          // O holds PV up to tile j-1: wait for it, then scale it in place
-          // before PV(j) is issued (which needs p_full below).
-          ok = mbar_wait(&sm.o_full[s], (j - 1) & 1, abort_flag, gstatus,
-                         LCATTN_ERR_DEVICE_TIMEOUT);
+          ok = mbar_wait(&sm.s_full[s], (T + j) & 1, abort_flag, gstatus, LCATTN_ERR_DEVICE_TIMEOUT);
           if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
           tc_fence_after();
+          uint32_t xr[128];
+          tmem_ld32(tS + 0, xr + 0);
+          tmem_ld32(tS + 32, xr + 32);
+          tmem_ld32(tS + 64, xr + 64);
+          tmem_ld32(tS + 96, xr + 96);
+          tmem_ld_wait();
+          float x[128];
+          #pragma unroll
+          for (int c = 0; c < 128; ++c) x[c] = __uint_as_float(xr[c]);
+          if (masked) {
+            const uint32_t w0 = mw[0], w1 = mw[1], w2 = mw[2], w3 = mw[3];
+            #pragma unroll
+            for (int c = 0; c < 128; ++c) {
+              const uint32_t w = c < 32 ? w0 : (c < 64 ? w1 : (c < 96 ? w2 : w3));
+              if (!((w >> (c & 31)) & 1u)) x[c] = -INFINITY;
+            }
+          }
+          // Row max as 8 independent chains (a single 128-long chain is latency bound).
+          float m8[8];
+          #pragma unroll
+          for (int c = 0; c < 8; ++c) m8[c] = x[c];
+          #pragma unroll
+          for (int c = 8; c < 128; ++c) m8[c & 7] = fmaxf(m8[c & 7], x[c]);
+          #pragma unroll
+          for (int w = 4; w > 0; w >>= 1)
+            #pragma unroll
+            for (int c = 0; c < w; ++c) m8[c] = fmaxf(m8[c], m8[c + w]);
+          const float m_tile = m8[0] * sl2;  // -inf stays -inf
+          const bool need = m_tile > m_run + kRescaleThreshold;
+          const bool warp_rescale = __any_sync(0xffffffffu, need) && j > 0;
+          const float m_new = need ? m_tile : m_run;
+          const float alpha = need ? fast_exp2(m_run - m_new) : 1.f;  // exp2(-inf) = 0
+          m_run = m_new;
+          const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
+          float s8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+          #pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            uint32_t pk[32];
+            #pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const float p0 = fast_exp2(fmaf(x[c * 64 + 2 * i], sl2, -m_use));
+              const float p1 = fast_exp2(fmaf(x[c * 64 + 2 * i + 1], sl2, -m_use));
+              s8[i & 7] += p0 + p1;
+              pk[i] = pack_bf16x2(p0, p1);
+            }
+            tmem_st32(tS + c * 32, pk);
+          }
+          #pragma unroll
+          for (int w = 4; w > 0; w >>= 1)
+            #pragma unroll
+            for (int c = 0; c < w; ++c) s8[c] += s8[c + w];
+          l_run = l_run * alpha + s8[0];
+          if (warp_rescale) {
+            // O holds PV up to tile j-1: wait for it, then scale it in place
+            // before PV(j) is issued (which needs p_full below).
+            ok = mbar_wait(&sm.o_full[s], (T + j - 1) & 1, abort_flag, gstatus,
+                           LCATTN_ERR_DEVICE_TIMEOUT);
+            if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+            tc_fence_after();
+            #pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              uint32_t o32[32];
+              tmem_ld32(tO + c * 32, o32);
+              tmem_ld_wait();
+              #pragma unroll
+              for (int i = 0; i < 32; ++i) o32[i] = __float_as_uint(__uint_as_float(o32[i]) * alpha);
+              tmem_st32(tO + c * 32, o32);
+            }
+          }
+          tmem_st_wait();
+          tc_fence_before();
+          mbar_arrive(&sm.p_full[s]);
+        }
+        // ---- epilogue: O / l and LSE.  O is read (and the read waited for)
+        // before the next item's first P is released, which is what lets the
+        // next item's first PV overwrite it.
+        bool have_o = ok && n > 0;
+        if (have_o) {
+          have_o = mbar_wait(&sm.o_full[s], (T + n - 1) & 1, abort_flag, gstatus,
+                             LCATTN_ERR_DEVICE_TIMEOUT);
+          have_o = __all_sync(0xffffffffu, have_o);
+          tc_fence_after();
+        }
+        if (ok && (have_o || n == 0)) {
+          const bool live = l_run > 0.f;
+          const float inv = live ? 1.f / l_run : 0.f;
+          __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(a.o) + (int64_t)b * a.o_sb +
+                                (int64_t)row * a.o_ss + (int64_t)h * a.o_sh;
           #pragma unroll
           for (int c = 0; c < 4; ++c) {
             uint32_t o32[32];
-            tmem_ld32(tO + c * 32, o32);
-            tmem_ld_wait();
+            if (have_o) {
+              tmem_ld32(tO + c * 32, o32);
+              tmem_ld_wait();
+            } else {
+              #pragma unroll
+              for (int i = 0; i < 32; ++i) o32[i] = 0u;
+            }
+            uint32_t pk[16];
             #pragma unroll
-            for (int i = 0; i < 32; ++i) o32[i] = __float_as_uint(__uint_as_float(o32[i]) * alpha);
-            tmem_st32(tO + c * 32, o32);
+            for (int i = 0; i < 16; ++i)
+              pk[i] = pack_bf16x2(__uint_as_float(o32[2 * i]) * inv,
+                                  __uint_as_float(o32[2 * i + 1]) * inv);
+            if (row < pr.Sq) {
+              uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+              #pragma unroll
+              for (int i = 0; i < 4; ++i)
+                dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+            }
           }
+          if (row < pr.Sq)
+            a.lse[((int64_t)b * pr.Hq + h) * pr.Sq + row] =
+                live ? (m_run + __log2f(l_run)) * 0.69314718055994531f : -INFINITY;
         }
-        tmem_st_wait();
-        tc_fence_before();
-        mbar_arrive(&sm.p_full[s]);
-      }
-      // ---- epilogue: O / l and LSE
-      bool have_o = ok && n > 0;
-      if (have_o) {
-        have_o = mbar_wait(&sm.o_full[s], (n - 1) & 1, abort_flag, gstatus,
-                           LCATTN_ERR_DEVICE_TIMEOUT);
-        have_o = __all_sync(0xffffffffu, have_o);
-        tc_fence_after();
-      }
-      if (ok) {
-        const bool live = l_run > 0.f;
-        const float inv = live ? 1.f / l_run : 0.f;
-        __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(a.o) + (int64_t)b * a.o_sb +
-                              (int64_t)row * a.o_ss + (int64_t)h * a.o_sh;
-        #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t o32[32];
-          if (have_o) {
-            tmem_ld32(tO + c * 32, o32);
-            tmem_ld_wait();
-          } else {
-            #pragma unroll
-            for (int i = 0; i < 32; ++i) o32[i] = 0u;
-          }
-          uint32_t pk[16];
-          #pragma unroll
-          for (int i = 0; i < 16; ++i)
-            pk[i] = pack_bf16x2(__uint_as_float(o32[2 * i]) * inv,
-                                __uint_as_float(o32[2 * i + 1]) * inv);
-          if (row < pr.Sq) {
-            uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
-            #pragma unroll
-            for (int i = 0; i < 4; ++i)
-              dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
-          }
-        }
-        if (row < pr.Sq)
-          a.lse[((int64_t)b * pr.Hq + h) * pr.Sq + row] =
-              live ? (m_run + __log2f(l_run)) * 0.69314718055994531f : -INFINITY;
+        if (n > 0 && !have_o) ok = false;
+        T += n;
       }
     }
   }
@@ -467,12 +627,20 @@ cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
     if (e != cudaSuccess) return e;
     attr_done = true;
   }
+  int dev = 0, nsm = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
   FwdKernelArgs ka;
   ka.a = a;
   // Two query heads per CTA when they share the key tiles and the tile list.
   ka.heads_per_cta = (a.meta.nH == 1 && a.pr.G % 2 == 0) ? 2 : 1;
-  dim3 grid(a.pr.Hq / ka.heads_per_cta, a.meta.nQt, a.pr.B);
-  fwd_kernel<<<grid, kThreads, smem, st>>>(tq, tk, tv, ka);
+  const int64_t total = (int64_t)(a.pr.Hq / ka.heads_per_cta) * a.pr.B * a.meta.nQt;
+  if (total > 0x7fffffffLL) return cudaErrorInvalidValue;  // far beyond any problem that fits in memory
+  ka.total_items = static_cast<int>(total);
+  // Persistent: one CTA per SM (shared memory admits one), never more CTAs than items.
+  const int grid = ka.total_items < nsm ? ka.total_items : nsm;
+  fwd_kernel<<<(unsigned)grid, kThreads, smem, st>>>(tq, tk, tv, ka);
   return cudaGetLastError();
 }
 

@@ -27,6 +27,7 @@ struct MaskDev {
 // Pointers into a tile-meta buffer.
 struct TileMetaDev {
   int32_t* status;
+  unsigned long long* sched;  // [0] next forward item, [1] forward CTAs done fetching
   uint8_t* cls;
   int32_t* fwd_cnt;
   int32_t* fwd_lst;

@@ -48,7 +48,6 @@ __global__ void classify_kernel(ProblemDev pr, MaskDev m, TileMetaDev t) {
        w += warps_total) {
     const int kt = (int)(w % t.nKt);
     const int qt = (int)((w / t.nKt) % t.nQt);
-    const int h = (int)((w / ((int64_t)t.nKt * t.nQt)) % t.nH);
     const int b = (int)(w / ((int64_t)t.nKt * t.nQt * t.nH));
     const int r0 = qt * kBM, r1 = min(pr.Sq, r0 + kBM);
     const int c0 = kt * kBN, c1 = min(pr.Sk, c0 + kBN);
@@ -186,7 +185,7 @@ __global__ void order_kernel(TileMetaDev t) {
 
 cudaError_t launch_mask_compile(const ProblemDev& pr, const MaskDev& m, const TileMetaDev& t,
                                 cudaStream_t st) {
-  cudaError_t e = cudaMemsetAsync(t.status, 0, 16, st);
+  cudaError_t e = cudaMemsetAsync(t.status, 0, 32, st);  // status and scheduler words
   if (e != cudaSuccess) return e;
   if (m.kind == LCATTN_MASK_BLOCKMAP) {
     validate_offsets_kernel<<<1, 32, 0, st>>>(m, pr.Sq, pr.Sk, t.status);

@@ -247,6 +247,18 @@ __device__ __forceinline__ void tma_load_4d_e(void* dst, const CUtensorMap* m, u
       : "memory");
 }
 
+// L2 prefetch of one tensor-map box: no shared-memory destination and no
+// completion signal (a hint; coordinates past the tensor are ignored).
+__device__ __forceinline__ void tma_prefetch_l2_4d_e(const CUtensorMap* m, int32_t c0, int32_t c1,
+                                                     int32_t c2, int32_t c3) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];\n\t}\n"
+      :: "l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+      : "memory");
+}
+
 // 32 lanes x 32 columns of 32 bit: thread t of the warp receives lane (base + t),
 // columns col .. col+31.
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t* r) {

@@ -54,6 +54,9 @@ def test_layout_sizes_and_alignment():
     offs = [L.off_status, L.off_class, L.off_fwd_cnt, L.off_fwd_lst, L.off_fwd_ord,
             L.off_bwd_cnt, L.off_bwd_lst, L.off_bwd_ord, L.total_bytes]
     assert all(o % 256 == 0 for o in offs) and offs == sorted(offs)
+    # the scheduler words sit right behind the four status words, which
+    # lcattn_clear_status (given only the base pointer) relies on
+    assert L.off_status == 0 and L.off_sched == 16 and L.off_sched + 16 <= L.off_class
     assert L.off_fwd_lst - L.off_fwd_cnt >= 4 * 3
     assert L.off_fwd_ord - L.off_fwd_lst >= 4 * 9
     # block maps carry one list per query head
