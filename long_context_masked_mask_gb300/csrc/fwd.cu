@@ -503,41 +503,39 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
               if (!((w >> (c & 31)) & 1u)) x[c] = -INFINITY;
             }
           }
-          // Row max as 8 independent chains (a single 128-long chain is latency bound).
-          float m8[8];
+          // Row max: four independent chains of three-input maxima (two new
+          // columns per instruction; one long chain would be latency bound).
+          float m4[4];
           #pragma unroll
-          for (int c = 0; c < 8; ++c) m8[c] = x[c];
+          for (int c = 0; c < 4; ++c) m4[c] = fmaxf(x[2 * c], x[2 * c + 1]);
           #pragma unroll
-          for (int c = 8; c < 128; ++c) m8[c & 7] = fmaxf(m8[c & 7], x[c]);
-          #pragma unroll
-          for (int w = 4; w > 0; w >>= 1)
-            #pragma unroll
-            for (int c = 0; c < w; ++c) m8[c] = fmaxf(m8[c], m8[c + w]);
-          const float m_tile = m8[0] * sl2;  // -inf stays -inf
+          for (int c = 8; c < 128; c += 2) m4[(c >> 1) & 3] = fmax3(m4[(c >> 1) & 3], x[c], x[c + 1]);
+          const float m_tile = fmaxf(fmax3(m4[0], m4[1], m4[2]), m4[3]) * sl2;  // -inf stays -inf
           const bool need = m_tile > m_run + kRescaleThreshold;
           const bool warp_rescale = __any_sync(0xffffffffu, need) && j > 0;
           const float m_new = need ? m_tile : m_run;
           const float alpha = need ? fast_exp2(m_run - m_new) : 1.f;  // exp2(-inf) = 0
           m_run = m_new;
           const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
-          float s8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+          // P = exp2(S * scale * log2(e) - m): the scaling and the row sum run
+          // on column pairs (paired fp32 instructions), the exponentials one by one.
+          const float2 sl2v = make_float2(sl2, sl2), negm = make_float2(-m_use, -m_use);
+          float2 s4[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                          make_float2(0.f, 0.f)};
           #pragma unroll
           for (int c = 0; c < 2; ++c) {
             uint32_t pk[32];
             #pragma unroll
             for (int i = 0; i < 32; ++i) {
-              const float p0 = fast_exp2(fmaf(x[c * 64 + 2 * i], sl2, -m_use));
-              const float p1 = fast_exp2(fmaf(x[c * 64 + 2 * i + 1], sl2, -m_use));
-              s8[i & 7] += p0 + p1;
-              pk[i] = pack_bf16x2(p0, p1);
+              const float2 y = fma2(make_float2(x[c * 64 + 2 * i], x[c * 64 + 2 * i + 1]), sl2v, negm);
+              const float2 p = make_float2(fast_exp2(y.x), fast_exp2(y.y));
+              s4[i & 3] = add2(s4[i & 3], p);
+              pk[i] = pack_bf16x2(p.x, p.y);
             }
             tmem_st32(tS + c * 32, pk);
           }
-          #pragma unroll
-          for (int w = 4; w > 0; w >>= 1)
-            #pragma unroll
-            for (int c = 0; c < w; ++c) s8[c] += s8[c + w];
-          l_run = l_run * alpha + s8[0];
+          const float2 s2 = add2(add2(s4[0], s4[1]), add2(s4[2], s4[3]));
+          l_run = l_run * alpha + (s2.x + s2.y);
           if (warp_rescale) {
             // O holds PV up to tile j-1: wait for it, then scale it in place
             // before PV(j) is issued (which needs p_full below).

@@ -199,3 +199,41 @@ def test_bad_block_offsets_reported_on_device():
     assert lc.lcattn_read_status(meta) == lc.LCATTN_ERR_DEVICE_MASK
     lc.lcattn_clear_status(meta)
     assert lc.lcattn_read_status(meta) == 0
+
+
+def _sched_words(meta):
+    torch.cuda.synchronize()
+    return meta[16:32].view(torch.int64).cpu().tolist()
+
+
+def test_persistent_forward_repeats_exactly():
+    """The forward's CTAs take work items from a counter in the tile-meta
+    scheduler words, and the last CTA to run out of work resets it.  Repeated
+    calls on one compiled mask give identical bits and leave the words at zero;
+    with more items than CTAs (256 here: 8 query tiles x 32 head pairs) every
+    query tile is still covered, which the sampled oracle rows check."""
+    N, Hq, Hkv = 1000, 64, 8
+    spec = spec_for("CAUSAL_DOCUMENT", N, Hq, seed=3)
+    x = qkv(1, N, Hq, Hkv, 128, seed=11, with_do=False)
+    dev = {k: t.cuda() for k, t in x.items()}
+    mask = lc.DeviceMask(spec, N, Hq)
+    shape = lc.make_shape(dev["q"], dev["k"], dev["v"])
+    meta = lc.lcattn_mask_compile(shape, mask)
+    assert _sched_words(meta) == [0, 0]
+    outs = []
+    for _ in range(3):
+        o, lse = lc.lcattn_fwd(dev["q"], dev["k"], dev["v"], mask, meta)
+        assert _sched_words(meta) == [0, 0]
+        outs.append((o.clone(), lse.clone()))
+    assert lc.lcattn_read_status(meta) == 0
+    for o, lse in outs[1:]:
+        assert torch.equal(o, outs[0][0]) and torch.equal(lse, outs[0][1])
+    q, k, v = (x[n].double().numpy() for n in ("q", "k", "v"))
+    scale = 1.0 / math.sqrt(128)
+    rows = np.array([0, 127, 128, 500, 871, 999])
+    o, lse = outs[0]
+    for h in (0, 1, 37, 63):
+        ro, rl = oracle.attention_fwd_rows(q, k, v, spec, scale, 0, h, rows)
+        got = o[0, rows, h].double().cpu().numpy()
+        assert np.abs(got - ro).max() <= O_MAXABS
+        assert np.abs(lse[0, h, rows].double().cpu().numpy() - rl).max() <= LSE_MAXABS
