@@ -480,16 +480,21 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
         tmem_ld32(tS + c0, s0);
         tmem_ld32(tS + c0 + 32, s1);
         tmem_ld_wait();
+        const float2 sl2v = make_float2(sl2, sl2);
         #pragma unroll
         for (int c4 = 0; c4 < 8; ++c4) {
           const float4 la = lse4[c4], lb = lse4[8 + c4];
-          const float l_a[4] = {la.x, la.y, la.z, la.w}, l_b[4] = {lb.x, lb.y, lb.z, lb.w};
-          float pa[4], pb[4];
-          #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            pa[u] = fast_exp2(fmaf(__uint_as_float(s0[4 * c4 + u]), sl2, -l_a[u]));
-            pb[u] = fast_exp2(fmaf(__uint_as_float(s1[4 * c4 + u]), sl2, -l_b[u]));
-          }
+          // exp2(S * scale * log2(e) - lse2) on column pairs (paired fp32 FMA).
+          const float2 ya0 = fma2(make_float2(__uint_as_float(s0[4 * c4]), __uint_as_float(s0[4 * c4 + 1])),
+                                  sl2v, make_float2(-la.x, -la.y));
+          const float2 ya1 = fma2(make_float2(__uint_as_float(s0[4 * c4 + 2]), __uint_as_float(s0[4 * c4 + 3])),
+                                  sl2v, make_float2(-la.z, -la.w));
+          const float2 yb0 = fma2(make_float2(__uint_as_float(s1[4 * c4]), __uint_as_float(s1[4 * c4 + 1])),
+                                  sl2v, make_float2(-lb.x, -lb.y));
+          const float2 yb1 = fma2(make_float2(__uint_as_float(s1[4 * c4 + 2]), __uint_as_float(s1[4 * c4 + 3])),
+                                  sl2v, make_float2(-lb.z, -lb.w));
+          float pa[4] = {fast_exp2(ya0.x), fast_exp2(ya0.y), fast_exp2(ya1.x), fast_exp2(ya1.y)};
+          float pb[4] = {fast_exp2(yb0.x), fast_exp2(yb0.y), fast_exp2(yb1.x), fast_exp2(yb1.y)};
           if (masked) {
             #pragma unroll
             for (int u = 0; u < 4; ++u) {
@@ -517,16 +522,21 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
         #pragma unroll
         for (int c4 = 0; c4 < 8; ++c4) {
           const float4 da = dv4[c4], db = dv4[8 + c4];
-          const float D_a[4] = {da.x, da.y, da.z, da.w}, D_b[4] = {db.x, db.y, db.z, db.w};
-          float sa[4], sb[4];
-          #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const uint32_t wa = pk[2 * c4 + (u >> 1)], wb = pk[16 + 2 * c4 + (u >> 1)];
-            const float p_a = __uint_as_float((u & 1) ? (wa & 0xffff0000u) : (wa << 16));
-            const float p_b = __uint_as_float((u & 1) ? (wb & 0xffff0000u) : (wb << 16));
-            sa[u] = p_a * (__uint_as_float(d0[4 * c4 + u]) - D_a[u]);
-            sb[u] = p_b * (__uint_as_float(d1[4 * c4 + u]) - D_b[u]);
-          }
+          // P' (bf16 pairs -> fp32) times (dP - D), on column pairs.
+          auto unpack = [](uint32_t w) {
+            return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+          };
+          const float2 ta0 = add2(make_float2(__uint_as_float(d0[4 * c4]), __uint_as_float(d0[4 * c4 + 1])),
+                                  make_float2(-da.x, -da.y));
+          const float2 ta1 = add2(make_float2(__uint_as_float(d0[4 * c4 + 2]), __uint_as_float(d0[4 * c4 + 3])),
+                                  make_float2(-da.z, -da.w));
+          const float2 tb0 = add2(make_float2(__uint_as_float(d1[4 * c4]), __uint_as_float(d1[4 * c4 + 1])),
+                                  make_float2(-db.x, -db.y));
+          const float2 tb1 = add2(make_float2(__uint_as_float(d1[4 * c4 + 2]), __uint_as_float(d1[4 * c4 + 3])),
+                                  make_float2(-db.z, -db.w));
+          const float2 za0 = mul2(unpack(pk[2 * c4]), ta0), za1 = mul2(unpack(pk[2 * c4 + 1]), ta1);
+          const float2 zb0 = mul2(unpack(pk[16 + 2 * c4]), tb0), zb1 = mul2(unpack(pk[16 + 2 * c4 + 1]), tb1);
+          const float sa[4] = {za0.x, za0.y, za1.x, za1.y}, sb[4] = {zb0.x, zb0.y, zb1.x, zb1.y};
           dk[2 * c4] = pack_bf16x2(sa[0], sa[1]);
           dk[2 * c4 + 1] = pack_bf16x2(sa[2], sa[3]);
           dk[16 + 2 * c4] = pack_bf16x2(sb[0], sb[1]);

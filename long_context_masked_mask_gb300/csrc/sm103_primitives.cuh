@@ -391,6 +391,17 @@ __device__ __forceinline__ float2 add2(float2 a, float2 b) {
   return r;
 }
 
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
+  float2 r;
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "mul.f32x2 rd, ra, rb;\n\t"
+      "mov.b64 {%0, %1}, rd;\n\t}\n"
+      : "=f"(r.x), "=f"(r.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return r;
+}
+
 // Three-input maximum (same NaN rule as fmaxf: a NaN operand is ignored).
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float r;
