@@ -91,6 +91,16 @@ typedef struct lcattn_mask_desc {
   const int32_t* k_block_offs;
   int32_t nQb;
   int32_t nKb;
+  /* kind 1, optional (device) int32 [B][Sq][4] = {c0, d0, c1, d1}: query row i
+   * may attend key j iff c0 <= j < d0 or c1 <= j < d1 -- the same mask as
+   * col_bounds, transposed (every static family of the pages has at most two
+   * key intervals per row).  Any int32 values; intervals are clipped to
+   * [0, Sk).  When given, the forward builds the row masks of partial tiles
+   * from it (a few instructions per row instead of 128 column tests); tile
+   * classification and the backward always use col_bounds.  The library cannot
+   * check that the two forms agree: that is the caller's promise.  NULL = not
+   * given.  16-byte aligned.                                                  */
+  const int32_t* row_bounds;
 } lcattn_mask_desc;
 
 /* Tile classes written by the mask compiler (one byte per 128x128 tile). */

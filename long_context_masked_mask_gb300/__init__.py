@@ -64,7 +64,8 @@ class lcattn_shape(ctypes.Structure):
 class lcattn_mask_desc(ctypes.Structure):
     _fields_ = [("kind", ctypes.c_int32), ("col_bounds", ctypes.c_void_p),
                 ("block_map", ctypes.c_void_p), ("q_block_offs", ctypes.c_void_p),
-                ("k_block_offs", ctypes.c_void_p), ("nQb", ctypes.c_int32), ("nKb", ctypes.c_int32)]
+                ("k_block_offs", ctypes.c_void_p), ("nQb", ctypes.c_int32), ("nKb", ctypes.c_int32),
+                ("row_bounds", ctypes.c_void_p)]
 
 
 class lcattn_tile_meta_layout(ctypes.Structure):
@@ -159,7 +160,8 @@ class DeviceMask:
     host builders of :mod:`.masks`; the same descriptor serves every batch
     entry (it is replicated ``B`` times)."""
 
-    def __init__(self, spec, N: int, Hq: int, B: int = 1, device: str = "cuda"):
+    def __init__(self, spec, N: int, Hq: int, B: int = 1, device: str = "cuda",
+                 row_bounds: bool = True):
         self.spec = spec
         self.N, self.Hq, self.B = N, Hq, B
         self.desc = lcattn_mask_desc()
@@ -181,6 +183,10 @@ class DeviceMask:
             self.col_bounds = torch.from_numpy(np.broadcast_to(cb, (B,) + cb.shape).copy()).to(device)
             self.desc.kind = LCATTN_MASK_COLBOUNDS
             self.desc.col_bounds = self.col_bounds.data_ptr()
+            if row_bounds:  # the same mask per query row, for the forward's partial tiles
+                rb = masks.row_bounds(spec, N)
+                self.row_bounds = torch.from_numpy(np.broadcast_to(rb, (B,) + rb.shape).copy()).to(device)
+                self.desc.row_bounds = self.row_bounds.data_ptr()
 
     @property
     def allowed_pairs(self) -> int:

@@ -41,6 +41,7 @@ int validate_mask(const lcattn_shape* s, const lcattn_mask_desc* m) {
   if (!m) return LCATTN_ERR_INVALID_ARG;
   if (m->kind == LCATTN_MASK_COLBOUNDS) {
     if (!m->col_bounds || !aligned16(m->col_bounds)) return LCATTN_ERR_INVALID_ARG;
+    if (m->row_bounds && !aligned16(m->row_bounds)) return LCATTN_ERR_INVALID_ARG;
     return LCATTN_OK;
   }
   if (m->kind == LCATTN_MASK_BLOCKMAP) {
@@ -86,6 +87,8 @@ MaskDev mask_of(const lcattn_mask_desc* m) {
   MaskDev d;
   d.kind = m->kind;
   d.col_bounds = reinterpret_cast<const int4*>(m->col_bounds);
+  d.row_bounds = m->kind == LCATTN_MASK_COLBOUNDS ? reinterpret_cast<const int4*>(m->row_bounds)
+                                                  : nullptr;
   d.block_map = m->block_map;
   d.q_offs = m->q_block_offs;
   d.k_offs = m->k_block_offs;

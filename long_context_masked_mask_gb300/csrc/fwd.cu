@@ -437,6 +437,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
       const float sl2 = a.scale_log2;
       const int last_kt = (pr.Sk - 1) / kBN;
       const bool ragged_k = (pr.Sk % kBN) != 0;
+      const bool use_rows = a.mask.kind == LCATTN_MASK_COLBOUNDS && a.mask.row_bounds != nullptr;
       bool ok = true;
       int T = 0;          // tiles of this CTA processed before the current item
       int n_partial = 0;  // partial column-bounds tiles staged so far (selects the buffer)
@@ -456,6 +457,10 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
         int qb_row = 0;
         if (a.mask.kind == LCATTN_MASK_BLOCKMAP)
           qb_row = block_of(a.mask.q_offs, a.mask.nQb, min(row, pr.Sq - 1));
+        // This row's allowed keys [c0, d0) U [c1, d1), when the descriptor carries
+        // the per-row form (rows past Sq allow nothing).
+        int4 rb = make_int4(0, 0, 0, 0);
+        if (use_rows && row < pr.Sq) rb = __ldg(a.mask.row_bounds + (int64_t)b * pr.Sq + row);
         float m_run = -INFINITY, l_run = 0.f;
         int e_next = n > 0 ? __ldg(it.list) : 0;
         for (int j = 0; j < n; ++j) {
@@ -465,7 +470,15 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
           const bool partial = (e & 1) != 0;
           const bool masked = partial || (ragged_k && kt == last_kt);
           uint32_t mw[4];
-          if (masked) {
+          if (masked && partial && use_rows) {
+            // The row's two key intervals, clipped to the tile's valid columns.
+            const int j0 = kt * kBN, j1 = min(pr.Sk, j0 + kBN);
+            const int lo0 = max(rb.x, j0) - j0, hi0 = min(rb.y, j1) - j0;
+            const int lo1 = max(rb.z, j0) - j0, hi1 = min(rb.w, j1) - j0;
+            #pragma unroll
+            for (int w = 0; w < 4; ++w)
+              mw[w] = range_bits(lo0, hi0, 32 * w) | range_bits(lo1, hi1, 32 * w);
+          } else if (masked) {
             const int4* bnd = nullptr;
             if (partial && a.mask.kind == LCATTN_MASK_COLBOUNDS) {
               // Stage the tile's 128 column bounds in shared memory: one coalesced

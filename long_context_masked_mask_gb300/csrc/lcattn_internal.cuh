@@ -18,6 +18,7 @@ constexpr int kD = 128;              // head dim
 struct MaskDev {
   int kind;                  // LCATTN_MASK_COLBOUNDS / LCATTN_MASK_BLOCKMAP
   const int4* col_bounds;    // [B][Sk] {a0,b0,a1,b1}
+  const int4* row_bounds;    // [B][Sq] {c0,d0,c1,d1}, or null (column bounds only)
   const uint8_t* block_map;  // [B][Hq][nQb][nKb]
   const int32_t* q_offs;     // [nQb+1]
   const int32_t* k_offs;     // [nKb+1]

@@ -101,6 +101,75 @@ def col_bounds(spec, N: int) -> np.ndarray:
     return np.ascontiguousarray(out.astype(np.int32))
 
 
+def row_bounds(spec, N: int) -> np.ndarray:
+    """int32 [N, 4] = (c0, d0, c1, d1) per query row: row i may attend the keys
+    [c0, d0) U [c1, d1).  The same mask as :func:`col_bounds`, transposed; every
+    static family has at most two key intervals per row.  The forward kernel
+    uses this form to build a partial tile's row masks cheaply."""
+    k, p = spec.kind, spec.params
+    i = np.arange(N, dtype=np.int64)
+    c0 = np.zeros(N, np.int64)
+    d0 = np.full(N, N, np.int64)
+    c1 = np.zeros(N, np.int64)
+    d1 = np.zeros(N, np.int64)  # second interval empty unless set
+    if k == "FULL":
+        pass
+    elif k == "CAUSAL":
+        d0 = i + 1
+    elif k == "FULL_DOCUMENT":
+        _, c0, d0 = _per_key(p["doc_lens"], N)
+    elif k == "CAUSAL_DOCUMENT":
+        _, c0, _ = _per_key(p["doc_lens"], N)
+        d0 = i + 1
+    elif k == "FULL_SLIDING_WINDOW":
+        w = int(p["window"])
+        c0 = np.maximum(0, i - w + 1)
+        d0 = np.minimum(N, i + w)
+    elif k == "CAUSAL_SLIDING_WINDOW":
+        w = int(p["window"])
+        c0 = np.maximum(0, i - w + 1)
+        d0 = i + 1
+    elif k == "SHARED_QUESTION":
+        q = int(p["question_len"])
+        lens = [q] + [int(x) for x in p["answer_lens"]]
+        seg, start, _ = _per_key(lens, N)
+        # the question's rows: causal over the question; an answer's rows: the
+        # whole question, then causal inside their own answer
+        c0 = np.where(seg == 0, 0, start)
+        d0 = i + 1
+        d1 = np.where(seg == 0, 0, min(q, N))
+    elif k == "GLOBAL_SLIDING":
+        g, w = int(p["global_tokens"]), int(p["window"])
+        glob = i < g
+        c0 = np.where(glob, 0, np.maximum(0, i - w + 1))
+        d0 = np.where(glob, N, np.minimum(N, i + w))
+        d1 = np.where(glob, 0, min(g, N))  # every row sees the global keys
+    elif k == "CAUSAL_BLOCKWISE":
+        bs = int(p["block"])
+        last = (N - 1) // bs
+        blk = i // bs
+        c0 = np.where(blk == last, 0, blk * bs)  # the final block's rows see every earlier key
+        d0 = i + 1
+    elif k == "PREFIX_LM_CAUSAL":
+        pre = min(int(p["prefix"]), N)
+        d0 = np.maximum(pre, i + 1)
+    elif k == "PREFIX_LM_DOCUMENT":
+        seg, start, end = _per_key(p["doc_lens"], N)
+        pref = np.minimum(np.asarray(p["prefix_lens"], dtype=np.int64)[seg], end - start)
+        c0 = start
+        d0 = np.maximum(start + pref, i + 1)
+    elif k == "BLOCK_CAUSAL_DOCUMENT":
+        _, dstart, _ = _per_key(p["doc_lens"], N)
+        flat = [int(x) for doc in p["block_lens"] for x in doc]
+        _, _, bend = _per_key(flat, N)
+        c0 = dstart  # keys from the row's document start to the end of its block
+        d0 = bend
+    else:
+        raise ValueError(f"{k} is not a column-bounds mask")
+    out = np.stack([c0, d0, c1, d1], axis=1)
+    return np.ascontiguousarray(out.astype(np.int32))
+
+
 def block_map(spec, N: int, Hq: int):
     """(keep uint8 [Hq, nQb, nKb], q_offs int32 [nQb+1], k_offs int32 [nKb+1])."""
     k, p = spec.kind, spec.params

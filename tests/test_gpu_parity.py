@@ -112,6 +112,33 @@ def test_mask_family_gqa_ragged(kind):
     run_and_compare(spec_for(kind, N, Hq), 1, N, Hq, Hkv)
 
 
+COLUMN_KINDS = [k for k in KINDS if not k.startswith(("UNIFORM", "VARIABLE"))]
+
+
+@pytest.mark.parametrize("kind", COLUMN_KINDS)
+def test_forward_column_path_matches_row_path(kind):
+    """A column-bounds descriptor without the per-row form makes the forward
+    build partial-tile masks from the 128 column bounds (staged in shared
+    memory) instead of the row intervals: the oracle and the row path agree."""
+    N, Hq, Hkv = 392, 4, 2
+    spec = spec_for(kind, N, Hq)
+    x = qkv(1, N, Hq, Hkv, 128, seed=6, with_do=False)
+    dev = {k: t.cuda() for k, t in x.items()}
+    shape = lc.make_shape(dev["q"], dev["k"], dev["v"])
+    outs = []
+    for rows in (True, False):
+        mask = lc.DeviceMask(spec, N, Hq, row_bounds=rows)
+        meta = lc.lcattn_mask_compile(shape, mask)
+        o, lse = lc.lcattn_fwd(dev["q"], dev["k"], dev["v"], mask, meta)
+        assert lc.lcattn_read_status(meta) == 0
+        outs.append((o.clone(), lse.clone()))
+    assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
+    f64 = {k: t.double().numpy() for k, t in x.items()}
+    O, LSE = oracle.attention_fwd(f64["q"], f64["k"], f64["v"], spec, 1.0 / math.sqrt(128))
+    o = outs[1][0].double().cpu().numpy()
+    assert np.abs(o - O).max() <= O_MAXABS and relf(o, O) <= O_RELF
+
+
 @pytest.mark.parametrize("kind", ["CAUSAL", "GLOBAL_SLIDING", "SHARED_QUESTION", "UNIFORM_BLOCK"])
 def test_mha_and_batch(kind):
     N, Hq = 512, 2

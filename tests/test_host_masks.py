@@ -1,6 +1,6 @@
 """Host-side mask descriptors (product) against the oracle's predicates (CPU only).
 
-The column-bounds and block-map builders of ``long_context_masked_mask_gb300.masks``
+The column-bounds, row-bounds and block-map builders of ``long_context_masked_mask_gb300.masks``
 are expanded back to boolean masks here and compared element by element with
 ``oracle.allowed``, which evaluates each family's predicate directly.  The
 allowed-pair counts used by the FLOP metric are checked the same way.
@@ -59,6 +59,21 @@ def test_col_bounds_match_predicates(N, seed):
         assert masks.allowed_pairs_from_bounds(cb, N) == allowed_pairs(spec, N), spec.kind
 
 
+def expand_rows(rb, N):
+    j = np.arange(N)[None, :]
+    c0, d0, c1, d1 = (rb[:, k][:, None] for k in range(4))
+    return ((c0 <= j) & (j < d0)) | ((c1 <= j) & (j < d1))
+
+
+@pytest.mark.parametrize("N,seed", [(6, 0), (9, 1), (64, 2), (130, 3), (257, 4), (1000, 5)])
+def test_row_bounds_match_predicates(N, seed):
+    """The per-row form (key intervals of each query row) is the same mask."""
+    for spec in static_specs(N, seed):
+        rb = masks.row_bounds(spec, N)
+        assert rb.dtype == np.int32 and rb.shape == (N, 4)
+        np.testing.assert_array_equal(expand_rows(rb, N), allowed(spec, N), err_msg=spec.kind)
+
+
 def test_single_token_sequence():
     for spec in (MaskSpec("FULL"), MaskSpec("CAUSAL"), MaskSpec("CAUSAL_SLIDING_WINDOW", {"window": 4})):
         cb = masks.col_bounds(spec, 1)
@@ -82,6 +97,8 @@ def test_config_masks_match_predicates():
         a0, b0, a1, b1 = (cb[:, k][None, :] for k in range(4))
         got = ((a0 <= i) & (i < b0)) | ((a1 <= i) & (i < b1))
         np.testing.assert_array_equal(got, allowed(spec, N, rows), err_msg=spec.kind)
+        rb = masks.row_bounds(spec, N)[rows]
+        np.testing.assert_array_equal(expand_rows(rb, N), allowed(spec, N, rows), err_msg=spec.kind)
 
 
 @pytest.mark.parametrize("seed", [0, 1, 2])
