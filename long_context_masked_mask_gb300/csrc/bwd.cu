@@ -44,10 +44,12 @@ constexpr int kTileBytes = 32768;
 constexpr int kHalfBytes = 16384;
 constexpr int kThreadsDkdv = 512;      // 4 warpgroups
 // Register split for dK/dV (launch: 512 threads x 128): the two elementwise
-// warpgroups and the drain warpgroup 136 each, producer/MMA warpgroup 104.
-constexpr int kRegsWork = 136;
-constexpr int kRegsCtl = 104;
-static_assert(128 * (3 * kRegsWork + kRegsCtl) <= kThreadsDkdv * 128, "register split");
+// warpgroups 128 each, the dQ drain 136 (a whole dQ^T row in registers),
+// producer/MMA warpgroup 120.
+constexpr int kRegsWork = 128;
+constexpr int kRegsDrain = 136;
+constexpr int kRegsCtl = 120;
+static_assert(128 * (2 * kRegsWork + kRegsDrain + kRegsCtl) <= kThreadsDkdv * 128, "register split");
 constexpr float kLog2e = 1.4426950408889634f;
 
 // ---------------------------------------------------------------------------
@@ -124,7 +126,7 @@ struct BwdSmem {
   uint64_t kv_full;
   uint64_t q_full[2];
   uint64_t q_empty[2];
-  uint64_t s_full, dp_full, ds_ready, dq_full, dq_free, done;
+  uint64_t s_full, dp_full, p_ready, ds_ready, dq_full, dq_free, done;
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -208,6 +210,7 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
     }
     mbar_init(&sm.s_full, 1);
     mbar_init(&sm.dp_full, 1);
+    mbar_init(&sm.p_ready, 256);
     mbar_init(&sm.ds_ready, 256);
     mbar_init(&sm.dq_full, 1);
     mbar_init(&sm.dq_free, 128);
@@ -283,8 +286,9 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
     }
   } else if (warp == 13) {
     // ------------------------------------------------------------ MMA issuer
-    // Per item i: dP^T(i) | wait dS(i) | dV, dK | S^T(i+1) | dQ^T(i).  S^T(i+1)
-    // goes before dQ^T(i) so that P(i+1) is computed while dQ^T(i) runs.  The
+    // Per item i: wait P'(i) | dV(i) | S^T(i+1) | wait dS(i) | dK(i) | dQ^T(i) |
+    // wait drain | dP^T(i+1).  dV needs only P', so S^T(i+1) can follow it
+    // while dS(i) is still being formed, and P'(i+1) starts right after.  The
     // whole warp runs the loop; each tcgen05.mma / commit is issued by one
     // elected lane.
     {
@@ -313,45 +317,38 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
           mma_ss_e<1>(d, sdesc_add(a0, off), sdesc_add(b0, off), id_kmaj);
         }
       };
+      // Prologue: S^T(0) and dP^T(0).
       if (ok && it.valid()) {
         ok = __all_sync(0xffffffffu, mbar_wait(&sm.q_full[0], 0, abort_flag, gstatus, TO));
         if (ok) {
           tc_fence_after();
           issue_kmaj(tS, dK_k, dQ_k);  // S^T(0) = K Q_0^T
           tc_commit_e(&sm.s_full);
+          issue_kmaj(tP, dV_k, dO_k);  // dP^T(0) = V dO_0^T
+          tc_commit_e(&sm.dp_full);
         }
       }
       int i = 0;
       for (; ok && it.valid(); ++i) {
         const int st = i & 1;
         const uint32_t qoff = st * kTileBytes;
-        // dP^T = V dO^T, into the columns dQ^T(i-1) used: wait for its drain.
-        if (i > 0) {
-          ok = __all_sync(0xffffffffu, mbar_wait(&sm.dq_free, (i - 1) & 1, abort_flag, gstatus, TO));
-          if (!ok) break;
-          tc_fence_after();
-        }
-        issue_kmaj(tP, dV_k, sdesc_add(dO_k, qoff));
-        tc_commit_e(&sm.dp_full);
-        ok = __all_sync(0xffffffffu, mbar_wait(&sm.ds_ready, i & 1, abort_flag, gstatus, TO));
+        // dV += P'^T dO as soon as P'(i) is in TMEM (A from TMEM: queries 0-63
+        // sit in the first 32 columns of each half's region, 64-127 at +64).
+        ok = __all_sync(0xffffffffu, mbar_wait(&sm.p_ready, i & 1, abort_flag, gstatus, TO));
         if (!ok) break;
         tc_fence_after();
-        // dV += P'^T dO ; dK += dS^T Q.  A from TMEM: queries 0-63 sit in the
-        // first 32 columns of each half's region, queries 64-127 at +64.
         {
-          const uint64_t bo = sdesc_add(dO_mn, qoff), bq = sdesc_add(dQ_mn, qoff);
+          const uint64_t bo = sdesc_add(dO_mn, qoff);
           mma_ts_er(tdV, tS, bo, id_ts, i > 0 ? 1u : 0u);
           #pragma unroll
           for (int kk = 1; kk < 8; ++kk)
             mma_ts_e<1>(tdV, tS + (kk >> 2) * 64 + (kk & 3) * 8, sdesc_add(bo, kk * 2048), id_ts);
-          mma_ts_er(tdK, tP, bq, id_ts, i > 0 ? 1u : 0u);
-          #pragma unroll
-          for (int kk = 1; kk < 8; ++kk)
-            mma_ts_e<1>(tdK, tP + (kk >> 2) * 64 + (kk & 3) * 8, sdesc_add(bq, kk * 2048), id_ts);
         }
-        tc_commit_e(&sm.q_empty[st]);
+        // S^T(i+1) right behind it: it overwrites P'(i), which dV(i) read
+        // before (in-order), and the elementwise pass keeps P' in registers.
         it.next();
-        if (it.valid()) {
+        const bool more = it.valid();
+        if (more) {
           const int st2 = (i + 1) & 1;
           ok = __all_sync(0xffffffffu, mbar_wait(&sm.q_full[st2], ((i + 1) >> 1) & 1, abort_flag, gstatus, TO));
           if (!ok) break;
@@ -359,6 +356,18 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
           issue_kmaj(tS, dK_k, sdesc_add(dQ_k, st2 * kTileBytes));  // S^T(i+1)
           tc_commit_e(&sm.s_full);
         }
+        // dK += dS^T Q once dS(i) is ready (A = dS^T from TMEM).
+        ok = __all_sync(0xffffffffu, mbar_wait(&sm.ds_ready, i & 1, abort_flag, gstatus, TO));
+        if (!ok) break;
+        tc_fence_after();
+        {
+          const uint64_t bq = sdesc_add(dQ_mn, qoff);
+          mma_ts_er(tdK, tP, bq, id_ts, i > 0 ? 1u : 0u);
+          #pragma unroll
+          for (int kk = 1; kk < 8; ++kk)
+            mma_ts_e<1>(tdK, tP + (kk >> 2) * 64 + (kk & 3) * 8, sdesc_add(bq, kk * 2048), id_ts);
+        }
+        tc_commit_e(&sm.q_empty[st]);  // Q(i), dO(i), LSE(i), D(i) are read for good
         // dQ^T = K^T dS^T: A = K read MN-major (M = head dim), B = dS^T read
         // MN-major (N = queries).  Lands in [128, 256): lane = head dim.
         mma_ss_e<0>(tP, dK_mn, dS_mn, id_mn);
@@ -366,6 +375,14 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
         for (int kk = 1; kk < 8; ++kk)
           mma_ss_e<1>(tP, sdesc_add(dK_mn, kk * 2048), sdesc_add(dS_mn, kk * 2048), id_mn);
         tc_commit_e(&sm.dq_full);
+        // dP^T(i+1) = V dO^T, into the columns dQ^T(i) uses: wait for its drain.
+        if (more) {
+          ok = __all_sync(0xffffffffu, mbar_wait(&sm.dq_free, i & 1, abort_flag, gstatus, TO));
+          if (!ok) break;
+          tc_fence_after();
+          issue_kmaj(tP, dV_k, sdesc_add(dO_k, ((i + 1) & 1) * kTileBytes));
+          tc_commit_e(&sm.dp_full);
+        }
       }
       tc_commit_e(&sm.done);
       int dummy = 0;
@@ -373,7 +390,7 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
     }
   }
   } else if (warp >= 8) {
-    regs_inc<kRegsWork>();
+    regs_inc<kRegsDrain>();
     // ------------------------------------------------------------ dQ drain
     const int r = 32 * (warp & 3) + lane;  // head-dim row of dQ^T (TMEM lane)
     const uint32_t tQ = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16) + 128;
@@ -443,13 +460,12 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
         m0 = m1 = 0u;
       } else if (masked) {
         if (a.mask.kind == LCATTN_MASK_COLBOUNDS) {
-          m0 = m1 = 0u;
-          #pragma unroll
-          for (int c = 0; c < 32; ++c) {
-            const int q = q0 + c, q2 = q0 + 32 + c;
-            m0 |= (((cb.x <= q && q < cb.y) || (cb.z <= q && q < cb.w)) ? 1u : 0u) << c;
-            m1 |= (((cb.x <= q2 && q2 < cb.y) || (cb.z <= q2 && q2 < cb.w)) ? 1u : 0u) << c;
-          }
+          // This key's allowed query rows [a0, b0) U [a1, b1), clipped to the
+          // 64 columns [q0, q0 + 64) of this warpgroup: two bit ranges.
+          const int lo0 = max(cb.x, q0) - q0, hi0 = min(cb.y, q0 + 64) - q0;
+          const int lo1 = max(cb.z, q0) - q0, hi1 = min(cb.w, q0 + 64) - q0;
+          m0 = range_bits(lo0, hi0, 0) | range_bits(lo1, hi1, 0);
+          m1 = range_bits(lo0, hi0, 32) | range_bits(lo1, hi1, 32);
         } else {
           m0 = m1 = 0u;
           const uint8_t* map = a.mask.block_map +
@@ -508,6 +524,9 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
           pk[16 + 2 * c4 + 1] = pack_bf16x2(pb[2], pb[3]);
         }
         tmem_st32(tS + c0, pk);  // columns [64x, 64x + 32): only this warpgroup read them
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&sm.p_ready);  // dV(i) may start; P' stays in registers for dS
       }
       // ---- dS^T = P'^T (dP^T - D) = scale * P^T (dP^T - D), from the bf16 P'
       ok = mbar_wait(&sm.dp_full, i & 1, abort_flag, gstatus, TO);
