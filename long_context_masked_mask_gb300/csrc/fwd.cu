@@ -294,17 +294,22 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
         tma_load_4d_e(sm.kv[stage], tm, &sm.kv_full[stage], 0, g, kt * kBN, it.b);
         tma_load_4d_e(sm.kv[stage] + kHalfBytes, tm, &sm.kv_full[stage], 64, g, kt * kBN, it.b);
         if (u == 0) {
+          // Two heads: buffer s holds slot s's Q for every item.  One head:
+          // the two buffers alternate between items, so the next item's Q
+          // never waits for this item's last S GEMM.
           for (int s = 0; s < hpc && ok; ++s) {
-            if (nq > 0) {
-              ok = mbar_wait(&sm.q_empty[s], (nq - 1) & 1, abort_flag, gstatus,
+            const int qb = hpc == 1 ? (nq & 1) : s;
+            const int quse = hpc == 1 ? (nq >> 1) : nq;
+            if (quse > 0) {
+              ok = mbar_wait(&sm.q_empty[qb], (quse - 1) & 1, abort_flag, gstatus,
                              LCATTN_ERR_DEVICE_TIMEOUT);
               if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
             }
-            mbar_expect_tx_e(&sm.q_full[s], kTileBytes);
-            tma_load_4d_e(sm.q[s], &tmQ, &sm.q_full[s], 0, it.h0 + s, it.qt * kBM, it.b);
-            tma_load_4d_e(sm.q[s] + kHalfBytes, &tmQ, &sm.q_full[s], 64, it.h0 + s,
+            mbar_expect_tx_e(&sm.q_full[qb], kTileBytes);
+            tma_load_4d_e(sm.q[qb], &tmQ, &sm.q_full[qb], 0, it.h0 + s, it.qt * kBM, it.b);
+            tma_load_4d_e(sm.q[qb] + kHalfBytes, &tmQ, &sm.q_full[qb], 64, it.h0 + s,
                           it.qt * kBM, it.b);
-            ++q_issued[s];
+            ++q_issued[qb];
           }
           if (!ok) { ++t; break; }
           ++nq;
@@ -359,6 +364,74 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
         tc_commit_e(&sm.o_full[s]);
         return true;
       };
+      if (hpc == 1) {
+        // One head per item: S is double-buffered in the two S regions, and
+        // S(t) is issued before PV(t-1), so the softmax of tile t-1 overlaps
+        // S(t) and finds S(t) done when it finishes.  S(t) overwrites the
+        // buffer of P(t-2), which PV(t-2), issued before it, has read.
+        const uint32_t tO = tmem + 256;
+        uint32_t acc_prev = 0u;
+        auto issue_pv1 = [&](int tt, uint32_t acc) -> bool {
+          const int tv = 2 * tt + 1;
+          bool okw = mbar_wait(&sm.kv_full[tv % kStages], (tv / kStages) & 1, abort_flag, gstatus,
+                               LCATTN_ERR_DEVICE_TIMEOUT);
+          // P(tt) is released on the barrier of its S buffer: one barrier per
+          // buffer keeps the softmax (which can run a tile ahead) from
+          // completing a second phase before this wait has seen the first.
+          if (okw) okw = mbar_wait(&sm.p_full[tt & 1], (tt >> 1) & 1, abort_flag, gstatus,
+                                   LCATTN_ERR_DEVICE_TIMEOUT);
+          if (!__all_sync(0xffffffffu, okw)) return false;
+          tc_fence_after();
+          const uint64_t vb = sdesc_add(dv0, (tv % kStages) * kTileBytes);
+          const uint32_t tP = tmem + (tt & 1) * 128;
+          mma_ts_er(tO, tP, vb, idesc_pv, acc);
+          #pragma unroll
+          for (int kk = 1; kk < 8; ++kk) mma_ts_e<1>(tO, tP + kk * 8, sdesc_add(vb, kk * 2048), idesc_pv);
+          tc_commit_e(&sm.o_full[0]);
+          tc_commit_e(&sm.kv_empty[tv % kStages]);
+          return true;
+        };
+        for (int k = 0; ok; ++k) {
+          const int e = k % kItemQ;
+          ok = mbar_wait(&sm.item_full[e], (k / kItemQ) & 1, abort_flag, gstatus,
+                         LCATTN_ERR_DEVICE_TIMEOUT);
+          if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+          const int idx = sm.items[e];
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sm.item_empty[e]);
+          if (idx < 0) break;
+          const int n = fwd_item(a, hpc, idx).n;
+          if (n == 0) continue;
+          const int qb = nq & 1;
+          ok = __all_sync(0xffffffffu, mbar_wait(&sm.q_full[qb], (nq >> 1) & 1, abort_flag, gstatus,
+                                                 LCATTN_ERR_DEVICE_TIMEOUT));
+          if (!ok) break;
+          const uint64_t qd = qb ? dq1 : dq0;
+          for (int j = 0; j < n; ++j, ++T) {
+            const int tk = 2 * T;
+            ok = __all_sync(0xffffffffu, mbar_wait(&sm.kv_full[tk % kStages], (tk / kStages) & 1,
+                                                   abort_flag, gstatus, LCATTN_ERR_DEVICE_TIMEOUT));
+            if (!ok) break;
+            tc_fence_after();
+            const uint64_t kb = sdesc_add(dk0, (tk % kStages) * kTileBytes);
+            const uint32_t tS = tmem + (T & 1) * 128;
+            mma_ss_e<0>(tS, qd, kb, idesc_qk);
+            #pragma unroll
+            for (int kk = 1; kk < 8; ++kk) {
+              constexpr uint32_t kHalf = kHalfBytes;
+              const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
+              mma_ss_e<1>(tS, sdesc_add(qd, off), sdesc_add(kb, off), idesc_qk);
+            }
+            tc_commit_e(&sm.s_full[T & 1]);
+            tc_commit_e(&sm.kv_empty[tk % kStages]);
+            if (j == n - 1) tc_commit_e(&sm.q_empty[qb]);  // this item's Q is read for good
+            if (T > 0 && !issue_pv1(T - 1, acc_prev)) { ok = false; break; }
+            acc_prev = j > 0 ? 1u : 0u;
+          }
+          if (ok) ++nq;
+        }
+        if (ok && T > 0) issue_pv1(T - 1, acc_prev);
+      } else
       for (int k = 0; ok; ++k) {
         const int e = k % kItemQ;
         ok = mbar_wait(&sm.item_full[e], (k / kItemQ) & 1, abort_flag, gstatus,
@@ -407,8 +480,8 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
         }
         if (ok) ++nq;
       }
-      // The last PV of the sequence.
-      if (ok && T > 0) {
+      // The last PV of the sequence (two heads per item).
+      if (hpc != 1 && ok && T > 0) {
         const int tv = 2 * T - 1;
         ok = mbar_wait(&sm.kv_full[tv % kStages], (tv / kStages) & 1, abort_flag, gstatus,
                        LCATTN_ERR_DEVICE_TIMEOUT);
@@ -432,7 +505,6 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
     const int r = tid & 127;  // == 32 * (warp % 4) + lane: this thread's TMEM lane
     if (s < hpc) {
       const uint32_t lane_off = static_cast<uint32_t>(32 * (warp & 3)) << 16;
-      const uint32_t tS = tmem + lane_off + s * 128;
       const uint32_t tO = tmem + lane_off + 256 + s * 128;
       const float sl2 = a.scale_log2;
       const int last_kt = (pr.Sk - 1) / kBN;
@@ -496,7 +568,12 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
             }
             tile_mask_bits(a.mask, pr, b, h, row, qb_row, kt, partial, bnd, mw);
           }
-          ok = mbar_wait(&sm.s_full[s], (T + j) & 1, abort_flag, gstatus, LCATTN_ERR_DEVICE_TIMEOUT);
+          // Two heads: slot s's S region every tile.  One head: the two S
+          // regions alternate between tiles.
+          const int sb = hpc == 1 ? ((T + j) & 1) : s;
+          const uint32_t tS = tmem + lane_off + sb * 128;
+          ok = mbar_wait(&sm.s_full[sb], (hpc == 1 ? ((T + j) >> 1) : (T + j)) & 1, abort_flag, gstatus,
+                         LCATTN_ERR_DEVICE_TIMEOUT);
           if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
           tc_fence_after();
           uint32_t xr[128];
@@ -568,7 +645,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
           }
           tmem_st_wait();
           tc_fence_before();
-          mbar_arrive(&sm.p_full[s]);
+          mbar_arrive(&sm.p_full[sb]);
         }
         // ---- epilogue: O / l and LSE.  O is read (and the read waited for)
         // before the next item's first P is released, which is what lets the
