@@ -121,7 +121,9 @@ struct BwdSmem {
   alignas(1024) uint8_t q[2][kTileBytes];
   alignas(1024) uint8_t dO[2][kTileBytes];
   alignas(1024) uint8_t ds[kTileBytes];  // dS^T, keys x queries, read MN-major by dQ^T
-  alignas(16) float lse2[2][128];  // LSE*log2(e) - log2(scale); +inf where P must be 0
+  // Stored negated, so that the paired fp32 instructions take them as plain
+  // addends: -(LSE*log2(e) - log2(scale)) (-inf where P must be 0) and -D.
+  alignas(16) float lse2[2][128];
   alignas(16) float dvec_s[2][128];
   uint64_t kv_full;
   uint64_t q_full[2];
@@ -266,14 +268,14 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
       for (int k = 0; k < 4; ++k) {
         const int c = lane * 4 + k;
         const int q = qt * kBM + c;
-        float l2 = INFINITY, d = 0.f;
+        float l2 = -INFINITY, d = 0.f;
         if (q < pr.Sq) {
           const float l = __ldg(lse + q);
-          l2 = (l == -INFINITY) ? INFINITY : l * kLog2e - log2_scale;  // fully masked row: P = 0
+          l2 = (l == -INFINITY) ? -INFINITY : log2_scale - l * kLog2e;  // fully masked row: P = 0
           d = __ldg(dv + q);
         }
         sm.lse2[st][c] = l2;
-        sm.dvec_s[st][c] = d;
+        sm.dvec_s[st][c] = -d;
       }
       mbar_arrive(&sm.q_full[st]);
       issued = i + 1;
@@ -482,7 +484,7 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
           }
         }
       }
-      // Rows past Sq carry LSE = +inf (set by the producer), so P = 0 there.
+      // Rows past Sq carry a negated LSE of -inf (set by the producer), so P = 0 there.
       ok = mbar_wait(&sm.q_full[st], (i >> 1) & 1, abort_flag, gstatus, TO) &&
            mbar_wait(&sm.s_full, i & 1, abort_flag, gstatus, TO);
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
@@ -500,15 +502,15 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
         #pragma unroll
         for (int c4 = 0; c4 < 8; ++c4) {
           const float4 la = lse4[c4], lb = lse4[8 + c4];
-          // exp2(S * scale * log2(e) - lse2) on column pairs (paired fp32 FMA).
+          // exp2(S * scale * log2(e) + (-lse2)) on column pairs (paired fp32 FMA).
           const float2 ya0 = fma2(make_float2(__uint_as_float(s0[4 * c4]), __uint_as_float(s0[4 * c4 + 1])),
-                                  sl2v, make_float2(-la.x, -la.y));
+                                  sl2v, make_float2(la.x, la.y));
           const float2 ya1 = fma2(make_float2(__uint_as_float(s0[4 * c4 + 2]), __uint_as_float(s0[4 * c4 + 3])),
-                                  sl2v, make_float2(-la.z, -la.w));
+                                  sl2v, make_float2(la.z, la.w));
           const float2 yb0 = fma2(make_float2(__uint_as_float(s1[4 * c4]), __uint_as_float(s1[4 * c4 + 1])),
-                                  sl2v, make_float2(-lb.x, -lb.y));
+                                  sl2v, make_float2(lb.x, lb.y));
           const float2 yb1 = fma2(make_float2(__uint_as_float(s1[4 * c4 + 2]), __uint_as_float(s1[4 * c4 + 3])),
-                                  sl2v, make_float2(-lb.z, -lb.w));
+                                  sl2v, make_float2(lb.z, lb.w));
           float pa[4] = {fast_exp2(ya0.x), fast_exp2(ya0.y), fast_exp2(ya1.x), fast_exp2(ya1.y)};
           float pb[4] = {fast_exp2(yb0.x), fast_exp2(yb0.y), fast_exp2(yb1.x), fast_exp2(yb1.y)};
           if (masked) {
@@ -546,13 +548,13 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
             return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
           };
           const float2 ta0 = add2(make_float2(__uint_as_float(d0[4 * c4]), __uint_as_float(d0[4 * c4 + 1])),
-                                  make_float2(-da.x, -da.y));
+                                  make_float2(da.x, da.y));
           const float2 ta1 = add2(make_float2(__uint_as_float(d0[4 * c4 + 2]), __uint_as_float(d0[4 * c4 + 3])),
-                                  make_float2(-da.z, -da.w));
+                                  make_float2(da.z, da.w));
           const float2 tb0 = add2(make_float2(__uint_as_float(d1[4 * c4]), __uint_as_float(d1[4 * c4 + 1])),
-                                  make_float2(-db.x, -db.y));
+                                  make_float2(db.x, db.y));
           const float2 tb1 = add2(make_float2(__uint_as_float(d1[4 * c4 + 2]), __uint_as_float(d1[4 * c4 + 3])),
-                                  make_float2(-db.z, -db.w));
+                                  make_float2(db.z, db.w));
           const float2 za0 = mul2(unpack(pk[2 * c4]), ta0), za1 = mul2(unpack(pk[2 * c4 + 1]), ta1);
           const float2 zb0 = mul2(unpack(pk[16 + 2 * c4]), tb0), zb1 = mul2(unpack(pk[16 + 2 * c4 + 1]), tb1);
           const float sa[4] = {za0.x, za0.y, za1.x, za1.y}, sb[4] = {zb0.x, zb0.y, zb1.x, zb1.y};
