@@ -57,7 +57,8 @@ struct FwdSmem {
   uint64_t kv_empty[kStages];
   uint64_t s_full[2];
   uint64_t p_full[2];
-  uint64_t o_full[2];
+  uint64_t o_full[2];  // every PV of the slot has completed (one phase per PV)
+  uint64_t o_last[2];  // an item's last PV has completed (one phase per item)
   uint64_t drain;
   int items[kItemQ];           // item indices handed from the producer to the other roles
   uint64_t item_full[kItemQ];
@@ -190,6 +191,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
       mbar_init(&sm.s_full[s], 1);
       mbar_init(&sm.p_full[s], 128);
       mbar_init(&sm.o_full[s], 1);
+      mbar_init(&sm.o_last[s], 1);
     }
     for (int i = 0; i < kStages; ++i) {
       mbar_init(&sm.kv_full[i], 1);
@@ -349,7 +351,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
       bool ok = true;
       int T = 0, nq = 0;
       uint32_t pv_acc = 0u;  // accumulate flag of the pending PV(T-1)
-      auto issue_pv = [&](int s) -> bool {
+      auto issue_pv = [&](int s, bool last) -> bool {
         const uint32_t tS = tmem + s * 128, tO = tmem + 256 + s * 128;
         const bool okw = mbar_wait(&sm.p_full[s], (T - 1) & 1, abort_flag, gstatus,
                                    LCATTN_ERR_DEVICE_TIMEOUT);
@@ -362,6 +364,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
         #pragma unroll
         for (int kk = 1; kk < 8; ++kk) mma_ts_e<1>(tO, tS + kk * 8, sdesc_add(vb, kk * 2048), idesc_pv);
         tc_commit_e(&sm.o_full[s]);
+        if (last) tc_commit_e(&sm.o_last[s]);  // the item's O is complete
         return true;
       };
       if (hpc == 1) {
@@ -371,7 +374,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
         // buffer of P(t-2), which PV(t-2), issued before it, has read.
         const uint32_t tO = tmem + 256;
         uint32_t acc_prev = 0u;
-        auto issue_pv1 = [&](int tt, uint32_t acc) -> bool {
+        auto issue_pv1 = [&](int tt, uint32_t acc, bool last) -> bool {
           const int tv = 2 * tt + 1;
           bool okw = mbar_wait(&sm.kv_full[tv % kStages], (tv / kStages) & 1, abort_flag, gstatus,
                                LCATTN_ERR_DEVICE_TIMEOUT);
@@ -388,6 +391,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
           #pragma unroll
           for (int kk = 1; kk < 8; ++kk) mma_ts_e<1>(tO, tP + kk * 8, sdesc_add(vb, kk * 2048), idesc_pv);
           tc_commit_e(&sm.o_full[0]);
+          if (last) tc_commit_e(&sm.o_last[0]);  // the item's O is complete
           tc_commit_e(&sm.kv_empty[tv % kStages]);
           return true;
         };
@@ -425,12 +429,13 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
             tc_commit_e(&sm.s_full[T & 1]);
             tc_commit_e(&sm.kv_empty[tk % kStages]);
             if (j == n - 1) tc_commit_e(&sm.q_empty[qb]);  // this item's Q is read for good
-            if (T > 0 && !issue_pv1(T - 1, acc_prev)) { ok = false; break; }
+            // PV(T-1) closes the previous item when tile T opens a new one.
+            if (T > 0 && !issue_pv1(T - 1, acc_prev, j == 0)) { ok = false; break; }
             acc_prev = j > 0 ? 1u : 0u;
           }
           if (ok) ++nq;
         }
-        if (ok && T > 0) issue_pv1(T - 1, acc_prev);
+        if (ok && T > 0) issue_pv1(T - 1, acc_prev, true);
       } else
       for (int k = 0; ok; ++k) {
         const int e = k % kItemQ;
@@ -454,7 +459,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
           tc_fence_after();
           const uint64_t kb = sdesc_add(dk0, (tk % kStages) * kTileBytes);
           for (int s = 0; s < hpc; ++s) {
-            if (T > 0 && !issue_pv(s)) { ok = false; break; }
+            if (T > 0 && !issue_pv(s, j == 0)) { ok = false; break; }
             if (j == 0) {
               ok = mbar_wait(&sm.q_full[s], nq & 1, abort_flag, gstatus, LCATTN_ERR_DEVICE_TIMEOUT);
               if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
@@ -488,7 +493,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
         if (__all_sync(0xffffffffu, ok)) {
           tc_fence_after();
           for (int s = 0; s < hpc; ++s)
-            if (!issue_pv(s)) break;
+            if (!issue_pv(s, true)) break;
           tc_commit_e(&sm.kv_empty[tv % kStages]);
         }
       }
@@ -513,6 +518,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
       bool ok = true;
       int T = 0;          // tiles of this CTA processed before the current item
       int n_partial = 0;  // partial column-bounds tiles staged so far (selects the buffer)
+      int n_items = 0;    // items with at least one key tile finished so far
       for (int k = 0; ok; ++k) {
         const int e = k % kItemQ;
         ok = mbar_wait(&sm.item_full[e], (k / kItemQ) & 1, abort_flag, gstatus,
@@ -649,10 +655,13 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
         }
         // ---- epilogue: O / l and LSE.  O is read (and the read waited for)
         // before the next item's first P is released, which is what lets the
-        // next item's first PV overwrite it.
+        // next item's first PV overwrite it.  The wait is on the per-item
+        // barrier: with S issued ahead (one head per item) the softmax can
+        // finish an item while two of its PVs are still pending, and a parity
+        // wait on the per-PV barrier could then match an older phase.
         bool have_o = ok && n > 0;
         if (have_o) {
-          have_o = mbar_wait(&sm.o_full[s], (T + n - 1) & 1, abort_flag, gstatus,
+          have_o = mbar_wait(&sm.o_last[s], n_items & 1, abort_flag, gstatus,
                              LCATTN_ERR_DEVICE_TIMEOUT);
           have_o = __all_sync(0xffffffffu, have_o);
           tc_fence_after();
@@ -689,6 +698,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
                 live ? (m_run + __log2f(l_run)) * 0.69314718055994531f : -INFINITY;
         }
         if (n > 0 && !have_o) ok = false;
+        if (n > 0) ++n_items;
         T += n;
       }
     }
