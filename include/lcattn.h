@@ -168,7 +168,11 @@ int lcattn_fwd(const lcattn_shape* shape, const void* q, const void* k, const vo
                float* lse, lcattn_stream_t stream);
 
 /* Workspace (device bytes) lcattn_bwd needs: D = rowsum(dO * O) fp32
- * [B][Hq][Sq] and the fp32 dQ accumulator [B][Sq][Hq][128].                */
+ * [B][Hq][Sq], the fp32 dQ accumulator [B][Sq][Hq][128] and, when the dK/dV
+ * work units (key tiles x KV heads x batch) are too few to fill the GPU in
+ * several waves -- under 1216, and the GQA group splits evenly -- fp32 dK/dV
+ * partials [2 or 4][2][B][Sk][Hkv][128]: each unit is split over 2 or 4
+ * shares of its group's query heads and the partials are summed into dK, dV. */
 size_t lcattn_bwd_workspace_size(const lcattn_shape* shape);
 
 /* Backward of L = sum(O * dO).  Inputs as for lcattn_fwd plus o, d_o (bf16,
@@ -203,10 +207,11 @@ int lcattn_bwd_stage(int stage, const lcattn_shape* shape, const void* q, const 
  * Same arguments and results as lcattn_bwd without `workspace`.  The D vector
  * and the fp32 dQ accumulator live instead in one fixed device array inside the
  * library, LCATTN_NOALLOC_SCRATCH_BYTES (32 MiB) large; every GPU that loads
- * the library holds it until the process exits.  A problem whose
- * lcattn_bwd_workspace_size exceeds it returns LCATTN_ERR_SCRATCH_LIMIT and
- * launches nothing (32 MiB covers B * Hq * Sq up to 65,027 query rows, e.g.
- * 8 heads at 8K tokens).
+ * the library holds it until the process exits.  This call never splits
+ * dK/dV work units (it needs no partials).  A problem whose D vector and dQ
+ * accumulator exceed the array returns LCATTN_ERR_SCRATCH_LIMIT and launches
+ * nothing (32 MiB covers B * Hq * Sq up to 65,027 query rows, e.g. 8 heads at
+ * 8K tokens).
  *
  * The first call on a device looks the array's device address up (with that
  * device current) and caches it; make that first call before any stream

@@ -146,6 +146,28 @@ int encode_bshd(CUtensorMap* m, const void* ptr, int64_t B, int64_t S, int64_t H
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? LCATTN_OK : LCATTN_ERR_CUDA; }
 
+// dK/dV work units (key tile, KV head, batch) are split over shares of the
+// GQA group's query heads when there are too few units to fill the GPU in
+// several waves (a partly empty last wave of equal units costs up to a wave);
+// the shares' fp32 partials are summed afterwards.  Depends on the shape only,
+// so the workspace size does too.
+int bwd_parts(const lcattn_shape* s) {
+  const int64_t units = (s->Sk + kBN - 1) / kBN * s->Hkv * s->B;
+  const int64_t G = s->Hq / s->Hkv;
+  if (units < 304 && G % 4 == 0) return 4;
+  if (units < 1216 && G % 2 == 0) return 2;
+  return 1;
+}
+
+// Workspace: D [B][Hq][Sq], the fp32 dQ accumulator [B][Sq][Hq][128] and, for
+// split units, the fp32 dK/dV partials [parts][2][B][Sk][Hkv][128].
+int64_t bwd_ws_bytes(const lcattn_shape* s, int parts) {
+  const int64_t d_bytes = align_up(4 * s->B * s->Hq * s->Sq, 256);
+  const int64_t acc_bytes = align_up(4 * s->B * s->Sq * s->Hq * kD, 256);
+  const int64_t part_bytes = parts > 1 ? (int64_t)parts * 2 * 4 * s->B * s->Sk * s->Hkv * kD : 0;
+  return d_bytes + acc_bytes + part_bytes;
+}
+
 }  // namespace
 
 extern "C" {
@@ -200,9 +222,7 @@ int lcattn_fwd(const lcattn_shape* shape, const void* q, const void* k, const vo
 
 size_t lcattn_bwd_workspace_size(const lcattn_shape* shape) {
   if (validate_shape(shape) != LCATTN_OK) return 0;
-  const int64_t d_bytes = align_up(4 * shape->B * shape->Hq * shape->Sq, 256);
-  const int64_t acc_bytes = 4 * shape->B * shape->Sq * shape->Hq * kD;
-  return (size_t)(d_bytes + acc_bytes);
+  return (size_t)bwd_ws_bytes(shape, bwd_parts(shape));
 }
 
 }  // extern "C"
@@ -213,7 +233,8 @@ namespace {
 int bwd_run(unsigned stages, const lcattn_shape* shape, const void* q, const void* k,
             const void* v, const void* o, const void* d_o, const float* lse,
             const void* tile_meta, const lcattn_mask_desc* mask, float scale, void* dq, void* dk,
-            void* dv, void* workspace, size_t workspace_bytes, lcattn_stream_t stream) {
+            void* dv, void* workspace, size_t workspace_bytes, lcattn_stream_t stream,
+            bool allow_split = true) {
   lcattn_tile_meta_layout L;
   int st = layout_of(shape, mask, &L);
   if (st) return st;
@@ -223,7 +244,8 @@ int bwd_run(unsigned stages, const lcattn_shape* shape, const void* q, const voi
   for (auto p : ptrs)
     if (!aligned16(p)) return LCATTN_ERR_UNSUPPORTED;
   if (!(scale > 0.f) || !(scale < 1e30f)) return LCATTN_ERR_INVALID_ARG;
-  if (workspace_bytes < lcattn_bwd_workspace_size(shape)) return LCATTN_ERR_WORKSPACE;
+  const int parts = allow_split ? bwd_parts(shape) : 1;
+  if ((int64_t)workspace_bytes < bwd_ws_bytes(shape, parts)) return LCATTN_ERR_WORKSPACE;
   CUtensorMap tq, tk, tv, tdo;
   if ((st = encode_bshd(&tq, q, shape->B, shape->Sq, shape->Hq, shape->q_stride))) return st;
   if ((st = encode_bshd(&tk, k, shape->B, shape->Sk, shape->Hkv, shape->k_stride))) return st;
@@ -242,6 +264,8 @@ int bwd_run(unsigned stages, const lcattn_shape* shape, const void* q, const voi
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   a.dvec = reinterpret_cast<float*>(ws);
   a.dq_acc = reinterpret_cast<float*>(ws + align_up(4 * shape->B * shape->Hq * shape->Sq, 256));
+  a.parts = parts;
+  a.dkv_part = reinterpret_cast<float*>(ws + bwd_ws_bytes(shape, 1));
   a.dq = dq;
   a.q_sb = shape->q_stride[0]; a.q_ss = shape->q_stride[1]; a.q_sh = shape->q_stride[2];
   a.dk = dk;
@@ -317,12 +341,13 @@ int lcattn_bwd_noalloc(const lcattn_shape* shape, const void* q, const void* k, 
                        lcattn_stream_t stream) {
   int st = validate_shape(shape);
   if (st) return st;
-  const size_t need = lcattn_bwd_workspace_size(shape);
-  if (need > (size_t)LCATTN_NOALLOC_SCRATCH_BYTES) return LCATTN_ERR_SCRATCH_LIMIT;
+  // No split here: the fixed array holds D and the dQ accumulator only.
+  const int64_t need = bwd_ws_bytes(shape, 1);
+  if (need > (int64_t)LCATTN_NOALLOC_SCRATCH_BYTES) return LCATTN_ERR_SCRATCH_LIMIT;
   void* ws = nullptr;
   if ((st = noalloc_scratch(&ws))) return st;
   return bwd_run(7u, shape, q, k, v, o, d_o, lse, tile_meta, mask, scale, dq, dk, dv, ws,
-                 (size_t)LCATTN_NOALLOC_SCRATCH_BYTES, stream);
+                 (size_t)LCATTN_NOALLOC_SCRATCH_BYTES, stream, /*allow_split=*/false);
 }
 
 int lcattn_read_status(const void* tile_meta, lcattn_stream_t stream) {

@@ -112,6 +112,36 @@ __global__ void dq_convert_kernel(BwdArgs a) {
   }
 }
 
+// Sum of the split units' fp32 partials -> bf16 dK, dV (8 head dims per step).
+__global__ void dkv_reduce_kernel(BwdArgs a) {
+  const int64_t per = (int64_t)a.pr.B * a.pr.Sk * a.pr.Hkv * (kD / 8);  // 8-wide groups per tensor
+  const int64_t stride_part = 2 * (int64_t)a.pr.B * a.pr.Sk * a.pr.Hkv * kD;
+  for (int64_t v = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; v < 2 * per;
+       v += (int64_t)gridDim.x * blockDim.x) {
+    const int w = (int)(v / per);  // 0 = dV, 1 = dK
+    const int64_t r = v - (int64_t)w * per;
+    const int c = (int)(r % (kD / 8));
+    const int64_t row = r / (kD / 8);  // (b, key, g)
+    const int g = (int)(row % a.pr.Hkv);
+    const int key = (int)((row / a.pr.Hkv) % a.pr.Sk);
+    const int b = (int)(row / ((int64_t)a.pr.Hkv * a.pr.Sk));
+    const float* src = a.dkv_part + ((int64_t)w * a.pr.B * a.pr.Sk * a.pr.Hkv + row) * kD + c * 8;
+    float4 s0 = make_float4(0.f, 0.f, 0.f, 0.f), s1 = s0;
+    for (int p = 0; p < a.parts; ++p) {
+      const float4 x0 = reinterpret_cast<const float4*>(src + p * stride_part)[0];
+      const float4 x1 = reinterpret_cast<const float4*>(src + p * stride_part)[1];
+      s0.x += x0.x; s0.y += x0.y; s0.z += x0.z; s0.w += x0.w;
+      s1.x += x1.x; s1.y += x1.y; s1.z += x1.z; s1.w += x1.w;
+    }
+    __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(w == 0 ? a.dv : a.dk) +
+                         (int64_t)b * (w == 0 ? a.v_sb : a.k_sb) +
+                         (int64_t)key * (w == 0 ? a.v_ss : a.k_ss) +
+                         (int64_t)g * (w == 0 ? a.v_sh : a.k_sh) + c * 8;
+    *reinterpret_cast<uint4*>(dst) = make_uint4(pack_bf16x2(s0.x, s0.y), pack_bf16x2(s0.z, s0.w),
+                                                pack_bf16x2(s1.x, s1.y), pack_bf16x2(s1.z, s1.w));
+  }
+}
+
 // ---------------------------------------------------------------------------
 // 2. dK / dV
 // ---------------------------------------------------------------------------
@@ -146,18 +176,19 @@ __device__ __forceinline__ int block_of(const int32_t* offs, int n, int x) {
   return lo;
 }
 
-// Iterates the (query head in group, list index) pairs of one CTA in order.
+// Iterates the (query head in group, list index) pairs of one CTA in order,
+// for the group's query heads [h_lo, h_hi).
 struct ItemIter {
   const int32_t* cnt_base;  // bwd_cnt for (b, list head 0), stride nKt per list head
   const int32_t* lst_base;
-  int nH, nKt, nQt, kt, G, g;
+  int nH, nKt, nQt, kt, G, g, hend;
   int hi, idx, cnt, cur;
-  __device__ void init(const TileMetaDev& t, int b, int kt_, int G_, int g_) {
-    nH = t.nH; nKt = t.nKt; nQt = t.nQt; kt = kt_; G = G_; g = g_;
+  __device__ void init(const TileMetaDev& t, int b, int kt_, int G_, int g_, int h_lo, int h_hi) {
+    nH = t.nH; nKt = t.nKt; nQt = t.nQt; kt = kt_; G = G_; g = g_; hend = h_hi;
     cnt_base = t.bwd_cnt + (int64_t)b * t.nH * t.nKt;
     lst_base = t.bwd_lst + (int64_t)b * t.nH * t.nKt * t.nQt;
-    hi = 0; idx = 0;
-    cnt = count_of(0);
+    hi = h_lo; idx = 0;
+    cnt = hi < hend ? count_of(hi) : 0;
     skip_empty();
   }
   __device__ int list_head(int hh) const { return nH == 1 ? 0 : g * G + hh; }
@@ -165,10 +196,10 @@ struct ItemIter {
   // Advances past empty lists and loads the entry at the new position early,
   // so the load overlaps the rest of the current iteration.
   __device__ void skip_empty() {
-    while (hi < G && idx >= cnt) { ++hi; idx = 0; if (hi < G) cnt = count_of(hi); }
-    if (hi < G) cur = __ldg(lst_base + ((int64_t)list_head(hi) * nKt + kt) * nQt + idx);
+    while (hi < hend && idx >= cnt) { ++hi; idx = 0; if (hi < hend) cnt = count_of(hi); }
+    if (hi < hend) cur = __ldg(lst_base + ((int64_t)list_head(hi) * nKt + kt) * nQt + idx);
   }
-  __device__ bool valid() const { return hi < G; }
+  __device__ bool valid() const { return hi < hend; }
   __device__ int entry() const { return cur; }
   __device__ int head() const { return g * G + hi; }
   __device__ void next() { ++idx; skip_empty(); }
@@ -200,9 +231,13 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
   const int b = blockIdx.z;
   const int g = blockIdx.y;
   // Longest key tiles first.  With per-head lists the order of the group's
-  // first head is used.
+  // first head is used.  With a split, the parts of one key tile (shares of
+  // the group's query heads) are adjacent CTAs.
+  const int parts = a.parts;
+  const int part = (int)(blockIdx.x % parts);
+  const int h_lo = part * pr.G / parts, h_hi = (part + 1) * pr.G / parts;
   const int lh0 = a.meta.nH == 1 ? 0 : g * pr.G;
-  const int kt = __ldg(a.meta.bwd_ord + ((int64_t)b * a.meta.nH + lh0) * a.meta.nKt + blockIdx.x);
+  const int kt = __ldg(a.meta.bwd_ord + ((int64_t)b * a.meta.nH + lh0) * a.meta.nKt + blockIdx.x / parts);
 
   if (tid == 0) {
     mbar_init(&sm.kv_full, 1);
@@ -246,7 +281,7 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
     tma_load_4d_e(sm.v, &tmV, &sm.kv_full, 0, g, kt * kBN, b);
     tma_load_4d_e(sm.v + kHalfBytes, &tmV, &sm.kv_full, 64, g, kt * kBN, b);
     ItemIter it;
-    it.init(a.meta, b, kt, pr.G, g);
+    it.init(a.meta, b, kt, pr.G, g, h_lo, h_hi);
     int i = 0, issued = 0;
     for (; it.valid(); it.next(), ++i) {
       const int st = i & 1, use = i >> 1;
@@ -309,7 +344,7 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
       const uint64_t dS_mn = sdesc_sw128(smem_u32(sm.ds), kHalfBytes, 1024);
       bool ok = __all_sync(0xffffffffu, mbar_wait(&sm.kv_full, 0, abort_flag, gstatus, TO));
       ItemIter it;
-      it.init(a.meta, b, kt, pr.G, g);
+      it.init(a.meta, b, kt, pr.G, g, h_lo, h_hi);
       // Both operands K-major: 16-column steps inside a 64-column half, then the next half.
       auto issue_kmaj = [&](uint32_t d, uint64_t a0, uint64_t b0) {
         mma_ss_e<0>(d, a0, b0, id_kmaj);
@@ -398,7 +433,7 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
     const uint32_t tQ = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16) + 128;
     const int64_t dq_row_stride = (int64_t)pr.Hq * kD;
     ItemIter it;
-    it.init(a.meta, b, kt, pr.G, g);
+    it.init(a.meta, b, kt, pr.G, g, h_lo, h_hi);
     for (int i = 0; it.valid(); it.next(), ++i) {
       const int qt = it.entry() >> 1;
       const int h = it.head();
@@ -445,7 +480,7 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
       else kb = block_of(a.mask.k_offs, a.mask.nKb, key);
     }
     ItemIter it;
-    it.init(a.meta, b, kt, pr.G, g);
+    it.init(a.meta, b, kt, pr.G, g, h_lo, h_hi);
     int i = 0;
     bool ok = true;
     for (; it.valid(); it.next(), ++i) {
@@ -587,6 +622,9 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
       }
       const float mul = x == 0 ? 1.f / a.scale : 1.f;
       const uint32_t tacc = tmem + lane_off + (x == 0 ? 256 : 384);
+      // Split units write fp32 partials [part][dV, dK][B][Sk][Hkv][128]; a
+      // reduction kernel sums the parts into the bf16 outputs.
+      float* pdst = a.dkv_part + (((((int64_t)part * 2 + x) * pr.B + b) * pr.Sk + key) * pr.Hkv + g) * kD;
       __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(x == 0 ? a.dv : a.dk) +
                            (int64_t)b * (x == 0 ? a.v_sb : a.k_sb) +
                            (int64_t)key * (x == 0 ? a.v_ss : a.k_ss) +
@@ -601,7 +639,13 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
           #pragma unroll
           for (int k = 0; k < 32; ++k) xr[k] = 0u;
         }
-        if (key_ok) {
+        if (key_ok && parts > 1) {
+          float4* p4 = reinterpret_cast<float4*>(pdst + c * 32);
+          #pragma unroll
+          for (int u = 0; u < 8; ++u)
+            p4[u] = make_float4(__uint_as_float(xr[4 * u]) * mul, __uint_as_float(xr[4 * u + 1]) * mul,
+                                __uint_as_float(xr[4 * u + 2]) * mul, __uint_as_float(xr[4 * u + 3]) * mul);
+        } else if (key_ok) {
           uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
           #pragma unroll
           for (int u = 0; u < 4; ++u)
@@ -649,8 +693,17 @@ cudaError_t launch_bwd_dkdv(const CUtensorMap& tq, const CUtensorMap& tk, const 
   }
   BwdKernelArgs ka;
   ka.a = a;
-  dim3 grid(a.meta.nKt, a.pr.Hkv, a.pr.B);
+  dim3 grid(a.meta.nKt * a.parts, a.pr.Hkv, a.pr.B);
   dkdv_kernel<<<grid, kThreadsDkdv, smem, st>>>(tq, tk, tv, tdo, ka);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess || a.parts == 1) return e;
+  int dev = 0, nsm = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
+  const int64_t n = 2 * (int64_t)a.pr.B * a.pr.Sk * a.pr.Hkv * (kD / 8);
+  int64_t blocks = (n + 255) / 256;
+  if (blocks > (int64_t)nsm * 16) blocks = (int64_t)nsm * 16;
+  dkv_reduce_kernel<<<(unsigned)blocks, 256, 0, st>>>(a);
   return cudaGetLastError();
 }
 

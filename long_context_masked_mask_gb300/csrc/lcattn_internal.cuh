@@ -71,6 +71,8 @@ struct BwdArgs {
   const float* lse;
   float* dvec;   // D [B][Hq][Sq]
   float* dq_acc; // [B][Sq][Hq][128] fp32
+  int parts;       // dK/dV units split over this many shares of the GQA group's heads (1: none)
+  float* dkv_part; // parts > 1: fp32 partials [parts][dV, dK][B][Sk][Hkv][128]
   void* dq;
   int64_t q_sb, q_ss, q_sh;
   void* dk;

@@ -104,7 +104,12 @@ def test_calls_reject_bad_pointers_before_launch():
     st = lib.lcattn_mask_compile(ctypes.byref(s), ctypes.byref(d), 0x1000, 16, None)
     assert st == lc.LCATTN_ERR_WORKSPACE
     ws = lib.lcattn_bwd_workspace_size(ctypes.byref(s))
-    assert ws == 4 * 4 * 256 + 4 * 256 * 4 * 128
+    # D [B][Hq][Sq] + the dQ accumulator [B][Sq][Hq][128], fp32; this shape has
+    # 2 key tiles x 2 KV heads = 4 dK/dV units with GQA groups of 2, so the
+    # units are split over two head shares and the fp32 dK/dV partials
+    # [2][2][B][Sk][Hkv][128] follow.
+    assert (s.B, s.Sq, s.Sk, s.Hq, s.Hkv) == (1, 256, 256, 4, 2)
+    assert ws == 4 * 4 * 256 + 4 * 256 * 4 * 128 + 2 * 2 * 4 * 256 * 2 * 128
     st = lib.lcattn_bwd(ctypes.byref(s), *([0x1000] * 7), ctypes.byref(d), 0.1, 0x1000, 0x1000, 0x1000,
                         0x1000, ws - 1, None)
     assert st == lc.LCATTN_ERR_WORKSPACE
