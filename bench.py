@@ -368,20 +368,37 @@ def run_gpu(args, rank, world, dist):
             for r in runs]
     h2d = sum(t.numel() * t.element_size() for t in host.values())
     d2h = sum(t.numel() * t.element_size() for o in outs for t in o.values())
+    # Copies overlap compute the way a training loop would: dO goes up on a
+    # copy stream while the first forward runs, and each mask's results go down
+    # on it while the next mask computes.  Every byte still moves inside the
+    # timed region: e1 is recorded after the copy stream has been joined.
+    copy_stream = torch.cuda.Stream(device=dev)
     e2e_ms = []
     for i in range(args.warmup + args.e2e_steps):
         flush.zero_()
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
+        copy_stream.wait_stream(stream)
+        with torch.cuda.stream(copy_stream):
+            do_.copy_(host["do"], non_blocking=True)
+        do_ready = torch.cuda.Event()
+        do_ready.record(copy_stream)
         q_.copy_(host["q"], non_blocking=True)
         k_.copy_(host["k"], non_blocking=True)
         v_.copy_(host["v"], non_blocking=True)
-        do_.copy_(host["do"], non_blocking=True)
-        step(q_, k_, v_, do_)
-        for r, o in zip(runs, outs):
-            for n in o:
-                o[n].copy_(r[n], non_blocking=True)
+        for j, (r, o) in enumerate(zip(runs, outs)):
+            lc.lcattn_mask_compile(shape, r["mask"], r["meta"])
+            lc.lcattn_fwd(q_, k_, v_, r["mask"], r["meta"], o=r["o"], lse=r["lse"])
+            if j == 0:
+                stream.wait_event(do_ready)
+            lc.lcattn_bwd(q_, k_, v_, r["o"], do_, r["lse"], r["mask"], r["meta"],
+                          dq=r["dq"], dk=r["dk"], dv=r["dv"], workspace=ws)
+            copy_stream.wait_stream(stream)
+            with torch.cuda.stream(copy_stream):
+                for n in o:
+                    o[n].copy_(r[n], non_blocking=True)
+        stream.wait_stream(copy_stream)
         e1.record(stream)
         torch.cuda.synchronize()
         if i >= args.warmup:
@@ -392,7 +409,9 @@ def run_gpu(args, rank, world, dist):
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         e2e_t = float(t.item())
     e2e = {"value": world * step_flops / (e2e_t / 1e3) / 1e12, "unit": UNIT, "ms_per_step": e2e_t,
-           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+           "copies": "pinned host buffers; dO and each mask's results move on a copy stream that "
+                     "overlaps compute; all copies inside the timed region"}
 
     for r in runs:
         st = lc.lcattn_read_status(r["meta"])
