@@ -70,6 +70,7 @@ struct FwdSmem {
 struct FwdKernelArgs {
   FwdArgs a;
   int heads_per_cta;
+  int head_block;  // one head per item: heads per block of the item order
   int total_items;
 };
 
@@ -155,14 +156,30 @@ struct FwdItem {
 };
 
 // idx < total_items < 2^31 (the launcher checks), so 32-bit arithmetic suffices.
-__device__ __forceinline__ FwdItem fwd_item(const FwdArgs& a, int hpc, int idx) {
-  const int groups = a.pr.Hq / hpc;
-  const int per_rank = groups * a.pr.B;
-  const int rank = idx / per_rank;
-  const int rem = idx - rank * per_rank;
+// Two heads per item: rank-major over every (batch, head pair), so the items
+// in flight share K/V through their KV group.  One head per item: items come
+// in blocks of `hb` heads (whole GQA groups) of one batch entry, rank-major
+// within a block; the items in flight then cover a few heads' K/V, which stays
+// in L2 (with MHA every head has its own K/V, far more than L2 holds).
+__device__ __forceinline__ FwdItem fwd_item(const FwdArgs& a, int hpc, int hb, int idx) {
   FwdItem it;
-  it.b = rem / groups;
-  it.h0 = (rem - it.b * groups) * hpc;
+  int rank;
+  if (hpc == 1) {
+    const int per_block = hb * a.meta.nQt;
+    const int blk = idx / per_block;
+    const int r = idx - blk * per_block;
+    rank = r / hb;
+    const int nb = a.pr.Hq / hb;  // blocks per batch entry
+    it.b = blk / nb;
+    it.h0 = (blk - it.b * nb) * hb + (r - rank * hb);
+  } else {
+    const int groups = a.pr.Hq / hpc;
+    const int per_rank = groups * a.pr.B;
+    rank = idx / per_rank;
+    const int rem = idx - rank * per_rank;
+    it.b = rem / groups;
+    it.h0 = (rem - it.b * groups) * hpc;
+  }
   const int lh = a.meta.nH == 1 ? 0 : it.h0;
   const int64_t lbase = ((int64_t)it.b * a.meta.nH + lh) * a.meta.nQt;
   it.qt = __ldg(a.meta.fwd_ord + lbase + rank);
@@ -181,6 +198,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
   const ProblemDev& pr = a.pr;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int hpc = ka.heads_per_cta;
+  const int hb = ka.head_block;
   const int total = ka.total_items;
   int32_t* gstatus = a.meta.status;
 
@@ -270,11 +288,11 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
       if (!publish(cur)) { ok = false; break; }
       if (cur < 0) break;
       const int nxt = fetch();
-      const FwdItem it = fwd_item(a, hpc, cur);
+      const FwdItem it = fwd_item(a, hpc, hb, cur);
       cur = nxt;
       if (nxt >= 0) {
         // Warm L2 with the next item's query rows while this item runs.
-        const FwdItem nx = fwd_item(a, hpc, nxt);
+        const FwdItem nx = fwd_item(a, hpc, hb, nxt);
         if (nx.n > 0)
           for (int s = 0; s < hpc; ++s) {
             tma_prefetch_l2_4d_e(&tmQ, 0, nx.h0 + s, nx.qt * kBM, nx.b);
@@ -404,7 +422,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
           __syncwarp();
           if (lane == 0) mbar_arrive(&sm.item_empty[e]);
           if (idx < 0) break;
-          const int n = fwd_item(a, hpc, idx).n;
+          const int n = fwd_item(a, hpc, hb, idx).n;
           if (n == 0) continue;
           const int qb = nq & 1;
           ok = __all_sync(0xffffffffu, mbar_wait(&sm.q_full[qb], (nq >> 1) & 1, abort_flag, gstatus,
@@ -446,7 +464,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm.item_empty[e]);
         if (idx < 0) break;
-        const int n = fwd_item(a, hpc, idx).n;
+        const int n = fwd_item(a, hpc, hb, idx).n;
         if (n == 0) continue;
         for (int j = 0; j < n; ++j, ++T) {
           const int tk = 2 * T, tv = 2 * T - 1;
@@ -528,7 +546,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm.item_empty[e]);
         if (idx < 0) break;
-        const FwdItem it = fwd_item(a, hpc, idx);
+        const FwdItem it = fwd_item(a, hpc, hb, idx);
         const int n = it.n, b = it.b;
         const int h = it.h0 + s;
         const int row = it.qt * kBM + r;
@@ -671,21 +689,28 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
           const float inv = live ? 1.f / l_run : 0.f;
           __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(a.o) + (int64_t)b * a.o_sb +
                                 (int64_t)row * a.o_ss + (int64_t)h * a.o_sh;
+          // All 128 columns of O in one round trip, then O / l on column pairs.
+          uint32_t o32[128];
+          if (have_o) {
+            tmem_ld32(tO, o32);
+            tmem_ld32(tO + 32, o32 + 32);
+            tmem_ld32(tO + 64, o32 + 64);
+            tmem_ld32(tO + 96, o32 + 96);
+            tmem_ld_wait();
+          } else {
+            #pragma unroll
+            for (int i = 0; i < 128; ++i) o32[i] = 0u;
+          }
+          const float2 inv2 = make_float2(inv, inv);
           #pragma unroll
           for (int c = 0; c < 4; ++c) {
-            uint32_t o32[32];
-            if (have_o) {
-              tmem_ld32(tO + c * 32, o32);
-              tmem_ld_wait();
-            } else {
-              #pragma unroll
-              for (int i = 0; i < 32; ++i) o32[i] = 0u;
-            }
             uint32_t pk[16];
             #pragma unroll
-            for (int i = 0; i < 16; ++i)
-              pk[i] = pack_bf16x2(__uint_as_float(o32[2 * i]) * inv,
-                                  __uint_as_float(o32[2 * i + 1]) * inv);
+            for (int i = 0; i < 16; ++i) {
+              const float2 y = mul2(make_float2(__uint_as_float(o32[c * 32 + 2 * i]),
+                                                __uint_as_float(o32[c * 32 + 2 * i + 1])), inv2);
+              pk[i] = pack_bf16x2(y.x, y.y);
+            }
             if (row < pr.Sq) {
               uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
               #pragma unroll
@@ -733,6 +758,11 @@ cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
   ka.a = a;
   // Two query heads per CTA when they share the key tiles and the tile list.
   ka.heads_per_cta = (a.meta.nH == 1 && a.pr.G % 2 == 0) ? 2 : 1;
+  // One head per item: the smallest block of whole GQA groups (a divisor of Hq)
+  // whose items fill the GPU twice over.
+  ka.head_block = a.pr.Hq;
+  for (int d = a.pr.G; d <= a.pr.Hq; d += a.pr.G)
+    if (a.pr.Hq % d == 0 && (int64_t)d * a.meta.nQt >= 2 * (int64_t)nsm) { ka.head_block = d; break; }
   const int64_t total = (int64_t)(a.pr.Hq / ka.heads_per_cta) * a.pr.B * a.meta.nQt;
   if (total > 0x7fffffffLL) return cudaErrorInvalidValue;  // far beyond any problem that fits in memory
   ka.total_items = static_cast<int>(total);
