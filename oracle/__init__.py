@@ -16,17 +16,23 @@ formula, so the oracle writes out the textbook definition:
     LSE_i = log sum_{j allowed} exp(S_ij)
 
 and its gradients for L = <O, dO>.  Mask predicates are the plain readings of
-the mask names (see ``masks_ref``).
+the mask names (see ``masks_ref``).  ``block_select_ref`` writes out the step
+that produces a dynamic block map -- TopK / TopP selection of key blocks from
+pooled Q K^T scores, the criterion the paper's peer reviews name (tomesphere
+page, section "Peer Reviews") -- under the readings stated in its docstring.
 
 Pins (tests/test_oracle_*.py): torch's own fp64 scaled_dot_product_attention
 and autograd on tiny cases, central finite differences, closed forms (N = 1,
-uniform keys), row sums, hand-derived small masks in ``tests/golden``, and the
-invariants between mask families.  Every function here is pinned; none is
+uniform keys), row sums, hand-derived small masks and block selections in
+``tests/golden``, brute force over every subset for TopK / TopP, the
+bilinearity identity for pooled scores, and the invariants between mask
+families and selection parameters.  Every function here is pinned; none is
 "parity unpinned".
 """
+from . import block_select_ref
 from .masks_ref import allowed, allowed_pairs
 from .attention_ref import (attention_fwd, attention_bwd, attention_fwd_rows,
                             attention_bwd_sampled, classify_tiles, EMPTY, FULL, PARTIAL)
 
-__all__ = ["allowed", "allowed_pairs", "attention_fwd", "attention_bwd", "attention_fwd_rows",
+__all__ = ["block_select_ref", "allowed", "allowed_pairs", "attention_fwd", "attention_bwd", "attention_fwd_rows",
            "attention_bwd_sampled", "classify_tiles", "EMPTY", "FULL", "PARTIAL"]

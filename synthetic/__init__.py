@@ -122,6 +122,32 @@ def qkv_device(B: int, N: int, Hq: int, Hkv: int, D: int = 128, seed: int = 0,
     return {"q": mk(N, Hq), "k": mk(N, Hkv), "v": mk(N, Hkv), "do": mk(N, Hq)}
 
 
+def qkv_block_structured(B: int, N: int, Hq: int, Hkv: int, block: int, strength: float = 1.0,
+                         D: int = 128, seed: int = 0, device: str = "cpu") -> Dict[str, torch.Tensor]:
+    """Q, K, V, dO in [B, S, H, D] bf16 whose Q and K rows share a direction per
+    block of ``block`` positions.
+
+    Row r of query head h is N(0, I) noise plus ``strength`` * u[b, r // block, h],
+    and row r of KV head g is noise plus ``strength`` * w[b, r // block, g], with u
+    and w drawn N(0, I) once per block; V and dO are i.i.d. N(0, 1).  Draw order:
+    noise Q, K, V, dO, then u, w, all from one ``torch.Generator`` seeded with
+    ``seed`` on ``device``.  The dynamic sparse masks of the pages are chosen from
+    real activations, whose block averages differ from block to block; with
+    i.i.d. rows every pooled score would be close to zero and the selection close
+    to arbitrary, so the shared per-block direction stands in for that structure.
+    """
+    g = torch.Generator(device=device).manual_seed(seed)
+    mk = lambda *shape: torch.randn(*shape, generator=g, device=device, dtype=torch.float32)
+    q, k, v, do = mk(B, N, Hq, D), mk(B, N, Hkv, D), mk(B, N, Hkv, D), mk(B, N, Hq, D)
+    nb = (N + block - 1) // block
+    u, w = mk(B, nb, Hq, D), mk(B, nb, Hkv, D)
+    rows = torch.arange(N, device=device) // block
+    q += strength * u[:, rows]
+    k += strength * w[:, rows]
+    return {"q": q.to(torch.bfloat16), "k": k.to(torch.bfloat16), "v": v.to(torch.bfloat16),
+            "do": do.to(torch.bfloat16)}
+
+
 # --------------------------------------------------------------------------
 # Random structure for the masks
 # --------------------------------------------------------------------------

@@ -8,7 +8,10 @@ on the oracle's arithmetic to fail:
 
 * the hand-derived golden masks and tile classes under ``tests/golden``;
 * torch's fp64 ``scaled_dot_product_attention`` with autograd, on a small GQA
-  case that also has fully-masked query rows and several row chunks.
+  case that also has fully-masked query rows and several row chunks;
+* for the block selection: the hand-derived maps of ``select_small.json``,
+  brute force over subsets, the pooled-score identity and the causal rule
+  checked position by position (``test_oracle_block_select``).
 
 The mutants exist only in this test process; the oracle files are not touched.
 """
@@ -191,3 +194,37 @@ TILE_MUTANTS = [
 @pytest.mark.parametrize("name,old,new", TILE_MUTANTS, ids=[m[0] for m in TILE_MUTANTS])
 def test_golden_tiles_reject_tile_mutant(name, old, new):
     assert not golden_tiles_hold(mutant(attention_ref, old, new))
+
+
+# ---- block selection (TopK / TopP over pooled Q K^T) ------------------------
+import oracle.block_select_ref as block_select_ref  # noqa: E402
+from test_oracle_block_select import select_pins_hold  # noqa: E402
+
+
+def test_select_pins_accept_the_oracle():
+    assert select_pins_hold(block_select_ref)
+
+
+SELECT_MUTANTS = [
+    ("sum_pool", ".mean(axis=1)", ".sum(axis=1)", 0),
+    ("first_row_pool", "x[:, lo:hi, :, :].astype(np.float64).mean(axis=1)",
+     "x[:, lo, :, :].astype(np.float64)", 0),
+    ("block_end_off_by_one", "offs[i + 1])", "offs[i + 1]) - 1", 0),
+    ("gqa_modulo", "kb[:, h // G]", "kb[:, h % Hkv]", 0),
+    ("scale_dropped", "scale * np.einsum", "np.einsum", 0),
+    ("causal_le", "k_offs[:-1][None, :] < q_offs[1:][:, None]", "k_offs[:-1][None, :] <= q_offs[1:][:, None]", 0),
+    ("causal_query_start", "k_offs[:-1][None, :] < q_offs[1:][:, None]", "k_offs[:-1][None, :] < q_offs[:-1][:, None]", 0),
+    ("empty_key_block_kept", "c = q_nonempty[:, None] & k_nonempty[None, :]",
+     "c = q_nonempty[:, None] & np.ones_like(k_nonempty)[None, :]", 0),
+    ("rank_ascending", "np.lexsort((idx, -s))", "np.lexsort((idx, s))", 0),
+    ("tie_larger_index", "np.lexsort((idx, -s))", "np.lexsort((-idx, -s))", 0),
+    ("topk_off_by_one", "[:max(int(k), 0)]", "[:max(int(k) + 1, 0)]", 0),
+    ("topp_le", "mass_before < p", "mass_before <= p", 0),
+    ("topp_inclusive_mass", "np.concatenate([[0.0], np.cumsum(prob)[:-1]])", "np.cumsum(prob)", 0),
+    ("topp_unnormalised", "prob = e / e.sum()", "prob = e", 0),
+]
+
+
+@pytest.mark.parametrize("name,old,new,occ", SELECT_MUTANTS, ids=[m[0] for m in SELECT_MUTANTS])
+def test_select_pins_reject_mutant(name, old, new, occ):
+    assert not select_pins_hold(mutant(block_select_ref, old, new, occ))
