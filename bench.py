@@ -61,9 +61,26 @@ def peaks():
     return {"burst": 1900.0, "sustained": 1700.0, "hbm_gbs": 6800.0, "source": "fallback"}
 
 
+def mask_labels(wl):
+    return "+".join([s.label() for s in wl.masks] + [s.label() for s in wl.selects])
+
+
 def workload_desc(wl):
-    return (f"{wl.name}: B={wl.B}, N={wl.N}, Hq:Hkv={wl.Hq}:{wl.Hkv}, hd={wl.D}, bf16, masks "
-            + "+".join(s.label() for s in wl.masks))
+    desc = (f"{wl.name}: B={wl.B}, N={wl.N}, Hq:Hkv={wl.Hq}:{wl.Hkv}, hd={wl.D}, bf16, masks "
+            + mask_labels(wl))
+    if wl.selects:
+        desc += (f" (dynamic masks selected every step from block-structured Q/K, strength "
+                 f"{wl.structure:g}; the selection runs inside the step)")
+    return desc
+
+
+def offsets_uniform(N, block):
+    import numpy as np
+    return np.array(list(range(0, N, block)) + [N], dtype=np.int32)
+
+
+def select_kw(sel):
+    return {"top_k": sel.top_k} if sel.rule == "topk" else {"top_p": sel.top_p}
 
 
 # ----------------------------------------------------------------------------
@@ -74,17 +91,31 @@ def oracle_sample(wl, seed):
     """Inputs for the oracle sample: query head 0 with its KV head over the full
     sequence, every mask of the workload."""
     import numpy as np
-    from synthetic import qkv
-    x = qkv(1, wl.N, 1, 1, wl.D, seed=seed)
+    from synthetic import qkv, qkv_block_structured
+    if wl.structure > 0:
+        x = qkv_block_structured(1, wl.N, 1, 1, wl.selects[0].block, strength=wl.structure, seed=seed)
+    else:
+        x = qkv(1, wl.N, 1, 1, wl.D, seed=seed)
     return {k: t.double().numpy() for k, t in x.items()}
 
 
 def oracle_step(wl, sample):
     """One oracle pass over the sample; returns effective FLOPs of the sample."""
+    import numpy as np
     import oracle
+    from oracle import block_select_ref
+    from synthetic import MaskSpec
     flops = 0.0
     scale = 1.0 / math.sqrt(wl.D)
-    for spec in wl.masks:
+    specs = list(wl.masks)
+    for sel in wl.selects:  # the selection is part of the step, as on the GPU
+        offs = offsets_uniform(wl.N, sel.block)
+        keep, _ = block_select_ref.block_select(sample["q"], sample["k"], offs, offs, sel.rule, scale,
+                                                causal=sel.causal, **select_kw(sel))
+        specs.append(MaskSpec("VARIABLE_BLOCK", {"q_block_lens": np.diff(offs).tolist(),
+                                                 "k_block_lens": np.diff(offs).tolist(),
+                                                 "keep": keep[0].astype(bool)}))
+    for spec in specs:
         oracle.attention_bwd(sample["q"], sample["k"], sample["v"], sample["do"], spec, scale)
         pairs = oracle.allowed_pairs(spec, wl.N, head=0)
         flops += 4.0 * wl.D * pairs * 3.5
@@ -110,7 +141,7 @@ def cpu_baseline(wl, seed):
     return {"value": flops / dt / 1e12, "unit": UNIT, "cores": cpu_threads(), "kind": "oracle",
             "seconds": round(dt, 3),
             "sample": f"fp64 NumPy oracle fwd+bwd, query head 0 / KV head 0 of {wl.name} over the full "
-                      f"N={wl.N}, masks {'+'.join(s.label() for s in wl.masks)}; effective FLOPs of that head"}
+                      f"N={wl.N}, masks {mask_labels(wl)}; effective FLOPs of that head"}
 
 
 def run_reference(args, rank, world):
@@ -129,7 +160,7 @@ def run_reference(args, rank, world):
     ms = 1e3 * statistics.mean(times)
     value = flops / (ms / 1e3) / 1e12
     sample_desc = (f"query head 0 / KV head 0 of {wl.name} over the full N={wl.N}, "
-                   f"masks {'+'.join(s.label() for s in wl.masks)}")
+                   f"masks {mask_labels(wl)}")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
@@ -226,7 +257,7 @@ def traffic_lookup(kernel):
 def run_gpu(args, rank, world, dist):
     import torch
     import long_context_masked_mask_gb300 as lc
-    from synthetic import qkv, qkv_device, workload
+    from synthetic import qkv, qkv_block_structured, qkv_device, workload
 
     local = int(os.environ.get("LOCAL_RANK", "0"))
     torch.cuda.set_device(local)
@@ -234,7 +265,10 @@ def run_gpu(args, rank, world, dist):
     wl = workload(args.workload, args.seed)
     B, N, Hq, Hkv, D = wl.B, wl.N, wl.Hq, wl.Hkv, wl.D
     seed = args.seed + 1000 * rank
-    if wl.device_inputs:
+    if wl.structure > 0:
+        x = qkv_block_structured(B, N, Hq, Hkv, wl.selects[0].block, strength=wl.structure, seed=seed,
+                                 device=str(dev))
+    elif wl.device_inputs:
         x = qkv_device(B, N, Hq, Hkv, D, seed=seed, device=str(dev))
     else:
         x = {k: t.to(dev) for k, t in qkv(B, N, Hq, Hkv, D, seed=seed).items()}
@@ -251,13 +285,38 @@ def run_gpu(args, rank, world, dist):
                      "dq": torch.empty_like(q), "dk": torch.empty_like(k), "dv": torch.empty_like(v),
                      "fwd_flops": fwd_flops, "bwd_flops": 2.5 * fwd_flops,
                      "launches": (6 if spec.per_head else 5) + 1 + 3})
+    for sel in wl.selects:
+        offs = torch.from_numpy(offsets_uniform(N, sel.block)).to(dev)
+        bmap = torch.empty(B, Hq, offs.numel() - 1, offs.numel() - 1, dtype=torch.uint8, device=dev)
+        sws = torch.empty(lc.lcattn_block_select_workspace_size(q, k, lc.select_desc(
+            sel.rule, offs, offs, causal=sel.causal, **select_kw(sel))), dtype=torch.uint8, device=dev)
+        lc.lcattn_block_select(q, k, offs, offs, sel.rule, causal=sel.causal, block_map=bmap,
+                               workspace=sws, **select_kw(sel))
+        m = lc.DeviceMask.from_block_map(bmap, offs, offs)
+        meta = lc.lcattn_mask_compile(shape, m, device=dev)
+        # The inputs are fixed, so every step selects this same map (the
+        # selection is deterministic): its allowed pairs give the step's FLOPs.
+        fwd_flops = 4.0 * D * m.allowed_pairs
+        runs.append({"spec": sel, "sel": sel, "offs": offs, "sws": sws, "mask": m, "meta": meta,
+                     "o": torch.empty_like(q), "lse": torch.empty(B, Hq, N, dtype=torch.float32, device=dev),
+                     "dq": torch.empty_like(q), "dk": torch.empty_like(k), "dv": torch.empty_like(v),
+                     "fwd_flops": fwd_flops, "bwd_flops": 2.5 * fwd_flops,
+                     "launches": 2 + 6 + 1 + 3})
     step_flops = sum(r["fwd_flops"] + r["bwd_flops"] for r in runs)
     launches_per_step = sum(r["launches"] for r in runs)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
 
+    def select(r, qq, kk, stage=None):
+        sel = r["sel"]
+        lc.lcattn_block_select(qq, kk, r["offs"], r["offs"], sel.rule, causal=sel.causal,
+                               block_map=r["mask"].block_map, workspace=r["sws"], stage=stage,
+                               **select_kw(sel))
+
     def step(qq=q, kk=k, vv=v, dd=d_o):
         for r in runs:
+            if "sel" in r:
+                select(r, qq, kk)
             lc.lcattn_mask_compile(shape, r["mask"], r["meta"])
             lc.lcattn_fwd(qq, kk, vv, r["mask"], r["meta"], o=r["o"], lse=r["lse"])
             lc.lcattn_bwd(qq, kk, vv, r["o"], dd, r["lse"], r["mask"], r["meta"],
@@ -307,6 +366,10 @@ def run_gpu(args, rank, world, dist):
     pk = peaks()
     kernels = {"mask_compile": [0.0, 0.0, 0], "fwd_kernel": [0.0, 0.0, 0],
                "bwd_prepass": [0.0, 0.0, 0], "dkdv_kernel": [0.0, 0.0, 0], "dq_convert": [0.0, 0.0, 0]}
+    if wl.selects:
+        kernels["pool_kernel"] = [0.0, 0.0, 0]
+        kernels["select_kernel"] = [0.0, 0.0, 0]
+    select_roof = None
     per_mask = []
     reps = args.breakdown_reps
 
@@ -324,6 +387,24 @@ def run_gpu(args, rank, world, dist):
 
     for r in runs:
         m, meta = r["mask"], r["meta"]
+        t_sel = None
+        if "sel" in r:
+            t_pool = timed(lambda: select(r, q, k, stage=1))
+            t_pick = timed(lambda: select(r, q, k, stage=2))
+            t_sel = (t_pool, t_pick)
+            kernels["pool_kernel"][0] += t_pool
+            kernels["pool_kernel"][2] += 1
+            kernels["select_kernel"][0] += t_pick
+            kernels["select_kernel"][2] += 1
+            nb = r["offs"].numel() - 1
+            pool_bytes = (B * N * (Hq + Hkv) * D * q.element_size()       # Q and K read once
+                          + B * (Hq + Hkv) * nb * D * 4)                 # fp32 block means written
+            gbs = pool_bytes / (t_pool / 1e3) / 1e9
+            select_roof = {"kernel": "pool_kernel", "bound": "hbm", "achieved": round(gbs, 1),
+                           "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": round(gbs / pk["hbm_gbs"], 4),
+                           "algorithmic_bytes": pool_bytes,
+                           "peak_kind": f"{pk['source']} copy bandwidth",
+                           "traffic": (traffic_lookup("pool_kernel") or {}).get("bytes")}
         t_c = timed(lambda: lc.lcattn_mask_compile(shape, m, meta))
         t_f = timed(lambda: lc.lcattn_fwd(q, k, v, m, meta, o=r["o"], lse=r["lse"]))
         tb = []
@@ -345,6 +426,8 @@ def run_gpu(args, rank, world, dist):
                          "fwd_tflops": round(fwd_tf, 1), "bwd_tflops": round(bwd_tf, 1),
                          "fwd_frac_of_peak": round(fwd_tf / pk["sustained"], 4),
                          "bwd_frac_of_peak": round(bwd_tf / pk["sustained"], 4)})
+        if t_sel is not None:
+            per_mask[-1]["select_ms"] = [round(t_sel[0], 4), round(t_sel[1], 4)]
     dom = max(kernels, key=lambda n: kernels[n][0])
     t_dom, fl_dom, n_dom = kernels[dom]
     if fl_dom > 0:
@@ -388,6 +471,8 @@ def run_gpu(args, rank, world, dist):
         k_.copy_(host["k"], non_blocking=True)
         v_.copy_(host["v"], non_blocking=True)
         for j, (r, o) in enumerate(zip(runs, outs)):
+            if "sel" in r:
+                select(r, q_, k_)
             lc.lcattn_mask_compile(shape, r["mask"], r["meta"])
             lc.lcattn_fwd(q_, k_, v_, r["mask"], r["meta"], o=r["o"], lse=r["lse"])
             if j == 0:
@@ -434,6 +519,8 @@ def run_gpu(args, rank, world, dist):
             "kernel_ms": {n: round(v[0], 4) for n, v in kernels.items()},
             "roofline": roof, "e2e": e2e, "gpu_launches": launches_per_step * args.steps,
             "clocks": clocks}
+    if select_roof is not None:
+        line["roofline_select"] = select_roof
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl, args.seed)
     emit(line, args)

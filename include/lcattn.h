@@ -152,6 +152,73 @@ size_t lcattn_tile_meta_size(const lcattn_shape* shape, const lcattn_mask_desc* 
 int lcattn_mask_compile(const lcattn_shape* shape, const lcattn_mask_desc* mask,
                         void* tile_meta, size_t bytes, lcattn_stream_t stream);
 
+/* ---- dynamic block selection -------------------------------------------
+ * Builds the block map of a dynamic block-sparse mask from the activations:
+ * the selection step the paper's peer reviews name for dynamic block-sparse
+ * attention, blocks chosen by a TopK or a TopP criterion over pooled Q K^T
+ * (tomesphere page for "Long-Context Attention Benchmark", section "Peer
+ * Reviews"), producing the Uniform / Variable Block masks of the xllm-io blog
+ * (section "注意力掩码模式").  The pages do not write the criterion out; the
+ * library computes, for every batch b, query head h (KV head g = h / (Hq/Hkv))
+ * and query block i:
+ *   q_bar = mean of the query rows of block i (head h), k_bar[j] = mean of the
+ *   key rows of block j (head g); an empty block's mean is 0;
+ *   s[j] = scale * <q_bar, k_bar[j]>, written to `scores` when it is not NULL;
+ *   candidates: both blocks non-empty and, if `causal`, k_offs[j] < q_offs[i+1];
+ *   ranking: candidates by s descending, equal s by smaller j first;
+ *   TOPK keeps the first min(top_k, #candidates) of the ranking;
+ *   TOPP keeps a block while the softmax probability (over the candidates) of
+ *   the blocks ranked before it sums to less than top_p, i.e. the shortest
+ *   prefix of the ranking whose mass reaches top_p.
+ * Arithmetic: block means and scores in fp32 (bf16 inputs, fp32 sums); the
+ * TopK decision is exact on those fp32 scores; TopP's probabilities and
+ * running mass are fp32, so a block whose mass-before lies within about
+ * 1e-6 * #candidates of top_p may fall either way.                          */
+#define LCATTN_SELECT_TOPK 1
+#define LCATTN_SELECT_TOPP 2
+
+typedef struct lcattn_select_desc {
+  int32_t rule;    /* LCATTN_SELECT_TOPK or LCATTN_SELECT_TOPP                 */
+  int32_t top_k;   /* TOPK: key blocks kept per (batch, head, query block), >= 0 */
+  float top_p;     /* TOPP: mass threshold, finite; <= 0 keeps nothing, > 1 keeps
+                    * every candidate                                          */
+  int32_t causal;  /* 0 or 1 (see the candidate rule above)                    */
+  /* device int32 [nQb+1] / [nKb+1]: block boundaries, the same arrays the
+   * block-map descriptor takes.  Read clamped to [0, S] (block i covers
+   * [clamp(offs[i]), max(clamp(offs[i]), clamp(offs[i+1])))) so that no read
+   * leaves the tensors; offsets that are not nondecreasing from 0 to S give an
+   * unspecified map, and lcattn_mask_compile reports them for the map.      */
+  const int32_t* q_block_offs;
+  const int32_t* k_block_offs;
+  int32_t nQb;     /* 1 .. Sq                                                  */
+  int32_t nKb;     /* 1 .. min(Sk, LCATTN_SELECT_MAX_KB)                       */
+} lcattn_select_desc;
+
+#define LCATTN_SELECT_MAX_KB 16384
+
+/* Workspace (device bytes) lcattn_block_select needs: the fp32 block means
+ * q_bar [B][Hq][nQb][128] and k_bar [B][Hkv][nKb][128]; 0 for invalid input. */
+size_t lcattn_block_select_workspace_size(const lcattn_shape* shape, const lcattn_select_desc* sel);
+
+/* Block selection.  q [B][Sq][Hq][128] and k [B][Sk][Hkv][128] bf16 (device,
+ * strides from `shape`; v/o strides unused) -> block_map uint8 [B][Hq][nQb][nKb]
+ * (device, 1 = keep, 0 = drop; every byte written), ready for a block-map
+ * descriptor with the same offsets.  `scores` (device fp32 [B][Hq][nQb][nKb])
+ * is optional (NULL = not written).  `scale` > 0 is the softmax scale of the
+ * scores (use the attention's).  Two kernels run in order on `stream`: the
+ * block means (stage 1), then scores, ranking and selection (stage 2).     */
+int lcattn_block_select(const lcattn_shape* shape, const void* q, const void* k,
+                        const lcattn_select_desc* sel, float scale, uint8_t* block_map,
+                        float* scores, void* workspace, size_t workspace_bytes,
+                        lcattn_stream_t stream);
+
+/* One stage of lcattn_block_select, same arguments (1 = block means,
+ * 2 = scores and selection); any other stage returns LCATTN_ERR_INVALID_ARG. */
+int lcattn_block_select_stage(int stage, const lcattn_shape* shape, const void* q, const void* k,
+                              const lcattn_select_desc* sel, float scale, uint8_t* block_map,
+                              float* scores, void* workspace, size_t workspace_bytes,
+                              lcattn_stream_t stream);
+
 /* Forward.  q [B][Sq][Hq][128], k/v [B][Sk][Hkv][128] bf16 (device) ->
  * o [B][Sq][Hq][128] bf16 and lse [B][Hq][Sq] fp32 (natural log; -inf for a
  * row with no allowed key, whose O row is 0).  `tile_meta` must come from

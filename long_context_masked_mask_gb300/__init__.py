@@ -11,6 +11,7 @@ The functions carry the C names:
 * :func:`lcattn_fwd` -- O and LSE
 * :func:`lcattn_bwd` -- dQ, dK, dV
 * :func:`lcattn_read_status` -- device status words (bounded-wait expiry etc.)
+* :func:`lcattn_block_select` -- TopK / TopP block map from pooled Q K^T
 
 plus :class:`DeviceMask`, which uploads a host-built mask descriptor
 (see :mod:`.masks`).
@@ -44,6 +45,8 @@ LCATTN_NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024
 LCATTN_MASK_COLBOUNDS = 1
 LCATTN_MASK_BLOCKMAP = 2
 LCATTN_TILE_EMPTY, LCATTN_TILE_FULL, LCATTN_TILE_PARTIAL = 0, 1, 2
+LCATTN_SELECT_TOPK, LCATTN_SELECT_TOPP = 1, 2
+LCATTN_SELECT_MAX_KB = 16384
 BLOCK_M = BLOCK_N = 128
 
 # Every entry point include/lcattn.h declares.
@@ -51,6 +54,7 @@ EXPORTED = (
     "lcattn_tile_meta_layout_of", "lcattn_tile_meta_size", "lcattn_mask_compile", "lcattn_fwd",
     "lcattn_bwd_workspace_size", "lcattn_bwd", "lcattn_bwd_stage", "lcattn_read_status", "lcattn_clear_status",
     "lcattn_status_string", "lcattn_version", "lcattn_bwd_noalloc", "lcattn_selftest_wait_timeout",
+    "lcattn_block_select_workspace_size", "lcattn_block_select", "lcattn_block_select_stage",
 )
 
 
@@ -66,6 +70,12 @@ class lcattn_mask_desc(ctypes.Structure):
                 ("block_map", ctypes.c_void_p), ("q_block_offs", ctypes.c_void_p),
                 ("k_block_offs", ctypes.c_void_p), ("nQb", ctypes.c_int32), ("nKb", ctypes.c_int32),
                 ("row_bounds", ctypes.c_void_p)]
+
+
+class lcattn_select_desc(ctypes.Structure):
+    _fields_ = [("rule", ctypes.c_int32), ("top_k", ctypes.c_int32), ("top_p", ctypes.c_float),
+                ("causal", ctypes.c_int32), ("q_block_offs", ctypes.c_void_p),
+                ("k_block_offs", ctypes.c_void_p), ("nQb", ctypes.c_int32), ("nKb", ctypes.c_int32)]
 
 
 class lcattn_tile_meta_layout(ctypes.Structure):
@@ -89,6 +99,7 @@ def _load():
     P = ctypes.c_void_p
     S = ctypes.POINTER(lcattn_shape)
     M = ctypes.POINTER(lcattn_mask_desc)
+    SD = ctypes.POINTER(lcattn_select_desc)
     sig = {
         "lcattn_tile_meta_layout_of": (ctypes.c_int, [S, M, ctypes.POINTER(lcattn_tile_meta_layout)]),
         "lcattn_tile_meta_size": (ctypes.c_size_t, [S, M]),
@@ -105,6 +116,10 @@ def _load():
         "lcattn_selftest_wait_timeout": (ctypes.c_int, [P, P]),
         "lcattn_status_string": (ctypes.c_char_p, [ctypes.c_int]),
         "lcattn_version": (ctypes.c_int, []),
+        "lcattn_block_select_workspace_size": (ctypes.c_size_t, [S, SD]),
+        "lcattn_block_select": (ctypes.c_int, [S, P, P, SD, ctypes.c_float, P, P, P, ctypes.c_size_t, P]),
+        "lcattn_block_select_stage": (ctypes.c_int, [ctypes.c_int, S, P, P, SD, ctypes.c_float, P, P, P,
+                                                     ctypes.c_size_t, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -188,9 +203,38 @@ class DeviceMask:
                 self.row_bounds = torch.from_numpy(np.broadcast_to(rb, (B,) + rb.shape).copy()).to(device)
                 self.desc.row_bounds = self.row_bounds.data_ptr()
 
+    @classmethod
+    def from_block_map(cls, block_map: torch.Tensor, q_offs: torch.Tensor, k_offs: torch.Tensor):
+        """Block-map descriptor over device tensors the caller keeps alive: a uint8
+        map [B, Hq, nQb, nKb] (for example from :func:`lcattn_block_select`) and
+        int32 block offsets [nQb + 1], [nKb + 1]."""
+        if block_map.dtype != torch.uint8 or block_map.dim() != 4 or not block_map.is_contiguous():
+            raise ValueError("block_map must be a contiguous uint8 [B, Hq, nQb, nKb] tensor")
+        if q_offs.dtype != torch.int32 or k_offs.dtype != torch.int32:
+            raise ValueError("block offsets must be int32")
+        self = cls.__new__(cls)
+        self.spec = None
+        self.B, self.Hq = block_map.shape[0], block_map.shape[1]
+        self.N = None
+        self.block_map, self.q_offs, self.k_offs = block_map, q_offs, k_offs
+        self.desc = lcattn_mask_desc()
+        self.desc.kind = LCATTN_MASK_BLOCKMAP
+        self.desc.block_map = block_map.data_ptr()
+        self.desc.q_block_offs = q_offs.data_ptr()
+        self.desc.k_block_offs = k_offs.data_ptr()
+        self.desc.nQb = block_map.shape[2]
+        self.desc.nKb = block_map.shape[3]
+        self.pairs_per_batch = None
+        return self
+
     @property
     def allowed_pairs(self) -> int:
         """Allowed (query, key) pairs summed over batch and query heads."""
+        if self.pairs_per_batch is None:  # a device map: count its blocks' areas
+            qs = (self.q_offs[1:] - self.q_offs[:-1]).to(torch.float64)
+            ks = (self.k_offs[1:] - self.k_offs[:-1]).to(torch.float64)
+            area = (self.block_map.to(torch.float64) * qs[:, None] * ks[None, :]).sum()
+            return int(round(float(area)))
         return self.B * self.pairs_per_batch
 
 
@@ -286,6 +330,64 @@ def lcattn_bwd_noalloc(q, k, v, o, d_o, lse, mask: DeviceMask, tile_meta, scale:
                                    ctypes.byref(mask.desc), float(scale), dq.data_ptr(), dk.data_ptr(),
                                    dv.data_ptr(), _stream_ptr(stream)), "lcattn_bwd_noalloc")
     return dq, dk, dv
+
+
+def select_desc(rule: str, q_offs: torch.Tensor, k_offs: torch.Tensor, top_k: int = 0,
+                top_p: float = 0.0, causal: bool = False) -> lcattn_select_desc:
+    """lcattn_select_desc for ``rule`` in ("topk", "topp") over int32 device offsets."""
+    d = lcattn_select_desc()
+    d.rule = {"topk": LCATTN_SELECT_TOPK, "topp": LCATTN_SELECT_TOPP}[rule]
+    d.top_k = int(top_k)
+    d.top_p = float(top_p)
+    d.causal = 1 if causal else 0
+    if q_offs.dtype != torch.int32 or k_offs.dtype != torch.int32:
+        raise ValueError("block offsets must be int32")
+    d.q_block_offs = q_offs.data_ptr()
+    d.k_block_offs = k_offs.data_ptr()
+    d.nQb = q_offs.numel() - 1
+    d.nKb = k_offs.numel() - 1
+    return d
+
+
+def lcattn_block_select_workspace_size(q: torch.Tensor, k: torch.Tensor, sel: lcattn_select_desc) -> int:
+    shape = make_shape(q, k, k, q)
+    return int(_lib.lcattn_block_select_workspace_size(ctypes.byref(shape), ctypes.byref(sel)))
+
+
+def lcattn_block_select(q: torch.Tensor, k: torch.Tensor, q_offs: torch.Tensor, k_offs: torch.Tensor,
+                        rule: str, top_k: int = 0, top_p: float = 0.0, causal: bool = False,
+                        scale: Optional[float] = None, block_map: Optional[torch.Tensor] = None,
+                        scores: Optional[torch.Tensor] = None, want_scores: bool = False,
+                        workspace: Optional[torch.Tensor] = None, stream=None,
+                        stage: Optional[int] = None):
+    """Dynamic block selection (lcattn_block_select): returns (block_map uint8
+    [B, Hq, nQb, nKb], scores fp32 of the same shape or None).  With ``stage``
+    in (1, 2), runs only that stage (lcattn_block_select_stage)."""
+    for t in (q, k):
+        if t.dtype != torch.bfloat16:
+            raise TypeError("q and k must be bf16")
+    B, _, Hq, D = q.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    sel = select_desc(rule, q_offs, k_offs, top_k, top_p, causal)
+    shape = make_shape(q, k, k, q)
+    if block_map is None:
+        block_map = torch.empty(B, Hq, sel.nQb, sel.nKb, dtype=torch.uint8, device=q.device)
+    if scores is None and want_scores:
+        scores = torch.empty(B, Hq, sel.nQb, sel.nKb, dtype=torch.float32, device=q.device)
+    ws_bytes = int(_lib.lcattn_block_select_workspace_size(ctypes.byref(shape), ctypes.byref(sel)))
+    if ws_bytes == 0:
+        raise LcattnError(LCATTN_ERR_INVALID_ARG, "lcattn_block_select_workspace_size")
+    if workspace is None:
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device)
+    args = (ctypes.byref(shape), q.data_ptr(), k.data_ptr(), ctypes.byref(sel), float(scale),
+            block_map.data_ptr(), scores.data_ptr() if scores is not None else None,
+            workspace.data_ptr(), workspace.numel(), _stream_ptr(stream))
+    if stage is None:
+        _check(_lib.lcattn_block_select(*args), "lcattn_block_select")
+    else:
+        _check(_lib.lcattn_block_select_stage(int(stage), *args), f"lcattn_block_select_stage({stage})")
+    return block_map, scores
 
 
 def lcattn_read_status(tile_meta: torch.Tensor, stream=None) -> int:

@@ -350,6 +350,104 @@ int lcattn_bwd_noalloc(const lcattn_shape* shape, const void* q, const void* k, 
                  (size_t)LCATTN_NOALLOC_SCRATCH_BYTES, stream, /*allow_split=*/false);
 }
 
+}  // extern "C"
+
+namespace {
+
+int validate_select(const lcattn_shape* s, const lcattn_select_desc* d) {
+  int st = validate_shape(s);
+  if (st) return st;
+  if (!d || !d->q_block_offs || !d->k_block_offs) return LCATTN_ERR_INVALID_ARG;
+  if (d->rule == LCATTN_SELECT_TOPK) {
+    if (d->top_k < 0) return LCATTN_ERR_INVALID_ARG;
+  } else if (d->rule == LCATTN_SELECT_TOPP) {
+    if (!(d->top_p == d->top_p) || d->top_p > 3.0e38f || d->top_p < -3.0e38f)
+      return LCATTN_ERR_INVALID_ARG;  // NaN or infinite
+  } else {
+    return LCATTN_ERR_INVALID_ARG;
+  }
+  if (d->causal != 0 && d->causal != 1) return LCATTN_ERR_INVALID_ARG;
+  if (d->nQb < 1 || d->nKb < 1 || d->nQb > s->Sq || d->nKb > s->Sk) return LCATTN_ERR_INVALID_ARG;
+  if (d->nKb > LCATTN_SELECT_MAX_KB) return LCATTN_ERR_UNSUPPORTED;
+  // Grid sizes of the two kernels.
+  const int64_t slabs_q = (s->Hq + 7) / 8, slabs_k = (s->Hkv + 7) / 8;
+  if (s->B * (d->nQb * slabs_q + d->nKb * slabs_k) >= (int64_t(1) << 31)) return LCATTN_ERR_UNSUPPORTED;
+  if (s->B * s->Hq * (int64_t)d->nQb >= (int64_t(1) << 31)) return LCATTN_ERR_UNSUPPORTED;
+  return LCATTN_OK;
+}
+
+int64_t select_ws_bytes(const lcattn_shape* s, const lcattn_select_desc* d) {
+  return align_up(4 * kD * s->B * s->Hq * (int64_t)d->nQb, 256) +
+         align_up(4 * kD * s->B * s->Hkv * (int64_t)d->nKb, 256);
+}
+
+int select_run(unsigned stages, const lcattn_shape* shape, const void* q, const void* k,
+               const lcattn_select_desc* sel, float scale, uint8_t* block_map, float* scores,
+               void* workspace, size_t workspace_bytes, lcattn_stream_t stream) {
+  int st = validate_select(shape, sel);
+  if (st) return st;
+  if (!q || !k || !block_map || !workspace) return LCATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(workspace)) return LCATTN_ERR_UNSUPPORTED;
+  if (scores && (reinterpret_cast<uintptr_t>(scores) & 3u)) return LCATTN_ERR_UNSUPPORTED;
+  if (!(scale > 0.f) || !(scale < 1e30f)) return LCATTN_ERR_INVALID_ARG;
+  if ((int64_t)workspace_bytes < select_ws_bytes(shape, sel)) return LCATTN_ERR_WORKSPACE;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  float* qbar = reinterpret_cast<float*>(ws);
+  float* kbar = reinterpret_cast<float*>(ws + align_up(4 * kD * shape->B * shape->Hq * (int64_t)sel->nQb, 256));
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaSuccess;
+  if (stages & 1u) {
+    PoolSide qs, ks;
+    qs.x = static_cast<const uint16_t*>(q);
+    qs.sb = shape->q_stride[0]; qs.ss = shape->q_stride[1]; qs.sh = shape->q_stride[2];
+    qs.B = (int)shape->B; qs.S = (int)shape->Sq; qs.H = (int)shape->Hq; qs.nb = sel->nQb;
+    qs.slabs = (int)((shape->Hq + 7) / 8); qs.offs = sel->q_block_offs; qs.out = qbar;
+    ks.x = static_cast<const uint16_t*>(k);
+    ks.sb = shape->k_stride[0]; ks.ss = shape->k_stride[1]; ks.sh = shape->k_stride[2];
+    ks.B = (int)shape->B; ks.S = (int)shape->Sk; ks.H = (int)shape->Hkv; ks.nb = sel->nKb;
+    ks.slabs = (int)((shape->Hkv + 7) / 8); ks.offs = sel->k_block_offs; ks.out = kbar;
+    e = launch_block_pool(qs, ks, s);
+  }
+  if (e == cudaSuccess && (stages & 2u)) {
+    SelectArgs a;
+    a.qbar = qbar; a.kbar = kbar;
+    a.q_offs = sel->q_block_offs; a.k_offs = sel->k_block_offs;
+    a.B = (int)shape->B; a.Hq = (int)shape->Hq; a.G = (int)(shape->Hq / shape->Hkv);
+    a.nQb = sel->nQb; a.nKb = sel->nKb; a.Sq = (int)shape->Sq; a.Sk = (int)shape->Sk;
+    a.rule = sel->rule; a.top_k = sel->top_k; a.top_p = sel->top_p; a.causal = sel->causal;
+    a.scale = scale; a.map = block_map; a.scores = scores;
+    select_geometry(sel->nKb, &a.R, &a.n2);
+    e = launch_block_select(a, s);
+  }
+  return cuda_status(e);
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t lcattn_block_select_workspace_size(const lcattn_shape* shape, const lcattn_select_desc* sel) {
+  if (validate_select(shape, sel) != LCATTN_OK) return 0;
+  return (size_t)select_ws_bytes(shape, sel);
+}
+
+int lcattn_block_select(const lcattn_shape* shape, const void* q, const void* k,
+                        const lcattn_select_desc* sel, float scale, uint8_t* block_map,
+                        float* scores, void* workspace, size_t workspace_bytes,
+                        lcattn_stream_t stream) {
+  return select_run(3u, shape, q, k, sel, scale, block_map, scores, workspace, workspace_bytes,
+                    stream);
+}
+
+int lcattn_block_select_stage(int stage, const lcattn_shape* shape, const void* q, const void* k,
+                              const lcattn_select_desc* sel, float scale, uint8_t* block_map,
+                              float* scores, void* workspace, size_t workspace_bytes,
+                              lcattn_stream_t stream) {
+  if (stage < 1 || stage > 2) return LCATTN_ERR_INVALID_ARG;
+  return select_run(1u << (stage - 1), shape, q, k, sel, scale, block_map, scores, workspace,
+                    workspace_bytes, stream);
+}
+
 int lcattn_read_status(const void* tile_meta, lcattn_stream_t stream) {
   if (!tile_meta) return LCATTN_ERR_INVALID_ARG;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);

@@ -86,4 +86,33 @@ cudaError_t launch_bwd_dkdv(const CUtensorMap& tq, const CUtensorMap& tk, const 
 cudaError_t launch_bwd_dq_convert(const BwdArgs& a, cudaStream_t st);
 cudaError_t launch_selftest_wait_timeout(int32_t* status, cudaStream_t st);
 
+// ---- dynamic block selection (select.cu) ---------------------------------
+// One side (Q or K) of the block-mean pass.
+struct PoolSide {
+  const uint16_t* x;        // bf16 [B][S][H][128], element strides below
+  int64_t sb, ss, sh;
+  int B, S, H, nb, slabs;   // slabs = ceil(H / 8)
+  const int32_t* offs;      // [nb + 1], read clamped to [0, S]
+  float* out;               // [B][H][nb][128] block means
+};
+cudaError_t launch_block_pool(const PoolSide& qs, const PoolSide& ks, cudaStream_t st);
+
+struct SelectArgs {
+  const float* qbar;        // [B][Hq][nQb][128]
+  const float* kbar;        // [B][Hkv][nKb][128]
+  const int32_t* q_offs;
+  const int32_t* k_offs;
+  int B, Hq, G, nQb, nKb, Sq, Sk;
+  int rule, top_k;
+  float top_p;
+  int causal;
+  float scale;
+  uint8_t* map;             // [B][Hq][nQb][nKb]
+  float* scores;            // same shape, or null
+  int R, n2;                // query blocks per CTA; sort width (power of two >= nKb, >= 32)
+};
+void select_geometry(int nKb, int* R, int* n2);
+size_t select_smem_bytes(int R, int n2, int nKb);
+cudaError_t launch_block_select(const SelectArgs& a, cudaStream_t st);
+
 }  // namespace lcattn

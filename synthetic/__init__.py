@@ -199,6 +199,23 @@ def block_keep(Hq: int, nqb: int, nkb: int, p: float = 0.5, seed: int = 0,
 # --------------------------------------------------------------------------
 
 @dataclasses.dataclass
+class SelectSpec:
+    """A dynamic block mask chosen from the activations: TopK or TopP over pooled
+    Q K^T, with uniform blocks of ``block`` tokens (plain data; each side
+    interprets it on its own)."""
+
+    rule: str            # "topk" or "topp"
+    block: int = 128
+    top_k: int = 0
+    top_p: float = 0.0
+    causal: bool = False
+
+    def label(self) -> str:
+        crit = f"k{self.top_k}" if self.rule == "topk" else f"p{self.top_p:g}"
+        return f"{self.rule.upper()}_{crit}_b{self.block}{'_causal' if self.causal else ''}"
+
+
+@dataclasses.dataclass
 class Workload:
     name: str
     B: int
@@ -208,6 +225,8 @@ class Workload:
     D: int
     masks: List[MaskSpec]
     device_inputs: bool = False  # draw activations on the GPU (largest sizes only)
+    selects: List[SelectSpec] = dataclasses.field(default_factory=list)
+    structure: float = 0.0       # > 0: block-structured Q/K (qkv_block_structured strength)
 
 
 def workload(name: str, seed: int = 0) -> Workload:
@@ -220,6 +239,9 @@ def workload(name: str, seed: int = 0) -> Workload:
     * ``hetero_16k``: B=1, N=16384, MHA 64:64, the five heterogeneous masks.
     * ``long_128k``: B=1, N=131072, GQA 64:8, CAUSAL and a 128x128 uniform block
       mask kept with probability 0.5 per head (diagonal forced).
+    * ``dynamic_32k``: B=1, N=32768, GQA 64:8, block-structured Q/K (strength 1.5),
+      and two dynamic block masks chosen from them with 128-token blocks: TopK
+      with k = 32 of 256 key blocks, and causal TopP with p = 0.9.
     """
     if name == "causal_1k":
         return Workload(name, 1, 1024, 8, 8, 128, [MaskSpec("CAUSAL")])
@@ -246,7 +268,12 @@ def workload(name: str, seed: int = 0) -> Workload:
             MaskSpec("CAUSAL"),
             MaskSpec("UNIFORM_BLOCK", {"block": bs, "keep": block_keep(Hq, nb, nb, 0.5, seed)}),
         ], device_inputs=True)
+    if name == "dynamic_32k":
+        return Workload(name, 1, 32768, 64, 8, 128, [],
+                        selects=[SelectSpec("topk", 128, top_k=32),
+                                 SelectSpec("topp", 128, top_p=0.9, causal=True)],
+                        structure=1.5)
     raise KeyError(name)
 
 
-WORKLOADS = ("causal_1k", "dense_8k", "docs_32k", "hetero_16k", "long_128k")
+WORKLOADS = ("causal_1k", "dense_8k", "docs_32k", "hetero_16k", "long_128k", "dynamic_32k")

@@ -120,3 +120,52 @@ def test_status_strings():
         assert lc.status_string(code) not in ("", "unknown status")
     assert lc.status_string(-99) == "unknown status"
     assert lc.library().lcattn_version() >= 100
+
+
+def _select_desc(rule=1, top_k=4, top_p=0.9, causal=0, nQb=2, nKb=2, ptr=0x1000):
+    d = lc.lcattn_select_desc()
+    d.rule, d.top_k, d.top_p, d.causal = rule, top_k, top_p, causal
+    d.q_block_offs = ptr
+    d.k_block_offs = ptr
+    d.nQb, d.nKb = nQb, nKb
+    return d
+
+
+def test_block_select_workspace_and_validation():
+    lib = lc.library()
+    s = _shape(B=2, S=256, Hq=4, Hkv=2)
+    ws = lib.lcattn_block_select_workspace_size(ctypes.byref(s), ctypes.byref(_select_desc(nQb=3, nKb=5)))
+    # fp32 block means: q_bar [2][4][3][128], k_bar [2][2][5][128], each 256-aligned
+    assert ws == 4 * 128 * 2 * 4 * 3 + 4 * 128 * 2 * 2 * 5
+    bad = [
+        (_select_desc(rule=3), lc.LCATTN_ERR_INVALID_ARG),
+        (_select_desc(top_k=-1), lc.LCATTN_ERR_INVALID_ARG),
+        (_select_desc(rule=2, top_p=float("nan")), lc.LCATTN_ERR_INVALID_ARG),
+        (_select_desc(rule=2, top_p=float("inf")), lc.LCATTN_ERR_INVALID_ARG),
+        (_select_desc(causal=2), lc.LCATTN_ERR_INVALID_ARG),
+        (_select_desc(nQb=0), lc.LCATTN_ERR_INVALID_ARG),
+        (_select_desc(nKb=257), lc.LCATTN_ERR_INVALID_ARG),
+        (_select_desc(ptr=0), lc.LCATTN_ERR_INVALID_ARG),
+    ]
+    for d, status in bad:
+        assert lib.lcattn_block_select_workspace_size(ctypes.byref(s), ctypes.byref(d)) == 0
+        st = lib.lcattn_block_select(ctypes.byref(s), 0x1000, 0x1000, ctypes.byref(d), 0.1, 0x1000,
+                                     None, 0x1000, 1 << 30, None)
+        assert st == status, (d.rule, d.top_k, d.top_p, d.causal, d.nQb, d.nKb)
+    big = _shape(S=1 << 20, Hq=1, Hkv=1)
+    assert lib.lcattn_block_select(ctypes.byref(big), 0x1000, 0x1000,
+                                   ctypes.byref(_select_desc(nKb=lc.LCATTN_SELECT_MAX_KB + 1)), 0.1,
+                                   0x1000, None, 0x1000, 1 << 40, None) == lc.LCATTN_ERR_UNSUPPORTED
+    good = _select_desc()
+    assert lib.lcattn_block_select(ctypes.byref(s), 0x1001, 0x1000, ctypes.byref(good), 0.1, 0x1000,
+                                   None, 0x1000, 1 << 30, None) == lc.LCATTN_ERR_UNSUPPORTED
+    assert lib.lcattn_block_select(ctypes.byref(s), 0x1000, 0x1000, ctypes.byref(good), 0.1, 0x1000,
+                                   0x1002, 0x1000, 1 << 30, None) == lc.LCATTN_ERR_UNSUPPORTED
+    assert lib.lcattn_block_select(ctypes.byref(s), 0x1000, 0x1000, ctypes.byref(good), 0.0, 0x1000,
+                                   None, 0x1000, 1 << 30, None) == lc.LCATTN_ERR_INVALID_ARG
+    assert lib.lcattn_block_select(ctypes.byref(s), 0x1000, 0x1000, ctypes.byref(good), 0.1, 0x1000,
+                                   None, 0x1000, 16, None) == lc.LCATTN_ERR_WORKSPACE
+    for stage in (0, 3):
+        assert lib.lcattn_block_select_stage(stage, ctypes.byref(s), 0x1000, 0x1000, ctypes.byref(good),
+                                             0.1, 0x1000, None, 0x1000, 1 << 30, None) == \
+            lc.LCATTN_ERR_INVALID_ARG
