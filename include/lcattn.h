@@ -197,7 +197,8 @@ typedef struct lcattn_select_desc {
 #define LCATTN_SELECT_MAX_KB 16384
 
 /* Workspace (device bytes) lcattn_block_select needs: the fp32 block means
- * q_bar [B][Hq][nQb][128] and k_bar [B][Hkv][nKb][128]; 0 for invalid input. */
+ * q_bar [B][Hq][nQb][128] and k_bar [B][Hkv][128][nKb] (transposed), each
+ * 256-byte aligned; 0 for invalid input.                                    */
 size_t lcattn_block_select_workspace_size(const lcattn_shape* shape, const lcattn_select_desc* sel);
 
 /* Block selection.  q [B][Sq][Hq][128] and k [B][Sk][Hkv][128] bf16 (device,

@@ -402,10 +402,12 @@ int select_run(unsigned stages, const lcattn_shape* shape, const void* q, const 
     qs.sb = shape->q_stride[0]; qs.ss = shape->q_stride[1]; qs.sh = shape->q_stride[2];
     qs.B = (int)shape->B; qs.S = (int)shape->Sq; qs.H = (int)shape->Hq; qs.nb = sel->nQb;
     qs.slabs = (int)((shape->Hq + 7) / 8); qs.offs = sel->q_block_offs; qs.out = qbar;
+    qs.transposed = 0;
     ks.x = static_cast<const uint16_t*>(k);
     ks.sb = shape->k_stride[0]; ks.ss = shape->k_stride[1]; ks.sh = shape->k_stride[2];
     ks.B = (int)shape->B; ks.S = (int)shape->Sk; ks.H = (int)shape->Hkv; ks.nb = sel->nKb;
     ks.slabs = (int)((shape->Hkv + 7) / 8); ks.offs = sel->k_block_offs; ks.out = kbar;
+    ks.transposed = 1;
     e = launch_block_pool(qs, ks, s);
   }
   if (e == cudaSuccess && (stages & 2u)) {

@@ -93,13 +93,14 @@ struct PoolSide {
   int64_t sb, ss, sh;
   int B, S, H, nb, slabs;   // slabs = ceil(H / 8)
   const int32_t* offs;      // [nb + 1], read clamped to [0, S]
-  float* out;               // [B][H][nb][128] block means
+  float* out;               // block means, [B][H][nb][128] or (transposed) [B][H][128][nb]
+  int transposed;
 };
 cudaError_t launch_block_pool(const PoolSide& qs, const PoolSide& ks, cudaStream_t st);
 
 struct SelectArgs {
   const float* qbar;        // [B][Hq][nQb][128]
-  const float* kbar;        // [B][Hkv][nKb][128]
+  const float* kbar;        // [B][Hkv][128][nKb]
   const int32_t* q_offs;
   const int32_t* k_offs;
   int B, Hq, G, nQb, nKb, Sq, Sk;

@@ -27,14 +27,16 @@ __device__ __forceinline__ int block_of(const int32_t* offs, int n, int x) {
   return lo;
 }
 
-// Checks that block offsets run nondecreasing from 0 to S.
+// Checks that block offsets run nondecreasing from 0 to S (one CTA; each
+// thread checks a strided share of the adjacent pairs).
 __global__ void validate_offsets_kernel(MaskDev m, int Sq, int Sk, int32_t* status) {
-  if (threadIdx.x != 0 || blockIdx.x != 0) return;
-  bool ok = m.nQb > 0 && m.nKb > 0 && m.q_offs[0] == 0 && m.k_offs[0] == 0 &&
-            m.q_offs[m.nQb] == Sq && m.k_offs[m.nKb] == Sk;
-  for (int i = 0; ok && i < m.nQb; ++i) ok = m.q_offs[i] <= m.q_offs[i + 1];
-  for (int i = 0; ok && i < m.nKb; ++i) ok = m.k_offs[i] <= m.k_offs[i + 1];
-  if (!ok) atomicCAS(status, 0, LCATTN_ERR_DEVICE_MASK);
+  bool ok = true;
+  if (threadIdx.x == 0)
+    ok = m.nQb > 0 && m.nKb > 0 && m.q_offs[0] == 0 && m.k_offs[0] == 0 &&
+         m.q_offs[m.nQb] == Sq && m.k_offs[m.nKb] == Sk;
+  for (int i = threadIdx.x; i < m.nQb; i += blockDim.x) ok &= __ldg(m.q_offs + i) <= __ldg(m.q_offs + i + 1);
+  for (int i = threadIdx.x; i < m.nKb; i += blockDim.x) ok &= __ldg(m.k_offs + i) <= __ldg(m.k_offs + i + 1);
+  if (!__syncthreads_and(ok) && threadIdx.x == 0) atomicCAS(status, 0, LCATTN_ERR_DEVICE_MASK);
 }
 
 // Column bounds, one warp per tile: count the allowed rows of each column
@@ -188,7 +190,7 @@ cudaError_t launch_mask_compile(const ProblemDev& pr, const MaskDev& m, const Ti
   cudaError_t e = cudaMemsetAsync(t.status, 0, 32, st);  // status and scheduler words
   if (e != cudaSuccess) return e;
   if (m.kind == LCATTN_MASK_BLOCKMAP) {
-    validate_offsets_kernel<<<1, 32, 0, st>>>(m, pr.Sq, pr.Sk, t.status);
+    validate_offsets_kernel<<<1, 512, 0, st>>>(m, pr.Sq, pr.Sk, t.status);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   int dev = 0, nsm = 0;

@@ -17,11 +17,11 @@
 //                  two row groups of 128 threads, 16-byte loads kept eight
 //                  deep per thread.
 //   select_kernel  one CTA per (batch, head, R consecutive query blocks):
-//                  fp32 scores against every key block's mean (the means
-//                  come from L2), a bitonic sort of 64-bit (score, index) keys
-//                  per row in shared memory, then TopK by rank or TopP by a
-//                  warp scan of the softmax mass, and a coalesced write of the
-//                  map rows.
+//                  fp32 scores against every key block's mean (read from L2,
+//                  stored transposed so that a warp's loads coalesce), a
+//                  bitonic sort of 64-bit (score, index) keys per row in
+//                  shared memory, then TopK by rank or TopP by a warp scan of
+//                  the softmax mass, and a coalesced write of the map rows.
 #include <climits>
 
 #include "lcattn_internal.cuh"
@@ -89,9 +89,18 @@ __global__ void __launch_bounds__(kPoolThreads) pool_kernel(PoolSide qs, PoolSid
     float m[8];
     #pragma unroll
     for (int e = 0; e < 8; ++e) m[e] = n > 0 ? (acc[e] + part[t][e]) / (float)n : 0.f;
-    float4* out = reinterpret_cast<float4*>(p.out + (((int64_t)b * p.H + h) * p.nb + i) * kD + e0);
-    out[0] = make_float4(m[0], m[1], m[2], m[3]);
-    out[1] = make_float4(m[4], m[5], m[6], m[7]);
+    if (p.transposed) {
+      // [B][H][128][nb]: the select kernel's threads (one key block each) then
+      // read consecutive addresses.  These 4-byte stores are scattered, but the
+      // means are 1/128 of the bytes read.
+      float* out = p.out + ((int64_t)b * p.H + h) * kD * p.nb + i;
+      #pragma unroll
+      for (int e = 0; e < 8; ++e) out[(int64_t)(e0 + e) * p.nb] = m[e];
+    } else {
+      float4* out = reinterpret_cast<float4*>(p.out + (((int64_t)b * p.H + h) * p.nb + i) * kD + e0);
+      out[0] = make_float4(m[0], m[1], m[2], m[3]);
+      out[1] = make_float4(m[4], m[5], m[6], m[7]);
+    }
   }
 }
 
@@ -108,9 +117,10 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelectArgs a) {
   extern __shared__ __align__(16) uint8_t smem[];
   const int R = a.R, n2 = a.n2;
   unsigned long long* keys = reinterpret_cast<unsigned long long*>(smem);  // [R][n2]
-  float* qsm = reinterpret_cast<float*>(keys + (size_t)R * n2);           // [R][128]
-  int* qend = reinterpret_cast<int*>(qsm + R * kD);                       // [R]
-  uint8_t* flags = reinterpret_cast<uint8_t*>(qend + kMaxRows);          // [R][nKbp]
+  float* qsm = reinterpret_cast<float*>(keys + (size_t)R * n2);           // [128][kMaxRows]
+  int* qend = reinterpret_cast<int*>(qsm + kMaxRows * kD);                // [kMaxRows]
+  int* span = qend + kMaxRows;                                            // [1] (+3 pad)
+  uint8_t* flags = reinterpret_cast<uint8_t*>(span + 4);                  // [R][nKbp]
   const int nKbp = (a.nKb + 15) & ~15;
 
   const int tid = threadIdx.x;
@@ -126,9 +136,9 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelectArgs a) {
   const int Hkv = a.Hq / a.G;
 
   const int64_t row0 = ((int64_t)b * a.Hq + h) * a.nQb + i0;  // first map / score row
-  for (int x = tid; x < R * kD; x += kSelThreads) {
-    const int r = x / kD;
-    qsm[x] = r < rows ? a.qbar[(row0 + r) * kD + (x % kD)] : 0.f;
+  for (int x = tid; x < kMaxRows * kD; x += kSelThreads) {
+    const int r = x / kD, c = x % kD;
+    qsm[c * kMaxRows + r] = r < rows ? a.qbar[(row0 + r) * kD + c] : 0.f;
   }
   if (tid < R) {
     int e = INT_MIN;  // INT_MIN: not a candidate row (past the end, or an empty block)
@@ -139,12 +149,14 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelectArgs a) {
     }
     qend[tid] = e;
   }
+  if (tid == 0) *span = 0;
   for (int x = tid; x < R * nKbp; x += kSelThreads) flags[x] = 0;
   __syncthreads();
 
-  // Scores: thread j takes key block j; dot products run over c = 0..127 in order.
+  // Scores: thread j takes key block j; dot products run over c = 0..127 in
+  // order.  k_bar is stored [128][nKb], so a warp's loads are consecutive.
   const float4* q4 = reinterpret_cast<const float4*>(qsm);
-  const float* kbar = a.kbar + ((int64_t)b * Hkv + g) * a.nKb * kD;
+  const float* kbar = a.kbar + ((int64_t)b * Hkv + g) * kD * a.nKb;
   for (int j = tid; j < n2; j += kSelThreads) {
     if (j >= a.nKb) {
       for (int r = 0; r < R; ++r) keys[(size_t)r * n2 + j] = 0ull;
@@ -155,21 +167,21 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelectArgs a) {
     float acc[kMaxRows];
     #pragma unroll
     for (int r = 0; r < kMaxRows; ++r) acc[r] = 0.f;
-    const float4* kp = reinterpret_cast<const float4*>(kbar + (int64_t)j * kD);
-    #pragma unroll 4
-    for (int c = 0; c < kD / 4; ++c) {
-      const float4 kv = __ldg(kp + c);
-      #pragma unroll
-      for (int r = 0; r < kMaxRows; ++r) {
-        if (r < R) {
-          const float4 qv = q4[r * (kD / 4) + c];
-          acc[r] = fmaf(qv.x, kv.x, acc[r]);
-          acc[r] = fmaf(qv.y, kv.y, acc[r]);
-          acc[r] = fmaf(qv.z, kv.z, acc[r]);
-          acc[r] = fmaf(qv.w, kv.w, acc[r]);
-        }
-      }
+    const float* kp = kbar + j;
+    #pragma unroll 8
+    for (int c = 0; c < kD; ++c) {
+      const float kv = __ldg(kp + (int64_t)c * a.nKb);
+      const float4 qa = q4[c * 2], qb = q4[c * 2 + 1];
+      acc[0] = fmaf(qa.x, kv, acc[0]);
+      acc[1] = fmaf(qa.y, kv, acc[1]);
+      acc[2] = fmaf(qa.z, kv, acc[2]);
+      acc[3] = fmaf(qa.w, kv, acc[3]);
+      acc[4] = fmaf(qb.x, kv, acc[4]);
+      acc[5] = fmaf(qb.y, kv, acc[5]);
+      acc[6] = fmaf(qb.z, kv, acc[6]);
+      acc[7] = fmaf(qb.w, kv, acc[7]);
     }
+    bool any = false;
     #pragma unroll
     for (int r = 0; r < kMaxRows; ++r) {
       if (r < R) {
@@ -177,24 +189,36 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelectArgs a) {
         if (a.scores && r < rows) a.scores[(row0 + r) * a.nKb + j] = s;
         const int qe = qend[r];
         const bool cand = qe != INT_MIN && khi > klo && (!a.causal || klo < qe);
+        any |= cand;
         keys[(size_t)r * n2 + j] =
             cand ? ((unsigned long long)ord_of(s) << 32) | (uint32_t)(~(uint32_t)j) : 0ull;
       }
     }
+    if (any) atomicMax(span, j + 1);
   }
   __syncthreads();
 
   // Bitonic sort of every row, descending.  A candidate's key is never 0, so
   // candidates come first, in ranking order, then the zeros.
-  const int half = n2 >> 1;
-  for (int k = 2; k <= n2; k <<= 1) {
-    for (int jj = k >> 1; jj > 0; jj >>= 1) {
-      for (int x = tid; x < R * half; x += kSelThreads) {
-        const int r = x / half, pidx = x - r * half;
-        const int lo_i = (pidx / jj) * 2 * jj + (pidx % jj);
-        unsigned long long* row = keys + (size_t)r * n2;
+  // Only the first ns keys of each row can be non-zero (ns: a power of two
+  // covering the last candidate of any row of this CTA, at least 32), so the
+  // sort and the selection run over that prefix; causal rows near the start
+  // sort far less than n2.  Every index below is a shift or a mask.
+  const int lg2 = __ffs(n2) - 1;
+  int lgs = 5;
+  while ((1 << lgs) < *span) ++lgs;
+  const int ns = 1 << lgs;
+  const int lgh = lgs - 1;
+  const int pairs = R << lgh;
+  for (int lk = 1; lk <= lgs; ++lk) {
+    for (int lj = lk - 1; lj >= 0; --lj) {
+      const int jj = 1 << lj;
+      for (int x = tid; x < pairs; x += kSelThreads) {
+        const int r = x >> lgh, pidx = x & ((1 << lgh) - 1);
+        const int lo_i = ((pidx >> lj) << (lj + 1)) | (pidx & (jj - 1));
+        unsigned long long* row = keys + ((size_t)r << lg2);
         const unsigned long long u = row[lo_i], v = row[lo_i + jj];
-        const bool desc = (lo_i & k) == 0;
+        const bool desc = ((lo_i >> lk) & 1) == 0;
         if (desc ? (u < v) : (u > v)) {
           row[lo_i] = v;
           row[lo_i + jj] = u;
@@ -205,11 +229,11 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelectArgs a) {
   }
 
   if (a.rule == LCATTN_SELECT_TOPK) {
-    const int kk = min(a.top_k, n2);
-    for (int x = tid; x < R * kk; x += kSelThreads) {
-      const int r = x / kk, pos = x - r * kk;
-      const unsigned long long key = keys[(size_t)r * n2 + pos];
-      if (key) flags[r * nKbp + (int)(~(uint32_t)key)] = 1;
+    const int kk = min(a.top_k, ns);
+    for (int x = tid; x < (R << lgs); x += kSelThreads) {
+      const int r = x >> lgs, pos = x & (ns - 1);
+      const unsigned long long key = keys[((size_t)r << lg2) + pos];
+      if (pos < kk && key) flags[r * nKbp + (int)(~(uint32_t)key)] = 1;
     }
   } else {
     // TopP: one warp per row.  Z = sum over candidates of exp(s - s_max)
@@ -222,7 +246,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelectArgs a) {
       if (row[0] == 0ull) continue;
       const float s0 = float_of((uint32_t)(row[0] >> 32));
       float z = 0.f;
-      for (int pos = lane; pos < n2; pos += 32) {
+      for (int pos = lane; pos < ns; pos += 32) {
         const unsigned long long key = row[pos];
         if (key) z += expf(float_of((uint32_t)(key >> 32)) - s0);
       }
@@ -230,7 +254,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(SelectArgs a) {
       for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
       const float pz = a.top_p * z;
       float carry = 0.f;
-      for (int base = 0; base < n2; base += 32) {
+      for (int base = 0; base < ns; base += 32) {
         const unsigned long long key = row[base + lane];
         const float e = key ? expf(float_of((uint32_t)(key >> 32)) - s0) : 0.f;
         float incl = e;
@@ -267,7 +291,7 @@ cudaError_t launch_block_pool(const PoolSide& qs, const PoolSide& ks, cudaStream
 
 size_t select_smem_bytes(int R, int n2, int nKb) {
   const int nKbp = (nKb + 15) & ~15;
-  return (size_t)R * n2 * 8 + (size_t)R * kD * 4 + kMaxRows * 4 + (size_t)R * nKbp;
+  return (size_t)R * n2 * 8 + (size_t)kMaxRows * kD * 4 + kMaxRows * 4 + 16 + (size_t)R * nKbp;
 }
 
 void select_geometry(int nKb, int* R, int* n2) {
