@@ -52,8 +52,9 @@ def _rows_fwd(qr, k, v, M, scale):
 
 
 def attention_fwd(q, k, v, spec, scale, chunk: int = 1024):
-    """O [B, N, Hq, D] and LSE [B, Hq, N] for fp64 arrays q [B,N,Hq,D], k/v [B,N,Hkv,D]."""
+    """O [B, N, Hq, D] and LSE [B, Hq, N] for fp64 arrays q [B,N,Hq,D], k/v [B,Sk,Hkv,D]."""
     B, N, Hq, D = q.shape
+    Sk = k.shape[1]
     Hkv = k.shape[2]
     G = Hq // Hkv
     O = np.zeros((B, N, Hq, v.shape[3]), dtype=np.float64)
@@ -63,7 +64,7 @@ def attention_fwd(q, k, v, spec, scale, chunk: int = 1024):
             g = h // G
             for r0 in range(0, N, chunk):
                 rows = np.arange(r0, min(N, r0 + chunk))
-                M = allowed(spec, N, rows, head=h)
+                M = allowed(spec, N, rows, head=h, Sk=Sk)
                 o, lse, _ = _rows_fwd(q[b, rows, h], k[b, :, g], v[b, :, g], M, scale)
                 O[b, rows, h] = o
                 LSE[b, h, rows] = lse
@@ -72,10 +73,10 @@ def attention_fwd(q, k, v, spec, scale, chunk: int = 1024):
 
 def attention_fwd_rows(q, k, v, spec, scale, b: int, h: int, rows):
     """O [R, D] and LSE [R] for selected query rows of one (batch, head)."""
-    N = k.shape[1]
+    N, Sk = q.shape[1], k.shape[1]
     G = q.shape[2] // k.shape[2]
     rows = np.asarray(rows, dtype=np.int64)
-    M = allowed(spec, N, rows, head=h)
+    M = allowed(spec, N, rows, head=h, Sk=Sk)
     o, lse, _ = _rows_fwd(q[b, rows, h], k[b, :, h // G], v[b, :, h // G], M, scale)
     return o, lse
 
@@ -83,6 +84,7 @@ def attention_fwd_rows(q, k, v, spec, scale, b: int, h: int, rows):
 def attention_bwd(q, k, v, do, spec, scale, chunk: int = 1024):
     """(dQ, dK, dV, O, LSE) for the whole problem, from the definition above."""
     B, N, Hq, D = q.shape
+    Sk = k.shape[1]
     Hkv = k.shape[2]
     G = Hq // Hkv
     O, LSE = attention_fwd(q, k, v, spec, scale, chunk)
@@ -95,7 +97,7 @@ def attention_bwd(q, k, v, do, spec, scale, chunk: int = 1024):
             kk, vv = k[b, :, g], v[b, :, g]
             for r0 in range(0, N, chunk):
                 rows = np.arange(r0, min(N, r0 + chunk))
-                M = allowed(spec, N, rows, head=h)
+                M = allowed(spec, N, rows, head=h, Sk=Sk)
                 lse = LSE[b, h, rows]
                 has = np.isfinite(lse)
                 S = scale * (q[b, rows, h] @ kk.T)
@@ -120,7 +122,7 @@ def attention_bwd_sampled(q, k, v, do, spec, scale, b: int, g: int, q_rows, k_co
     those rows are found from the mask and computed in full, so the cost is
     proportional to the number of such rows times N.
     """
-    N = k.shape[1]
+    N, Sk = q.shape[1], k.shape[1]
     Hq, Hkv = q.shape[2], k.shape[2]
     G = Hq // Hkv
     kk, vv = k[b, :, g], v[b, :, g]
@@ -132,7 +134,7 @@ def attention_bwd_sampled(q, k, v, do, spec, scale, b: int, g: int, q_rows, k_co
     for hi in range(G):
         h = g * G + hi
         # dQ rows: each needs its own full row of P and dP.
-        M = allowed(spec, N, q_rows, head=h)
+        M = allowed(spec, N, q_rows, head=h, Sk=Sk)
         o, lse, P = _rows_fwd(q[b, q_rows, h], kk, vv, M, scale)
         dOr = do[b, q_rows, h]
         dP = dOr @ vv.T
@@ -142,11 +144,11 @@ def attention_bwd_sampled(q, k, v, do, spec, scale, b: int, g: int, q_rows, k_co
         # dK/dV columns: find every row that attends at least one sampled key.
         for r0 in range(0, N, 8192):
             rows = np.arange(r0, min(N, r0 + 8192))
-            need = allowed(spec, N, rows, head=h, cols=k_cols).any(axis=1)
+            need = allowed(spec, N, rows, head=h, cols=k_cols, Sk=Sk).any(axis=1)
             if not need.any():
                 continue
             rr = rows[need]
-            Mr = allowed(spec, N, rr, head=h)
+            Mr = allowed(spec, N, rr, head=h, Sk=Sk)
             o, lse, P = _rows_fwd(q[b, rr, h], kk, vv, Mr, scale)
             dOr = do[b, rr, h]
             Pc = P[:, k_cols]
@@ -159,20 +161,22 @@ def attention_bwd_sampled(q, k, v, do, spec, scale, b: int, g: int, q_rows, k_co
 
 
 def classify_tiles(spec, N: int, BM: int = 128, BN: int = 128, head: int = 0,
-                   q_tiles=None) -> np.ndarray:
+                   q_tiles=None, Sk=None) -> np.ndarray:
     """Class of every (query tile, key tile) pair: EMPTY when no in-range pair of
-    the tile is allowed, FULL when all are, PARTIAL otherwise.  Rows and columns
-    past N (a ragged last tile) are not part of the tile.  With ``q_tiles``,
-    only those rows of tiles are classified (output row r = q_tiles[r])."""
+    the tile is allowed, FULL when all are, PARTIAL otherwise.  Rows past N and
+    columns past Sk (default N; a ragged last tile) are not part of the tile.
+    With ``q_tiles``, only those rows of tiles are classified (output row r =
+    q_tiles[r])."""
+    Sk = N if Sk is None else int(Sk)
     nQt = (N + BM - 1) // BM
-    nKt = (N + BN - 1) // BN
+    nKt = (Sk + BN - 1) // BN
     tiles = range(nQt) if q_tiles is None else list(q_tiles)
     out = np.zeros((len(tiles), nKt), dtype=np.uint8)
     for r, qt in enumerate(tiles):
         rows = np.arange(qt * BM, min(N, (qt + 1) * BM))
-        M = allowed(spec, N, rows, head=head)
+        M = allowed(spec, N, rows, head=head, Sk=Sk)
         for kt in range(nKt):
-            blk = M[:, kt * BN:min(N, (kt + 1) * BN)]
+            blk = M[:, kt * BN:min(Sk, (kt + 1) * BN)]
             if not blk.any():
                 out[r, kt] = EMPTY
             elif blk.all():

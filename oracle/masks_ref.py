@@ -26,6 +26,15 @@ when the predicate is true:
     BLOCK_CAUSAL_DOCUMENT   doc(i) == doc(j) and blk(j) <= blk(i)
     UNIFORM_BLOCK           keep[h, i // bs, j // bs]
     VARIABLE_BLOCK          keep[h, qblk(i), kblk(j)]
+
+Query and key lengths may differ (Sq queries, Sk keys) for FULL, CAUSAL and the
+two sliding windows, the variants the pages' kernels take for decode-style and
+chunked rows.  The reading is bottom-right alignment: query i stands at key
+position i + (Sk - Sq), and the predicates above apply with that position in
+place of i (so CAUSAL is j <= i + Sk - Sq; for Sq > Sk the first Sq - Sk rows
+allow nothing).  With Sq = Sk the shift is 0.  Block maps index query and key
+blocks on their own axes, with no shift.  The other families are defined for
+Sq = Sk only.
 """
 from __future__ import annotations
 
@@ -43,16 +52,31 @@ def _segment_start(seg: np.ndarray, lens) -> np.ndarray:
     return starts[seg]
 
 
-def allowed(spec, N: int, rows=None, head: int = 0, cols=None) -> np.ndarray:
+RECTANGULAR = ("FULL", "CAUSAL", "FULL_SLIDING_WINDOW", "CAUSAL_SLIDING_WINDOW",
+               "UNIFORM_BLOCK", "VARIABLE_BLOCK")
+
+
+def allowed(spec, N: int, rows=None, head: int = 0, cols=None, Sk=None) -> np.ndarray:
     """Boolean mask rows: ``out[r, c]`` is True when query ``rows[r]`` may attend
-    key ``cols[c]`` (all keys 0..N-1 by default) under ``spec`` for query head
-    ``head``."""
+    key ``cols[c]`` under ``spec`` for query head ``head``.  ``N`` is the number
+    of queries and ``Sk`` of keys (default ``N``); ``cols`` defaults to every key."""
+    Sk = N if Sk is None else int(Sk)
     if rows is None:
         rows = np.arange(N)
     i = np.asarray(rows, dtype=np.int64)[:, None]
-    j = (np.arange(N, dtype=np.int64) if cols is None else np.asarray(cols, dtype=np.int64))[None, :]
+    j = (np.arange(Sk, dtype=np.int64) if cols is None else np.asarray(cols, dtype=np.int64))[None, :]
     k = spec.kind
     p = spec.params
+    if Sk != N and k not in RECTANGULAR:
+        raise ValueError(f"{k} is defined for equal query and key lengths only")
+    if k == "UNIFORM_BLOCK":
+        bs = p["block"]
+        keep = np.asarray(p["keep"], dtype=bool)[head]
+        return keep[i // bs, j // bs]
+    if k == "VARIABLE_BLOCK":
+        keep = np.asarray(p["keep"], dtype=bool)[head]
+        return keep[_segment_of(i, p["q_block_lens"]), _segment_of(j, p["k_block_lens"])]
+    i = i + (Sk - N)  # the query's position on the key axis (bottom-right alignment)
     if k == "FULL":
         return np.ones((i.shape[0], j.shape[1]), dtype=bool)
     if k == "CAUSAL":
@@ -91,19 +115,12 @@ def allowed(spec, N: int, rows=None, head: int = 0, cols=None) -> np.ndarray:
         di, dj = _segment_of(i, lens), _segment_of(j, lens)
         bi, bj = _segment_of(i, flat_blocks), _segment_of(j, flat_blocks)
         return (di == dj) & (bj <= bi)
-    if k == "UNIFORM_BLOCK":
-        bs = p["block"]
-        keep = np.asarray(p["keep"], dtype=bool)[head]
-        return keep[i // bs, j // bs]
-    if k == "VARIABLE_BLOCK":
-        keep = np.asarray(p["keep"], dtype=bool)[head]
-        return keep[_segment_of(i, p["q_block_lens"]), _segment_of(j, p["k_block_lens"])]
     raise ValueError(k)
 
 
-def allowed_pairs(spec, N: int, head: int = 0, chunk: int = 4096) -> int:
+def allowed_pairs(spec, N: int, head: int = 0, chunk: int = 4096, Sk=None) -> int:
     """Number of allowed (i, j) pairs for one head, by explicit enumeration."""
     total = 0
     for r0 in range(0, N, chunk):
-        total += int(allowed(spec, N, np.arange(r0, min(N, r0 + chunk)), head).sum())
+        total += int(allowed(spec, N, np.arange(r0, min(N, r0 + chunk)), head, Sk=Sk).sum())
     return total

@@ -18,6 +18,7 @@ import torch
 from oracle import (allowed, attention_bwd, attention_bwd_sampled, attention_fwd,
                     attention_fwd_rows)
 from oracle.attention_ref import _rows_fwd
+import oracle
 from synthetic import MaskSpec, block_keep
 
 SPECS = [
@@ -215,3 +216,66 @@ def test_gradient_sum_identities():
     dQ, dK, dV, _, _ = attention_bwd(q, k, v, do, spec, 0.25)
     np.testing.assert_allclose(dK.sum(1), 0.0, atol=1e-12)
     np.testing.assert_allclose(dV.sum(1), do.reshape(1, N, 2, 2, D).sum(axis=(1, 3)), atol=1e-12)
+
+
+# ---- query and key lengths that differ (bottom-right alignment) -------------
+
+def _rect_inputs(B, Sq, Sk, Hq, Hkv, D, seed):
+    rng = np.random.default_rng(seed)
+    return (rng.standard_normal((B, Sq, Hq, D)), rng.standard_normal((B, Sk, Hkv, D)),
+            rng.standard_normal((B, Sk, Hkv, D)), rng.standard_normal((B, Sq, Hq, D)))
+
+
+@pytest.mark.parametrize("Sq,Sk", [(5, 13), (1, 9), (9, 4), (7, 7)])
+def test_causal_rectangular_matches_torch_lower_right(Sq, Sk):
+    """CAUSAL with Sq != Sk against torch's own lower-right causal bias
+    (torch.nn.attention.bias.causal_lower_right) and autograd, in fp64."""
+    from torch.nn.attention.bias import causal_lower_right
+    B, Hq, Hkv, D = 1, 4, 2, 8
+    q, k, v, do = _rect_inputs(B, Sq, Sk, Hq, Hkv, D, 17)
+    scale = 0.31
+    spec = MaskSpec("CAUSAL")
+    dQ, dK, dV, O, LSE = oracle.attention_bwd(q, k, v, do, spec, scale, chunk=3)
+    G = Hq // Hkv
+    qt, kt, vt = (torch.tensor(x).permute(0, 2, 1, 3).requires_grad_(True) for x in (q, k, v))
+    bias = causal_lower_right(Sq, Sk)
+    dense = bias._materialize(device=torch.device("cpu"))          # True = allowed, [Sq, Sk]
+    has = dense.any(-1)
+    o = torch.nn.functional.scaled_dot_product_attention(
+        qt, kt.repeat_interleave(G, 1), vt.repeat_interleave(G, 1),
+        attn_mask=dense | ~has[:, None], scale=scale)
+    o = o * has[None, None, :, None]
+    (o * torch.tensor(do).permute(0, 2, 1, 3)).sum().backward()
+    back = lambda t: t.detach().permute(0, 2, 1, 3).numpy()
+    for got, want in ((O, back(o)), (dQ, back(qt.grad)), (dK, back(kt.grad)), (dV, back(vt.grad))):
+        np.testing.assert_allclose(got, want, rtol=0, atol=1e-10)
+    np.testing.assert_array_equal(np.isfinite(LSE[0, 0]), has.numpy())
+    assert int(has.sum()) == min(Sq, Sk) if Sq > Sk else int(has.sum()) == Sq
+
+
+@pytest.mark.parametrize("kind,params", [("CAUSAL", {}), ("CAUSAL_SLIDING_WINDOW", {"window": 4}),
+                                         ("FULL_SLIDING_WINDOW", {"window": 3}), ("FULL", {})])
+@pytest.mark.parametrize("Sq", [1, 4, 11])
+def test_rectangular_is_the_suffix_of_the_square_problem(kind, params, Sq):
+    """Bottom-right alignment: the Sq queries behave exactly like the last Sq
+    rows of the square problem over the same Sk keys.  With dO = 0 on the other
+    rows, dK and dV agree too."""
+    B, Sk, Hq, Hkv, D = 1, 12, 2, 1, 8
+    q, k, v, do = _rect_inputs(B, Sq, Sk, Hq, Hkv, D, 5)
+    spec = MaskSpec(kind, params)
+    scale = 0.4
+    rng = np.random.default_rng(6)
+    qs = np.concatenate([rng.standard_normal((B, Sk - Sq, Hq, D)), q], axis=1)
+    dos = np.concatenate([np.zeros((B, Sk - Sq, Hq, D)), do], axis=1)
+    r = oracle.attention_bwd(q, k, v, do, spec, scale)
+    s = oracle.attention_bwd(qs, k, v, dos, spec, scale)
+    np.testing.assert_allclose(r[3], s[3][:, Sk - Sq:], rtol=0, atol=1e-12)        # O
+    np.testing.assert_allclose(r[4], s[4][:, :, Sk - Sq:], rtol=0, atol=1e-12)     # LSE
+    np.testing.assert_allclose(r[0], s[0][:, Sk - Sq:], rtol=0, atol=1e-12)        # dQ
+    np.testing.assert_allclose(r[1], s[1], rtol=0, atol=1e-12)                     # dK
+    np.testing.assert_allclose(r[2], s[2], rtol=0, atol=1e-12)                     # dV
+
+
+def test_rectangular_only_where_defined():
+    with pytest.raises(ValueError):
+        oracle.allowed(MaskSpec("CAUSAL_DOCUMENT", {"doc_lens": [3, 2]}), 5, Sk=7)

@@ -29,7 +29,7 @@ def test_mask_golden(case):
     if "keep" in spec.params:
         spec.params["keep"] = np.array(spec.params["keep"], dtype=bool)
     want = np.array([[c == "1" for c in row] for row in case["rows"]], dtype=bool)
-    got = allowed(spec, case["N"])
+    got = allowed(spec, case["N"], Sk=case.get("Sk"))
     np.testing.assert_array_equal(got, want)
 
 

@@ -62,7 +62,7 @@ def _params(case):
 def golden_masks_hold(mr):
     for case in _golden("masks_small.json"):
         want = np.array([[c == "1" for c in row] for row in case["rows"]], dtype=bool)
-        got = mr.allowed(MaskSpec(case["kind"], _params(case)), case["N"])
+        got = mr.allowed(MaskSpec(case["kind"], _params(case)), case["N"], Sk=case.get("Sk"))
         if got.shape != want.shape or not np.array_equal(got, want):
             return False
     return True
@@ -150,6 +150,8 @@ MASK_MUTANTS = [
     ("block causal strict", "(bj <= bi)", "(bj < bi)"),
     ("segment boundary side", "side=\"right\"", "side=\"left\""),
     ("uniform block transposed", "keep[i // bs, j // bs]", "keep[j // bs, i // bs]"),
+    ("top-left alignment for Sq != Sk", "i = i + (Sk - N)", "i = i + 0"),
+    ("alignment shift reversed", "i = i + (Sk - N)", "i = i + (N - Sk)"),
     ("variable block lens swapped", "keep[_segment_of(i, p[\"q_block_lens\"]), _segment_of(j, p[\"k_block_lens\"])]",
      "keep[_segment_of(i, p[\"k_block_lens\"]), _segment_of(j, p[\"q_block_lens\"])]"),
 ]
@@ -172,8 +174,8 @@ ATTN_MUTANTS = [
     ("dQ without scale", "dQ[b, rows, h] = scale * (dS @ kk)", "dQ[b, rows, h] = (dS @ kk)", 0),
     ("dK transposed operand", "scale * (dS.T @ q[b, rows, h])", "scale * (dS.T @ do[b, rows, h])", 0),
     ("dP transposed operand", "dP = dOr @ vv.T\n                Dr", "dP = dOr @ kk.T\n                Dr", 0),
-    ("sampled path misses rows", "need = allowed(spec, N, rows, head=h, cols=k_cols).any(axis=1)",
-     "need = allowed(spec, N, rows, head=h, cols=k_cols).all(axis=1)", 0),
+    ("sampled path misses rows", "need = allowed(spec, N, rows, head=h, cols=k_cols, Sk=Sk).any(axis=1)",
+     "need = allowed(spec, N, rows, head=h, cols=k_cols, Sk=Sk).all(axis=1)", 0),
     ("sampled dK without scale", "dK += scale * (dSc.T @ q[b, rr, h])", "dK += (dSc.T @ q[b, rr, h])", 0),
     ("sampled dQ drops D", "dS = P * (dP - Dr[:, None])", "dS = P * dP", 1),
 ]
@@ -185,7 +187,7 @@ def test_torch_pin_rejects_attention_mutant(name, old, new, occ):
 
 
 TILE_MUTANTS = [
-    ("ragged column tile one wider", "M[:, kt * BN:min(N, (kt + 1) * BN)]", "M[:, kt * BN:min(N, (kt + 1) * BN + 1)]"),
+    ("ragged column tile one wider", "M[:, kt * BN:min(Sk, (kt + 1) * BN)]", "M[:, kt * BN:min(Sk, (kt + 1) * BN + 1)]"),
     ("ragged row tile cut short", "np.arange(qt * BM, min(N, (qt + 1) * BM))", "np.arange(qt * BM, min(N - 1, (qt + 1) * BM))"),
     ("FULL and PARTIAL swapped", "out[r, kt] = FULL\n", "out[r, kt] = PARTIAL\n"),
 ]
