@@ -176,12 +176,13 @@ class DeviceMask:
     entry (it is replicated ``B`` times)."""
 
     def __init__(self, spec, N: int, Hq: int, B: int = 1, device: str = "cuda",
-                 row_bounds: bool = True):
+                 row_bounds: bool = True, Sk: Optional[int] = None):
         self.spec = spec
         self.N, self.Hq, self.B = N, Hq, B
+        self.Sk = N if Sk is None else int(Sk)
         self.desc = lcattn_mask_desc()
         if spec.kind in ("UNIFORM_BLOCK", "VARIABLE_BLOCK"):
-            keep, q_offs, k_offs = masks.block_map(spec, N, Hq)
+            keep, q_offs, k_offs = masks.block_map(spec, N, Hq, self.Sk)
             self.pairs_per_batch = masks.allowed_pairs_from_blocks(keep, q_offs, k_offs)
             self.block_map = torch.from_numpy(np.broadcast_to(keep, (B,) + keep.shape).copy()).to(device)
             self.q_offs = torch.from_numpy(q_offs).to(device)
@@ -193,13 +194,13 @@ class DeviceMask:
             self.desc.nQb = keep.shape[1]
             self.desc.nKb = keep.shape[2]
         else:
-            cb = masks.col_bounds(spec, N)
+            cb = masks.col_bounds(spec, N, self.Sk)
             self.pairs_per_batch = Hq * masks.allowed_pairs_from_bounds(cb, N)
             self.col_bounds = torch.from_numpy(np.broadcast_to(cb, (B,) + cb.shape).copy()).to(device)
             self.desc.kind = LCATTN_MASK_COLBOUNDS
             self.desc.col_bounds = self.col_bounds.data_ptr()
             if row_bounds:  # the same mask per query row, for the forward's partial tiles
-                rb = masks.row_bounds(spec, N)
+                rb = masks.row_bounds(spec, N, self.Sk)
                 self.row_bounds = torch.from_numpy(np.broadcast_to(rb, (B,) + rb.shape).copy()).to(device)
                 self.desc.row_bounds = self.row_bounds.data_ptr()
 
@@ -431,7 +432,7 @@ def attention(q, k, v, spec, scale=None, d_o=None, stream=None):
     """Convenience composition of the C calls: compile the mask, run the
     forward, and (when ``d_o`` is given) the backward.  Returns a dict."""
     B, N, Hq, _ = q.shape
-    mask = DeviceMask(spec, N, Hq, B, device=q.device)
+    mask = DeviceMask(spec, N, Hq, B, device=q.device, Sk=k.shape[1])
     shape = make_shape(q, k, v)
     meta = lcattn_mask_compile(shape, mask, stream=stream, device=q.device)
     o, lse = lcattn_fwd(q, k, v, mask, meta, scale, stream=stream)

@@ -34,18 +34,33 @@ def _per_key(lens: Sequence[int], N: int):
     return seg, starts[seg], ends[seg]
 
 
-def col_bounds(spec, N: int) -> np.ndarray:
-    """int32 [N, 4] = (a0, b0, a1, b1) per key column for a static mask."""
+# Families with a reading for query and key lengths that differ: query i
+# stands at key position i + (Sk - Sq) (bottom-right alignment, the decode /
+# chunked-prefill convention); the rest are defined for Sq = Sk only.
+RECTANGULAR = ("FULL", "CAUSAL", "FULL_SLIDING_WINDOW", "CAUSAL_SLIDING_WINDOW")
+
+
+def _lengths(spec, N: int, Sk):
+    Sk = N if Sk is None else int(Sk)
+    if Sk != N and spec.kind not in RECTANGULAR + ("UNIFORM_BLOCK", "VARIABLE_BLOCK"):
+        raise ValueError(f"{spec.kind} needs equal query and key lengths")
+    return Sk, Sk - N
+
+
+def col_bounds(spec, N: int, Sk=None) -> np.ndarray:
+    """int32 [Sk, 4] = (a0, b0, a1, b1) per key column for a static mask over N
+    query rows and Sk keys (default N)."""
     k, p = spec.kind, spec.params
-    j = np.arange(N, dtype=np.int64)
-    a0 = np.zeros(N, np.int64)
-    b0 = np.full(N, N, np.int64)
-    a1 = np.zeros(N, np.int64)
-    b1 = np.zeros(N, np.int64)  # second interval empty unless set
+    Sk, off = _lengths(spec, N, Sk)
+    j = np.arange(Sk, dtype=np.int64)
+    a0 = np.zeros(Sk, np.int64)
+    b0 = np.full(Sk, N, np.int64)
+    a1 = np.zeros(Sk, np.int64)
+    b1 = np.zeros(Sk, np.int64)  # second interval empty unless set
     if k == "FULL":
         pass
     elif k == "CAUSAL":
-        a0 = j.copy()
+        a0 = np.maximum(0, j - off)
     elif k == "FULL_DOCUMENT":
         _, a0, b0 = _per_key(p["doc_lens"], N)
     elif k == "CAUSAL_DOCUMENT":
@@ -53,12 +68,12 @@ def col_bounds(spec, N: int) -> np.ndarray:
         a0 = j.copy()
     elif k == "FULL_SLIDING_WINDOW":
         w = int(p["window"])
-        a0 = np.maximum(0, j - w + 1)
-        b0 = np.minimum(N, j + w)
+        a0 = np.maximum(0, j - w + 1 - off)
+        b0 = np.clip(j + w - off, 0, N)
     elif k == "CAUSAL_SLIDING_WINDOW":
         w = int(p["window"])
-        a0 = j.copy()
-        b0 = np.minimum(N, j + w)
+        a0 = np.maximum(0, j - off)
+        b0 = np.clip(j + w - off, 0, N)
     elif k == "SHARED_QUESTION":
         lens = [int(p["question_len"])] + [int(x) for x in p["answer_lens"]]
         seg, _, end = _per_key(lens, N)
@@ -101,21 +116,22 @@ def col_bounds(spec, N: int) -> np.ndarray:
     return np.ascontiguousarray(out.astype(np.int32))
 
 
-def row_bounds(spec, N: int) -> np.ndarray:
+def row_bounds(spec, N: int, Sk=None) -> np.ndarray:
     """int32 [N, 4] = (c0, d0, c1, d1) per query row: row i may attend the keys
     [c0, d0) U [c1, d1).  The same mask as :func:`col_bounds`, transposed; every
     static family has at most two key intervals per row.  The forward kernel
     uses this form to build a partial tile's row masks cheaply."""
     k, p = spec.kind, spec.params
+    Sk, off = _lengths(spec, N, Sk)
     i = np.arange(N, dtype=np.int64)
     c0 = np.zeros(N, np.int64)
-    d0 = np.full(N, N, np.int64)
+    d0 = np.full(N, Sk, np.int64)
     c1 = np.zeros(N, np.int64)
     d1 = np.zeros(N, np.int64)  # second interval empty unless set
     if k == "FULL":
         pass
     elif k == "CAUSAL":
-        d0 = i + 1
+        d0 = np.clip(i + off + 1, 0, Sk)
     elif k == "FULL_DOCUMENT":
         _, c0, d0 = _per_key(p["doc_lens"], N)
     elif k == "CAUSAL_DOCUMENT":
@@ -123,12 +139,12 @@ def row_bounds(spec, N: int) -> np.ndarray:
         d0 = i + 1
     elif k == "FULL_SLIDING_WINDOW":
         w = int(p["window"])
-        c0 = np.maximum(0, i - w + 1)
-        d0 = np.minimum(N, i + w)
+        c0 = np.maximum(0, i + off - w + 1)
+        d0 = np.clip(i + off + w, 0, Sk)
     elif k == "CAUSAL_SLIDING_WINDOW":
         w = int(p["window"])
-        c0 = np.maximum(0, i - w + 1)
-        d0 = i + 1
+        c0 = np.maximum(0, i + off - w + 1)
+        d0 = np.clip(i + off + 1, 0, Sk)
     elif k == "SHARED_QUESTION":
         q = int(p["question_len"])
         lens = [q] + [int(x) for x in p["answer_lens"]]
@@ -170,14 +186,16 @@ def row_bounds(spec, N: int) -> np.ndarray:
     return np.ascontiguousarray(out.astype(np.int32))
 
 
-def block_map(spec, N: int, Hq: int):
-    """(keep uint8 [Hq, nQb, nKb], q_offs int32 [nQb+1], k_offs int32 [nKb+1])."""
+def block_map(spec, N: int, Hq: int, Sk=None):
+    """(keep uint8 [Hq, nQb, nKb], q_offs int32 [nQb+1], k_offs int32 [nKb+1])
+    for N query rows and Sk keys (default N)."""
     k, p = spec.kind, spec.params
+    Sk = N if Sk is None else int(Sk)
     if k == "UNIFORM_BLOCK":
         bs = int(p["block"])
-        nb = (N + bs - 1) // bs
-        offs = np.minimum(np.arange(nb + 1, dtype=np.int64) * bs, N)
-        q_offs = k_offs = offs
+        nqb, nkb = (N + bs - 1) // bs, (Sk + bs - 1) // bs
+        q_offs = np.minimum(np.arange(nqb + 1, dtype=np.int64) * bs, N)
+        k_offs = np.minimum(np.arange(nkb + 1, dtype=np.int64) * bs, Sk)
     elif k == "VARIABLE_BLOCK":
         q_offs = np.concatenate([[0], np.cumsum(np.asarray(p["q_block_lens"], np.int64))])
         k_offs = np.concatenate([[0], np.cumsum(np.asarray(p["k_block_lens"], np.int64))])

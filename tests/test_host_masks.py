@@ -125,3 +125,38 @@ def test_builders_reject_bad_lengths():
         masks.col_bounds(MaskSpec("FULL_DOCUMENT", {"doc_lens": [3, 4]}), 8)
     with pytest.raises(ValueError):
         masks.col_bounds(MaskSpec("UNIFORM_BLOCK", {"block": 4, "keep": np.ones((1, 2, 2))}), 8)
+
+
+@pytest.mark.parametrize("Sq,Sk", [(1, 9), (5, 130), (130, 5), (3, 3), (64, 257), (200, 64)])
+def test_rectangular_bounds_match_predicates(Sq, Sk):
+    """Query and key lengths that differ (bottom-right alignment): column and
+    row bounds of FULL, CAUSAL and the sliding windows against the oracle's
+    predicates, and block maps with separate query and key blocks."""
+    rng = np.random.default_rng(Sq * 1000 + Sk)
+    specs = [MaskSpec("FULL"), MaskSpec("CAUSAL")]
+    for w in (1, 2, int(rng.integers(1, Sk + 3)), Sk + Sq):
+        specs += [MaskSpec("FULL_SLIDING_WINDOW", {"window": w}),
+                  MaskSpec("CAUSAL_SLIDING_WINDOW", {"window": w})]
+    for spec in specs:
+        want = allowed(spec, Sq, Sk=Sk)
+        cb = masks.col_bounds(spec, Sq, Sk)
+        assert cb.shape == (Sk, 4)
+        np.testing.assert_array_equal(expand_bounds(cb, Sq), want, err_msg=spec.label())
+        assert masks.allowed_pairs_from_bounds(cb, Sq) == int(want.sum())
+        rb = masks.row_bounds(spec, Sq, Sk)
+        assert rb.shape == (Sq, 4)
+        np.testing.assert_array_equal(expand_rows(rb, Sk), want, err_msg=spec.label())
+    bs = 16
+    keep = rng.random((2, -(-Sq // bs), -(-Sk // bs))) < 0.5
+    spec = MaskSpec("UNIFORM_BLOCK", {"block": bs, "keep": keep})
+    kp, qo, ko = masks.block_map(spec, Sq, 2, Sk)
+    assert qo[-1] == Sq and ko[-1] == Sk
+    for h in range(2):
+        ql, kl = np.diff(qo), np.diff(ko)
+        dense = np.repeat(np.repeat(kp[h].astype(bool), ql, 0), kl, 1)
+        np.testing.assert_array_equal(dense, allowed(spec, Sq, head=h, Sk=Sk))
+
+
+def test_rectangular_rejected_where_undefined():
+    with pytest.raises(ValueError):
+        masks.col_bounds(MaskSpec("PREFIX_LM_CAUSAL", {"prefix": 2}), 4, 6)
