@@ -71,6 +71,10 @@ def workload_desc(wl):
     if wl.selects:
         desc += (f" (dynamic masks selected every step from block-structured Q/K, strength "
                  f"{wl.structure:g}; the selection runs inside the step)")
+    if wl.Sq is not None:
+        desc += f", Sq={wl.Sq} queries per sequence against the N keys (bottom-right aligned)"
+    if wl.forward_only:
+        desc += ", forward only (decode-style rows); FLOPs and bytes of the forward"
     return desc
 
 
@@ -95,7 +99,7 @@ def oracle_sample(wl, seed):
     if wl.structure > 0:
         x = qkv_block_structured(1, wl.N, 1, 1, wl.selects[0].block, strength=wl.structure, seed=seed)
     else:
-        x = qkv(1, wl.N, 1, 1, wl.D, seed=seed)
+        x = qkv(1, wl.q_len, 1, 1, wl.D, seed=seed, Sk=wl.N)
     return {k: t.double().numpy() for k, t in x.items()}
 
 
@@ -116,9 +120,13 @@ def oracle_step(wl, sample):
                                                  "k_block_lens": np.diff(offs).tolist(),
                                                  "keep": keep[0].astype(bool)}))
     for spec in specs:
-        oracle.attention_bwd(sample["q"], sample["k"], sample["v"], sample["do"], spec, scale)
-        pairs = oracle.allowed_pairs(spec, wl.N, head=0)
-        flops += 4.0 * wl.D * pairs * 3.5
+        pairs = oracle.allowed_pairs(spec, wl.q_len, head=0, Sk=wl.N)
+        if wl.forward_only:
+            oracle.attention_fwd(sample["q"], sample["k"], sample["v"], spec, scale)
+            flops += 4.0 * wl.D * pairs
+        else:
+            oracle.attention_bwd(sample["q"], sample["k"], sample["v"], sample["do"], spec, scale)
+            flops += 4.0 * wl.D * pairs * 3.5
     return flops
 
 
@@ -140,7 +148,7 @@ def cpu_baseline(wl, seed):
     dt = time.perf_counter() - t0
     return {"value": flops / dt / 1e12, "unit": UNIT, "cores": cpu_threads(), "kind": "oracle",
             "seconds": round(dt, 3),
-            "sample": f"fp64 NumPy oracle fwd+bwd, query head 0 / KV head 0 of {wl.name} over the full "
+            "sample": f"fp64 NumPy oracle {'fwd' if wl.forward_only else 'fwd+bwd'}, query head 0 / KV head 0 of {wl.name} over the full "
                       f"N={wl.N}, masks {mask_labels(wl)}; effective FLOPs of that head"}
 
 
@@ -237,15 +245,15 @@ class ClockSampler:
 # GPU arm
 # ----------------------------------------------------------------------------
 
-def traffic_lookup(kernel):
-    """DRAM bytes per launch recorded from an ncu capture, if the kernel's source
-    has not changed since (profiles/traffic.json)."""
+def traffic_lookup(kernel, workload):
+    """DRAM bytes per launch recorded from an ncu capture of this kernel on this
+    workload, if the kernel's source has not changed since (profiles/traffic.json)."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
     with open(path) as f:
         rec = json.load(f).get(kernel)
-    if not rec:
+    if not rec or rec.get("workload") != workload:
         return None
     src = os.path.join(ROOT, "long_context_masked_mask_gb300", "csrc", rec["source"])
     sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
@@ -271,20 +279,22 @@ def run_gpu(args, rank, world, dist):
     elif wl.device_inputs:
         x = qkv_device(B, N, Hq, Hkv, D, seed=seed, device=str(dev))
     else:
-        x = {k: t.to(dev) for k, t in qkv(B, N, Hq, Hkv, D, seed=seed).items()}
+        x = {k: t.to(dev) for k, t in qkv(B, wl.q_len, Hq, Hkv, D, seed=seed, Sk=N).items()}
     q, k, v, d_o = x["q"], x["k"], x["v"], x["do"]
+    Sq = q.shape[1]
+    fwd_only = wl.forward_only
     shape = lc.make_shape(q, k, v)
     ws = torch.empty(lc.lcattn_bwd_workspace_size(shape), dtype=torch.uint8, device=dev)
     runs = []
     for spec in wl.masks:
-        m = lc.DeviceMask(spec, N, Hq, B, device=dev)
+        m = lc.DeviceMask(spec, Sq, Hq, B, device=dev, Sk=N)
         meta = lc.lcattn_mask_compile(shape, m, device=dev)
         fwd_flops = 4.0 * D * m.allowed_pairs
         runs.append({"spec": spec, "mask": m, "meta": meta, "o": torch.empty_like(q),
-                     "lse": torch.empty(B, Hq, N, dtype=torch.float32, device=dev),
+                     "lse": torch.empty(B, Hq, Sq, dtype=torch.float32, device=dev),
                      "dq": torch.empty_like(q), "dk": torch.empty_like(k), "dv": torch.empty_like(v),
-                     "fwd_flops": fwd_flops, "bwd_flops": 2.5 * fwd_flops,
-                     "launches": (6 if spec.per_head else 5) + 1 + 3})
+                     "fwd_flops": fwd_flops, "bwd_flops": 0.0 if fwd_only else 2.5 * fwd_flops,
+                     "launches": (6 if spec.per_head else 5) + (0 if fwd_only else 3)})
     for sel in wl.selects:
         offs = torch.from_numpy(offsets_uniform(N, sel.block)).to(dev)
         bmap = torch.empty(B, Hq, offs.numel() - 1, offs.numel() - 1, dtype=torch.uint8, device=dev)
@@ -301,7 +311,12 @@ def run_gpu(args, rank, world, dist):
                      "o": torch.empty_like(q), "lse": torch.empty(B, Hq, N, dtype=torch.float32, device=dev),
                      "dq": torch.empty_like(q), "dk": torch.empty_like(k), "dv": torch.empty_like(v),
                      "fwd_flops": fwd_flops, "bwd_flops": 2.5 * fwd_flops,
-                     "launches": 2 + 6 + 1 + 3})
+                     "launches": 2 + 6 + 3})
+    for r in runs:  # the forward's split-KV workspace (empty unless the query side is short)
+        fws = lc.lcattn_fwd_workspace_size(shape, r["mask"])
+        r["fws"] = torch.empty(max(16, fws), dtype=torch.uint8, device=dev)
+        r["split"] = fws > 0
+        r["launches"] += 2 if fws > 0 else 1  # split-KV forward: slices + merge
     step_flops = sum(r["fwd_flops"] + r["bwd_flops"] for r in runs)
     launches_per_step = sum(r["launches"] for r in runs)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
@@ -318,9 +333,10 @@ def run_gpu(args, rank, world, dist):
             if "sel" in r:
                 select(r, qq, kk)
             lc.lcattn_mask_compile(shape, r["mask"], r["meta"])
-            lc.lcattn_fwd(qq, kk, vv, r["mask"], r["meta"], o=r["o"], lse=r["lse"])
-            lc.lcattn_bwd(qq, kk, vv, r["o"], dd, r["lse"], r["mask"], r["meta"],
-                          dq=r["dq"], dk=r["dk"], dv=r["dv"], workspace=ws)
+            lc.lcattn_fwd_ws(qq, kk, vv, r["mask"], r["meta"], o=r["o"], lse=r["lse"], workspace=r["fws"])
+            if not fwd_only:
+                lc.lcattn_bwd(qq, kk, vv, r["o"], dd, r["lse"], r["mask"], r["meta"],
+                              dq=r["dq"], dk=r["dk"], dv=r["dv"], workspace=ws)
 
     def barrier():
         if dist is not None:
@@ -426,13 +442,14 @@ def run_gpu(args, rank, world, dist):
                            "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": round(gbs / pk["hbm_gbs"], 4),
                            "algorithmic_bytes": pool_bytes,
                            "peak_kind": f"{pk['source']} copy bandwidth",
-                           "traffic": (traffic_lookup("pool_kernel") or {}).get("bytes")}
+                           "traffic": (traffic_lookup("pool_kernel", wl.name) or {}).get("bytes")}
         t_c = timed(lambda: lc.lcattn_mask_compile(shape, m, meta))
-        t_f = timed(lambda: lc.lcattn_fwd(q, k, v, m, meta, o=r["o"], lse=r["lse"]))
-        tb = []
-        for stage in (1, 2, 3):
-            tb.append(timed(lambda: lc.lcattn_bwd(q, k, v, r["o"], d_o, r["lse"], m, meta, dq=r["dq"],
-                                                  dk=r["dk"], dv=r["dv"], workspace=ws, stage=stage)))
+        t_f = timed(lambda: lc.lcattn_fwd_ws(q, k, v, m, meta, o=r["o"], lse=r["lse"], workspace=r["fws"]))
+        tb = [0.0, 0.0, 0.0]
+        if not fwd_only:
+            tb = [timed(lambda: lc.lcattn_bwd(q, k, v, r["o"], d_o, r["lse"], m, meta, dq=r["dq"],
+                                              dk=r["dk"], dv=r["dv"], workspace=ws, stage=stage))
+                  for stage in (1, 2, 3)]
         for name, t, fl in (("mask_compile", t_c, 0.0), ("fwd_kernel", t_f, r["fwd_flops"]),
                             ("bwd_prepass", tb[0], 0.0), ("dkdv_kernel", tb[1], r["bwd_flops"]),
                             ("dq_convert", tb[2], 0.0)):
@@ -440,9 +457,10 @@ def run_gpu(args, rank, world, dist):
             kernels[name][1] += fl
             kernels[name][2] += 1
         fwd_tf = r["fwd_flops"] / (t_f / 1e3) / 1e12
-        bwd_tf = r["bwd_flops"] / (sum(tb) / 1e3) / 1e12
+        bwd_tf = r["bwd_flops"] / (sum(tb) / 1e3) / 1e12 if not fwd_only else 0.0
         per_mask.append({"mask": r["spec"].label(), "allowed_pairs": r["mask"].allowed_pairs,
-                         "density": r["mask"].allowed_pairs / (B * Hq * N * N),
+                         "density": r["mask"].allowed_pairs / (B * Hq * Sq * N),
+                         "forward_path": "split-KV (heads packed)" if r["split"] else "persistent",
                          "fwd_ms": round(t_f, 4), "bwd_ms": round(sum(tb), 4),
                          "bwd_stage_ms": [round(t, 4) for t in tb], "mask_compile_ms": round(t_c, 4),
                          "fwd_tflops": round(fwd_tf, 1), "bwd_tflops": round(bwd_tf, 1),
@@ -452,7 +470,17 @@ def run_gpu(args, rank, world, dist):
             per_mask[-1]["select_ms"] = [round(t_sel[0], 4), round(t_sel[1], 4)]
     dom = max(kernels, key=lambda n: kernels[n][0])
     t_dom, fl_dom, n_dom = kernels[dom]
-    if fl_dom > 0:
+    if fwd_only:
+        # Decode-style rows read every K/V byte once per step and do little
+        # arithmetic per byte: the forward is bound by HBM.  Algorithmic bytes:
+        # Q, K, V read, O and LSE written, per mask.
+        fwd_bytes = (q.numel() + k.numel() + v.numel() + q.numel()) * q.element_size() + B * Hq * Sq * 4
+        gbs = fwd_bytes * n_dom / (t_dom / 1e3) / 1e9
+        roof = {"kernel": "split_kernel + combine_kernel" if runs[0]["split"] else "fwd_kernel",
+                "bound": "hbm", "achieved": round(gbs, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
+                "frac": round(gbs / pk["hbm_gbs"], 4), "algorithmic_bytes": fwd_bytes,
+                "peak_kind": f"{pk['source']} copy bandwidth"}
+    elif fl_dom > 0:
         achieved = fl_dom / (t_dom / 1e3) / 1e12
         roof = {"kernel": dom, "bound": "tensor", "achieved": round(achieved, 1), "peak": pk["sustained"],
                 "unit": "TFLOP/s", "frac": round(achieved / pk["sustained"], 4),
@@ -460,16 +488,18 @@ def run_gpu(args, rank, world, dist):
     else:  # a memory-bound kernel dominating would be reported against HBM
         roof = {"kernel": dom, "bound": "hbm", "achieved": None, "peak": pk["hbm_gbs"], "unit": "GB/s",
                 "frac": None, "peak_kind": f"{pk['source']} copy bandwidth"}
-    tr = traffic_lookup(dom)
+    tr = traffic_lookup(dom, wl.name) if not fwd_only else None
     roof["traffic"] = tr["bytes"] if tr else None
     if tr:
         roof["traffic_launch"] = tr["launch"]
 
     # ---- end to end through the C ABI with host buffers ----------------------
-    host = {n: t.cpu().pin_memory() for n, t in (("q", q), ("k", k), ("v", v), ("do", d_o))}
+    ins = (("q", q), ("k", k), ("v", v)) + ((("do", d_o),) if not fwd_only else ())
+    host = {n: t.cpu().pin_memory() for n, t in ins}
     dq_, dk_, dv_, do_ = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v), torch.empty_like(d_o)
     q_, k_, v_ = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    outs = [{n: torch.empty(r[n].shape, dtype=r[n].dtype, pin_memory=True) for n in ("o", "lse", "dq", "dk", "dv")}
+    out_names = ("o", "lse") if fwd_only else ("o", "lse", "dq", "dk", "dv")
+    outs = [{n: torch.empty(r[n].shape, dtype=r[n].dtype, pin_memory=True) for n in out_names}
             for r in runs]
     h2d = sum(t.numel() * t.element_size() for t in host.values())
     d2h = sum(t.numel() * t.element_size() for o in outs for t in o.values())
@@ -486,7 +516,8 @@ def run_gpu(args, rank, world, dist):
         e0.record(stream)
         copy_stream.wait_stream(stream)
         with torch.cuda.stream(copy_stream):
-            do_.copy_(host["do"], non_blocking=True)
+            if not fwd_only:
+                do_.copy_(host["do"], non_blocking=True)
         do_ready = torch.cuda.Event()
         do_ready.record(copy_stream)
         q_.copy_(host["q"], non_blocking=True)
@@ -496,11 +527,12 @@ def run_gpu(args, rank, world, dist):
             if "sel" in r:
                 select(r, q_, k_)
             lc.lcattn_mask_compile(shape, r["mask"], r["meta"])
-            lc.lcattn_fwd(q_, k_, v_, r["mask"], r["meta"], o=r["o"], lse=r["lse"])
+            lc.lcattn_fwd_ws(q_, k_, v_, r["mask"], r["meta"], o=r["o"], lse=r["lse"], workspace=r["fws"])
             if j == 0:
                 stream.wait_event(do_ready)
-            lc.lcattn_bwd(q_, k_, v_, r["o"], do_, r["lse"], r["mask"], r["meta"],
-                          dq=r["dq"], dk=r["dk"], dv=r["dv"], workspace=ws)
+            if not fwd_only:
+                lc.lcattn_bwd(q_, k_, v_, r["o"], do_, r["lse"], r["mask"], r["meta"],
+                              dq=r["dq"], dk=r["dk"], dv=r["dv"], workspace=ws)
             copy_stream.wait_stream(stream)
             with torch.cuda.stream(copy_stream):
                 for n in o:

@@ -235,6 +235,26 @@ int lcattn_fwd(const lcattn_shape* shape, const void* q, const void* k, const vo
                const void* tile_meta, const lcattn_mask_desc* mask, float scale, void* o,
                float* lse, lcattn_stream_t stream);
 
+/* Forward with a workspace, for short query sides.  When the regular
+ * forward's work items (query tiles x head pairs x batch) are fewer than the
+ * GPU's SMs -- decode-style rows, or a short chunk of queries against a long
+ * key sequence (Sq < Sk, bottom-right aligned) -- and the mask is column
+ * bounds, this call splits every query tile's key-tile list into slices that
+ * run on separate SMs and merges them by their LSE (flash-decoding).  The
+ * query heads of a GQA group share each K/V tile: they are packed into one
+ * 128-row tile (Gp heads x 128/Gp positions, Gp the largest power of two
+ * dividing Hq/Hkv, at most 128).  Otherwise it is exactly lcattn_fwd.
+ * Same arguments and results as lcattn_fwd plus a workspace of
+ * lcattn_fwd_workspace_size bytes (device, 16-byte aligned): fp32 per-slice
+ * O / l [splits][B][Sq][Hq][128] and LSE [splits][B][Hq][Sq].  The split
+ * count, and so the size, depends on the shape, the mask kind and the
+ * current device's SM count; 0 means the call will not split (workspace may
+ * then be NULL).  Two kernels run on `stream`: the slices, then the merge.  */
+size_t lcattn_fwd_workspace_size(const lcattn_shape* shape, const lcattn_mask_desc* mask);
+int lcattn_fwd_ws(const lcattn_shape* shape, const void* q, const void* k, const void* v,
+                  const void* tile_meta, const lcattn_mask_desc* mask, float scale, void* o,
+                  float* lse, void* workspace, size_t workspace_bytes, lcattn_stream_t stream);
+
 /* Workspace (device bytes) lcattn_bwd needs: D = rowsum(dO * O) fp32
  * [B][Hq][Sq], the fp32 dQ accumulator [B][Sq][Hq][128] and, when the dK/dV
  * work units (key tiles x KV heads x batch) are too few to fill the GPU in

@@ -9,6 +9,7 @@ The functions carry the C names:
 
 * :func:`lcattn_mask_compile` -- descriptor -> tile classes and tile lists
 * :func:`lcattn_fwd` -- O and LSE
+* :func:`lcattn_fwd_ws` -- the same, split over the key side for short query sides
 * :func:`lcattn_bwd` -- dQ, dK, dV
 * :func:`lcattn_read_status` -- device status words (bounded-wait expiry etc.)
 * :func:`lcattn_block_select` -- TopK / TopP block map from pooled Q K^T
@@ -55,6 +56,7 @@ EXPORTED = (
     "lcattn_bwd_workspace_size", "lcattn_bwd", "lcattn_bwd_stage", "lcattn_read_status", "lcattn_clear_status",
     "lcattn_status_string", "lcattn_version", "lcattn_bwd_noalloc", "lcattn_selftest_wait_timeout",
     "lcattn_block_select_workspace_size", "lcattn_block_select", "lcattn_block_select_stage",
+    "lcattn_fwd_workspace_size", "lcattn_fwd_ws",
 )
 
 
@@ -116,6 +118,8 @@ def _load():
         "lcattn_selftest_wait_timeout": (ctypes.c_int, [P, P]),
         "lcattn_status_string": (ctypes.c_char_p, [ctypes.c_int]),
         "lcattn_version": (ctypes.c_int, []),
+        "lcattn_fwd_workspace_size": (ctypes.c_size_t, [S, M]),
+        "lcattn_fwd_ws": (ctypes.c_int, [S, P, P, P, P, M, ctypes.c_float, P, P, P, ctypes.c_size_t, P]),
         "lcattn_block_select_workspace_size": (ctypes.c_size_t, [S, SD]),
         "lcattn_block_select": (ctypes.c_int, [S, P, P, SD, ctypes.c_float, P, P, P, ctypes.c_size_t, P]),
         "lcattn_block_select_stage": (ctypes.c_int, [ctypes.c_int, S, P, P, SD, ctypes.c_float, P, P, P,
@@ -281,6 +285,38 @@ def lcattn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, mask: DeviceMa
     return o, lse
 
 
+def lcattn_fwd_workspace_size(shape: lcattn_shape, mask: DeviceMask) -> int:
+    return int(_lib.lcattn_fwd_workspace_size(ctypes.byref(shape), ctypes.byref(mask.desc)))
+
+
+def lcattn_fwd_ws(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, mask: DeviceMask,
+                  tile_meta: torch.Tensor, scale: Optional[float] = None,
+                  o: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                  workspace: Optional[torch.Tensor] = None, stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Forward through lcattn_fwd_ws: splits the key side over SMs when the query
+    side is too short to fill the GPU (decode-style rows), else lcattn_fwd."""
+    B, Sq, Hq, D = q.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty(B, Hq, Sq, dtype=torch.float32, device=q.device)
+    for t in (q, k, v, o):
+        if t.dtype != torch.bfloat16:
+            raise TypeError("q, k, v and o must be bf16")
+    shape = make_shape(q, k, v, o)
+    nbytes = lcattn_fwd_workspace_size(shape, mask)
+    if workspace is None and nbytes > 0:
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
+    ws_ptr = workspace.data_ptr() if workspace is not None else None
+    ws_len = workspace.numel() if workspace is not None else 0
+    _check(_lib.lcattn_fwd_ws(ctypes.byref(shape), q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                              tile_meta.data_ptr(), ctypes.byref(mask.desc), float(scale), o.data_ptr(),
+                              lse.data_ptr(), ws_ptr, ws_len, _stream_ptr(stream)), "lcattn_fwd_ws")
+    return o, lse
+
+
 def lcattn_bwd_workspace_size(shape: lcattn_shape) -> int:
     return int(_lib.lcattn_bwd_workspace_size(ctypes.byref(shape)))
 
@@ -435,7 +471,7 @@ def attention(q, k, v, spec, scale=None, d_o=None, stream=None):
     mask = DeviceMask(spec, N, Hq, B, device=q.device, Sk=k.shape[1])
     shape = make_shape(q, k, v)
     meta = lcattn_mask_compile(shape, mask, stream=stream, device=q.device)
-    o, lse = lcattn_fwd(q, k, v, mask, meta, scale, stream=stream)
+    o, lse = lcattn_fwd_ws(q, k, v, mask, meta, scale, stream=stream)
     out = {"o": o, "lse": lse, "mask": mask, "tile_meta": meta}
     if d_o is not None:
         out["dq"], out["dk"], out["dv"] = lcattn_bwd(q, k, v, o, d_o, lse, mask, meta, scale, stream=stream)

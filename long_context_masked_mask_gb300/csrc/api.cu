@@ -3,6 +3,7 @@
 // compiler, forward and backward kernels.  Allocates nothing.
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <cstring>
 #include <mutex>
 
@@ -127,16 +128,24 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 // [B][S][H][128] bf16 with element strides (b, s, h): 4-D map with a
-// 64-element x 1 head x 128 row box and 128-byte swizzle (one K-major half
-// tile per copy).
+// 64-element x box_h heads x box_s rows box (box_h * box_s = 128 rows of
+// 128 bytes) and 128-byte swizzle (one K-major half tile per copy).
+int encode_bshd_box(CUtensorMap* m, const void* ptr, int64_t B, int64_t S, int64_t H,
+                    const int64_t st[3], uint32_t box_h, uint32_t box_s);
+
 int encode_bshd(CUtensorMap* m, const void* ptr, int64_t B, int64_t S, int64_t H,
                 const int64_t st[3]) {
+  return encode_bshd_box(m, ptr, B, S, H, st, 1, 128);
+}
+
+int encode_bshd_box(CUtensorMap* m, const void* ptr, int64_t B, int64_t S, int64_t H,
+                    const int64_t st[3], uint32_t box_h, uint32_t box_s) {
   auto fn = encode_fn();
   if (!fn) return LCATTN_ERR_CUDA;
   cuuint64_t dims[4] = {(cuuint64_t)kD, (cuuint64_t)H, (cuuint64_t)S, (cuuint64_t)B};
   cuuint64_t strides[3] = {(cuuint64_t)st[2] * 2, (cuuint64_t)st[1] * 2,
                            (cuuint64_t)(st[0] > 0 ? st[0] : S * st[1]) * 2};
-  cuuint32_t box[4] = {64, 1, 128, 1};
+  cuuint32_t box[4] = {64, box_h, box_s, 1};
   cuuint32_t es[4] = {1, 1, 1, 1};
   CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims, strides,
                   box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -218,6 +227,112 @@ int lcattn_fwd(const lcattn_shape* shape, const void* q, const void* k, const vo
   a.o_sb = shape->o_stride[0]; a.o_ss = shape->o_stride[1]; a.o_sh = shape->o_stride[2];
   a.lse = lse;
   return cuda_status(launch_fwd(tq, tk, tv, a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"
+
+namespace {
+
+// Plan for the packed / split-KV forward (short query sides, column bounds).
+// It pays when packing the GQA group's heads into one tile needs at most half
+// the (query tile, key tile) passes of the regular forward -- well under 128
+// query rows per head -- or when the regular forward's items cannot fill the
+// GPU and each walks a long key list.  The split count minimises a simple cost: waves of one CTA per SM
+// times (a fixed cost of about four tiles for launch, pipeline fill and
+// epilogue + the tiles of one slice).
+struct SplitPlan {
+  int splits = 0;  // 0: use the regular forward
+  int Gp = 1, Rq = 128, nQc = 0;
+};
+
+SplitPlan split_plan(const lcattn_shape* s, const lcattn_mask_desc* m) {
+  SplitPlan p;
+  if (m->kind != LCATTN_MASK_COLBOUNDS) return p;
+  int dev = 0, nsm = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || nsm <= 0)
+    return p;
+  const int64_t G = s->Hq / s->Hkv;
+  const int64_t nQt = (s->Sq + kBM - 1) / kBM, nKt = (s->Sk + kBN - 1) / kBN;
+  if (nKt < 4) return p;
+  const int gp = split_heads_packed((int)G);
+  const int64_t rq = 128 / gp;
+  const int64_t nqc = (s->Sq + rq - 1) / rq;
+  const int64_t passes_regular = s->Hq * nQt, passes_packed = s->Hq / gp * nqc;
+  const int64_t hpc = G % 2 == 0 ? 2 : 1;
+  const int64_t items = s->Hq / hpc * s->B * nQt;
+  // Filling idle SMs pays only when each item has a long key list (at 8 key
+  // tiles the slices' merge costs more than the idle SMs: 1K causal, 105 ->
+  // 90 TFLOP/s forward when split).
+  const bool packs = 2 * passes_packed <= passes_regular;
+  const bool fills = items < nsm && nKt >= 16;
+  if (!packs && !fills) return p;
+  const int64_t base = s->B * s->Hkv * (G / gp) * nqc;
+  const int64_t max_splits = std::max<int64_t>(1, std::min<int64_t>(64, nKt / 4));
+  int64_t best = 1;
+  double best_cost = 0.0;
+  for (int64_t k = 1; k <= max_splits; ++k) {
+    const int64_t waves = (base * k + nsm - 1) / nsm;
+    const double cost = (double)waves * (4.0 + (double)nKt / (double)k);
+    if (k == 1 || cost < best_cost) { best = k; best_cost = cost; }
+  }
+  p.Gp = gp;
+  p.Rq = (int)rq;
+  p.nQc = (int)nqc;
+  p.splits = (int)best;
+  return p;
+}
+
+int64_t split_ws_bytes(const lcattn_shape* s, const SplitPlan& p) {
+  if (p.splits == 0) return 0;
+  return align_up((int64_t)p.splits * s->B * s->Sq * s->Hq * kD * 4, 256) +
+         align_up((int64_t)p.splits * s->B * s->Hq * s->Sq * 4, 256);
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t lcattn_fwd_workspace_size(const lcattn_shape* shape, const lcattn_mask_desc* mask) {
+  lcattn_tile_meta_layout L;
+  if (layout_of(shape, mask, &L) != LCATTN_OK) return 0;
+  return (size_t)split_ws_bytes(shape, split_plan(shape, mask));
+}
+
+int lcattn_fwd_ws(const lcattn_shape* shape, const void* q, const void* k, const void* v,
+                  const void* tile_meta, const lcattn_mask_desc* mask, float scale, void* o,
+                  float* lse, void* workspace, size_t workspace_bytes, lcattn_stream_t stream) {
+  lcattn_tile_meta_layout L;
+  int st = layout_of(shape, mask, &L);
+  if (st) return st;
+  const SplitPlan p = split_plan(shape, mask);
+  if (p.splits == 0)
+    return lcattn_fwd(shape, q, k, v, tile_meta, mask, scale, o, lse, stream);
+  if (!q || !k || !v || !o || !lse || !tile_meta || !workspace) return LCATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(tile_meta) ||
+      !aligned16(workspace))
+    return LCATTN_ERR_UNSUPPORTED;
+  if (!(scale > 0.f) || !(scale < 1e30f)) return LCATTN_ERR_INVALID_ARG;
+  if ((int64_t)workspace_bytes < split_ws_bytes(shape, p)) return LCATTN_ERR_WORKSPACE;
+  CUtensorMap tq, tk, tv;
+  if ((st = encode_bshd_box(&tq, q, shape->B, shape->Sq, shape->Hq, shape->q_stride, p.Gp, p.Rq)))
+    return st;
+  if ((st = encode_bshd(&tk, k, shape->B, shape->Sk, shape->Hkv, shape->k_stride))) return st;
+  if ((st = encode_bshd(&tv, v, shape->B, shape->Sk, shape->Hkv, shape->v_stride))) return st;
+  SplitArgs a;
+  a.pr = problem_of(shape);
+  a.mask = mask_of(mask);
+  a.meta = meta_of(L, tile_meta);
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.Gp = p.Gp; a.Rq = p.Rq; a.nQc = p.nQc; a.splits = p.splits;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  a.o_part = reinterpret_cast<float*>(ws);
+  a.lse_part = reinterpret_cast<float*>(
+      ws + align_up((int64_t)p.splits * shape->B * shape->Sq * shape->Hq * kD * 4, 256));
+  a.o = o;
+  a.o_sb = shape->o_stride[0]; a.o_ss = shape->o_stride[1]; a.o_sh = shape->o_stride[2];
+  a.lse = lse;
+  return cuda_status(launch_fwd_split(tq, tk, tv, a, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 size_t lcattn_bwd_workspace_size(const lcattn_shape* shape) {

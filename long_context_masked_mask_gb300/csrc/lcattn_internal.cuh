@@ -59,6 +59,26 @@ struct FwdArgs {
 cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const FwdArgs& a, cudaStream_t st);
 
+// Split-KV forward for short query sides (fwd_split.cu).
+struct SplitArgs {
+  ProblemDev pr;
+  MaskDev mask;             // column bounds (+ optional row bounds) only
+  TileMetaDev meta;
+  float scale_log2;
+  int Gp;                   // query heads packed per tile (a power of two dividing G)
+  int Rq;                   // query positions per tile, Gp * Rq = 128
+  int nQc;                  // query chunks, ceil(Sq / Rq)
+  int splits;               // slices of each key-tile list
+  float* o_part;            // [splits][B][Sq][Hq][128] fp32, O / l of each slice
+  float* lse_part;          // [splits][B][Hq][Sq]
+  void* o;
+  int64_t o_sb, o_ss, o_sh;
+  float* lse;
+};
+int split_heads_packed(int G);
+cudaError_t launch_fwd_split(const CUtensorMap& tq_packed, const CUtensorMap& tk,
+                             const CUtensorMap& tv, const SplitArgs& a, cudaStream_t st);
+
 struct BwdArgs {
   ProblemDev pr;
   MaskDev mask;

@@ -227,6 +227,12 @@ class Workload:
     device_inputs: bool = False  # draw activations on the GPU (largest sizes only)
     selects: List[SelectSpec] = dataclasses.field(default_factory=list)
     structure: float = 0.0       # > 0: block-structured Q/K (qkv_block_structured strength)
+    Sq: Optional[int] = None     # query length when it differs from the key length N
+    forward_only: bool = False   # decode-style rows: the step is the forward alone
+
+    @property
+    def q_len(self) -> int:
+        return self.N if self.Sq is None else self.Sq
 
 
 def workload(name: str, seed: int = 0) -> Workload:
@@ -239,6 +245,8 @@ def workload(name: str, seed: int = 0) -> Workload:
     * ``hetero_16k``: B=1, N=16384, MHA 64:64, the five heterogeneous masks.
     * ``long_128k``: B=1, N=131072, GQA 64:8, CAUSAL and a 128x128 uniform block
       mask kept with probability 0.5 per head (diagonal forced).
+    * ``decode_32k``: B=8 sequences of one query row each against N=32768 keys,
+      GQA 64:8, CAUSAL (bottom-right aligned: the row sees every key), forward only.
     * ``dynamic_32k``: B=1, N=32768, GQA 64:8, block-structured Q/K (strength 1.5),
       and two dynamic block masks chosen from them with 128-token blocks: TopK
       with k = 32 of 256 key blocks, and causal TopP with p = 0.9.
@@ -268,6 +276,8 @@ def workload(name: str, seed: int = 0) -> Workload:
             MaskSpec("CAUSAL"),
             MaskSpec("UNIFORM_BLOCK", {"block": bs, "keep": block_keep(Hq, nb, nb, 0.5, seed)}),
         ], device_inputs=True)
+    if name == "decode_32k":
+        return Workload(name, 8, 32768, 64, 8, 128, [MaskSpec("CAUSAL")], Sq=1, forward_only=True)
     if name == "dynamic_32k":
         return Workload(name, 1, 32768, 64, 8, 128, [],
                         selects=[SelectSpec("topk", 128, top_k=32),
@@ -276,4 +286,4 @@ def workload(name: str, seed: int = 0) -> Workload:
     raise KeyError(name)
 
 
-WORKLOADS = ("causal_1k", "dense_8k", "docs_32k", "hetero_16k", "long_128k", "dynamic_32k")
+WORKLOADS = ("causal_1k", "dense_8k", "docs_32k", "hetero_16k", "long_128k", "dynamic_32k", "decode_32k")

@@ -96,6 +96,15 @@ def run_and_compare(spec, B, N, Hq, Hkv, seed=0, check_classes=True):
         g = out[name].double().cpu().numpy()
         assert np.isfinite(g).all(), name
         assert relf(g, ref) <= G_RELF, (name, relf(g, ref))
+    # attention() runs lcattn_fwd_ws, which takes the split-KV path on small
+    # problems with column bounds; the regular persistent forward must match too.
+    o2, lse2 = lc.lcattn_fwd(dev["q"], dev["k"], dev["v"], out["mask"], out["tile_meta"])
+    o2 = o2.double().cpu().numpy()
+    lse2 = lse2.double().cpu().numpy()
+    assert np.abs(o2 - O).max() <= O_MAXABS and relf(o2, O) <= O_RELF
+    np.testing.assert_array_equal(np.isneginf(lse2), inf_ref)
+    if (~inf_ref).any():
+        assert np.abs(lse2[~inf_ref] - LSE[~inf_ref]).max() <= LSE_MAXABS
     if check_classes:
         shape = lc.make_shape(dev["q"], dev["k"], dev["v"])
         cls = lc.tile_classes(out["tile_meta"], shape, out["mask"]).cpu().numpy()
