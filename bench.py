@@ -488,7 +488,7 @@ def run_gpu(args, rank, world, dist):
     else:  # a memory-bound kernel dominating would be reported against HBM
         roof = {"kernel": dom, "bound": "hbm", "achieved": None, "peak": pk["hbm_gbs"], "unit": "GB/s",
                 "frac": None, "peak_kind": f"{pk['source']} copy bandwidth"}
-    tr = traffic_lookup(dom, wl.name) if not fwd_only else None
+    tr = traffic_lookup("split_kernel" if fwd_only and runs[0]["split"] else dom, wl.name)
     roof["traffic"] = tr["bytes"] if tr else None
     if tr:
         roof["traffic_launch"] = tr["launch"]
