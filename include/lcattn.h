@@ -5,7 +5,8 @@
  * the pages benchmarks ("Long-Context Attention Benchmark: From Kernel
  * Efficiency to Distributed Context Parallelism", xllm-io blog review, sections
  * "密集注意力内核" and "稀疏注意力内核"): softmax attention under a mask, forward
- * and backward, bf16 inputs, head dim 128, MHA and GQA (section "实验设置").
+ * and backward, bf16 inputs, head dim 128 (the pages' setting, section
+ * "实验设置") or 64, MHA and GQA.
  *
  *   S = scale * Q K^T,  P = row softmax over the allowed keys,  O = P V,
  *   LSE_i = ln sum_{j allowed} exp(S_ij)   (-inf for a row that allows nothing)
@@ -28,7 +29,7 @@
  *   - Arguments are validated on the host before anything is launched; an
  *     invalid call returns a negative status and launches nothing.
  *   - Tensors are bf16 (except LSE / D / accumulators, fp32) with the last
- *     dimension (head dim, 128 elements) contiguous; the (batch, sequence,
+ *     dimension (head dim, 64 or 128 elements) contiguous; the (batch, sequence,
  *     head) strides are given in elements and must be multiples of 8 (16
  *     bytes), and base pointers must be 16-byte aligned.
  *   - Query head h reads KV head h / (Hq / Hkv) (contiguous GQA groups).
@@ -48,7 +49,7 @@ typedef struct CUstream_st* lcattn_stream_t; /* same handle as cudaStream_t */
 /* ---- status codes ------------------------------------------------------ */
 #define LCATTN_OK 0
 #define LCATTN_ERR_INVALID_ARG (-1)   /* null pointer, bad size, bad stride      */
-#define LCATTN_ERR_UNSUPPORTED (-2)   /* head dim != 128, Hq % Hkv != 0, alignment */
+#define LCATTN_ERR_UNSUPPORTED (-2)   /* head dim not 64/128, Hq % Hkv != 0, alignment */
 #define LCATTN_ERR_WORKSPACE (-3)     /* buffer smaller than the size query says  */
 #define LCATTN_ERR_CUDA (-4)          /* a CUDA call or launch failed             */
 #define LCATTN_ERR_DEVICE_TIMEOUT (-5)/* a kernel gave up waiting (bounded wait)  */
@@ -62,7 +63,7 @@ typedef struct lcattn_shape {
   int64_t Sk;   /* key length                                               */
   int64_t Hq;   /* query heads                                              */
   int64_t Hkv;  /* key/value heads; Hq % Hkv == 0                          */
-  int64_t D;    /* head dim; must be 128                                    */
+  int64_t D;    /* head dim: 128 or 64 (block selection: 128 only)          */
   /* element strides of (batch, sequence, head); the head dim is contiguous.
    * dO and dQ use q_stride's layout rules with o_stride / q_stride:
    *   O and dO share o_stride, Q and dQ share q_stride,
@@ -202,6 +203,7 @@ typedef struct lcattn_select_desc {
 size_t lcattn_block_select_workspace_size(const lcattn_shape* shape, const lcattn_select_desc* sel);
 
 /* Block selection.  q [B][Sq][Hq][128] and k [B][Sk][Hkv][128] bf16 (device,
+ * head dim 128 only; LCATTN_ERR_UNSUPPORTED otherwise;
  * strides from `shape`; v/o strides unused) -> block_map uint8 [B][Hq][nQb][nKb]
  * (device, 1 = keep, 0 = drop; every byte written), ready for a block-map
  * descriptor with the same offsets.  `scores` (device fp32 [B][Hq][nQb][nKb])
@@ -220,8 +222,8 @@ int lcattn_block_select_stage(int stage, const lcattn_shape* shape, const void* 
                               float* scores, void* workspace, size_t workspace_bytes,
                               lcattn_stream_t stream);
 
-/* Forward.  q [B][Sq][Hq][128], k/v [B][Sk][Hkv][128] bf16 (device) ->
- * o [B][Sq][Hq][128] bf16 and lse [B][Hq][Sq] fp32 (natural log; -inf for a
+/* Forward.  q [B][Sq][Hq][D], k/v [B][Sk][Hkv][D] bf16 (device) ->
+ * o [B][Sq][Hq][D] bf16 and lse [B][Hq][Sq] fp32 (natural log; -inf for a
  * row with no allowed key, whose O row is 0).  `tile_meta` must come from
  * lcattn_mask_compile with the same shape sizes and descriptor, and `mask`
  * is needed again because partial tiles evaluate the mask per element.
@@ -246,7 +248,7 @@ int lcattn_fwd(const lcattn_shape* shape, const void* q, const void* k, const vo
  * dividing Hq/Hkv, at most 128).  Otherwise it is exactly lcattn_fwd.
  * Same arguments and results as lcattn_fwd plus a workspace of
  * lcattn_fwd_workspace_size bytes (device, 16-byte aligned): fp32 per-slice
- * O / l [splits][B][Sq][Hq][128] and LSE [splits][B][Hq][Sq].  The split
+ * O / l [splits][B][Sq][Hq][D] and LSE [splits][B][Hq][Sq].  The split
  * count, and so the size, depends on the shape, the mask kind and the
  * current device's SM count; 0 means the call will not split (workspace may
  * then be NULL).  Two kernels run on `stream`: the slices, then the merge.  */
@@ -256,10 +258,10 @@ int lcattn_fwd_ws(const lcattn_shape* shape, const void* q, const void* k, const
                   float* lse, void* workspace, size_t workspace_bytes, lcattn_stream_t stream);
 
 /* Workspace (device bytes) lcattn_bwd needs: D = rowsum(dO * O) fp32
- * [B][Hq][Sq], the fp32 dQ accumulator [B][Sq][Hq][128] and, when the dK/dV
+ * [B][Hq][Sq], the fp32 dQ accumulator [B][Sq][Hq][D] and, when the dK/dV
  * work units (key tiles x KV heads x batch) are too few to fill the GPU in
  * several waves -- under 1216, and the GQA group splits evenly -- fp32 dK/dV
- * partials [2 or 4][2][B][Sk][Hkv][128]: each unit is split over 2 or 4
+ * partials [2 or 4][2][B][Sk][Hkv][D]: each unit is split over 2 or 4
  * shares of its group's query heads and the partials are summed into dK, dV. */
 size_t lcattn_bwd_workspace_size(const lcattn_shape* shape);
 

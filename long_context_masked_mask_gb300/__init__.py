@@ -1,4 +1,4 @@
-"""GB300-native fused masked attention (forward and backward), bf16, head dim 128.
+"""GB300-native fused masked attention (forward and backward), bf16, head dim 128 or 64.
 
 Python binding of the C-ABI library ``liblcattn.so`` (declared in
 ``include/lcattn.h``).  This module only marshals arguments: every step of the

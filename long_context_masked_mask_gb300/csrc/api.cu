@@ -24,7 +24,7 @@ int validate_shape(const lcattn_shape* s) {
   if (s->B < 1 || s->Sq < 1 || s->Sk < 1 || s->Hq < 1 || s->Hkv < 1) return LCATTN_ERR_INVALID_ARG;
   if (s->Sq > kMaxSeq || s->Sk > kMaxSeq || s->B > 65535 || s->Hq > 65535)
     return LCATTN_ERR_UNSUPPORTED;
-  if (s->D != kD) return LCATTN_ERR_UNSUPPORTED;
+  if (s->D != 128 && s->D != 64) return LCATTN_ERR_UNSUPPORTED;
   if (s->Hq % s->Hkv != 0) return LCATTN_ERR_UNSUPPORTED;
   const int64_t* st[4] = {s->q_stride, s->k_stride, s->v_stride, s->o_stride};
   for (auto x : st)
@@ -34,7 +34,7 @@ int validate_shape(const lcattn_shape* s) {
     }
   // The head and sequence strides must at least separate rows.
   for (auto x : st)
-    if (x[2] < kD || x[1] < kD) return LCATTN_ERR_INVALID_ARG;
+    if (x[2] < s->D || x[1] < s->D) return LCATTN_ERR_INVALID_ARG;
   return LCATTN_OK;
 }
 
@@ -81,6 +81,7 @@ ProblemDev problem_of(const lcattn_shape* s) {
   ProblemDev p;
   p.B = (int)s->B; p.Sq = (int)s->Sq; p.Sk = (int)s->Sk;
   p.Hq = (int)s->Hq; p.Hkv = (int)s->Hkv; p.G = (int)(s->Hq / s->Hkv);
+  p.D = (int)s->D;
   return p;
 }
 
@@ -130,19 +131,19 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 // [B][S][H][128] bf16 with element strides (b, s, h): 4-D map with a
 // 64-element x box_h heads x box_s rows box (box_h * box_s = 128 rows of
 // 128 bytes) and 128-byte swizzle (one K-major half tile per copy).
-int encode_bshd_box(CUtensorMap* m, const void* ptr, int64_t B, int64_t S, int64_t H,
+int encode_bshd_box(CUtensorMap* m, const void* ptr, int64_t B, int64_t S, int64_t H, int64_t D,
                     const int64_t st[3], uint32_t box_h, uint32_t box_s);
 
-int encode_bshd(CUtensorMap* m, const void* ptr, int64_t B, int64_t S, int64_t H,
+int encode_bshd(CUtensorMap* m, const void* ptr, int64_t B, int64_t S, int64_t H, int64_t D,
                 const int64_t st[3]) {
-  return encode_bshd_box(m, ptr, B, S, H, st, 1, 128);
+  return encode_bshd_box(m, ptr, B, S, H, D, st, 1, 128);
 }
 
-int encode_bshd_box(CUtensorMap* m, const void* ptr, int64_t B, int64_t S, int64_t H,
+int encode_bshd_box(CUtensorMap* m, const void* ptr, int64_t B, int64_t S, int64_t H, int64_t D,
                     const int64_t st[3], uint32_t box_h, uint32_t box_s) {
   auto fn = encode_fn();
   if (!fn) return LCATTN_ERR_CUDA;
-  cuuint64_t dims[4] = {(cuuint64_t)kD, (cuuint64_t)H, (cuuint64_t)S, (cuuint64_t)B};
+  cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)S, (cuuint64_t)B};
   cuuint64_t strides[3] = {(cuuint64_t)st[2] * 2, (cuuint64_t)st[1] * 2,
                            (cuuint64_t)(st[0] > 0 ? st[0] : S * st[1]) * 2};
   cuuint32_t box[4] = {64, box_h, box_s, 1};
@@ -172,8 +173,8 @@ int bwd_parts(const lcattn_shape* s) {
 // split units, the fp32 dK/dV partials [parts][2][B][Sk][Hkv][128].
 int64_t bwd_ws_bytes(const lcattn_shape* s, int parts) {
   const int64_t d_bytes = align_up(4 * s->B * s->Hq * s->Sq, 256);
-  const int64_t acc_bytes = align_up(4 * s->B * s->Sq * s->Hq * kD, 256);
-  const int64_t part_bytes = parts > 1 ? (int64_t)parts * 2 * 4 * s->B * s->Sk * s->Hkv * kD : 0;
+  const int64_t acc_bytes = align_up(4 * s->B * s->Sq * s->Hq * s->D, 256);
+  const int64_t part_bytes = parts > 1 ? (int64_t)parts * 2 * 4 * s->B * s->Sk * s->Hkv * s->D : 0;
   return d_bytes + acc_bytes + part_bytes;
 }
 
@@ -215,9 +216,9 @@ int lcattn_fwd(const lcattn_shape* shape, const void* q, const void* k, const vo
     return LCATTN_ERR_UNSUPPORTED;
   if (!(scale > 0.f) || !(scale < 1e30f)) return LCATTN_ERR_INVALID_ARG;
   CUtensorMap tq, tk, tv;
-  if ((st = encode_bshd(&tq, q, shape->B, shape->Sq, shape->Hq, shape->q_stride))) return st;
-  if ((st = encode_bshd(&tk, k, shape->B, shape->Sk, shape->Hkv, shape->k_stride))) return st;
-  if ((st = encode_bshd(&tv, v, shape->B, shape->Sk, shape->Hkv, shape->v_stride))) return st;
+  if ((st = encode_bshd(&tq, q, shape->B, shape->Sq, shape->Hq, shape->D, shape->q_stride))) return st;
+  if ((st = encode_bshd(&tk, k, shape->B, shape->Sk, shape->Hkv, shape->D, shape->k_stride))) return st;
+  if ((st = encode_bshd(&tv, v, shape->B, shape->Sk, shape->Hkv, shape->D, shape->v_stride))) return st;
   FwdArgs a;
   a.pr = problem_of(shape);
   a.mask = mask_of(mask);
@@ -285,7 +286,7 @@ SplitPlan split_plan(const lcattn_shape* s, const lcattn_mask_desc* m) {
 
 int64_t split_ws_bytes(const lcattn_shape* s, const SplitPlan& p) {
   if (p.splits == 0) return 0;
-  return align_up((int64_t)p.splits * s->B * s->Sq * s->Hq * kD * 4, 256) +
+  return align_up((int64_t)p.splits * s->B * s->Sq * s->Hq * s->D * 4, 256) +
          align_up((int64_t)p.splits * s->B * s->Hq * s->Sq * 4, 256);
 }
 
@@ -315,10 +316,10 @@ int lcattn_fwd_ws(const lcattn_shape* shape, const void* q, const void* k, const
   if (!(scale > 0.f) || !(scale < 1e30f)) return LCATTN_ERR_INVALID_ARG;
   if ((int64_t)workspace_bytes < split_ws_bytes(shape, p)) return LCATTN_ERR_WORKSPACE;
   CUtensorMap tq, tk, tv;
-  if ((st = encode_bshd_box(&tq, q, shape->B, shape->Sq, shape->Hq, shape->q_stride, p.Gp, p.Rq)))
+  if ((st = encode_bshd_box(&tq, q, shape->B, shape->Sq, shape->Hq, shape->D, shape->q_stride, p.Gp, p.Rq)))
     return st;
-  if ((st = encode_bshd(&tk, k, shape->B, shape->Sk, shape->Hkv, shape->k_stride))) return st;
-  if ((st = encode_bshd(&tv, v, shape->B, shape->Sk, shape->Hkv, shape->v_stride))) return st;
+  if ((st = encode_bshd(&tk, k, shape->B, shape->Sk, shape->Hkv, shape->D, shape->k_stride))) return st;
+  if ((st = encode_bshd(&tv, v, shape->B, shape->Sk, shape->Hkv, shape->D, shape->v_stride))) return st;
   SplitArgs a;
   a.pr = problem_of(shape);
   a.mask = mask_of(mask);
@@ -328,7 +329,7 @@ int lcattn_fwd_ws(const lcattn_shape* shape, const void* q, const void* k, const
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   a.o_part = reinterpret_cast<float*>(ws);
   a.lse_part = reinterpret_cast<float*>(
-      ws + align_up((int64_t)p.splits * shape->B * shape->Sq * shape->Hq * kD * 4, 256));
+      ws + align_up((int64_t)p.splits * shape->B * shape->Sq * shape->Hq * shape->D * 4, 256));
   a.o = o;
   a.o_sb = shape->o_stride[0]; a.o_ss = shape->o_stride[1]; a.o_sh = shape->o_stride[2];
   a.lse = lse;
@@ -362,10 +363,10 @@ int bwd_run(unsigned stages, const lcattn_shape* shape, const void* q, const voi
   const int parts = allow_split ? bwd_parts(shape) : 1;
   if ((int64_t)workspace_bytes < bwd_ws_bytes(shape, parts)) return LCATTN_ERR_WORKSPACE;
   CUtensorMap tq, tk, tv, tdo;
-  if ((st = encode_bshd(&tq, q, shape->B, shape->Sq, shape->Hq, shape->q_stride))) return st;
-  if ((st = encode_bshd(&tk, k, shape->B, shape->Sk, shape->Hkv, shape->k_stride))) return st;
-  if ((st = encode_bshd(&tv, v, shape->B, shape->Sk, shape->Hkv, shape->v_stride))) return st;
-  if ((st = encode_bshd(&tdo, d_o, shape->B, shape->Sq, shape->Hq, shape->o_stride))) return st;
+  if ((st = encode_bshd(&tq, q, shape->B, shape->Sq, shape->Hq, shape->D, shape->q_stride))) return st;
+  if ((st = encode_bshd(&tk, k, shape->B, shape->Sk, shape->Hkv, shape->D, shape->k_stride))) return st;
+  if ((st = encode_bshd(&tv, v, shape->B, shape->Sk, shape->Hkv, shape->D, shape->v_stride))) return st;
+  if ((st = encode_bshd(&tdo, d_o, shape->B, shape->Sq, shape->Hq, shape->D, shape->o_stride))) return st;
   BwdArgs a;
   a.pr = problem_of(shape);
   a.mask = mask_of(mask);
@@ -484,6 +485,7 @@ int validate_select(const lcattn_shape* s, const lcattn_select_desc* d) {
   if (d->causal != 0 && d->causal != 1) return LCATTN_ERR_INVALID_ARG;
   if (d->nQb < 1 || d->nKb < 1 || d->nQb > s->Sq || d->nKb > s->Sk) return LCATTN_ERR_INVALID_ARG;
   if (d->nKb > LCATTN_SELECT_MAX_KB) return LCATTN_ERR_UNSUPPORTED;
+  if (s->D != 128) return LCATTN_ERR_UNSUPPORTED;  // block means are taken over 128 columns
   // Grid sizes of the two kernels.
   const int64_t slabs_q = (s->Hq + 7) / 8, slabs_k = (s->Hkv + 7) / 8;
   if (s->B * (d->nQb * slabs_q + d->nKb * slabs_k) >= (int64_t(1) << 31)) return LCATTN_ERR_UNSUPPORTED;

@@ -40,8 +40,16 @@ namespace {
 
 using namespace dev;
 
-constexpr int kTileBytes = 32768;
+// Head dim D (64 or 128) is a template parameter.  Q, dO and V tiles are 128
+// rows x D bf16 (D/64 boxes of 64 columns).  The K buffer is always two
+// 64-column halves: with D = 64 its second half stays zero, so that the
+// dQ^T = K^T dS^T product keeps M = 128 (head-dim rows 64-127 come out zero
+// and are not drained).
 constexpr int kHalfBytes = 16384;
+template <int D> struct BwdGeom {
+  static constexpr int kTileBytes = 128 * D * 2;
+  static constexpr int kBoxes = D / 64;
+};
 constexpr int kThreadsDkdv = 512;      // 4 warpgroups
 // Register split for dK/dV (launch: 512 threads x 128): the two elementwise
 // warpgroups 128 each, the dQ drain 136 (a whole dQ^T row in registers),
@@ -55,7 +63,9 @@ constexpr float kLog2e = 1.4426950408889634f;
 // ---------------------------------------------------------------------------
 // 1. D pre-pass
 // ---------------------------------------------------------------------------
+template <int D>
 __global__ void prepass_kernel(BwdArgs a) {
+  constexpr int kPer = D / 32;  // head-dim elements per lane
   const int lane = threadIdx.x & 31;
   const int64_t nrows = (int64_t)a.pr.B * a.pr.Sq * a.pr.Hq;
   const int64_t wstride = (int64_t)gridDim.x * (blockDim.x >> 5);
@@ -64,42 +74,42 @@ __global__ void prepass_kernel(BwdArgs a) {
     const int h = (int)(w % a.pr.Hq);
     const int i = (int)((w / a.pr.Hq) % a.pr.Sq);
     const int b = (int)(w / ((int64_t)a.pr.Hq * a.pr.Sq));
-    const int64_t off = (int64_t)b * a.o_sb + (int64_t)i * a.o_ss + (int64_t)h * a.o_sh;
-    const uint2 ov = __ldg(reinterpret_cast<const uint2*>(
-        reinterpret_cast<const __nv_bfloat16*>(a.o) + off) + lane);
-    const uint2 dv = __ldg(reinterpret_cast<const uint2*>(
-        reinterpret_cast<const __nv_bfloat16*>(a.d_o) + off) + lane);
-    const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(&ov);
-    const __nv_bfloat162* d2 = reinterpret_cast<const __nv_bfloat162*>(&dv);
+    const int64_t off = (int64_t)b * a.o_sb + (int64_t)i * a.o_ss + (int64_t)h * a.o_sh + lane * kPer;
+    const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(
+        reinterpret_cast<const __nv_bfloat16*>(a.o) + off);
+    const __nv_bfloat162* d2 = reinterpret_cast<const __nv_bfloat162*>(
+        reinterpret_cast<const __nv_bfloat16*>(a.d_o) + off);
     float acc = 0.f;
     #pragma unroll
-    for (int k = 0; k < 2; ++k) {
-      const float2 of = __bfloat1622float2(o2[k]);
-      const float2 df = __bfloat1622float2(d2[k]);
+    for (int k = 0; k < kPer / 2; ++k) {
+      const float2 of = __bfloat1622float2(__ldg(o2 + k));
+      const float2 df = __bfloat1622float2(__ldg(d2 + k));
       acc = fmaf(of.x, df.x, acc);
       acc = fmaf(of.y, df.y, acc);
     }
     #pragma unroll
     for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
     if (lane == 0) a.dvec[((int64_t)b * a.pr.Hq + h) * a.pr.Sq + i] = acc;
-    float4* dq = reinterpret_cast<float4*>(a.dq_acc + (((int64_t)b * a.pr.Sq + i) * a.pr.Hq + h) * kD);
-    dq[lane] = make_float4(0.f, 0.f, 0.f, 0.f);
+    float* dq = a.dq_acc + (((int64_t)b * a.pr.Sq + i) * a.pr.Hq + h) * D + lane * kPer;
+    #pragma unroll
+    for (int k = 0; k < kPer; k += 2) *reinterpret_cast<float2*>(dq + k) = make_float2(0.f, 0.f);
   }
 }
 
 // ---------------------------------------------------------------------------
 // 3. dQ conversion
 // ---------------------------------------------------------------------------
+template <int D>
 __global__ void dq_convert_kernel(BwdArgs a) {
-  const int64_t nvec = (int64_t)a.pr.B * a.pr.Sq * a.pr.Hq * (kD / 8);
+  const int64_t nvec = (int64_t)a.pr.B * a.pr.Sq * a.pr.Hq * (D / 8);
   for (int64_t v = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; v < nvec;
        v += (int64_t)gridDim.x * blockDim.x) {
-    const int c = (int)(v % (kD / 8));
-    const int64_t row = v / (kD / 8);  // (b, i, h)
+    const int c = (int)(v % (D / 8));
+    const int64_t row = v / (D / 8);  // (b, i, h)
     const int h = (int)(row % a.pr.Hq);
     const int i = (int)((row / a.pr.Hq) % a.pr.Sq);
     const int b = (int)(row / ((int64_t)a.pr.Hq * a.pr.Sq));
-    const float4* src = reinterpret_cast<const float4*>(a.dq_acc + row * kD + c * 8);
+    const float4* src = reinterpret_cast<const float4*>(a.dq_acc + row * D + c * 8);
     const float4 x = src[0], y = src[1];
     uint4 out;
     out.x = pack_bf16x2(x.x, x.y);
@@ -113,19 +123,20 @@ __global__ void dq_convert_kernel(BwdArgs a) {
 }
 
 // Sum of the split units' fp32 partials -> bf16 dK, dV (8 head dims per step).
+template <int D>
 __global__ void dkv_reduce_kernel(BwdArgs a) {
-  const int64_t per = (int64_t)a.pr.B * a.pr.Sk * a.pr.Hkv * (kD / 8);  // 8-wide groups per tensor
-  const int64_t stride_part = 2 * (int64_t)a.pr.B * a.pr.Sk * a.pr.Hkv * kD;
+  const int64_t per = (int64_t)a.pr.B * a.pr.Sk * a.pr.Hkv * (D / 8);  // 8-wide groups per tensor
+  const int64_t stride_part = 2 * (int64_t)a.pr.B * a.pr.Sk * a.pr.Hkv * D;
   for (int64_t v = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; v < 2 * per;
        v += (int64_t)gridDim.x * blockDim.x) {
     const int w = (int)(v / per);  // 0 = dV, 1 = dK
     const int64_t r = v - (int64_t)w * per;
-    const int c = (int)(r % (kD / 8));
-    const int64_t row = r / (kD / 8);  // (b, key, g)
+    const int c = (int)(r % (D / 8));
+    const int64_t row = r / (D / 8);  // (b, key, g)
     const int g = (int)(row % a.pr.Hkv);
     const int key = (int)((row / a.pr.Hkv) % a.pr.Sk);
     const int b = (int)(row / ((int64_t)a.pr.Hkv * a.pr.Sk));
-    const float* src = a.dkv_part + ((int64_t)w * a.pr.B * a.pr.Sk * a.pr.Hkv + row) * kD + c * 8;
+    const float* src = a.dkv_part + ((int64_t)w * a.pr.B * a.pr.Sk * a.pr.Hkv + row) * D + c * 8;
     float4 s0 = make_float4(0.f, 0.f, 0.f, 0.f), s1 = s0;
     for (int p = 0; p < a.parts; ++p) {
       const float4 x0 = reinterpret_cast<const float4*>(src + p * stride_part)[0];
@@ -145,12 +156,14 @@ __global__ void dkv_reduce_kernel(BwdArgs a) {
 // ---------------------------------------------------------------------------
 // 2. dK / dV
 // ---------------------------------------------------------------------------
+template <int D>
 struct BwdSmem {
-  alignas(1024) uint8_t k[kTileBytes];
+  static constexpr int kTileBytes = BwdGeom<D>::kTileBytes;
+  alignas(1024) uint8_t k[2 * kHalfBytes];  // second half zero when D = 64
   alignas(1024) uint8_t v[kTileBytes];
   alignas(1024) uint8_t q[2][kTileBytes];
   alignas(1024) uint8_t dO[2][kTileBytes];
-  alignas(1024) uint8_t ds[kTileBytes];  // dS^T, keys x queries, read MN-major by dQ^T
+  alignas(1024) uint8_t ds[2 * kHalfBytes];  // dS^T, keys x queries, read MN-major by dQ^T
   // Stored negated, so that the paired fp32 instructions take them as plain
   // addends: -(LSE*log2(e) - log2(scale)) (-inf where P must be 0) and -D.
   alignas(16) float lse2[2][128];
@@ -213,10 +226,13 @@ __device__ __forceinline__ uint32_t range_bits(int lo, int hi, int base) {
   return (n == 32) ? 0xffffffffu : (((1u << n) - 1u) << (a - base));
 }
 
+template <int D>
 __global__ void __launch_bounds__(kThreadsDkdv, 1)
 dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
             const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
             const __grid_constant__ BwdKernelArgs ka) {
+  constexpr int kTileBytes = BwdGeom<D>::kTileBytes;
+  constexpr int kBoxes = BwdGeom<D>::kBoxes;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const BwdArgs& a = ka.a;
   const ProblemDev& pr = a.pr;
@@ -225,7 +241,7 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
     if (threadIdx.x == 0) atomicCAS(gstatus, 0, LCATTN_ERR_CUDA);
     return;
   }
-  BwdSmem& sm = *reinterpret_cast<BwdSmem*>(smem_raw);
+  BwdSmem<D>& sm = *reinterpret_cast<BwdSmem<D>*>(smem_raw);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   const int b = blockIdx.z;
@@ -256,6 +272,13 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
     fence_barrier_init();
   }
   if (warp == 13) tmem_alloc(&sm.tmem_base, 512);
+  if (D == 64) {
+    // Zero half of the K buffer: head-dim rows 64-127 of the padded dQ^T
+    // product.  Written by the generic proxy, read by the tensor cores.
+    reinterpret_cast<uint4*>(sm.k + kHalfBytes)[tid] = make_uint4(0u, 0u, 0u, 0u);
+    reinterpret_cast<uint4*>(sm.k + kHalfBytes)[tid + kThreadsDkdv] = make_uint4(0u, 0u, 0u, 0u);
+    fence_proxy_async_smem();
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -276,10 +299,10 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
     }
     __syncwarp();
     mbar_expect_tx_e(&sm.kv_full, 2 * kTileBytes);
-    tma_load_4d_e(sm.k, &tmK, &sm.kv_full, 0, g, kt * kBN, b);
-    tma_load_4d_e(sm.k + kHalfBytes, &tmK, &sm.kv_full, 64, g, kt * kBN, b);
-    tma_load_4d_e(sm.v, &tmV, &sm.kv_full, 0, g, kt * kBN, b);
-    tma_load_4d_e(sm.v + kHalfBytes, &tmV, &sm.kv_full, 64, g, kt * kBN, b);
+    for (int bx = 0; bx < kBoxes; ++bx) {
+      tma_load_4d_e(sm.k + bx * kHalfBytes, &tmK, &sm.kv_full, 64 * bx, g, kt * kBN, b);
+      tma_load_4d_e(sm.v + bx * kHalfBytes, &tmV, &sm.kv_full, 64 * bx, g, kt * kBN, b);
+    }
     ItemIter it;
     it.init(a.meta, b, kt, pr.G, g, h_lo, h_hi);
     int i = 0, issued = 0;
@@ -292,10 +315,10 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
       const int qt = it.entry() >> 1;
       const int h = it.head();
       mbar_expect_tx_e(&sm.q_full[st], 2 * kTileBytes);
-      tma_load_4d_e(sm.q[st], &tmQ, &sm.q_full[st], 0, h, qt * kBM, b);
-      tma_load_4d_e(sm.q[st] + kHalfBytes, &tmQ, &sm.q_full[st], 64, h, qt * kBM, b);
-      tma_load_4d_e(sm.dO[st], &tmdO, &sm.q_full[st], 0, h, qt * kBM, b);
-      tma_load_4d_e(sm.dO[st] + kHalfBytes, &tmdO, &sm.q_full[st], 64, h, qt * kBM, b);
+      for (int bx = 0; bx < kBoxes; ++bx) {
+        tma_load_4d_e(sm.q[st] + bx * kHalfBytes, &tmQ, &sm.q_full[st], 64 * bx, h, qt * kBM, b);
+        tma_load_4d_e(sm.dO[st] + bx * kHalfBytes, &tmdO, &sm.q_full[st], 64 * bx, h, qt * kBM, b);
+      }
       const float log2_scale = log2f(a.scale);
       const float* lse = a.lse + ((int64_t)b * pr.Hq + h) * pr.Sq;
       const float* dv = a.dvec + ((int64_t)b * pr.Hq + h) * pr.Sq;
@@ -330,7 +353,7 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
     // elected lane.
     {
       const uint32_t id_kmaj = idesc_bf16_f32(128, 128, false, false);
-      const uint32_t id_ts = idesc_bf16_f32(128, 128, false, true);
+      const uint32_t id_ts = idesc_bf16_f32(128, D, false, true);
       const uint32_t id_mn = idesc_bf16_f32(128, 128, true, true);
       const uint32_t tS = tmem, tP = tmem + 128, tdV = tmem + 256, tdK = tmem + 384;
       // Base descriptors (K-major and MN-major views); ring stage st is kTileBytes on.
@@ -349,7 +372,7 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
       auto issue_kmaj = [&](uint32_t d, uint64_t a0, uint64_t b0) {
         mma_ss_e<0>(d, a0, b0, id_kmaj);
         #pragma unroll
-        for (int kk = 1; kk < 8; ++kk) {
+        for (int kk = 1; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
           mma_ss_e<1>(d, sdesc_add(a0, off), sdesc_add(b0, off), id_kmaj);
         }
@@ -431,7 +454,7 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
     // ------------------------------------------------------------ dQ drain
     const int r = 32 * (warp & 3) + lane;  // head-dim row of dQ^T (TMEM lane)
     const uint32_t tQ = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16) + 128;
-    const int64_t dq_row_stride = (int64_t)pr.Hq * kD;
+    const int64_t dq_row_stride = (int64_t)pr.Hq * D;
     ItemIter it;
     it.init(a.meta, b, kt, pr.G, g, h_lo, h_hi);
     for (int i = 0; it.valid(); it.next(), ++i) {
@@ -439,6 +462,10 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
       const int h = it.head();
       bool ok = mbar_wait(&sm.dq_full, i & 1, abort_flag, gstatus, TO);
       if (!__all_sync(0xffffffffu, ok)) break;
+      if (r >= D) {  // zero rows of the padded product (D = 64): nothing to add
+        mbar_arrive(&sm.dq_free);
+        continue;
+      }
       tc_fence_after();
       uint32_t d[128];
       tmem_ld32(tQ, d);
@@ -450,7 +477,7 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
       mbar_arrive(&sm.dq_free);  // columns [128, 256) may take dP^T(i+1) now
       const int q0 = qt * kBM;
       const int nq = min(kBM, pr.Sq - q0);
-      float* dst = a.dq_acc + (((int64_t)b * pr.Sq + q0) * pr.Hq + h) * kD + r;
+      float* dst = a.dq_acc + (((int64_t)b * pr.Sq + q0) * pr.Hq + h) * D + r;
       if (nq == kBM) {
         #pragma unroll
         for (int c = 0; c < 128; ++c) atomicAdd(dst + c * dq_row_stride, __uint_as_float(d[c]));
@@ -624,13 +651,13 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
       const uint32_t tacc = tmem + lane_off + (x == 0 ? 256 : 384);
       // Split units write fp32 partials [part][dV, dK][B][Sk][Hkv][128]; a
       // reduction kernel sums the parts into the bf16 outputs.
-      float* pdst = a.dkv_part + (((((int64_t)part * 2 + x) * pr.B + b) * pr.Sk + key) * pr.Hkv + g) * kD;
+      float* pdst = a.dkv_part + (((((int64_t)part * 2 + x) * pr.B + b) * pr.Sk + key) * pr.Hkv + g) * D;
       __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(x == 0 ? a.dv : a.dk) +
                            (int64_t)b * (x == 0 ? a.v_sb : a.k_sb) +
                            (int64_t)key * (x == 0 ? a.v_ss : a.k_ss) +
                            (int64_t)g * (x == 0 ? a.v_sh : a.k_sh);
       #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < D / 32; ++c) {
         uint32_t xr[32];
         if (have) {
           tmem_ld32(tacc + c * 32, xr);
@@ -668,6 +695,33 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
   }
 }
 
+template <int D>
+cudaError_t launch_dkdv_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                          const CUtensorMap& tdo, const BwdArgs& a, cudaStream_t st) {
+  static bool attr_done = false;
+  const size_t smem = sizeof(BwdSmem<D>);
+  if (!attr_done) {
+    cudaError_t e =
+        cudaFuncSetAttribute(dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    attr_done = true;
+  }
+  BwdKernelArgs ka;
+  ka.a = a;
+  dim3 grid(a.meta.nKt * a.parts, a.pr.Hkv, a.pr.B);
+  dkdv_kernel<D><<<grid, kThreadsDkdv, smem, st>>>(tq, tk, tv, tdo, ka);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess || a.parts == 1) return e;
+  int dev = 0, nsm = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
+  const int64_t n = 2 * (int64_t)a.pr.B * a.pr.Sk * a.pr.Hkv * (D / 8);
+  int64_t blocks = (n + 255) / 256;
+  if (blocks > (int64_t)nsm * 16) blocks = (int64_t)nsm * 16;
+  dkv_reduce_kernel<D><<<(unsigned)blocks, 256, 0, st>>>(a);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t launch_bwd_prepass(const BwdArgs& a, cudaStream_t st) {
@@ -677,44 +731,26 @@ cudaError_t launch_bwd_prepass(const BwdArgs& a, cudaStream_t st) {
   const int64_t rows = (int64_t)a.pr.B * a.pr.Sq * a.pr.Hq;
   int64_t blocks = (rows + 7) / 8;
   if (blocks > (int64_t)nsm * 32) blocks = (int64_t)nsm * 32;
-  prepass_kernel<<<(unsigned)blocks, 256, 0, st>>>(a);
+  if (a.pr.D == 64) prepass_kernel<64><<<(unsigned)blocks, 256, 0, st>>>(a);
+  else prepass_kernel<128><<<(unsigned)blocks, 256, 0, st>>>(a);
   return cudaGetLastError();
 }
 
 cudaError_t launch_bwd_dkdv(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             const CUtensorMap& tdo, const BwdArgs& a, cudaStream_t st) {
-  static bool attr_done = false;
-  const size_t smem = sizeof(BwdSmem);
-  if (!attr_done) {
-    cudaError_t e =
-        cudaFuncSetAttribute(dkdv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    attr_done = true;
-  }
-  BwdKernelArgs ka;
-  ka.a = a;
-  dim3 grid(a.meta.nKt * a.parts, a.pr.Hkv, a.pr.B);
-  dkdv_kernel<<<grid, kThreadsDkdv, smem, st>>>(tq, tk, tv, tdo, ka);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess || a.parts == 1) return e;
-  int dev = 0, nsm = 0;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
-  const int64_t n = 2 * (int64_t)a.pr.B * a.pr.Sk * a.pr.Hkv * (kD / 8);
-  int64_t blocks = (n + 255) / 256;
-  if (blocks > (int64_t)nsm * 16) blocks = (int64_t)nsm * 16;
-  dkv_reduce_kernel<<<(unsigned)blocks, 256, 0, st>>>(a);
-  return cudaGetLastError();
+  return a.pr.D == 64 ? launch_dkdv_d<64>(tq, tk, tv, tdo, a, st)
+                      : launch_dkdv_d<128>(tq, tk, tv, tdo, a, st);
 }
 
 cudaError_t launch_bwd_dq_convert(const BwdArgs& a, cudaStream_t st) {
   int dev = 0, nsm = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
-  const int64_t nvec = (int64_t)a.pr.B * a.pr.Sq * a.pr.Hq * (kD / 8);
+  const int64_t nvec = (int64_t)a.pr.B * a.pr.Sq * a.pr.Hq * (a.pr.D / 8);
   int64_t blocks = (nvec + 255) / 256;
   if (blocks > (int64_t)nsm * 32) blocks = (int64_t)nsm * 32;
-  dq_convert_kernel<<<(unsigned)blocks, 256, 0, st>>>(a);
+  if (a.pr.D == 64) dq_convert_kernel<64><<<(unsigned)blocks, 256, 0, st>>>(a);
+  else dq_convert_kernel<128><<<(unsigned)blocks, 256, 0, st>>>(a);
   return cudaGetLastError();
 }
 

@@ -34,10 +34,16 @@ namespace {
 
 using namespace dev;
 
-constexpr int kStages = 4;          // K/V ring depth (K and V tiles alternate)
+// Head dim D (64 or 128) is a template parameter: a Q, K or V tile is 128 rows
+// x D bf16, loaded as D/64 boxes of 64 columns; the K/V ring holds the same
+// bytes for both (4 stages of 128-wide tiles or 8 of 64-wide ones).
+template <int D> struct FwdGeom {
+  static constexpr int kTileBytes = 128 * D * 2;
+  static constexpr int kBoxes = D / 64;
+  static constexpr int kStages = D == 64 ? 8 : 4;  // K/V ring depth (K and V tiles alternate)
+};
 constexpr int kItemQ = 4;           // depth of the work-item queue (producer -> other roles)
-constexpr int kTileBytes = 32768;   // 128 rows x 128 bf16
-constexpr int kHalfBytes = 16384;   // one 64-column TMA box
+constexpr int kHalfBytes = 16384;   // one 64-column TMA box of 128 rows
 constexpr int kThreads = 384;        // 3 warpgroups
 // Register split (launch: 384 threads x 168): softmax warpgroups 216 each,
 // producer/MMA warpgroup 72.  128 * (216 + 216 + 72) = 384 * 168.
@@ -46,7 +52,10 @@ constexpr int kRegsOther = 72;
 static_assert(128 * (2 * kRegsSoftmax + kRegsOther) <= kThreads * 168, "register split");
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
+template <int D>
 struct FwdSmem {
+  static constexpr int kStages = FwdGeom<D>::kStages;
+  static constexpr int kTileBytes = FwdGeom<D>::kTileBytes;
   alignas(1024) uint8_t q[2][kTileBytes];
   alignas(1024) uint8_t kv[kStages][kTileBytes];
   int4 bnd[2][2][kBN];  // column bounds of a partial tile, per slot, double-buffered
@@ -188,11 +197,15 @@ __device__ __forceinline__ FwdItem fwd_item(const FwdArgs& a, int hpc, int hb, i
   return it;
 }
 
+template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
 fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
            const __grid_constant__ CUtensorMap tmV, const __grid_constant__ FwdKernelArgs ka) {
+  constexpr int kStages = FwdGeom<D>::kStages;
+  constexpr int kTileBytes = FwdGeom<D>::kTileBytes;
+  constexpr int kBoxes = FwdGeom<D>::kBoxes;
   extern __shared__ uint8_t smem_raw[];
-  FwdSmem& sm = *reinterpret_cast<FwdSmem*>(
+  FwdSmem<D>& sm = *reinterpret_cast<FwdSmem<D>*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const FwdArgs& a = ka.a;
   const ProblemDev& pr = a.pr;
@@ -294,10 +307,9 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
         // Warm L2 with the next item's query rows while this item runs.
         const FwdItem nx = fwd_item(a, hpc, hb, nxt);
         if (nx.n > 0)
-          for (int s = 0; s < hpc; ++s) {
-            tma_prefetch_l2_4d_e(&tmQ, 0, nx.h0 + s, nx.qt * kBM, nx.b);
-            tma_prefetch_l2_4d_e(&tmQ, 64, nx.h0 + s, nx.qt * kBM, nx.b);
-          }
+          for (int s = 0; s < hpc; ++s)
+            for (int bx = 0; bx < kBoxes; ++bx)
+              tma_prefetch_l2_4d_e(&tmQ, 64 * bx, nx.h0 + s, nx.qt * kBM, nx.b);
       }
       if (it.n == 0) continue;
       const int g = it.h0 / pr.G;
@@ -311,8 +323,8 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
         const int kt = __ldg(it.list + (u >> 1)) >> 1;
         const CUtensorMap* tm = (u & 1) ? &tmV : &tmK;
         mbar_expect_tx_e(&sm.kv_full[stage], kTileBytes);
-        tma_load_4d_e(sm.kv[stage], tm, &sm.kv_full[stage], 0, g, kt * kBN, it.b);
-        tma_load_4d_e(sm.kv[stage] + kHalfBytes, tm, &sm.kv_full[stage], 64, g, kt * kBN, it.b);
+        for (int bx = 0; bx < kBoxes; ++bx)
+          tma_load_4d_e(sm.kv[stage] + bx * kHalfBytes, tm, &sm.kv_full[stage], 64 * bx, g, kt * kBN, it.b);
         if (u == 0) {
           // Two heads: buffer s holds slot s's Q for every item.  One head:
           // the two buffers alternate between items, so the next item's Q
@@ -326,9 +338,9 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
               if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
             }
             mbar_expect_tx_e(&sm.q_full[qb], kTileBytes);
-            tma_load_4d_e(sm.q[qb], &tmQ, &sm.q_full[qb], 0, it.h0 + s, it.qt * kBM, it.b);
-            tma_load_4d_e(sm.q[qb] + kHalfBytes, &tmQ, &sm.q_full[qb], 64, it.h0 + s,
-                          it.qt * kBM, it.b);
+            for (int bx = 0; bx < kBoxes; ++bx)
+              tma_load_4d_e(sm.q[qb] + bx * kHalfBytes, &tmQ, &sm.q_full[qb], 64 * bx, it.h0 + s,
+                            it.qt * kBM, it.b);
             ++q_issued[qb];
           }
           if (!ok) { ++t; break; }
@@ -360,7 +372,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
     // first P).
     {
       const uint32_t idesc_qk = idesc_bf16_f32(128, 128, false, false);
-      const uint32_t idesc_pv = idesc_bf16_f32(128, 128, false, true);
+      const uint32_t idesc_pv = idesc_bf16_f32(128, D, false, true);
       // Base descriptors; stage s of the ring is kTileBytes further on.
       const uint64_t dq0 = sdesc_sw128(smem_u32(sm.q[0]), 16, 1024);
       const uint64_t dq1 = sdesc_sw128(smem_u32(sm.q[1]), 16, 1024);
@@ -439,7 +451,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
             const uint32_t tS = tmem + (T & 1) * 128;
             mma_ss_e<0>(tS, qd, kb, idesc_qk);
             #pragma unroll
-            for (int kk = 1; kk < 8; ++kk) {
+            for (int kk = 1; kk < D / 16; ++kk) {
               constexpr uint32_t kHalf = kHalfBytes;
               const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
               mma_ss_e<1>(tS, sdesc_add(qd, off), sdesc_add(kb, off), idesc_qk);
@@ -488,7 +500,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
             const uint64_t qd = s ? dq1 : dq0;
             mma_ss_e<0>(tS, qd, kb, idesc_qk);
             #pragma unroll
-            for (int kk = 1; kk < 8; ++kk) {
+            for (int kk = 1; kk < D / 16; ++kk) {
               constexpr uint32_t kHalf = kHalfBytes;
               const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
               mma_ss_e<1>(tS, sdesc_add(qd, off), sdesc_add(kb, off), idesc_qk);
@@ -658,7 +670,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
             if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
             tc_fence_after();
             #pragma unroll
-            for (int c = 0; c < 4; ++c) {
+            for (int c = 0; c < D / 32; ++c) {
               uint32_t o32[32];
               tmem_ld32(tO + c * 32, o32);
               tmem_ld_wait();
@@ -690,20 +702,18 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
           __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(a.o) + (int64_t)b * a.o_sb +
                                 (int64_t)row * a.o_ss + (int64_t)h * a.o_sh;
           // All 128 columns of O in one round trip, then O / l on column pairs.
-          uint32_t o32[128];
+          uint32_t o32[D];
           if (have_o) {
-            tmem_ld32(tO, o32);
-            tmem_ld32(tO + 32, o32 + 32);
-            tmem_ld32(tO + 64, o32 + 64);
-            tmem_ld32(tO + 96, o32 + 96);
+            #pragma unroll
+            for (int c = 0; c < D / 32; ++c) tmem_ld32(tO + c * 32, o32 + c * 32);
             tmem_ld_wait();
           } else {
             #pragma unroll
-            for (int i = 0; i < 128; ++i) o32[i] = 0u;
+            for (int i = 0; i < D; ++i) o32[i] = 0u;
           }
           const float2 inv2 = make_float2(inv, inv);
           #pragma unroll
-          for (int c = 0; c < 4; ++c) {
+          for (int c = 0; c < D / 32; ++c) {
             uint32_t pk[16];
             #pragma unroll
             for (int i = 0; i < 16; ++i) {
@@ -738,15 +748,14 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
   }
 }
 
-}  // namespace
-
-cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                       const FwdArgs& a, cudaStream_t st) {
+template <int D>
+cudaError_t launch_fwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                         const FwdArgs& a, cudaStream_t st) {
   static bool attr_done = false;
-  const size_t smem = sizeof(FwdSmem) + 1024;
+  const size_t smem = sizeof(FwdSmem<D>) + 1024;
   if (!attr_done) {
     cudaError_t e =
-        cudaFuncSetAttribute(fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        cudaFuncSetAttribute(fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     attr_done = true;
   }
@@ -768,8 +777,15 @@ cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
   ka.total_items = static_cast<int>(total);
   // Persistent: one CTA per SM (shared memory admits one), never more CTAs than items.
   const int grid = ka.total_items < nsm ? ka.total_items : nsm;
-  fwd_kernel<<<(unsigned)grid, kThreads, smem, st>>>(tq, tk, tv, ka);
+  fwd_kernel<D><<<(unsigned)grid, kThreads, smem, st>>>(tq, tk, tv, ka);
   return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                       const FwdArgs& a, cudaStream_t st) {
+  return a.pr.D == 64 ? launch_fwd_d<64>(tq, tk, tv, a, st) : launch_fwd_d<128>(tq, tk, tv, a, st);
 }
 
 }  // namespace lcattn

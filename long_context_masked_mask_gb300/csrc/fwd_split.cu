@@ -14,8 +14,9 @@
 //     and its LSE to a workspace;
 //   * combine_kernel merges the slices: LSE = log sum_c exp(LSE_c),
 //     O = sum_c exp(LSE_c - LSE) O_c, written as bf16 with the final LSE.
-// The per-tile pipeline is the regular forward's one-head mode: a 4-stage K/V
-// ring, S double-buffered in TMEM and issued one tile ahead of PV, P written
+// The per-tile pipeline is the regular forward's one-head mode: a K/V ring (4
+// stages of 128-wide tiles, 8 of 64-wide ones), S double-buffered in TMEM and
+// issued one tile ahead of PV, P written
 // over S as bf16 and read from TMEM by the PV GEMM.  Column-bounds masks only
 // (the packed rows of different heads share the mask).
 #include <cuda_bf16.h>
@@ -28,13 +29,21 @@ namespace {
 
 using namespace dev;
 
-constexpr int kStages = 4;
-constexpr int kTileBytes = 32768;
+// Head dim D (64 or 128): tiles are 128 rows x D bf16 (D/64 boxes of 64
+// columns); the K/V ring keeps the same bytes in flight for both.
+template <int D> struct SplitGeom {
+  static constexpr int kTileBytes = 128 * D * 2;
+  static constexpr int kBoxes = D / 64;
+  static constexpr int kStages = D == 64 ? 8 : 4;
+};
 constexpr int kHalfBytes = 16384;
 constexpr int kThreads = 256;  // warps 0-3 softmax, 4 producer, 5 MMA, 6-7 idle
 constexpr float kRescaleThreshold = 8.0f;
 
+template <int D>
 struct SplitSmem {
+  static constexpr int kStages = SplitGeom<D>::kStages;
+  static constexpr int kTileBytes = SplitGeom<D>::kTileBytes;
   alignas(1024) uint8_t q[kTileBytes];
   alignas(1024) uint8_t kv[kStages][kTileBytes];
   int4 bnd[2][kBN];
@@ -73,11 +82,15 @@ __device__ __forceinline__ Unit unit_of(const SplitArgs& a, int u) {
   return x;
 }
 
+template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
 split_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
              const __grid_constant__ CUtensorMap tmV, const __grid_constant__ SplitArgs a) {
+  constexpr int kStages = SplitGeom<D>::kStages;
+  constexpr int kTileBytes = SplitGeom<D>::kTileBytes;
+  constexpr int kBoxes = SplitGeom<D>::kBoxes;
   extern __shared__ uint8_t smem_raw[];
-  SplitSmem& sm = *reinterpret_cast<SplitSmem*>(
+  SplitSmem<D>& sm = *reinterpret_cast<SplitSmem<D>*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const ProblemDev& pr = a.pr;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -137,13 +150,13 @@ split_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
       const int kt = __ldg(list + (u >> 1)) >> 1;
       const CUtensorMap* tm = (u & 1) ? &tmV : &tmK;
       mbar_expect_tx_e(&sm.kv_full[stage], kTileBytes);
-      tma_load_4d_e(sm.kv[stage], tm, &sm.kv_full[stage], 0, un.g, kt * kBN, un.b);
-      tma_load_4d_e(sm.kv[stage] + kHalfBytes, tm, &sm.kv_full[stage], 64, un.g, kt * kBN, un.b);
+      for (int bx = 0; bx < kBoxes; ++bx)
+        tma_load_4d_e(sm.kv[stage] + bx * kHalfBytes, tm, &sm.kv_full[stage], 64 * bx, un.g, kt * kBN, un.b);
       if (u == 0) {
         // Packed query tile: Gp heads x Rq positions; row = position * Gp + head.
         mbar_expect_tx_e(&sm.q_full, kTileBytes);
-        tma_load_4d_e(sm.q, &tmQ, &sm.q_full, 0, h_first, qs0, un.b);
-        tma_load_4d_e(sm.q + kHalfBytes, &tmQ, &sm.q_full, 64, h_first, qs0, un.b);
+        for (int bx = 0; bx < kBoxes; ++bx)
+          tma_load_4d_e(sm.q + bx * kHalfBytes, &tmQ, &sm.q_full, 64 * bx, h_first, qs0, un.b);
       }
     }
     // Never leave copies in flight.
@@ -159,7 +172,7 @@ split_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
   } else if (warp == 5 && n > 0) {
     // ---------------------------------------------------------------- MMA issuer
     const uint32_t idesc_qk = idesc_bf16_f32(128, 128, false, false);
-    const uint32_t idesc_pv = idesc_bf16_f32(128, 128, false, true);
+    const uint32_t idesc_pv = idesc_bf16_f32(128, D, false, true);
     const uint64_t dq = sdesc_sw128(smem_u32(sm.q), 16, 1024);
     const uint64_t dk0 = sdesc_sw128(smem_u32(sm.kv[0]), 16, 1024);
     const uint64_t dv0 = sdesc_sw128(smem_u32(sm.kv[0]), kHalfBytes, 1024);
@@ -196,7 +209,7 @@ split_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
       const uint32_t tS = tmem + (j & 1) * 128;
       mma_ss_e<0>(tS, dq, kb, idesc_qk);
       #pragma unroll
-      for (int kk = 1; kk < 8; ++kk) {
+      for (int kk = 1; kk < D / 16; ++kk) {
         const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
         mma_ss_e<1>(tS, sdesc_add(dq, off), sdesc_add(kb, off), idesc_qk);
       }
@@ -317,7 +330,7 @@ split_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
         tc_fence_after();
         #pragma unroll
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < D / 32; ++c) {
           uint32_t o32[32];
           tmem_ld32(tO + c * 32, o32);
           tmem_ld_wait();
@@ -340,22 +353,20 @@ split_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
     if (ok && (have_o || n == 0)) {
       const bool live = l_run > 0.f;
       const float inv = live ? 1.f / l_run : 0.f;
-      uint32_t o32[128];
+      uint32_t o32[D];
       if (have_o) {
-        tmem_ld32(tO, o32);
-        tmem_ld32(tO + 32, o32 + 32);
-        tmem_ld32(tO + 64, o32 + 64);
-        tmem_ld32(tO + 96, o32 + 96);
+        #pragma unroll
+        for (int c = 0; c < D / 32; ++c) tmem_ld32(tO + c * 32, o32 + c * 32);
         tmem_ld_wait();
       } else {
         #pragma unroll
-        for (int i = 0; i < 128; ++i) o32[i] = 0u;
+        for (int i = 0; i < D; ++i) o32[i] = 0u;
       }
       if (s_pos < pr.Sq) {
         float4* dst = reinterpret_cast<float4*>(
-            a.o_part + ((((int64_t)un.c * pr.B + un.b) * pr.Sq + s_pos) * pr.Hq + h) * kD);
+            a.o_part + ((((int64_t)un.c * pr.B + un.b) * pr.Sq + s_pos) * pr.Hq + h) * D);
         #pragma unroll
-        for (int i = 0; i < 32; ++i)
+        for (int i = 0; i < D / 4; ++i)
           dst[i] = make_float4(__uint_as_float(o32[4 * i]) * inv, __uint_as_float(o32[4 * i + 1]) * inv,
                                __uint_as_float(o32[4 * i + 2]) * inv, __uint_as_float(o32[4 * i + 3]) * inv);
         a.lse_part[(((int64_t)un.c * pr.B + un.b) * pr.Hq + h) * pr.Sq + s_pos] =
@@ -373,13 +384,16 @@ split_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
   }
 }
 
-// One warp per (batch, query position, head): merge the slices.
+// One warp per (batch, query position, head): merge the slices.  Lane l owns
+// columns [l * D/32, (l + 1) * D/32).
+template <int D>
 __global__ void __launch_bounds__(256) combine_kernel(SplitArgs a) {
+  constexpr int kPer = D / 32;
   const ProblemDev& pr = a.pr;
   const int lane = threadIdx.x & 31;
   const int64_t rows = (int64_t)pr.B * pr.Sq * pr.Hq;
   const int64_t stride = (int64_t)gridDim.x * (blockDim.x >> 5);
-  const int64_t per_split_o = (int64_t)pr.B * pr.Sq * pr.Hq * kD;
+  const int64_t per_split_o = (int64_t)pr.B * pr.Sq * pr.Hq * D;
   const int64_t per_split_l = (int64_t)pr.B * pr.Hq * pr.Sq;
   for (int64_t w = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); w < rows; w += stride) {
     const int h = (int)(w % pr.Hq);
@@ -388,23 +402,27 @@ __global__ void __launch_bounds__(256) combine_kernel(SplitArgs a) {
     const int64_t li = ((int64_t)b * pr.Hq + h) * pr.Sq + s;
     float m = -INFINITY;
     for (int c = 0; c < a.splits; ++c) m = fmaxf(m, a.lse_part[c * per_split_l + li]);
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float acc[kPer];
+    #pragma unroll
+    for (int i = 0; i < kPer; ++i) acc[i] = 0.f;
     float wsum = 0.f;
     if (m != -INFINITY) {
       for (int c = 0; c < a.splits; ++c) {
         const float l = a.lse_part[c * per_split_l + li];
         if (l == -INFINITY) continue;
         const float wgt = __expf(l - m);
-        const float4 o = reinterpret_cast<const float4*>(a.o_part + c * per_split_o + w * kD)[lane];
-        acc.x += wgt * o.x; acc.y += wgt * o.y; acc.z += wgt * o.z; acc.w += wgt * o.w;
+        const float* o = a.o_part + c * per_split_o + w * D + lane * kPer;
+        #pragma unroll
+        for (int i = 0; i < kPer; ++i) acc[i] += wgt * o[i];
         wsum += wgt;
       }
     }
     const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
     __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(a.o) + (int64_t)b * a.o_sb +
-                          (int64_t)s * a.o_ss + (int64_t)h * a.o_sh;
-    const uint2 pk = make_uint2(pack_bf16x2(acc.x * inv, acc.y * inv), pack_bf16x2(acc.z * inv, acc.w * inv));
-    reinterpret_cast<uint2*>(orow)[lane] = pk;
+                          (int64_t)s * a.o_ss + (int64_t)h * a.o_sh + lane * kPer;
+    #pragma unroll
+    for (int i = 0; i < kPer; i += 2)
+      reinterpret_cast<uint32_t*>(orow)[i / 2] = pack_bf16x2(acc[i] * inv, acc[i + 1] * inv);
     if (lane == 0) a.lse[li] = wsum > 0.f ? m + __logf(wsum) : -INFINITY;
   }
 }
@@ -417,26 +435,37 @@ int split_heads_packed(int G) {
   return gp;
 }
 
-cudaError_t launch_fwd_split(const CUtensorMap& tq_packed, const CUtensorMap& tk,
-                             const CUtensorMap& tv, const SplitArgs& a, cudaStream_t st) {
+namespace {
+
+template <int D>
+cudaError_t launch_split_d(const CUtensorMap& tq_packed, const CUtensorMap& tk,
+                           const CUtensorMap& tv, const SplitArgs& a, cudaStream_t st) {
   static bool attr_done = false;
-  const size_t smem = sizeof(SplitSmem) + 1024;
+  const size_t smem = sizeof(SplitSmem<D>) + 1024;
   if (!attr_done) {
     cudaError_t e =
-        cudaFuncSetAttribute(split_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        cudaFuncSetAttribute(split_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     attr_done = true;
   }
   const int64_t units = (int64_t)a.pr.B * a.pr.Hkv * (a.pr.G / a.Gp) * a.nQc * a.splits;
   if (units > 0x7fffffffLL) return cudaErrorInvalidValue;
-  split_kernel<<<(unsigned)units, kThreads, smem, st>>>(tq_packed, tk, tv, a);
+  split_kernel<D><<<(unsigned)units, kThreads, smem, st>>>(tq_packed, tk, tv, a);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int64_t rows = (int64_t)a.pr.B * a.pr.Sq * a.pr.Hq;
   int64_t blocks = (rows + 7) / 8;
   if (blocks > 152 * 32) blocks = 152 * 32;
-  combine_kernel<<<(unsigned)blocks, 256, 0, st>>>(a);
+  combine_kernel<D><<<(unsigned)blocks, 256, 0, st>>>(a);
   return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fwd_split(const CUtensorMap& tq_packed, const CUtensorMap& tk,
+                             const CUtensorMap& tv, const SplitArgs& a, cudaStream_t st) {
+  return a.pr.D == 64 ? launch_split_d<64>(tq_packed, tk, tv, a, st)
+                      : launch_split_d<128>(tq_packed, tk, tv, a, st);
 }
 
 }  // namespace lcattn

@@ -41,6 +41,7 @@ struct TileMetaDev {
 
 struct ProblemDev {
   int B, Sq, Sk, Hq, Hkv, G;
+  int D;  // head dim: 64 or 128
 };
 
 // ---- launchers (defined in the kernel translation units) -----------------

@@ -67,7 +67,8 @@ def test_layout_sizes_and_alignment():
 
 
 @pytest.mark.parametrize("field,value,status", [
-    ("D", 64, lc.LCATTN_ERR_UNSUPPORTED),
+    ("D", 96, lc.LCATTN_ERR_UNSUPPORTED),
+    ("D", 256, lc.LCATTN_ERR_UNSUPPORTED),
     ("Hkv", 3, lc.LCATTN_ERR_UNSUPPORTED),
     ("Sq", 0, lc.LCATTN_ERR_INVALID_ARG),
     ("B", 0, lc.LCATTN_ERR_INVALID_ARG),
@@ -169,3 +170,22 @@ def test_block_select_workspace_and_validation():
         assert lib.lcattn_block_select_stage(stage, ctypes.byref(s), 0x1000, 0x1000, ctypes.byref(good),
                                              0.1, 0x1000, None, 0x1000, 1 << 30, None) == \
             lc.LCATTN_ERR_INVALID_ARG
+
+
+def test_head_dim_64_is_accepted():
+    """Head dim 64 is a supported variant (its strides must still separate rows);
+    block selection takes head dim 128 only."""
+    s = _shape(D=64)
+    for name, H in (("q_stride", 4), ("k_stride", 2), ("v_stride", 2), ("o_stride", 4)):
+        getattr(s, name)[:] = (256 * H * 64, H * 64, 64)
+    st, L = _layout(s, _colbounds_desc())
+    assert st == 0
+    assert lc.library().lcattn_bwd_workspace_size(ctypes.byref(s)) == \
+        4 * 4 * 256 + 4 * 256 * 4 * 64 + 2 * 2 * 4 * 256 * 2 * 64
+    s.q_stride[2] = 32  # head stride below the head dim
+    assert _layout(s, _colbounds_desc())[0] == lc.LCATTN_ERR_INVALID_ARG
+    s.q_stride[2] = 64
+    sel = _select_desc()
+    assert lc.library().lcattn_block_select_workspace_size(ctypes.byref(s), ctypes.byref(sel)) == 0
+    assert lc.library().lcattn_block_select(ctypes.byref(s), 0x1000, 0x1000, ctypes.byref(sel), 0.1, 0x1000,
+                                            None, 0x1000, 1 << 30, None) == lc.LCATTN_ERR_UNSUPPORTED

@@ -74,8 +74,7 @@ KINDS = ["FULL", "CAUSAL", "FULL_DOCUMENT", "CAUSAL_DOCUMENT", "FULL_SLIDING_WIN
          "UNIFORM_BLOCK_128", "VARIABLE_BLOCK"]
 
 
-def run_and_compare(spec, B, N, Hq, Hkv, seed=0, check_classes=True):
-    D = 128
+def run_and_compare(spec, B, N, Hq, Hkv, seed=0, check_classes=True, D=128):
     x = qkv(B, N, Hq, Hkv, D, seed=seed)
     dev = {k: t.cuda() for k, t in x.items()}
     out = lc.attention(dev["q"], dev["k"], dev["v"], spec, d_o=dev["do"])
