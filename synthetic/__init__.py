@@ -245,6 +245,8 @@ def workload(name: str, seed: int = 0) -> Workload:
     * ``hetero_16k``: B=1, N=16384, MHA 64:64, the five heterogeneous masks.
     * ``long_128k``: B=1, N=131072, GQA 64:8, CAUSAL and a 128x128 uniform block
       mask kept with probability 0.5 per head (diagonal forced).
+    * ``dense_8k_hd64``: as ``dense_8k`` with head dim 64 (the variant next to the
+      pages' 128).
     * ``decode_32k``: B=8 sequences of one query row each against N=32768 keys,
       GQA 64:8, CAUSAL (bottom-right aligned: the row sees every key), forward only.
     * ``dynamic_32k``: B=1, N=32768, GQA 64:8, block-structured Q/K (strength 1.5),
@@ -276,6 +278,8 @@ def workload(name: str, seed: int = 0) -> Workload:
             MaskSpec("CAUSAL"),
             MaskSpec("UNIFORM_BLOCK", {"block": bs, "keep": block_keep(Hq, nb, nb, 0.5, seed)}),
         ], device_inputs=True)
+    if name == "dense_8k_hd64":
+        return Workload(name, 1, 8192, 64, 8, 64, [MaskSpec("FULL"), MaskSpec("CAUSAL")])
     if name == "decode_32k":
         return Workload(name, 8, 32768, 64, 8, 128, [MaskSpec("CAUSAL")], Sq=1, forward_only=True)
     if name == "dynamic_32k":
@@ -286,4 +290,5 @@ def workload(name: str, seed: int = 0) -> Workload:
     raise KeyError(name)
 
 
-WORKLOADS = ("causal_1k", "dense_8k", "docs_32k", "hetero_16k", "long_128k", "dynamic_32k", "decode_32k")
+WORKLOADS = ("causal_1k", "dense_8k", "docs_32k", "hetero_16k", "long_128k", "dynamic_32k", "decode_32k",
+             "dense_8k_hd64")
