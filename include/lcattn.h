@@ -6,7 +6,7 @@
  * Efficiency to Distributed Context Parallelism", xllm-io blog review, sections
  * "密集注意力内核" and "稀疏注意力内核"): softmax attention under a mask, forward
  * and backward, bf16 inputs, head dim 128 (the pages' setting, section
- * "实验设置") or 64, MHA and GQA.
+ * "实验设置") or 64, and head dim 256 forward only; MHA and GQA.
  *
  *   S = scale * Q K^T,  P = row softmax over the allowed keys,  O = P V,
  *   LSE_i = ln sum_{j allowed} exp(S_ij)   (-inf for a row that allows nothing)
@@ -29,7 +29,7 @@
  *   - Arguments are validated on the host before anything is launched; an
  *     invalid call returns a negative status and launches nothing.
  *   - Tensors are bf16 (except LSE / D / accumulators, fp32) with the last
- *     dimension (head dim, 64 or 128 elements) contiguous; the (batch, sequence,
+ *     dimension (head dim: 64, 128 or 256 elements) contiguous; the (batch, sequence,
  *     head) strides are given in elements and must be multiples of 8 (16
  *     bytes), and base pointers must be 16-byte aligned.
  *   - Query head h reads KV head h / (Hq / Hkv) (contiguous GQA groups).
@@ -49,7 +49,7 @@ typedef struct CUstream_st* lcattn_stream_t; /* same handle as cudaStream_t */
 /* ---- status codes ------------------------------------------------------ */
 #define LCATTN_OK 0
 #define LCATTN_ERR_INVALID_ARG (-1)   /* null pointer, bad size, bad stride      */
-#define LCATTN_ERR_UNSUPPORTED (-2)   /* head dim not 64/128, Hq % Hkv != 0, alignment */
+#define LCATTN_ERR_UNSUPPORTED (-2)   /* head dim, Hq % Hkv != 0, alignment         */
 #define LCATTN_ERR_WORKSPACE (-3)     /* buffer smaller than the size query says  */
 #define LCATTN_ERR_CUDA (-4)          /* a CUDA call or launch failed             */
 #define LCATTN_ERR_DEVICE_TIMEOUT (-5)/* a kernel gave up waiting (bounded wait)  */
@@ -63,7 +63,8 @@ typedef struct lcattn_shape {
   int64_t Sk;   /* key length                                               */
   int64_t Hq;   /* query heads                                              */
   int64_t Hkv;  /* key/value heads; Hq % Hkv == 0                          */
-  int64_t D;    /* head dim: 128 or 64 (block selection: 128 only)          */
+  int64_t D;    /* head dim: 128, 64 or 256 (256: forward only; block
+                 * selection: 128 only)                                     */
   /* element strides of (batch, sequence, head); the head dim is contiguous.
    * dO and dQ use q_stride's layout rules with o_stride / q_stride:
    *   O and dO share o_stride, Q and dQ share q_stride,
@@ -257,7 +258,11 @@ int lcattn_fwd_ws(const lcattn_shape* shape, const void* q, const void* k, const
                   const void* tile_meta, const lcattn_mask_desc* mask, float scale, void* o,
                   float* lse, void* workspace, size_t workspace_bytes, lcattn_stream_t stream);
 
-/* Workspace (device bytes) lcattn_bwd needs: D = rowsum(dO * O) fp32
+/* The backward calls below take head dim 64 or 128; head dim 256 returns
+ * LCATTN_ERR_UNSUPPORTED (its dK and dV accumulators, 2 x 256 fp32 columns,
+ * do not fit in tensor memory beside S and dP) and its workspace size is 0.
+ *
+ * Workspace (device bytes) lcattn_bwd needs: D = rowsum(dO * O) fp32
  * [B][Hq][Sq], the fp32 dQ accumulator [B][Sq][Hq][D] and, when the dK/dV
  * work units (key tiles x KV heads x batch) are too few to fill the GPU in
  * several waves -- under 1216, and the GQA group splits evenly -- fp32 dK/dV

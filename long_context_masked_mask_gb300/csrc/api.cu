@@ -24,7 +24,7 @@ int validate_shape(const lcattn_shape* s) {
   if (s->B < 1 || s->Sq < 1 || s->Sk < 1 || s->Hq < 1 || s->Hkv < 1) return LCATTN_ERR_INVALID_ARG;
   if (s->Sq > kMaxSeq || s->Sk > kMaxSeq || s->B > 65535 || s->Hq > 65535)
     return LCATTN_ERR_UNSUPPORTED;
-  if (s->D != 128 && s->D != 64) return LCATTN_ERR_UNSUPPORTED;
+  if (s->D != 128 && s->D != 64 && s->D != 256) return LCATTN_ERR_UNSUPPORTED;
   if (s->Hq % s->Hkv != 0) return LCATTN_ERR_UNSUPPORTED;
   const int64_t* st[4] = {s->q_stride, s->k_stride, s->v_stride, s->o_stride};
   for (auto x : st)
@@ -337,7 +337,7 @@ int lcattn_fwd_ws(const lcattn_shape* shape, const void* q, const void* k, const
 }
 
 size_t lcattn_bwd_workspace_size(const lcattn_shape* shape) {
-  if (validate_shape(shape) != LCATTN_OK) return 0;
+  if (validate_shape(shape) != LCATTN_OK || shape->D > 128) return 0;
   return (size_t)bwd_ws_bytes(shape, bwd_parts(shape));
 }
 
@@ -354,6 +354,7 @@ int bwd_run(unsigned stages, const lcattn_shape* shape, const void* q, const voi
   lcattn_tile_meta_layout L;
   int st = layout_of(shape, mask, &L);
   if (st) return st;
+  if (shape->D > 128) return LCATTN_ERR_UNSUPPORTED;  // head dim 256: forward only
   if (!q || !k || !v || !o || !d_o || !lse || !tile_meta || !dq || !dk || !dv || !workspace)
     return LCATTN_ERR_INVALID_ARG;
   const void* ptrs[] = {q, k, v, o, d_o, dq, dk, dv, workspace, tile_meta};
@@ -457,6 +458,7 @@ int lcattn_bwd_noalloc(const lcattn_shape* shape, const void* q, const void* k, 
                        lcattn_stream_t stream) {
   int st = validate_shape(shape);
   if (st) return st;
+  if (shape->D > 128) return LCATTN_ERR_UNSUPPORTED;  // head dim 256: forward only
   // No split here: the fixed array holds D and the dQ accumulator only.
   const int64_t need = bwd_ws_bytes(shape, 1);
   if (need > (int64_t)LCATTN_NOALLOC_SCRATCH_BYTES) return LCATTN_ERR_SCRATCH_LIMIT;

@@ -34,13 +34,16 @@ namespace {
 
 using namespace dev;
 
-// Head dim D (64 or 128) is a template parameter: a Q, K or V tile is 128 rows
-// x D bf16, loaded as D/64 boxes of 64 columns; the K/V ring holds the same
-// bytes for both (4 stages of 128-wide tiles or 8 of 64-wide ones).
+// Head dim D (64, 128 or 256) is a template parameter: a Q, K or V tile is 128
+// rows x D bf16, loaded as D/64 boxes of 64 columns.  The K/V ring holds 128 KB
+// (8 stages of 64-wide tiles, 4 of 128-wide, 2 of 256-wide).  At D = 256 an
+// item is always one head (TMEM: two S buffers + a 256-column O) and there is
+// one Q buffer (two would not fit beside the ring).
 template <int D> struct FwdGeom {
   static constexpr int kTileBytes = 128 * D * 2;
   static constexpr int kBoxes = D / 64;
-  static constexpr int kStages = D == 64 ? 8 : 4;  // K/V ring depth (K and V tiles alternate)
+  static constexpr int kStages = D == 64 ? 8 : (D == 128 ? 4 : 2);  // K/V ring depth
+  static constexpr int kQBufs = D == 256 ? 1 : 2;
 };
 constexpr int kItemQ = 4;           // depth of the work-item queue (producer -> other roles)
 constexpr int kHalfBytes = 16384;   // one 64-column TMA box of 128 rows
@@ -56,7 +59,7 @@ template <int D>
 struct FwdSmem {
   static constexpr int kStages = FwdGeom<D>::kStages;
   static constexpr int kTileBytes = FwdGeom<D>::kTileBytes;
-  alignas(1024) uint8_t q[2][kTileBytes];
+  alignas(1024) uint8_t q[FwdGeom<D>::kQBufs][kTileBytes];
   alignas(1024) uint8_t kv[kStages][kTileBytes];
   int4 bnd[2][2][kBN];  // column bounds of a partial tile, per slot, double-buffered
   uint64_t bnd_ready[2][2];
@@ -204,6 +207,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
   constexpr int kStages = FwdGeom<D>::kStages;
   constexpr int kTileBytes = FwdGeom<D>::kTileBytes;
   constexpr int kBoxes = FwdGeom<D>::kBoxes;
+  constexpr int kQBufs = FwdGeom<D>::kQBufs;
   extern __shared__ uint8_t smem_raw[];
   FwdSmem<D>& sm = *reinterpret_cast<FwdSmem<D>*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -330,8 +334,8 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
           // the two buffers alternate between items, so the next item's Q
           // never waits for this item's last S GEMM.
           for (int s = 0; s < hpc && ok; ++s) {
-            const int qb = hpc == 1 ? (nq & 1) : s;
-            const int quse = hpc == 1 ? (nq >> 1) : nq;
+            const int qb = hpc == 1 ? (kQBufs == 2 ? (nq & 1) : 0) : s;
+            const int quse = hpc == 1 && kQBufs == 2 ? (nq >> 1) : nq;
             if (quse > 0) {
               ok = mbar_wait(&sm.q_empty[qb], (quse - 1) & 1, abort_flag, gstatus,
                              LCATTN_ERR_DEVICE_TIMEOUT);
@@ -375,7 +379,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
       const uint32_t idesc_pv = idesc_bf16_f32(128, D, false, true);
       // Base descriptors; stage s of the ring is kTileBytes further on.
       const uint64_t dq0 = sdesc_sw128(smem_u32(sm.q[0]), 16, 1024);
-      const uint64_t dq1 = sdesc_sw128(smem_u32(sm.q[1]), 16, 1024);
+      const uint64_t dq1 = sdesc_sw128(smem_u32(sm.q[kQBufs - 1]), 16, 1024);
       const uint64_t dk0 = sdesc_sw128(smem_u32(sm.kv[0]), 16, 1024);          // K tile, K-major
       const uint64_t dv0 = sdesc_sw128(smem_u32(sm.kv[0]), kHalfBytes, 1024);  // V tile, MN-major
       bool ok = true;
@@ -436,8 +440,9 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
           if (idx < 0) break;
           const int n = fwd_item(a, hpc, hb, idx).n;
           if (n == 0) continue;
-          const int qb = nq & 1;
-          ok = __all_sync(0xffffffffu, mbar_wait(&sm.q_full[qb], (nq >> 1) & 1, abort_flag, gstatus,
+          const int qb = kQBufs == 2 ? (nq & 1) : 0;
+          const int quse = kQBufs == 2 ? (nq >> 1) : nq;
+          ok = __all_sync(0xffffffffu, mbar_wait(&sm.q_full[qb], quse & 1, abort_flag, gstatus,
                                                  LCATTN_ERR_DEVICE_TIMEOUT));
           if (!ok) break;
           const uint64_t qd = qb ? dq1 : dq0;
@@ -450,7 +455,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
             const uint64_t kb = sdesc_add(dk0, (tk % kStages) * kTileBytes);
             const uint32_t tS = tmem + (T & 1) * 128;
             mma_ss_e<0>(tS, qd, kb, idesc_qk);
-            #pragma unroll
+            #pragma unroll (D <= 128 ? D / 16 - 1 : 1)  // the MMA warp has 72 registers
             for (int kk = 1; kk < D / 16; ++kk) {
               constexpr uint32_t kHalf = kHalfBytes;
               const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
@@ -466,7 +471,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
           if (ok) ++nq;
         }
         if (ok && T > 0) issue_pv1(T - 1, acc_prev, true);
-      } else
+      } else if (D <= 128)  // two heads per item (never at D = 256)
       for (int k = 0; ok; ++k) {
         const int e = k % kItemQ;
         ok = mbar_wait(&sm.item_full[e], (k / kItemQ) & 1, abort_flag, gstatus,
@@ -499,7 +504,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
             const uint32_t tS = tmem + s * 128;
             const uint64_t qd = s ? dq1 : dq0;
             mma_ss_e<0>(tS, qd, kb, idesc_qk);
-            #pragma unroll
+            #pragma unroll (D <= 128 ? D / 16 - 1 : 1)  // the MMA warp has 72 registers
             for (int kk = 1; kk < D / 16; ++kk) {
               constexpr uint32_t kHalf = kHalfBytes;
               const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
@@ -669,7 +674,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
                            LCATTN_ERR_DEVICE_TIMEOUT);
             if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
             tc_fence_after();
-            #pragma unroll
+            #pragma unroll (D <= 128 ? D / 32 : 1)
             for (int c = 0; c < D / 32; ++c) {
               uint32_t o32[32];
               tmem_ld32(tO + c * 32, o32);
@@ -702,18 +707,23 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
           __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(a.o) + (int64_t)b * a.o_sb +
                                 (int64_t)row * a.o_ss + (int64_t)h * a.o_sh;
           // All 128 columns of O in one round trip, then O / l on column pairs.
-          uint32_t o32[D];
+          // All of O in one round trip when it fits the registers (D <= 128),
+          // else 32 columns at a time; then O / l on column pairs.
+          constexpr int kBatch = D <= 128 ? D : 32;
+          const float2 inv2 = make_float2(inv, inv);
+          #pragma unroll 1
+          for (int c0 = 0; c0 < D; c0 += kBatch) {
+          uint32_t o32[kBatch];
           if (have_o) {
             #pragma unroll
-            for (int c = 0; c < D / 32; ++c) tmem_ld32(tO + c * 32, o32 + c * 32);
+            for (int c = 0; c < kBatch / 32; ++c) tmem_ld32(tO + c0 + c * 32, o32 + c * 32);
             tmem_ld_wait();
           } else {
             #pragma unroll
-            for (int i = 0; i < D; ++i) o32[i] = 0u;
+            for (int i = 0; i < kBatch; ++i) o32[i] = 0u;
           }
-          const float2 inv2 = make_float2(inv, inv);
           #pragma unroll
-          for (int c = 0; c < D / 32; ++c) {
+          for (int c = 0; c < kBatch / 32; ++c) {
             uint32_t pk[16];
             #pragma unroll
             for (int i = 0; i < 16; ++i) {
@@ -722,11 +732,12 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
               pk[i] = pack_bf16x2(y.x, y.y);
             }
             if (row < pr.Sq) {
-              uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+              uint4* dst = reinterpret_cast<uint4*>(orow + c0 + c * 32);
               #pragma unroll
               for (int i = 0; i < 4; ++i)
                 dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
             }
+          }
           }
           if (row < pr.Sq)
             a.lse[((int64_t)b * pr.Hq + h) * pr.Sq + row] =
@@ -765,8 +776,9 @@ cudaError_t launch_fwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
   if (e != cudaSuccess) return e;
   FwdKernelArgs ka;
   ka.a = a;
-  // Two query heads per CTA when they share the key tiles and the tile list.
-  ka.heads_per_cta = (a.meta.nH == 1 && a.pr.G % 2 == 0) ? 2 : 1;
+  // Two query heads per CTA when they share the key tiles and the tile list
+  // (and two 256-column O accumulators would not fit in TMEM at D = 256).
+  ka.heads_per_cta = (D <= 128 && a.meta.nH == 1 && a.pr.G % 2 == 0) ? 2 : 1;
   // One head per item: the smallest block of whole GQA groups (a divisor of Hq)
   // whose items fill the GPU twice over.
   ka.head_block = a.pr.Hq;
@@ -785,7 +797,9 @@ cudaError_t launch_fwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
 
 cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const FwdArgs& a, cudaStream_t st) {
-  return a.pr.D == 64 ? launch_fwd_d<64>(tq, tk, tv, a, st) : launch_fwd_d<128>(tq, tk, tv, a, st);
+  if (a.pr.D == 64) return launch_fwd_d<64>(tq, tk, tv, a, st);
+  if (a.pr.D == 256) return launch_fwd_d<256>(tq, tk, tv, a, st);
+  return launch_fwd_d<128>(tq, tk, tv, a, st);
 }
 
 }  // namespace lcattn

@@ -29,12 +29,12 @@ namespace {
 
 using namespace dev;
 
-// Head dim D (64 or 128): tiles are 128 rows x D bf16 (D/64 boxes of 64
-// columns); the K/V ring keeps the same bytes in flight for both.
+// Head dim D (64, 128 or 256): tiles are 128 rows x D bf16 (D/64 boxes of 64
+// columns); the K/V ring holds 128 KB (8, 4 or 2 stages).
 template <int D> struct SplitGeom {
   static constexpr int kTileBytes = 128 * D * 2;
   static constexpr int kBoxes = D / 64;
-  static constexpr int kStages = D == 64 ? 8 : 4;
+  static constexpr int kStages = D == 64 ? 8 : (D == 128 ? 4 : 2);
 };
 constexpr int kHalfBytes = 16384;
 constexpr int kThreads = 256;  // warps 0-3 softmax, 4 producer, 5 MMA, 6-7 idle
@@ -208,7 +208,7 @@ split_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
       const uint64_t kb = sdesc_add(dk0, (tk % kStages) * kTileBytes);
       const uint32_t tS = tmem + (j & 1) * 128;
       mma_ss_e<0>(tS, dq, kb, idesc_qk);
-      #pragma unroll
+      #pragma unroll (D <= 128 ? D / 16 - 1 : 1)
       for (int kk = 1; kk < D / 16; ++kk) {
         const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
         mma_ss_e<1>(tS, sdesc_add(dq, off), sdesc_add(kb, off), idesc_qk);
@@ -329,7 +329,7 @@ split_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
         ok = mbar_wait(&sm.o_full, (j - 1) & 1, abort_flag, gstatus, LCATTN_ERR_DEVICE_TIMEOUT);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
         tc_fence_after();
-        #pragma unroll
+        #pragma unroll (D <= 128 ? D / 32 : 1)
         for (int c = 0; c < D / 32; ++c) {
           uint32_t o32[32];
           tmem_ld32(tO + c * 32, o32);
@@ -353,22 +353,29 @@ split_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
     if (ok && (have_o || n == 0)) {
       const bool live = l_run > 0.f;
       const float inv = live ? 1.f / l_run : 0.f;
-      uint32_t o32[D];
-      if (have_o) {
-        #pragma unroll
-        for (int c = 0; c < D / 32; ++c) tmem_ld32(tO + c * 32, o32 + c * 32);
-        tmem_ld_wait();
-      } else {
-        #pragma unroll
-        for (int i = 0; i < D; ++i) o32[i] = 0u;
+      // O in batches that fit the registers (all of it up to D = 128).
+      constexpr int kBatch = D <= 128 ? D : 32;
+      float4* dst = reinterpret_cast<float4*>(
+          a.o_part + ((((int64_t)un.c * pr.B + un.b) * pr.Sq + s_pos) * pr.Hq + h) * D);
+      #pragma unroll 1
+      for (int c0 = 0; c0 < D; c0 += kBatch) {
+        uint32_t o32[kBatch];
+        if (have_o) {
+          #pragma unroll
+          for (int c = 0; c < kBatch / 32; ++c) tmem_ld32(tO + c0 + c * 32, o32 + c * 32);
+          tmem_ld_wait();
+        } else {
+          #pragma unroll
+          for (int i = 0; i < kBatch; ++i) o32[i] = 0u;
+        }
+        if (s_pos < pr.Sq) {
+          #pragma unroll
+          for (int i = 0; i < kBatch / 4; ++i)
+            dst[c0 / 4 + i] = make_float4(__uint_as_float(o32[4 * i]) * inv, __uint_as_float(o32[4 * i + 1]) * inv,
+                                          __uint_as_float(o32[4 * i + 2]) * inv, __uint_as_float(o32[4 * i + 3]) * inv);
+        }
       }
       if (s_pos < pr.Sq) {
-        float4* dst = reinterpret_cast<float4*>(
-            a.o_part + ((((int64_t)un.c * pr.B + un.b) * pr.Sq + s_pos) * pr.Hq + h) * D);
-        #pragma unroll
-        for (int i = 0; i < D / 4; ++i)
-          dst[i] = make_float4(__uint_as_float(o32[4 * i]) * inv, __uint_as_float(o32[4 * i + 1]) * inv,
-                               __uint_as_float(o32[4 * i + 2]) * inv, __uint_as_float(o32[4 * i + 3]) * inv);
         a.lse_part[(((int64_t)un.c * pr.B + un.b) * pr.Hq + h) * pr.Sq + s_pos] =
             live ? (m_run + __log2f(l_run)) * 0.69314718055994531f : -INFINITY;
       }
@@ -464,8 +471,9 @@ cudaError_t launch_split_d(const CUtensorMap& tq_packed, const CUtensorMap& tk,
 
 cudaError_t launch_fwd_split(const CUtensorMap& tq_packed, const CUtensorMap& tk,
                              const CUtensorMap& tv, const SplitArgs& a, cudaStream_t st) {
-  return a.pr.D == 64 ? launch_split_d<64>(tq_packed, tk, tv, a, st)
-                      : launch_split_d<128>(tq_packed, tk, tv, a, st);
+  if (a.pr.D == 64) return launch_split_d<64>(tq_packed, tk, tv, a, st);
+  if (a.pr.D == 256) return launch_split_d<256>(tq_packed, tk, tv, a, st);
+  return launch_split_d<128>(tq_packed, tk, tv, a, st);
 }
 
 }  // namespace lcattn

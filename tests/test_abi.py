@@ -68,7 +68,7 @@ def test_layout_sizes_and_alignment():
 
 @pytest.mark.parametrize("field,value,status", [
     ("D", 96, lc.LCATTN_ERR_UNSUPPORTED),
-    ("D", 256, lc.LCATTN_ERR_UNSUPPORTED),
+    ("D", 512, lc.LCATTN_ERR_UNSUPPORTED),
     ("Hkv", 3, lc.LCATTN_ERR_UNSUPPORTED),
     ("Sq", 0, lc.LCATTN_ERR_INVALID_ARG),
     ("B", 0, lc.LCATTN_ERR_INVALID_ARG),
@@ -189,3 +189,22 @@ def test_head_dim_64_is_accepted():
     assert lc.library().lcattn_block_select_workspace_size(ctypes.byref(s), ctypes.byref(sel)) == 0
     assert lc.library().lcattn_block_select(ctypes.byref(s), 0x1000, 0x1000, ctypes.byref(sel), 0.1, 0x1000,
                                             None, 0x1000, 1 << 30, None) == lc.LCATTN_ERR_UNSUPPORTED
+
+
+def test_head_dim_256_is_forward_only():
+    s = _shape(D=256)
+    for name, H in (("q_stride", 4), ("k_stride", 2), ("v_stride", 2), ("o_stride", 4)):
+        getattr(s, name)[:] = (256 * H * 256, H * 256, 256)
+    d = _colbounds_desc()
+    st, L = _layout(s, d)
+    assert st == 0
+    lib = lc.library()
+    assert lib.lcattn_bwd_workspace_size(ctypes.byref(s)) == 0
+    P = 0x1000
+    args = (ctypes.byref(s), P, P, P, P, P, P, P, ctypes.byref(d), 0.1, P, P, P)
+    assert lib.lcattn_bwd(*args, P, 1 << 30, None) == lc.LCATTN_ERR_UNSUPPORTED
+    assert lib.lcattn_bwd_noalloc(*args, None) == lc.LCATTN_ERR_UNSUPPORTED
+    for stage in (1, 2, 3):
+        assert lib.lcattn_bwd_stage(stage, *args, P, 1 << 30, None) == lc.LCATTN_ERR_UNSUPPORTED
+    s.D = 512
+    assert _layout(s, d)[0] == lc.LCATTN_ERR_UNSUPPORTED
