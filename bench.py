@@ -470,11 +470,14 @@ def run_gpu(args, rank, world, dist):
             per_mask[-1]["select_ms"] = [round(t_sel[0], 4), round(t_sel[1], 4)]
     dom = max(kernels, key=lambda n: kernels[n][0])
     t_dom, fl_dom, n_dom = kernels[dom]
-    if fwd_only:
+    fwd_bytes = (q.numel() + k.numel() + v.numel() + q.numel()) * q.element_size() + B * Hq * Sq * 4
+    # A forward-only step is HBM-bound when its arithmetic intensity (FLOPs per
+    # algorithmic byte) is below the ridge point of the two measured peaks.
+    hbm_bound = fwd_only and (step_flops / len(runs)) / fwd_bytes < pk["sustained"] * 1e12 / (pk["hbm_gbs"] * 1e9)
+    if hbm_bound:
         # Decode-style rows read every K/V byte once per step and do little
-        # arithmetic per byte: the forward is bound by HBM.  Algorithmic bytes:
-        # Q, K, V read, O and LSE written, per mask.
-        fwd_bytes = (q.numel() + k.numel() + v.numel() + q.numel()) * q.element_size() + B * Hq * Sq * 4
+        # arithmetic per byte.  Algorithmic bytes: Q, K, V read, O and LSE
+        # written, per mask.
         gbs = fwd_bytes * n_dom / (t_dom / 1e3) / 1e9
         roof = {"kernel": "split_kernel + combine_kernel" if runs[0]["split"] else "fwd_kernel",
                 "bound": "hbm", "achieved": round(gbs, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
@@ -488,7 +491,7 @@ def run_gpu(args, rank, world, dist):
     else:  # a memory-bound kernel dominating would be reported against HBM
         roof = {"kernel": dom, "bound": "hbm", "achieved": None, "peak": pk["hbm_gbs"], "unit": "GB/s",
                 "frac": None, "peak_kind": f"{pk['source']} copy bandwidth"}
-    tr = traffic_lookup("split_kernel" if fwd_only and runs[0]["split"] else dom, wl.name)
+    tr = traffic_lookup("split_kernel" if hbm_bound and runs[0]["split"] else dom, wl.name)
     roof["traffic"] = tr["bytes"] if tr else None
     if tr:
         roof["traffic_launch"] = tr["launch"]

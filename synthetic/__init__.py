@@ -247,6 +247,8 @@ def workload(name: str, seed: int = 0) -> Workload:
       mask kept with probability 0.5 per head (diagonal forced).
     * ``dense_8k_hd64``: as ``dense_8k`` with head dim 64 (the variant next to the
       pages' 128).
+    * ``dense_8k_hd256_fwd``: B=1, N=8192, GQA 32:8, head dim 256, FULL and CAUSAL,
+      forward only (the head dim whose backward is not built).
     * ``decode_32k``: B=8 sequences of one query row each against N=32768 keys,
       GQA 64:8, CAUSAL (bottom-right aligned: the row sees every key), forward only.
     * ``dynamic_32k``: B=1, N=32768, GQA 64:8, block-structured Q/K (strength 1.5),
@@ -280,6 +282,8 @@ def workload(name: str, seed: int = 0) -> Workload:
         ], device_inputs=True)
     if name == "dense_8k_hd64":
         return Workload(name, 1, 8192, 64, 8, 64, [MaskSpec("FULL"), MaskSpec("CAUSAL")])
+    if name == "dense_8k_hd256_fwd":
+        return Workload(name, 1, 8192, 32, 8, 256, [MaskSpec("FULL"), MaskSpec("CAUSAL")], forward_only=True)
     if name == "decode_32k":
         return Workload(name, 8, 32768, 64, 8, 128, [MaskSpec("CAUSAL")], Sq=1, forward_only=True)
     if name == "dynamic_32k":
@@ -291,4 +295,4 @@ def workload(name: str, seed: int = 0) -> Workload:
 
 
 WORKLOADS = ("causal_1k", "dense_8k", "docs_32k", "hetero_16k", "long_128k", "dynamic_32k", "decode_32k",
-             "dense_8k_hd64")
+             "dense_8k_hd64", "dense_8k_hd256_fwd")
