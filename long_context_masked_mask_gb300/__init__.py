@@ -476,3 +476,30 @@ def attention(q, k, v, spec, scale=None, d_o=None, stream=None):
     if d_o is not None:
         out["dq"], out["dk"], out["dv"] = lcattn_bwd(q, k, v, o, d_o, lse, mask, meta, scale, stream=stream)
     return out
+
+
+class MaskedAttention(torch.autograd.Function):
+    """Autograd binding of the C calls, for use inside a PyTorch training graph:
+    ``MaskedAttention.apply(q, k, v, mask, tile_meta, scale)`` runs lcattn_fwd_ws
+    and, on backward, lcattn_bwd.  ``mask`` is a :class:`DeviceMask` and
+    ``tile_meta`` its compiled buffer (:func:`lcattn_mask_compile`), built once
+    and reused across steps.  Inputs are [B, S, H, D] bf16 tensors with a
+    contiguous last dim; gradients come back in the inputs' layouts."""
+
+    @staticmethod
+    def forward(ctx, q, k, v, mask, tile_meta, scale=None):
+        o, lse = lcattn_fwd_ws(q, k, v, mask, tile_meta, scale)
+        ctx.save_for_backward(q, k, v, o, lse)
+        ctx.mask, ctx.tile_meta, ctx.scale = mask, tile_meta, scale
+        return o
+
+    @staticmethod
+    def backward(ctx, d_o):
+        q, k, v, o, lse = ctx.saved_tensors
+        if d_o.stride() != o.stride():
+            d_o = d_o.contiguous() if o.is_contiguous() else torch.empty_like(o).copy_(d_o)
+        dq = torch.empty_strided(q.shape, q.stride(), dtype=q.dtype, device=q.device)
+        dk = torch.empty_strided(k.shape, k.stride(), dtype=k.dtype, device=k.device)
+        dv = torch.empty_strided(v.shape, v.stride(), dtype=v.dtype, device=v.device)
+        lcattn_bwd(q, k, v, o, d_o, lse, ctx.mask, ctx.tile_meta, ctx.scale, dq=dq, dk=dk, dv=dv)
+        return dq, dk, dv, None, None, None

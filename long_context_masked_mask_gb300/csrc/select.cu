@@ -306,9 +306,15 @@ void select_geometry(int nKb, int* R, int* n2) {
 
 cudaError_t launch_block_select(const SelectArgs& a, cudaStream_t st) {
   const size_t smem = select_smem_bytes(a.R, a.n2, a.nKb);
-  cudaError_t e = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)smem);
-  if (e != cudaSuccess) return e;
+  // Raise the kernel's shared-memory limit only when a call needs more than
+  // any call before (so repeated calls, and graph capture, make no such call).
+  static size_t smem_set = 48 * 1024;
+  if (smem > smem_set) {
+    cudaError_t e = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
+    if (e != cudaSuccess) return e;
+    smem_set = smem;
+  }
   const long long ctas = (long long)a.B * a.Hq * ((a.nQb + a.R - 1) / a.R);
   select_kernel<<<(unsigned)ctas, kSelThreads, smem, st>>>(a);
   return cudaGetLastError();
