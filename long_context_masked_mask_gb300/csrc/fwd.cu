@@ -35,14 +35,19 @@ namespace {
 using namespace dev;
 
 // Head dim D (64, 128 or 256) is a template parameter: a Q, K or V tile is 128
-// rows x D bf16, loaded as D/64 boxes of 64 columns.  The K/V ring holds 128 KB
-// (8 stages of 64-wide tiles, 4 of 128-wide, 2 of 256-wide).  At D = 256 an
-// item is always one head (TMEM: two S buffers + a 256-column O) and there is
-// one Q buffer (two would not fit beside the ring).
+// rows x D bf16, loaded as D/64 boxes of 64 columns.  The K/V ring holds 128 KB.
+// An entry is a whole K or V tile for D <= 128 (8 stages of 64-wide tiles, 4
+// of 128-wide); at D = 256 a tile is two entries, its head-dim halves (4
+// stages of 32 KB), so that the next tile's K streams in while this tile's
+// halves are consumed.  At D = 256 an item is always one head (TMEM: two S
+// buffers + a 256-column O) and there is one Q buffer.
 template <int D> struct FwdGeom {
   static constexpr int kTileBytes = 128 * D * 2;
   static constexpr int kBoxes = D / 64;
-  static constexpr int kStages = D == 64 ? 8 : (D == 128 ? 4 : 2);  // K/V ring depth
+  static constexpr int kParts = D == 256 ? 2 : 1;            // ring entries per K (or V) tile
+  static constexpr int kEntryBytes = kTileBytes / kParts;
+  static constexpr int kBoxesPerEntry = kBoxes / kParts;
+  static constexpr int kStages = D == 64 ? 8 : 4;            // K/V ring depth (entries)
   static constexpr int kQBufs = D == 256 ? 1 : 2;
 };
 constexpr int kItemQ = 4;           // depth of the work-item queue (producer -> other roles)
@@ -60,7 +65,7 @@ struct FwdSmem {
   static constexpr int kStages = FwdGeom<D>::kStages;
   static constexpr int kTileBytes = FwdGeom<D>::kTileBytes;
   alignas(1024) uint8_t q[FwdGeom<D>::kQBufs][kTileBytes];
-  alignas(1024) uint8_t kv[kStages][kTileBytes];
+  alignas(1024) uint8_t kv[kStages][FwdGeom<D>::kEntryBytes];
   int4 bnd[2][2][kBN];  // column bounds of a partial tile, per slot, double-buffered
   uint64_t bnd_ready[2][2];
   uint64_t q_full[2];
@@ -208,6 +213,10 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
   constexpr int kTileBytes = FwdGeom<D>::kTileBytes;
   constexpr int kBoxes = FwdGeom<D>::kBoxes;
   constexpr int kQBufs = FwdGeom<D>::kQBufs;
+  constexpr int kParts = FwdGeom<D>::kParts;
+  constexpr int kEntryBytes = FwdGeom<D>::kEntryBytes;
+  constexpr int kBoxesPerEntry = FwdGeom<D>::kBoxesPerEntry;
+  constexpr int kE = 2 * kParts;  // ring entries per key tile
   extern __shared__ uint8_t smem_raw[];
   FwdSmem<D>& sm = *reinterpret_cast<FwdSmem<D>*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -253,8 +262,8 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
     if (warp == 8) {
     // ---------------------------------------------------------------- producer
     // The whole warp runs the loop (waits included); the elected lane issues.
-    // Ring entry t (counted across items) holds K of tile t/2 for even t and V
-    // of tile t/2 for odd t.  An item's Q tiles go in after its first K tile,
+    // Ring entries (counted across items) go K, V per key tile (K halves then
+    // V halves at D = 256).  An item's Q tiles go in after its first K entry,
     // once the previous item's last S GEMM of that slot has released them.
     if (lane == 0) {
       tma_prefetch_desc(&tmQ);
@@ -317,18 +326,20 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
       }
       if (it.n == 0) continue;
       const int g = it.h0 / pr.G;
-      for (int u = 0; u < 2 * it.n; ++u, ++t) {
+      for (int u = 0; u < kE * it.n; ++u, ++t) {
         const int stage = t % kStages, use = t / kStages;
         if (use > 0) {
           ok = mbar_wait(&sm.kv_empty[stage], (use - 1) & 1, abort_flag, gstatus,
                          LCATTN_ERR_DEVICE_TIMEOUT);
           if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
         }
-        const int kt = __ldg(it.list + (u >> 1)) >> 1;
-        const CUtensorMap* tm = (u & 1) ? &tmV : &tmK;
-        mbar_expect_tx_e(&sm.kv_full[stage], kTileBytes);
-        for (int bx = 0; bx < kBoxes; ++bx)
-          tma_load_4d_e(sm.kv[stage] + bx * kHalfBytes, tm, &sm.kv_full[stage], 64 * bx, g, kt * kBN, it.b);
+        const int part = u % kParts;
+        const int kt = __ldg(it.list + u / kE) >> 1;
+        const CUtensorMap* tm = ((u / kParts) & 1) ? &tmV : &tmK;
+        mbar_expect_tx_e(&sm.kv_full[stage], kEntryBytes);
+        for (int bx = 0; bx < kBoxesPerEntry; ++bx)
+          tma_load_4d_e(sm.kv[stage] + bx * kHalfBytes, tm, &sm.kv_full[stage],
+                        128 * part + 64 * bx, g, kt * kBN, it.b);
         if (u == 0) {
           // Two heads: buffer s holds slot s's Q for every item.  One head:
           // the two buffers alternate between items, so the next item's Q
@@ -376,7 +387,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
     // first P).
     {
       const uint32_t idesc_qk = idesc_bf16_f32(128, 128, false, false);
-      const uint32_t idesc_pv = idesc_bf16_f32(128, D, false, true);
+      const uint32_t idesc_pv = idesc_bf16_f32(128, D / kParts, false, true);
       // Base descriptors; stage s of the ring is kTileBytes further on.
       const uint64_t dq0 = sdesc_sw128(smem_u32(sm.q[0]), 16, 1024);
       const uint64_t dq1 = sdesc_sw128(smem_u32(sm.q[kQBufs - 1]), 16, 1024);
@@ -409,24 +420,28 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
         const uint32_t tO = tmem + 256;
         uint32_t acc_prev = 0u;
         auto issue_pv1 = [&](int tt, uint32_t acc, bool last) -> bool {
-          const int tv = 2 * tt + 1;
-          bool okw = mbar_wait(&sm.kv_full[tv % kStages], (tv / kStages) & 1, abort_flag, gstatus,
-                               LCATTN_ERR_DEVICE_TIMEOUT);
           // P(tt) is released on the barrier of its S buffer: one barrier per
           // buffer keeps the softmax (which can run a tile ahead) from
           // completing a second phase before this wait has seen the first.
-          if (okw) okw = mbar_wait(&sm.p_full[tt & 1], (tt >> 1) & 1, abort_flag, gstatus,
-                                   LCATTN_ERR_DEVICE_TIMEOUT);
-          if (!__all_sync(0xffffffffu, okw)) return false;
-          tc_fence_after();
-          const uint64_t vb = sdesc_add(dv0, (tv % kStages) * kTileBytes);
+          bool okw = mbar_wait(&sm.p_full[tt & 1], (tt >> 1) & 1, abort_flag, gstatus,
+                               LCATTN_ERR_DEVICE_TIMEOUT);
           const uint32_t tP = tmem + (tt & 1) * 128;
-          mma_ts_er(tO, tP, vb, idesc_pv, acc);
-          #pragma unroll
-          for (int kk = 1; kk < 8; ++kk) mma_ts_e<1>(tO, tP + kk * 8, sdesc_add(vb, kk * 2048), idesc_pv);
+          #pragma unroll 1
+          for (int part = 0; part < kParts; ++part) {
+            const int tv = kE * tt + kParts + part;  // V entry: columns [part * D/kParts, ...) of O
+            if (okw) okw = mbar_wait(&sm.kv_full[tv % kStages], (tv / kStages) & 1, abort_flag, gstatus,
+                                     LCATTN_ERR_DEVICE_TIMEOUT);
+            if (!__all_sync(0xffffffffu, okw)) return false;
+            tc_fence_after();
+            const uint64_t vb = sdesc_add(dv0, (tv % kStages) * kEntryBytes);
+            const uint32_t tOp = tO + part * (D / kParts);
+            mma_ts_er(tOp, tP, vb, idesc_pv, acc);
+            #pragma unroll
+            for (int kk = 1; kk < 8; ++kk) mma_ts_e<1>(tOp, tP + kk * 8, sdesc_add(vb, kk * 2048), idesc_pv);
+            tc_commit_e(&sm.kv_empty[tv % kStages]);
+          }
           tc_commit_e(&sm.o_full[0]);
           if (last) tc_commit_e(&sm.o_last[0]);  // the item's O is complete
-          tc_commit_e(&sm.kv_empty[tv % kStages]);
           return true;
         };
         for (int k = 0; ok; ++k) {
@@ -447,22 +462,28 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
           if (!ok) break;
           const uint64_t qd = qb ? dq1 : dq0;
           for (int j = 0; j < n; ++j, ++T) {
-            const int tk = 2 * T;
-            ok = __all_sync(0xffffffffu, mbar_wait(&sm.kv_full[tk % kStages], (tk / kStages) & 1,
-                                                   abort_flag, gstatus, LCATTN_ERR_DEVICE_TIMEOUT));
-            if (!ok) break;
-            tc_fence_after();
-            const uint64_t kb = sdesc_add(dk0, (tk % kStages) * kTileBytes);
             const uint32_t tS = tmem + (T & 1) * 128;
-            mma_ss_e<0>(tS, qd, kb, idesc_qk);
-            #pragma unroll (D <= 128 ? D / 16 - 1 : 1)  // the MMA warp has 72 registers
-            for (int kk = 1; kk < D / 16; ++kk) {
-              constexpr uint32_t kHalf = kHalfBytes;
-              const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
-              mma_ss_e<1>(tS, sdesc_add(qd, off), sdesc_add(kb, off), idesc_qk);
+            #pragma unroll 1
+            for (int part = 0; part < kParts; ++part) {  // K entries: head-dim parts of the tile
+              const int tk = kE * T + part;
+              ok = __all_sync(0xffffffffu, mbar_wait(&sm.kv_full[tk % kStages], (tk / kStages) & 1,
+                                                     abort_flag, gstatus, LCATTN_ERR_DEVICE_TIMEOUT));
+              if (!ok) break;
+              tc_fence_after();
+              const uint64_t kb = sdesc_add(dk0, (tk % kStages) * kEntryBytes);
+              const uint64_t qp = sdesc_add(qd, part * kEntryBytes);
+              if (part == 0) mma_ss_e<0>(tS, qp, kb, idesc_qk);
+              else mma_ss_e<1>(tS, qp, kb, idesc_qk);
+              #pragma unroll
+              for (int kk = 1; kk < D / kParts / 16; ++kk) {
+                constexpr uint32_t kHalf = kHalfBytes;
+                const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
+                mma_ss_e<1>(tS, sdesc_add(qp, off), sdesc_add(kb, off), idesc_qk);
+              }
+              tc_commit_e(&sm.kv_empty[tk % kStages]);
             }
+            if (!ok) break;
             tc_commit_e(&sm.s_full[T & 1]);
-            tc_commit_e(&sm.kv_empty[tk % kStages]);
             if (j == n - 1) tc_commit_e(&sm.q_empty[qb]);  // this item's Q is read for good
             // PV(T-1) closes the previous item when tile T opens a new one.
             if (T > 0 && !issue_pv1(T - 1, acc_prev, j == 0)) { ok = false; break; }

@@ -30,11 +30,16 @@ namespace {
 using namespace dev;
 
 // Head dim D (64, 128 or 256): tiles are 128 rows x D bf16 (D/64 boxes of 64
-// columns); the K/V ring holds 128 KB (8, 4 or 2 stages).
+// columns); the K/V ring holds 128 KB.  A ring entry is a whole K or V tile for
+// D <= 128 (8 or 4 stages) and a head-dim half of one at D = 256 (4 stages of
+// 32 KB, so the next tile's K streams in while this tile is consumed).
 template <int D> struct SplitGeom {
   static constexpr int kTileBytes = 128 * D * 2;
   static constexpr int kBoxes = D / 64;
-  static constexpr int kStages = D == 64 ? 8 : (D == 128 ? 4 : 2);
+  static constexpr int kParts = D == 256 ? 2 : 1;
+  static constexpr int kEntryBytes = kTileBytes / kParts;
+  static constexpr int kBoxesPerEntry = kBoxes / kParts;
+  static constexpr int kStages = D == 64 ? 8 : 4;
 };
 constexpr int kHalfBytes = 16384;
 constexpr int kThreads = 256;  // warps 0-3 softmax, 4 producer, 5 MMA, 6-7 idle
@@ -45,7 +50,7 @@ struct SplitSmem {
   static constexpr int kStages = SplitGeom<D>::kStages;
   static constexpr int kTileBytes = SplitGeom<D>::kTileBytes;
   alignas(1024) uint8_t q[kTileBytes];
-  alignas(1024) uint8_t kv[kStages][kTileBytes];
+  alignas(1024) uint8_t kv[kStages][SplitGeom<D>::kEntryBytes];
   int4 bnd[2][kBN];
   uint64_t bnd_ready[2];
   uint64_t q_full;
@@ -89,6 +94,10 @@ split_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
   constexpr int kStages = SplitGeom<D>::kStages;
   constexpr int kTileBytes = SplitGeom<D>::kTileBytes;
   constexpr int kBoxes = SplitGeom<D>::kBoxes;
+  constexpr int kParts = SplitGeom<D>::kParts;
+  constexpr int kEntryBytes = SplitGeom<D>::kEntryBytes;
+  constexpr int kBoxesPerEntry = SplitGeom<D>::kBoxesPerEntry;
+  constexpr int kE = 2 * kParts;  // ring entries per key tile
   extern __shared__ uint8_t smem_raw[];
   SplitSmem<D>& sm = *reinterpret_cast<SplitSmem<D>*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -140,18 +149,20 @@ split_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
     __syncwarp();
     bool ok = true;
     int t = 0;
-    for (int u = 0; u < 2 * n; ++u, ++t) {
+    for (int u = 0; u < kE * n; ++u, ++t) {
       const int stage = t % kStages, use = t / kStages;
       if (use > 0) {
         ok = mbar_wait(&sm.kv_empty[stage], (use - 1) & 1, abort_flag, gstatus,
                        LCATTN_ERR_DEVICE_TIMEOUT);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       }
-      const int kt = __ldg(list + (u >> 1)) >> 1;
-      const CUtensorMap* tm = (u & 1) ? &tmV : &tmK;
-      mbar_expect_tx_e(&sm.kv_full[stage], kTileBytes);
-      for (int bx = 0; bx < kBoxes; ++bx)
-        tma_load_4d_e(sm.kv[stage] + bx * kHalfBytes, tm, &sm.kv_full[stage], 64 * bx, un.g, kt * kBN, un.b);
+      const int part = u % kParts;
+      const int kt = __ldg(list + u / kE) >> 1;
+      const CUtensorMap* tm = ((u / kParts) & 1) ? &tmV : &tmK;
+      mbar_expect_tx_e(&sm.kv_full[stage], kEntryBytes);
+      for (int bx = 0; bx < kBoxesPerEntry; ++bx)
+        tma_load_4d_e(sm.kv[stage] + bx * kHalfBytes, tm, &sm.kv_full[stage], 128 * part + 64 * bx,
+                      un.g, kt * kBN, un.b);
       if (u == 0) {
         // Packed query tile: Gp heads x Rq positions; row = position * Gp + head.
         mbar_expect_tx_e(&sm.q_full, kTileBytes);
@@ -172,7 +183,7 @@ split_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
   } else if (warp == 5 && n > 0) {
     // ---------------------------------------------------------------- MMA issuer
     const uint32_t idesc_qk = idesc_bf16_f32(128, 128, false, false);
-    const uint32_t idesc_pv = idesc_bf16_f32(128, D, false, true);
+    const uint32_t idesc_pv = idesc_bf16_f32(128, D / kParts, false, true);
     const uint64_t dq = sdesc_sw128(smem_u32(sm.q), 16, 1024);
     const uint64_t dk0 = sdesc_sw128(smem_u32(sm.kv[0]), 16, 1024);
     const uint64_t dv0 = sdesc_sw128(smem_u32(sm.kv[0]), kHalfBytes, 1024);
@@ -181,40 +192,50 @@ split_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
                                                 LCATTN_ERR_DEVICE_TIMEOUT));
     // PV(tt): O (+)= P(tt) V(tt), once the softmax has released P(tt).
     auto issue_pv = [&](int tt) -> bool {
-      const int tv = 2 * tt + 1;
-      bool okw = mbar_wait(&sm.kv_full[tv % kStages], (tv / kStages) & 1, abort_flag, gstatus,
+      bool okw = mbar_wait(&sm.p_full[tt & 1], (tt >> 1) & 1, abort_flag, gstatus,
                            LCATTN_ERR_DEVICE_TIMEOUT);
-      if (okw) okw = mbar_wait(&sm.p_full[tt & 1], (tt >> 1) & 1, abort_flag, gstatus,
-                               LCATTN_ERR_DEVICE_TIMEOUT);
-      if (!__all_sync(0xffffffffu, okw)) return false;
-      tc_fence_after();
-      const uint64_t vb = sdesc_add(dv0, (tv % kStages) * kTileBytes);
       const uint32_t tP = tmem + (tt & 1) * 128;
-      mma_ts_er(tO, tP, vb, idesc_pv, tt > 0 ? 1u : 0u);
-      #pragma unroll
-      for (int kk = 1; kk < 8; ++kk) mma_ts_e<1>(tO, tP + kk * 8, sdesc_add(vb, kk * 2048), idesc_pv);
+      #pragma unroll 1
+      for (int part = 0; part < kParts; ++part) {  // V entries: columns [part * D/kParts, ...) of O
+        const int tv = kE * tt + kParts + part;
+        if (okw) okw = mbar_wait(&sm.kv_full[tv % kStages], (tv / kStages) & 1, abort_flag, gstatus,
+                                 LCATTN_ERR_DEVICE_TIMEOUT);
+        if (!__all_sync(0xffffffffu, okw)) return false;
+        tc_fence_after();
+        const uint64_t vb = sdesc_add(dv0, (tv % kStages) * kEntryBytes);
+        const uint32_t tOp = tO + part * (D / kParts);
+        mma_ts_er(tOp, tP, vb, idesc_pv, tt > 0 ? 1u : 0u);
+        #pragma unroll
+        for (int kk = 1; kk < 8; ++kk) mma_ts_e<1>(tOp, tP + kk * 8, sdesc_add(vb, kk * 2048), idesc_pv);
+        tc_commit_e(&sm.kv_empty[tv % kStages]);
+      }
       tc_commit_e(&sm.o_full);
       if (tt == n - 1) tc_commit_e(&sm.o_done);
-      tc_commit_e(&sm.kv_empty[tv % kStages]);
       return true;
     };
     if (ok) tc_fence_after();
     for (int j = 0; ok && j < n; ++j) {
-      const int tk = 2 * j;
-      ok = __all_sync(0xffffffffu, mbar_wait(&sm.kv_full[tk % kStages], (tk / kStages) & 1,
-                                             abort_flag, gstatus, LCATTN_ERR_DEVICE_TIMEOUT));
-      if (!ok) break;
-      tc_fence_after();
-      const uint64_t kb = sdesc_add(dk0, (tk % kStages) * kTileBytes);
       const uint32_t tS = tmem + (j & 1) * 128;
-      mma_ss_e<0>(tS, dq, kb, idesc_qk);
-      #pragma unroll (D <= 128 ? D / 16 - 1 : 1)
-      for (int kk = 1; kk < D / 16; ++kk) {
-        const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
-        mma_ss_e<1>(tS, sdesc_add(dq, off), sdesc_add(kb, off), idesc_qk);
+      #pragma unroll 1
+      for (int part = 0; part < kParts; ++part) {  // K entries: head-dim parts of the tile
+        const int tk = kE * j + part;
+        ok = __all_sync(0xffffffffu, mbar_wait(&sm.kv_full[tk % kStages], (tk / kStages) & 1,
+                                               abort_flag, gstatus, LCATTN_ERR_DEVICE_TIMEOUT));
+        if (!ok) break;
+        tc_fence_after();
+        const uint64_t kb = sdesc_add(dk0, (tk % kStages) * kEntryBytes);
+        const uint64_t qp = sdesc_add(dq, part * kEntryBytes);
+        if (part == 0) mma_ss_e<0>(tS, qp, kb, idesc_qk);
+        else mma_ss_e<1>(tS, qp, kb, idesc_qk);
+        #pragma unroll
+        for (int kk = 1; kk < D / kParts / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
+          mma_ss_e<1>(tS, sdesc_add(qp, off), sdesc_add(kb, off), idesc_qk);
+        }
+        tc_commit_e(&sm.kv_empty[tk % kStages]);
       }
+      if (!ok) break;
       tc_commit_e(&sm.s_full[j & 1]);
-      tc_commit_e(&sm.kv_empty[tk % kStages]);
       if (j > 0 && !issue_pv(j - 1)) { ok = false; break; }
     }
     if (ok) issue_pv(n - 1);
