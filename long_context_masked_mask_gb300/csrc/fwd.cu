@@ -217,6 +217,11 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
   constexpr int kEntryBytes = FwdGeom<D>::kEntryBytes;
   constexpr int kBoxesPerEntry = FwdGeom<D>::kBoxesPerEntry;
   constexpr int kE = 2 * kParts;  // ring entries per key tile
+  // With half-tile entries the ring holds one tile, so K runs a tile ahead of
+  // V: entries go K(0), K(1), V(0), K(2), V(1), ..., V(last) -- the order the
+  // MMA warp consumes them (S(T) before PV(T-1)) -- and K(T+1) streams in as
+  // soon as S(T) frees its stages instead of after PV(T-1).
+  constexpr bool kAhead = kParts == 2;
   extern __shared__ uint8_t smem_raw[];
   FwdSmem<D>& sm = *reinterpret_cast<FwdSmem<D>*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -309,6 +314,23 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
       ++published;
       return true;
     };
+    // One ring entry: wait for its stage, then the TMA copies of a K or V
+    // tile (or of its head-dim half `part`).
+    auto load_entry = [&](const CUtensorMap* tm, int kt, int eb, int eg, int part) -> bool {
+      const int stage = t % kStages, use = t / kStages;
+      if (use > 0) {
+        const bool okw = mbar_wait(&sm.kv_empty[stage], (use - 1) & 1, abort_flag, gstatus,
+                                   LCATTN_ERR_DEVICE_TIMEOUT);
+        if (!__all_sync(0xffffffffu, okw)) return false;
+      }
+      mbar_expect_tx_e(&sm.kv_full[stage], kEntryBytes);
+      for (int bx = 0; bx < kBoxesPerEntry; ++bx)
+        tma_load_4d_e(sm.kv[stage] + bx * kHalfBytes, tm, &sm.kv_full[stage],
+                      128 * part + 64 * bx, eg, kt * kBN, eb);
+      ++t;
+      return true;
+    };
+    int prev_kt = -1, prev_b = 0, prev_g = 0;  // K ahead of V: the tile whose V is still to come
     int cur = fetch();
     while (ok) {
       if (!publish(cur)) { ok = false; break; }
@@ -326,20 +348,19 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
       }
       if (it.n == 0) continue;
       const int g = it.h0 / pr.G;
-      for (int u = 0; u < kE * it.n; ++u, ++t) {
-        const int stage = t % kStages, use = t / kStages;
-        if (use > 0) {
-          ok = mbar_wait(&sm.kv_empty[stage], (use - 1) & 1, abort_flag, gstatus,
-                         LCATTN_ERR_DEVICE_TIMEOUT);
-          if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+      for (int u = 0; u < kE * it.n && ok; ++u) {
+        const int j = u / kE, e = u % kE;
+        const int part = e % kParts;
+        const int kt_j = __ldg(it.list + j) >> 1;
+        const bool is_v = e >= kParts;
+        int kt = kt_j, eb = it.b, eg = g;
+        bool skip = false;
+        if (kAhead && is_v) {  // V of the previous tile (none before the stream's first)
+          if (prev_kt < 0) skip = true;
+          else { kt = prev_kt; eb = prev_b; eg = prev_g; }
         }
-        const int part = u % kParts;
-        const int kt = __ldg(it.list + u / kE) >> 1;
-        const CUtensorMap* tm = ((u / kParts) & 1) ? &tmV : &tmK;
-        mbar_expect_tx_e(&sm.kv_full[stage], kEntryBytes);
-        for (int bx = 0; bx < kBoxesPerEntry; ++bx)
-          tma_load_4d_e(sm.kv[stage] + bx * kHalfBytes, tm, &sm.kv_full[stage],
-                        128 * part + 64 * bx, g, kt * kBN, it.b);
+        if (!skip && !load_entry(is_v ? &tmV : &tmK, kt, eb, eg, part)) { ok = false; break; }
+        if (kAhead && e == kE - 1) { prev_kt = kt_j; prev_b = it.b; prev_g = g; }
         if (u == 0) {
           // Two heads: buffer s holds slot s's Q for every item.  One head:
           // the two buffers alternate between items, so the next item's Q
@@ -358,11 +379,14 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
                             it.qt * kBM, it.b);
             ++q_issued[qb];
           }
-          if (!ok) { ++t; break; }
+          if (!ok) break;
           ++nq;
         }
       }
     }
+    // The last tile's V (K ran one tile ahead).
+    if (kAhead && ok && prev_kt >= 0)
+      for (int part = 0; part < kParts && ok; ++part) ok = load_entry(&tmV, prev_kt, prev_b, prev_g, part);
     // Never leave copies in flight: wait (bounded, ignoring the abort word) for
     // the last load issued on each ring stage and for the last Q tiles.
     for (int u = max(0, t - kStages); u < t; ++u) {
@@ -419,7 +443,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
         // buffer of P(t-2), which PV(t-2), issued before it, has read.
         const uint32_t tO = tmem + 256;
         uint32_t acc_prev = 0u;
-        auto issue_pv1 = [&](int tt, uint32_t acc, bool last) -> bool {
+        auto issue_pv1 = [&](int tt, uint32_t acc, bool last, bool stream_last) -> bool {
           // P(tt) is released on the barrier of its S buffer: one barrier per
           // buffer keeps the softmax (which can run a tile ahead) from
           // completing a second phase before this wait has seen the first.
@@ -428,7 +452,8 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
           const uint32_t tP = tmem + (tt & 1) * 128;
           #pragma unroll 1
           for (int part = 0; part < kParts; ++part) {
-            const int tv = kE * tt + kParts + part;  // V entry: columns [part * D/kParts, ...) of O
+            // V entry of tile tt: columns [part * D/kParts, ...) of O.
+            const int tv = !kAhead || stream_last ? kE * tt + kParts + part : kE * tt + kE + part;
             if (okw) okw = mbar_wait(&sm.kv_full[tv % kStages], (tv / kStages) & 1, abort_flag, gstatus,
                                      LCATTN_ERR_DEVICE_TIMEOUT);
             if (!__all_sync(0xffffffffu, okw)) return false;
@@ -465,7 +490,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
             const uint32_t tS = tmem + (T & 1) * 128;
             #pragma unroll 1
             for (int part = 0; part < kParts; ++part) {  // K entries: head-dim parts of the tile
-              const int tk = kE * T + part;
+              const int tk = !kAhead ? kE * T + part : (T == 0 ? part : kE * T - kParts + part);
               ok = __all_sync(0xffffffffu, mbar_wait(&sm.kv_full[tk % kStages], (tk / kStages) & 1,
                                                      abort_flag, gstatus, LCATTN_ERR_DEVICE_TIMEOUT));
               if (!ok) break;
@@ -486,12 +511,12 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
             tc_commit_e(&sm.s_full[T & 1]);
             if (j == n - 1) tc_commit_e(&sm.q_empty[qb]);  // this item's Q is read for good
             // PV(T-1) closes the previous item when tile T opens a new one.
-            if (T > 0 && !issue_pv1(T - 1, acc_prev, j == 0)) { ok = false; break; }
+            if (T > 0 && !issue_pv1(T - 1, acc_prev, j == 0, false)) { ok = false; break; }
             acc_prev = j > 0 ? 1u : 0u;
           }
           if (ok) ++nq;
         }
-        if (ok && T > 0) issue_pv1(T - 1, acc_prev, true);
+        if (ok && T > 0) issue_pv1(T - 1, acc_prev, true, true);
       } else if (D <= 128)  // two heads per item (never at D = 256)
       for (int k = 0; ok; ++k) {
         const int e = k % kItemQ;

@@ -98,6 +98,9 @@ split_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
   constexpr int kEntryBytes = SplitGeom<D>::kEntryBytes;
   constexpr int kBoxesPerEntry = SplitGeom<D>::kBoxesPerEntry;
   constexpr int kE = 2 * kParts;  // ring entries per key tile
+  // Half-tile entries: K runs a tile ahead of V (K(0), K(1), V(0), ..., V(n-1)),
+  // the order the MMA warp consumes them.
+  constexpr bool kAhead = kParts == 2;
   extern __shared__ uint8_t smem_raw[];
   SplitSmem<D>& sm = *reinterpret_cast<SplitSmem<D>*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -149,20 +152,28 @@ split_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
     __syncwarp();
     bool ok = true;
     int t = 0;
-    for (int u = 0; u < kE * n; ++u, ++t) {
+    auto load_entry = [&](const CUtensorMap* tm, int kt, int part) -> bool {
       const int stage = t % kStages, use = t / kStages;
       if (use > 0) {
-        ok = mbar_wait(&sm.kv_empty[stage], (use - 1) & 1, abort_flag, gstatus,
-                       LCATTN_ERR_DEVICE_TIMEOUT);
-        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+        const bool okw = mbar_wait(&sm.kv_empty[stage], (use - 1) & 1, abort_flag, gstatus,
+                                   LCATTN_ERR_DEVICE_TIMEOUT);
+        if (!__all_sync(0xffffffffu, okw)) return false;
       }
-      const int part = u % kParts;
-      const int kt = __ldg(list + u / kE) >> 1;
-      const CUtensorMap* tm = ((u / kParts) & 1) ? &tmV : &tmK;
       mbar_expect_tx_e(&sm.kv_full[stage], kEntryBytes);
       for (int bx = 0; bx < kBoxesPerEntry; ++bx)
         tma_load_4d_e(sm.kv[stage] + bx * kHalfBytes, tm, &sm.kv_full[stage], 128 * part + 64 * bx,
                       un.g, kt * kBN, un.b);
+      ++t;
+      return true;
+    };
+    for (int u = 0; u < kE * n; ++u) {
+      const int j = u / kE, e = u % kE;
+      const int part = e % kParts;
+      const bool is_v = e >= kParts;
+      if (!(kAhead && is_v && j == 0)) {  // K ahead of V: no V before the first K pair
+        const int kt = __ldg(list + (kAhead && is_v ? j - 1 : j)) >> 1;
+        if (!load_entry(is_v ? &tmV : &tmK, kt, part)) { ok = false; break; }
+      }
       if (u == 0) {
         // Packed query tile: Gp heads x Rq positions; row = position * Gp + head.
         mbar_expect_tx_e(&sm.q_full, kTileBytes);
@@ -170,6 +181,8 @@ split_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
           tma_load_4d_e(sm.q + bx * kHalfBytes, &tmQ, &sm.q_full, 64 * bx, h_first, qs0, un.b);
       }
     }
+    if (kAhead && ok)  // the last tile's V
+      for (int part = 0; part < kParts && ok; ++part) ok = load_entry(&tmV, __ldg(list + n - 1) >> 1, part);
     // Never leave copies in flight.
     for (int u = max(0, t - kStages); u < t; ++u) {
       int dummy = 0;
@@ -197,7 +210,7 @@ split_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
       const uint32_t tP = tmem + (tt & 1) * 128;
       #pragma unroll 1
       for (int part = 0; part < kParts; ++part) {  // V entries: columns [part * D/kParts, ...) of O
-        const int tv = kE * tt + kParts + part;
+        const int tv = !kAhead || tt == n - 1 ? kE * tt + kParts + part : kE * tt + kE + part;
         if (okw) okw = mbar_wait(&sm.kv_full[tv % kStages], (tv / kStages) & 1, abort_flag, gstatus,
                                  LCATTN_ERR_DEVICE_TIMEOUT);
         if (!__all_sync(0xffffffffu, okw)) return false;
@@ -218,7 +231,7 @@ split_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
       const uint32_t tS = tmem + (j & 1) * 128;
       #pragma unroll 1
       for (int part = 0; part < kParts; ++part) {  // K entries: head-dim parts of the tile
-        const int tk = kE * j + part;
+        const int tk = !kAhead ? kE * j + part : (j == 0 ? part : kE * j - kParts + part);
         ok = __all_sync(0xffffffffu, mbar_wait(&sm.kv_full[tk % kStages], (tk / kStages) & 1,
                                                abort_flag, gstatus, LCATTN_ERR_DEVICE_TIMEOUT));
         if (!ok) break;
