@@ -330,9 +330,35 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
       ++t;
       return true;
     };
+    // Items with an empty key list never enter the queue: the producer writes
+    // their rows itself (O = 0, LSE = -inf).  Queued, they could deadlock the
+    // CTA: an item's softmax waits for its last PV, which the MMA warp issues
+    // when it opens the next non-empty item, and the longest-first order puts
+    // empty items last, possibly more of them in a row than the queue holds.
+    auto zero_item = [&](const FwdItem& x) {
+      for (int s = 0; s < hpc; ++s) {
+        const int h = x.h0 + s;
+        for (int c = lane; c < kBM * (D / 8); c += 32) {
+          const int r = c / (D / 8), ch = c % (D / 8);
+          const int row = x.qt * kBM + r;
+          if (row >= pr.Sq) continue;
+          __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(a.o) + (int64_t)x.b * a.o_sb +
+                                (int64_t)row * a.o_ss + (int64_t)h * a.o_sh;
+          reinterpret_cast<uint4*>(orow)[ch] = make_uint4(0u, 0u, 0u, 0u);
+          if (ch == 0) a.lse[((int64_t)x.b * pr.Hq + h) * pr.Sq + row] = -INFINITY;
+        }
+      }
+    };
     int prev_kt = -1, prev_b = 0, prev_g = 0;  // K ahead of V: the tile whose V is still to come
     int cur = fetch();
+    int cur_n = cur >= 0 ? fwd_item(a, hpc, hb, cur).n : 0;  // key tiles of item `cur`
     while (ok) {
+      if (cur >= 0 && cur_n == 0) {  // an empty item: written here, never queued
+        zero_item(fwd_item(a, hpc, hb, cur));
+        cur = fetch();
+        cur_n = cur >= 0 ? fwd_item(a, hpc, hb, cur).n : 0;
+        continue;
+      }
       if (!publish(cur)) { ok = false; break; }
       if (cur < 0) break;
       const int nxt = fetch();
@@ -341,6 +367,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
       if (nxt >= 0) {
         // Warm L2 with the next item's query rows while this item runs.
         const FwdItem nx = fwd_item(a, hpc, hb, nxt);
+        cur_n = nx.n;
         if (nx.n > 0)
           for (int s = 0; s < hpc; ++s)
             for (int bx = 0; bx < kBoxes; ++bx)

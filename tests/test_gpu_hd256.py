@@ -67,3 +67,42 @@ def test_hd256_backward_is_refused():
         lc.lcattn_bwd(dev["q"], dev["k"], dev["v"], o, torch.ones_like(o), lse, mask, meta,
                       workspace=torch.empty(16, dtype=torch.uint8, device="cuda"))
     assert err.value.status == lc.LCATTN_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("kind", ["CAUSAL", "UNIFORM_BLOCK_EMPTY_ROWS"])
+def test_hd256_many_items_per_cta(kind):
+    """More work items than SMs (several per persistent CTA), of uneven length
+    and some empty, so the K/V ring's order runs across item boundaries
+    (an item's last V is produced after the next item's first K)."""
+    B, N, Hq, Hkv = 1, 4096, 16, 4
+    if kind == "CAUSAL":
+        spec = MaskSpec("CAUSAL")
+    else:
+        from synthetic import block_keep
+        nb = N // 128
+        keep = block_keep(Hq, nb, nb, 0.3, 11, force_diagonal=False)
+        keep[:, ::3, :] = False  # every third query block of every head has an empty list
+        spec = MaskSpec("UNIFORM_BLOCK", {"block": 128, "keep": keep})
+    x = qkv(B, N, Hq, Hkv, D, seed=13, with_do=False)
+    dev = {n: t.cuda() for n, t in x.items()}
+    mask = lc.DeviceMask(spec, N, Hq, B, device="cuda")
+    shape = lc.make_shape(dev["q"], dev["k"], dev["v"])
+    meta = lc.lcattn_mask_compile(shape, mask)
+    o, lse = lc.lcattn_fwd(dev["q"], dev["k"], dev["v"], mask, meta)
+    o_again, _ = lc.lcattn_fwd(dev["q"], dev["k"], dev["v"], mask, meta)
+    torch.cuda.synchronize()
+    assert lc.lcattn_read_status(meta) == 0
+    assert torch.equal(o, o_again)
+    f64 = {n: t.double().numpy() for n, t in x.items()}
+    rng = np.random.default_rng(1)
+    rows = np.array(sorted({0, 127, 128, 129, N - 1} | {int(r) for r in rng.integers(0, N, 40)}))
+    scale = 1.0 / math.sqrt(D)
+    for h in (0, 5, Hq - 1):
+        ref_o, ref_l = oracle.attention_fwd_rows(f64["q"], f64["k"], f64["v"], spec, scale, 0, h, rows)
+        g = o[0, rows, h].double().cpu().numpy()
+        assert np.abs(g - ref_o).max() <= 2e-2 and relf(g, ref_o) <= 1e-2, h
+        gl = lse[0, h, rows].double().cpu().numpy()
+        fin = np.isfinite(ref_l)
+        np.testing.assert_array_equal(np.isfinite(gl), fin)
+        if fin.any():
+            assert np.abs(gl[fin] - ref_l[fin]).max() <= 5e-3
