@@ -8,7 +8,9 @@
 // Persistent: one CTA per SM walks a sequence of work items.  An item is up to
 // two 128-row query tiles ("slots") that share one list of key tiles: two query
 // heads of the same GQA group (the mask is head independent for column
-// bounds), or a single tile otherwise.  Roles:
+// bounds), or a single tile otherwise.  With single-tile items (D <= 128) the
+// items alternate between the two slots, so one slot's epilogue overlaps the
+// other slot's first tiles.  Roles:
 //   warps 0-3  softmax for slot 0 (thread = query row = TMEM lane)
 //   warps 4-7  softmax for slot 1
 //   warp  8    TMA producer: per item its Q tiles, then K_j, V_j into a 4-deep
@@ -72,10 +74,10 @@ struct FwdSmem {
   uint64_t q_empty[2];
   uint64_t kv_full[kStages];
   uint64_t kv_empty[kStages];
-  uint64_t s_full[2];
+  uint64_t s_full[4];  // per slot (two heads), per S buffer (one head), per slot and buffer (alternating)
   uint64_t p_full[2];
-  uint64_t o_full[2];  // every PV of the slot has completed (one phase per PV)
-  uint64_t o_last[2];  // an item's last PV has completed (one phase per item)
+  uint64_t o_full[2];  // every PV into the slot's O has completed (one phase per PV)
+  uint64_t o_last[2];  // an item's last PV into the slot's O has completed (one phase per item)
   uint64_t drain;
   int items[kItemQ];           // item indices handed from the producer to the other roles
   uint64_t item_full[kItemQ];
@@ -205,7 +207,9 @@ __device__ __forceinline__ FwdItem fwd_item(const FwdArgs& a, int hpc, int hb, i
   return it;
 }
 
-template <int D>
+// HPC: query heads per item (2, or 1); a template parameter so that each
+// mode's loops are compiled for it alone.
+template <int D, int HPC>
 __global__ void __launch_bounds__(kThreads, 1)
 fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
            const __grid_constant__ CUtensorMap tmV, const __grid_constant__ FwdKernelArgs ka) {
@@ -228,9 +232,15 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
   const FwdArgs& a = ka.a;
   const ProblemDev& pr = a.pr;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int hpc = ka.heads_per_cta;
+  constexpr int hpc = HPC;
+  static_assert(HPC == 1 || (HPC == 2 && D <= 128), "two heads per item need two O regions");
   const int hb = ka.head_block;
   const int total = ka.total_items;
+  // One head per item at D <= 128: the items alternate between the two
+  // softmax warpgroups ("slots"), each with its own O in TMEM, so that one
+  // slot's epilogue (O / l, the stores) overlaps the other slot's softmax.
+  constexpr bool alt = hpc == 1 && D <= 128;
+  constexpr int nsw = (hpc == 2 || alt) ? 2 : 1;  // active softmax warpgroups
   int32_t* gstatus = a.meta.status;
 
   if (tid == 0) {
@@ -238,6 +248,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
       mbar_init(&sm.q_full[s], 1);
       mbar_init(&sm.q_empty[s], 1);
       mbar_init(&sm.s_full[s], 1);
+      mbar_init(&sm.s_full[2 + s], 1);
       mbar_init(&sm.p_full[s], 128);
       mbar_init(&sm.o_full[s], 1);
       mbar_init(&sm.o_last[s], 1);
@@ -251,7 +262,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
       for (int u = 0; u < 2; ++u) mbar_init(&sm.bnd_ready[s][u], 128);
     for (int e = 0; e < kItemQ; ++e) {
       mbar_init(&sm.item_full[e], 1);
-      mbar_init(&sm.item_empty[e], 1 + 4 * hpc);  // the MMA warp and every active softmax warp
+      mbar_init(&sm.item_empty[e], 1 + 4 * nsw);  // the MMA warp and every active softmax warp
     }
     sm.abort_flag = 0;
     fence_barrier_init();
@@ -467,10 +478,12 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
         // One head per item: S is double-buffered in the two S regions, and
         // S(t) is issued before PV(t-1), so the softmax of tile t-1 overlaps
         // S(t) and finds S(t) done when it finishes.  S(t) overwrites the
-        // buffer of P(t-2), which PV(t-2), issued before it, has read.
-        const uint32_t tO = tmem + 256;
+        // buffer of P(t-2), which PV(t-2), issued before it, has read.  With
+        // alternating slots, the item's slot (its Q buffer) picks the O region
+        // and the S barriers.
         uint32_t acc_prev = 0u;
-        auto issue_pv1 = [&](int tt, uint32_t acc, bool last, bool stream_last) -> bool {
+        int prev_slot = 0;  // slot of the item of tile T-1
+        auto issue_pv1 = [&](int tt, uint32_t acc, bool last, bool stream_last, int ps) -> bool {
           // P(tt) is released on the barrier of its S buffer: one barrier per
           // buffer keeps the softmax (which can run a tile ahead) from
           // completing a second phase before this wait has seen the first.
@@ -486,14 +499,14 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
             if (!__all_sync(0xffffffffu, okw)) return false;
             tc_fence_after();
             const uint64_t vb = sdesc_add(dv0, (tv % kStages) * kEntryBytes);
-            const uint32_t tOp = tO + part * (D / kParts);
+            const uint32_t tOp = tmem + 256 + ps * 128 + part * (D / kParts);
             mma_ts_er(tOp, tP, vb, idesc_pv, acc);
             #pragma unroll
             for (int kk = 1; kk < 8; ++kk) mma_ts_e<1>(tOp, tP + kk * 8, sdesc_add(vb, kk * 2048), idesc_pv);
             tc_commit_e(&sm.kv_empty[tv % kStages]);
           }
-          tc_commit_e(&sm.o_full[0]);
-          if (last) tc_commit_e(&sm.o_last[0]);  // the item's O is complete
+          tc_commit_e(&sm.o_full[ps]);
+          if (last) tc_commit_e(&sm.o_last[ps]);  // the item's O is complete
           return true;
         };
         for (int k = 0; ok; ++k) {
@@ -513,6 +526,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
                                                  LCATTN_ERR_DEVICE_TIMEOUT));
           if (!ok) break;
           const uint64_t qd = qb ? dq1 : dq0;
+          const int slot = alt ? qb : 0;
           for (int j = 0; j < n; ++j, ++T) {
             const uint32_t tS = tmem + (T & 1) * 128;
             #pragma unroll 1
@@ -535,15 +549,16 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
               tc_commit_e(&sm.kv_empty[tk % kStages]);
             }
             if (!ok) break;
-            tc_commit_e(&sm.s_full[T & 1]);
+            tc_commit_e(&sm.s_full[2 * slot + (T & 1)]);
             if (j == n - 1) tc_commit_e(&sm.q_empty[qb]);  // this item's Q is read for good
             // PV(T-1) closes the previous item when tile T opens a new one.
-            if (T > 0 && !issue_pv1(T - 1, acc_prev, j == 0, false)) { ok = false; break; }
+            if (T > 0 && !issue_pv1(T - 1, acc_prev, j == 0, false, prev_slot)) { ok = false; break; }
             acc_prev = j > 0 ? 1u : 0u;
+            prev_slot = slot;
           }
           if (ok) ++nq;
         }
-        if (ok && T > 0) issue_pv1(T - 1, acc_prev, true, true);
+        if (ok && T > 0) issue_pv1(T - 1, acc_prev, true, true, prev_slot);
       } else if (D <= 128)  // two heads per item (never at D = 256)
       for (int k = 0; ok; ++k) {
         const int e = k % kItemQ;
@@ -566,6 +581,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
           if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
           tc_fence_after();
           const uint64_t kb = sdesc_add(dk0, (tk % kStages) * kTileBytes);
+          #pragma unroll 1  // the MMA warp has 72 registers
           for (int s = 0; s < hpc; ++s) {
             if (T > 0 && !issue_pv(s, j == 0)) { ok = false; break; }
             if (j == 0) {
@@ -616,7 +632,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
     // ---------------------------------------------------------------- softmax
     const int s = warp >> 2;
     const int r = tid & 127;  // == 32 * (warp % 4) + lane: this thread's TMEM lane
-    if (s < hpc) {
+    if (s < nsw) {
       const uint32_t lane_off = static_cast<uint32_t>(32 * (warp & 3)) << 16;
       const uint32_t tO = tmem + lane_off + 256 + s * 128;
       const float sl2 = a.scale_log2;
@@ -626,7 +642,11 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
       bool ok = true;
       int T = 0;          // tiles of this CTA processed before the current item
       int n_partial = 0;  // partial column-bounds tiles staged so far (selects the buffer)
-      int n_items = 0;    // items with at least one key tile finished so far
+      // Counter parities (the barrier waits need no more).  Alternating slots:
+      // bit b < 2 = this slot's key tiles so far in S buffer b, bit 2 = items
+      // with at least one key tile seen by either slot.  Bit 3 = this slot's
+      // items with at least one key tile finished so far.
+      uint32_t pbits = 0u;
       for (int k = 0; ok; ++k) {
         const int e = k % kItemQ;
         ok = mbar_wait(&sm.item_full[e], (k / kItemQ) & 1, abort_flag, gstatus,
@@ -638,7 +658,12 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
         if (idx < 0) break;
         const FwdItem it = fwd_item(a, hpc, hb, idx);
         const int n = it.n, b = it.b;
-        const int h = it.h0 + s;
+        if (alt && n > 0) {
+          const bool mine = static_cast<int>((pbits >> 2) & 1u) == s;
+          pbits ^= 4u;
+          if (!mine) { T += n; continue; }  // the other slot's item
+        }
+        const int h = it.h0 + (hpc == 2 ? s : 0);
         const int row = it.qt * kBM + r;
         int qb_row = 0;
         if (a.mask.kind == LCATTN_MASK_BLOCKMAP)
@@ -686,8 +711,16 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
           // regions alternate between tiles.
           const int sb = hpc == 1 ? ((T + j) & 1) : s;
           const uint32_t tS = tmem + lane_off + sb * 128;
-          ok = mbar_wait(&sm.s_full[sb], (hpc == 1 ? ((T + j) >> 1) : (T + j)) & 1, abort_flag, gstatus,
-                         LCATTN_ERR_DEVICE_TIMEOUT);
+          // S barriers: per slot (two heads, a phase per tile), per buffer
+          // (one head), per slot and buffer (alternating: a phase per tile of
+          // this slot in that buffer, so a slot never waits on a phase that
+          // the other slot's tiles could have run past).
+          const int sfi = hpc == 2 ? s : (alt ? 2 * s + sb : sb);
+          int sph;
+          if (hpc == 2) sph = T + j;
+          else if (alt) { sph = static_cast<int>(pbits >> sb); pbits ^= 1u << sb; }
+          else sph = (T + j) >> 1;
+          ok = mbar_wait(&sm.s_full[sfi], sph & 1, abort_flag, gstatus, LCATTN_ERR_DEVICE_TIMEOUT);
           if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
           tc_fence_after();
           uint32_t xr[128];
@@ -743,8 +776,10 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
           if (warp_rescale) {
             // O holds PV up to tile j-1: wait for it, then scale it in place
             // before PV(j) is issued (which needs p_full below).
-            ok = mbar_wait(&sm.o_full[s], (T + j - 1) & 1, abort_flag, gstatus,
-                           LCATTN_ERR_DEVICE_TIMEOUT);
+            // PV(j-1) of this item: phase (slot's tiles so far) - 2, whose
+            // parity is that of the slot's tile count (bits 0 and 1).
+            const int oph = alt ? static_cast<int>(pbits ^ (pbits >> 1)) : (T + j - 1);
+            ok = mbar_wait(&sm.o_full[s], oph & 1, abort_flag, gstatus, LCATTN_ERR_DEVICE_TIMEOUT);
             if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
             tc_fence_after();
             #pragma unroll (D <= 128 ? D / 32 : 1)
@@ -769,7 +804,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
         // wait on the per-PV barrier could then match an older phase.
         bool have_o = ok && n > 0;
         if (have_o) {
-          have_o = mbar_wait(&sm.o_last[s], n_items & 1, abort_flag, gstatus,
+          have_o = mbar_wait(&sm.o_last[s], (pbits >> 3) & 1, abort_flag, gstatus,
                              LCATTN_ERR_DEVICE_TIMEOUT);
           have_o = __all_sync(0xffffffffu, have_o);
           tc_fence_after();
@@ -817,7 +852,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
                 live ? (m_run + __log2f(l_run)) * 0.69314718055994531f : -INFINITY;
         }
         if (n > 0 && !have_o) ok = false;
-        if (n > 0) ++n_items;
+        if (n > 0) pbits ^= 8u;
         T += n;
       }
     }
@@ -832,17 +867,24 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
   }
 }
 
-template <int D>
-cudaError_t launch_fwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                         const FwdArgs& a, cudaStream_t st) {
+template <int D, int HPC>
+cudaError_t launch_fwd_mode(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                            const FwdKernelArgs& ka, int grid, cudaStream_t st) {
   static bool attr_done = false;
   const size_t smem = sizeof(FwdSmem<D>) + 1024;
   if (!attr_done) {
-    cudaError_t e =
-        cudaFuncSetAttribute(fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = cudaFuncSetAttribute(fwd_kernel<D, HPC>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     attr_done = true;
   }
+  fwd_kernel<D, HPC><<<(unsigned)grid, kThreads, smem, st>>>(tq, tk, tv, ka);
+  return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_fwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                         const FwdArgs& a, cudaStream_t st) {
   int dev = 0, nsm = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
@@ -862,8 +904,9 @@ cudaError_t launch_fwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
   ka.total_items = static_cast<int>(total);
   // Persistent: one CTA per SM (shared memory admits one), never more CTAs than items.
   const int grid = ka.total_items < nsm ? ka.total_items : nsm;
-  fwd_kernel<D><<<(unsigned)grid, kThreads, smem, st>>>(tq, tk, tv, ka);
-  return cudaGetLastError();
+  if constexpr (D <= 128)
+    if (ka.heads_per_cta == 2) return launch_fwd_mode<D, 2>(tq, tk, tv, ka, grid, st);
+  return launch_fwd_mode<D, 1>(tq, tk, tv, ka, grid, st);
 }
 
 }  // namespace
