@@ -215,10 +215,11 @@ int lcattn_fwd(const lcattn_shape* shape, const void* q, const void* k, const vo
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(tile_meta))
     return LCATTN_ERR_UNSUPPORTED;
   if (!(scale > 0.f) || !(scale < 1e30f)) return LCATTN_ERR_INVALID_ARG;
-  CUtensorMap tq, tk, tv;
+  CUtensorMap tq, tk, tv, to;
   if ((st = encode_bshd(&tq, q, shape->B, shape->Sq, shape->Hq, shape->D, shape->q_stride))) return st;
   if ((st = encode_bshd(&tk, k, shape->B, shape->Sk, shape->Hkv, shape->D, shape->k_stride))) return st;
   if ((st = encode_bshd(&tv, v, shape->B, shape->Sk, shape->Hkv, shape->D, shape->v_stride))) return st;
+  if ((st = encode_bshd(&to, o, shape->B, shape->Sq, shape->Hq, shape->D, shape->o_stride))) return st;
   FwdArgs a;
   a.pr = problem_of(shape);
   a.mask = mask_of(mask);
@@ -227,7 +228,7 @@ int lcattn_fwd(const lcattn_shape* shape, const void* q, const void* k, const vo
   a.o = o;
   a.o_sb = shape->o_stride[0]; a.o_ss = shape->o_stride[1]; a.o_sh = shape->o_stride[2];
   a.lse = lse;
-  return cuda_status(launch_fwd(tq, tk, tv, a, reinterpret_cast<cudaStream_t>(stream)));
+  return cuda_status(launch_fwd(tq, tk, tv, to, a, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 }  // extern "C"

@@ -68,7 +68,10 @@ struct FwdSmem {
   static constexpr int kTileBytes = FwdGeom<D>::kTileBytes;
   alignas(1024) uint8_t q[FwdGeom<D>::kQBufs][kTileBytes];
   alignas(1024) uint8_t kv[kStages][FwdGeom<D>::kEntryBytes];
-  int4 bnd[2][2][kBN];  // column bounds of a partial tile, per slot, double-buffered
+  // Per slot: O staging for the epilogue's TMA stores (one 64-column box of
+  // 128 rows, 128-byte swizzled).  Between epilogues its first 4 KB hold the
+  // column bounds of partial tiles (two buffers of 128 int4).
+  alignas(1024) uint8_t stg[2][kHalfBytes];
   uint64_t bnd_ready[2][2];
   uint64_t q_full[2];
   uint64_t q_empty[2];
@@ -79,6 +82,8 @@ struct FwdSmem {
   uint64_t o_full[2];  // every PV into the slot's O has completed (one phase per PV)
   uint64_t o_last[2];  // an item's last PV into the slot's O has completed (one phase per item)
   uint64_t drain;
+  uint64_t stg_full[2];  // a slot's staging box is written (128 arrivals; one phase per epilogue)
+  uint64_t stg_free[2];  // ... and read by its TMA stores (one phase per epilogue)
   int items[kItemQ];           // item indices handed from the producer to the other roles
   uint64_t item_full[kItemQ];
   uint64_t item_empty[kItemQ];
@@ -212,7 +217,8 @@ __device__ __forceinline__ FwdItem fwd_item(const FwdArgs& a, int hpc, int hb, i
 template <int D, int HPC>
 __global__ void __launch_bounds__(kThreads, 1)
 fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-           const __grid_constant__ CUtensorMap tmV, const __grid_constant__ FwdKernelArgs ka) {
+           const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+           const __grid_constant__ FwdKernelArgs ka) {
   constexpr int kStages = FwdGeom<D>::kStages;
   constexpr int kTileBytes = FwdGeom<D>::kTileBytes;
   constexpr int kBoxes = FwdGeom<D>::kBoxes;
@@ -258,6 +264,10 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
       mbar_init(&sm.kv_empty[i], 1);
     }
     mbar_init(&sm.drain, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&sm.stg_full[s], 128);
+      mbar_init(&sm.stg_free[s], 1);
+    }
     for (int s = 0; s < 2; ++s)
       for (int u = 0; u < 2; ++u) mbar_init(&sm.bnd_ready[s][u], 128);
     for (int e = 0; e < kItemQ; ++e) {
@@ -645,8 +655,25 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
       // Counter parities (the barrier waits need no more).  Alternating slots:
       // bit b < 2 = this slot's key tiles so far in S buffer b, bit 2 = items
       // with at least one key tile seen by either slot.  Bit 3 = this slot's
-      // items with at least one key tile finished so far.
+      // items with at least one key tile finished so far.  Bit 4 = epilogues
+      // so far; bit 5 = the staging buffers may still be read by TMA stores.
       uint32_t pbits = 0u;
+      // The staging buffers (and the column bounds that share them) are free
+      // again once the last epilogue's TMA stores have read them: its issuing
+      // lane waits for that and releases the buffers; every thread of the slot
+      // waits for the release before writing there again.
+      auto stg_reclaim = [&]() -> bool {
+        if (!(pbits & 32u)) return true;
+        if (warp == 4 * s && lane == 0) {
+          bulk_wait_read0();
+          mbar_arrive(&sm.stg_free[s]);
+        }
+        __syncwarp();
+        const bool okw = mbar_wait(&sm.stg_free[s], ((pbits >> 4) & 1u) ^ 1u, abort_flag, gstatus,
+                                   LCATTN_ERR_DEVICE_TIMEOUT);
+        pbits &= ~32u;
+        return __all_sync(0xffffffffu, okw);
+      };
       for (int k = 0; ok; ++k) {
         const int e = k % kItemQ;
         ok = mbar_wait(&sm.item_full[e], (k / kItemQ) & 1, abort_flag, gstatus,
@@ -662,6 +689,9 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
           const bool mine = static_cast<int>((pbits >> 2) & 1u) == s;
           pbits ^= 4u;
           if (!mine) { T += n; continue; }  // the other slot's item
+          // Alternating slots: this slot's previous epilogue was an item ago,
+          // so its stores have long read the staging buffer.
+          if (!stg_reclaim()) { ok = false; break; }
         }
         const int h = it.h0 + (hpc == 2 ? s : 0);
         const int row = it.qt * kBM + r;
@@ -694,15 +724,17 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
             if (partial && a.mask.kind == LCATTN_MASK_COLBOUNDS) {
               // Stage the tile's 128 column bounds in shared memory: one coalesced
               // load per thread instead of 128 dependent loads per thread.
+              if (!alt && !stg_reclaim()) { ok = false; break; }
               const int u = n_partial & 1;
               const int key = kt * kBN + r;
-              sm.bnd[s][u][r] = key < pr.Sk ? __ldg(a.mask.col_bounds + (int64_t)b * pr.Sk + key)
+              int4* bs = reinterpret_cast<int4*>(sm.stg[s]) + u * kBN;
+              bs[r] = key < pr.Sk ? __ldg(a.mask.col_bounds + (int64_t)b * pr.Sk + key)
                                             : make_int4(0, 0, 0, 0);
               mbar_arrive(&sm.bnd_ready[s][u]);
               ok = mbar_wait(&sm.bnd_ready[s][u], (n_partial >> 1) & 1, abort_flag, gstatus,
                              LCATTN_ERR_DEVICE_TIMEOUT);
               if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-              bnd = sm.bnd[s][u];
+              bnd = bs;
               ++n_partial;
             }
             tile_mask_bits(a.mask, pr, b, h, row, qb_row, kt, partial, bnd, mw);
@@ -809,12 +841,16 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
           have_o = __all_sync(0xffffffffu, have_o);
           tc_fence_after();
         }
+        if (!alt && ok && (have_o || n == 0) && !stg_reclaim()) ok = false;
         if (ok && (have_o || n == 0)) {
           const bool live = l_run > 0.f;
           const float inv = live ? 1.f / l_run : 0.f;
           __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(a.o) + (int64_t)b * a.o_sb +
                                 (int64_t)row * a.o_ss + (int64_t)h * a.o_sh;
-          // All 128 columns of O in one round trip, then O / l on column pairs.
+          // The first kTmaCols columns go out through shared memory and TMA
+          // stores (one 64-column box per slot; two with one slot), the rest
+          // as 32-byte stores from the registers, one row per thread.
+          constexpr int kTmaCols = nsw == 2 ? 64 : (D < 128 ? D : 128);
           // All of O in one round trip when it fits the registers (D <= 128),
           // else 32 columns at a time; then O / l on column pairs.
           constexpr int kBatch = D <= 128 ? D : 32;
@@ -839,14 +875,48 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
                                                 __uint_as_float(o32[c * 32 + 2 * i + 1])), inv2);
               pk[i] = pack_bf16x2(y.x, y.y);
             }
-            if (row < pr.Sq) {
-              uint4* dst = reinterpret_cast<uint4*>(orow + c0 + c * 32);
+            const int cc = c0 + c * 32;
+            if (cc < kTmaCols) {
+              // Row r of a 128-byte-swizzled box: 16-byte chunk j sits at j ^ (r % 8).
+              uint8_t* srow = sm.stg[nsw == 2 ? s : (cc >> 6)] + r * 128;
+              const int j0 = (cc & 63) >> 3;
               #pragma unroll
               for (int i = 0; i < 4; ++i)
-                dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+                *reinterpret_cast<uint4*>(srow + (((j0 + i) ^ (r & 7)) << 4)) =
+                    make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+              if (cc + 32 == kTmaCols) {
+                fence_proxy_async_smem();
+                mbar_arrive(&sm.stg_full[s]);
+                if (warp == 4 * s) {
+                  const bool okf = __all_sync(0xffffffffu,
+                                              mbar_wait(&sm.stg_full[s], (pbits >> 4) & 1u, abort_flag,
+                                                        gstatus, LCATTN_ERR_DEVICE_TIMEOUT));
+                  if (okf && lane == 0) {
+                    #pragma unroll
+                    for (int bx = 0; bx < kTmaCols / 64; ++bx)
+                      tma_store_4d(&tmO, sm.stg[nsw == 2 ? s : bx], 64 * bx, h, it.qt * kBM, b);
+                    bulk_commit();
+                  }
+                  __syncwarp();
+                  if (!okf) ok = false;
+                }
+                pbits |= 32u;
+              }
+            } else if (row < pr.Sq) {
+              __nv_bfloat16* dst = orow + cc;
+              if ((reinterpret_cast<uintptr_t>(dst) & 31u) == 0) {
+                st_global_v8(dst, pk);
+                st_global_v8(dst + 16, pk + 8);
+              } else {
+                #pragma unroll
+                for (int i = 0; i < 4; ++i)
+                  reinterpret_cast<uint4*>(dst)[i] =
+                      make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+              }
             }
           }
           }
+          pbits ^= 16u;
           if (row < pr.Sq)
             a.lse[((int64_t)b * pr.Hq + h) * pr.Sq + row] =
                 live ? (m_run + __log2f(l_run)) * 0.69314718055994531f : -INFINITY;
@@ -855,6 +925,8 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
         if (n > 0) pbits ^= 8u;
         T += n;
       }
+      // The shared memory goes away with the CTA: let the last TMA stores finish.
+      if (warp == 4 * s && lane == 0) bulk_wait0();
     }
   }
 
@@ -869,7 +941,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
 
 template <int D, int HPC>
 cudaError_t launch_fwd_mode(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                            const FwdKernelArgs& ka, int grid, cudaStream_t st) {
+                            const CUtensorMap& to, const FwdKernelArgs& ka, int grid, cudaStream_t st) {
   static bool attr_done = false;
   const size_t smem = sizeof(FwdSmem<D>) + 1024;
   if (!attr_done) {
@@ -878,13 +950,13 @@ cudaError_t launch_fwd_mode(const CUtensorMap& tq, const CUtensorMap& tk, const 
     if (e != cudaSuccess) return e;
     attr_done = true;
   }
-  fwd_kernel<D, HPC><<<(unsigned)grid, kThreads, smem, st>>>(tq, tk, tv, ka);
+  fwd_kernel<D, HPC><<<(unsigned)grid, kThreads, smem, st>>>(tq, tk, tv, to, ka);
   return cudaGetLastError();
 }
 
 template <int D>
 cudaError_t launch_fwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                         const FwdArgs& a, cudaStream_t st) {
+                         const CUtensorMap& to, const FwdArgs& a, cudaStream_t st) {
   int dev = 0, nsm = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
@@ -905,17 +977,17 @@ cudaError_t launch_fwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
   // Persistent: one CTA per SM (shared memory admits one), never more CTAs than items.
   const int grid = ka.total_items < nsm ? ka.total_items : nsm;
   if constexpr (D <= 128)
-    if (ka.heads_per_cta == 2) return launch_fwd_mode<D, 2>(tq, tk, tv, ka, grid, st);
-  return launch_fwd_mode<D, 1>(tq, tk, tv, ka, grid, st);
+    if (ka.heads_per_cta == 2) return launch_fwd_mode<D, 2>(tq, tk, tv, to, ka, grid, st);
+  return launch_fwd_mode<D, 1>(tq, tk, tv, to, ka, grid, st);
 }
 
 }  // namespace
 
 cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                       const FwdArgs& a, cudaStream_t st) {
-  if (a.pr.D == 64) return launch_fwd_d<64>(tq, tk, tv, a, st);
-  if (a.pr.D == 256) return launch_fwd_d<256>(tq, tk, tv, a, st);
-  return launch_fwd_d<128>(tq, tk, tv, a, st);
+                       const CUtensorMap& to, const FwdArgs& a, cudaStream_t st) {
+  if (a.pr.D == 64) return launch_fwd_d<64>(tq, tk, tv, to, a, st);
+  if (a.pr.D == 256) return launch_fwd_d<256>(tq, tk, tv, to, a, st);
+  return launch_fwd_d<128>(tq, tk, tv, to, a, st);
 }
 
 }  // namespace lcattn

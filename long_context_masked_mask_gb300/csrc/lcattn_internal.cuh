@@ -57,8 +57,9 @@ struct FwdArgs {
   int64_t o_sb, o_ss, o_sh;
   float* lse;
 };
+// `to`: O as a TMA map with the same box as Q (the epilogue's stores).
 cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                       const FwdArgs& a, cudaStream_t st);
+                       const CUtensorMap& to, const FwdArgs& a, cudaStream_t st);
 
 // Split-KV forward for short query sides (fwd_split.cu).
 struct SplitArgs {

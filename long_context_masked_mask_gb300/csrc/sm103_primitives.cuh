@@ -259,6 +259,35 @@ __device__ __forceinline__ void tma_prefetch_l2_4d_e(const CUtensorMap* m, int32
       : "memory");
 }
 
+// TMA store of one tensor-map box from shared memory (the calling thread
+// issues it; rows past the tensor's extent are not written).  The shared
+// memory must not be rewritten before bulk_wait_read0() in the same thread.
+__device__ __forceinline__ void tma_store_4d(const CUtensorMap* m, const void* src, int32_t c0,
+                                             int32_t c1, int32_t c2, int32_t c3) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4, %5}], [%1];"
+      :: "l"(reinterpret_cast<uint64_t>(m)), "r"(smem_u32(src)), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// This thread's bulk stores have read their shared-memory sources.
+__device__ __forceinline__ void bulk_wait_read0() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// This thread's bulk stores have completed.
+__device__ __forceinline__ void bulk_wait0() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+// 32-byte global store (the address must be 32-byte aligned).
+__device__ __forceinline__ void st_global_v8(void* p, const uint32_t* w) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};"
+               :: "l"(p), "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]),
+                  "r"(w[6]), "r"(w[7])
+               : "memory");
+}
+
 // 32 lanes x 32 columns of 32 bit: thread t of the warp receives lane (base + t),
 // columns col .. col+31.
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t* r) {
