@@ -247,13 +247,17 @@ class ClockSampler:
 
 def traffic_lookup(kernel, workload):
     """DRAM bytes per launch recorded from an ncu capture of this kernel on this
-    workload, if the kernel's source has not changed since (profiles/traffic.json)."""
+    workload, if the kernel's source has not changed since (profiles/traffic.json:
+    per kernel, one record or a list of records, one per workload)."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
     with open(path) as f:
-        rec = json.load(f).get(kernel)
-    if not rec or rec.get("workload") != workload:
+        recs = json.load(f).get(kernel)
+    if isinstance(recs, dict):
+        recs = [recs]
+    rec = next((r for r in recs or [] if r.get("workload") == workload), None)
+    if rec is None:
         return None
     src = os.path.join(ROOT, "long_context_masked_mask_gb300", "csrc", rec["source"])
     sha = hashlib.sha256(open(src, "rb").read()).hexdigest()

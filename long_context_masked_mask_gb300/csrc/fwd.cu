@@ -925,8 +925,9 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
         if (n > 0) pbits ^= 8u;
         T += n;
       }
-      // The shared memory goes away with the CTA: let the last TMA stores finish.
-      if (warp == 4 * s && lane == 0) bulk_wait0();
+      // The shared memory goes away with the CTA: the last TMA stores must
+      // have read it (their global writes complete with the grid).
+      if (warp == 4 * s && lane == 0) bulk_wait_read0();
     }
   }
 

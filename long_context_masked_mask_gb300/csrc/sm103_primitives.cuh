@@ -276,10 +276,6 @@ __device__ __forceinline__ void bulk_commit() {
 __device__ __forceinline__ void bulk_wait_read0() {
   asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
-// This thread's bulk stores have completed.
-__device__ __forceinline__ void bulk_wait0() {
-  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
-}
 // 32-byte global store (the address must be 32-byte aligned).
 __device__ __forceinline__ void st_global_v8(void* p, const uint32_t* w) {
   asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};"
