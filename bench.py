@@ -245,6 +245,23 @@ class ClockSampler:
 # GPU arm
 # ----------------------------------------------------------------------------
 
+def max_over_ranks(x, dist, device=None):
+    """The largest of the ranks' values of `x` (each rank passes its own), or `x`
+    itself without a process group: the whole job is as slow as its slowest rank."""
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(world, flops_per_rank_step, ms):
+    """TFLOP/s of the whole job: every rank does `flops_per_rank_step` per step
+    (independent replicas, weak scaling) and a step takes `ms` (max over ranks)."""
+    return world * flops_per_rank_step / (ms / 1e3) / 1e12
+
+
 def traffic_lookup(kernel, workload):
     """DRAM bytes per launch recorded from an ncu capture of this kernel on this
     workload, if the kernel's source has not changed since (profiles/traffic.json:
@@ -375,12 +392,8 @@ def run_gpu(args, rank, world, dist):
     barrier()
     clocks = sampler.stop()
     ms_steps = [e0.elapsed_time(e1) for e0, e1 in evs]
-    ms = statistics.mean(ms_steps)
-    if dist is not None:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-    value = world * step_flops / (ms / 1e3) / 1e12
+    ms = max_over_ranks(statistics.mean(ms_steps), dist, dev)
+    value = whole_job_rate(world, step_flops, ms)
 
     # ---- per-kernel breakdown (CUDA events on the launching stream) ---------
     pk = peaks()
@@ -549,12 +562,8 @@ def run_gpu(args, rank, world, dist):
         torch.cuda.synchronize()
         if i >= args.warmup:
             e2e_ms.append(e0.elapsed_time(e1))
-    e2e_t = statistics.mean(e2e_ms)
-    if dist is not None:
-        t = torch.tensor([e2e_t], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_t = float(t.item())
-    e2e = {"value": world * step_flops / (e2e_t / 1e3) / 1e12, "unit": UNIT, "ms_per_step": e2e_t,
+    e2e_t = max_over_ranks(statistics.mean(e2e_ms), dist, dev)
+    e2e = {"value": whole_job_rate(world, step_flops, e2e_t), "unit": UNIT, "ms_per_step": e2e_t,
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
            "copies": "pinned host buffers; dO and each mask's results move on a copy stream that "
                      "overlaps compute; all copies inside the timed region"}
