@@ -233,7 +233,10 @@ int lcattn_block_select_stage(int stage, const lcattn_shape* shape, const void* 
  * to run out of work puts the counter back to zero.  So forward calls that
  * share one `tile_meta` must not overlap in time (issue them on one stream);
  * after a DEVICE_TIMEOUT status, lcattn_clear_status also resets the counter.
- * The forward only reads the rest of `tile_meta`.                           */
+ * The forward only reads the rest of `tile_meta`.  Part of every O tile is
+ * written by TMA tensor stores through O's strides (the rest by plain
+ * stores), so `o` must not overlap q, k or v; rows of padding between
+ * sequences (a batch stride above Sq x the sequence stride) are never written. */
 int lcattn_fwd(const lcattn_shape* shape, const void* q, const void* k, const void* v,
                const void* tile_meta, const lcattn_mask_desc* mask, float scale, void* o,
                float* lse, lcattn_stream_t stream);
