@@ -208,3 +208,38 @@ def test_head_dim_256_is_forward_only():
         assert lib.lcattn_bwd_stage(stage, *args, P, 1 << 30, None) == lc.LCATTN_ERR_UNSUPPORTED
     s.D = 512
     assert _layout(s, d)[0] == lc.LCATTN_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("B,Sq,Sk,Hq,Hkv,kind", [
+    (1, 1, 1, 1, 1, "cb"), (1, 127, 4097, 4, 2, "cb"), (3, 129, 128, 6, 3, "cb"),
+    (2, 1000, 300, 8, 1, "bm"), (1, 4097, 129, 4, 4, "bm"), (2, 128, 128, 2, 2, "bm"),
+])
+def test_layout_regions_hold_their_contents(B, Sq, Sk, Hq, Hkv, kind):
+    """Every tile-metadata region is 256-byte aligned, follows the previous one,
+    and has room for what it holds: a class byte per (batch, list head, query
+    tile, key tile), per-list counts and orders, and full-length lists in both
+    directions (a list head is one query head for block maps, else all heads)."""
+    s = _shape(B=B, S=Sq, Hq=Hq, Hkv=Hkv)
+    s.Sk = Sk
+    for name, H in (("k_stride", Hkv), ("v_stride", Hkv)):
+        getattr(s, name)[:] = (Sk * H * 128, H * 128, 128)
+    if kind == "cb":
+        d = _colbounds_desc()
+    else:
+        d = lc.lcattn_mask_desc()
+        d.kind, d.block_map, d.q_block_offs, d.k_block_offs = lc.LCATTN_MASK_BLOCKMAP, 0x1000, 0x2000, 0x3000
+        d.nQb, d.nKb = 1, 1
+    st, L = _layout(s, d)
+    assert st == 0
+    nQt, nKt = -(-Sq // 128), -(-Sk // 128)
+    nH = Hq if kind == "bm" else 1
+    assert (L.nQt, L.nKt, L.nH, L.B) == (nQt, nKt, nH, B)
+    lists = B * nH
+    regions = [(L.off_status, 32), (L.off_class, lists * nQt * nKt), (L.off_fwd_cnt, 4 * lists * nQt),
+               (L.off_fwd_lst, 4 * lists * nQt * nKt), (L.off_fwd_ord, 4 * lists * nQt),
+               (L.off_bwd_cnt, 4 * lists * nKt), (L.off_bwd_lst, 4 * lists * nKt * nQt),
+               (L.off_bwd_ord, 4 * lists * nKt)]
+    for (o, n), (o_next, _) in zip(regions, regions[1:] + [(L.total_bytes, 0)]):
+        assert o % 256 == 0 and o + n <= o_next
+    size = lc.library().lcattn_tile_meta_size(ctypes.byref(s), ctypes.byref(d))
+    assert size == L.total_bytes
