@@ -226,6 +226,9 @@ def _rect_inputs(B, Sq, Sk, Hq, Hkv, D, seed):
             rng.standard_normal((B, Sk, Hkv, D)), rng.standard_normal((B, Sq, Hq, D)))
 
 
+# torch warns that its lower-right bias gives NaN rows when Sq > Sk; the test
+# compares only the rows that allow a key.
+@pytest.mark.filterwarnings("ignore:Lower right causal bias")
 @pytest.mark.parametrize("Sq,Sk", [(5, 13), (1, 9), (9, 4), (7, 7)])
 def test_causal_rectangular_matches_torch_lower_right(Sq, Sk):
     """CAUSAL with Sq != Sk against torch's own lower-right causal bias
