@@ -3,11 +3,19 @@
 
 One step is the whole hot path over one synthetic batch, for every mask of the
 workload: mask compile -> forward -> backward (D pre-pass, dK/dV, dQ).  The
-default workload is dense attention at 8K: B=1, N=8192, GQA 64:8, head dim
-128, bf16, FULL and CAUSAL masks.
+default workload, the one the JSON line's ``value`` is measured on, is the
+long-context configuration: B=1, N=131072, GQA 64:8, head dim 128, bf16, the
+CAUSAL mask and a uniform 128x128 block-sparse mask (each block kept with
+probability 0.5 per query head, diagonal kept).  The same run then times the
+dense 8K (FULL, CAUSAL), packed-document 32K (FULL/CAUSAL DOCUMENT) and
+heterogeneous 16K MHA workloads and reports them under ``per_workload``.
 
 Effective FLOPs count only allowed (query, key) pairs: forward 4*D per pair
 and query head, backward 2.5x the forward (five GEMMs against two).
+
+Fractions of peak: a kernel timed alone (the per-mask and roofline figures)
+is divided by the measured burst bf16 GEMM rate; the whole step, timed over
+many back-to-back steps, is also given against the sustained rate.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
     python bench.py --impl reference ...   # the fp64 CPU oracle, same metric
@@ -34,21 +42,29 @@ sys.path.insert(0, ROOT)
 METRIC = "effective attention TFLOP/s fwd/bwd (unmasked FLOPs) and % of GB300 bf16 peak"
 UNIT = "TFLOP/s"
 L2_FLUSH_BYTES = 512 << 20  # > 129 MB of L2, written before every timed step
+DEFAULT_WORKLOAD = "long_128k"
+DEFAULT_PER_WORKLOAD = "dense_8k,docs_32k,hetero_16k"
+# Pairs of one head the oracle sample covers per mask (about a second of
+# fp64 work on 16 cores per mask for the forward and backward together).
+ORACLE_SAMPLE_PAIRS = 1 << 25
 
 
-def parse():
+def parse(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="lcattn", choices=["lcattn", "reference"])
-    ap.add_argument("--workload", default="dense_8k")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--per-workload", default=DEFAULT_PER_WORKLOAD,
+                    help="comma-separated workloads also timed in this run ('' for none)")
+    ap.add_argument("--per-workload-steps", type=int, default=10)
     ap.add_argument("--seed", type=int, default=0)
-    ap.add_argument("--breakdown-reps", type=int, default=5)
-    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--breakdown-reps", type=int, default=3)
+    ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--out", default=None, help="also write the JSON line to this file")
-    return ap.parse_args()
+    return ap.parse_args(argv)
 
 
 def peaks():
@@ -91,26 +107,46 @@ def select_kw(sel):
 # oracle timing (CPU): the bounded sample shared by cpu_baseline and --impl reference
 # ----------------------------------------------------------------------------
 
+def oracle_sample_rows(wl):
+    """Query rows of the oracle sample: the last R rows of the sequence, R a
+    multiple of 128 chosen so that R x N stays near ORACLE_SAMPLE_PAIRS (all
+    rows for short query sides)."""
+    import numpy as np
+    Sq = wl.q_len
+    R = max(128, (ORACLE_SAMPLE_PAIRS // max(1, wl.N)) // 128 * 128)
+    return np.arange(max(0, Sq - R), Sq)
+
+
 def oracle_sample(wl, seed):
     """Inputs for the oracle sample: query head 0 with its KV head over the full
-    sequence, every mask of the workload."""
-    import numpy as np
+    key sequence (the query rows are chosen by oracle_sample_rows)."""
     from synthetic import qkv, qkv_block_structured
     if wl.structure > 0:
         x = qkv_block_structured(1, wl.N, 1, 1, wl.selects[0].block, strength=wl.structure, seed=seed)
     else:
         x = qkv(1, wl.q_len, 1, 1, wl.D, seed=seed, Sk=wl.N)
-    return {k: t.double().numpy() for k, t in x.items()}
+    out = {k: t.double().numpy() for k, t in x.items()}
+    out["rows"] = oracle_sample_rows(wl)
+    return out
+
+
+def sample_desc(wl, sample):
+    rows = sample["rows"]
+    what = "fwd" if wl.forward_only else "fwd+bwd"
+    return (f"fp64 NumPy oracle {what} of query head 0 / KV head 0 of {wl.name}: query rows "
+            f"{int(rows[0])}..{int(rows[-1])} ({len(rows)} of {wl.q_len}) against all N={wl.N} keys, "
+            f"masks {mask_labels(wl)}; effective FLOPs of those rows")
 
 
 def oracle_step(wl, sample):
-    """One oracle pass over the sample; returns effective FLOPs of the sample."""
+    """One oracle pass over the sample; returns the sample's effective FLOPs."""
     import numpy as np
     import oracle
     from oracle import block_select_ref
     from synthetic import MaskSpec
     flops = 0.0
     scale = 1.0 / math.sqrt(wl.D)
+    rows = sample["rows"]
     specs = list(wl.masks)
     for sel in wl.selects:  # the selection is part of the step, as on the GPU
         offs = offsets_uniform(wl.N, sel.block)
@@ -120,12 +156,13 @@ def oracle_step(wl, sample):
                                                  "k_block_lens": np.diff(offs).tolist(),
                                                  "keep": keep[0].astype(bool)}))
     for spec in specs:
-        pairs = oracle.allowed_pairs(spec, wl.q_len, head=0, Sk=wl.N)
+        pairs = int(oracle.allowed(spec, wl.q_len, rows, head=0, Sk=wl.N).sum())
         if wl.forward_only:
-            oracle.attention_fwd(sample["q"], sample["k"], sample["v"], spec, scale)
+            oracle.attention_fwd_rows(sample["q"], sample["k"], sample["v"], spec, scale, 0, 0, rows)
             flops += 4.0 * wl.D * pairs
         else:
-            oracle.attention_bwd(sample["q"], sample["k"], sample["v"], sample["do"], spec, scale)
+            oracle.attention_bwd_rows(sample["q"], sample["k"], sample["v"], sample["do"], spec, scale,
+                                      0, 0, rows)
             flops += 4.0 * wl.D * pairs * 3.5
     return flops
 
@@ -143,13 +180,15 @@ def cpu_threads():
 
 def cpu_baseline(wl, seed):
     sample = oracle_sample(wl, seed)
+    oracle_step(wl, sample)  # first touch of the inputs and the BLAS threads
     t0 = time.perf_counter()
-    flops = oracle_step(wl, sample)
+    reps, flops = 0, 0.0
+    while reps < 1 or (time.perf_counter() - t0 < 10.0 and reps < 8):
+        flops += oracle_step(wl, sample)
+        reps += 1
     dt = time.perf_counter() - t0
     return {"value": flops / dt / 1e12, "unit": UNIT, "cores": cpu_threads(), "kind": "oracle",
-            "seconds": round(dt, 3),
-            "sample": f"fp64 NumPy oracle {'fwd' if wl.forward_only else 'fwd+bwd'}, query head 0 / KV head 0 of {wl.name} over the full "
-                      f"N={wl.N}, masks {mask_labels(wl)}; effective FLOPs of that head"}
+            "seconds": round(dt, 3), "passes": reps, "sample": sample_desc(wl, sample)}
 
 
 def run_reference(args, rank, world):
@@ -167,14 +206,13 @@ def run_reference(args, rank, world):
         times.append(time.perf_counter() - t0)
     ms = 1e3 * statistics.mean(times)
     value = flops / (ms / 1e3) / 1e12
-    sample_desc = (f"query head 0 / KV head 0 of {wl.name} over the full N={wl.N}, "
-                   f"masks {mask_labels(wl)}")
+    desc = sample_desc(wl, sample)
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": workload_desc(wl), "sample": sample_desc},
+            "config": {"workload": workload_desc(wl), "sample": desc},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_threads(), "kind": "oracle",
-                             "sample": sample_desc},
+                             "sample": desc},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     emit(line, args)
 
@@ -280,298 +318,379 @@ def traffic_lookup(kernel, workload):
     sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
     if sha != rec["source_sha256"]:
         return None
-    return {"bytes": rec["dram_bytes_per_launch"], "launch": rec["launch"]}
+    out = {"bytes": rec["dram_bytes_per_launch"], "launch": rec["launch"]}
+    if "scaled_from" in rec:
+        out["scaled_from"] = rec["scaled_from"]
+    return out
+
+
+class Leg:
+    """One workload on one GPU: inputs, compiled masks and buffers, and the
+    timings of its step (all through the C ABI of the library)."""
+
+    def __init__(self, name, seed, rank, dev):
+        import torch
+        import long_context_masked_mask_gb300 as lc
+        from synthetic import qkv, qkv_block_structured, qkv_device, workload
+        self.torch, self.lc, self.dev = torch, lc, dev
+        self.wl = wl = workload(name, seed)
+        B, N, Hq, Hkv, D = wl.B, wl.N, wl.Hq, wl.Hkv, wl.D
+        s = seed + 1000 * rank
+        if wl.structure > 0:
+            x = qkv_block_structured(B, N, Hq, Hkv, wl.selects[0].block, strength=wl.structure, seed=s,
+                                     device=str(dev))
+        elif wl.device_inputs:
+            x = qkv_device(B, N, Hq, Hkv, D, seed=s, device=str(dev))
+        else:
+            x = {k: t.to(dev) for k, t in qkv(B, wl.q_len, Hq, Hkv, D, seed=s, Sk=N).items()}
+        self.q, self.k, self.v, self.d_o = x["q"], x["k"], x["v"], x["do"]
+        q = self.q
+        self.Sq = Sq = q.shape[1]
+        self.fwd_only = wl.forward_only
+        self.shape = shape = lc.make_shape(self.q, self.k, self.v)
+        self.ws = torch.empty(max(16, lc.lcattn_bwd_workspace_size(shape)), dtype=torch.uint8, device=dev)
+        runs = []
+        for spec in wl.masks:
+            m = lc.DeviceMask(spec, Sq, Hq, B, device=dev, Sk=N)
+            meta = lc.lcattn_mask_compile(shape, m, device=dev)
+            fwd_flops = 4.0 * D * m.allowed_pairs
+            runs.append({"spec": spec, "mask": m, "meta": meta,
+                         "fwd_flops": fwd_flops, "bwd_flops": 0.0 if self.fwd_only else 2.5 * fwd_flops,
+                         "launches": (6 if spec.per_head else 5) + (0 if self.fwd_only else 3)})
+        for sel in wl.selects:
+            offs = torch.from_numpy(offsets_uniform(N, sel.block)).to(dev)
+            bmap = torch.empty(B, Hq, offs.numel() - 1, offs.numel() - 1, dtype=torch.uint8, device=dev)
+            sws = torch.empty(lc.lcattn_block_select_workspace_size(q, self.k, lc.select_desc(
+                sel.rule, offs, offs, causal=sel.causal, **select_kw(sel))), dtype=torch.uint8, device=dev)
+            lc.lcattn_block_select(q, self.k, offs, offs, sel.rule, causal=sel.causal, block_map=bmap,
+                                   workspace=sws, **select_kw(sel))
+            m = lc.DeviceMask.from_block_map(bmap, offs, offs)
+            meta = lc.lcattn_mask_compile(shape, m, device=dev)
+            # The inputs are fixed, so every step selects this same map (the
+            # selection is deterministic): its allowed pairs give the step's FLOPs.
+            fwd_flops = 4.0 * D * m.allowed_pairs
+            runs.append({"spec": sel, "sel": sel, "offs": offs, "sws": sws, "mask": m, "meta": meta,
+                         "fwd_flops": fwd_flops, "bwd_flops": 2.5 * fwd_flops, "launches": 2 + 6 + 3})
+        for r in runs:
+            r["o"] = torch.empty_like(q)
+            r["lse"] = torch.empty(B, Hq, Sq, dtype=torch.float32, device=dev)
+            if not self.fwd_only:
+                r["dq"], r["dk"], r["dv"] = torch.empty_like(q), torch.empty_like(self.k), torch.empty_like(self.v)
+            # The forward's split-KV workspace (empty unless the query side is short).
+            fws = lc.lcattn_fwd_workspace_size(shape, r["mask"])
+            r["fws"] = torch.empty(max(16, fws), dtype=torch.uint8, device=dev)
+            r["split"] = fws > 0
+            r["launches"] += 2 if fws > 0 else 1  # split-KV forward: slices + merge
+        self.runs = runs
+        self.step_flops = sum(r["fwd_flops"] + r["bwd_flops"] for r in runs)
+        self.launches_per_step = sum(r["launches"] for r in runs)
+
+    def select(self, r, qq, kk, stage=None):
+        sel = r["sel"]
+        self.lc.lcattn_block_select(qq, kk, r["offs"], r["offs"], sel.rule, causal=sel.causal,
+                                    block_map=r["mask"].block_map, workspace=r["sws"], stage=stage,
+                                    **select_kw(sel))
+
+    def step(self, qq=None, kk=None, vv=None, dd=None):
+        lc = self.lc
+        qq = self.q if qq is None else qq
+        kk = self.k if kk is None else kk
+        vv = self.v if vv is None else vv
+        dd = self.d_o if dd is None else dd
+        for r in self.runs:
+            if "sel" in r:
+                self.select(r, qq, kk)
+            lc.lcattn_mask_compile(self.shape, r["mask"], r["meta"])
+            lc.lcattn_fwd_ws(qq, kk, vv, r["mask"], r["meta"], o=r["o"], lse=r["lse"], workspace=r["fws"])
+            if not self.fwd_only:
+                lc.lcattn_bwd(qq, kk, vv, r["o"], dd, r["lse"], r["mask"], r["meta"],
+                              dq=r["dq"], dk=r["dk"], dv=r["dv"], workspace=self.ws)
+
+    def check_status(self):
+        for r in self.runs:
+            st = self.lc.lcattn_read_status(r["meta"])
+            if st != 0:
+                raise RuntimeError(f"{self.wl.name}: device status {st}: {self.lc.status_string(st)}")
+
+    def time_steps(self, steps, warmup, flush, stream, barrier=lambda: None):
+        """Device time (ms) of each of `steps` steps after `warmup` untimed ones;
+        L2 is flushed before every step."""
+        torch = self.torch
+        for _ in range(warmup):
+            flush.zero_()
+            self.step()
+        torch.cuda.synchronize()
+        self.check_status()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(steps)]
+        barrier()
+        torch.cuda.synchronize()
+        for e0, e1 in evs:
+            flush.zero_()
+            e0.record(stream)
+            self.step()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        return [e0.elapsed_time(e1) for e0, e1 in evs]
+
+    def breakdown(self, reps, flush, stream, pk):
+        """Each kernel alone (CUDA events on the launching stream, L2 flushed
+        before each launch): per-mask forward / backward rates and the total
+        time per kernel name."""
+        torch, lc = self.torch, self.lc
+        wl, q, k, v, d_o = self.wl, self.q, self.k, self.v, self.d_o
+        B, N, Hq, Hkv, D = wl.B, wl.N, wl.Hq, wl.Hkv, wl.D
+        kernels = {"mask_compile": [0.0, 0.0, 0], "fwd_kernel": [0.0, 0.0, 0],
+                   "bwd_prepass": [0.0, 0.0, 0], "dkdv_kernel": [0.0, 0.0, 0], "dq_convert": [0.0, 0.0, 0]}
+        if wl.selects:
+            kernels["pool_kernel"] = [0.0, 0.0, 0]
+            kernels["select_kernel"] = [0.0, 0.0, 0]
+        self.select_roof = None
+
+        def timed(fn):
+            tot = 0.0
+            for _ in range(reps):
+                flush.zero_()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                fn()
+                e1.record(stream)
+                torch.cuda.synchronize()
+                tot += e0.elapsed_time(e1)
+            return tot / reps
+
+        def graph_timed(fn, n=8):
+            """Average device time of fn's launches, replayed from a CUDA graph of n
+            back-to-back calls (no host launch overhead between them).  Used for the
+            sub-millisecond selection kernels; the pool kernel's inputs (Q and K) are
+            larger than L2, so consecutive launches still stream them from HBM."""
+            fn()
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                for _ in range(n):
+                    fn()
+            tot = 0.0
+            for _ in range(reps):
+                flush.zero_()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                g.replay()
+                e1.record(stream)
+                torch.cuda.synchronize()
+                tot += e0.elapsed_time(e1)
+            return tot / reps / n
+
+        per_mask = []
+        for r in self.runs:
+            m, meta = r["mask"], r["meta"]
+            t_sel = None
+            if "sel" in r:
+                t_pool = graph_timed(lambda: self.select(r, q, k, stage=1))
+                t_pick = graph_timed(lambda: self.select(r, q, k, stage=2))
+                t_sel = (t_pool, t_pick)
+                kernels["pool_kernel"][0] += t_pool
+                kernels["pool_kernel"][2] += 1
+                kernels["select_kernel"][0] += t_pick
+                kernels["select_kernel"][2] += 1
+                nb = r["offs"].numel() - 1
+                pool_bytes = (B * N * (Hq + Hkv) * D * q.element_size()       # Q and K read once
+                              + B * (Hq + Hkv) * nb * D * 4)                 # fp32 block means written
+                gbs = pool_bytes / (t_pool / 1e3) / 1e9
+                self.select_roof = {"kernel": "pool_kernel", "bound": "hbm", "achieved": round(gbs, 1),
+                                    "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": round(gbs / pk["hbm_gbs"], 4),
+                                    "algorithmic_bytes": pool_bytes,
+                                    "peak_kind": f"{pk['source']} copy bandwidth",
+                                    "traffic": (traffic_lookup("pool_kernel", wl.name) or {}).get("bytes")}
+            t_c = timed(lambda: lc.lcattn_mask_compile(self.shape, m, meta))
+            t_f = timed(lambda: lc.lcattn_fwd_ws(q, k, v, m, meta, o=r["o"], lse=r["lse"], workspace=r["fws"]))
+            tb = [0.0, 0.0, 0.0]
+            if not self.fwd_only:
+                tb = [timed(lambda: lc.lcattn_bwd(q, k, v, r["o"], d_o, r["lse"], m, meta, dq=r["dq"],
+                                                  dk=r["dk"], dv=r["dv"], workspace=self.ws, stage=stage))
+                      for stage in (1, 2, 3)]
+            for name, t, fl in (("mask_compile", t_c, 0.0), ("fwd_kernel", t_f, r["fwd_flops"]),
+                                ("bwd_prepass", tb[0], 0.0), ("dkdv_kernel", tb[1], r["bwd_flops"]),
+                                ("dq_convert", tb[2], 0.0)):
+                kernels[name][0] += t
+                kernels[name][1] += fl
+                kernels[name][2] += 1
+            fwd_tf = r["fwd_flops"] / (t_f / 1e3) / 1e12
+            bwd_tf = r["bwd_flops"] / (sum(tb) / 1e3) / 1e12 if not self.fwd_only else 0.0
+            per_mask.append({"mask": r["spec"].label(), "allowed_pairs": r["mask"].allowed_pairs,
+                             "density": r["mask"].allowed_pairs / (B * Hq * self.Sq * N),
+                             "forward_path": "split-KV (heads packed)" if r["split"] else "persistent",
+                             "fwd_ms": round(t_f, 4), "bwd_ms": round(sum(tb), 4),
+                             "bwd_stage_ms": [round(t, 4) for t in tb], "mask_compile_ms": round(t_c, 4),
+                             "fwd_tflops": round(fwd_tf, 1), "bwd_tflops": round(bwd_tf, 1),
+                             "fwd_frac_of_peak": round(fwd_tf / pk["burst"], 4),
+                             "bwd_frac_of_peak": round(bwd_tf / pk["burst"], 4)})
+            if t_sel is not None:
+                per_mask[-1]["select_ms"] = [round(t_sel[0], 4), round(t_sel[1], 4)]
+        self.kernels = kernels
+        return per_mask, kernels
+
+    def roofline(self, pk):
+        """The dominant kernel (most event time in the breakdown) against its roof."""
+        kernels, wl, q = self.kernels, self.wl, self.q
+        B, Hq = wl.B, wl.Hq
+        dom = max(kernels, key=lambda n: kernels[n][0])
+        t_dom, fl_dom, n_dom = kernels[dom]
+        fwd_bytes = (q.numel() + self.k.numel() + self.v.numel() + q.numel()) * q.element_size() + B * Hq * self.Sq * 4
+        # A forward-only step is HBM-bound when its arithmetic intensity (FLOPs per
+        # algorithmic byte) is below the ridge point of the two measured peaks.
+        hbm_bound = self.fwd_only and (self.step_flops / len(self.runs)) / fwd_bytes < \
+            pk["burst"] * 1e12 / (pk["hbm_gbs"] * 1e9)
+        if hbm_bound:
+            # Decode-style rows read every K/V byte once per step and do little
+            # arithmetic per byte.  Algorithmic bytes: Q, K, V read, O and LSE
+            # written, per mask.
+            gbs = fwd_bytes * n_dom / (t_dom / 1e3) / 1e9
+            roof = {"kernel": "split_kernel + combine_kernel" if self.runs[0]["split"] else "fwd_kernel",
+                    "bound": "hbm", "achieved": round(gbs, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
+                    "frac": round(gbs / pk["hbm_gbs"], 4), "algorithmic_bytes": fwd_bytes,
+                    "peak_kind": f"{pk['source']} copy bandwidth"}
+        elif fl_dom > 0:
+            achieved = fl_dom / (t_dom / 1e3) / 1e12
+            roof = {"kernel": dom, "bound": "tensor", "achieved": round(achieved, 1), "peak": pk["burst"],
+                    "unit": "TFLOP/s", "frac": round(achieved / pk["burst"], 4),
+                    "frac_of_sustained": round(achieved / pk["sustained"], 4),
+                    "algorithmic_flops_per_launch": fl_dom / max(1, n_dom),
+                    "launches": n_dom, "ms_per_launch": round(t_dom / max(1, n_dom), 4),
+                    "peak_kind": f"bf16 dense, {pk['source']} burst (each kernel timed alone)"}
+        else:  # a memory-bound kernel dominating would be reported against HBM
+            roof = {"kernel": dom, "bound": "hbm", "achieved": None, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                    "frac": None, "peak_kind": f"{pk['source']} copy bandwidth"}
+        tr = traffic_lookup("split_kernel" if hbm_bound and self.runs[0]["split"] else dom, wl.name)
+        roof["traffic"] = tr["bytes"] if tr else None
+        if tr:
+            roof["traffic_launch"] = tr["launch"]
+            if "scaled_from" in tr:
+                roof["traffic_scaled_from"] = tr["scaled_from"]
+        return roof
+
+    def e2e(self, warmup, steps, flush, stream):
+        """The same step end to end through the C ABI with host buffers: pinned
+        host inputs copied up and every result copied down inside the timed region."""
+        torch, lc = self.torch, self.lc
+        q, k, v, d_o = self.q, self.k, self.v, self.d_o
+        ins = (("q", q), ("k", k), ("v", v)) + ((("do", d_o),) if not self.fwd_only else ())
+        host = {n: t.cpu().pin_memory() for n, t in ins}
+        q_, k_, v_, do_ = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v), torch.empty_like(d_o)
+        out_names = ("o", "lse") if self.fwd_only else ("o", "lse", "dq", "dk", "dv")
+        outs = [{n: torch.empty(r[n].shape, dtype=r[n].dtype, pin_memory=True) for n in out_names}
+                for r in self.runs]
+        h2d = sum(t.numel() * t.element_size() for t in host.values())
+        d2h = sum(t.numel() * t.element_size() for o in outs for t in o.values())
+        # Copies overlap compute the way a training loop would: dO goes up on a
+        # copy stream while the first forward runs, and each mask's results go down
+        # on it while the next mask computes.  Every byte still moves inside the
+        # timed region: e1 is recorded after the copy stream has been joined.
+        copy_stream = torch.cuda.Stream(device=self.dev)
+        ms = []
+        for i in range(warmup + steps):
+            flush.zero_()
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            copy_stream.wait_stream(stream)
+            with torch.cuda.stream(copy_stream):
+                if not self.fwd_only:
+                    do_.copy_(host["do"], non_blocking=True)
+            do_ready = torch.cuda.Event()
+            do_ready.record(copy_stream)
+            q_.copy_(host["q"], non_blocking=True)
+            k_.copy_(host["k"], non_blocking=True)
+            v_.copy_(host["v"], non_blocking=True)
+            for j, (r, o) in enumerate(zip(self.runs, outs)):
+                if "sel" in r:
+                    self.select(r, q_, k_)
+                lc.lcattn_mask_compile(self.shape, r["mask"], r["meta"])
+                lc.lcattn_fwd_ws(q_, k_, v_, r["mask"], r["meta"], o=r["o"], lse=r["lse"], workspace=r["fws"])
+                if j == 0:
+                    stream.wait_event(do_ready)
+                if not self.fwd_only:
+                    lc.lcattn_bwd(q_, k_, v_, r["o"], do_, r["lse"], r["mask"], r["meta"],
+                                  dq=r["dq"], dk=r["dk"], dv=r["dv"], workspace=self.ws)
+                copy_stream.wait_stream(stream)
+                with torch.cuda.stream(copy_stream):
+                    for n in o:
+                        o[n].copy_(r[n], non_blocking=True)
+            stream.wait_stream(copy_stream)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            if i >= warmup:
+                ms.append(e0.elapsed_time(e1))
+        return ms, h2d, d2h
+
+    def summary(self, steps, ms, world, per_mask, kernels, roof):
+        return {"workload": workload_desc(self.wl), "steps": steps, "ms_per_step": round(ms, 4),
+                "value": round(whole_job_rate(world, self.step_flops, ms), 2), "unit": UNIT,
+                "per_mask": per_mask, "kernel_ms": {n: round(v[0], 4) for n, v in kernels.items()},
+                "roofline": roof}
 
 
 def run_gpu(args, rank, world, dist):
     import torch
-    import long_context_masked_mask_gb300 as lc
-    from synthetic import qkv, qkv_block_structured, qkv_device, workload
 
     local = int(os.environ.get("LOCAL_RANK", "0"))
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    wl = workload(args.workload, args.seed)
-    B, N, Hq, Hkv, D = wl.B, wl.N, wl.Hq, wl.Hkv, wl.D
-    seed = args.seed + 1000 * rank
-    if wl.structure > 0:
-        x = qkv_block_structured(B, N, Hq, Hkv, wl.selects[0].block, strength=wl.structure, seed=seed,
-                                 device=str(dev))
-    elif wl.device_inputs:
-        x = qkv_device(B, N, Hq, Hkv, D, seed=seed, device=str(dev))
-    else:
-        x = {k: t.to(dev) for k, t in qkv(B, wl.q_len, Hq, Hkv, D, seed=seed, Sk=N).items()}
-    q, k, v, d_o = x["q"], x["k"], x["v"], x["do"]
-    Sq = q.shape[1]
-    fwd_only = wl.forward_only
-    shape = lc.make_shape(q, k, v)
-    ws = torch.empty(lc.lcattn_bwd_workspace_size(shape), dtype=torch.uint8, device=dev)
-    runs = []
-    for spec in wl.masks:
-        m = lc.DeviceMask(spec, Sq, Hq, B, device=dev, Sk=N)
-        meta = lc.lcattn_mask_compile(shape, m, device=dev)
-        fwd_flops = 4.0 * D * m.allowed_pairs
-        runs.append({"spec": spec, "mask": m, "meta": meta, "o": torch.empty_like(q),
-                     "lse": torch.empty(B, Hq, Sq, dtype=torch.float32, device=dev),
-                     "dq": torch.empty_like(q), "dk": torch.empty_like(k), "dv": torch.empty_like(v),
-                     "fwd_flops": fwd_flops, "bwd_flops": 0.0 if fwd_only else 2.5 * fwd_flops,
-                     "launches": (6 if spec.per_head else 5) + (0 if fwd_only else 3)})
-    for sel in wl.selects:
-        offs = torch.from_numpy(offsets_uniform(N, sel.block)).to(dev)
-        bmap = torch.empty(B, Hq, offs.numel() - 1, offs.numel() - 1, dtype=torch.uint8, device=dev)
-        sws = torch.empty(lc.lcattn_block_select_workspace_size(q, k, lc.select_desc(
-            sel.rule, offs, offs, causal=sel.causal, **select_kw(sel))), dtype=torch.uint8, device=dev)
-        lc.lcattn_block_select(q, k, offs, offs, sel.rule, causal=sel.causal, block_map=bmap,
-                               workspace=sws, **select_kw(sel))
-        m = lc.DeviceMask.from_block_map(bmap, offs, offs)
-        meta = lc.lcattn_mask_compile(shape, m, device=dev)
-        # The inputs are fixed, so every step selects this same map (the
-        # selection is deterministic): its allowed pairs give the step's FLOPs.
-        fwd_flops = 4.0 * D * m.allowed_pairs
-        runs.append({"spec": sel, "sel": sel, "offs": offs, "sws": sws, "mask": m, "meta": meta,
-                     "o": torch.empty_like(q), "lse": torch.empty(B, Hq, N, dtype=torch.float32, device=dev),
-                     "dq": torch.empty_like(q), "dk": torch.empty_like(k), "dv": torch.empty_like(v),
-                     "fwd_flops": fwd_flops, "bwd_flops": 2.5 * fwd_flops,
-                     "launches": 2 + 6 + 3})
-    for r in runs:  # the forward's split-KV workspace (empty unless the query side is short)
-        fws = lc.lcattn_fwd_workspace_size(shape, r["mask"])
-        r["fws"] = torch.empty(max(16, fws), dtype=torch.uint8, device=dev)
-        r["split"] = fws > 0
-        r["launches"] += 2 if fws > 0 else 1  # split-KV forward: slices + merge
-    step_flops = sum(r["fwd_flops"] + r["bwd_flops"] for r in runs)
-    launches_per_step = sum(r["launches"] for r in runs)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
-
-    def select(r, qq, kk, stage=None):
-        sel = r["sel"]
-        lc.lcattn_block_select(qq, kk, r["offs"], r["offs"], sel.rule, causal=sel.causal,
-                               block_map=r["mask"].block_map, workspace=r["sws"], stage=stage,
-                               **select_kw(sel))
-
-    def step(qq=q, kk=k, vv=v, dd=d_o):
-        for r in runs:
-            if "sel" in r:
-                select(r, qq, kk)
-            lc.lcattn_mask_compile(shape, r["mask"], r["meta"])
-            lc.lcattn_fwd_ws(qq, kk, vv, r["mask"], r["meta"], o=r["o"], lse=r["lse"], workspace=r["fws"])
-            if not fwd_only:
-                lc.lcattn_bwd(qq, kk, vv, r["o"], dd, r["lse"], r["mask"], r["meta"],
-                              dq=r["dq"], dk=r["dk"], dv=r["dv"], workspace=ws)
+    pk = peaks()
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
 
     def barrier():
         if dist is not None:
             dist.barrier()
 
-    for _ in range(args.warmup):
-        flush.zero_()
-        step()
-    torch.cuda.synchronize()
-    for r in runs:
-        st = lc.lcattn_read_status(r["meta"])
-        if st != 0:
-            raise RuntimeError(f"device status {st}: {lc.status_string(st)}")
-
-    # ---- timed region -------------------------------------------------------
+    # ---- headline workload -------------------------------------------------
+    leg = Leg(args.workload, args.seed, rank, dev)
+    wl = leg.wl
     try:
         gpu_sel = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
     except Exception:
         gpu_sel = str(local)
+    # Warm-up first, then the clock sampler: it must see the timed region.
+    for _ in range(args.warmup):
+        flush.zero_()
+        leg.step()
+    torch.cuda.synchronize()
     sampler = ClockSampler(gpu_sel)
     time.sleep(0.3)
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(args.steps)]
-    barrier()
-    torch.cuda.synchronize()
-    for e0, e1 in evs:
-        flush.zero_()
-        e0.record(stream)
-        step()
-        e1.record(stream)
-    torch.cuda.synchronize()
-    barrier()
+    ms_steps = leg.time_steps(args.steps, 0, flush, stream, barrier)
     clocks = sampler.stop()
-    ms_steps = [e0.elapsed_time(e1) for e0, e1 in evs]
     ms = max_over_ranks(statistics.mean(ms_steps), dist, dev)
-    value = whole_job_rate(world, step_flops, ms)
-
-    # ---- per-kernel breakdown (CUDA events on the launching stream) ---------
-    pk = peaks()
-    kernels = {"mask_compile": [0.0, 0.0, 0], "fwd_kernel": [0.0, 0.0, 0],
-               "bwd_prepass": [0.0, 0.0, 0], "dkdv_kernel": [0.0, 0.0, 0], "dq_convert": [0.0, 0.0, 0]}
-    if wl.selects:
-        kernels["pool_kernel"] = [0.0, 0.0, 0]
-        kernels["select_kernel"] = [0.0, 0.0, 0]
-    select_roof = None
-    per_mask = []
-    reps = args.breakdown_reps
-
-    def timed(fn):
-        tot = 0.0
-        for _ in range(reps):
-            flush.zero_()
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            fn()
-            e1.record(stream)
-            torch.cuda.synchronize()
-            tot += e0.elapsed_time(e1)
-        return tot / reps
-
-    def graph_timed(fn, n=8):
-        """Average device time of fn's launches, replayed from a CUDA graph of n
-        back-to-back calls (no host launch overhead between them).  Used for the
-        sub-millisecond selection kernels; the pool kernel's inputs (Q and K) are
-        larger than L2, so consecutive launches still stream them from HBM."""
-        fn()
-        torch.cuda.synchronize()
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g):
-            for _ in range(n):
-                fn()
-        tot = 0.0
-        for _ in range(reps):
-            flush.zero_()
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            g.replay()
-            e1.record(stream)
-            torch.cuda.synchronize()
-            tot += e0.elapsed_time(e1)
-        return tot / reps / n
-
-    for r in runs:
-        m, meta = r["mask"], r["meta"]
-        t_sel = None
-        if "sel" in r:
-            t_pool = graph_timed(lambda: select(r, q, k, stage=1))
-            t_pick = graph_timed(lambda: select(r, q, k, stage=2))
-            t_sel = (t_pool, t_pick)
-            kernels["pool_kernel"][0] += t_pool
-            kernels["pool_kernel"][2] += 1
-            kernels["select_kernel"][0] += t_pick
-            kernels["select_kernel"][2] += 1
-            nb = r["offs"].numel() - 1
-            pool_bytes = (B * N * (Hq + Hkv) * D * q.element_size()       # Q and K read once
-                          + B * (Hq + Hkv) * nb * D * 4)                 # fp32 block means written
-            gbs = pool_bytes / (t_pool / 1e3) / 1e9
-            select_roof = {"kernel": "pool_kernel", "bound": "hbm", "achieved": round(gbs, 1),
-                           "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": round(gbs / pk["hbm_gbs"], 4),
-                           "algorithmic_bytes": pool_bytes,
-                           "peak_kind": f"{pk['source']} copy bandwidth",
-                           "traffic": (traffic_lookup("pool_kernel", wl.name) or {}).get("bytes")}
-        t_c = timed(lambda: lc.lcattn_mask_compile(shape, m, meta))
-        t_f = timed(lambda: lc.lcattn_fwd_ws(q, k, v, m, meta, o=r["o"], lse=r["lse"], workspace=r["fws"]))
-        tb = [0.0, 0.0, 0.0]
-        if not fwd_only:
-            tb = [timed(lambda: lc.lcattn_bwd(q, k, v, r["o"], d_o, r["lse"], m, meta, dq=r["dq"],
-                                              dk=r["dk"], dv=r["dv"], workspace=ws, stage=stage))
-                  for stage in (1, 2, 3)]
-        for name, t, fl in (("mask_compile", t_c, 0.0), ("fwd_kernel", t_f, r["fwd_flops"]),
-                            ("bwd_prepass", tb[0], 0.0), ("dkdv_kernel", tb[1], r["bwd_flops"]),
-                            ("dq_convert", tb[2], 0.0)):
-            kernels[name][0] += t
-            kernels[name][1] += fl
-            kernels[name][2] += 1
-        fwd_tf = r["fwd_flops"] / (t_f / 1e3) / 1e12
-        bwd_tf = r["bwd_flops"] / (sum(tb) / 1e3) / 1e12 if not fwd_only else 0.0
-        per_mask.append({"mask": r["spec"].label(), "allowed_pairs": r["mask"].allowed_pairs,
-                         "density": r["mask"].allowed_pairs / (B * Hq * Sq * N),
-                         "forward_path": "split-KV (heads packed)" if r["split"] else "persistent",
-                         "fwd_ms": round(t_f, 4), "bwd_ms": round(sum(tb), 4),
-                         "bwd_stage_ms": [round(t, 4) for t in tb], "mask_compile_ms": round(t_c, 4),
-                         "fwd_tflops": round(fwd_tf, 1), "bwd_tflops": round(bwd_tf, 1),
-                         "fwd_frac_of_peak": round(fwd_tf / pk["sustained"], 4),
-                         "bwd_frac_of_peak": round(bwd_tf / pk["sustained"], 4)})
-        if t_sel is not None:
-            per_mask[-1]["select_ms"] = [round(t_sel[0], 4), round(t_sel[1], 4)]
-    dom = max(kernels, key=lambda n: kernels[n][0])
-    t_dom, fl_dom, n_dom = kernels[dom]
-    fwd_bytes = (q.numel() + k.numel() + v.numel() + q.numel()) * q.element_size() + B * Hq * Sq * 4
-    # A forward-only step is HBM-bound when its arithmetic intensity (FLOPs per
-    # algorithmic byte) is below the ridge point of the two measured peaks.
-    hbm_bound = fwd_only and (step_flops / len(runs)) / fwd_bytes < pk["sustained"] * 1e12 / (pk["hbm_gbs"] * 1e9)
-    if hbm_bound:
-        # Decode-style rows read every K/V byte once per step and do little
-        # arithmetic per byte.  Algorithmic bytes: Q, K, V read, O and LSE
-        # written, per mask.
-        gbs = fwd_bytes * n_dom / (t_dom / 1e3) / 1e9
-        roof = {"kernel": "split_kernel + combine_kernel" if runs[0]["split"] else "fwd_kernel",
-                "bound": "hbm", "achieved": round(gbs, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
-                "frac": round(gbs / pk["hbm_gbs"], 4), "algorithmic_bytes": fwd_bytes,
-                "peak_kind": f"{pk['source']} copy bandwidth"}
-    elif fl_dom > 0:
-        achieved = fl_dom / (t_dom / 1e3) / 1e12
-        roof = {"kernel": dom, "bound": "tensor", "achieved": round(achieved, 1), "peak": pk["sustained"],
-                "unit": "TFLOP/s", "frac": round(achieved / pk["sustained"], 4),
-                "peak_kind": f"bf16 dense, {pk['source']} sustained"}
-    else:  # a memory-bound kernel dominating would be reported against HBM
-        roof = {"kernel": dom, "bound": "hbm", "achieved": None, "peak": pk["hbm_gbs"], "unit": "GB/s",
-                "frac": None, "peak_kind": f"{pk['source']} copy bandwidth"}
-    tr = traffic_lookup("split_kernel" if hbm_bound and runs[0]["split"] else dom, wl.name)
-    roof["traffic"] = tr["bytes"] if tr else None
-    if tr:
-        roof["traffic_launch"] = tr["launch"]
-
-    # ---- end to end through the C ABI with host buffers ----------------------
-    ins = (("q", q), ("k", k), ("v", v)) + ((("do", d_o),) if not fwd_only else ())
-    host = {n: t.cpu().pin_memory() for n, t in ins}
-    dq_, dk_, dv_, do_ = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v), torch.empty_like(d_o)
-    q_, k_, v_ = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    out_names = ("o", "lse") if fwd_only else ("o", "lse", "dq", "dk", "dv")
-    outs = [{n: torch.empty(r[n].shape, dtype=r[n].dtype, pin_memory=True) for n in out_names}
-            for r in runs]
-    h2d = sum(t.numel() * t.element_size() for t in host.values())
-    d2h = sum(t.numel() * t.element_size() for o in outs for t in o.values())
-    # Copies overlap compute the way a training loop would: dO goes up on a
-    # copy stream while the first forward runs, and each mask's results go down
-    # on it while the next mask computes.  Every byte still moves inside the
-    # timed region: e1 is recorded after the copy stream has been joined.
-    copy_stream = torch.cuda.Stream(device=dev)
-    e2e_ms = []
-    for i in range(args.warmup + args.e2e_steps):
-        flush.zero_()
-        torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        copy_stream.wait_stream(stream)
-        with torch.cuda.stream(copy_stream):
-            if not fwd_only:
-                do_.copy_(host["do"], non_blocking=True)
-        do_ready = torch.cuda.Event()
-        do_ready.record(copy_stream)
-        q_.copy_(host["q"], non_blocking=True)
-        k_.copy_(host["k"], non_blocking=True)
-        v_.copy_(host["v"], non_blocking=True)
-        for j, (r, o) in enumerate(zip(runs, outs)):
-            if "sel" in r:
-                select(r, q_, k_)
-            lc.lcattn_mask_compile(shape, r["mask"], r["meta"])
-            lc.lcattn_fwd_ws(q_, k_, v_, r["mask"], r["meta"], o=r["o"], lse=r["lse"], workspace=r["fws"])
-            if j == 0:
-                stream.wait_event(do_ready)
-            if not fwd_only:
-                lc.lcattn_bwd(q_, k_, v_, r["o"], do_, r["lse"], r["mask"], r["meta"],
-                              dq=r["dq"], dk=r["dk"], dv=r["dv"], workspace=ws)
-            copy_stream.wait_stream(stream)
-            with torch.cuda.stream(copy_stream):
-                for n in o:
-                    o[n].copy_(r[n], non_blocking=True)
-        stream.wait_stream(copy_stream)
-        e1.record(stream)
-        torch.cuda.synchronize()
-        if i >= args.warmup:
-            e2e_ms.append(e0.elapsed_time(e1))
+    value = whole_job_rate(world, leg.step_flops, ms)
+    per_mask, kernels = leg.breakdown(args.breakdown_reps, flush, stream, pk)
+    roof = leg.roofline(pk)
+    e2e_ms, h2d, d2h = leg.e2e(min(args.warmup, 3), args.e2e_steps, flush, stream)
     e2e_t = max_over_ranks(statistics.mean(e2e_ms), dist, dev)
-    e2e = {"value": whole_job_rate(world, step_flops, e2e_t), "unit": UNIT, "ms_per_step": e2e_t,
+    e2e = {"value": whole_job_rate(world, leg.step_flops, e2e_t), "unit": UNIT, "ms_per_step": e2e_t,
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
            "copies": "pinned host buffers; dO and each mask's results move on a copy stream that "
                      "overlaps compute; all copies inside the timed region"}
+    leg.check_status()
+    select_roof = getattr(leg, "select_roof", None)
+    launches = leg.launches_per_step * args.steps
+    headline = {"B": wl.B, "N": wl.N, "Hq": wl.Hq, "Hkv": wl.Hkv, "D": wl.D}
+    del leg
+    torch.cuda.empty_cache()
 
-    for r in runs:
-        st = lc.lcattn_read_status(r["meta"])
-        if st != 0:
-            raise RuntimeError(f"device status {st}: {lc.status_string(st)}")
+    # ---- the other configurations, timed in the same run ----------------------
+    per_workload = []
+    names = [n for n in (args.per_workload or "").split(",") if n and n != args.workload]
+    for name in names:
+        other = Leg(name, args.seed, rank, dev)
+        ms_o = other.time_steps(args.per_workload_steps, max(3, min(args.warmup, 5)), flush, stream, barrier)
+        ms_o = max_over_ranks(statistics.mean(ms_o), dist, dev)
+        pm, kn = other.breakdown(args.breakdown_reps, flush, stream, pk)
+        summary = other.summary(args.per_workload_steps, ms_o, world, pm, kn, other.roofline(pk))
+        other.check_status()
+        per_workload.append(summary)
+        del other
+        torch.cuda.empty_cache()
 
     if rank != 0:
         return
@@ -579,16 +698,19 @@ def run_gpu(args, rank, world, dist):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic",
-            "config": {"workload": workload_desc(wl), "seq_len": N, "global_batch": B * world,
-                       "heads": f"{Hq}:{Hkv}", "head_dim": D,
+            "config": {"workload": workload_desc(wl), "seq_len": headline["N"],
+                       "global_batch": headline["B"] * world,
+                       "heads": f"{headline['Hq']}:{headline['Hkv']}", "head_dim": headline["D"],
                        "parallelism": f"replicas x{world} (independent batches, no collective)",
                        "l2": f"flushed by a {L2_FLUSH_BYTES >> 20} MiB write before every timed step"},
-            "frac_of_peak": round(value / pk["sustained"], 4),
-            "peak_tflops": {"sustained": pk["sustained"], "burst": pk["burst"], "source": pk["source"]},
+            "frac_of_peak": round(value / pk["burst"], 4),
+            "frac_of_sustained_peak": round(value / pk["sustained"], 4),
+            "peak_tflops": {"burst": pk["burst"], "sustained": pk["sustained"], "source": pk["source"],
+                            "per_mask_and_roofline": "burst (each kernel timed alone)"},
             "per_mask": per_mask,
             "kernel_ms": {n: round(v[0], 4) for n, v in kernels.items()},
-            "roofline": roof, "e2e": e2e, "gpu_launches": launches_per_step * args.steps,
-            "clocks": clocks}
+            "roofline": roof, "e2e": e2e, "gpu_launches": launches,
+            "clocks": clocks, "per_workload": per_workload}
     if select_roof is not None:
         line["roofline_select"] = select_roof
     if world == 1 and not args.no_cpu_baseline:

@@ -22,8 +22,11 @@
  *
  * Conventions for every call:
  *   - Pointers marked "device" point to GPU memory, owned by the caller.  The
- *     library allocates nothing, frees nothing and keeps no state between calls
- *     besides cached kernel attributes.
+ *     library allocates nothing and frees nothing.  Between calls it keeps
+ *     cached kernel attributes and, for lcattn_bwd_noalloc only, one fixed
+ *     device array of LCATTN_NOALLOC_SCRATCH_BYTES per GPU (part of the
+ *     library's image, held until the process exits) with its device address
+ *     cached per GPU; that array's contents carry over from call to call.
  *   - Calls are asynchronous on `stream` (NULL = the legacy default stream); the
  *     library never synchronises except in lcattn_read_status.
  *   - Arguments are validated on the host before anything is launched; an
@@ -31,7 +34,9 @@
  *   - Tensors are bf16 (except LSE / D / accumulators, fp32) with the last
  *     dimension (head dim: 64, 128 or 256 elements) contiguous; the (batch, sequence,
  *     head) strides are given in elements and must be multiples of 8 (16
- *     bytes), and base pointers must be 16-byte aligned.
+ *     bytes), and base pointers must be 16-byte aligned.  With B > 1 every
+ *     batch stride must be at least the head dim (a zero, broadcast batch
+ *     stride is refused with LCATTN_ERR_UNSUPPORTED); with B = 1 it is unused.
  *   - Query head h reads KV head h / (Hq / Hkv) (contiguous GQA groups).
  */
 #ifndef LCATTN_H_
@@ -223,7 +228,12 @@ int lcattn_block_select_stage(int stage, const lcattn_shape* shape, const void* 
                               float* scores, void* workspace, size_t workspace_bytes,
                               lcattn_stream_t stream);
 
-/* Forward.  q [B][Sq][Hq][D], k/v [B][Sk][Hkv][D] bf16 (device) ->
+/* Forward: the attention operator every dense and sparse kernel on the pages
+ * computes ("Long-Context Attention Benchmark", xllm-io blog review, sections
+ * "密集注意力内核" and "稀疏注意力内核"), restricted to the tiles the mask
+ * compiler left non-empty; LSE is the per-row log-sum-exp that the pages'
+ * distributed section ("分布式注意力机制", Ring P2P) merges partial results by.
+ * q [B][Sq][Hq][D], k/v [B][Sk][Hkv][D] bf16 (device) ->
  * o [B][Sq][Hq][D] bf16 and lse [B][Hq][Sq] fp32 (natural log; -inf for a
  * row with no allowed key, whose O row is 0).  `tile_meta` must come from
  * lcattn_mask_compile with the same shape sizes and descriptor, and `mask`
@@ -241,7 +251,9 @@ int lcattn_fwd(const lcattn_shape* shape, const void* q, const void* k, const vo
                const void* tile_meta, const lcattn_mask_desc* mask, float scale, void* o,
                float* lse, lcattn_stream_t stream);
 
-/* Forward with a workspace, for short query sides.  When the regular
+/* Forward with a workspace, for short query sides (the same operator as
+ * lcattn_fwd, blog sections "密集注意力内核" / "稀疏注意力内核"; the split over
+ * the key side is the flash-decoding scheme, merged by LSE).  When the regular
  * forward's work items (query tiles x head pairs x batch) are fewer than the
  * GPU's SMs -- decode-style rows, or a short chunk of queries against a long
  * key sequence (Sq < Sk, bottom-right aligned) -- and the mask is column
@@ -261,7 +273,10 @@ int lcattn_fwd_ws(const lcattn_shape* shape, const void* q, const void* k, const
                   const void* tile_meta, const lcattn_mask_desc* mask, float scale, void* o,
                   float* lse, void* workspace, size_t workspace_bytes, lcattn_stream_t stream);
 
-/* The backward calls below take head dim 64 or 128; head dim 256 returns
+/* The backward calls below compute the gradients of the same operator (blog
+ * sections "密集注意力内核" / "稀疏注意力内核"; the pages' sparse-kernel findings,
+ * sections "稀疏内核性能" and "核心发现总结", single the backward out as the main
+ * bottleneck).  They take head dim 64 or 128; head dim 256 returns
  * LCATTN_ERR_UNSUPPORTED (its dK and dV accumulators, 2 x 256 fp32 columns,
  * do not fit in tensor memory beside S and dP) and its workspace size is 0.
  *
@@ -273,7 +288,9 @@ int lcattn_fwd_ws(const lcattn_shape* shape, const void* q, const void* k, const
  * shares of its group's query heads and the partials are summed into dK, dV. */
 size_t lcattn_bwd_workspace_size(const lcattn_shape* shape);
 
-/* Backward of L = sum(O * dO).  Inputs as for lcattn_fwd plus o, d_o (bf16,
+/* Backward of L = sum(O * dO) (blog sections "密集注意力内核" / "稀疏注意力内核":
+ * the textbook gradients dV = P^T dO, dS = P * (dO V^T - rowsum(dO * O)),
+ * dQ = scale * dS K, dK = scale * dS^T Q).  Inputs as for lcattn_fwd plus o, d_o (bf16,
  * o_stride) and lse from the forward.  Outputs dq (bf16, q_stride), dk
  * (k_stride) and dv (v_stride); dk/dv hold the sum over each GQA group.  The
  * three steps run in order on `stream`: D pre-pass (also zeroes the dQ
@@ -284,7 +301,7 @@ int lcattn_bwd(const lcattn_shape* shape, const void* q, const void* k, const vo
                const lcattn_mask_desc* mask, float scale, void* dq, void* dk, void* dv,
                void* workspace, size_t workspace_bytes, lcattn_stream_t stream);
 
-/* One stage of lcattn_bwd, same arguments: stage 1 = D pre-pass (and zeroing
+/* One stage of lcattn_bwd (same operator and sections), same arguments: stage 1 = D pre-pass (and zeroing
  * of the dQ accumulator), 2 = dK/dV with dQ partials, 3 = dQ conversion.
  * Running stages 1, 2, 3 in order on one stream is exactly lcattn_bwd; the
  * stages exist so that each kernel can be scheduled or timed on its own.
@@ -308,8 +325,10 @@ int lcattn_bwd_stage(int stage, const lcattn_shape* shape, const void* q, const 
  * the library holds it until the process exits.  This call never splits
  * dK/dV work units (it needs no partials).  A problem whose D vector and dQ
  * accumulator exceed the array returns LCATTN_ERR_SCRATCH_LIMIT and launches
- * nothing (32 MiB covers B * Hq * Sq up to 65,027 query rows, e.g. 8 heads at
- * 8K tokens).
+ * nothing.  The need is 4 * B*Hq*Sq bytes for D plus 4 * D * B*Hq*Sq bytes for
+ * the accumulator, each rounded up to 256 bytes: 32 MiB covers B * Hq * Sq up
+ * to 65,027 query rows at head dim 128 (e.g. 8 heads at 8K tokens) and
+ * 129,055 at head dim 64.
  *
  * The first call on a device looks the array's device address up (with that
  * device current) and caches it; make that first call before any stream

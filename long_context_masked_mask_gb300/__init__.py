@@ -317,6 +317,24 @@ def lcattn_fwd_ws(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, mask: Devic
     return o, lse
 
 
+def _grad_buffers(q, k, v, o, d_o, dq, dk, dv):
+    """The gradient outputs of a backward call.  The library reads dO through
+    O's strides and writes dQ, dK, dV through Q's, K's and V's, so those
+    layouts must agree; missing gradients are allocated with their inputs'
+    strides (a view such as a slice of a fused QKV buffer included)."""
+    if d_o.shape != o.shape or d_o.stride() != o.stride():
+        raise ValueError("dO must have O's shape and strides")
+    dq = torch.empty_strided(q.shape, q.stride(), dtype=q.dtype, device=q.device) if dq is None else dq
+    dk = torch.empty_strided(k.shape, k.stride(), dtype=k.dtype, device=k.device) if dk is None else dk
+    dv = torch.empty_strided(v.shape, v.stride(), dtype=v.dtype, device=v.device) if dv is None else dv
+    for g, x in ((dq, q), (dk, k), (dv, v)):
+        if g.shape != x.shape or g.stride() != x.stride():
+            raise ValueError("gradients must have their inputs' shapes and strides")
+        if g.dtype != torch.bfloat16:
+            raise TypeError("gradients must be bf16")
+    return dq, dk, dv
+
+
 def lcattn_bwd_workspace_size(shape: lcattn_shape) -> int:
     return int(_lib.lcattn_bwd_workspace_size(ctypes.byref(shape)))
 
@@ -328,13 +346,7 @@ def lcattn_bwd(q, k, v, o, d_o, lse, mask: DeviceMask, tile_meta, scale: Optiona
     D = q.shape[3]
     if scale is None:
         scale = 1.0 / math.sqrt(D)
-    if d_o.stride() != o.stride():
-        raise ValueError("dO must have O's strides")
-    dq = torch.empty_like(q) if dq is None else dq
-    dk = torch.empty_like(k) if dk is None else dk
-    dv = torch.empty_like(v) if dv is None else dv
-    if dq.stride() != q.stride() or dk.stride() != k.stride() or dv.stride() != v.stride():
-        raise ValueError("gradients must have their inputs' strides")
+    dq, dk, dv = _grad_buffers(q, k, v, o, d_o, dq, dk, dv)
     shape = make_shape(q, k, v, o)
     ws_bytes = lcattn_bwd_workspace_size(shape)
     if workspace is None:
@@ -358,9 +370,7 @@ def lcattn_bwd_noalloc(q, k, v, o, d_o, lse, mask: DeviceMask, tile_meta, scale:
     place (this wrapper allocates them only when they are omitted)."""
     if scale is None:
         scale = 1.0 / math.sqrt(q.shape[3])
-    dq = torch.empty_like(q) if dq is None else dq
-    dk = torch.empty_like(k) if dk is None else dk
-    dv = torch.empty_like(v) if dv is None else dv
+    dq, dk, dv = _grad_buffers(q, k, v, o, d_o, dq, dk, dv)
     shape = make_shape(q, k, v, o)
     _check(_lib.lcattn_bwd_noalloc(ctypes.byref(shape), q.data_ptr(), k.data_ptr(), v.data_ptr(),
                                    o.data_ptr(), d_o.data_ptr(), lse.data_ptr(), tile_meta.data_ptr(),

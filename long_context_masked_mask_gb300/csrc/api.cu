@@ -35,6 +35,13 @@ int validate_shape(const lcattn_shape* s) {
   // The head and sequence strides must at least separate rows.
   for (auto x : st)
     if (x[2] < s->D || x[1] < s->D) return LCATTN_ERR_INVALID_ARG;
+  // With more than one batch entry, the batch stride must separate them too: a
+  // zero stride (a broadcast view) would make the TMA and plain-load paths
+  // disagree, and every output would have overlapping batch entries.  With
+  // B = 1 the batch stride is never applied.
+  if (s->B > 1)
+    for (auto x : st)
+      if (x[0] < s->D) return LCATTN_ERR_UNSUPPORTED;
   return LCATTN_OK;
 }
 

@@ -31,8 +31,8 @@ families and selection parameters.  Every function here is pinned; none is
 """
 from . import block_select_ref
 from .masks_ref import allowed, allowed_pairs
-from .attention_ref import (attention_fwd, attention_bwd, attention_fwd_rows,
+from .attention_ref import (attention_fwd, attention_bwd, attention_fwd_rows, attention_bwd_rows,
                             attention_bwd_sampled, classify_tiles, EMPTY, FULL, PARTIAL)
 
 __all__ = ["block_select_ref", "allowed", "allowed_pairs", "attention_fwd", "attention_bwd", "attention_fwd_rows",
-           "attention_bwd_sampled", "classify_tiles", "EMPTY", "FULL", "PARTIAL"]
+           "attention_bwd_rows", "attention_bwd_sampled", "classify_tiles", "EMPTY", "FULL", "PARTIAL"]

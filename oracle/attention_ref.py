@@ -112,6 +112,33 @@ def attention_bwd(q, k, v, do, spec, scale, chunk: int = 1024):
     return dQ, dK, dV, O, LSE
 
 
+def attention_bwd_rows(q, k, v, do, spec, scale, b: int, h: int, rows):
+    """The backward restricted to selected query rows of one (batch, query head h):
+
+    * O [R, D], LSE [R] and dQ [R, D] of those rows;
+    * dK, dV [Sk, D]: the terms of dK_j = s * sum_i dS_ij q_i and
+      dV_j = sum_i P_ij dO_i that come from those rows (for head h only).
+
+    The same formulas as :func:`attention_bwd`, applied to the rows given; over a
+    partition of every head's rows the dK/dV terms add up to the full result.
+    Used for bounded timing samples of long sequences.
+    """
+    N, Sk = q.shape[1], k.shape[1]
+    G = q.shape[2] // k.shape[2]
+    rows = np.asarray(rows, dtype=np.int64)
+    kk, vv = k[b, :, h // G], v[b, :, h // G]
+    M = allowed(spec, N, rows, head=h, Sk=Sk)
+    o, lse, P = _rows_fwd(q[b, rows, h], kk, vv, M, scale)
+    dOr = do[b, rows, h]
+    dV = P.T @ dOr
+    dP = dOr @ vv.T
+    Dr = (dOr * o).sum(axis=1)
+    dS = P * (dP - Dr[:, None])
+    dQ = scale * (dS @ kk)
+    dK = scale * (dS.T @ q[b, rows, h])
+    return dQ, dK, dV, o, lse
+
+
 def attention_bwd_sampled(q, k, v, do, spec, scale, b: int, g: int, q_rows, k_cols):
     """Gradients at sampled positions of one (batch, KV head g):
 

@@ -81,6 +81,40 @@ def test_shape_validation(field, value, status):
     assert lc.library().lcattn_tile_meta_size(ctypes.byref(s), ctypes.byref(_colbounds_desc())) == 0
 
 
+@pytest.mark.parametrize("name", ["q_stride", "k_stride", "v_stride", "o_stride"])
+def test_zero_batch_stride_refused_for_several_batch_entries(name):
+    """A broadcast view (batch stride 0, what tensor.expand gives) cannot serve
+    B > 1: outputs would overlap and the TMA and plain-load paths would read
+    different rows.  With B = 1 the batch stride is never applied."""
+    s = _shape(B=2)
+    getattr(s, name)[0] = 0
+    st, _ = _layout(s, _colbounds_desc())
+    assert st == lc.LCATTN_ERR_UNSUPPORTED
+    s = _shape(B=1)
+    getattr(s, name)[0] = 0
+    st, _ = _layout(s, _colbounds_desc())
+    assert st == lc.LCATTN_OK
+
+
+def test_backward_wrappers_check_gradient_layouts():
+    """Both backward wrappers (workspace and no-allocation) refuse a dO whose
+    strides differ from O's and gradients whose strides differ from their
+    inputs', before any call into the library (CPU tensors suffice)."""
+    import torch
+    fused = torch.zeros(1, 64, 3 * 4, 128, dtype=torch.bfloat16)
+    q, k, v = fused[:, :, 0:4], fused[:, :, 4:8], fused[:, :, 8:12]
+    o = torch.zeros(1, 64, 4, 128, dtype=torch.bfloat16)
+    d_o = torch.zeros(1, 64, 4, 128, dtype=torch.bfloat16)
+    for fn in (lc.lcattn_bwd, lc.lcattn_bwd_noalloc):
+        with pytest.raises(ValueError):
+            fn(q, k, v, o, d_o.transpose(1, 2).contiguous().transpose(1, 2), None, None, None)
+        with pytest.raises(ValueError):  # a dense dq for a strided q
+            fn(q, k, v, o, d_o, None, None, None, dq=torch.empty(1, 64, 4, 128, dtype=torch.bfloat16))
+    # Missing gradients take their inputs' strides.
+    dq, dk, dv = lc._grad_buffers(q, k, v, o, d_o, None, None, None)
+    assert dq.stride() == q.stride() and dk.stride() == k.stride() and dv.stride() == v.stride()
+
+
 def test_stride_and_descriptor_validation():
     s = _shape()
     s.q_stride[2] = 130  # not a multiple of 8 elements

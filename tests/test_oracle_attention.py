@@ -205,6 +205,39 @@ def test_sampled_paths_match_full():
     np.testing.assert_allclose(sdv, dV[0, cols, 1], atol=1e-12)
 
 
+@pytest.mark.parametrize("spec", [MaskSpec("CAUSAL_DOCUMENT", {"doc_lens": [11, 20, 9]}),
+                                  MaskSpec("UNIFORM_BLOCK", {"block": 8, "keep": block_keep(4, 5, 5, 0.5, 3)})],
+                         ids=lambda s: s.kind)
+def test_bwd_rows_vs_torch_with_do_zero_elsewhere(spec):
+    """attention_bwd_rows for rows R of head h equals torch's fp64 SDPA autograd
+    on a problem whose dO is zero outside (R, h): then only those rows reach the
+    loss, so torch's dK/dV are exactly their terms and its dQ rows are theirs."""
+    B, N, Hq, Hkv, D = 1, 40, 4, 2, 8
+    q, k, v, do = _rand(B, N, Hq, Hkv, D, seed=53)
+    s, h = 0.3, 3
+    rows = np.array([2, 9, 10, 25, 39])
+    do_sel = np.zeros_like(do)
+    do_sel[0, rows, h] = do[0, rows, h]
+    o, (qt, kt, vt), _ = _sdpa_torch(q, k, v, spec, s)
+    (o * torch.tensor(do_sel).permute(0, 2, 1, 3)).sum().backward()
+    dQ, dK, dV, O, LSE = oracle.attention_bwd_rows(q, k, v, do, spec, s, 0, h, rows)
+    np.testing.assert_allclose(O, o.detach().permute(0, 2, 1, 3).numpy()[0, rows, h], atol=1e-12)
+    np.testing.assert_allclose(dQ, qt.grad.permute(0, 2, 1, 3).numpy()[0, rows, h], atol=1e-12)
+    np.testing.assert_allclose(dK, kt.grad.permute(0, 2, 1, 3).numpy()[0, :, h // 2], atol=1e-12)
+    np.testing.assert_allclose(dV, vt.grad.permute(0, 2, 1, 3).numpy()[0, :, h // 2], atol=1e-12)
+    # Over a partition of every head's rows the terms add up to the full backward.
+    fdQ, fdK, fdV, _, fLSE = attention_bwd(q, k, v, do, spec, s)
+    np.testing.assert_allclose(LSE, fLSE[0, h, rows], atol=1e-12)
+    sk, sv = np.zeros_like(k[0]), np.zeros_like(v[0])
+    for hh in range(Hq):
+        for part in (np.arange(0, 17), np.arange(17, N)):
+            _, dk_, dv_, _, _ = oracle.attention_bwd_rows(q, k, v, do, spec, s, 0, hh, part)
+            sk[:, hh // 2] += dk_
+            sv[:, hh // 2] += dv_
+    np.testing.assert_allclose(sk, fdK[0], atol=1e-11)
+    np.testing.assert_allclose(sv, fdV[0], atol=1e-11)
+
+
 def test_gradient_sum_identities():
     """sum_j dK_j = 0 and sum_j dV_j = sum over non-empty rows of dO (per KV head).
 

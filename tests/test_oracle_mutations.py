@@ -122,6 +122,18 @@ def torch_pin_holds(ar):
             return False
         if not np.array_equal(np.isfinite(LSE[0]), has):
             return False
+        # Row subsets: dQ and O rows as torch's, and the dK/dV terms of a
+        # partition of every head's rows summing to torch's dK/dV.
+        rK, rV = np.zeros_like(dK[0]), np.zeros_like(dV[0])
+        for h in range(_HQ):
+            for part in (np.arange(0, 6), np.arange(6, _N)):
+                pQ, pK, pV, pO, _ = ar.attention_bwd_rows(q, k, v, do, spec, scale, 0, h, part)
+                if not (close(pQ, dQ[0, part, h]) and close(pO, O[0, part, h])):
+                    return False
+                rK[:, h // 2] += pK
+                rV[:, h // 2] += pV
+        if not (close(rK, dK[0]) and close(rV, dV[0])):
+            return False
         cols, rows = np.array([0, 4, 7, 12]), np.array([1, 5, 12])
         for g in range(_HKV):
             sQ, sK, sV = ar.attention_bwd_sampled(q, k, v, do, spec, scale, 0, g, rows, cols)
@@ -177,7 +189,11 @@ ATTN_MUTANTS = [
     ("sampled path misses rows", "need = allowed(spec, N, rows, head=h, cols=k_cols, Sk=Sk).any(axis=1)",
      "need = allowed(spec, N, rows, head=h, cols=k_cols, Sk=Sk).all(axis=1)", 0),
     ("sampled dK without scale", "dK += scale * (dSc.T @ q[b, rr, h])", "dK += (dSc.T @ q[b, rr, h])", 0),
-    ("sampled dQ drops D", "dS = P * (dP - Dr[:, None])", "dS = P * dP", 1),
+    ("row-subset dS drops D", "dS = P * (dP - Dr[:, None])", "dS = P * dP", 1),
+    ("row-subset dK without scale", "dK = scale * (dS.T @ q[b, rows, h])", "dK = (dS.T @ q[b, rows, h])", 0),
+    ("row-subset dV from Q", "dV = P.T @ dOr", "dV = P.T @ q[b, rows, h]", 0),
+    ("row-subset GQA head map", "kk, vv = k[b, :, h // G], v[b, :, h // G]", "kk, vv = k[b, :, h % 2], v[b, :, h % 2]", 0),
+    ("sampled dQ drops D", "dS = P * (dP - Dr[:, None])", "dS = P * dP", 2),
 ]
 
 
