@@ -281,7 +281,7 @@ int lcattn_fwd_ws(const lcattn_shape* shape, const void* q, const void* k, const
  * do not fit in tensor memory beside S and dP) and its workspace size is 0.
  *
  * Workspace (device bytes) lcattn_bwd needs: D = rowsum(dO * O) fp32
- * [B][Hq][Sq], the fp32 dQ accumulator [B][Sq][Hq][D] and, when the dK/dV
+ * [B][Hq][Sq], the fp32 dQ accumulator [B][Hq][Sq][D] (head-major) and, when the dK/dV
  * work units (key tiles x KV heads x batch) are too few to fill the GPU in
  * several waves -- under 1216, and the GQA group splits evenly -- fp32 dK/dV
  * partials [2 or 4][2][B][Sk][Hkv][D]: each unit is split over 2 or 4
@@ -342,6 +342,78 @@ int lcattn_bwd_noalloc(const lcattn_shape* shape, const void* q, const void* k, 
                        const void* o, const void* d_o, const float* lse, const void* tile_meta,
                        const lcattn_mask_desc* mask, float scale, void* dq, void* dk, void* dv,
                        lcattn_stream_t stream);
+
+/* ---- context parallelism by Ring P2P: the per-device building blocks -----
+ * The pages' distributed half (xllm-io blog review, section "分布式注意力机制",
+ * Ring P2P: several rounds of point-to-point exchange, overlapped with the
+ * computation; the qualitative results are in section "分布式性能") splits the
+ * sequence over devices.  Device r holds query shard r and K/V shard r; in
+ * round t it computes its query shard against the K/V shard it holds, hands
+ * that shard on to the next device, and merges the round's partial result
+ * into its running one by log-sum-exp.  The backward walks the same ring:
+ * each round adds the query shard's dQ terms locally and the K/V shard's dK/dV
+ * terms into accumulators that travel with the shard back to its owner.
+ * The calls below are what one device runs in one round; moving the shards
+ * between devices is the caller's (any point-to-point transport into local
+ * buffers).
+ *
+ * Shard descriptor: the mask of query rows [q0, q0 + Sq_s) against keys
+ * [k0, k0 + Sk_s) of a global Sq x Sk problem (per batch entry), as a
+ * descriptor of the Sq_s x Sk_s problem that lcattn_mask_compile and the
+ * attention calls take.
+ *   Column bounds (global->kind 1): col_bounds_out (device int32
+ *   [B][Sk_s][4], 16-byte aligned) = clamp(col_bounds[b][k0 + j] - q0, 0,
+ *   Sq_s) componentwise; if row_bounds_out is not NULL (global->row_bounds must
+ *   then be given), row_bounds_out [B][Sq_s][4] = clamp(row_bounds[b][q0 + i] -
+ *   k0, 0, Sk_s).  q_offs_out / k_offs_out are unused.
+ *   Block maps (kind 2): q_offs_out [nQb+1] = clamp(q_block_offs - q0, 0, Sq_s)
+ *   and k_offs_out [nKb+1] likewise; the map itself is reused as it is (same
+ *   [B][Hq][nQb][nKb] array), the blocks outside the shard becoming empty.  The
+ *   shard's descriptor must still have nQb <= Sq_s and nKb <= Sk_s.
+ * One small kernel per output array on `stream`; LCATTN_ERR_INVALID_ARG for
+ * shards outside the global problem or missing buffers.                     */
+int lcattn_mask_shard(const lcattn_mask_desc* global, int64_t B, int64_t Sq, int64_t Sk,
+                      int64_t q0, int64_t Sq_s, int64_t k0, int64_t Sk_s,
+                      int32_t* col_bounds_out, int32_t* row_bounds_out,
+                      int32_t* q_offs_out, int32_t* k_offs_out, lcattn_stream_t stream);
+
+/* Merge of one round's partial forward result into the running result of a
+ * query shard.  shape: the shard problem (B, Sq = query rows, Hq, D; its
+ * o_stride is the layout of o_part and o_out).  o_acc (device fp32
+ * [B][Sq][Hq][D], contiguous) and lse_acc ([B][Hq][Sq]) are the running
+ * result; o_part (bf16) and lse_part ([B][Hq][Sq]) are the round's, from
+ * lcattn_fwd on the shard pair.  With first = 1 the running result is set to
+ * the part; otherwise, per row, with m = max(lse_acc, lse_part):
+ *   o_acc <- (exp(lse_acc - m) o_acc + exp(lse_part - m) o_part) / (sum of the two weights),
+ *   lse_acc <- m + ln(sum of the two weights),
+ * and a row no round has allowed so far stays O = 0, LSE = -inf.  If o_out is
+ * not NULL the merged O is also written there as bf16 (pass it in the last
+ * round), with element strides o_out_stride (batch, sequence, head; NULL =
+ * the shape's o_stride).  One kernel on `stream`.                          */
+int lcattn_lse_merge(const lcattn_shape* shape, float* o_acc, float* lse_acc, const void* o_part,
+                     const float* lse_part, void* o_out, const int64_t* o_out_stride, int first,
+                     lcattn_stream_t stream);
+
+/* Shard backward: lcattn_bwd's gradients of one shard pair, added into fp32
+ * accumulators instead of written as bf16.  o and lse must be the query
+ * shard's final (merged) O and LSE, so that P and D = rowsum(dO * O) are the
+ * global ones.  dq_acc (device fp32 [B][Sq][Hq][D], contiguous) receives the
+ * dQ terms of this key shard; dk_acc / dv_acc (fp32 [B][Sk][Hkv][D],
+ * contiguous) receive the K/V shard's dK / dV terms from this query shard.
+ * Nothing is zeroed: the caller clears the accumulators once.  The workspace
+ * holds D only (lcattn_bwd_accum_workspace_size bytes).  Two kernels on
+ * `stream` (the D pre-pass, then dK/dV with the dQ terms); head dim 64 or 128. */
+size_t lcattn_bwd_accum_workspace_size(const lcattn_shape* shape);
+int lcattn_bwd_accum(const lcattn_shape* shape, const void* q, const void* k, const void* v,
+                     const void* o, const void* d_o, const float* lse, const void* tile_meta,
+                     const lcattn_mask_desc* mask, float scale, float* dq_acc, float* dk_acc,
+                     float* dv_acc, void* workspace, size_t workspace_bytes, lcattn_stream_t stream);
+
+/* fp32 [B][S][H][D] (device, contiguous) -> bf16 with element strides
+ * dst_stride = (batch, sequence, head), e.g. the accumulated gradients of the
+ * ring backward into dQ, dK, dV.  D is 64, 128 or 256.                      */
+int lcattn_f32_to_bf16(const float* src, void* dst, int64_t B, int64_t S, int64_t H, int64_t D,
+                       const int64_t dst_stride[3], lcattn_stream_t stream);
 
 /* Synchronises `stream`, then returns the first nonzero device status word of
  * `tile_meta` (LCATTN_ERR_DEVICE_*), or LCATTN_OK.  Clears nothing.          */

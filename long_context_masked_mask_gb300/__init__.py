@@ -57,6 +57,8 @@ EXPORTED = (
     "lcattn_status_string", "lcattn_version", "lcattn_bwd_noalloc", "lcattn_selftest_wait_timeout",
     "lcattn_block_select_workspace_size", "lcattn_block_select", "lcattn_block_select_stage",
     "lcattn_fwd_workspace_size", "lcattn_fwd_ws",
+    "lcattn_mask_shard", "lcattn_lse_merge", "lcattn_bwd_accum_workspace_size", "lcattn_bwd_accum",
+    "lcattn_f32_to_bf16",
 )
 
 
@@ -124,6 +126,12 @@ def _load():
         "lcattn_block_select": (ctypes.c_int, [S, P, P, SD, ctypes.c_float, P, P, P, ctypes.c_size_t, P]),
         "lcattn_block_select_stage": (ctypes.c_int, [ctypes.c_int, S, P, P, SD, ctypes.c_float, P, P, P,
                                                      ctypes.c_size_t, P]),
+        "lcattn_mask_shard": (ctypes.c_int, [M] + [ctypes.c_int64] * 7 + [P, P, P, P, P]),
+        "lcattn_lse_merge": (ctypes.c_int, [S, P, P, P, P, P, ctypes.POINTER(ctypes.c_int64), ctypes.c_int, P]),
+        "lcattn_bwd_accum_workspace_size": (ctypes.c_size_t, [S]),
+        "lcattn_bwd_accum": (ctypes.c_int, [S, P, P, P, P, P, P, P, M, ctypes.c_float, P, P, P, P,
+                                            ctypes.c_size_t, P]),
+        "lcattn_f32_to_bf16": (ctypes.c_int, [P, P] + [ctypes.c_int64] * 4 + [ctypes.POINTER(ctypes.c_int64), P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -377,6 +385,91 @@ def lcattn_bwd_noalloc(q, k, v, o, d_o, lse, mask: DeviceMask, tile_meta, scale:
                                    ctypes.byref(mask.desc), float(scale), dq.data_ptr(), dk.data_ptr(),
                                    dv.data_ptr(), _stream_ptr(stream)), "lcattn_bwd_noalloc")
     return dq, dk, dv
+
+
+def lcattn_mask_shard(mask: "DeviceMask", B: int, Sq: int, Sk: int, q0: int, Sq_s: int, k0: int,
+                      Sk_s: int, stream=None) -> "DeviceMask":
+    """Descriptor of query rows [q0, q0+Sq_s) against keys [k0, k0+Sk_s) of the
+    global mask ``mask`` (lcattn_mask_shard): a :class:`DeviceMask` of the
+    Sq_s x Sk_s problem, holding its own device buffers (a block map's map
+    array is shared with ``mask``)."""
+    dev = (mask.col_bounds if mask.desc.kind == LCATTN_MASK_COLBOUNDS else mask.block_map).device
+    out = DeviceMask.__new__(DeviceMask)
+    out.spec, out.N, out.Sk, out.Hq, out.B = None, Sq_s, Sk_s, mask.Hq, B
+    out.pairs_per_batch = None
+    out.desc = lcattn_mask_desc()
+    out.desc.kind = mask.desc.kind
+    col = row = qo = ko = None
+    if mask.desc.kind == LCATTN_MASK_COLBOUNDS:
+        out.col_bounds = col = torch.empty(B, Sk_s, 4, dtype=torch.int32, device=dev)
+        out.desc.col_bounds = col.data_ptr()
+        if mask.desc.row_bounds:
+            out.row_bounds = row = torch.empty(B, Sq_s, 4, dtype=torch.int32, device=dev)
+            out.desc.row_bounds = row.data_ptr()
+    else:
+        out.block_map = mask.block_map
+        out.q_offs = qo = torch.empty(mask.desc.nQb + 1, dtype=torch.int32, device=dev)
+        out.k_offs = ko = torch.empty(mask.desc.nKb + 1, dtype=torch.int32, device=dev)
+        out.desc.block_map = mask.desc.block_map
+        out.desc.q_block_offs, out.desc.k_block_offs = qo.data_ptr(), ko.data_ptr()
+        out.desc.nQb, out.desc.nKb = mask.desc.nQb, mask.desc.nKb
+    ptr = lambda t: t.data_ptr() if t is not None else None
+    _check(_lib.lcattn_mask_shard(ctypes.byref(mask.desc), B, Sq, Sk, q0, Sq_s, k0, Sk_s, ptr(col), ptr(row),
+                                  ptr(qo), ptr(ko), _stream_ptr(stream)), "lcattn_mask_shard")
+    return out
+
+
+def lcattn_lse_merge(o_acc: torch.Tensor, lse_acc: torch.Tensor, o_part: torch.Tensor, lse_part: torch.Tensor,
+                     o_out: Optional[torch.Tensor] = None, first: bool = False, stream=None) -> None:
+    """Merges a shard pair's (O, LSE) into the running fp32 (o_acc, lse_acc) of a
+    query shard by log-sum-exp (lcattn_lse_merge); writes bf16 ``o_out`` too
+    when given.  o_acc [B, Sq, Hq, D] fp32 contiguous, lse [B, Hq, Sq] fp32."""
+    if o_acc.dtype != torch.float32 or not o_acc.is_contiguous():
+        raise ValueError("o_acc must be a contiguous fp32 [B, Sq, Hq, D] tensor")
+    if o_out is not None and (o_out.shape != o_part.shape or o_out.dtype != torch.bfloat16):
+        raise ValueError("o_out must be bf16 with o_part's shape")
+    for t in (lse_acc, lse_part):
+        if t.dtype != torch.float32 or not t.is_contiguous() or t.shape != (o_acc.shape[0], o_acc.shape[2], o_acc.shape[1]):
+            raise ValueError("LSE tensors must be contiguous fp32 [B, Hq, Sq]")
+    shape = make_shape(o_part, o_part, o_part, o_part)
+    out_st = (ctypes.c_int64 * 3)(*_bshd_strides(o_out)) if o_out is not None else None
+    _check(_lib.lcattn_lse_merge(ctypes.byref(shape), o_acc.data_ptr(), lse_acc.data_ptr(), o_part.data_ptr(),
+                                 lse_part.data_ptr(), o_out.data_ptr() if o_out is not None else None, out_st,
+                                 1 if first else 0, _stream_ptr(stream)), "lcattn_lse_merge")
+
+
+def lcattn_bwd_accum(q, k, v, o, d_o, lse, mask: "DeviceMask", tile_meta, dq_acc, dk_acc, dv_acc,
+                     scale: Optional[float] = None, workspace=None, stream=None) -> None:
+    """Shard backward (lcattn_bwd_accum): adds this shard pair's dQ terms into
+    ``dq_acc`` [B, Sq, Hq, D] and its dK / dV terms into ``dk_acc`` / ``dv_acc``
+    [B, Sk, Hkv, D] (fp32, contiguous).  ``o`` and ``lse`` are the query
+    shard's final (merged) output and LSE."""
+    if scale is None:
+        scale = 1.0 / math.sqrt(q.shape[3])
+    if d_o.shape != o.shape or d_o.stride() != o.stride():
+        raise ValueError("dO must have O's shape and strides")
+    for acc, x in ((dq_acc, q), (dk_acc, k), (dv_acc, v)):
+        if acc.dtype != torch.float32 or not acc.is_contiguous() or acc.shape != x.shape:
+            raise ValueError("accumulators must be contiguous fp32 tensors shaped like q, k, v")
+    shape = make_shape(q, k, v, o)
+    nbytes = int(_lib.lcattn_bwd_accum_workspace_size(ctypes.byref(shape)))
+    if workspace is None:
+        workspace = torch.empty(max(16, nbytes), dtype=torch.uint8, device=q.device)
+    _check(_lib.lcattn_bwd_accum(ctypes.byref(shape), q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                 d_o.data_ptr(), lse.data_ptr(), tile_meta.data_ptr(), ctypes.byref(mask.desc),
+                                 float(scale), dq_acc.data_ptr(), dk_acc.data_ptr(), dv_acc.data_ptr(),
+                                 workspace.data_ptr(), workspace.numel(), _stream_ptr(stream)), "lcattn_bwd_accum")
+
+
+def lcattn_f32_to_bf16(src: torch.Tensor, dst: torch.Tensor, stream=None) -> torch.Tensor:
+    """Contiguous fp32 [B, S, H, D] -> bf16 ``dst`` of the same shape (any BSHD strides)."""
+    if src.dtype != torch.float32 or not src.is_contiguous() or dst.dtype != torch.bfloat16 or src.shape != dst.shape:
+        raise ValueError("src must be contiguous fp32 and dst bf16 of the same shape")
+    B, S, H, D = src.shape
+    st = (ctypes.c_int64 * 3)(*_bshd_strides(dst))
+    _check(_lib.lcattn_f32_to_bf16(src.data_ptr(), dst.data_ptr(), B, S, H, D, st, _stream_ptr(stream)),
+           "lcattn_f32_to_bf16")
+    return dst
 
 
 def select_desc(rule: str, q_offs: torch.Tensor, k_offs: torch.Tensor, top_k: int = 0,

@@ -176,7 +176,7 @@ int bwd_parts(const lcattn_shape* s) {
   return 1;
 }
 
-// Workspace: D [B][Hq][Sq], the fp32 dQ accumulator [B][Sq][Hq][128] and, for
+// Workspace: D [B][Hq][Sq], the fp32 dQ accumulator [B][Hq][Sq][D] and, for
 // split units, the fp32 dK/dV partials [parts][2][B][Sk][Hkv][128].
 int64_t bwd_ws_bytes(const lcattn_shape* s, int parts) {
   const int64_t d_bytes = align_up(4 * s->B * s->Hq * s->Sq, 256);
@@ -353,16 +353,29 @@ size_t lcattn_bwd_workspace_size(const lcattn_shape* shape) {
 
 namespace {
 
+// Caller-owned fp32 accumulators of the accumulate mode (all null otherwise).
+struct AccumOut {
+  float* dq = nullptr;
+  float* dk = nullptr;
+  float* dv = nullptr;
+  bool on() const { return dq != nullptr; }
+};
+
 // Stages: bit 0 = pre-pass, bit 1 = dK/dV, bit 2 = dQ conversion.
 int bwd_run(unsigned stages, const lcattn_shape* shape, const void* q, const void* k,
             const void* v, const void* o, const void* d_o, const float* lse,
             const void* tile_meta, const lcattn_mask_desc* mask, float scale, void* dq, void* dk,
             void* dv, void* workspace, size_t workspace_bytes, lcattn_stream_t stream,
-            bool allow_split = true) {
+            bool allow_split = true, AccumOut acc = AccumOut()) {
   lcattn_tile_meta_layout L;
   int st = layout_of(shape, mask, &L);
   if (st) return st;
   if (shape->D > 128) return LCATTN_ERR_UNSUPPORTED;  // head dim 256: forward only
+  if (acc.on()) {
+    if (!acc.dk || !acc.dv) return LCATTN_ERR_INVALID_ARG;
+    // The outputs are the accumulators; the bf16 pointers are not used.
+    dq = acc.dq; dk = acc.dk; dv = acc.dv;
+  }
   if (!q || !k || !v || !o || !d_o || !lse || !tile_meta || !dq || !dk || !dv || !workspace)
     return LCATTN_ERR_INVALID_ARG;
   const void* ptrs[] = {q, k, v, o, d_o, dq, dk, dv, workspace, tile_meta};
@@ -370,7 +383,11 @@ int bwd_run(unsigned stages, const lcattn_shape* shape, const void* q, const voi
     if (!aligned16(p)) return LCATTN_ERR_UNSUPPORTED;
   if (!(scale > 0.f) || !(scale < 1e30f)) return LCATTN_ERR_INVALID_ARG;
   const int parts = allow_split ? bwd_parts(shape) : 1;
-  if ((int64_t)workspace_bytes < bwd_ws_bytes(shape, parts)) return LCATTN_ERR_WORKSPACE;
+  // Accumulate mode needs only D: dQ goes to the caller's accumulator and the
+  // split units reduce-add their dK/dV shares directly.
+  const int64_t need = acc.on() ? align_up(4 * shape->B * shape->Hq * shape->Sq, 256)
+                                : bwd_ws_bytes(shape, parts);
+  if ((int64_t)workspace_bytes < need) return LCATTN_ERR_WORKSPACE;
   CUtensorMap tq, tk, tv, tdo;
   if ((st = encode_bshd(&tq, q, shape->B, shape->Sq, shape->Hq, shape->D, shape->q_stride))) return st;
   if ((st = encode_bshd(&tk, k, shape->B, shape->Sk, shape->Hkv, shape->D, shape->k_stride))) return st;
@@ -391,6 +408,24 @@ int bwd_run(unsigned stages, const lcattn_shape* shape, const void* q, const voi
   a.dq_acc = reinterpret_cast<float*>(ws + align_up(4 * shape->B * shape->Hq * shape->Sq, 256));
   a.parts = parts;
   a.dkv_part = reinterpret_cast<float*>(ws + bwd_ws_bytes(shape, 1));
+  // The workspace accumulator is head-major, [B][Hq][Sq][D]: the rows one
+  // head's dK/dV units add into are contiguous, so the units in flight (which
+  // mostly work on the same head) keep a compact set of lines in L2.  The
+  // caller's accumulator of the accumulate mode is [B][Sq][Hq][D].
+  a.dqa_sb = shape->Hq * shape->Sq * shape->D;
+  a.dqa_sh = shape->Sq * shape->D;
+  a.dqa_ss = shape->D;
+  a.accum = acc.on() ? 1 : 0;
+  a.dk_acc = acc.dk;
+  a.dv_acc = acc.dv;
+  if (acc.on()) {
+    a.dq_acc = acc.dq;
+    a.dqa_sb = shape->Sq * shape->Hq * shape->D;
+    a.dqa_ss = shape->Hq * shape->D;
+    a.dqa_sh = shape->D;
+    a.dkv_part = nullptr;
+    stages &= 3u;  // no bf16 conversion: the accumulators are the outputs
+  }
   a.dq = dq;
   a.q_sb = shape->q_stride[0]; a.q_ss = shape->q_stride[1]; a.q_sh = shape->q_stride[2];
   a.dk = dk;
@@ -425,6 +460,109 @@ int lcattn_bwd_stage(int stage, const lcattn_shape* shape, const void* q, const 
   if (stage < 1 || stage > 3) return LCATTN_ERR_INVALID_ARG;
   return bwd_run(1u << (stage - 1), shape, q, k, v, o, d_o, lse, tile_meta, mask, scale, dq, dk,
                  dv, workspace, workspace_bytes, stream);
+}
+
+size_t lcattn_bwd_accum_workspace_size(const lcattn_shape* shape) {
+  if (validate_shape(shape) != LCATTN_OK || shape->D > 128) return 0;
+  return (size_t)align_up(4 * shape->B * shape->Hq * shape->Sq, 256);
+}
+
+int lcattn_bwd_accum(const lcattn_shape* shape, const void* q, const void* k, const void* v,
+                     const void* o, const void* d_o, const float* lse, const void* tile_meta,
+                     const lcattn_mask_desc* mask, float scale, float* dq_acc, float* dk_acc,
+                     float* dv_acc, void* workspace, size_t workspace_bytes, lcattn_stream_t stream) {
+  if (!dq_acc || !dk_acc || !dv_acc) return LCATTN_ERR_INVALID_ARG;
+  AccumOut acc;
+  acc.dq = dq_acc; acc.dk = dk_acc; acc.dv = dv_acc;
+  return bwd_run(3u, shape, q, k, v, o, d_o, lse, tile_meta, mask, scale, nullptr, nullptr, nullptr,
+                 workspace, workspace_bytes, stream, /*allow_split=*/true, acc);
+}
+
+int lcattn_mask_shard(const lcattn_mask_desc* global, int64_t B, int64_t Sq, int64_t Sk, int64_t q0,
+                      int64_t Sq_s, int64_t k0, int64_t Sk_s, int32_t* col_bounds_out,
+                      int32_t* row_bounds_out, int32_t* q_offs_out, int32_t* k_offs_out,
+                      lcattn_stream_t stream) {
+  if (!global || B < 1 || B > 65535 || Sq < 1 || Sk < 1 || Sq > kMaxSeq || Sk > kMaxSeq)
+    return LCATTN_ERR_INVALID_ARG;
+  if (q0 < 0 || Sq_s < 1 || q0 + Sq_s > Sq || k0 < 0 || Sk_s < 1 || k0 + Sk_s > Sk)
+    return LCATTN_ERR_INVALID_ARG;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (global->kind == LCATTN_MASK_COLBOUNDS) {
+    if (!global->col_bounds || !aligned16(global->col_bounds) || !col_bounds_out ||
+        !aligned16(col_bounds_out))
+      return LCATTN_ERR_INVALID_ARG;
+    if (row_bounds_out && (!global->row_bounds || !aligned16(global->row_bounds) ||
+                           !aligned16(row_bounds_out)))
+      return LCATTN_ERR_INVALID_ARG;
+    ShardBoundsArgs c;
+    c.in = reinterpret_cast<const int4*>(global->col_bounds);
+    c.out = reinterpret_cast<int4*>(col_bounds_out);
+    c.S_in = Sk; c.start = k0; c.n = Sk_s; c.B = (int)B; c.shift = (int)q0; c.limit = (int)Sq_s;
+    cudaError_t e = launch_shard_bounds(c, s);
+    if (e == cudaSuccess && row_bounds_out) {
+      ShardBoundsArgs r;
+      r.in = reinterpret_cast<const int4*>(global->row_bounds);
+      r.out = reinterpret_cast<int4*>(row_bounds_out);
+      r.S_in = Sq; r.start = q0; r.n = Sq_s; r.B = (int)B; r.shift = (int)k0; r.limit = (int)Sk_s;
+      e = launch_shard_bounds(r, s);
+    }
+    return cuda_status(e);
+  }
+  if (global->kind == LCATTN_MASK_BLOCKMAP) {
+    if (!global->q_block_offs || !global->k_block_offs || !q_offs_out || !k_offs_out ||
+        global->nQb < 1 || global->nKb < 1)
+      return LCATTN_ERR_INVALID_ARG;
+    cudaError_t e = launch_shard_offsets(global->q_block_offs, q_offs_out, global->nQb, (int)q0,
+                                         (int)Sq_s, s);
+    if (e == cudaSuccess)
+      e = launch_shard_offsets(global->k_block_offs, k_offs_out, global->nKb, (int)k0, (int)Sk_s, s);
+    return cuda_status(e);
+  }
+  return LCATTN_ERR_INVALID_ARG;
+}
+
+int lcattn_lse_merge(const lcattn_shape* shape, float* o_acc, float* lse_acc, const void* o_part,
+                     const float* lse_part, void* o_out, const int64_t* o_out_stride, int first,
+                     lcattn_stream_t stream) {
+  int st = validate_shape(shape);
+  if (st) return st;
+  if (!o_acc || !lse_acc || !o_part || !lse_part) return LCATTN_ERR_INVALID_ARG;
+  if (first != 0 && first != 1) return LCATTN_ERR_INVALID_ARG;
+  if (!aligned16(o_acc) || !aligned16(o_part) || (o_out && !aligned16(o_out)) ||
+      (reinterpret_cast<uintptr_t>(lse_acc) & 3u) || (reinterpret_cast<uintptr_t>(lse_part) & 3u))
+    return LCATTN_ERR_UNSUPPORTED;
+  MergeArgs a;
+  a.pr = problem_of(shape);
+  a.o_acc = o_acc; a.lse_acc = lse_acc;
+  a.o_part = o_part;
+  a.p_sb = shape->o_stride[0]; a.p_ss = shape->o_stride[1]; a.p_sh = shape->o_stride[2];
+  a.lse_part = lse_part;
+  a.o_out = o_out;
+  const int64_t* os = o_out_stride ? o_out_stride : shape->o_stride;
+  if (o_out) {
+    for (int i = 0; i < 3; ++i) {
+      if (os[i] < 0) return LCATTN_ERR_INVALID_ARG;
+      if (os[i] % 8 != 0) return LCATTN_ERR_UNSUPPORTED;
+    }
+    if (os[2] < shape->D || os[1] < shape->D || (shape->B > 1 && os[0] < shape->D)) return LCATTN_ERR_INVALID_ARG;
+  }
+  a.o_sb = os[0]; a.o_ss = os[1]; a.o_sh = os[2];
+  a.first = first;
+  return cuda_status(launch_lse_merge(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int lcattn_f32_to_bf16(const float* src, void* dst, int64_t B, int64_t S, int64_t H, int64_t D,
+                       const int64_t dst_stride[3], lcattn_stream_t stream) {
+  if (!src || !dst || !dst_stride || B < 1 || S < 1 || H < 1) return LCATTN_ERR_INVALID_ARG;
+  if (D != 64 && D != 128 && D != 256) return LCATTN_ERR_UNSUPPORTED;
+  for (int i = 0; i < 3; ++i) {
+    if (dst_stride[i] < 0) return LCATTN_ERR_INVALID_ARG;
+    if (dst_stride[i] % 8 != 0) return LCATTN_ERR_UNSUPPORTED;
+  }
+  if (dst_stride[2] < D || dst_stride[1] < D || (B > 1 && dst_stride[0] < D)) return LCATTN_ERR_INVALID_ARG;
+  if (!aligned16(src) || !aligned16(dst)) return LCATTN_ERR_UNSUPPORTED;
+  return cuda_status(launch_f32_to_bf16(src, dst, B, S, H, D, dst_stride[0], dst_stride[1], dst_stride[2],
+                                        reinterpret_cast<cudaStream_t>(stream)));
 }
 
 }  // extern "C"

@@ -90,7 +90,8 @@ __global__ void prepass_kernel(BwdArgs a) {
     #pragma unroll
     for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
     if (lane == 0) a.dvec[((int64_t)b * a.pr.Hq + h) * a.pr.Sq + i] = acc;
-    float* dq = a.dq_acc + (((int64_t)b * a.pr.Sq + i) * a.pr.Hq + h) * D + lane * kPer;
+    if (a.accum) continue;  // the caller's accumulator keeps its contents
+    float* dq = a.dq_acc + (int64_t)b * a.dqa_sb + (int64_t)i * a.dqa_ss + (int64_t)h * a.dqa_sh + lane * kPer;
     #pragma unroll
     for (int k = 0; k < kPer; k += 2) *reinterpret_cast<float2*>(dq + k) = make_float2(0.f, 0.f);
   }
@@ -109,7 +110,8 @@ __global__ void dq_convert_kernel(BwdArgs a) {
     const int h = (int)(row % a.pr.Hq);
     const int i = (int)((row / a.pr.Hq) % a.pr.Sq);
     const int b = (int)(row / ((int64_t)a.pr.Hq * a.pr.Sq));
-    const float4* src = reinterpret_cast<const float4*>(a.dq_acc + row * D + c * 8);
+    const float4* src = reinterpret_cast<const float4*>(a.dq_acc + (int64_t)b * a.dqa_sb + (int64_t)i * a.dqa_ss +
+                                                        (int64_t)h * a.dqa_sh + c * 8);
     const float4 x = src[0], y = src[1];
     uint4 out;
     out.x = pack_bf16x2(x.x, x.y);
@@ -454,7 +456,7 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
     // ------------------------------------------------------------ dQ drain
     const int r = 32 * (warp & 3) + lane;  // head-dim row of dQ^T (TMEM lane)
     const uint32_t tQ = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16) + 128;
-    const int64_t dq_row_stride = (int64_t)pr.Hq * D;
+    const int64_t dq_row_stride = a.dqa_ss;
     ItemIter it;
     it.init(a.meta, b, kt, pr.G, g, h_lo, h_hi);
     for (int i = 0; it.valid(); it.next(), ++i) {
@@ -477,7 +479,7 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
       mbar_arrive(&sm.dq_free);  // columns [128, 256) may take dP^T(i+1) now
       const int q0 = qt * kBM;
       const int nq = min(kBM, pr.Sq - q0);
-      float* dst = a.dq_acc + (((int64_t)b * pr.Sq + q0) * pr.Hq + h) * D + r;
+      float* dst = a.dq_acc + (int64_t)b * a.dqa_sb + (int64_t)q0 * a.dqa_ss + (int64_t)h * a.dqa_sh + r;
       if (nq == kBM) {
         #pragma unroll
         for (int c = 0; c < 128; ++c) atomicAdd(dst + c * dq_row_stride, __uint_as_float(d[c]));
@@ -640,7 +642,9 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
     }
     // ---- dV (warpgroup 0) / dK (warpgroup 1) out, bf16; zero when no query
     // tile touched this key tile.  dV accumulated P' = scale * P: undo it.
-    if (ok) {
+    // In accumulate mode the fp32 values are reduce-added into the caller's
+    // accumulators instead (nothing to add when no query tile touched the tile).
+    if (ok && !(a.accum && i == 0)) {
       bool have = i > 0;
       if (have) {
         have = mbar_wait(&sm.done, 0, abort_flag, gstatus, TO);
@@ -666,7 +670,13 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
           #pragma unroll
           for (int k = 0; k < 32; ++k) xr[k] = 0u;
         }
-        if (key_ok && parts > 1) {
+        if (key_ok && a.accum) {
+          float* adst = (x == 0 ? a.dv_acc : a.dk_acc) + (((int64_t)b * pr.Sk + key) * pr.Hkv + g) * D + c * 32;
+          #pragma unroll
+          for (int u = 0; u < 8; ++u)
+            red_add_v4(adst + 4 * u, __uint_as_float(xr[4 * u]) * mul, __uint_as_float(xr[4 * u + 1]) * mul,
+                       __uint_as_float(xr[4 * u + 2]) * mul, __uint_as_float(xr[4 * u + 3]) * mul);
+        } else if (key_ok && parts > 1) {
           float4* p4 = reinterpret_cast<float4*>(pdst + c * 32);
           #pragma unroll
           for (int u = 0; u < 8; ++u)
@@ -711,7 +721,7 @@ cudaError_t launch_dkdv_d(const CUtensorMap& tq, const CUtensorMap& tk, const CU
   dim3 grid(a.meta.nKt * a.parts, a.pr.Hkv, a.pr.B);
   dkdv_kernel<D><<<grid, kThreadsDkdv, smem, st>>>(tq, tk, tv, tdo, ka);
   cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess || a.parts == 1) return e;
+  if (e != cudaSuccess || a.parts == 1 || a.accum) return e;
   int dev = 0, nsm = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);

@@ -92,9 +92,16 @@ struct BwdArgs {
   int64_t o_sb, o_ss, o_sh;
   const float* lse;
   float* dvec;   // D [B][Hq][Sq]
-  float* dq_acc; // [B][Sq][Hq][128] fp32
+  float* dq_acc; // fp32 dQ accumulator, element strides below (head dim contiguous)
+  int64_t dqa_sb, dqa_ss, dqa_sh;
   int parts;       // dK/dV units split over this many shares of the GQA group's heads (1: none)
   float* dkv_part; // parts > 1: fp32 partials [parts][dV, dK][B][Sk][Hkv][128]
+  // Accumulate mode (context-parallel shards): dq_acc is the caller's fp32
+  // accumulator and is not zeroed; dK and dV are reduce-added in fp32 into
+  // dk_acc / dv_acc [B][Sk][Hkv][D] instead of being stored as bf16.
+  int accum;
+  float* dk_acc;
+  float* dv_acc;
   void* dq;
   int64_t q_sb, q_ss, q_sh;
   void* dk;
@@ -106,6 +113,38 @@ cudaError_t launch_bwd_prepass(const BwdArgs& a, cudaStream_t st);
 cudaError_t launch_bwd_dkdv(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             const CUtensorMap& tdo, const BwdArgs& a, cudaStream_t st);
 cudaError_t launch_bwd_dq_convert(const BwdArgs& a, cudaStream_t st);
+
+// ---- context-parallel building blocks (ring.cu) ---------------------------
+// Column / row bounds of one shard pair: out = clamp(in - shift, 0, limit),
+// per int32, over n int4 entries of each batch's window [start, start + n).
+struct ShardBoundsArgs {
+  const int4* in;      // [B][S_in] global bounds
+  int4* out;           // [B][n]
+  int64_t S_in, start, n;
+  int B;
+  int shift, limit;
+};
+cudaError_t launch_shard_bounds(const ShardBoundsArgs& a, cudaStream_t st);
+// Block offsets of one shard: out[i] = clamp(in[i] - shift, 0, limit), i <= n.
+cudaError_t launch_shard_offsets(const int32_t* in, int32_t* out, int n, int shift, int limit,
+                                 cudaStream_t st);
+
+struct MergeArgs {
+  ProblemDev pr;
+  float* o_acc;         // [B][Sq][Hq][D] fp32
+  float* lse_acc;       // [B][Hq][Sq]
+  const void* o_part;   // bf16 with o_part strides
+  int64_t p_sb, p_ss, p_sh;
+  const float* lse_part;
+  void* o_out;          // bf16 with o_out strides, or null
+  int64_t o_sb, o_ss, o_sh;
+  int first;
+};
+cudaError_t launch_lse_merge(const MergeArgs& a, cudaStream_t st);
+
+// fp32 [B][S][H][D] contiguous -> bf16 with strides (b, s, h).
+cudaError_t launch_f32_to_bf16(const float* src, void* dst, int64_t B, int64_t S, int64_t H, int64_t D,
+                               int64_t sb, int64_t ss, int64_t sh, cudaStream_t st);
 cudaError_t launch_selftest_wait_timeout(int32_t* status, cudaStream_t st);
 
 // ---- dynamic block selection (select.cu) ---------------------------------

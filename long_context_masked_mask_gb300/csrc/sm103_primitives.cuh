@@ -284,6 +284,13 @@ __device__ __forceinline__ void st_global_v8(void* p, const uint32_t* w) {
                : "memory");
 }
 
+// Four fp32 reduce-adds into global memory in one instruction (the address
+// must be 16-byte aligned); no return value.
+__device__ __forceinline__ void red_add_v4(float* p, float a, float b, float c, float d) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};"
+               :: "l"(p), "f"(a), "f"(b), "f"(c), "f"(d) : "memory");
+}
+
 // 32 lanes x 32 columns of 32 bit: thread t of the warp receives lane (base + t),
 // columns col .. col+31.
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t* r) {

@@ -139,7 +139,7 @@ def test_calls_reject_bad_pointers_before_launch():
     st = lib.lcattn_mask_compile(ctypes.byref(s), ctypes.byref(d), 0x1000, 16, None)
     assert st == lc.LCATTN_ERR_WORKSPACE
     ws = lib.lcattn_bwd_workspace_size(ctypes.byref(s))
-    # D [B][Hq][Sq] + the dQ accumulator [B][Sq][Hq][128], fp32; this shape has
+    # D [B][Hq][Sq] + the dQ accumulator [B][Hq][Sq][128], fp32; this shape has
     # 2 key tiles x 2 KV heads = 4 dK/dV units with GQA groups of 2, so the
     # units are split over two head shares and the fp32 dK/dV partials
     # [2][2][B][Sk][Hkv][128] follow.
@@ -277,3 +277,34 @@ def test_layout_regions_hold_their_contents(B, Sq, Sk, Hq, Hkv, kind):
         assert o % 256 == 0 and o + n <= o_next
     size = lc.library().lcattn_tile_meta_size(ctypes.byref(s), ctypes.byref(d))
     assert size == L.total_bytes
+
+
+def test_ring_building_blocks_validate_before_launch():
+    lib = lc.library()
+    d = _colbounds_desc()
+    # shard outside the global problem
+    st = lib.lcattn_mask_shard(ctypes.byref(d), 1, 256, 256, 200, 100, 0, 256, 0x1000, None, None, None, None)
+    assert st == lc.LCATTN_ERR_INVALID_ARG
+    st = lib.lcattn_mask_shard(ctypes.byref(d), 1, 256, 256, 0, 128, -1, 10, 0x1000, None, None, None, None)
+    assert st == lc.LCATTN_ERR_INVALID_ARG
+    st = lib.lcattn_mask_shard(ctypes.byref(d), 1, 256, 256, 0, 128, 0, 128, None, None, None, None, None)
+    assert st == lc.LCATTN_ERR_INVALID_ARG  # no output buffer
+    st = lib.lcattn_mask_shard(ctypes.byref(d), 1, 256, 256, 0, 128, 0, 128, 0x1000, 0x2000, None, None, None)
+    assert st == lc.LCATTN_ERR_INVALID_ARG  # row bounds asked for, none given
+    s = _shape()
+    st = lib.lcattn_lse_merge(ctypes.byref(s), 0x1000, 0x1000, 0x1000, 0x1000, None, None, 2, None)
+    assert st == lc.LCATTN_ERR_INVALID_ARG
+    st = lib.lcattn_lse_merge(ctypes.byref(s), 0x1008, 0x1000, 0x1000, 0x1000, None, None, 0, None)
+    assert st == lc.LCATTN_ERR_UNSUPPORTED  # misaligned accumulator
+    # accumulate-mode backward: D only, and all three accumulators required
+    assert lib.lcattn_bwd_accum_workspace_size(ctypes.byref(s)) == 4 * 4 * 256
+    st = lib.lcattn_bwd_accum(ctypes.byref(s), *([0x1000] * 7), ctypes.byref(d), 0.1, 0x1000, None, 0x1000,
+                              0x1000, 4096, None)
+    assert st == lc.LCATTN_ERR_INVALID_ARG
+    st = lib.lcattn_bwd_accum(ctypes.byref(s), *([0x1000] * 7), ctypes.byref(d), 0.1, 0x1000, 0x1000, 0x1000,
+                              0x1000, 4 * 4 * 256 - 1, None)
+    assert st == lc.LCATTN_ERR_WORKSPACE
+    st3 = (ctypes.c_int64 * 3)(256 * 4 * 128, 4 * 128, 128)
+    assert lib.lcattn_f32_to_bf16(0x1000, 0x1000, 1, 256, 4, 96, st3, None) == lc.LCATTN_ERR_UNSUPPORTED
+    bad = (ctypes.c_int64 * 3)(256 * 4 * 128, 4 * 128, 100)
+    assert lib.lcattn_f32_to_bf16(0x1000, 0x1000, 1, 256, 4, 128, bad, None) == lc.LCATTN_ERR_UNSUPPORTED
