@@ -168,8 +168,8 @@ int cuda_status(cudaError_t e) { return e == cudaSuccess ? LCATTN_OK : LCATTN_ER
 // several waves (a partly empty last wave of equal units costs up to a wave);
 // the shares' fp32 partials are summed afterwards.  Depends on the shape only,
 // so the workspace size does too.
-int bwd_parts(const lcattn_shape* s) {
-  const int64_t units = (s->Sk + kBN - 1) / kBN * s->Hkv * s->B;
+int bwd_parts(const lcattn_shape* s, int64_t nchunks = 1) {
+  const int64_t units = (s->Sk + kBN - 1) / kBN * s->Hkv * s->B * nchunks;
   const int64_t G = s->Hq / s->Hkv;
   if (units < 304 && G % 4 == 0) return 4;
   if (units < 1216 && G % 2 == 0) return 2;
@@ -177,12 +177,32 @@ int bwd_parts(const lcattn_shape* s) {
 }
 
 // Workspace: D [B][Hq][Sq], the fp32 dQ accumulator [B][Hq][Sq][D] and, for
-// split units, the fp32 dK/dV partials [parts][2][B][Sk][Hkv][128].
-int64_t bwd_ws_bytes(const lcattn_shape* s, int parts) {
+// split units, the fp32 dK/dV partials [parts][2][B][Sk][Hkv][D]; with
+// `chunk_room`, at least one such slot for the dK/dV accumulator of chunked
+// units.
+int64_t bwd_ws_bytes(const lcattn_shape* s, int parts, bool chunk_room) {
   const int64_t d_bytes = align_up(4 * s->B * s->Hq * s->Sq, 256);
   const int64_t acc_bytes = align_up(4 * s->B * s->Sq * s->Hq * s->D, 256);
-  const int64_t part_bytes = parts > 1 ? (int64_t)parts * 2 * 4 * s->B * s->Sk * s->Hkv * s->D : 0;
+  const int64_t slot = 2 * 4 * s->B * s->Sk * s->Hkv * s->D;
+  const int64_t part_bytes = std::max<int64_t>(parts > 1 ? (int64_t)parts * slot : 0, chunk_room ? slot : 0);
   return d_bytes + acc_bytes + part_bytes;
+}
+
+// Block maps carry one tile list per query head.  Units of one (key tile, KV
+// head) walk every head's list in turn, and after a few waves the units in
+// flight sit at unrelated heads and positions: their dQ reductions and Q/dO
+// reads then spread over the whole group's rows and miss L2 (measured at 128K:
+// 83% of the reduction sectors missed).  Such units are split into chunks of
+// kChunkTiles query tiles, launched chunk-major, so that the units in flight
+// share one chunk's rows.  Chunking pays from about 512 query tiles (64K
+// tokens: +7%; 128K: +21%); at 256 the rows still fit and the extra per-unit
+// work costs 8%.  Sizes measured: 16, 32, 64 and 128 tiles, 64 the fastest.
+constexpr int64_t kChunkTiles = 64;
+constexpr int64_t kChunkMinTiles = 512;
+int64_t bwd_chunks(const lcattn_shape* s, const lcattn_mask_desc* m) {
+  const int64_t nQt = (s->Sq + kBM - 1) / kBM;
+  if (m->kind != LCATTN_MASK_BLOCKMAP || nQt < kChunkMinTiles) return 1;
+  return (nQt + kChunkTiles - 1) / kChunkTiles;
 }
 
 }  // namespace
@@ -346,7 +366,7 @@ int lcattn_fwd_ws(const lcattn_shape* shape, const void* q, const void* k, const
 
 size_t lcattn_bwd_workspace_size(const lcattn_shape* shape) {
   if (validate_shape(shape) != LCATTN_OK || shape->D > 128) return 0;
-  return (size_t)bwd_ws_bytes(shape, bwd_parts(shape));
+  return (size_t)bwd_ws_bytes(shape, bwd_parts(shape), true);
 }
 
 }  // extern "C"
@@ -382,11 +402,13 @@ int bwd_run(unsigned stages, const lcattn_shape* shape, const void* q, const voi
   for (auto p : ptrs)
     if (!aligned16(p)) return LCATTN_ERR_UNSUPPORTED;
   if (!(scale > 0.f) || !(scale < 1e30f)) return LCATTN_ERR_INVALID_ARG;
-  const int parts = allow_split ? bwd_parts(shape) : 1;
+  // (The accumulate mode serves shards of a split sequence and never chunks.)
+  const int64_t nchunks = allow_split && !acc.on() ? bwd_chunks(shape, mask) : 1;
+  const int parts = allow_split ? bwd_parts(shape, nchunks) : 1;
   // Accumulate mode needs only D: dQ goes to the caller's accumulator and the
   // split units reduce-add their dK/dV shares directly.
   const int64_t need = acc.on() ? align_up(4 * shape->B * shape->Hq * shape->Sq, 256)
-                                : bwd_ws_bytes(shape, parts);
+                                : bwd_ws_bytes(shape, nchunks > 1 ? 1 : parts, nchunks > 1);
   if ((int64_t)workspace_bytes < need) return LCATTN_ERR_WORKSPACE;
   CUtensorMap tq, tk, tv, tdo;
   if ((st = encode_bshd(&tq, q, shape->B, shape->Sq, shape->Hq, shape->D, shape->q_stride))) return st;
@@ -407,7 +429,10 @@ int bwd_run(unsigned stages, const lcattn_shape* shape, const void* q, const voi
   a.dvec = reinterpret_cast<float*>(ws);
   a.dq_acc = reinterpret_cast<float*>(ws + align_up(4 * shape->B * shape->Hq * shape->Sq, 256));
   a.parts = parts;
-  a.dkv_part = reinterpret_cast<float*>(ws + bwd_ws_bytes(shape, 1));
+  a.dkv_part = reinterpret_cast<float*>(ws + bwd_ws_bytes(shape, 1, false));
+  a.nchunks = (int)nchunks;
+  a.chunk_tiles = (int)kChunkTiles;
+  a.red_parts = nchunks > 1 ? 1 : (parts > 1 ? parts : 0);
   // The workspace accumulator is head-major, [B][Hq][Sq][D]: the rows one
   // head's dK/dV units add into are contiguous, so the units in flight (which
   // mostly work on the same head) keep a compact set of lines in L2.  The
@@ -418,6 +443,10 @@ int bwd_run(unsigned stages, const lcattn_shape* shape, const void* q, const voi
   a.accum = acc.on() ? 1 : 0;
   a.dk_acc = acc.dk;
   a.dv_acc = acc.dv;
+  if (!acc.on() && nchunks > 1) {  // chunked units: dV then dK, fp32, in the partial slot
+    a.dv_acc = a.dkv_part;
+    a.dk_acc = a.dkv_part + shape->B * shape->Sk * shape->Hkv * shape->D;
+  }
   if (acc.on()) {
     a.dq_acc = acc.dq;
     a.dqa_sb = shape->Sq * shape->Hq * shape->D;
@@ -606,7 +635,7 @@ int lcattn_bwd_noalloc(const lcattn_shape* shape, const void* q, const void* k, 
   if (st) return st;
   if (shape->D > 128) return LCATTN_ERR_UNSUPPORTED;  // head dim 256: forward only
   // No split here: the fixed array holds D and the dQ accumulator only.
-  const int64_t need = bwd_ws_bytes(shape, 1);
+  const int64_t need = bwd_ws_bytes(shape, 1, false);
   if (need > (int64_t)LCATTN_NOALLOC_SCRATCH_BYTES) return LCATTN_ERR_SCRATCH_LIMIT;
   void* ws = nullptr;
   if ((st = noalloc_scratch(&ws))) return st;

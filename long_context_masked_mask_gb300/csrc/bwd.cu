@@ -95,6 +95,13 @@ __global__ void prepass_kernel(BwdArgs a) {
     #pragma unroll
     for (int k = 0; k < kPer; k += 2) *reinterpret_cast<float2*>(dq + k) = make_float2(0.f, 0.f);
   }
+  // Chunked units reduce-add dK and dV into an fp32 accumulator: clear it.
+  if (a.nchunks > 1 && !a.accum) {
+    const int64_t n4 = 2 * (int64_t)a.pr.B * a.pr.Sk * a.pr.Hkv * D / 4;
+    float4* z = reinterpret_cast<float4*>(a.dkv_part);
+    for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < n4; t += (int64_t)gridDim.x * blockDim.x)
+      z[t] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -140,7 +147,7 @@ __global__ void dkv_reduce_kernel(BwdArgs a) {
     const int b = (int)(row / ((int64_t)a.pr.Hkv * a.pr.Sk));
     const float* src = a.dkv_part + ((int64_t)w * a.pr.B * a.pr.Sk * a.pr.Hkv + row) * D + c * 8;
     float4 s0 = make_float4(0.f, 0.f, 0.f, 0.f), s1 = s0;
-    for (int p = 0; p < a.parts; ++p) {
+    for (int p = 0; p < a.red_parts; ++p) {
       const float4 x0 = reinterpret_cast<const float4*>(src + p * stride_part)[0];
       const float4 x1 = reinterpret_cast<const float4*>(src + p * stride_part)[1];
       s0.x += x0.x; s0.y += x0.y; s0.z += x0.z; s0.w += x0.w;
@@ -192,26 +199,50 @@ __device__ __forceinline__ int block_of(const int32_t* offs, int n, int x) {
 }
 
 // Iterates the (query head in group, list index) pairs of one CTA in order,
-// for the group's query heads [h_lo, h_hi).
+// for the group's query heads [h_lo, h_hi).  Chunked units (kChunked) take
+// only the entries whose query tile lies in [qlo, qhi): each list is sorted
+// by query tile, so that is a contiguous index range, found by two binary
+// searches per head.
+template <bool kChunked>
 struct ItemIter {
   const int32_t* cnt_base;  // bwd_cnt for (b, list head 0), stride nKt per list head
   const int32_t* lst_base;
-  int nH, nKt, nQt, kt, G, g, hend;
+  int nH, nKt, nQt, kt, G, g, hend, qlo, qhi;
   int hi, idx, cnt, cur;
-  __device__ void init(const TileMetaDev& t, int b, int kt_, int G_, int g_, int h_lo, int h_hi) {
-    nH = t.nH; nKt = t.nKt; nQt = t.nQt; kt = kt_; G = G_; g = g_; hend = h_hi;
+  __device__ void init(const TileMetaDev& t, int b, int kt_, int G_, int g_, int h_lo, int h_hi,
+                       int qlo_ = 0, int qhi_ = 0) {
+    nH = t.nH; nKt = t.nKt; nQt = t.nQt; kt = kt_; G = G_; g = g_; hend = h_hi; qlo = qlo_; qhi = qhi_;
     cnt_base = t.bwd_cnt + (int64_t)b * t.nH * t.nKt;
     lst_base = t.bwd_lst + (int64_t)b * t.nH * t.nKt * t.nQt;
     hi = h_lo; idx = 0;
-    cnt = hi < hend ? count_of(hi) : 0;
+    cnt = 0;
+    if (hi < hend) range_of(hi);
     skip_empty();
   }
   __device__ int list_head(int hh) const { return nH == 1 ? 0 : g * G + hh; }
   __device__ int count_of(int hh) const { return __ldg(cnt_base + (int64_t)list_head(hh) * nKt + kt); }
+  // First index in [0, n) of list `l` whose query tile is >= q (n if none).
+  __device__ int lower(const int32_t* l, int n, int q) const {
+    int lo = 0, hi_ = n;
+    while (lo < hi_) {
+      const int mid = (lo + hi_) >> 1;
+      if ((__ldg(l + mid) >> 1) < q) lo = mid + 1; else hi_ = mid;
+    }
+    return lo;
+  }
+  __device__ void range_of(int hh) {
+    cnt = count_of(hh);
+    idx = 0;
+    if (kChunked) {
+      const int32_t* l = lst_base + ((int64_t)list_head(hh) * nKt + kt) * nQt;
+      idx = lower(l, cnt, qlo);
+      cnt = lower(l, cnt, qhi);
+    }
+  }
   // Advances past empty lists and loads the entry at the new position early,
   // so the load overlaps the rest of the current iteration.
   __device__ void skip_empty() {
-    while (hi < hend && idx >= cnt) { ++hi; idx = 0; if (hi < hend) cnt = count_of(hi); }
+    while (hi < hend && idx >= cnt) { ++hi; if (hi < hend) range_of(hi); }
     if (hi < hend) cur = __ldg(lst_base + ((int64_t)list_head(hi) * nKt + kt) * nQt + idx);
   }
   __device__ bool valid() const { return hi < hend; }
@@ -228,7 +259,7 @@ __device__ __forceinline__ uint32_t range_bits(int lo, int hi, int base) {
   return (n == 32) ? 0xffffffffu : (((1u << n) - 1u) << (a - base));
 }
 
-template <int D>
+template <int D, bool kChunked>
 __global__ void __launch_bounds__(kThreadsDkdv, 1)
 dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
             const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
@@ -246,7 +277,11 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
   BwdSmem<D>& sm = *reinterpret_cast<BwdSmem<D>*>(smem_raw);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
-  const int b = blockIdx.z;
+  // Chunked units (per-head lists): blockIdx.z = batch * nchunks + query chunk,
+  // so the units launched one after another share a chunk of query tiles.
+  const int b = kChunked ? (int)(blockIdx.z / a.nchunks) : (int)blockIdx.z;
+  const int chunk = kChunked ? (int)(blockIdx.z % a.nchunks) : 0;
+  const int qlo = chunk * a.chunk_tiles, qhi = min(a.meta.nQt, qlo + a.chunk_tiles);
   const int g = blockIdx.y;
   // Longest key tiles first.  With per-head lists the order of the group's
   // first head is used.  With a split, the parts of one key tile (shares of
@@ -305,8 +340,8 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
       tma_load_4d_e(sm.k + bx * kHalfBytes, &tmK, &sm.kv_full, 64 * bx, g, kt * kBN, b);
       tma_load_4d_e(sm.v + bx * kHalfBytes, &tmV, &sm.kv_full, 64 * bx, g, kt * kBN, b);
     }
-    ItemIter it;
-    it.init(a.meta, b, kt, pr.G, g, h_lo, h_hi);
+    ItemIter<kChunked> it;
+    it.init(a.meta, b, kt, pr.G, g, h_lo, h_hi, qlo, qhi);
     int i = 0, issued = 0;
     for (; it.valid(); it.next(), ++i) {
       const int st = i & 1, use = i >> 1;
@@ -368,8 +403,8 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
       const uint64_t dO_mn = sdesc_sw128(smem_u32(sm.dO[0]), kHalfBytes, 1024);
       const uint64_t dS_mn = sdesc_sw128(smem_u32(sm.ds), kHalfBytes, 1024);
       bool ok = __all_sync(0xffffffffu, mbar_wait(&sm.kv_full, 0, abort_flag, gstatus, TO));
-      ItemIter it;
-      it.init(a.meta, b, kt, pr.G, g, h_lo, h_hi);
+      ItemIter<kChunked> it;
+      it.init(a.meta, b, kt, pr.G, g, h_lo, h_hi, qlo, qhi);
       // Both operands K-major: 16-column steps inside a 64-column half, then the next half.
       auto issue_kmaj = [&](uint32_t d, uint64_t a0, uint64_t b0) {
         mma_ss_e<0>(d, a0, b0, id_kmaj);
@@ -457,8 +492,8 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
     const int r = 32 * (warp & 3) + lane;  // head-dim row of dQ^T (TMEM lane)
     const uint32_t tQ = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16) + 128;
     const int64_t dq_row_stride = a.dqa_ss;
-    ItemIter it;
-    it.init(a.meta, b, kt, pr.G, g, h_lo, h_hi);
+    ItemIter<kChunked> it;
+    it.init(a.meta, b, kt, pr.G, g, h_lo, h_hi, qlo, qhi);
     for (int i = 0; it.valid(); it.next(), ++i) {
       const int qt = it.entry() >> 1;
       const int h = it.head();
@@ -508,8 +543,8 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
       if (a.mask.kind == LCATTN_MASK_COLBOUNDS) cb = __ldg(a.mask.col_bounds + (int64_t)b * pr.Sk + key);
       else kb = block_of(a.mask.k_offs, a.mask.nKb, key);
     }
-    ItemIter it;
-    it.init(a.meta, b, kt, pr.G, g, h_lo, h_hi);
+    ItemIter<kChunked> it;
+    it.init(a.meta, b, kt, pr.G, g, h_lo, h_hi, qlo, qhi);
     int i = 0;
     bool ok = true;
     for (; it.valid(); it.next(), ++i) {
@@ -644,7 +679,8 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
     // tile touched this key tile.  dV accumulated P' = scale * P: undo it.
     // In accumulate mode the fp32 values are reduce-added into the caller's
     // accumulators instead (nothing to add when no query tile touched the tile).
-    if (ok && !(a.accum && i == 0)) {
+    const bool red_out = a.accum || kChunked;
+    if (ok && !(red_out && i == 0)) {
       bool have = i > 0;
       if (have) {
         have = mbar_wait(&sm.done, 0, abort_flag, gstatus, TO);
@@ -670,7 +706,7 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
           #pragma unroll
           for (int k = 0; k < 32; ++k) xr[k] = 0u;
         }
-        if (key_ok && a.accum) {
+        if (key_ok && red_out) {
           float* adst = (x == 0 ? a.dv_acc : a.dk_acc) + (((int64_t)b * pr.Sk + key) * pr.Hkv + g) * D + c * 32;
           #pragma unroll
           for (int u = 0; u < 8; ++u)
@@ -705,23 +741,32 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
   }
 }
 
-template <int D>
-cudaError_t launch_dkdv_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                          const CUtensorMap& tdo, const BwdArgs& a, cudaStream_t st) {
+template <int D, bool kChunked>
+cudaError_t launch_dkdv_dc(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                           const CUtensorMap& tdo, const BwdArgs& a, cudaStream_t st) {
   static bool attr_done = false;
   const size_t smem = sizeof(BwdSmem<D>);
   if (!attr_done) {
-    cudaError_t e =
-        cudaFuncSetAttribute(dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = cudaFuncSetAttribute(dkdv_kernel<D, kChunked>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
     if (e != cudaSuccess) return e;
     attr_done = true;
   }
   BwdKernelArgs ka;
   ka.a = a;
-  dim3 grid(a.meta.nKt * a.parts, a.pr.Hkv, a.pr.B);
-  dkdv_kernel<D><<<grid, kThreadsDkdv, smem, st>>>(tq, tk, tv, tdo, ka);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess || a.parts == 1 || a.accum) return e;
+  dim3 grid(a.meta.nKt * a.parts, a.pr.Hkv, a.pr.B * a.nchunks);
+  dkdv_kernel<D, kChunked><<<grid, kThreadsDkdv, smem, st>>>(tq, tk, tv, tdo, ka);
+  return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_dkdv_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                          const CUtensorMap& tdo, const BwdArgs& a, cudaStream_t st) {
+  cudaError_t e = a.nchunks > 1 ? launch_dkdv_dc<D, true>(tq, tk, tv, tdo, a, st)
+                                : launch_dkdv_dc<D, false>(tq, tk, tv, tdo, a, st);
+  // Split or chunked units leave fp32 dK/dV (partials, or one accumulator):
+  // sum / convert them into the bf16 outputs.  The accumulate mode keeps fp32.
+  if (e != cudaSuccess || a.accum || a.red_parts == 0) return e;
   int dev = 0, nsm = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);

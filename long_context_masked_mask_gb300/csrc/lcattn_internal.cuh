@@ -102,6 +102,12 @@ struct BwdArgs {
   int accum;
   float* dk_acc;
   float* dv_acc;
+  // Chunked units (per-head lists): each (key tile, KV head) unit is split
+  // into nchunks units over query-tile ranges of chunk_tiles tiles; their dK
+  // and dV go into the fp32 accumulator at dkv_part ([dV, dK][B][Sk][Hkv][D]).
+  int nchunks, chunk_tiles;
+  // fp32 dK/dV slots the reduction kernel sums into the bf16 outputs (0 = none).
+  int red_parts;
   void* dq;
   int64_t q_sb, q_ss, q_sh;
   void* dk;
