@@ -312,6 +312,24 @@ int lcattn_bwd_stage(int stage, const lcattn_shape* shape, const void* q, const 
                      void* dk, void* dv, void* workspace, size_t workspace_bytes,
                      lcattn_stream_t stream);
 
+/* Deterministic backward: the same gradients as lcattn_bwd (same arguments
+ * and results), computed with no atomic or reduce-add anywhere, so that two
+ * calls on the same inputs give identical bits.  dK and dV come from the
+ * dK/dV pass without its dQ product; dQ comes from a pass of its own, one CTA
+ * per (query tile, query head), that recomputes S = scale * Q K^T and
+ * dP = dO V^T over the query tile's key list and accumulates dQ = dS K in
+ * tensor memory (7 GEMMs per tile pair against lcattn_bwd's 5: measured 2-12%
+ * slower, e.g. dense 8K 1018 against 1153 TFLOP/s).  Its workspace holds D
+ * and, for split dK/dV units, their fp32 partials -- no fp32 dQ accumulator
+ * (lcattn_bwd_deterministic_workspace_size bytes, smaller than lcattn_bwd's).
+ * Three kernels in order on `stream` (D pre-pass, dK/dV, dQ), plus the
+ * partials' sum when units are split.  Head dim 64 or 128.                 */
+size_t lcattn_bwd_deterministic_workspace_size(const lcattn_shape* shape);
+int lcattn_bwd_deterministic(const lcattn_shape* shape, const void* q, const void* k, const void* v,
+                             const void* o, const void* d_o, const float* lse, const void* tile_meta,
+                             const lcattn_mask_desc* mask, float scale, void* dq, void* dk, void* dv,
+                             void* workspace, size_t workspace_bytes, lcattn_stream_t stream);
+
 /* Backward that allocates nothing and takes no workspace.  The pages have no
  * counterpart: this is an interface for callers that cannot hand the library
  * device memory of their own -- for example a plugin inside a host runtime that

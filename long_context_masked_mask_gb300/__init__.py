@@ -58,7 +58,7 @@ EXPORTED = (
     "lcattn_block_select_workspace_size", "lcattn_block_select", "lcattn_block_select_stage",
     "lcattn_fwd_workspace_size", "lcattn_fwd_ws",
     "lcattn_mask_shard", "lcattn_lse_merge", "lcattn_bwd_accum_workspace_size", "lcattn_bwd_accum",
-    "lcattn_f32_to_bf16",
+    "lcattn_f32_to_bf16", "lcattn_bwd_deterministic_workspace_size", "lcattn_bwd_deterministic",
 )
 
 
@@ -115,6 +115,9 @@ def _load():
         "lcattn_bwd_stage": (ctypes.c_int, [ctypes.c_int, S, P, P, P, P, P, P, P, M, ctypes.c_float,
                                             P, P, P, P, ctypes.c_size_t, P]),
         "lcattn_bwd_noalloc": (ctypes.c_int, [S, P, P, P, P, P, P, P, M, ctypes.c_float, P, P, P, P]),
+        "lcattn_bwd_deterministic_workspace_size": (ctypes.c_size_t, [S]),
+        "lcattn_bwd_deterministic": (ctypes.c_int, [S, P, P, P, P, P, P, P, M, ctypes.c_float, P, P, P, P,
+                                                    ctypes.c_size_t, P]),
         "lcattn_read_status": (ctypes.c_int, [P, P]),
         "lcattn_clear_status": (ctypes.c_int, [P, P]),
         "lcattn_selftest_wait_timeout": (ctypes.c_int, [P, P]),
@@ -367,6 +370,30 @@ def lcattn_bwd(q, k, v, o, d_o, lse, mask: DeviceMask, tile_meta, scale: Optiona
         _check(_lib.lcattn_bwd(*args), "lcattn_bwd")
     else:
         _check(_lib.lcattn_bwd_stage(int(stage), *args), f"lcattn_bwd_stage({stage})")
+    return dq, dk, dv
+
+
+def lcattn_bwd_deterministic_workspace_size(shape: lcattn_shape) -> int:
+    return int(_lib.lcattn_bwd_deterministic_workspace_size(ctypes.byref(shape)))
+
+
+def lcattn_bwd_deterministic(q, k, v, o, d_o, lse, mask: DeviceMask, tile_meta, scale: Optional[float] = None,
+                            dq=None, dk=None, dv=None, workspace=None, stream=None):
+    """Backward through lcattn_bwd_deterministic: the same gradients as
+    :func:`lcattn_bwd` with no atomics, so repeated calls give identical bits."""
+    D = q.shape[3]
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    dq, dk, dv = _grad_buffers(q, k, v, o, d_o, dq, dk, dv)
+    shape = make_shape(q, k, v, o)
+    ws_bytes = lcattn_bwd_deterministic_workspace_size(shape)
+    if workspace is None:
+        workspace = torch.empty(max(16, ws_bytes), dtype=torch.uint8, device=q.device)
+    _check(_lib.lcattn_bwd_deterministic(ctypes.byref(shape), q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                                         o.data_ptr(), d_o.data_ptr(), lse.data_ptr(), tile_meta.data_ptr(),
+                                         ctypes.byref(mask.desc), float(scale), dq.data_ptr(), dk.data_ptr(),
+                                         dv.data_ptr(), workspace.data_ptr(), workspace.numel(),
+                                         _stream_ptr(stream)), "lcattn_bwd_deterministic")
     return dq, dk, dv
 
 

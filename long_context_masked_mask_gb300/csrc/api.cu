@@ -188,6 +188,14 @@ int64_t bwd_ws_bytes(const lcattn_shape* s, int parts, bool chunk_room) {
   return d_bytes + acc_bytes + part_bytes;
 }
 
+// Workspace of the deterministic backward: D [B][Hq][Sq] and, for split units,
+// the fp32 dK/dV partials [parts][2][B][Sk][Hkv][D] (no dQ accumulator).
+int64_t bwd_det_ws_bytes(const lcattn_shape* s, int parts) {
+  const int64_t d_bytes = align_up(4 * s->B * s->Hq * s->Sq, 256);
+  const int64_t slot = 2 * 4 * s->B * s->Sk * s->Hkv * s->D;
+  return d_bytes + (parts > 1 ? (int64_t)parts * slot : 0);
+}
+
 // Block maps carry one tile list per query head.  Units of one (key tile, KV
 // head) walk every head's list in turn, and after a few waves the units in
 // flight sit at unrelated heads and positions: their dQ reductions and Q/dO
@@ -386,7 +394,7 @@ int bwd_run(unsigned stages, const lcattn_shape* shape, const void* q, const voi
             const void* v, const void* o, const void* d_o, const float* lse,
             const void* tile_meta, const lcattn_mask_desc* mask, float scale, void* dq, void* dk,
             void* dv, void* workspace, size_t workspace_bytes, lcattn_stream_t stream,
-            bool allow_split = true, AccumOut acc = AccumOut()) {
+            bool allow_split = true, AccumOut acc = AccumOut(), bool deterministic = false) {
   lcattn_tile_meta_layout L;
   int st = layout_of(shape, mask, &L);
   if (st) return st;
@@ -402,13 +410,15 @@ int bwd_run(unsigned stages, const lcattn_shape* shape, const void* q, const voi
   for (auto p : ptrs)
     if (!aligned16(p)) return LCATTN_ERR_UNSUPPORTED;
   if (!(scale > 0.f) || !(scale < 1e30f)) return LCATTN_ERR_INVALID_ARG;
-  // (The accumulate mode serves shards of a split sequence and never chunks.)
-  const int64_t nchunks = allow_split && !acc.on() ? bwd_chunks(shape, mask) : 1;
+  // (The accumulate mode serves shards of a split sequence and never chunks;
+  // the deterministic backward never chunks either: chunked units reduce-add.)
+  const int64_t nchunks = allow_split && !acc.on() && !deterministic ? bwd_chunks(shape, mask) : 1;
   const int parts = allow_split ? bwd_parts(shape, nchunks) : 1;
   // Accumulate mode needs only D: dQ goes to the caller's accumulator and the
   // split units reduce-add their dK/dV shares directly.
   const int64_t need = acc.on() ? align_up(4 * shape->B * shape->Hq * shape->Sq, 256)
-                                : bwd_ws_bytes(shape, nchunks > 1 ? 1 : parts, nchunks > 1);
+                     : deterministic ? bwd_det_ws_bytes(shape, parts)
+                                     : bwd_ws_bytes(shape, nchunks > 1 ? 1 : parts, nchunks > 1);
   if ((int64_t)workspace_bytes < need) return LCATTN_ERR_WORKSPACE;
   CUtensorMap tq, tk, tv, tdo;
   if ((st = encode_bshd(&tq, q, shape->B, shape->Sq, shape->Hq, shape->D, shape->q_stride))) return st;
@@ -429,10 +439,17 @@ int bwd_run(unsigned stages, const lcattn_shape* shape, const void* q, const voi
   a.dvec = reinterpret_cast<float*>(ws);
   a.dq_acc = reinterpret_cast<float*>(ws + align_up(4 * shape->B * shape->Hq * shape->Sq, 256));
   a.parts = parts;
-  a.dkv_part = reinterpret_cast<float*>(ws + bwd_ws_bytes(shape, 1, false));
+  a.dkv_part = reinterpret_cast<float*>(ws + (deterministic ? align_up(4 * shape->B * shape->Hq * shape->Sq, 256)
+                                                             : bwd_ws_bytes(shape, 1, false)));
   a.nchunks = (int)nchunks;
   a.chunk_tiles = (int)kChunkTiles;
   a.red_parts = nchunks > 1 ? 1 : (parts > 1 ? parts : 0);
+  // dQ from its own kernel (dq.cu: no fp32 reductions, so every output is
+  // reproducible bit for bit) in the deterministic backward.  The fused form
+  // (dQ partials reduce-added by the dK/dV kernel) is faster on every measured
+  // workload but one: the separate kernel recomputes S and dP, 7 GEMMs against
+  // 5 (dense 8K: 1018 against 1153 TFLOP/s; 128K block map: 1073 against 1053).
+  a.dq_sep = deterministic ? 1 : 0;
   // The workspace accumulator is head-major, [B][Hq][Sq][D]: the rows one
   // head's dK/dV units add into are contiguous, so the units in flight (which
   // mostly work on the same head) keep a compact set of lines in L2.  The
@@ -465,7 +482,8 @@ int bwd_run(unsigned stages, const lcattn_shape* shape, const void* q, const voi
   cudaError_t e = cudaSuccess;
   if (stages & 1u) e = launch_bwd_prepass(a, s);
   if (e == cudaSuccess && (stages & 2u)) e = launch_bwd_dkdv(tq, tk, tv, tdo, a, s);
-  if (e == cudaSuccess && (stages & 4u)) e = launch_bwd_dq_convert(a, s);
+  if (e == cudaSuccess && (stages & 4u))
+    e = a.dq_sep ? launch_bwd_dq(tq, tk, tv, tdo, a, s) : launch_bwd_dq_convert(a, s);
   return cuda_status(e);
 }
 
@@ -489,6 +507,19 @@ int lcattn_bwd_stage(int stage, const lcattn_shape* shape, const void* q, const 
   if (stage < 1 || stage > 3) return LCATTN_ERR_INVALID_ARG;
   return bwd_run(1u << (stage - 1), shape, q, k, v, o, d_o, lse, tile_meta, mask, scale, dq, dk,
                  dv, workspace, workspace_bytes, stream);
+}
+
+size_t lcattn_bwd_deterministic_workspace_size(const lcattn_shape* shape) {
+  if (validate_shape(shape) != LCATTN_OK || shape->D > 128) return 0;
+  return (size_t)bwd_det_ws_bytes(shape, bwd_parts(shape));
+}
+
+int lcattn_bwd_deterministic(const lcattn_shape* shape, const void* q, const void* k, const void* v,
+                             const void* o, const void* d_o, const float* lse, const void* tile_meta,
+                             const lcattn_mask_desc* mask, float scale, void* dq, void* dk, void* dv,
+                             void* workspace, size_t workspace_bytes, lcattn_stream_t stream) {
+  return bwd_run(7u, shape, q, k, v, o, d_o, lse, tile_meta, mask, scale, dq, dk, dv, workspace,
+                 workspace_bytes, stream, /*allow_split=*/true, AccumOut(), /*deterministic=*/true);
 }
 
 size_t lcattn_bwd_accum_workspace_size(const lcattn_shape* shape) {

@@ -90,7 +90,7 @@ __global__ void prepass_kernel(BwdArgs a) {
     #pragma unroll
     for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
     if (lane == 0) a.dvec[((int64_t)b * a.pr.Hq + h) * a.pr.Sq + i] = acc;
-    if (a.accum) continue;  // the caller's accumulator keeps its contents
+    if (a.accum || a.dq_sep) continue;  // the caller's accumulator keeps its contents / no accumulator
     float* dq = a.dq_acc + (int64_t)b * a.dqa_sb + (int64_t)i * a.dqa_ss + (int64_t)h * a.dqa_sh + lane * kPer;
     #pragma unroll
     for (int k = 0; k < kPer; k += 2) *reinterpret_cast<float2*>(dq + k) = make_float2(0.f, 0.f);
@@ -259,7 +259,9 @@ __device__ __forceinline__ uint32_t range_bits(int lo, int hi, int base) {
   return (n == 32) ? 0xffffffffu : (((1u << n) - 1u) << (a - base));
 }
 
-template <int D, bool kChunked>
+// kDq = false: the dQ product, its drain and the dS^T copy in shared memory
+// are left out (dQ then comes from the separate dQ kernel, dq.cu).
+template <int D, bool kChunked, bool kDq>
 __global__ void __launch_bounds__(kThreadsDkdv, 1)
 dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
             const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
@@ -465,17 +467,22 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
             mma_ts_e<1>(tdK, tP + (kk >> 2) * 64 + (kk & 3) * 8, sdesc_add(bq, kk * 2048), id_ts);
         }
         tc_commit_e(&sm.q_empty[st]);  // Q(i), dO(i), LSE(i), D(i) are read for good
-        // dQ^T = K^T dS^T: A = K read MN-major (M = head dim), B = dS^T read
-        // MN-major (N = queries).  Lands in [128, 256): lane = head dim.
-        mma_ss_e<0>(tP, dK_mn, dS_mn, id_mn);
-        #pragma unroll
-        for (int kk = 1; kk < 8; ++kk)
-          mma_ss_e<1>(tP, sdesc_add(dK_mn, kk * 2048), sdesc_add(dS_mn, kk * 2048), id_mn);
-        tc_commit_e(&sm.dq_full);
-        // dP^T(i+1) = V dO^T, into the columns dQ^T(i) uses: wait for its drain.
+        if (kDq) {
+          // dQ^T = K^T dS^T: A = K read MN-major (M = head dim), B = dS^T read
+          // MN-major (N = queries).  Lands in [128, 256): lane = head dim.
+          mma_ss_e<0>(tP, dK_mn, dS_mn, id_mn);
+          #pragma unroll
+          for (int kk = 1; kk < 8; ++kk)
+            mma_ss_e<1>(tP, sdesc_add(dK_mn, kk * 2048), sdesc_add(dS_mn, kk * 2048), id_mn);
+          tc_commit_e(&sm.dq_full);
+        }
+        // dP^T(i+1) = V dO^T, into the columns dQ^T(i) uses: wait for its drain
+        // (without the dQ product, dK(i) read dS^T(i) from them first, in order).
         if (more) {
-          ok = __all_sync(0xffffffffu, mbar_wait(&sm.dq_free, i & 1, abort_flag, gstatus, TO));
-          if (!ok) break;
+          if (kDq) {
+            ok = __all_sync(0xffffffffu, mbar_wait(&sm.dq_free, i & 1, abort_flag, gstatus, TO));
+            if (!ok) break;
+          }
           tc_fence_after();
           issue_kmaj(tP, dV_k, sdesc_add(dO_k, ((i + 1) & 1) * kTileBytes));
           tc_commit_e(&sm.dp_full);
@@ -489,6 +496,7 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
   } else if (warp >= 8) {
     regs_inc<kRegsDrain>();
     // ------------------------------------------------------------ dQ drain
+    if (kDq) {
     const int r = 32 * (warp & 3) + lane;  // head-dim row of dQ^T (TMEM lane)
     const uint32_t tQ = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16) + 128;
     const int64_t dq_row_stride = a.dqa_ss;
@@ -523,6 +531,7 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
         for (int c = 0; c < 128; ++c)
           if (c < nq) atomicAdd(dst + c * dq_row_stride, __uint_as_float(d[c]));
       }
+    }
     }
   } else {
     regs_inc<kRegsWork>();
@@ -663,15 +672,17 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
           dk[16 + 2 * c4 + 1] = pack_bf16x2(sb[2], sb[3]);
         }
         tmem_st32(tP + c0, dk);
-        // dS^T row r, queries [64x, 64x+64) -> 8 swizzled 16-byte chunks of half x.
-        uint8_t* ds_row = sm.ds + x * kHalfBytes + r * 128;
-        #pragma unroll
-        for (int u = 0; u < 8; ++u)
-          *reinterpret_cast<uint4*>(ds_row + ((u ^ (r & 7)) << 4)) =
-              make_uint4(dk[4 * u], dk[4 * u + 1], dk[4 * u + 2], dk[4 * u + 3]);
+        if (kDq) {
+          // dS^T row r, queries [64x, 64x+64) -> 8 swizzled 16-byte chunks of half x.
+          uint8_t* ds_row = sm.ds + x * kHalfBytes + r * 128;
+          #pragma unroll
+          for (int u = 0; u < 8; ++u)
+            *reinterpret_cast<uint4*>(ds_row + ((u ^ (r & 7)) << 4)) =
+                make_uint4(dk[4 * u], dk[4 * u + 1], dk[4 * u + 2], dk[4 * u + 3]);
+        }
       }
       tmem_st_wait();
-      fence_proxy_async_smem();
+      if (kDq) fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(&sm.ds_ready);
     }
@@ -741,29 +752,34 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
   }
 }
 
-template <int D, bool kChunked>
+template <int D, bool kChunked, bool kDq>
 cudaError_t launch_dkdv_dc(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                            const CUtensorMap& tdo, const BwdArgs& a, cudaStream_t st) {
   static bool attr_done = false;
   const size_t smem = sizeof(BwdSmem<D>);
   if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(dkdv_kernel<D, kChunked>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
+    cudaError_t e = cudaFuncSetAttribute(dkdv_kernel<D, kChunked, kDq>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     attr_done = true;
   }
   BwdKernelArgs ka;
   ka.a = a;
   dim3 grid(a.meta.nKt * a.parts, a.pr.Hkv, a.pr.B * a.nchunks);
-  dkdv_kernel<D, kChunked><<<grid, kThreadsDkdv, smem, st>>>(tq, tk, tv, tdo, ka);
+  dkdv_kernel<D, kChunked, kDq><<<grid, kThreadsDkdv, smem, st>>>(tq, tk, tv, tdo, ka);
   return cudaGetLastError();
 }
 
 template <int D>
 cudaError_t launch_dkdv_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                           const CUtensorMap& tdo, const BwdArgs& a, cudaStream_t st) {
-  cudaError_t e = a.nchunks > 1 ? launch_dkdv_dc<D, true>(tq, tk, tv, tdo, a, st)
-                                : launch_dkdv_dc<D, false>(tq, tk, tv, tdo, a, st);
+  cudaError_t e;
+  if (a.dq_sep)
+    e = a.nchunks > 1 ? launch_dkdv_dc<D, true, false>(tq, tk, tv, tdo, a, st)
+                      : launch_dkdv_dc<D, false, false>(tq, tk, tv, tdo, a, st);
+  else
+    e = a.nchunks > 1 ? launch_dkdv_dc<D, true, true>(tq, tk, tv, tdo, a, st)
+                      : launch_dkdv_dc<D, false, true>(tq, tk, tv, tdo, a, st);
   // Split or chunked units leave fp32 dK/dV (partials, or one accumulator):
   // sum / convert them into the bf16 outputs.  The accumulate mode keeps fp32.
   if (e != cudaSuccess || a.accum || a.red_parts == 0) return e;

@@ -108,6 +108,9 @@ struct BwdArgs {
   int nchunks, chunk_tiles;
   // fp32 dK/dV slots the reduction kernel sums into the bf16 outputs (0 = none).
   int red_parts;
+  // 1: dQ from the separate dQ kernel (dq.cu), written as bf16 with no fp32
+  // accumulator; the dK/dV kernel then skips its dQ product.
+  int dq_sep;
   void* dq;
   int64_t q_sb, q_ss, q_sh;
   void* dk;
@@ -119,6 +122,8 @@ cudaError_t launch_bwd_prepass(const BwdArgs& a, cudaStream_t st);
 cudaError_t launch_bwd_dkdv(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             const CUtensorMap& tdo, const BwdArgs& a, cudaStream_t st);
 cudaError_t launch_bwd_dq_convert(const BwdArgs& a, cudaStream_t st);
+cudaError_t launch_bwd_dq(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                          const CUtensorMap& tdo, const BwdArgs& a, cudaStream_t st);
 
 // ---- context-parallel building blocks (ring.cu) ---------------------------
 // Column / row bounds of one shard pair: out = clamp(in - shift, 0, limit),

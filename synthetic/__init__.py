@@ -245,6 +245,8 @@ def workload(name: str, seed: int = 0) -> Workload:
     * ``hetero_16k``: B=1, N=16384, MHA 64:64, the five heterogeneous masks.
     * ``long_128k``: B=1, N=131072, GQA 64:8, CAUSAL and a 128x128 uniform block
       mask kept with probability 0.5 per head (diagonal forced).
+    * ``long_128k_8to1``: the same with GQA 8:1 (one KV group), for profiler
+      captures of the 128K kernels at a size a multi-pass capture can hold.
     * ``dense_8k_hd64``: as ``dense_8k`` with head dim 64 (the variant next to the
       pages' 128).
     * ``dense_8k_hd256_fwd``: B=1, N=8192, GQA 32:8, head dim 256, FULL and CAUSAL,
@@ -280,6 +282,16 @@ def workload(name: str, seed: int = 0) -> Workload:
             MaskSpec("CAUSAL"),
             MaskSpec("UNIFORM_BLOCK", {"block": bs, "keep": block_keep(Hq, nb, nb, 0.5, seed)}),
         ], device_inputs=True)
+    if name == "long_128k_8to1":
+        # The 128K workload with one KV group (8 query heads): the same masks,
+        # lists and per-unit work, 1/8 of the units; small enough (about 1.8 GB
+        # on the device) for multi-pass profiler captures.
+        N, bs, Hq = 131072, 128, 8
+        nb = N // bs
+        return Workload(name, 1, N, Hq, 1, 128, [
+            MaskSpec("CAUSAL"),
+            MaskSpec("UNIFORM_BLOCK", {"block": bs, "keep": block_keep(Hq, nb, nb, 0.5, seed)}),
+        ], device_inputs=True)
     if name == "dense_8k_hd64":
         return Workload(name, 1, 8192, 64, 8, 64, [MaskSpec("FULL"), MaskSpec("CAUSAL")])
     if name == "dense_8k_hd256_fwd":
@@ -294,5 +306,6 @@ def workload(name: str, seed: int = 0) -> Workload:
     raise KeyError(name)
 
 
-WORKLOADS = ("causal_1k", "dense_8k", "docs_32k", "hetero_16k", "long_128k", "dynamic_32k", "decode_32k",
+WORKLOADS = ("causal_1k", "dense_8k", "docs_32k", "hetero_16k", "long_128k", "long_128k_8to1", "dynamic_32k",
+             "decode_32k",
              "dense_8k_hd64", "dense_8k_hd256_fwd")
