@@ -273,6 +273,29 @@ int lcattn_fwd_ws(const lcattn_shape* shape, const void* q, const void* k, const
                   const void* tile_meta, const lcattn_mask_desc* mask, float scale, void* o,
                   float* lse, void* workspace, size_t workspace_bytes, lcattn_stream_t stream);
 
+/* FP8 forward: the same operator with e4m3 inputs (blog sections "密集注意力内核" /
+ * "稀疏注意力内核"; the pages run bf16 and fix no fp8 semantics, so these are
+ * the library's).  q [B][Sq][Hq][128], k and v [B][Sk][Hkv][128] hold OCP FP8
+ * E4M3 codes (device, one byte per element; strides in elements = bytes, all
+ * multiples of 16; 16-byte aligned); the real inputs are code * q_scale,
+ * code * k_scale, code * v_scale (per-tensor factors > 0).  Head dim 128 only
+ * (LCATTN_ERR_UNSUPPORTED otherwise).  Computes, per query row, with exact
+ * fp32 logits scale * q_scale * k_scale * <q8, k8> and their exact running
+ * max m: P = exp(logit - m) quantized to e4m3 as P * 256 for the P V product
+ * (fp32 accumulation in tensor memory), l = sum of the unquantized P, and
+ * writes o (bf16, o_stride, [B][Sq][Hq][128]) = v_scale * (P8 V8) / (256 l)
+ * and lse = m + ln l (fp32 [B][Hq][Sq]; -inf and O = 0 for rows that allow
+ * nothing).  `tile_meta` from lcattn_mask_compile on the same shape and mask.
+ * The workspace (lcattn_fwd_fp8_workspace_size bytes, 16-byte aligned) receives
+ * V^T [B][Hkv][128][Skp] (e4m3, Skp = Sk rounded up to 16), written by a first
+ * kernel so that both operands of the P V product are K-major; the forward
+ * kernel follows on `stream`.                                              */
+size_t lcattn_fwd_fp8_workspace_size(const lcattn_shape* shape);
+int lcattn_fwd_fp8(const lcattn_shape* shape, const void* q, const void* k, const void* v, float q_scale,
+                   float k_scale, float v_scale, const void* tile_meta, const lcattn_mask_desc* mask,
+                   float scale, void* o, float* lse, void* workspace, size_t workspace_bytes,
+                   lcattn_stream_t stream);
+
 /* The backward calls below compute the gradients of the same operator (blog
  * sections "密集注意力内核" / "稀疏注意力内核"; the pages' sparse-kernel findings,
  * sections "稀疏内核性能" and "核心发现总结", single the backward out as the main

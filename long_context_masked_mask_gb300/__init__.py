@@ -59,6 +59,7 @@ EXPORTED = (
     "lcattn_fwd_workspace_size", "lcattn_fwd_ws",
     "lcattn_mask_shard", "lcattn_lse_merge", "lcattn_bwd_accum_workspace_size", "lcattn_bwd_accum",
     "lcattn_f32_to_bf16", "lcattn_bwd_deterministic_workspace_size", "lcattn_bwd_deterministic",
+    "lcattn_fwd_fp8_workspace_size", "lcattn_fwd_fp8",
 )
 
 
@@ -116,6 +117,9 @@ def _load():
                                             P, P, P, P, ctypes.c_size_t, P]),
         "lcattn_bwd_noalloc": (ctypes.c_int, [S, P, P, P, P, P, P, P, M, ctypes.c_float, P, P, P, P]),
         "lcattn_bwd_deterministic_workspace_size": (ctypes.c_size_t, [S]),
+        "lcattn_fwd_fp8_workspace_size": (ctypes.c_size_t, [S]),
+        "lcattn_fwd_fp8": (ctypes.c_int, [S, P, P, P, ctypes.c_float, ctypes.c_float, ctypes.c_float, P, M,
+                                          ctypes.c_float, P, P, P, ctypes.c_size_t, P]),
         "lcattn_bwd_deterministic": (ctypes.c_int, [S, P, P, P, P, P, P, P, M, ctypes.c_float, P, P, P, P,
                                                     ctypes.c_size_t, P]),
         "lcattn_read_status": (ctypes.c_int, [P, P]),
@@ -293,6 +297,35 @@ def lcattn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, mask: DeviceMa
     _check(_lib.lcattn_fwd(ctypes.byref(shape), q.data_ptr(), k.data_ptr(), v.data_ptr(),
                            tile_meta.data_ptr(), ctypes.byref(mask.desc), float(scale), o.data_ptr(),
                            lse.data_ptr(), _stream_ptr(stream)), "lcattn_fwd")
+    return o, lse
+
+
+def lcattn_fwd_fp8(q8: torch.Tensor, k8: torch.Tensor, v8: torch.Tensor, q_scale: float, k_scale: float,
+                   v_scale: float, mask: DeviceMask, tile_meta: torch.Tensor, scale: Optional[float] = None,
+                   o: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                   workspace: Optional[torch.Tensor] = None, stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """FP8 forward (lcattn_fwd_fp8): q8, k8, v8 are uint8 tensors of e4m3 codes,
+    [B, S, H, 128], with per-tensor descale factors.  Returns (O bf16, LSE fp32)."""
+    for t in (q8, k8, v8):
+        if t.dtype != torch.uint8:
+            raise TypeError("q8, k8 and v8 must hold e4m3 codes as uint8")
+    B, Sq, Hq, D = q8.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if o is None:
+        o = torch.empty(B, Sq, Hq, D, dtype=torch.bfloat16, device=q8.device)
+    if lse is None:
+        lse = torch.empty(B, Hq, Sq, dtype=torch.float32, device=q8.device)
+    shape = make_shape(q8, k8, v8, o)
+    nbytes = int(_lib.lcattn_fwd_fp8_workspace_size(ctypes.byref(shape)))
+    if nbytes == 0:
+        raise LcattnError(LCATTN_ERR_UNSUPPORTED, "lcattn_fwd_fp8_workspace_size")
+    if workspace is None:
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=q8.device)
+    _check(_lib.lcattn_fwd_fp8(ctypes.byref(shape), q8.data_ptr(), k8.data_ptr(), v8.data_ptr(), float(q_scale),
+                               float(k_scale), float(v_scale), tile_meta.data_ptr(), ctypes.byref(mask.desc),
+                               float(scale), o.data_ptr(), lse.data_ptr(), workspace.data_ptr(), workspace.numel(),
+                               _stream_ptr(stream)), "lcattn_fwd_fp8")
     return o, lse
 
 

@@ -17,7 +17,7 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(os.path.dirname(PKG), "_build")
 LIB = os.path.join(PKG, "liblcattn.so")
 SOURCES = ["api.cu", "mask_compile.cu", "fwd.cu", "fwd_split.cu", "bwd.cu", "select.cu", "selftest.cu",
-           "ring.cu", "dq.cu"]
+           "ring.cu", "dq.cu", "fwd8.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CFLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
           "--expt-relaxed-constexpr"]

@@ -163,6 +163,51 @@ int encode_bshd_box(CUtensorMap* m, const void* ptr, int64_t B, int64_t S, int64
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? LCATTN_OK : LCATTN_ERR_CUDA; }
 
+// [B][S][H][128] e4m3 (one byte per element) with byte strides (b, s, h): a
+// 4-D map with a 128-byte x 1 head x 128 rows box and 128-byte swizzle (one
+// K-major 128 x 128 tile per copy).
+int encode_bshd8(CUtensorMap* m, const void* ptr, int64_t B, int64_t S, int64_t H, const int64_t st[3]) {
+  auto fn = encode_fn();
+  if (!fn) return LCATTN_ERR_CUDA;
+  cuuint64_t dims[4] = {128, (cuuint64_t)H, (cuuint64_t)S, (cuuint64_t)B};
+  cuuint64_t strides[3] = {(cuuint64_t)st[2], (cuuint64_t)st[1], (cuuint64_t)(st[0] > 0 ? st[0] : S * st[1])};
+  cuuint32_t box[4] = {128, 1, 128, 1};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(ptr), dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? LCATTN_OK : LCATTN_ERR_UNSUPPORTED;
+}
+
+// V^T [B][Hkv][128][Skp] e4m3: box of 128 keys x 128 head-dim rows.
+int encode_vt8(CUtensorMap* m, const void* ptr, int64_t B, int64_t Hkv, int64_t Skp) {
+  auto fn = encode_fn();
+  if (!fn) return LCATTN_ERR_CUDA;
+  cuuint64_t dims[4] = {(cuuint64_t)Skp, 128, (cuuint64_t)Hkv, (cuuint64_t)B};
+  cuuint64_t strides[3] = {(cuuint64_t)Skp, (cuuint64_t)(128 * Skp), (cuuint64_t)(Hkv * 128 * Skp)};
+  cuuint32_t box[4] = {128, 128, 1, 1};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(ptr), dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? LCATTN_OK : LCATTN_ERR_UNSUPPORTED;
+}
+
+int64_t fp8_skp(const lcattn_shape* s) { return align_up(s->Sk, 16); }
+
+int64_t fwd8_ws_bytes(const lcattn_shape* s) { return align_up(s->B * s->Hkv * 128 * fp8_skp(s), 256); }
+
+// The FP8 forward's extra rules: head dim 128, and every e4m3 row 16-byte
+// aligned (strides in elements = bytes, multiples of 16).
+int validate_fp8(const lcattn_shape* s) {
+  if (s->D != 128) return LCATTN_ERR_UNSUPPORTED;
+  const int64_t* st[3] = {s->q_stride, s->k_stride, s->v_stride};
+  for (auto x : st)
+    for (int i = 0; i < 3; ++i)
+      if (x[i] % 16 != 0) return LCATTN_ERR_UNSUPPORTED;
+  return LCATTN_OK;
+}
+
 // dK/dV work units (key tile, KV head, batch) are split over shares of the
 // GQA group's query heads when there are too few units to fill the GPU in
 // several waves (a partly empty last wave of equal units costs up to a wave);
@@ -370,6 +415,44 @@ int lcattn_fwd_ws(const lcattn_shape* shape, const void* q, const void* k, const
   a.o_sb = shape->o_stride[0]; a.o_ss = shape->o_stride[1]; a.o_sh = shape->o_stride[2];
   a.lse = lse;
   return cuda_status(launch_fwd_split(tq, tk, tv, a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+size_t lcattn_fwd_fp8_workspace_size(const lcattn_shape* shape) {
+  if (validate_shape(shape) != LCATTN_OK || validate_fp8(shape) != LCATTN_OK) return 0;
+  return (size_t)fwd8_ws_bytes(shape);
+}
+
+int lcattn_fwd_fp8(const lcattn_shape* shape, const void* q, const void* k, const void* v, float q_scale,
+                   float k_scale, float v_scale, const void* tile_meta, const lcattn_mask_desc* mask, float scale,
+                   void* o, float* lse, void* workspace, size_t workspace_bytes, lcattn_stream_t stream) {
+  lcattn_tile_meta_layout L;
+  int st = layout_of(shape, mask, &L);
+  if (st) return st;
+  if ((st = validate_fp8(shape))) return st;
+  if (!q || !k || !v || !o || !lse || !tile_meta || !workspace) return LCATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(tile_meta) ||
+      !aligned16(workspace))
+    return LCATTN_ERR_UNSUPPORTED;
+  for (float x : {scale, q_scale, k_scale, v_scale})
+    if (!(x > 0.f) || !(x < 1e30f)) return LCATTN_ERR_INVALID_ARG;
+  if ((int64_t)workspace_bytes < fwd8_ws_bytes(shape)) return LCATTN_ERR_WORKSPACE;
+  const int64_t skp = fp8_skp(shape);
+  CUtensorMap tq, tk, tvt;
+  if ((st = encode_bshd8(&tq, q, shape->B, shape->Sq, shape->Hq, shape->q_stride))) return st;
+  if ((st = encode_bshd8(&tk, k, shape->B, shape->Sk, shape->Hkv, shape->k_stride))) return st;
+  if ((st = encode_vt8(&tvt, workspace, shape->B, shape->Hkv, skp))) return st;
+  Fwd8Args a;
+  a.pr = problem_of(shape);
+  a.mask = mask_of(mask);
+  a.meta = meta_of(L, tile_meta);
+  a.logit_scale_log2 = scale * q_scale * k_scale * 1.4426950408889634f;
+  a.v_scale = v_scale;
+  a.o = o;
+  a.o_sb = shape->o_stride[0]; a.o_ss = shape->o_stride[1]; a.o_sh = shape->o_stride[2];
+  a.lse = lse;
+  return cuda_status(launch_fwd8(tq, tk, tvt, a, static_cast<const uint8_t*>(v), shape->v_stride[0],
+                                 shape->v_stride[1], shape->v_stride[2], static_cast<uint8_t*>(workspace),
+                                 (int)skp, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 size_t lcattn_bwd_workspace_size(const lcattn_shape* shape) {

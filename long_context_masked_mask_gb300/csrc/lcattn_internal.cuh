@@ -125,6 +125,23 @@ cudaError_t launch_bwd_dq_convert(const BwdArgs& a, cudaStream_t st);
 cudaError_t launch_bwd_dq(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                           const CUtensorMap& tdo, const BwdArgs& a, cudaStream_t st);
 
+// ---- FP8 forward (fwd8.cu) --------------------------------------------------
+struct Fwd8Args {
+  ProblemDev pr;            // D = 128
+  MaskDev mask;
+  TileMetaDev meta;
+  float logit_scale_log2;   // scale * q_scale * k_scale * log2(e)
+  float v_scale;
+  void* o;                  // bf16
+  int64_t o_sb, o_ss, o_sh;
+  float* lse;
+};
+// Writes V^T (e4m3 [B][Hkv][128][Skp], keys past Sk zero) into `vt`, then runs
+// the forward; `tvt` maps `vt`.
+cudaError_t launch_fwd8(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tvt,
+                        const Fwd8Args& a, const uint8_t* v, int64_t v_sb, int64_t v_ss, int64_t v_sh,
+                        uint8_t* vt, int Skp, cudaStream_t st);
+
 // ---- context-parallel building blocks (ring.cu) ---------------------------
 // Column / row bounds of one shard pair: out = clamp(in - shift, 0, limit),
 // per int32, over n int4 entries of each batch's window [start, start + n).

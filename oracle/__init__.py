@@ -29,10 +29,10 @@ bilinearity identity for pooled scores, and the invariants between mask
 families and selection parameters.  Every function here is pinned; none is
 "parity unpinned".
 """
-from . import block_select_ref
+from . import block_select_ref, fp8_ref
 from .masks_ref import allowed, allowed_pairs
 from .attention_ref import (attention_fwd, attention_bwd, attention_fwd_rows, attention_bwd_rows,
                             attention_bwd_sampled, classify_tiles, EMPTY, FULL, PARTIAL)
 
-__all__ = ["block_select_ref", "allowed", "allowed_pairs", "attention_fwd", "attention_bwd", "attention_fwd_rows",
+__all__ = ["block_select_ref", "fp8_ref", "allowed", "allowed_pairs", "attention_fwd", "attention_bwd", "attention_fwd_rows",
            "attention_bwd_rows", "attention_bwd_sampled", "classify_tiles", "EMPTY", "FULL", "PARTIAL"]

@@ -109,6 +109,25 @@ def qkv(B: int, N: int, Hq: int, Hkv: int, D: int = 128, seed: int = 0,
     return out
 
 
+def qkv_fp8(B: int, N: int, Hq: int, Hkv: int, D: int = 128, seed: int = 0,
+            Sk: Optional[int] = None, device: str = "cpu") -> Dict[str, Any]:
+    """Q, K, V as OCP FP8 E4M3 codes (uint8 tensors, [B, S, H, D]) with per-tensor
+    descale factors: each tensor is drawn i.i.d. N(0,1) in fp32 as in
+    :func:`qkv` (order Q, K, V, one ``torch.Generator`` seeded with ``seed`` on
+    ``device``), divided by its factor amax / 448 and rounded to E4M3 by torch's
+    float8_e4m3fn conversion, so its largest magnitude maps to E4M3's largest
+    finite value.  The real inputs are code value x factor."""
+    Sk = N if Sk is None else Sk
+    g = torch.Generator(device=device).manual_seed(seed)
+    out: Dict[str, Any] = {}
+    for name, S, H in (("q", N, Hq), ("k", Sk, Hkv), ("v", Sk, Hkv)):
+        x = torch.randn(B, S, H, D, generator=g, device=device, dtype=torch.float32)
+        f = float(x.abs().max()) / 448.0
+        out[name + "8"] = (x / f).to(torch.float8_e4m3fn).view(torch.uint8)
+        out[name + "_scale"] = f
+    return out
+
+
 def qkv_device(B: int, N: int, Hq: int, Hkv: int, D: int = 128, seed: int = 0,
                device: str = "cuda") -> Dict[str, torch.Tensor]:
     """Same distribution as :func:`qkv`, drawn directly on ``device``.

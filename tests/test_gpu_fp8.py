@@ -1,0 +1,100 @@
+"""The FP8 forward (lcattn_fwd_fp8) through the C ABI against the fp64 oracle
+on the decoded E4M3 inputs (oracle.fp8_ref).
+
+Tolerance, from the arithmetic: the logits and the row sum are exact fp32
+functions of the fp8 inputs, but P enters the P V product as e4m3(P * 256),
+which rounds each P to 3 mantissa bits, a relative error of at most 2^-4.  So:
+O relative Frobenius error <= 5e-2 (the rounding errors of many P partly
+cancel: a CPU model of exactly this arithmetic gave 1.7e-2 to 2.6e-2 on these
+shapes), O max-abs <= 2^-4 * max|O| + 1e-2 (bf16 output rounding), LSE
+max-abs <= 5e-3 with -inf exactly where the oracle has it (P's rounding does
+not enter the LSE)."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle import fp8_ref
+from synthetic import MaskSpec, block_keep, qkv_fp8, segment_lengths
+
+pytestmark = pytest.mark.gpu
+
+lc = pytest.importorskip("long_context_masked_mask_gb300")
+
+
+def _spec(kind, N, Hq):
+    if kind == "CAUSAL_DOCUMENT":
+        return MaskSpec("CAUSAL_DOCUMENT", {"doc_lens": segment_lengths(N, N // 6, N // 2, 1)})
+    if kind == "UNIFORM_BLOCK":
+        nb = -(-N // 64)
+        return MaskSpec("UNIFORM_BLOCK", {"block": 64, "keep": block_keep(Hq, nb, nb, 0.5, 2)})
+    if kind == "VARIABLE_BLOCK":
+        ql, kl = segment_lengths(N, 32, 200, 3), segment_lengths(N, 32, 200, 4)
+        keep = block_keep(Hq, len(ql), len(kl), 0.5, 5, force_diagonal=False)
+        keep[:, 1, :] = False  # fully masked rows
+        return MaskSpec("VARIABLE_BLOCK", {"q_block_lens": ql, "k_block_lens": kl, "keep": keep})
+    if kind == "GLOBAL_SLIDING":
+        return MaskSpec("GLOBAL_SLIDING", {"global_tokens": 40, "window": 100})
+    return MaskSpec(kind)
+
+
+def _check(o, lse, O, L):
+    o = o.double().cpu().numpy()
+    lse = lse.double().cpu().numpy()
+    relf = float(np.linalg.norm(o - O) / max(np.linalg.norm(O), 1e-30))
+    assert relf <= 5e-2, relf
+    assert np.abs(o - O).max() <= 2.0 ** -4 * max(1.0, np.abs(O).max()) + 1e-2
+    assert np.array_equal(np.isneginf(lse), np.isneginf(L))
+    fin = np.isfinite(L)
+    if fin.any():
+        assert np.abs(lse[fin] - L[fin]).max() <= 5e-3
+
+
+@pytest.mark.parametrize("kind,B,N,Hq,Hkv", [
+    ("CAUSAL", 1, 392, 4, 2), ("FULL", 1, 700, 8, 2), ("CAUSAL_DOCUMENT", 2, 520, 4, 4),
+    ("GLOBAL_SLIDING", 1, 600, 4, 1), ("UNIFORM_BLOCK", 1, 400, 4, 2), ("VARIABLE_BLOCK", 1, 600, 2, 2),
+    ("CAUSAL", 1, 1, 2, 1), ("FULL", 1, 129, 2, 2),
+])
+def test_fp8_forward_matches_oracle(kind, B, N, Hq, Hkv):
+    spec = _spec(kind, N, Hq)
+    x = qkv_fp8(B, N, Hq, Hkv, 128, seed=11)
+    dev = {k: (t.cuda() if torch.is_tensor(t) else t) for k, t in x.items()}
+    mask = lc.DeviceMask(spec, N, Hq, B)
+    shape = lc.make_shape(dev["q8"], dev["k8"], dev["v8"])
+    meta = lc.lcattn_mask_compile(shape, mask)
+    o, lse = lc.lcattn_fwd_fp8(dev["q8"], dev["k8"], dev["v8"], x["q_scale"], x["k_scale"], x["v_scale"], mask, meta)
+    torch.cuda.synchronize()
+    assert lc.lcattn_read_status(meta) == 0
+    O, L = fp8_ref.attention_fwd_fp8(x["q8"].numpy(), x["k8"].numpy(), x["v8"].numpy(), x["q_scale"],
+                                     x["k_scale"], x["v_scale"], spec, 1.0 / math.sqrt(128))
+    _check(o, lse, O, L)
+
+
+def test_fp8_rectangular_and_column_bounds_only():
+    """Sq != Sk (bottom-right causal, a ragged key tail) and the column-bounds path
+    without row bounds, which must give the same bits as with them."""
+    Sq, Sk, Hq, Hkv = 300, 777, 4, 2
+    x = qkv_fp8(1, Sq, Hq, Hkv, 128, seed=13, Sk=Sk)
+    dev = {k: (t.cuda() if torch.is_tensor(t) else t) for k, t in x.items()}
+    spec = MaskSpec("CAUSAL")
+    outs = []
+    for rows in (True, False):
+        mask = lc.DeviceMask(spec, Sq, Hq, 1, Sk=Sk, row_bounds=rows)
+        meta = lc.lcattn_mask_compile(lc.make_shape(dev["q8"], dev["k8"], dev["v8"]), mask)
+        outs.append(lc.lcattn_fwd_fp8(dev["q8"], dev["k8"], dev["v8"], x["q_scale"], x["k_scale"], x["v_scale"],
+                                      mask, meta))
+    torch.cuda.synchronize()
+    assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
+    O, L = fp8_ref.attention_fwd_fp8(x["q8"].numpy(), x["k8"].numpy(), x["v8"].numpy(), x["q_scale"],
+                                     x["k_scale"], x["v_scale"], spec, 1.0 / math.sqrt(128))
+    _check(outs[0][0], outs[0][1], O, L)
+
+
+def test_fp8_refuses_other_head_dims_and_strides():
+    x = torch.zeros(1, 64, 2, 64, dtype=torch.uint8, device="cuda")
+    m = lc.DeviceMask(MaskSpec("FULL"), 64, 2, 1)
+    meta = lc.lcattn_mask_compile(lc.make_shape(x, x, x), m)
+    with pytest.raises(lc.LcattnError):
+        lc.lcattn_fwd_fp8(x, x, x, 1.0, 1.0, 1.0, m, meta)
