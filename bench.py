@@ -82,7 +82,8 @@ def mask_labels(wl):
 
 
 def workload_desc(wl):
-    desc = (f"{wl.name}: B={wl.B}, N={wl.N}, Hq:Hkv={wl.Hq}:{wl.Hkv}, hd={wl.D}, bf16, masks "
+    desc = (f"{wl.name}: B={wl.B}, N={wl.N}, Hq:Hkv={wl.Hq}:{wl.Hkv}, hd={wl.D}, "
+            f"{'e4m3 inputs (per-tensor factors), bf16 O' if wl.fp8 else 'bf16'}, masks "
             + mask_labels(wl))
     if wl.selects:
         desc += (f" (dynamic masks selected every step from block-structured Q/K, strength "
@@ -90,7 +91,8 @@ def workload_desc(wl):
     if wl.Sq is not None:
         desc += f", Sq={wl.Sq} queries per sequence against the N keys (bottom-right aligned)"
     if wl.forward_only:
-        desc += ", forward only (decode-style rows); FLOPs and bytes of the forward"
+        desc += (", forward only; FLOPs of the forward" if wl.fp8 else
+                 ", forward only (decode-style rows); FLOPs and bytes of the forward")
     return desc
 
 
@@ -120,7 +122,13 @@ def oracle_sample_rows(wl):
 def oracle_sample(wl, seed):
     """Inputs for the oracle sample: query head 0 with its KV head over the full
     key sequence (the query rows are chosen by oracle_sample_rows)."""
-    from synthetic import qkv, qkv_block_structured
+    from synthetic import qkv, qkv_block_structured, qkv_fp8
+    if wl.fp8:
+        from oracle import fp8_ref
+        x = qkv_fp8(1, wl.q_len, 1, 1, wl.D, seed=seed, Sk=wl.N)
+        out = {n: fp8_ref.e4m3_decode(x[n + "8"].numpy()) * x[n + "_scale"] for n in ("q", "k", "v")}
+        out["rows"] = oracle_sample_rows(wl)
+        return out
     if wl.structure > 0:
         x = qkv_block_structured(1, wl.N, 1, 1, wl.selects[0].block, strength=wl.structure, seed=seed)
     else:
@@ -331,12 +339,18 @@ class Leg:
     def __init__(self, name, seed, rank, dev):
         import torch
         import long_context_masked_mask_gb300 as lc
-        from synthetic import qkv, qkv_block_structured, qkv_device, workload
+        from synthetic import qkv, qkv_block_structured, qkv_device, qkv_fp8, workload
         self.torch, self.lc, self.dev = torch, lc, dev
         self.wl = wl = workload(name, seed)
         B, N, Hq, Hkv, D = wl.B, wl.N, wl.Hq, wl.Hkv, wl.D
         s = seed + 1000 * rank
-        if wl.structure > 0:
+        self.fp8 = wl.fp8
+        self.peak_mult = 2.0 if wl.fp8 else 1.0
+        if wl.fp8:  # e4m3 codes (uint8) with per-tensor factors; forward only
+            x = qkv_fp8(B, N, Hq, Hkv, D, seed=s, Sk=N, device=str(dev))
+            self.scales = (x["q_scale"], x["k_scale"], x["v_scale"])
+            x = {"q": x["q8"], "k": x["k8"], "v": x["v8"], "do": None}
+        elif wl.structure > 0:
             x = qkv_block_structured(B, N, Hq, Hkv, wl.selects[0].block, strength=wl.structure, seed=s,
                                      device=str(dev))
         elif wl.device_inputs:
@@ -348,7 +362,8 @@ class Leg:
         self.Sq = Sq = q.shape[1]
         self.fwd_only = wl.forward_only
         self.shape = shape = lc.make_shape(self.q, self.k, self.v)
-        self.ws = torch.empty(max(16, lc.lcattn_bwd_workspace_size(shape)), dtype=torch.uint8, device=dev)
+        self.ws = torch.empty(max(16, 0 if self.fwd_only else lc.lcattn_bwd_workspace_size(shape)),
+                              dtype=torch.uint8, device=dev)
         runs = []
         for spec in wl.masks:
             m = lc.DeviceMask(spec, Sq, Hq, B, device=dev, Sk=N)
@@ -372,10 +387,16 @@ class Leg:
             runs.append({"spec": sel, "sel": sel, "offs": offs, "sws": sws, "mask": m, "meta": meta,
                          "fwd_flops": fwd_flops, "bwd_flops": 2.5 * fwd_flops, "launches": 2 + 6 + 3})
         for r in runs:
-            r["o"] = torch.empty_like(q)
+            r["o"] = torch.empty(B, Sq, Hq, D, dtype=torch.bfloat16, device=dev)
             r["lse"] = torch.empty(B, Hq, Sq, dtype=torch.float32, device=dev)
             if not self.fwd_only:
                 r["dq"], r["dk"], r["dv"] = torch.empty_like(q), torch.empty_like(self.k), torch.empty_like(self.v)
+            if self.fp8:  # the V^T pre-pass's workspace; two launches (V^T, forward)
+                fws = int(lc.library().lcattn_fwd_fp8_workspace_size(lc.ctypes.byref(shape)))
+                r["fws"] = torch.empty(max(16, fws), dtype=torch.uint8, device=dev)
+                r["split"] = False
+                r["launches"] += 2
+                continue
             # The forward's split-KV workspace (empty unless the query side is short).
             fws = lc.lcattn_fwd_workspace_size(shape, r["mask"])
             r["fws"] = torch.empty(max(16, fws), dtype=torch.uint8, device=dev)
@@ -384,6 +405,13 @@ class Leg:
         self.runs = runs
         self.step_flops = sum(r["fwd_flops"] + r["bwd_flops"] for r in runs)
         self.launches_per_step = sum(r["launches"] for r in runs)
+
+    def fwd(self, r, qq, kk, vv):
+        if self.fp8:
+            self.lc.lcattn_fwd_fp8(qq, kk, vv, *self.scales, r["mask"], r["meta"], o=r["o"], lse=r["lse"],
+                                   workspace=r["fws"])
+        else:
+            self.lc.lcattn_fwd_ws(qq, kk, vv, r["mask"], r["meta"], o=r["o"], lse=r["lse"], workspace=r["fws"])
 
     def select(self, r, qq, kk, stage=None):
         sel = r["sel"]
@@ -401,7 +429,7 @@ class Leg:
             if "sel" in r:
                 self.select(r, qq, kk)
             lc.lcattn_mask_compile(self.shape, r["mask"], r["meta"])
-            lc.lcattn_fwd_ws(qq, kk, vv, r["mask"], r["meta"], o=r["o"], lse=r["lse"], workspace=r["fws"])
+            self.fwd(r, qq, kk, vv)
             if not self.fwd_only:
                 lc.lcattn_bwd(qq, kk, vv, r["o"], dd, r["lse"], r["mask"], r["meta"],
                               dq=r["dq"], dk=r["dk"], dv=r["dv"], workspace=self.ws)
@@ -504,7 +532,7 @@ class Leg:
                                     "peak_kind": f"{pk['source']} copy bandwidth",
                                     "traffic": (traffic_lookup("pool_kernel", wl.name) or {}).get("bytes")}
             t_c = timed(lambda: lc.lcattn_mask_compile(self.shape, m, meta))
-            t_f = timed(lambda: lc.lcattn_fwd_ws(q, k, v, m, meta, o=r["o"], lse=r["lse"], workspace=r["fws"]))
+            t_f = timed(lambda: self.fwd(r, q, k, v))
             tb = [0.0, 0.0, 0.0]
             if not self.fwd_only:
                 tb = [timed(lambda: lc.lcattn_bwd(q, k, v, r["o"], d_o, r["lse"], m, meta, dq=r["dq"],
@@ -524,7 +552,7 @@ class Leg:
                              "fwd_ms": round(t_f, 4), "bwd_ms": round(sum(tb), 4),
                              "bwd_stage_ms": [round(t, 4) for t in tb], "mask_compile_ms": round(t_c, 4),
                              "fwd_tflops": round(fwd_tf, 1), "bwd_tflops": round(bwd_tf, 1),
-                             "fwd_frac_of_peak": round(fwd_tf / pk["burst"], 4),
+                             "fwd_frac_of_peak": round(fwd_tf / (pk["burst"] * self.peak_mult), 4),
                              "bwd_frac_of_peak": round(bwd_tf / pk["burst"], 4)})
             if t_sel is not None:
                 per_mask[-1]["select_ms"] = [round(t_sel[0], 4), round(t_sel[1], 4)]
@@ -553,12 +581,14 @@ class Leg:
                     "peak_kind": f"{pk['source']} copy bandwidth"}
         elif fl_dom > 0:
             achieved = fl_dom / (t_dom / 1e3) / 1e12
-            roof = {"kernel": dom, "bound": "tensor", "achieved": round(achieved, 1), "peak": pk["burst"],
-                    "unit": "TFLOP/s", "frac": round(achieved / pk["burst"], 4),
-                    "frac_of_sustained": round(achieved / pk["sustained"], 4),
+            peak = pk["burst"] * self.peak_mult
+            roof = {"kernel": "fwd8_kernel" if self.fp8 else dom, "bound": "tensor", "achieved": round(achieved, 1),
+                    "peak": peak, "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
+                    "frac_of_sustained": round(achieved / (pk["sustained"] * self.peak_mult), 4),
                     "algorithmic_flops_per_launch": fl_dom / max(1, n_dom),
                     "launches": n_dom, "ms_per_launch": round(t_dom / max(1, n_dom), 4),
-                    "peak_kind": f"bf16 dense, {pk['source']} burst (each kernel timed alone)"}
+                    "peak_kind": (f"e4m3 dense: 2x the {pk['source']} bf16 burst (the nominal fp8/bf16 ratio)"
+                                  if self.fp8 else f"bf16 dense, {pk['source']} burst (each kernel timed alone)")}
         else:  # a memory-bound kernel dominating would be reported against HBM
             roof = {"kernel": dom, "bound": "hbm", "achieved": None, "peak": pk["hbm_gbs"], "unit": "GB/s",
                     "frac": None, "peak_kind": f"{pk['source']} copy bandwidth"}
@@ -577,7 +607,8 @@ class Leg:
         q, k, v, d_o = self.q, self.k, self.v, self.d_o
         ins = (("q", q), ("k", k), ("v", v)) + ((("do", d_o),) if not self.fwd_only else ())
         host = {n: t.cpu().pin_memory() for n, t in ins}
-        q_, k_, v_, do_ = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v), torch.empty_like(d_o)
+        q_, k_, v_ = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        do_ = torch.empty_like(d_o) if d_o is not None else None
         out_names = ("o", "lse") if self.fwd_only else ("o", "lse", "dq", "dk", "dv")
         outs = [{n: torch.empty(r[n].shape, dtype=r[n].dtype, pin_memory=True) for n in out_names}
                 for r in self.runs]
@@ -607,7 +638,7 @@ class Leg:
                 if "sel" in r:
                     self.select(r, q_, k_)
                 lc.lcattn_mask_compile(self.shape, r["mask"], r["meta"])
-                lc.lcattn_fwd_ws(q_, k_, v_, r["mask"], r["meta"], o=r["o"], lse=r["lse"], workspace=r["fws"])
+                self.fwd(r, q_, k_, v_)
                 if j == 0:
                     stream.wait_event(do_ready)
                 if not self.fwd_only:
@@ -696,7 +727,8 @@ def run_gpu(args, rank, world, dist):
         return
     line = {"metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "e4m3" if wl.fp8 else "bf16",
             "data": "synthetic",
             "config": {"workload": workload_desc(wl), "seq_len": headline["N"],
                        "global_batch": headline["B"] * world,

@@ -248,6 +248,7 @@ class Workload:
     structure: float = 0.0       # > 0: block-structured Q/K (qkv_block_structured strength)
     Sq: Optional[int] = None     # query length when it differs from the key length N
     forward_only: bool = False   # decode-style rows: the step is the forward alone
+    fp8: bool = False            # e4m3 Q, K, V with per-tensor factors (forward only)
 
     @property
     def q_len(self) -> int:
@@ -266,6 +267,8 @@ def workload(name: str, seed: int = 0) -> Workload:
       mask kept with probability 0.5 per head (diagonal forced).
     * ``long_128k_8to1``: the same with GQA 8:1 (one KV group), for profiler
       captures of the 128K kernels at a size a multi-pass capture can hold.
+    * ``dense_8k_fp8``: as ``dense_8k`` with e4m3 Q, K, V (per-tensor factors,
+      :func:`qkv_fp8`), forward only.
     * ``dense_8k_hd64``: as ``dense_8k`` with head dim 64 (the variant next to the
       pages' 128).
     * ``dense_8k_hd256_fwd``: B=1, N=8192, GQA 32:8, head dim 256, FULL and CAUSAL,
@@ -311,6 +314,9 @@ def workload(name: str, seed: int = 0) -> Workload:
             MaskSpec("CAUSAL"),
             MaskSpec("UNIFORM_BLOCK", {"block": bs, "keep": block_keep(Hq, nb, nb, 0.5, seed)}),
         ], device_inputs=True)
+    if name == "dense_8k_fp8":
+        return Workload(name, 1, 8192, 64, 8, 128, [MaskSpec("FULL"), MaskSpec("CAUSAL")], forward_only=True,
+                        fp8=True)
     if name == "dense_8k_hd64":
         return Workload(name, 1, 8192, 64, 8, 64, [MaskSpec("FULL"), MaskSpec("CAUSAL")])
     if name == "dense_8k_hd256_fwd":
@@ -326,5 +332,5 @@ def workload(name: str, seed: int = 0) -> Workload:
 
 
 WORKLOADS = ("causal_1k", "dense_8k", "docs_32k", "hetero_16k", "long_128k", "long_128k_8to1", "dynamic_32k",
-             "decode_32k",
+             "decode_32k", "dense_8k_fp8",
              "dense_8k_hd64", "dense_8k_hd256_fwd")
