@@ -582,7 +582,7 @@ class Leg:
         elif fl_dom > 0:
             achieved = fl_dom / (t_dom / 1e3) / 1e12
             peak = pk["burst"] * self.peak_mult
-            roof = {"kernel": "fwd8_kernel" if self.fp8 else dom, "bound": "tensor", "achieved": round(achieved, 1),
+            roof = {"kernel": "vt8_kernel + fwd_kernel (e4m3)" if self.fp8 else dom, "bound": "tensor", "achieved": round(achieved, 1),
                     "peak": peak, "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
                     "frac_of_sustained": round(achieved / (pk["sustained"] * self.peak_mult), 4),
                     "algorithmic_flops_per_launch": fl_dom / max(1, n_dom),

@@ -437,22 +437,26 @@ int lcattn_fwd_fp8(const lcattn_shape* shape, const void* q, const void* k, cons
     if (!(x > 0.f) || !(x < 1e30f)) return LCATTN_ERR_INVALID_ARG;
   if ((int64_t)workspace_bytes < fwd8_ws_bytes(shape)) return LCATTN_ERR_WORKSPACE;
   const int64_t skp = fp8_skp(shape);
-  CUtensorMap tq, tk, tvt;
+  CUtensorMap tq, tk, tvt, to;
   if ((st = encode_bshd8(&tq, q, shape->B, shape->Sq, shape->Hq, shape->q_stride))) return st;
   if ((st = encode_bshd8(&tk, k, shape->B, shape->Sk, shape->Hkv, shape->k_stride))) return st;
   if ((st = encode_vt8(&tvt, workspace, shape->B, shape->Hkv, skp))) return st;
-  Fwd8Args a;
+  if ((st = encode_bshd(&to, o, shape->B, shape->Sq, shape->Hq, shape->D, shape->o_stride))) return st;
+  FwdArgs a;
   a.pr = problem_of(shape);
   a.mask = mask_of(mask);
   a.meta = meta_of(L, tile_meta);
-  a.logit_scale_log2 = scale * q_scale * k_scale * 1.4426950408889634f;
-  a.v_scale = v_scale;
+  a.scale_log2 = scale * q_scale * k_scale * 1.4426950408889634f;
+  a.o_scale = v_scale;
   a.o = o;
   a.o_sb = shape->o_stride[0]; a.o_ss = shape->o_stride[1]; a.o_sh = shape->o_stride[2];
   a.lse = lse;
-  return cuda_status(launch_fwd8(tq, tk, tvt, a, static_cast<const uint8_t*>(v), shape->v_stride[0],
-                                 shape->v_stride[1], shape->v_stride[2], static_cast<uint8_t*>(workspace),
-                                 (int)skp, reinterpret_cast<cudaStream_t>(stream)));
+  const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_vt8(static_cast<const uint8_t*>(v), shape->v_stride[0], shape->v_stride[1],
+                             shape->v_stride[2], static_cast<uint8_t*>(workspace), (int)shape->B, (int)shape->Sk,
+                             (int)skp, (int)shape->Hkv, cs);
+  if (e != cudaSuccess) return cuda_status(e);
+  return cuda_status(launch_fwd_e4m3(tq, tk, tvt, to, a, cs));
 }
 
 size_t lcattn_bwd_workspace_size(const lcattn_shape* shape) {

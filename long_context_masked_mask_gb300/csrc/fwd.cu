@@ -43,14 +43,30 @@ using namespace dev;
 // stages of 32 KB), so that the next tile's K streams in while this tile's
 // halves are consumed.  At D = 256 an item is always one head (TMEM: two S
 // buffers + a 256-column O) and there is one Q buffer.
-template <int D> struct FwdGeom {
-  static constexpr int kTileBytes = 128 * D * 2;
-  static constexpr int kBoxes = D / 64;
+// F8 (e4m3 inputs, D = 128 only): a tile is 128 rows x 128 bytes, one box, and
+// the ring has 8 stages of 16 KB; the V entries are tiles of V^T (a 128 x 128
+// block of the key-contiguous V^T written by a pre-pass), so that both
+// kind::f8f6f4 operands of the PV product are K-major.
+template <int D, bool F8 = false> struct FwdGeom {
+  static_assert(!F8 || D == 128, "the e4m3 forward is built for head dim 128");
+  static constexpr int kElem = F8 ? 1 : 2;                      // bytes per element
+  static constexpr int kTileBytes = 128 * D * kElem;
+  static constexpr int kBoxCols = F8 ? 128 : 64;                // elements per 128-byte box row
+  static constexpr int kBoxes = D / kBoxCols;
   static constexpr int kParts = D == 256 ? 2 : 1;            // ring entries per K (or V) tile
   static constexpr int kEntryBytes = kTileBytes / kParts;
   static constexpr int kBoxesPerEntry = kBoxes / kParts;
-  static constexpr int kStages = D == 64 ? 8 : 4;            // K/V ring depth (entries)
+  static constexpr int kStages = (D == 64 || F8) ? 8 : 4;    // K/V ring depth (entries)
   static constexpr int kQBufs = D == 256 ? 1 : 2;
+  // k-steps of the S product per entry (32 bytes of the contraction each) and
+  // of the PV product per tile (16 keys for bf16 P, 32 for e4m3 P: 8 TMEM columns each).
+  static constexpr int kSSteps = D * kElem / 32 / kParts;
+  static constexpr int kPvSteps = F8 ? 4 : 8;
+  // Largest P in the log2-domain online softmax: the running max moves only
+  // when a row max grows by more than kRescaleThreshold, so P <= 2^threshold.
+  // e4m3 P is stored as P * kPScale (at most 2^(4 + 4) = 256, inside e4m3's 448).
+  static constexpr float kRescaleThreshold = F8 ? 4.0f : 8.0f;
+  static constexpr float kPScale = F8 ? 16.0f : 1.0f;
 };
 constexpr int kItemQ = 4;           // depth of the work-item queue (producer -> other roles)
 constexpr int kHalfBytes = 16384;   // one 64-column TMA box of 128 rows
@@ -60,14 +76,13 @@ constexpr int kThreads = 384;        // 3 warpgroups
 constexpr int kRegsSoftmax = 216;
 constexpr int kRegsOther = 72;
 static_assert(128 * (2 * kRegsSoftmax + kRegsOther) <= kThreads * 168, "register split");
-constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
-template <int D>
+template <int D, bool F8 = false>
 struct FwdSmem {
-  static constexpr int kStages = FwdGeom<D>::kStages;
-  static constexpr int kTileBytes = FwdGeom<D>::kTileBytes;
-  alignas(1024) uint8_t q[FwdGeom<D>::kQBufs][kTileBytes];
-  alignas(1024) uint8_t kv[kStages][FwdGeom<D>::kEntryBytes];
+  static constexpr int kStages = FwdGeom<D, F8>::kStages;
+  static constexpr int kTileBytes = FwdGeom<D, F8>::kTileBytes;
+  alignas(1024) uint8_t q[FwdGeom<D, F8>::kQBufs][kTileBytes];
+  alignas(1024) uint8_t kv[kStages][FwdGeom<D, F8>::kEntryBytes];
   // Per slot: O staging for the epilogue's TMA stores (one 64-column box of
   // 128 rows, 128-byte swizzled).  Between epilogues its first 4 KB hold the
   // column bounds of partial tiles (two buffers of 128 int4).
@@ -213,19 +228,21 @@ __device__ __forceinline__ FwdItem fwd_item(const FwdArgs& a, int hpc, int hb, i
 }
 
 // HPC: query heads per item (2, or 1); a template parameter so that each
-// mode's loops are compiled for it alone.
-template <int D, int HPC>
+// mode's loops are compiled for it alone.  F8: e4m3 Q, K and V^T tiles (tmV
+// then maps V^T), kind::f8f6f4 products, e4m3 P.
+template <int D, int HPC, bool F8>
 __global__ void __launch_bounds__(kThreads, 1)
 fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
            const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
            const __grid_constant__ FwdKernelArgs ka) {
-  constexpr int kStages = FwdGeom<D>::kStages;
-  constexpr int kTileBytes = FwdGeom<D>::kTileBytes;
-  constexpr int kBoxes = FwdGeom<D>::kBoxes;
-  constexpr int kQBufs = FwdGeom<D>::kQBufs;
-  constexpr int kParts = FwdGeom<D>::kParts;
-  constexpr int kEntryBytes = FwdGeom<D>::kEntryBytes;
-  constexpr int kBoxesPerEntry = FwdGeom<D>::kBoxesPerEntry;
+  constexpr int kStages = FwdGeom<D, F8>::kStages;
+  constexpr int kTileBytes = FwdGeom<D, F8>::kTileBytes;
+  constexpr int kBoxes = FwdGeom<D, F8>::kBoxes;
+  constexpr int kQBufs = FwdGeom<D, F8>::kQBufs;
+  constexpr int kParts = FwdGeom<D, F8>::kParts;
+  constexpr int kEntryBytes = FwdGeom<D, F8>::kEntryBytes;
+  constexpr int kBoxesPerEntry = FwdGeom<D, F8>::kBoxesPerEntry;
+  constexpr int kBoxCols = FwdGeom<D, F8>::kBoxCols;
   constexpr int kE = 2 * kParts;  // ring entries per key tile
   // With half-tile entries the ring holds one tile, so K runs a tile ahead of
   // V: entries go K(0), K(1), V(0), K(2), V(1), ..., V(last) -- the order the
@@ -233,7 +250,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
   // soon as S(T) frees its stages instead of after PV(T-1).
   constexpr bool kAhead = kParts == 2;
   extern __shared__ uint8_t smem_raw[];
-  FwdSmem<D>& sm = *reinterpret_cast<FwdSmem<D>*>(
+  FwdSmem<D, F8>& sm = *reinterpret_cast<FwdSmem<D, F8>*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const FwdArgs& a = ka.a;
   const ProblemDev& pr = a.pr;
@@ -345,9 +362,14 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
         if (!__all_sync(0xffffffffu, okw)) return false;
       }
       mbar_expect_tx_e(&sm.kv_full[stage], kEntryBytes);
-      for (int bx = 0; bx < kBoxesPerEntry; ++bx)
-        tma_load_4d_e(sm.kv[stage] + bx * kHalfBytes, tm, &sm.kv_full[stage],
-                      128 * part + 64 * bx, eg, kt * kBN, eb);
+      if (F8 && tm == &tmV) {
+        // V^T [B][Hkv][128][keys]: the 128 keys of tile kt x all 128 head-dim rows.
+        tma_load_4d_e(sm.kv[stage], tm, &sm.kv_full[stage], kt * kBN, 0, eg, eb);
+      } else {
+        for (int bx = 0; bx < kBoxesPerEntry; ++bx)
+          tma_load_4d_e(sm.kv[stage] + bx * kHalfBytes, tm, &sm.kv_full[stage],
+                        128 * part + kBoxCols * bx, eg, kt * kBN, eb);
+      }
       ++t;
       return true;
     };
@@ -392,7 +414,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
         if (nx.n > 0)
           for (int s = 0; s < hpc; ++s)
             for (int bx = 0; bx < kBoxes; ++bx)
-              tma_prefetch_l2_4d_e(&tmQ, 64 * bx, nx.h0 + s, nx.qt * kBM, nx.b);
+              tma_prefetch_l2_4d_e(&tmQ, kBoxCols * bx, nx.h0 + s, nx.qt * kBM, nx.b);
       }
       if (it.n == 0) continue;
       const int g = it.h0 / pr.G;
@@ -423,7 +445,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
             }
             mbar_expect_tx_e(&sm.q_full[qb], kTileBytes);
             for (int bx = 0; bx < kBoxes; ++bx)
-              tma_load_4d_e(sm.q[qb] + bx * kHalfBytes, &tmQ, &sm.q_full[qb], 64 * bx, it.h0 + s,
+              tma_load_4d_e(sm.q[qb] + bx * kHalfBytes, &tmQ, &sm.q_full[qb], kBoxCols * bx, it.h0 + s,
                             it.qt * kBM, it.b);
             ++q_issued[qb];
           }
@@ -458,13 +480,47 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
     // has read the previous item's O (it does so before releasing the item's
     // first P).
     {
-      const uint32_t idesc_qk = idesc_bf16_f32(128, 128, false, false);
-      const uint32_t idesc_pv = idesc_bf16_f32(128, D / kParts, false, true);
+      const uint32_t idesc_qk = F8 ? idesc_e4m3_f32(128, 128) : idesc_bf16_f32(128, 128, false, false);
+      const uint32_t idesc_pv = F8 ? idesc_e4m3_f32(128, D) : idesc_bf16_f32(128, D / kParts, false, true);
       // Base descriptors; stage s of the ring is kTileBytes further on.
       const uint64_t dq0 = sdesc_sw128(smem_u32(sm.q[0]), 16, 1024);
       const uint64_t dq1 = sdesc_sw128(smem_u32(sm.q[kQBufs - 1]), 16, 1024);
       const uint64_t dk0 = sdesc_sw128(smem_u32(sm.kv[0]), 16, 1024);          // K tile, K-major
-      const uint64_t dv0 = sdesc_sw128(smem_u32(sm.kv[0]), kHalfBytes, 1024);  // V tile, MN-major
+      // V tile read MN-major (bf16), or V^T tile read K-major (e4m3).
+      const uint64_t dv0 = sdesc_sw128(smem_u32(sm.kv[0]), F8 ? 16u : static_cast<uint32_t>(kHalfBytes), 1024);
+      // S (+)= Q K^T over one ring entry: k-steps of 32 bytes inside the
+      // 128-byte swizzled rows, the next 64-column box after four of them.
+      auto gemm_s = [&](uint32_t tS, uint64_t qp, uint64_t kb, bool first) {
+        if constexpr (F8) {
+          if (first) mma8_ss_e<0>(tS, qp, kb, idesc_qk);
+          else mma8_ss_e<1>(tS, qp, kb, idesc_qk);
+        } else {
+          if (first) mma_ss_e<0>(tS, qp, kb, idesc_qk);
+          else mma_ss_e<1>(tS, qp, kb, idesc_qk);
+        }
+        #pragma unroll
+        for (int kk = 1; kk < FwdGeom<D, F8>::kSSteps; ++kk) {
+          const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
+          if constexpr (F8) mma8_ss_e<1>(tS, sdesc_add(qp, off), sdesc_add(kb, off), idesc_qk);
+          else mma_ss_e<1>(tS, sdesc_add(qp, off), sdesc_add(kb, off), idesc_qk);
+        }
+      };
+      // O (+)= P V: A = P from TMEM (8 columns per k-step: 16 bf16 or 32 e4m3
+      // keys), B = V read MN-major (16 key rows, 2048 bytes, per k-step) or V^T
+      // read K-major (32 keys, 32 bytes, per k-step).
+      auto gemm_pv = [&](uint32_t tO, uint32_t tP, uint64_t vb, uint32_t acc) {
+        if constexpr (F8) {
+          mma8_ts_er(tO, tP, vb, idesc_pv, acc);
+          #pragma unroll
+          for (int kk = 1; kk < FwdGeom<D, F8>::kPvSteps; ++kk)
+            mma8_ts_er(tO, tP + kk * 8, sdesc_add(vb, kk * 32), idesc_pv, 1u);
+        } else {
+          mma_ts_er(tO, tP, vb, idesc_pv, acc);
+          #pragma unroll
+          for (int kk = 1; kk < FwdGeom<D, F8>::kPvSteps; ++kk)
+            mma_ts_e<1>(tO, tP + kk * 8, sdesc_add(vb, kk * 2048), idesc_pv);
+        }
+      };
       bool ok = true;
       int T = 0, nq = 0;
       uint32_t pv_acc = 0u;  // accumulate flag of the pending PV(T-1)
@@ -476,10 +532,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
         tc_fence_after();
         const int tv = 2 * T - 1;
         const uint64_t vb = sdesc_add(dv0, (tv % kStages) * kTileBytes);
-        // O += P V: A = P (bf16 pairs in TMEM), B = V read MN-major.
-        mma_ts_er(tO, tS, vb, idesc_pv, pv_acc);
-        #pragma unroll
-        for (int kk = 1; kk < 8; ++kk) mma_ts_e<1>(tO, tS + kk * 8, sdesc_add(vb, kk * 2048), idesc_pv);
+        gemm_pv(tO, tS, vb, pv_acc);  // O += P V
         tc_commit_e(&sm.o_full[s]);
         if (last) tc_commit_e(&sm.o_last[s]);  // the item's O is complete
         return true;
@@ -510,9 +563,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
             tc_fence_after();
             const uint64_t vb = sdesc_add(dv0, (tv % kStages) * kEntryBytes);
             const uint32_t tOp = tmem + 256 + ps * 128 + part * (D / kParts);
-            mma_ts_er(tOp, tP, vb, idesc_pv, acc);
-            #pragma unroll
-            for (int kk = 1; kk < 8; ++kk) mma_ts_e<1>(tOp, tP + kk * 8, sdesc_add(vb, kk * 2048), idesc_pv);
+            gemm_pv(tOp, tP, vb, acc);
             tc_commit_e(&sm.kv_empty[tv % kStages]);
           }
           tc_commit_e(&sm.o_full[ps]);
@@ -548,14 +599,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
               tc_fence_after();
               const uint64_t kb = sdesc_add(dk0, (tk % kStages) * kEntryBytes);
               const uint64_t qp = sdesc_add(qd, part * kEntryBytes);
-              if (part == 0) mma_ss_e<0>(tS, qp, kb, idesc_qk);
-              else mma_ss_e<1>(tS, qp, kb, idesc_qk);
-              #pragma unroll
-              for (int kk = 1; kk < D / kParts / 16; ++kk) {
-                constexpr uint32_t kHalf = kHalfBytes;
-                const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
-                mma_ss_e<1>(tS, sdesc_add(qp, off), sdesc_add(kb, off), idesc_qk);
-              }
+              gemm_s(tS, qp, kb, part == 0);
               tc_commit_e(&sm.kv_empty[tk % kStages]);
             }
             if (!ok) break;
@@ -602,13 +646,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
             // S = Q K^T, both K-major.
             const uint32_t tS = tmem + s * 128;
             const uint64_t qd = s ? dq1 : dq0;
-            mma_ss_e<0>(tS, qd, kb, idesc_qk);
-            #pragma unroll (D <= 128 ? D / 16 - 1 : 1)  // the MMA warp has 72 registers
-            for (int kk = 1; kk < D / 16; ++kk) {
-              constexpr uint32_t kHalf = kHalfBytes;
-              const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
-              mma_ss_e<1>(tS, sdesc_add(qd, off), sdesc_add(kb, off), idesc_qk);
-            }
+            gemm_s(tS, qd, kb, true);
             tc_commit_e(&sm.s_full[s]);
             if (j == n - 1) tc_commit_e(&sm.q_empty[s]);  // Q of this slot is read for good
           }
@@ -646,6 +684,8 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
       const uint32_t lane_off = static_cast<uint32_t>(32 * (warp & 3)) << 16;
       const uint32_t tO = tmem + lane_off + 256 + s * 128;
       const float sl2 = a.scale_log2;
+      constexpr float kLog2PScale = F8 ? 4.0f : 0.0f;  // log2 of FwdGeom::kPScale
+      static_assert(FwdGeom<D, F8>::kPScale == (F8 ? 16.0f : 1.0f), "P scale and its log2");
       const int last_kt = (pr.Sk - 1) / kBN;
       const bool ragged_k = (pr.Sk % kBN) != 0;
       const bool use_rows = a.mask.kind == LCATTN_MASK_COLBOUNDS && a.mask.row_bounds != nullptr;
@@ -780,7 +820,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
           #pragma unroll
           for (int c = 8; c < 128; c += 2) m4[(c >> 1) & 3] = fmax3(m4[(c >> 1) & 3], x[c], x[c + 1]);
           const float m_tile = fmaxf(fmax3(m4[0], m4[1], m4[2]), m4[3]) * sl2;  // -inf stays -inf
-          const bool need = m_tile > m_run + kRescaleThreshold;
+          const bool need = m_tile > m_run + FwdGeom<D, F8>::kRescaleThreshold;
           const bool warp_rescale = __any_sync(0xffffffffu, need) && j > 0;
           const float m_new = need ? m_tile : m_run;
           const float alpha = need ? fast_exp2(m_run - m_new) : 1.f;  // exp2(-inf) = 0
@@ -788,20 +828,37 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
           const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
           // P = exp2(S * scale * log2(e) - m): the scaling and the row sum run
           // on column pairs (paired fp32 instructions), the exponentials one by one.
-          const float2 sl2v = make_float2(sl2, sl2), negm = make_float2(-m_use, -m_use);
+          // e4m3 P is P * kPScale (the shift folded into the exponent); the row
+          // sum l then carries the same factor, which cancels in O / l.
+          const float negm_s = -(m_use - kLog2PScale);
+          const float2 sl2v = make_float2(sl2, sl2), negm = make_float2(negm_s, negm_s);
           float2 s4[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                           make_float2(0.f, 0.f)};
-          #pragma unroll
-          for (int c = 0; c < 2; ++c) {
-            uint32_t pk[32];
+          if constexpr (F8) {
+            uint32_t pk[32];  // four keys per column
             #pragma unroll
             for (int i = 0; i < 32; ++i) {
-              const float2 y = fma2(make_float2(x[c * 64 + 2 * i], x[c * 64 + 2 * i + 1]), sl2v, negm);
-              const float2 p = make_float2(fast_exp2(y.x), fast_exp2(y.y));
-              s4[i & 3] = add2(s4[i & 3], p);
-              pk[i] = pack_bf16x2(p.x, p.y);
+              const float2 y0 = fma2(make_float2(x[4 * i], x[4 * i + 1]), sl2v, negm);
+              const float2 y1 = fma2(make_float2(x[4 * i + 2], x[4 * i + 3]), sl2v, negm);
+              const float2 p0 = make_float2(fast_exp2(y0.x), fast_exp2(y0.y));
+              const float2 p1 = make_float2(fast_exp2(y1.x), fast_exp2(y1.y));
+              s4[i & 3] = add2(s4[i & 3], add2(p0, p1));
+              pk[i] = pack_e4m3x4(p0.x, p0.y, p1.x, p1.y);
             }
-            tmem_st32(tS + c * 32, pk);
+            tmem_st32(tS, pk);
+          } else {
+            #pragma unroll
+            for (int c = 0; c < 2; ++c) {
+              uint32_t pk[32];
+              #pragma unroll
+              for (int i = 0; i < 32; ++i) {
+                const float2 y = fma2(make_float2(x[c * 64 + 2 * i], x[c * 64 + 2 * i + 1]), sl2v, negm);
+                const float2 p = make_float2(fast_exp2(y.x), fast_exp2(y.y));
+                s4[i & 3] = add2(s4[i & 3], p);
+                pk[i] = pack_bf16x2(p.x, p.y);
+              }
+              tmem_st32(tS + c * 32, pk);
+            }
           }
           const float2 s2 = add2(add2(s4[0], s4[1]), add2(s4[2], s4[3]));
           l_run = l_run * alpha + (s2.x + s2.y);
@@ -844,7 +901,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
         if (!alt && ok && (have_o || n == 0) && !stg_reclaim()) ok = false;
         if (ok && (have_o || n == 0)) {
           const bool live = l_run > 0.f;
-          const float inv = live ? 1.f / l_run : 0.f;
+          const float inv = live ? a.o_scale / l_run : 0.f;
           __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(a.o) + (int64_t)b * a.o_sb +
                                 (int64_t)row * a.o_ss + (int64_t)h * a.o_sh;
           // The first kTmaCols columns go out through shared memory and TMA
@@ -919,7 +976,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
           pbits ^= 16u;
           if (row < pr.Sq)
             a.lse[((int64_t)b * pr.Hq + h) * pr.Sq + row] =
-                live ? (m_run + __log2f(l_run)) * 0.69314718055994531f : -INFINITY;
+                live ? (m_run - kLog2PScale + __log2f(l_run)) * 0.69314718055994531f : -INFINITY;
         }
         if (n > 0 && !have_o) ok = false;
         if (n > 0) pbits ^= 8u;
@@ -940,22 +997,22 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
   }
 }
 
-template <int D, int HPC>
+template <int D, int HPC, bool F8>
 cudaError_t launch_fwd_mode(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             const CUtensorMap& to, const FwdKernelArgs& ka, int grid, cudaStream_t st) {
   static bool attr_done = false;
-  const size_t smem = sizeof(FwdSmem<D>) + 1024;
+  const size_t smem = sizeof(FwdSmem<D, F8>) + 1024;
   if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(fwd_kernel<D, HPC>,
+    cudaError_t e = cudaFuncSetAttribute(fwd_kernel<D, HPC, F8>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     attr_done = true;
   }
-  fwd_kernel<D, HPC><<<(unsigned)grid, kThreads, smem, st>>>(tq, tk, tv, to, ka);
+  fwd_kernel<D, HPC, F8><<<(unsigned)grid, kThreads, smem, st>>>(tq, tk, tv, to, ka);
   return cudaGetLastError();
 }
 
-template <int D>
+template <int D, bool F8 = false>
 cudaError_t launch_fwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                          const CUtensorMap& to, const FwdArgs& a, cudaStream_t st) {
   int dev = 0, nsm = 0;
@@ -978,8 +1035,8 @@ cudaError_t launch_fwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
   // Persistent: one CTA per SM (shared memory admits one), never more CTAs than items.
   const int grid = ka.total_items < nsm ? ka.total_items : nsm;
   if constexpr (D <= 128)
-    if (ka.heads_per_cta == 2) return launch_fwd_mode<D, 2>(tq, tk, tv, to, ka, grid, st);
-  return launch_fwd_mode<D, 1>(tq, tk, tv, to, ka, grid, st);
+    if (ka.heads_per_cta == 2) return launch_fwd_mode<D, 2, F8>(tq, tk, tv, to, ka, grid, st);
+  return launch_fwd_mode<D, 1, F8>(tq, tk, tv, to, ka, grid, st);
 }
 
 }  // namespace
@@ -989,6 +1046,12 @@ cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
   if (a.pr.D == 64) return launch_fwd_d<64>(tq, tk, tv, to, a, st);
   if (a.pr.D == 256) return launch_fwd_d<256>(tq, tk, tv, to, a, st);
   return launch_fwd_d<128>(tq, tk, tv, to, a, st);
+}
+
+cudaError_t launch_fwd_e4m3(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tvt,
+                            const CUtensorMap& to, const FwdArgs& a, cudaStream_t st) {
+  if (a.pr.D != 128) return cudaErrorInvalidValue;
+  return launch_fwd_d<128, true>(tq, tk, tvt, to, a, st);
 }
 
 }  // namespace lcattn

@@ -52,7 +52,8 @@ struct FwdArgs {
   ProblemDev pr;
   MaskDev mask;
   TileMetaDev meta;
-  float scale_log2;
+  float scale_log2;         // scale * log2(e) (e4m3: times the Q and K factors)
+  float o_scale = 1.f;      // factor of O / l (e4m3: the V factor)
   void* o;
   int64_t o_sb, o_ss, o_sh;
   float* lse;
@@ -60,6 +61,11 @@ struct FwdArgs {
 // `to`: O as a TMA map with the same box as Q (the epilogue's stores).
 cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const CUtensorMap& to, const FwdArgs& a, cudaStream_t st);
+// The same forward with e4m3 Q and K (maps of 128-byte boxes) and `tvt`
+// mapping V^T [B][Hkv][128][Skp] e4m3 (box: 128 keys x 128 head-dim rows);
+// D = 128, O bf16.  a.scale_log2 carries the Q and K factors, a.o_scale the V factor.
+cudaError_t launch_fwd_e4m3(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tvt,
+                            const CUtensorMap& to, const FwdArgs& a, cudaStream_t st);
 
 // Split-KV forward for short query sides (fwd_split.cu).
 struct SplitArgs {
@@ -125,22 +131,11 @@ cudaError_t launch_bwd_dq_convert(const BwdArgs& a, cudaStream_t st);
 cudaError_t launch_bwd_dq(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                           const CUtensorMap& tdo, const BwdArgs& a, cudaStream_t st);
 
-// ---- FP8 forward (fwd8.cu) --------------------------------------------------
-struct Fwd8Args {
-  ProblemDev pr;            // D = 128
-  MaskDev mask;
-  TileMetaDev meta;
-  float logit_scale_log2;   // scale * q_scale * k_scale * log2(e)
-  float v_scale;
-  void* o;                  // bf16
-  int64_t o_sb, o_ss, o_sh;
-  float* lse;
-};
-// Writes V^T (e4m3 [B][Hkv][128][Skp], keys past Sk zero) into `vt`, then runs
-// the forward; `tvt` maps `vt`.
-cudaError_t launch_fwd8(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tvt,
-                        const Fwd8Args& a, const uint8_t* v, int64_t v_sb, int64_t v_ss, int64_t v_sh,
-                        uint8_t* vt, int Skp, cudaStream_t st);
+// ---- FP8 forward: the V^T pre-pass (fwd8.cu) ---------------------------------
+// V [B][Sk][Hkv][128] e4m3 (byte strides) -> V^T [B][Hkv][128][Skp] e4m3, keys
+// in [Sk, Skp) written as 0.  The forward is launch_fwd_e4m3 (fwd.cu).
+cudaError_t launch_vt8(const uint8_t* v, int64_t v_sb, int64_t v_ss, int64_t v_sh, uint8_t* vt, int B, int Sk,
+                       int Skp, int Hkv, cudaStream_t st);
 
 // ---- context-parallel building blocks (ring.cu) ---------------------------
 // Column / row bounds of one shard pair: out = clamp(in - shift, 0, limit),
