@@ -6,7 +6,7 @@
  * Efficiency to Distributed Context Parallelism", xllm-io blog review, sections
  * "密集注意力内核" and "稀疏注意力内核"): softmax attention under a mask, forward
  * and backward, bf16 inputs, head dim 128 (the pages' setting, section
- * "实验设置") or 64, and head dim 256 forward only; MHA and GQA.
+ * "实验设置"), 64 or 256; MHA and GQA; an e4m3 forward at head dim 128.
  *
  *   S = scale * Q K^T,  P = row softmax over the allowed keys,  O = P V,
  *   LSE_i = ln sum_{j allowed} exp(S_ij)   (-inf for a row that allows nothing)
@@ -68,8 +68,8 @@ typedef struct lcattn_shape {
   int64_t Sk;   /* key length                                               */
   int64_t Hq;   /* query heads                                              */
   int64_t Hkv;  /* key/value heads; Hq % Hkv == 0                          */
-  int64_t D;    /* head dim: 128, 64 or 256 (256: forward only; block
-                 * selection: 128 only)                                     */
+  int64_t D;    /* head dim: 128, 64 or 256 (256: no deterministic
+                 * backward; block selection and fp8: 128 only)             */
   /* element strides of (batch, sequence, head); the head dim is contiguous.
    * dO and dQ use q_stride's layout rules with o_stride / q_stride:
    *   O and dO share o_stride, Q and dQ share q_stride,
@@ -280,12 +280,13 @@ int lcattn_fwd_ws(const lcattn_shape* shape, const void* q, const void* k, const
  * multiples of 16; 16-byte aligned); the real inputs are code * q_scale,
  * code * k_scale, code * v_scale (per-tensor factors > 0).  Head dim 128 only
  * (LCATTN_ERR_UNSUPPORTED otherwise).  Computes, per query row, with exact
- * fp32 logits scale * q_scale * k_scale * <q8, k8> and their exact running
- * max m: P = exp(logit - m) quantized to e4m3 as P * 256 for the P V product
- * (fp32 accumulation in tensor memory), l = sum of the unquantized P, and
- * writes o (bf16, o_stride, [B][Sq][Hq][128]) = v_scale * (P8 V8) / (256 l)
- * and lse = m + ln l (fp32 [B][Hq][Sq]; -inf and O = 0 for rows that allow
- * nothing).  `tile_meta` from lcattn_mask_compile on the same shape and mask.
+ * fp32 logits scale * q_scale * k_scale * <q8, k8> and a running reference
+ * m that moves to the row max whenever the max exceeds it by more than 4 (log2
+ * units), so P = exp(logit - m) <= 16: P is quantized to e4m3 as 16 P for the
+ * P V product (fp32 accumulation in tensor memory), l = sum of the
+ * unquantized P, and o (bf16, o_stride, [B][Sq][Hq][128]) =
+ * v_scale * (P8 V8) / (16 l) and lse = m + ln l are written (fp32
+ * [B][Hq][Sq]; -inf and O = 0 for rows that allow nothing).  `tile_meta` from lcattn_mask_compile on the same shape and mask.
  * The workspace (lcattn_fwd_fp8_workspace_size bytes, 16-byte aligned) receives
  * V^T [B][Hkv][128][Skp] (e4m3, Skp = Sk rounded up to 16), written by a first
  * kernel so that both operands of the P V product are K-major; the forward
@@ -299,14 +300,17 @@ int lcattn_fwd_fp8(const lcattn_shape* shape, const void* q, const void* k, cons
 /* The backward calls below compute the gradients of the same operator (blog
  * sections "密集注意力内核" / "稀疏注意力内核"; the pages' sparse-kernel findings,
  * sections "稀疏内核性能" and "核心发现总结", single the backward out as the main
- * bottleneck).  They take head dim 64 or 128; head dim 256 returns
- * LCATTN_ERR_UNSUPPORTED (its dK and dV accumulators, 2 x 256 fp32 columns,
- * do not fit in tensor memory beside S and dP) and its workspace size is 0.
+ * bottleneck).  They take head dim 64, 128 or 256; at 256 each dK/dV unit is
+ * two CTAs, one per half of the head dim (the dK and dV accumulators of a
+ * whole 128-key tile, 2 x 256 fp32 columns, do not fit in tensor memory beside
+ * S and dP), and the deterministic backward returns LCATTN_ERR_UNSUPPORTED
+ * with a workspace size of 0.
  *
  * Workspace (device bytes) lcattn_bwd needs: D = rowsum(dO * O) fp32
  * [B][Hq][Sq], the fp32 dQ accumulator [B][Hq][Sq][D] (head-major) and, when the dK/dV
- * work units (key tiles x KV heads x batch) are too few to fill the GPU in
- * several waves -- under 1216, and the GQA group splits evenly -- fp32 dK/dV
+ * work units (key tiles x KV heads x batch, times 2 at head dim 256) are too
+ * few to fill the GPU in several waves -- under 1216, and the GQA group splits
+ * evenly -- fp32 dK/dV
  * partials [2 or 4][2][B][Sk][Hkv][D]: each unit is split over 2 or 4
  * shares of its group's query heads and the partials are summed into dK, dV. */
 size_t lcattn_bwd_workspace_size(const lcattn_shape* shape);

@@ -214,7 +214,8 @@ int validate_fp8(const lcattn_shape* s) {
 // the shares' fp32 partials are summed afterwards.  Depends on the shape only,
 // so the workspace size does too.
 int bwd_parts(const lcattn_shape* s, int64_t nchunks = 1) {
-  const int64_t units = (s->Sk + kBN - 1) / kBN * s->Hkv * s->B * nchunks;
+  // (At head dim 256 every unit is two CTAs, one per half of the head dim.)
+  const int64_t units = (s->Sk + kBN - 1) / kBN * s->Hkv * s->B * nchunks * (s->D == 256 ? 2 : 1);
   const int64_t G = s->Hq / s->Hkv;
   if (units < 304 && G % 4 == 0) return 4;
   if (units < 1216 && G % 2 == 0) return 2;
@@ -460,7 +461,7 @@ int lcattn_fwd_fp8(const lcattn_shape* shape, const void* q, const void* k, cons
 }
 
 size_t lcattn_bwd_workspace_size(const lcattn_shape* shape) {
-  if (validate_shape(shape) != LCATTN_OK || shape->D > 128) return 0;
+  if (validate_shape(shape) != LCATTN_OK) return 0;
   return (size_t)bwd_ws_bytes(shape, bwd_parts(shape), true);
 }
 
@@ -485,7 +486,7 @@ int bwd_run(unsigned stages, const lcattn_shape* shape, const void* q, const voi
   lcattn_tile_meta_layout L;
   int st = layout_of(shape, mask, &L);
   if (st) return st;
-  if (shape->D > 128) return LCATTN_ERR_UNSUPPORTED;  // head dim 256: forward only
+  if (shape->D > 128 && deterministic) return LCATTN_ERR_UNSUPPORTED;  // no dQ kernel at head dim 256
   if (acc.on()) {
     if (!acc.dk || !acc.dv) return LCATTN_ERR_INVALID_ARG;
     // The outputs are the accumulators; the bf16 pointers are not used.
@@ -610,7 +611,7 @@ int lcattn_bwd_deterministic(const lcattn_shape* shape, const void* q, const voi
 }
 
 size_t lcattn_bwd_accum_workspace_size(const lcattn_shape* shape) {
-  if (validate_shape(shape) != LCATTN_OK || shape->D > 128) return 0;
+  if (validate_shape(shape) != LCATTN_OK) return 0;
   return (size_t)align_up(4 * shape->B * shape->Hq * shape->Sq, 256);
 }
 
@@ -751,7 +752,6 @@ int lcattn_bwd_noalloc(const lcattn_shape* shape, const void* q, const void* k, 
                        lcattn_stream_t stream) {
   int st = validate_shape(shape);
   if (st) return st;
-  if (shape->D > 128) return LCATTN_ERR_UNSUPPORTED;  // head dim 256: forward only
   // No split here: the fixed array holds D and the dQ accumulator only.
   const int64_t need = bwd_ws_bytes(shape, 1, false);
   if (need > (int64_t)LCATTN_NOALLOC_SCRATCH_BYTES) return LCATTN_ERR_SCRATCH_LIMIT;

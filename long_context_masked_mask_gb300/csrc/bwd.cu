@@ -185,6 +185,30 @@ struct BwdSmem {
   int abort_flag;
 };
 
+// Head dim 256: a unit is (key tile, KV head, head-dim half hd).  S^T and dP^T
+// need the whole head dim, so K and V stay resident (64 KB each) and the Q and
+// dO tiles stream through a 2-stage ring of 128-column halves (32 KB); the
+// unit's own half of a Q or dO tile is loaded a second time for dK and dV, so
+// that the ring is consumed strictly in order.  TMEM is laid out as at
+// D = 128: dV and dK of the own half take 128 columns each.  227 KB in all.
+template <>
+struct BwdSmem<256> {
+  alignas(1024) uint8_t k[4 * kHalfBytes];
+  alignas(1024) uint8_t v[4 * kHalfBytes];
+  alignas(1024) uint8_t ring[2][2 * kHalfBytes];
+  alignas(1024) uint8_t ds[2 * kHalfBytes];
+  alignas(16) float lse2[2][128];
+  alignas(16) float dvec_s[2][128];
+  uint64_t kv_full;
+  uint64_t q_full[2];   // LSE / D rows of an item (32 producer lanes)
+  uint64_t q_empty[2];
+  uint64_t r_full[2], r_empty[2];
+  uint64_t s_full, dp_full, p_ready, ds_ready, dq_full, dq_free, done;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+static_assert(sizeof(BwdSmem<256>) <= 232448, "head dim 256: shared memory");
+
 struct BwdKernelArgs {
   BwdArgs a;
 };
@@ -268,6 +292,8 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
             const __grid_constant__ BwdKernelArgs ka) {
   constexpr int kTileBytes = BwdGeom<D>::kTileBytes;
   constexpr int kBoxes = BwdGeom<D>::kBoxes;
+  static_assert(D != 256 || kDq, "head dim 256 has no separate dQ kernel");
+  constexpr int kOut = D == 256 ? 128 : D;  // head-dim columns of dK / dV / dQ this unit owns
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const BwdArgs& a = ka.a;
   const ProblemDev& pr = a.pr;
@@ -287,18 +313,28 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
   const int g = blockIdx.y;
   // Longest key tiles first.  With per-head lists the order of the group's
   // first head is used.  With a split, the parts of one key tile (shares of
-  // the group's query heads) are adjacent CTAs.
+  // the group's query heads) are adjacent CTAs; at D = 256 the two head-dim
+  // halves of a unit are adjacent too.
+  const int hd = D == 256 ? (int)(blockIdx.x & 1u) : 0;
+  const int col0 = hd * 128;  // first head-dim column this unit owns
+  const int ux = D == 256 ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
   const int parts = a.parts;
-  const int part = (int)(blockIdx.x % parts);
+  const int part = ux % parts;
   const int h_lo = part * pr.G / parts, h_hi = (part + 1) * pr.G / parts;
   const int lh0 = a.meta.nH == 1 ? 0 : g * pr.G;
-  const int kt = __ldg(a.meta.bwd_ord + ((int64_t)b * a.meta.nH + lh0) * a.meta.nKt + blockIdx.x / parts);
+  const int kt = __ldg(a.meta.bwd_ord + ((int64_t)b * a.meta.nH + lh0) * a.meta.nKt + ux / parts);
 
   if (tid == 0) {
     mbar_init(&sm.kv_full, 1);
     for (int s = 0; s < 2; ++s) {
-      mbar_init(&sm.q_full[s], 33);
+      mbar_init(&sm.q_full[s], D == 256 ? 32 : 33);  // (+ the expect-tx arrival of the Q/dO tiles)
       mbar_init(&sm.q_empty[s], 1);
+    }
+    if constexpr (D == 256) {
+      for (int s = 0; s < 2; ++s) {
+        mbar_init(&sm.r_full[s], 1);
+        mbar_init(&sm.r_empty[s], 1);
+      }
     }
     mbar_init(&sm.s_full, 1);
     mbar_init(&sm.dp_full, 1);
@@ -344,6 +380,75 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
     }
     ItemIter<kChunked> it;
     it.init(a.meta, b, kt, pr.G, g, h_lo, h_hi, qlo, qhi);
+    // LSE / D rows of item i (query tile qt of head h) into row slot i & 1, stored
+    // negated: -(LSE*log2(e) - log2(scale)) (-inf for a fully masked row: P = 0) and -D.
+    auto stage_rows = [&](int st, int h, int qt) {
+      const float log2_scale = log2f(a.scale);
+      const float* lse = a.lse + ((int64_t)b * pr.Hq + h) * pr.Sq;
+      const float* dv = a.dvec + ((int64_t)b * pr.Hq + h) * pr.Sq;
+      #pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int c = lane * 4 + k;
+        const int q = qt * kBM + c;
+        float l2 = -INFINITY, d = 0.f;
+        if (q < pr.Sq) {
+          const float l = __ldg(lse + q);
+          l2 = (l == -INFINITY) ? -INFINITY : log2_scale - l * kLog2e;
+          d = __ldg(dv + q);
+        }
+        sm.lse2[st][c] = l2;
+        sm.dvec_s[st][c] = -d;
+      }
+    };
+    if constexpr (D == 256) {
+      // Ring entries in the MMA warp's order: Q(0) and dO(0) (both halves),
+      // then per item i: the own half of dO(i) (dV), Q(i+1) (S^T), the own half
+      // of Q(i) (dK), dO(i+1) (dP^T).
+      int t = 0;  // ring entries issued
+      auto load_half = [&](const CUtensorMap* tm, int h, int qt, int half) -> bool {
+        const int stg = t & 1, use = t >> 1;
+        if (use > 0) {
+          const bool w = mbar_wait(&sm.r_empty[stg], (use - 1) & 1, abort_flag, gstatus, TO);
+          if (!__all_sync(0xffffffffu, w)) return false;
+        }
+        mbar_expect_tx_e(&sm.r_full[stg], 2 * kHalfBytes);
+        tma_load_4d_e(sm.ring[stg], tm, &sm.r_full[stg], 128 * half, h, qt * kBM, b);
+        tma_load_4d_e(sm.ring[stg] + kHalfBytes, tm, &sm.r_full[stg], 128 * half + 64, h, qt * kBM, b);
+        ++t;
+        return true;
+      };
+      auto load_rows = [&](int i, int h, int qt) -> bool {
+        const int st = i & 1, use = i >> 1;
+        if (use > 0) {
+          const bool w = mbar_wait(&sm.q_empty[st], (use - 1) & 1, abort_flag, gstatus, TO);
+          if (!__all_sync(0xffffffffu, w)) return false;
+        }
+        stage_rows(st, h, qt);
+        mbar_arrive(&sm.q_full[st]);
+        return true;
+      };
+      if (it.valid()) {
+        int h = it.head(), qt = it.entry() >> 1;
+        bool ok = load_rows(0, h, qt) && load_half(&tmQ, h, qt, 0) && load_half(&tmQ, h, qt, 1) &&
+                  load_half(&tmdO, h, qt, 0) && load_half(&tmdO, h, qt, 1);
+        for (int i = 0; ok; ++i) {
+          it.next();
+          const bool more = it.valid();
+          const int h2 = more ? it.head() : 0, qt2 = more ? it.entry() >> 1 : 0;
+          ok = load_half(&tmdO, h, qt, hd);
+          if (ok && more) ok = load_rows(i + 1, h2, qt2) && load_half(&tmQ, h2, qt2, 0) && load_half(&tmQ, h2, qt2, 1);
+          if (ok) ok = load_half(&tmQ, h, qt, hd);
+          if (ok && more) ok = load_half(&tmdO, h2, qt2, 0) && load_half(&tmdO, h2, qt2, 1);
+          if (!more) break;
+          h = h2;
+          qt = qt2;
+        }
+      }
+      // Never leave copies in flight (bounded waits that ignore the abort word).
+      int dummy = 0;
+      for (int u = max(0, t - 2); u < t; ++u) mbar_wait(&sm.r_full[u & 1], (u >> 1) & 1, &dummy, gstatus, TO);
+      mbar_wait(&sm.kv_full, 0, &dummy, gstatus, TO);
+    } else {
     int i = 0, issued = 0;
     for (; it.valid(); it.next(), ++i) {
       const int st = i & 1, use = i >> 1;
@@ -358,22 +463,7 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
         tma_load_4d_e(sm.q[st] + bx * kHalfBytes, &tmQ, &sm.q_full[st], 64 * bx, h, qt * kBM, b);
         tma_load_4d_e(sm.dO[st] + bx * kHalfBytes, &tmdO, &sm.q_full[st], 64 * bx, h, qt * kBM, b);
       }
-      const float log2_scale = log2f(a.scale);
-      const float* lse = a.lse + ((int64_t)b * pr.Hq + h) * pr.Sq;
-      const float* dv = a.dvec + ((int64_t)b * pr.Hq + h) * pr.Sq;
-      #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const int c = lane * 4 + k;
-        const int q = qt * kBM + c;
-        float l2 = -INFINITY, d = 0.f;
-        if (q < pr.Sq) {
-          const float l = __ldg(lse + q);
-          l2 = (l == -INFINITY) ? -INFINITY : log2_scale - l * kLog2e;  // fully masked row: P = 0
-          d = __ldg(dv + q);
-        }
-        sm.lse2[st][c] = l2;
-        sm.dvec_s[st][c] = -d;
-      }
+      stage_rows(st, h, qt);
       mbar_arrive(&sm.q_full[st]);
       issued = i + 1;
     }
@@ -383,6 +473,7 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
         mbar_wait(&sm.q_full[t & 1], (t >> 1) & 1, &dummy, gstatus, TO);
       mbar_wait(&sm.kv_full, 0, &dummy, gstatus, TO);
     }
+    }
   } else if (warp == 13) {
     // ------------------------------------------------------------ MMA issuer
     // Per item i: wait P'(i) | dV(i) | S^T(i+1) | wait dS(i) | dK(i) | dQ^T(i) |
@@ -390,6 +481,104 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
     // while dS(i) is still being formed, and P'(i+1) starts right after.  The
     // whole warp runs the loop; each tcgen05.mma / commit is issued by one
     // elected lane.
+    if constexpr (D == 256) {
+      // Head dim 256: the same order, with S^T / dP^T over both halves of the
+      // head dim (two ring entries each) and dV / dK / dQ^T over the own half.
+      const uint32_t id_kmaj = idesc_bf16_f32(128, 128, false, false);
+      const uint32_t id_ts = idesc_bf16_f32(128, 128, false, true);
+      const uint32_t id_mn = idesc_bf16_f32(128, 128, true, true);
+      const uint32_t tS = tmem, tP = tmem + 128, tdV = tmem + 256, tdK = tmem + 384;
+      const uint64_t dK_k = sdesc_sw128(smem_u32(sm.k), 16, 1024);
+      const uint64_t dV_k = sdesc_sw128(smem_u32(sm.v), 16, 1024);
+      const uint64_t dK_mn = sdesc_sw128(smem_u32(sm.k + hd * 2 * kHalfBytes), kHalfBytes, 1024);
+      const uint64_t r_k = sdesc_sw128(smem_u32(sm.ring[0]), 16, 1024);
+      const uint64_t r_mn = sdesc_sw128(smem_u32(sm.ring[0]), kHalfBytes, 1024);
+      const uint64_t dS_mn = sdesc_sw128(smem_u32(sm.ds), kHalfBytes, 1024);
+      bool ok = __all_sync(0xffffffffu, mbar_wait(&sm.kv_full, 0, abort_flag, gstatus, TO));
+      ItemIter<kChunked> it;
+      it.init(a.meta, b, kt, pr.G, g, h_lo, h_hi, qlo, qhi);
+      int t = 0;  // ring entries consumed
+      // Waits for ring entry t; its stage, or -1 when the wait gave up.
+      auto take = [&]() -> int {
+        const int stg = t & 1;
+        const bool w = mbar_wait(&sm.r_full[stg], (t >> 1) & 1, abort_flag, gstatus, TO);
+        if (!__all_sync(0xffffffffu, w)) return -1;
+        tc_fence_after();
+        return stg;
+      };
+      // d = A B^T over the whole head dim: A = K or V (resident, K-major), B =
+      // the two halves of a Q or dO tile (ring entries, K-major).
+      auto full_prod = [&](uint32_t d, uint64_t a_base) -> bool {
+        for (int half = 0; half < 2; ++half) {
+          const int stg = take();
+          if (stg < 0) return false;
+          const uint64_t a0 = sdesc_add(a_base, half * 2 * kHalfBytes);
+          const uint64_t b0 = sdesc_add(r_k, stg * 2 * kHalfBytes);
+          if (half == 0) mma_ss_e<0>(d, a0, b0, id_kmaj);
+          else mma_ss_e<1>(d, a0, b0, id_kmaj);
+          #pragma unroll
+          for (int kk = 1; kk < 8; ++kk) {
+            const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
+            mma_ss_e<1>(d, sdesc_add(a0, off), sdesc_add(b0, off), id_kmaj);
+          }
+          tc_commit_e(&sm.r_empty[stg]);
+          ++t;
+        }
+        return true;
+      };
+      // d (+)= A B: A = P'^T or dS^T from TMEM, B = the own half of dO or Q (MN-major).
+      auto half_prod = [&](uint32_t d, uint32_t a_tm, uint32_t acc) -> bool {
+        const int stg = take();
+        if (stg < 0) return false;
+        const uint64_t b0 = sdesc_add(r_mn, stg * 2 * kHalfBytes);
+        mma_ts_er(d, a_tm, b0, id_ts, acc);
+        #pragma unroll
+        for (int kk = 1; kk < 8; ++kk)
+          mma_ts_e<1>(d, a_tm + (kk >> 2) * 64 + (kk & 3) * 8, sdesc_add(b0, kk * 2048), id_ts);
+        tc_commit_e(&sm.r_empty[stg]);
+        ++t;
+        return true;
+      };
+      if (ok && it.valid()) {
+        ok = full_prod(tS, dK_k);  // S^T(0)
+        if (ok) tc_commit_e(&sm.s_full);
+        if (ok) ok = full_prod(tP, dV_k);  // dP^T(0)
+        if (ok) tc_commit_e(&sm.dp_full);
+      }
+      for (int i = 0; ok && it.valid(); ++i) {
+        ok = __all_sync(0xffffffffu, mbar_wait(&sm.p_ready, i & 1, abort_flag, gstatus, TO));
+        if (!ok) break;
+        tc_fence_after();
+        if (!(ok = half_prod(tdV, tS, i > 0 ? 1u : 0u))) break;  // dV(i)
+        it.next();
+        const bool more = it.valid();
+        if (more) {
+          if (!(ok = full_prod(tS, dK_k))) break;  // S^T(i+1)
+          tc_commit_e(&sm.s_full);
+        }
+        ok = __all_sync(0xffffffffu, mbar_wait(&sm.ds_ready, i & 1, abort_flag, gstatus, TO));
+        if (!ok) break;
+        tc_fence_after();
+        if (!(ok = half_prod(tdK, tP, i > 0 ? 1u : 0u))) break;  // dK(i)
+        tc_commit_e(&sm.q_empty[i & 1]);  // LSE(i), D(i) are read for good
+        // dQ^T (own half) = K_half^T dS^T into [128, 256).
+        mma_ss_e<0>(tP, dK_mn, dS_mn, id_mn);
+        #pragma unroll
+        for (int kk = 1; kk < 8; ++kk)
+          mma_ss_e<1>(tP, sdesc_add(dK_mn, kk * 2048), sdesc_add(dS_mn, kk * 2048), id_mn);
+        tc_commit_e(&sm.dq_full);
+        if (more) {
+          ok = __all_sync(0xffffffffu, mbar_wait(&sm.dq_free, i & 1, abort_flag, gstatus, TO));
+          if (!ok) break;
+          tc_fence_after();
+          if (!(ok = full_prod(tP, dV_k))) break;  // dP^T(i+1)
+          tc_commit_e(&sm.dp_full);
+        }
+      }
+      tc_commit_e(&sm.done);
+      int dummy = 0;
+      mbar_wait(&sm.done, 0, &dummy, gstatus, TO);
+    } else
     {
       const uint32_t id_kmaj = idesc_bf16_f32(128, 128, false, false);
       const uint32_t id_ts = idesc_bf16_f32(128, D, false, true);
@@ -522,7 +711,7 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
       mbar_arrive(&sm.dq_free);  // columns [128, 256) may take dP^T(i+1) now
       const int q0 = qt * kBM;
       const int nq = min(kBM, pr.Sq - q0);
-      float* dst = a.dq_acc + (int64_t)b * a.dqa_sb + (int64_t)q0 * a.dqa_ss + (int64_t)h * a.dqa_sh + r;
+      float* dst = a.dq_acc + (int64_t)b * a.dqa_sb + (int64_t)q0 * a.dqa_ss + (int64_t)h * a.dqa_sh + col0 + r;
       if (nq == kBM) {
         #pragma unroll
         for (int c = 0; c < 128; ++c) atomicAdd(dst + c * dq_row_stride, __uint_as_float(d[c]));
@@ -700,15 +889,15 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
       }
       const float mul = x == 0 ? 1.f / a.scale : 1.f;
       const uint32_t tacc = tmem + lane_off + (x == 0 ? 256 : 384);
-      // Split units write fp32 partials [part][dV, dK][B][Sk][Hkv][128]; a
+      // Split units write fp32 partials [part][dV, dK][B][Sk][Hkv][D]; a
       // reduction kernel sums the parts into the bf16 outputs.
-      float* pdst = a.dkv_part + (((((int64_t)part * 2 + x) * pr.B + b) * pr.Sk + key) * pr.Hkv + g) * D;
+      float* pdst = a.dkv_part + (((((int64_t)part * 2 + x) * pr.B + b) * pr.Sk + key) * pr.Hkv + g) * D + col0;
       __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(x == 0 ? a.dv : a.dk) +
                            (int64_t)b * (x == 0 ? a.v_sb : a.k_sb) +
                            (int64_t)key * (x == 0 ? a.v_ss : a.k_ss) +
                            (int64_t)g * (x == 0 ? a.v_sh : a.k_sh);
       #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
+      for (int c = 0; c < kOut / 32; ++c) {
         uint32_t xr[32];
         if (have) {
           tmem_ld32(tacc + c * 32, xr);
@@ -718,7 +907,7 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
           for (int k = 0; k < 32; ++k) xr[k] = 0u;
         }
         if (key_ok && red_out) {
-          float* adst = (x == 0 ? a.dv_acc : a.dk_acc) + (((int64_t)b * pr.Sk + key) * pr.Hkv + g) * D + c * 32;
+          float* adst = (x == 0 ? a.dv_acc : a.dk_acc) + (((int64_t)b * pr.Sk + key) * pr.Hkv + g) * D + col0 + c * 32;
           #pragma unroll
           for (int u = 0; u < 8; ++u)
             red_add_v4(adst + 4 * u, __uint_as_float(xr[4 * u]) * mul, __uint_as_float(xr[4 * u + 1]) * mul,
@@ -730,7 +919,7 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
             p4[u] = make_float4(__uint_as_float(xr[4 * u]) * mul, __uint_as_float(xr[4 * u + 1]) * mul,
                                 __uint_as_float(xr[4 * u + 2]) * mul, __uint_as_float(xr[4 * u + 3]) * mul);
         } else if (key_ok) {
-          uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
+          uint4* d4 = reinterpret_cast<uint4*>(dst + col0 + c * 32);
           #pragma unroll
           for (int u = 0; u < 4; ++u)
             d4[u] = make_uint4(
@@ -765,7 +954,7 @@ cudaError_t launch_dkdv_dc(const CUtensorMap& tq, const CUtensorMap& tk, const C
   }
   BwdKernelArgs ka;
   ka.a = a;
-  dim3 grid(a.meta.nKt * a.parts, a.pr.Hkv, a.pr.B * a.nchunks);
+  dim3 grid(a.meta.nKt * a.parts * (D == 256 ? 2 : 1), a.pr.Hkv, a.pr.B * a.nchunks);
   dkdv_kernel<D, kChunked, kDq><<<grid, kThreadsDkdv, smem, st>>>(tq, tk, tv, tdo, ka);
   return cudaGetLastError();
 }
@@ -774,7 +963,11 @@ template <int D>
 cudaError_t launch_dkdv_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                           const CUtensorMap& tdo, const BwdArgs& a, cudaStream_t st) {
   cudaError_t e;
-  if (a.dq_sep)
+  if constexpr (D == 256) {
+    if (a.dq_sep) return cudaErrorInvalidValue;  // no dQ kernel at D = 256
+    e = a.nchunks > 1 ? launch_dkdv_dc<D, true, true>(tq, tk, tv, tdo, a, st)
+                      : launch_dkdv_dc<D, false, true>(tq, tk, tv, tdo, a, st);
+  } else if (a.dq_sep)
     e = a.nchunks > 1 ? launch_dkdv_dc<D, true, false>(tq, tk, tv, tdo, a, st)
                       : launch_dkdv_dc<D, false, false>(tq, tk, tv, tdo, a, st);
   else
@@ -803,14 +996,16 @@ cudaError_t launch_bwd_prepass(const BwdArgs& a, cudaStream_t st) {
   int64_t blocks = (rows + 7) / 8;
   if (blocks > (int64_t)nsm * 32) blocks = (int64_t)nsm * 32;
   if (a.pr.D == 64) prepass_kernel<64><<<(unsigned)blocks, 256, 0, st>>>(a);
+  else if (a.pr.D == 256) prepass_kernel<256><<<(unsigned)blocks, 256, 0, st>>>(a);
   else prepass_kernel<128><<<(unsigned)blocks, 256, 0, st>>>(a);
   return cudaGetLastError();
 }
 
 cudaError_t launch_bwd_dkdv(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             const CUtensorMap& tdo, const BwdArgs& a, cudaStream_t st) {
-  return a.pr.D == 64 ? launch_dkdv_d<64>(tq, tk, tv, tdo, a, st)
-                      : launch_dkdv_d<128>(tq, tk, tv, tdo, a, st);
+  if (a.pr.D == 64) return launch_dkdv_d<64>(tq, tk, tv, tdo, a, st);
+  if (a.pr.D == 256) return launch_dkdv_d<256>(tq, tk, tv, tdo, a, st);
+  return launch_dkdv_d<128>(tq, tk, tv, tdo, a, st);
 }
 
 cudaError_t launch_bwd_dq_convert(const BwdArgs& a, cudaStream_t st) {
@@ -821,6 +1016,7 @@ cudaError_t launch_bwd_dq_convert(const BwdArgs& a, cudaStream_t st) {
   int64_t blocks = (nvec + 255) / 256;
   if (blocks > (int64_t)nsm * 32) blocks = (int64_t)nsm * 32;
   if (a.pr.D == 64) dq_convert_kernel<64><<<(unsigned)blocks, 256, 0, st>>>(a);
+  else if (a.pr.D == 256) dq_convert_kernel<256><<<(unsigned)blocks, 256, 0, st>>>(a);
   else dq_convert_kernel<128><<<(unsigned)blocks, 256, 0, st>>>(a);
   return cudaGetLastError();
 }

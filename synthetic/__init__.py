@@ -271,8 +271,8 @@ def workload(name: str, seed: int = 0) -> Workload:
       :func:`qkv_fp8`), forward only.
     * ``dense_8k_hd64``: as ``dense_8k`` with head dim 64 (the variant next to the
       pages' 128).
-    * ``dense_8k_hd256_fwd``: B=1, N=8192, GQA 32:8, head dim 256, FULL and CAUSAL,
-      forward only (the head dim whose backward is not built).
+    * ``dense_8k_hd256``: B=1, N=8192, GQA 32:8, head dim 256, FULL and CAUSAL.
+    * ``dense_8k_hd256_fwd``: the same, forward only.
     * ``decode_32k``: B=8 sequences of one query row each against N=32768 keys,
       GQA 64:8, CAUSAL (bottom-right aligned: the row sees every key), forward only.
     * ``dynamic_32k``: B=1, N=32768, GQA 64:8, block-structured Q/K (strength 1.5),
@@ -319,6 +319,8 @@ def workload(name: str, seed: int = 0) -> Workload:
                         fp8=True)
     if name == "dense_8k_hd64":
         return Workload(name, 1, 8192, 64, 8, 64, [MaskSpec("FULL"), MaskSpec("CAUSAL")])
+    if name == "dense_8k_hd256":
+        return Workload(name, 1, 8192, 32, 8, 256, [MaskSpec("FULL"), MaskSpec("CAUSAL")])
     if name == "dense_8k_hd256_fwd":
         return Workload(name, 1, 8192, 32, 8, 256, [MaskSpec("FULL"), MaskSpec("CAUSAL")], forward_only=True)
     if name == "decode_32k":
@@ -333,4 +335,4 @@ def workload(name: str, seed: int = 0) -> Workload:
 
 WORKLOADS = ("causal_1k", "dense_8k", "docs_32k", "hetero_16k", "long_128k", "long_128k_8to1", "dynamic_32k",
              "decode_32k", "dense_8k_fp8",
-             "dense_8k_hd64", "dense_8k_hd256_fwd")
+             "dense_8k_hd64", "dense_8k_hd256", "dense_8k_hd256_fwd")

@@ -225,7 +225,10 @@ def test_head_dim_64_is_accepted():
                                             None, 0x1000, 1 << 30, None) == lc.LCATTN_ERR_UNSUPPORTED
 
 
-def test_head_dim_256_is_forward_only():
+def test_head_dim_256_backward_sizes_and_refusals():
+    """Head dim 256: the backward's workspace counts the units twice (one CTA
+    per head-dim half) when choosing head-share splits; the deterministic
+    backward refuses it before touching the device."""
     s = _shape(D=256)
     for name, H in (("q_stride", 4), ("k_stride", 2), ("v_stride", 2), ("o_stride", 4)):
         getattr(s, name)[:] = (256 * H * 256, H * 256, 256)
@@ -233,13 +236,13 @@ def test_head_dim_256_is_forward_only():
     st, L = _layout(s, d)
     assert st == 0
     lib = lc.library()
-    assert lib.lcattn_bwd_workspace_size(ctypes.byref(s)) == 0
+    # D [1][4][256] fp32 + dQ accumulator [1][4][256][256] fp32 + 2 head shares of
+    # fp32 dK/dV partials [2][1][256][2][256] (2 key tiles x 2 KV heads x 2 halves = 8 units).
+    assert lib.lcattn_bwd_workspace_size(ctypes.byref(s)) == 4 * 4 * 256 + 4 * 256 * 4 * 256 + 2 * 2 * 4 * 256 * 2 * 256
+    assert lib.lcattn_bwd_deterministic_workspace_size(ctypes.byref(s)) == 0
     P = 0x1000
     args = (ctypes.byref(s), P, P, P, P, P, P, P, ctypes.byref(d), 0.1, P, P, P)
-    assert lib.lcattn_bwd(*args, P, 1 << 30, None) == lc.LCATTN_ERR_UNSUPPORTED
-    assert lib.lcattn_bwd_noalloc(*args, None) == lc.LCATTN_ERR_UNSUPPORTED
-    for stage in (1, 2, 3):
-        assert lib.lcattn_bwd_stage(stage, *args, P, 1 << 30, None) == lc.LCATTN_ERR_UNSUPPORTED
+    assert lib.lcattn_bwd_deterministic(*args, P, 1 << 30, None) == lc.LCATTN_ERR_UNSUPPORTED
     s.D = 512
     assert _layout(s, d)[0] == lc.LCATTN_ERR_UNSUPPORTED
 

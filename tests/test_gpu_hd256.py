@@ -1,7 +1,9 @@
-"""Head dim 256, forward only (its backward does not fit in tensor memory and
-returns LCATTN_ERR_UNSUPPORTED): O and LSE through the C ABI against the fp64
-oracle with the bars of the 128 case, on both descriptor kinds, MHA and GQA,
-ragged lengths, and the split-KV forward for decode-style rows."""
+"""Head dim 256: forward (O, LSE) and backward (dQ, dK, dV) through the C ABI
+against the fp64 oracle with the bars of the 128 case, on both descriptor
+kinds, MHA and GQA, ragged lengths, the split-KV forward for decode-style
+rows, and the backward's dK/dV units that run as two CTAs (one per half of the
+head dim) with split and unsplit head shares, the allocation-free and the
+accumulate entry points; the deterministic backward refuses head dim 256."""
 import math
 
 import numpy as np
@@ -10,7 +12,7 @@ import torch
 
 import oracle
 from synthetic import MaskSpec, qkv
-from test_gpu_parity import relf, spec_for
+from test_gpu_parity import relf, run_and_compare, spec_for
 
 pytestmark = pytest.mark.gpu
 
@@ -61,11 +63,50 @@ def test_hd256_split_forward(B, Sq, Sk, Hq, Hkv):
     forward_and_check(MaskSpec("CAUSAL"), B, Sq, Sk, Hq, Hkv, seed=7, expect_split=True)
 
 
-def test_hd256_backward_is_refused():
-    dev, mask, meta, o, lse = forward_and_check(MaskSpec("FULL"), 1, 256, 256, 2, 1, seed=9)
+@pytest.mark.parametrize("kind", ["FULL", "CAUSAL", "CAUSAL_DOCUMENT", "CAUSAL_SLIDING_WINDOW",
+                                  "PREFIX_LM_CAUSAL", "SHARED_QUESTION", "UNIFORM_BLOCK", "VARIABLE_BLOCK"])
+def test_hd256_backward_families(kind):
+    """GQA 4:2, N = 392 (a ragged last tile): split head shares (units are few)."""
+    N, Hq, Hkv = 392, 4, 2
+    run_and_compare(spec_for(kind, N, Hq), 1, N, Hq, Hkv, seed=21, D=D)
+
+
+@pytest.mark.parametrize("B,N,Hq,Hkv,kind", [(2, 300, 3, 3, "CAUSAL"), (1, 1100, 6, 1, "FULL_DOCUMENT"),
+                                             (1, 129, 2, 2, "GLOBAL_SLIDING")])
+def test_hd256_backward_batch_mha_mqa(B, N, Hq, Hkv, kind):
+    run_and_compare(spec_for(kind, N, Hq), B, N, Hq, Hkv, seed=22, D=D)
+
+
+def test_hd256_backward_unsplit_long_lists():
+    """2048 tokens, GQA 3:1 (a group that does not split evenly: no partials),
+    16 query tiles per unit, so the half-tile ring wraps many times."""
+    run_and_compare(spec_for("CAUSAL", 2048, 3), 1, 2048, 3, 1, seed=23, check_classes=False, D=D)
+
+
+def test_hd256_noalloc_and_accumulate_match_oracle():
+    """lcattn_bwd_noalloc and lcattn_bwd_accum (fp32 accumulators that start at
+    zero) at head dim 256 against the oracle; the deterministic backward refuses."""
+    B, N, Hq, Hkv = 1, 520, 4, 2
+    spec = MaskSpec("CAUSAL")
+    x = qkv(B, N, Hq, Hkv, D, seed=24)
+    dev = {n: t.cuda() for n, t in x.items()}
+    out = lc.attention(dev["q"], dev["k"], dev["v"], spec)
+    mask, meta = out["mask"], out["tile_meta"]
+    dq, dk, dv = lc.lcattn_bwd_noalloc(dev["q"], dev["k"], dev["v"], out["o"], dev["do"], out["lse"], mask, meta)
+    acc = {n: torch.zeros(t.shape, dtype=torch.float32, device="cuda") for n, t in
+           (("dq", dev["q"]), ("dk", dev["k"]), ("dv", dev["v"]))}
+    lc.lcattn_bwd_accum(dev["q"], dev["k"], dev["v"], out["o"], dev["do"], out["lse"], mask, meta,
+                        acc["dq"], acc["dk"], acc["dv"])
+    torch.cuda.synchronize()
+    assert lc.lcattn_read_status(meta) == 0
+    f64 = {n: t.double().numpy() for n, t in x.items()}
+    dQ, dK, dV, _, _ = oracle.attention_bwd(f64["q"], f64["k"], f64["v"], f64["do"], spec, 1.0 / math.sqrt(D))
+    for got in ((dq, dk, dv), (acc["dq"], acc["dk"], acc["dv"])):
+        for g, ref, name in zip(got, (dQ, dK, dV), ("dq", "dk", "dv")):
+            assert relf(g.double().cpu().numpy(), ref) <= 3e-2, name
     with pytest.raises(lc.LcattnError) as err:
-        lc.lcattn_bwd(dev["q"], dev["k"], dev["v"], o, torch.ones_like(o), lse, mask, meta,
-                      workspace=torch.empty(16, dtype=torch.uint8, device="cuda"))
+        lc.lcattn_bwd_deterministic(dev["q"], dev["k"], dev["v"], out["o"], dev["do"], out["lse"], mask, meta,
+                                    workspace=torch.empty(16, dtype=torch.uint8, device="cuda"))
     assert err.value.status == lc.LCATTN_ERR_UNSUPPORTED
 
 
