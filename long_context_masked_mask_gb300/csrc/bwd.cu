@@ -29,7 +29,9 @@
 //   warp  13   TMEM owner and MMA issuer; warps 14-15 idle (they complete the
 //              warpgroup for setmaxnreg).
 // TMEM: [0,128) S^T then P^T | [128,256) dP^T then dS^T, then dQ^T |
-//       [256,384) dV | [384,512) dK.
+//       [256,384) dV | [384,512) dK.  At D = 64, dV and dK take 64 columns
+//       each ([256,320), [320,384)) and dQ^T gets [384,512) of its own, so the
+//       next dP^T does not wait for the drain.
 #include <cuda_bf16.h>
 
 #include "lcattn_internal.cuh"
@@ -294,6 +296,10 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
   constexpr int kBoxes = BwdGeom<D>::kBoxes;
   static_assert(D != 256 || kDq, "head dim 256 has no separate dQ kernel");
   constexpr int kOut = D == 256 ? 128 : D;  // head-dim columns of dK / dV / dQ this unit owns
+  // TMEM columns of dK and dQ^T (dQ^T has a region of its own at D = 64).
+  constexpr bool kSepDq = D == 64;
+  constexpr uint32_t kColDK = D == 64 ? 320 : 384;
+  constexpr uint32_t kColDQ = kSepDq ? 384 : 128;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const BwdArgs& a = ka.a;
   const ProblemDev& pr = a.pr;
@@ -583,7 +589,8 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
       const uint32_t id_kmaj = idesc_bf16_f32(128, 128, false, false);
       const uint32_t id_ts = idesc_bf16_f32(128, D, false, true);
       const uint32_t id_mn = idesc_bf16_f32(128, 128, true, true);
-      const uint32_t tS = tmem, tP = tmem + 128, tdV = tmem + 256, tdK = tmem + 384;
+      const uint32_t tS = tmem, tP = tmem + 128, tdV = tmem + 256, tdK = tmem + kColDK;
+      const uint32_t tQd = tmem + kColDQ;
       // Base descriptors (K-major and MN-major views); ring stage st is kTileBytes on.
       const uint64_t dK_k = sdesc_sw128(smem_u32(sm.k), 16, 1024);
       const uint64_t dK_mn = sdesc_sw128(smem_u32(sm.k), kHalfBytes, 1024);
@@ -658,17 +665,24 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
         tc_commit_e(&sm.q_empty[st]);  // Q(i), dO(i), LSE(i), D(i) are read for good
         if (kDq) {
           // dQ^T = K^T dS^T: A = K read MN-major (M = head dim), B = dS^T read
-          // MN-major (N = queries).  Lands in [128, 256): lane = head dim.
-          mma_ss_e<0>(tP, dK_mn, dS_mn, id_mn);
+          // MN-major (N = queries).  Lands in [128, 256) (D = 64: [384, 512),
+          // once the drain has read dQ^T(i-1) there): lane = head dim.
+          if (kSepDq && i > 0) {
+            ok = __all_sync(0xffffffffu, mbar_wait(&sm.dq_free, (i - 1) & 1, abort_flag, gstatus, TO));
+            if (!ok) break;
+            tc_fence_after();
+          }
+          mma_ss_e<0>(tQd, dK_mn, dS_mn, id_mn);
           #pragma unroll
           for (int kk = 1; kk < 8; ++kk)
-            mma_ss_e<1>(tP, sdesc_add(dK_mn, kk * 2048), sdesc_add(dS_mn, kk * 2048), id_mn);
+            mma_ss_e<1>(tQd, sdesc_add(dK_mn, kk * 2048), sdesc_add(dS_mn, kk * 2048), id_mn);
           tc_commit_e(&sm.dq_full);
         }
         // dP^T(i+1) = V dO^T, into the columns dQ^T(i) uses: wait for its drain
-        // (without the dQ product, dK(i) read dS^T(i) from them first, in order).
+        // (without the dQ product, dK(i) read dS^T(i) from them first, in order;
+        // at D = 64 dQ^T has columns of its own).
         if (more) {
-          if (kDq) {
+          if (kDq && !kSepDq) {
             ok = __all_sync(0xffffffffu, mbar_wait(&sm.dq_free, i & 1, abort_flag, gstatus, TO));
             if (!ok) break;
           }
@@ -687,7 +701,7 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
     // ------------------------------------------------------------ dQ drain
     if (kDq) {
     const int r = 32 * (warp & 3) + lane;  // head-dim row of dQ^T (TMEM lane)
-    const uint32_t tQ = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16) + 128;
+    const uint32_t tQ = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16) + kColDQ;
     const int64_t dq_row_stride = a.dqa_ss;
     ItemIter<kChunked> it;
     it.init(a.meta, b, kt, pr.G, g, h_lo, h_hi, qlo, qhi);
@@ -888,7 +902,7 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
         tc_fence_after();
       }
       const float mul = x == 0 ? 1.f / a.scale : 1.f;
-      const uint32_t tacc = tmem + lane_off + (x == 0 ? 256 : 384);
+      const uint32_t tacc = tmem + lane_off + (x == 0 ? 256 : kColDK);
       // Split units write fp32 partials [part][dV, dK][B][Sk][Hkv][D]; a
       // reduction kernel sums the parts into the bf16 outputs.
       float* pdst = a.dkv_part + (((((int64_t)part * 2 + x) * pr.B + b) * pr.Sk + key) * pr.Hkv + g) * D + col0;
