@@ -1,4 +1,5 @@
-"""GPU parity at the five benchmark configurations' full sizes, in the launch
+"""GPU parity at the five benchmark configurations' full sizes (and the head dim
+64 / 256 bench workloads), in the launch
 configuration bench.py times (one compile, forward and backward per mask through
 the C ABI).  The oracle cannot run these problems whole, so it checks:
 
@@ -75,7 +76,8 @@ def cheap_cols(spec, N, rng, budget_rows=16384):
 
 
 CASES = [("causal_1k", 0), ("dense_8k", 0), ("dense_8k", 1), ("docs_32k", 0), ("docs_32k", 1)] + \
-        [("hetero_16k", i) for i in range(5)] + [("long_128k", 0), ("long_128k", 1)]
+        [("hetero_16k", i) for i in range(5)] + [("long_128k", 0), ("long_128k", 1)] + \
+        [("dense_8k_hd64", 0), ("dense_8k_hd256", 0), ("dense_8k_hd256", 1)]  # the head-dim variants' bench workloads
 
 
 @pytest.mark.parametrize("name,mi", CASES, ids=[f"{n}-{i}" for n, i in CASES])
