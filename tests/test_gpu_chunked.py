@@ -2,7 +2,8 @@
 of a mask with per-head lists and at least 512 query tiles into ranges of 64
 query tiles, launched chunk-major, with dK/dV reduce-added into an fp32
 accumulator.  Checked through the C ABI at N = 65836 (9 chunks, the last of
-one ragged tile), GQA 2:1, a uniform and a variable block map:
+one ragged tile), GQA 2:1, a uniform and a variable block map, and the uniform
+map at head dim 256 (two CTAs per unit, one per head-dim half):
 
 * dQ on sampled query rows (the ragged tail included) against the fp64 oracle,
   relF <= 3e-2, and O within the forward's bars;
@@ -29,9 +30,9 @@ def relf(g, r):
     return float(np.linalg.norm(g - r) / np.linalg.norm(r))
 
 
-@pytest.mark.parametrize("kind", ["UNIFORM_BLOCK", "VARIABLE_BLOCK"])
-def test_chunked_block_map_backward(kind):
-    B, N, Hq, Hkv, D = 1, 65836, 2, 1, 128  # 515 query tiles: 9 chunks of 64 (the last has 3)
+@pytest.mark.parametrize("kind,D", [("UNIFORM_BLOCK", 128), ("VARIABLE_BLOCK", 128), ("UNIFORM_BLOCK", 256)])
+def test_chunked_block_map_backward(kind, D):
+    B, N, Hq, Hkv = 1, 65836, 2, 1  # 515 query tiles: 9 chunks of 64 (the last has 3)
     if kind == "UNIFORM_BLOCK":
         nb = -(-N // 128)
         spec = MaskSpec("UNIFORM_BLOCK", {"block": 128, "keep": block_keep(Hq, nb, nb, 0.2, 1)})

@@ -124,3 +124,26 @@ def test_fp8_forward_full_size_sampled_rows(kind):
     for h in (0, 9, 63):
         O, L = oracle.attention_fwd_rows(q, k, v, spec, 1.0 / math.sqrt(128), 0, h, rows)
         _check(o[0, ri, h], lse[0, h, ri], O, L)
+
+
+def test_fp8_views_of_a_fused_qkv_buffer():
+    """Q, K and V as views of one fused [B, S, Hq + 2 Hkv, 128] e4m3 buffer (row
+    strides of (Hq + 2 Hkv) x 128 bytes) give the same bits as contiguous copies."""
+    B, N, Hq, Hkv = 2, 333, 4, 2
+    x = qkv_fp8(B, N, Hq, Hkv, 128, seed=19)
+    fused = torch.cat([x["q8"], x["k8"], x["v8"]], dim=2).cuda()
+    q, k, v = fused[:, :, :Hq], fused[:, :, Hq:Hq + Hkv], fused[:, :, Hq + Hkv:]
+    assert q.stride(1) == (Hq + 2 * Hkv) * 128
+    spec = MaskSpec("CAUSAL")
+    mask = lc.DeviceMask(spec, N, Hq, B)
+    meta = lc.lcattn_mask_compile(lc.make_shape(q, k, v), mask)
+    o_view, lse_view = lc.lcattn_fwd_fp8(q, k, v, x["q_scale"], x["k_scale"], x["v_scale"], mask, meta)
+    qc, kc, vc = q.contiguous(), k.contiguous(), v.contiguous()
+    meta_c = lc.lcattn_mask_compile(lc.make_shape(qc, kc, vc), mask)
+    o_c, lse_c = lc.lcattn_fwd_fp8(qc, kc, vc, x["q_scale"], x["k_scale"], x["v_scale"], mask, meta_c)
+    torch.cuda.synchronize()
+    assert lc.lcattn_read_status(meta) == 0 and lc.lcattn_read_status(meta_c) == 0
+    assert torch.equal(o_view, o_c) and torch.equal(lse_view, lse_c)
+    O, L = fp8_ref.attention_fwd_fp8(x["q8"].numpy(), x["k8"].numpy(), x["v8"].numpy(), x["q_scale"],
+                                     x["k_scale"], x["v_scale"], spec, 1.0 / math.sqrt(128))
+    _check(o_view, lse_view, O, L)

@@ -147,3 +147,28 @@ def test_hd256_many_items_per_cta(kind):
         np.testing.assert_array_equal(np.isfinite(gl), fin)
         if fin.any():
             assert np.abs(gl[fin] - ref_l[fin]).max() <= 5e-3
+
+
+@pytest.mark.parametrize("Sq,Sk,Hq,Hkv,kind", [(300, 777, 4, 2, "CAUSAL"), (700, 129, 2, 1, "FULL"),
+                                               (40, 2600, 4, 4, "CAUSAL_SLIDING_WINDOW")])
+def test_hd256_rectangular_backward(Sq, Sk, Hq, Hkv, kind):
+    """Sq != Sk at head dim 256 (bottom-right aligned), forward and backward
+    against the oracle: ragged tiles on both axes, more queries than keys."""
+    B = 1
+    spec = MaskSpec(kind, {"window": Sk // 3} if "WINDOW" in kind else {})
+    x = qkv(B, Sq, Hq, Hkv, D, seed=Sq + Sk, Sk=Sk)
+    dev = {n: t.cuda() for n, t in x.items()}
+    out = lc.attention(dev["q"], dev["k"], dev["v"], spec, d_o=dev["do"])
+    torch.cuda.synchronize()
+    assert lc.lcattn_read_status(out["tile_meta"]) == 0
+    f64 = {n: t.double().numpy() for n, t in x.items()}
+    dQ, dK, dV, O, LSE = oracle.attention_bwd(f64["q"], f64["k"], f64["v"], f64["do"], spec, 1.0 / math.sqrt(D))
+    g = out["o"].double().cpu().numpy()
+    assert np.abs(g - O).max() <= 2e-2 and relf(g, O) <= 1e-2
+    lse = out["lse"].double().cpu().numpy()
+    fin = np.isfinite(LSE)
+    np.testing.assert_array_equal(np.isfinite(lse), fin)
+    if fin.any():
+        assert np.abs(lse[fin] - LSE[fin]).max() <= 5e-3
+    for name, ref in (("dq", dQ), ("dk", dK), ("dv", dV)):
+        assert relf(out[name].double().cpu().numpy(), ref) <= 3e-2, name
