@@ -144,3 +144,18 @@ def test_shard_descriptor_bits():
     qo = m.q_offs.cpu().numpy().astype(np.int64)
     assert np.array_equal(sm.q_offs.cpu().numpy(), np.clip(qo - q0, 0, sq))
     assert np.array_equal(sm.k_offs.cpu().numpy(), np.clip(qo - k0, 0, sk))
+
+
+@pytest.mark.parametrize("kind", ["CAUSAL", "CAUSAL_DOCUMENT", "UNIFORM_BLOCK"])
+@pytest.mark.parametrize("world", [2, 3])
+def test_ring_zigzag_layout_matches_oracle(kind, world):
+    """Zigzag shards (an early and a late chunk per device): every device
+    computes two query chunks against the two K/V chunks it holds per round."""
+    B, N, Hq, Hkv, D = 1, 700, 4, 2, 128
+    spec = _spec(kind, N, Hq, seed=2)
+    x = qkv(B, N, Hq, Hkv, D, seed=31 + world)
+    dev = {k: t.cuda() for k, t in x.items()}
+    mask = lc.DeviceMask(spec, N, Hq, B)
+    out = ring.emulate(dev["q"], dev["k"], dev["v"], mask, world, d_o=dev["do"], layout="zigzag")
+    torch.cuda.synchronize()
+    _check(out, x, spec, D)

@@ -81,3 +81,32 @@ def test_hop_with_gloo_ranks(world):
     for rank, seen, acc in out:
         assert seen == [(rank - t) % world for t in range(world)]
         assert acc == [total] * 4                    # every device added to the owner's shard
+
+
+def test_zigzag_chunks_cover_the_sequence_and_balance_causal_work():
+    """Zigzag shards: every position in exactly one chunk; under CAUSAL every
+    device does the same work (allowed pairs of its query chunks against all
+    keys) to within 1% (chunk lengths differ by one row), while contiguous shards differ by about
+    2 * world - 1 between the first and the last device."""
+    import numpy as np
+    import oracle
+    from synthetic import MaskSpec
+    ring = _ring()
+    N = 999
+    for world in (2, 3, 4):
+        for layout in ("contiguous", "zigzag"):
+            sh = ring.shard_chunks(N, world, layout)
+            cover = np.zeros(N, int)
+            for chunks in sh:
+                for a, n in chunks:
+                    cover[a:a + n] += 1
+            assert (cover == 1).all()
+        M = oracle.allowed(MaskSpec("CAUSAL"), N, np.arange(N))
+        work = {lay: [sum(int(M[a:a + n].sum()) for a, n in chunks) for chunks in ring.shard_chunks(N, world, lay)]
+                for lay in ("contiguous", "zigzag")}
+        z = work["zigzag"]
+        assert max(z) <= 1.01 * min(z)                             # equal up to chunk rounding
+        c = work["contiguous"]
+        assert c[-1] / c[0] > 2 * world - 2                        # the imbalance zigzag removes
+    with pytest.raises(ValueError):
+        ring.shard_chunks(5, 3, "zigzag")
