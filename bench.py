@@ -91,8 +91,10 @@ def workload_desc(wl):
     if wl.Sq is not None:
         desc += f", Sq={wl.Sq} queries per sequence against the N keys (bottom-right aligned)"
     if wl.forward_only:
-        desc += (", forward only; FLOPs of the forward" if wl.fp8 else
+        desc += (", forward only; FLOPs of the forward" if wl.fp8 and wl.Sq is None else
                  ", forward only (decode-style rows); FLOPs and bytes of the forward")
+    if wl.vt_cache:
+        desc += "; V held transposed as an e4m3 K/V cache would hold it (V^T made once, outside the step)"
     return desc
 
 
@@ -347,7 +349,7 @@ class Leg:
         self.fp8 = wl.fp8
         self.peak_mult = 2.0 if wl.fp8 else 1.0
         if wl.fp8:  # e4m3 codes (uint8) with per-tensor factors; forward only
-            x = qkv_fp8(B, N, Hq, Hkv, D, seed=s, Sk=N, device=str(dev))
+            x = qkv_fp8(B, wl.q_len, Hq, Hkv, D, seed=s, Sk=N, device=str(dev))
             self.scales = (x["q_scale"], x["k_scale"], x["v_scale"])
             x = {"q": x["q8"], "k": x["k8"], "v": x["v8"], "do": None}
         elif wl.structure > 0:
@@ -362,6 +364,13 @@ class Leg:
         self.Sq = Sq = q.shape[1]
         self.fwd_only = wl.forward_only
         self.shape = shape = lc.make_shape(self.q, self.k, self.v)
+        # An e4m3 K/V cache keeps V transposed: the step's V input is then V^T,
+        # made once here (self.v_src keeps V's shape for the calls).
+        self.vt_cache = wl.vt_cache
+        if self.vt_cache:
+            self.v_src = self.v
+            self.v = lc.lcattn_fp8_transpose_v(self.v_src, self.k, self.q)
+            torch.cuda.synchronize()
         self.ws = torch.empty(max(16, 0 if self.fwd_only else lc.lcattn_bwd_workspace_size(shape)),
                               dtype=torch.uint8, device=dev)
         runs = []
@@ -391,11 +400,16 @@ class Leg:
             r["lse"] = torch.empty(B, Hq, Sq, dtype=torch.float32, device=dev)
             if not self.fwd_only:
                 r["dq"], r["dk"], r["dv"] = torch.empty_like(q), torch.empty_like(self.k), torch.empty_like(self.v)
-            if self.fp8:  # the V^T pre-pass's workspace; two launches (V^T, forward)
-                fws = int(lc.library().lcattn_fwd_fp8_workspace_size(lc.ctypes.byref(shape)))
+            if self.fp8:
+                # V^T pre-pass (unless V is held transposed) and the forward, through
+                # the split-KV path (slices + merge) for short query sides.
+                split_ws = int(lc.library().lcattn_fwd_fp8_vt_workspace_size(lc.ctypes.byref(shape),
+                                                                               lc.ctypes.byref(r["mask"].desc)))
+                fws = split_ws if self.vt_cache else \
+                    int(lc.library().lcattn_fwd_fp8_workspace_size(lc.ctypes.byref(shape)))
                 r["fws"] = torch.empty(max(16, fws), dtype=torch.uint8, device=dev)
-                r["split"] = False
-                r["launches"] += 2
+                r["split"] = split_ws > 0
+                r["launches"] += (0 if self.vt_cache else 1) + (2 if split_ws > 0 else 1)
                 continue
             # The forward's split-KV workspace (empty unless the query side is short).
             fws = lc.lcattn_fwd_workspace_size(shape, r["mask"])
@@ -407,7 +421,10 @@ class Leg:
         self.launches_per_step = sum(r["launches"] for r in runs)
 
     def fwd(self, r, qq, kk, vv):
-        if self.fp8:
+        if self.fp8 and self.vt_cache:  # vv is V^T
+            self.lc.lcattn_fwd_fp8_vt(qq, kk, vv, self.v_src, *self.scales, r["mask"], r["meta"], o=r["o"],
+                                      lse=r["lse"], workspace=r["fws"])
+        elif self.fp8:
             self.lc.lcattn_fwd_fp8(qq, kk, vv, *self.scales, r["mask"], r["meta"], o=r["o"], lse=r["lse"],
                                    workspace=r["fws"])
         else:
@@ -565,7 +582,9 @@ class Leg:
         B, Hq = wl.B, wl.Hq
         dom = max(kernels, key=lambda n: kernels[n][0])
         t_dom, fl_dom, n_dom = kernels[dom]
-        fwd_bytes = (q.numel() + self.k.numel() + self.v.numel() + q.numel()) * q.element_size() + B * Hq * self.Sq * 4
+        # Q, K and V (or V^T) read, O (bf16) and LSE (fp32) written.
+        fwd_bytes = (q.numel() * q.element_size() + self.k.numel() * self.k.element_size() +
+                     self.v.numel() * self.v.element_size() + q.numel() * 2 + B * Hq * self.Sq * 4)
         # A forward-only step is HBM-bound when its arithmetic intensity (FLOPs per
         # algorithmic byte) is below the ridge point of the two measured peaks.
         hbm_bound = self.fwd_only and (self.step_flops / len(self.runs)) / fwd_bytes < \
@@ -575,7 +594,8 @@ class Leg:
             # arithmetic per byte.  Algorithmic bytes: Q, K, V read, O and LSE
             # written, per mask.
             gbs = fwd_bytes * n_dom / (t_dom / 1e3) / 1e9
-            roof = {"kernel": "split_kernel + combine_kernel" if self.runs[0]["split"] else "fwd_kernel",
+            roof = {"kernel": ("split_kernel + combine_kernel" if self.runs[0]["split"] else "fwd_kernel") +
+                              (" (e4m3)" if self.fp8 else ""),
                     "bound": "hbm", "achieved": round(gbs, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
                     "frac": round(gbs / pk["hbm_gbs"], 4), "algorithmic_bytes": fwd_bytes,
                     "peak_kind": f"{pk['source']} copy bandwidth"}

@@ -289,13 +289,35 @@ int lcattn_fwd_ws(const lcattn_shape* shape, const void* q, const void* k, const
  * [B][Hq][Sq]; -inf and O = 0 for rows that allow nothing).  `tile_meta` from lcattn_mask_compile on the same shape and mask.
  * The workspace (lcattn_fwd_fp8_workspace_size bytes, 16-byte aligned) receives
  * V^T [B][Hkv][128][Skp] (e4m3, Skp = Sk rounded up to 16), written by a first
- * kernel so that both operands of the P V product are K-major; the forward
- * kernel follows on `stream`.                                              */
+ * kernel so that both operands of the P V product are K-major (as
+ * lcattn_fp8_transpose_v), and then holds the split-KV partials when the
+ * shape takes that path (as lcattn_fwd_fp8_vt); the forward follows on
+ * `stream`.  The size covers every mask of the shape.                     */
 size_t lcattn_fwd_fp8_workspace_size(const lcattn_shape* shape);
 int lcattn_fwd_fp8(const lcattn_shape* shape, const void* q, const void* k, const void* v, float q_scale,
                    float k_scale, float v_scale, const void* tile_meta, const lcattn_mask_desc* mask,
                    float scale, void* o, float* lse, void* workspace, size_t workspace_bytes,
                    lcattn_stream_t stream);
+
+/* The two halves of lcattn_fwd_fp8, for callers that keep V transposed (an
+ * e4m3 K/V cache written once and read by many decode steps, where a V^T
+ * pass per step would double the V traffic of an HBM-bound forward).
+ * lcattn_fp8_transpose_v writes vt = V^T [B][Hkv][128][Skp] e4m3 (contiguous,
+ * lcattn_fp8_vt_size bytes, 16-byte aligned; keys in [Sk, Skp) zero) from v
+ * (shape's v_stride).  lcattn_fwd_fp8_vt is the forward of lcattn_fwd_fp8 with
+ * V given as vt.  Query sides that the bf16 forward would split over the key
+ * list (lcattn_fwd_ws: decode rows, short query chunks; column bounds only)
+ * take the same split-KV path here, with the same packing of a GQA group's
+ * heads, and need lcattn_fwd_fp8_vt_workspace_size bytes of workspace for
+ * the slices' partials (0: no workspace, which may then be NULL).  Errors as
+ * for lcattn_fwd_fp8.                                                     */
+size_t lcattn_fp8_vt_size(const lcattn_shape* shape);
+int lcattn_fp8_transpose_v(const lcattn_shape* shape, const void* v, void* vt, lcattn_stream_t stream);
+size_t lcattn_fwd_fp8_vt_workspace_size(const lcattn_shape* shape, const lcattn_mask_desc* mask);
+int lcattn_fwd_fp8_vt(const lcattn_shape* shape, const void* q, const void* k, const void* vt, float q_scale,
+                      float k_scale, float v_scale, const void* tile_meta, const lcattn_mask_desc* mask,
+                      float scale, void* o, float* lse, void* workspace, size_t workspace_bytes,
+                      lcattn_stream_t stream);
 
 /* The backward calls below compute the gradients of the same operator (blog
  * sections "密集注意力内核" / "稀疏注意力内核"; the pages' sparse-kernel findings,

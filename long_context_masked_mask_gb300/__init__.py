@@ -59,7 +59,8 @@ EXPORTED = (
     "lcattn_fwd_workspace_size", "lcattn_fwd_ws",
     "lcattn_mask_shard", "lcattn_lse_merge", "lcattn_bwd_accum_workspace_size", "lcattn_bwd_accum",
     "lcattn_f32_to_bf16", "lcattn_bwd_deterministic_workspace_size", "lcattn_bwd_deterministic",
-    "lcattn_fwd_fp8_workspace_size", "lcattn_fwd_fp8",
+    "lcattn_fwd_fp8_workspace_size", "lcattn_fwd_fp8", "lcattn_fp8_vt_size", "lcattn_fp8_transpose_v",
+    "lcattn_fwd_fp8_vt_workspace_size", "lcattn_fwd_fp8_vt",
 )
 
 
@@ -120,6 +121,11 @@ def _load():
         "lcattn_fwd_fp8_workspace_size": (ctypes.c_size_t, [S]),
         "lcattn_fwd_fp8": (ctypes.c_int, [S, P, P, P, ctypes.c_float, ctypes.c_float, ctypes.c_float, P, M,
                                           ctypes.c_float, P, P, P, ctypes.c_size_t, P]),
+        "lcattn_fp8_vt_size": (ctypes.c_size_t, [S]),
+        "lcattn_fp8_transpose_v": (ctypes.c_int, [S, P, P, P]),
+        "lcattn_fwd_fp8_vt_workspace_size": (ctypes.c_size_t, [S, M]),
+        "lcattn_fwd_fp8_vt": (ctypes.c_int, [S, P, P, P, ctypes.c_float, ctypes.c_float, ctypes.c_float, P, M,
+                                             ctypes.c_float, P, P, P, ctypes.c_size_t, P]),
         "lcattn_bwd_deterministic": (ctypes.c_int, [S, P, P, P, P, P, P, P, M, ctypes.c_float, P, P, P, P,
                                                     ctypes.c_size_t, P]),
         "lcattn_read_status": (ctypes.c_int, [P, P]),
@@ -326,6 +332,57 @@ def lcattn_fwd_fp8(q8: torch.Tensor, k8: torch.Tensor, v8: torch.Tensor, q_scale
                                float(k_scale), float(v_scale), tile_meta.data_ptr(), ctypes.byref(mask.desc),
                                float(scale), o.data_ptr(), lse.data_ptr(), workspace.data_ptr(), workspace.numel(),
                                _stream_ptr(stream)), "lcattn_fwd_fp8")
+    return o, lse
+
+
+def lcattn_fp8_transpose_v(v8: torch.Tensor, k8: torch.Tensor, q8: torch.Tensor, vt: Optional[torch.Tensor] = None,
+                           stream=None) -> torch.Tensor:
+    """V^T of the e4m3 codes v8 [B, Sk, Hkv, 128] (lcattn_fp8_transpose_v): a
+    uint8 tensor [B, Hkv, 128, Skp], Skp = Sk rounded up to 16.  q8 and k8 give
+    the problem's shape (they are not read)."""
+    shape = make_shape(q8, k8, v8)
+    nbytes = int(_lib.lcattn_fp8_vt_size(ctypes.byref(shape)))
+    if nbytes == 0:
+        raise LcattnError(LCATTN_ERR_UNSUPPORTED, "lcattn_fp8_vt_size")
+    B, Sk, Hkv, _ = v8.shape
+    skp = -(-Sk // 16) * 16
+    if vt is None:
+        vt = torch.empty(B, Hkv, 128, skp, dtype=torch.uint8, device=v8.device)
+    if vt.numel() < B * Hkv * 128 * skp or not vt.is_contiguous():
+        raise ValueError("vt must be a contiguous uint8 tensor of B * Hkv * 128 * Skp elements")
+    _check(_lib.lcattn_fp8_transpose_v(ctypes.byref(shape), v8.data_ptr(), vt.data_ptr(), _stream_ptr(stream)),
+           "lcattn_fp8_transpose_v")
+    return vt
+
+
+def lcattn_fwd_fp8_vt(q8: torch.Tensor, k8: torch.Tensor, vt: torch.Tensor, v_shape_like: torch.Tensor,
+                      q_scale: float, k_scale: float, v_scale: float, mask: DeviceMask, tile_meta: torch.Tensor,
+                      scale: Optional[float] = None, o: Optional[torch.Tensor] = None,
+                      lse: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                      stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """FP8 forward on V^T from :func:`lcattn_fp8_transpose_v` (lcattn_fwd_fp8_vt).
+    ``v_shape_like`` is V (or any tensor of V's shape and strides): it gives the
+    problem's shape and is not read."""
+    for t in (q8, k8, vt):
+        if t.dtype != torch.uint8:
+            raise TypeError("q8, k8 and vt must hold e4m3 codes as uint8")
+    B, Sq, Hq, D = q8.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if o is None:
+        o = torch.empty(B, Sq, Hq, D, dtype=torch.bfloat16, device=q8.device)
+    if lse is None:
+        lse = torch.empty(B, Hq, Sq, dtype=torch.float32, device=q8.device)
+    shape = make_shape(q8, k8, v_shape_like, o)
+    nbytes = int(_lib.lcattn_fwd_fp8_vt_workspace_size(ctypes.byref(shape), ctypes.byref(mask.desc)))
+    if workspace is None and nbytes > 0:
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=q8.device)
+    ws_ptr = workspace.data_ptr() if workspace is not None else None
+    ws_len = workspace.numel() if workspace is not None else 0
+    _check(_lib.lcattn_fwd_fp8_vt(ctypes.byref(shape), q8.data_ptr(), k8.data_ptr(), vt.data_ptr(), float(q_scale),
+                                  float(k_scale), float(v_scale), tile_meta.data_ptr(), ctypes.byref(mask.desc),
+                                  float(scale), o.data_ptr(), lse.data_ptr(), ws_ptr, ws_len, _stream_ptr(stream)),
+           "lcattn_fwd_fp8_vt")
     return o, lse
 
 

@@ -166,12 +166,13 @@ int cuda_status(cudaError_t e) { return e == cudaSuccess ? LCATTN_OK : LCATTN_ER
 // [B][S][H][128] e4m3 (one byte per element) with byte strides (b, s, h): a
 // 4-D map with a 128-byte x 1 head x 128 rows box and 128-byte swizzle (one
 // K-major 128 x 128 tile per copy).
-int encode_bshd8(CUtensorMap* m, const void* ptr, int64_t B, int64_t S, int64_t H, const int64_t st[3]) {
+int encode_bshd8(CUtensorMap* m, const void* ptr, int64_t B, int64_t S, int64_t H, const int64_t st[3],
+                 uint32_t box_h = 1, uint32_t box_s = 128) {
   auto fn = encode_fn();
   if (!fn) return LCATTN_ERR_CUDA;
   cuuint64_t dims[4] = {128, (cuuint64_t)H, (cuuint64_t)S, (cuuint64_t)B};
   cuuint64_t strides[3] = {(cuuint64_t)st[2], (cuuint64_t)st[1], (cuuint64_t)(st[0] > 0 ? st[0] : S * st[1])};
-  cuuint32_t box[4] = {128, 1, 128, 1};
+  cuuint32_t box[4] = {128, box_h, box_s, 1};
   cuuint32_t es[4] = {1, 1, 1, 1};
   CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(ptr), dims, strides, box, es,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -418,30 +419,61 @@ int lcattn_fwd_ws(const lcattn_shape* shape, const void* q, const void* k, const
   return cuda_status(launch_fwd_split(tq, tk, tv, a, reinterpret_cast<cudaStream_t>(stream)));
 }
 
-size_t lcattn_fwd_fp8_workspace_size(const lcattn_shape* shape) {
-  if (validate_shape(shape) != LCATTN_OK || validate_fp8(shape) != LCATTN_OK) return 0;
-  return (size_t)fwd8_ws_bytes(shape);
+}  // extern "C"
+
+namespace {
+
+// Split partials of the e4m3 forward for a column-bounds mask (the only kind
+// the split-KV path takes): the most any mask of this shape needs.
+int64_t fwd8_split_bytes_max(const lcattn_shape* s) {
+  lcattn_mask_desc cb{};
+  cb.kind = LCATTN_MASK_COLBOUNDS;
+  return split_ws_bytes(s, split_plan(s, &cb));
 }
 
-int lcattn_fwd_fp8(const lcattn_shape* shape, const void* q, const void* k, const void* v, float q_scale,
-                   float k_scale, float v_scale, const void* tile_meta, const lcattn_mask_desc* mask, float scale,
-                   void* o, float* lse, void* workspace, size_t workspace_bytes, lcattn_stream_t stream) {
+// The e4m3 forward on V^T already in device memory (vt: [B][Hkv][128][Skp]).
+// Short query sides go through the split-KV kernel (partials in `workspace`),
+// the rest through the persistent kernel (no workspace).
+int fwd8_run(const lcattn_shape* shape, const void* q, const void* k, const void* vt, float q_scale,
+             float k_scale, float v_scale, const void* tile_meta, const lcattn_mask_desc* mask, float scale,
+             void* o, float* lse, void* workspace, size_t workspace_bytes, cudaStream_t cs) {
   lcattn_tile_meta_layout L;
   int st = layout_of(shape, mask, &L);
   if (st) return st;
   if ((st = validate_fp8(shape))) return st;
-  if (!q || !k || !v || !o || !lse || !tile_meta || !workspace) return LCATTN_ERR_INVALID_ARG;
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(tile_meta) ||
-      !aligned16(workspace))
+  if (!q || !k || !vt || !o || !lse || !tile_meta) return LCATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(vt) || !aligned16(o) || !aligned16(tile_meta))
     return LCATTN_ERR_UNSUPPORTED;
   for (float x : {scale, q_scale, k_scale, v_scale})
     if (!(x > 0.f) || !(x < 1e30f)) return LCATTN_ERR_INVALID_ARG;
-  if ((int64_t)workspace_bytes < fwd8_ws_bytes(shape)) return LCATTN_ERR_WORKSPACE;
   const int64_t skp = fp8_skp(shape);
-  CUtensorMap tq, tk, tvt, to;
-  if ((st = encode_bshd8(&tq, q, shape->B, shape->Sq, shape->Hq, shape->q_stride))) return st;
+  CUtensorMap tk, tvt;
   if ((st = encode_bshd8(&tk, k, shape->B, shape->Sk, shape->Hkv, shape->k_stride))) return st;
-  if ((st = encode_vt8(&tvt, workspace, shape->B, shape->Hkv, skp))) return st;
+  if ((st = encode_vt8(&tvt, vt, shape->B, shape->Hkv, skp))) return st;
+  const SplitPlan p = split_plan(shape, mask);
+  if (p.splits > 0) {
+    if (!workspace || !aligned16(workspace)) return LCATTN_ERR_INVALID_ARG;
+    if ((int64_t)workspace_bytes < split_ws_bytes(shape, p)) return LCATTN_ERR_WORKSPACE;
+    CUtensorMap tq;
+    if ((st = encode_bshd8(&tq, q, shape->B, shape->Sq, shape->Hq, shape->q_stride, p.Gp, p.Rq))) return st;
+    SplitArgs a;
+    a.pr = problem_of(shape);
+    a.mask = mask_of(mask);
+    a.meta = meta_of(L, tile_meta);
+    a.scale_log2 = scale * q_scale * k_scale * 1.4426950408889634f;
+    a.o_scale = v_scale;
+    a.Gp = p.Gp; a.Rq = p.Rq; a.nQc = p.nQc; a.splits = p.splits;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    a.o_part = reinterpret_cast<float*>(ws);
+    a.lse_part = reinterpret_cast<float*>(
+        ws + align_up((int64_t)p.splits * shape->B * shape->Sq * shape->Hq * shape->D * 4, 256));
+    a.o = o;
+    a.o_sb = shape->o_stride[0]; a.o_ss = shape->o_stride[1]; a.o_sh = shape->o_stride[2];
+    a.lse = lse;
+    return cuda_status(launch_fwd_split_e4m3(tq, tk, tvt, a, cs));
+  }
+  CUtensorMap tq, to;
+  if ((st = encode_bshd8(&tq, q, shape->B, shape->Sq, shape->Hq, shape->q_stride))) return st;
   if ((st = encode_bshd(&to, o, shape->B, shape->Sq, shape->Hq, shape->D, shape->o_stride))) return st;
   FwdArgs a;
   a.pr = problem_of(shape);
@@ -452,12 +484,68 @@ int lcattn_fwd_fp8(const lcattn_shape* shape, const void* q, const void* k, cons
   a.o = o;
   a.o_sb = shape->o_stride[0]; a.o_ss = shape->o_stride[1]; a.o_sh = shape->o_stride[2];
   a.lse = lse;
-  const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
-  cudaError_t e = launch_vt8(static_cast<const uint8_t*>(v), shape->v_stride[0], shape->v_stride[1],
-                             shape->v_stride[2], static_cast<uint8_t*>(workspace), (int)shape->B, (int)shape->Sk,
-                             (int)skp, (int)shape->Hkv, cs);
-  if (e != cudaSuccess) return cuda_status(e);
   return cuda_status(launch_fwd_e4m3(tq, tk, tvt, to, a, cs));
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t lcattn_fp8_vt_size(const lcattn_shape* shape) {
+  if (validate_shape(shape) != LCATTN_OK || validate_fp8(shape) != LCATTN_OK) return 0;
+  return (size_t)fwd8_ws_bytes(shape);
+}
+
+int lcattn_fp8_transpose_v(const lcattn_shape* shape, const void* v, void* vt, lcattn_stream_t stream) {
+  int st = validate_shape(shape);
+  if (st) return st;
+  if ((st = validate_fp8(shape))) return st;
+  if (!v || !vt) return LCATTN_ERR_INVALID_ARG;
+  if (!aligned16(v) || !aligned16(vt)) return LCATTN_ERR_UNSUPPORTED;
+  return cuda_status(launch_vt8(static_cast<const uint8_t*>(v), shape->v_stride[0], shape->v_stride[1],
+                                shape->v_stride[2], static_cast<uint8_t*>(vt), (int)shape->B, (int)shape->Sk,
+                                (int)fp8_skp(shape), (int)shape->Hkv, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+size_t lcattn_fwd_fp8_vt_workspace_size(const lcattn_shape* shape, const lcattn_mask_desc* mask) {
+  lcattn_tile_meta_layout L;
+  if (layout_of(shape, mask, &L) != LCATTN_OK || validate_fp8(shape) != LCATTN_OK) return 0;
+  return (size_t)split_ws_bytes(shape, split_plan(shape, mask));
+}
+
+int lcattn_fwd_fp8_vt(const lcattn_shape* shape, const void* q, const void* k, const void* vt, float q_scale,
+                      float k_scale, float v_scale, const void* tile_meta, const lcattn_mask_desc* mask, float scale,
+                      void* o, float* lse, void* workspace, size_t workspace_bytes, lcattn_stream_t stream) {
+  return fwd8_run(shape, q, k, vt, q_scale, k_scale, v_scale, tile_meta, mask, scale, o, lse, workspace,
+                  workspace_bytes, reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t lcattn_fwd_fp8_workspace_size(const lcattn_shape* shape) {
+  if (validate_shape(shape) != LCATTN_OK || validate_fp8(shape) != LCATTN_OK) return 0;
+  return (size_t)(fwd8_ws_bytes(shape) + fwd8_split_bytes_max(shape));
+}
+
+int lcattn_fwd_fp8(const lcattn_shape* shape, const void* q, const void* k, const void* v, float q_scale,
+                   float k_scale, float v_scale, const void* tile_meta, const lcattn_mask_desc* mask, float scale,
+                   void* o, float* lse, void* workspace, size_t workspace_bytes, lcattn_stream_t stream) {
+  lcattn_tile_meta_layout L;
+  int st = layout_of(shape, mask, &L);
+  if (st) return st;
+  if ((st = validate_fp8(shape))) return st;
+  if (!v || !workspace) return LCATTN_ERR_INVALID_ARG;
+  if (!aligned16(v) || !aligned16(workspace)) return LCATTN_ERR_UNSUPPORTED;
+  // Workspace: V^T first, then the split partials (when the shape takes the split path).
+  const int64_t vt_bytes = fwd8_ws_bytes(shape);
+  const int64_t split_bytes = split_ws_bytes(shape, split_plan(shape, mask));
+  if ((int64_t)workspace_bytes < vt_bytes + split_bytes) return LCATTN_ERR_WORKSPACE;
+  for (float x : {scale, q_scale, k_scale, v_scale})
+    if (!(x > 0.f) || !(x < 1e30f)) return LCATTN_ERR_INVALID_ARG;
+  if (!q || !k || !o || !lse || !tile_meta) return LCATTN_ERR_INVALID_ARG;
+  const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  if ((st = lcattn_fp8_transpose_v(shape, v, ws, stream))) return st;
+  return fwd8_run(shape, q, k, ws, q_scale, k_scale, v_scale, tile_meta, mask, scale, o, lse,
+                  split_bytes > 0 ? ws + vt_bytes : nullptr, (size_t)split_bytes, cs);
 }
 
 size_t lcattn_bwd_workspace_size(const lcattn_shape* shape) {

@@ -19,6 +19,9 @@
 // issued one tile ahead of PV, P written
 // over S as bf16 and read from TMEM by the PV GEMM.  Column-bounds masks only
 // (the packed rows of different heads share the mask).
+// The same kernel runs e4m3 Q and K with V^T tiles (F8): kind::f8f6f4
+// products, P as e4m3(16 P) under a rescale threshold of 4 -- the arithmetic
+// of the persistent forward's e4m3 instantiation.
 #include <cuda_bf16.h>
 
 #include "lcattn_internal.cuh"
@@ -33,24 +36,32 @@ using namespace dev;
 // columns); the K/V ring holds 128 KB.  A ring entry is a whole K or V tile for
 // D <= 128 (8 or 4 stages) and a head-dim half of one at D = 256 (4 stages of
 // 32 KB, so the next tile's K streams in while this tile is consumed).
-template <int D> struct SplitGeom {
-  static constexpr int kTileBytes = 128 * D * 2;
-  static constexpr int kBoxes = D / 64;
+// F8 (e4m3, D = 128): a tile is 128 rows x 128 bytes, one box; the V entries
+// are V^T tiles (keys contiguous), 8 stages of 16 KB.
+template <int D, bool F8 = false> struct SplitGeom {
+  static_assert(!F8 || D == 128, "the e4m3 path is built for head dim 128");
+  static constexpr int kElem = F8 ? 1 : 2;
+  static constexpr int kTileBytes = 128 * D * kElem;
+  static constexpr int kBoxCols = F8 ? 128 : 64;   // elements per 128-byte box row
+  static constexpr int kBoxes = D / kBoxCols;
   static constexpr int kParts = D == 256 ? 2 : 1;
   static constexpr int kEntryBytes = kTileBytes / kParts;
   static constexpr int kBoxesPerEntry = kBoxes / kParts;
-  static constexpr int kStages = D == 64 ? 8 : 4;
+  static constexpr int kStages = (D == 64 || F8) ? 8 : 4;
+  static constexpr int kSSteps = D * kElem / 32 / kParts;  // S k-steps of 32 bytes per entry
+  static constexpr int kPvSteps = F8 ? 4 : 8;              // PV k-steps (8 TMEM columns of P each)
+  static constexpr float kRescaleThreshold = F8 ? 4.0f : 8.0f;
+  static constexpr float kLog2PScale = F8 ? 4.0f : 0.0f;   // e4m3 P is stored as P * 2^4
 };
 constexpr int kHalfBytes = 16384;
 constexpr int kThreads = 256;  // warps 0-3 softmax, 4 producer, 5 MMA, 6-7 idle
-constexpr float kRescaleThreshold = 8.0f;
 
-template <int D>
+template <int D, bool F8 = false>
 struct SplitSmem {
-  static constexpr int kStages = SplitGeom<D>::kStages;
-  static constexpr int kTileBytes = SplitGeom<D>::kTileBytes;
+  static constexpr int kStages = SplitGeom<D, F8>::kStages;
+  static constexpr int kTileBytes = SplitGeom<D, F8>::kTileBytes;
   alignas(1024) uint8_t q[kTileBytes];
-  alignas(1024) uint8_t kv[kStages][SplitGeom<D>::kEntryBytes];
+  alignas(1024) uint8_t kv[kStages][SplitGeom<D, F8>::kEntryBytes];
   int4 bnd[2][kBN];
   uint64_t bnd_ready[2];
   uint64_t q_full;
@@ -87,22 +98,23 @@ __device__ __forceinline__ Unit unit_of(const SplitArgs& a, int u) {
   return x;
 }
 
-template <int D>
+template <int D, bool F8>
 __global__ void __launch_bounds__(kThreads, 1)
 split_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
              const __grid_constant__ CUtensorMap tmV, const __grid_constant__ SplitArgs a) {
-  constexpr int kStages = SplitGeom<D>::kStages;
-  constexpr int kTileBytes = SplitGeom<D>::kTileBytes;
-  constexpr int kBoxes = SplitGeom<D>::kBoxes;
-  constexpr int kParts = SplitGeom<D>::kParts;
-  constexpr int kEntryBytes = SplitGeom<D>::kEntryBytes;
-  constexpr int kBoxesPerEntry = SplitGeom<D>::kBoxesPerEntry;
+  constexpr int kStages = SplitGeom<D, F8>::kStages;
+  constexpr int kTileBytes = SplitGeom<D, F8>::kTileBytes;
+  constexpr int kBoxes = SplitGeom<D, F8>::kBoxes;
+  constexpr int kParts = SplitGeom<D, F8>::kParts;
+  constexpr int kEntryBytes = SplitGeom<D, F8>::kEntryBytes;
+  constexpr int kBoxesPerEntry = SplitGeom<D, F8>::kBoxesPerEntry;
+  constexpr int kBoxCols = SplitGeom<D, F8>::kBoxCols;
   constexpr int kE = 2 * kParts;  // ring entries per key tile
   // Half-tile entries: K runs a tile ahead of V (K(0), K(1), V(0), ..., V(n-1)),
   // the order the MMA warp consumes them.
   constexpr bool kAhead = kParts == 2;
   extern __shared__ uint8_t smem_raw[];
-  SplitSmem<D>& sm = *reinterpret_cast<SplitSmem<D>*>(
+  SplitSmem<D, F8>& sm = *reinterpret_cast<SplitSmem<D, F8>*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const ProblemDev& pr = a.pr;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -160,9 +172,14 @@ split_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
         if (!__all_sync(0xffffffffu, okw)) return false;
       }
       mbar_expect_tx_e(&sm.kv_full[stage], kEntryBytes);
-      for (int bx = 0; bx < kBoxesPerEntry; ++bx)
-        tma_load_4d_e(sm.kv[stage] + bx * kHalfBytes, tm, &sm.kv_full[stage], 128 * part + 64 * bx,
-                      un.g, kt * kBN, un.b);
+      if (F8 && tm == &tmV) {
+        // V^T [B][Hkv][128][keys]: the 128 keys of tile kt x all 128 head-dim rows.
+        tma_load_4d_e(sm.kv[stage], tm, &sm.kv_full[stage], kt * kBN, 0, un.g, un.b);
+      } else {
+        for (int bx = 0; bx < kBoxesPerEntry; ++bx)
+          tma_load_4d_e(sm.kv[stage] + bx * kHalfBytes, tm, &sm.kv_full[stage], 128 * part + kBoxCols * bx,
+                        un.g, kt * kBN, un.b);
+      }
       ++t;
       return true;
     };
@@ -178,7 +195,7 @@ split_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
         // Packed query tile: Gp heads x Rq positions; row = position * Gp + head.
         mbar_expect_tx_e(&sm.q_full, kTileBytes);
         for (int bx = 0; bx < kBoxes; ++bx)
-          tma_load_4d_e(sm.q + bx * kHalfBytes, &tmQ, &sm.q_full, 64 * bx, h_first, qs0, un.b);
+          tma_load_4d_e(sm.q + bx * kHalfBytes, &tmQ, &sm.q_full, kBoxCols * bx, h_first, qs0, un.b);
       }
     }
     if (kAhead && ok)  // the last tile's V
@@ -195,11 +212,43 @@ split_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
     }
   } else if (warp == 5 && n > 0) {
     // ---------------------------------------------------------------- MMA issuer
-    const uint32_t idesc_qk = idesc_bf16_f32(128, 128, false, false);
-    const uint32_t idesc_pv = idesc_bf16_f32(128, D / kParts, false, true);
+    const uint32_t idesc_qk = F8 ? idesc_e4m3_f32(128, 128) : idesc_bf16_f32(128, 128, false, false);
+    const uint32_t idesc_pv = F8 ? idesc_e4m3_f32(128, D) : idesc_bf16_f32(128, D / kParts, false, true);
     const uint64_t dq = sdesc_sw128(smem_u32(sm.q), 16, 1024);
     const uint64_t dk0 = sdesc_sw128(smem_u32(sm.kv[0]), 16, 1024);
-    const uint64_t dv0 = sdesc_sw128(smem_u32(sm.kv[0]), kHalfBytes, 1024);
+    // V tile read MN-major (bf16), or V^T tile read K-major (e4m3).
+    const uint64_t dv0 = sdesc_sw128(smem_u32(sm.kv[0]), F8 ? 16u : static_cast<uint32_t>(kHalfBytes), 1024);
+    // O (+)= P V: A = P from TMEM (8 columns per k-step), B = V (MN-major, 16
+    // key rows per k-step) or V^T (K-major, 32 keys per k-step).
+    auto gemm_pv = [&](uint32_t tOp, uint32_t tP, uint64_t vb, uint32_t acc) {
+      if constexpr (F8) {
+        mma8_ts_er(tOp, tP, vb, idesc_pv, acc);
+        #pragma unroll
+        for (int kk = 1; kk < SplitGeom<D, F8>::kPvSteps; ++kk)
+          mma8_ts_er(tOp, tP + kk * 8, sdesc_add(vb, kk * 32), idesc_pv, 1u);
+      } else {
+        mma_ts_er(tOp, tP, vb, idesc_pv, acc);
+        #pragma unroll
+        for (int kk = 1; kk < SplitGeom<D, F8>::kPvSteps; ++kk)
+          mma_ts_e<1>(tOp, tP + kk * 8, sdesc_add(vb, kk * 2048), idesc_pv);
+      }
+    };
+    // S (+)= Q K^T over one ring entry: k-steps of 32 bytes, the next box after four.
+    auto gemm_s = [&](uint32_t tS, uint64_t qp, uint64_t kb, bool first) {
+      if constexpr (F8) {
+        if (first) mma8_ss_e<0>(tS, qp, kb, idesc_qk);
+        else mma8_ss_e<1>(tS, qp, kb, idesc_qk);
+      } else {
+        if (first) mma_ss_e<0>(tS, qp, kb, idesc_qk);
+        else mma_ss_e<1>(tS, qp, kb, idesc_qk);
+      }
+      #pragma unroll
+      for (int kk = 1; kk < SplitGeom<D, F8>::kSSteps; ++kk) {
+        const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
+        if constexpr (F8) mma8_ss_e<1>(tS, sdesc_add(qp, off), sdesc_add(kb, off), idesc_qk);
+        else mma_ss_e<1>(tS, sdesc_add(qp, off), sdesc_add(kb, off), idesc_qk);
+      }
+    };
     const uint32_t tO = tmem + 256;
     bool ok = __all_sync(0xffffffffu, mbar_wait(&sm.q_full, 0, abort_flag, gstatus,
                                                 LCATTN_ERR_DEVICE_TIMEOUT));
@@ -217,9 +266,7 @@ split_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
         tc_fence_after();
         const uint64_t vb = sdesc_add(dv0, (tv % kStages) * kEntryBytes);
         const uint32_t tOp = tO + part * (D / kParts);
-        mma_ts_er(tOp, tP, vb, idesc_pv, tt > 0 ? 1u : 0u);
-        #pragma unroll
-        for (int kk = 1; kk < 8; ++kk) mma_ts_e<1>(tOp, tP + kk * 8, sdesc_add(vb, kk * 2048), idesc_pv);
+        gemm_pv(tOp, tP, vb, tt > 0 ? 1u : 0u);
         tc_commit_e(&sm.kv_empty[tv % kStages]);
       }
       tc_commit_e(&sm.o_full);
@@ -238,13 +285,7 @@ split_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
         tc_fence_after();
         const uint64_t kb = sdesc_add(dk0, (tk % kStages) * kEntryBytes);
         const uint64_t qp = sdesc_add(dq, part * kEntryBytes);
-        if (part == 0) mma_ss_e<0>(tS, qp, kb, idesc_qk);
-        else mma_ss_e<1>(tS, qp, kb, idesc_qk);
-        #pragma unroll
-        for (int kk = 1; kk < D / kParts / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
-          mma_ss_e<1>(tS, sdesc_add(qp, off), sdesc_add(kb, off), idesc_qk);
-        }
+        gemm_s(tS, qp, kb, part == 0);
         tc_commit_e(&sm.kv_empty[tk % kStages]);
       }
       if (!ok) break;
@@ -269,6 +310,11 @@ split_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
     int4 rb = make_int4(0, 0, 0, 0);
     if (use_rows && s_pos < pr.Sq) rb = __ldg(a.mask.row_bounds + (int64_t)un.b * pr.Sq + s_pos);
     float m_run = -INFINITY, l_run = 0.f;
+    // A warp whose 32 packed rows all lie past the last query position (decode
+    // rows fill 1/Rq of a tile) only keeps the barriers in step: it stages its
+    // share of the column bounds and releases P without computing it.  Its O
+    // rows are never written out.
+    const bool warp_live = __any_sync(0xffffffffu, s_pos < pr.Sq);
     bool ok = true;
     int n_partial = 0;
     for (int j = 0; j < n; ++j) {
@@ -313,6 +359,10 @@ split_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
       const uint32_t tS = tmem + lane_off + sb * 128;
       ok = mbar_wait(&sm.s_full[sb], (j >> 1) & 1, abort_flag, gstatus, LCATTN_ERR_DEVICE_TIMEOUT);
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+      if (!warp_live) {  // (waiting for S(j) keeps this warp's arrivals on P(j)'s phase)
+        mbar_arrive(&sm.p_full[sb]);
+        continue;
+      }
       tc_fence_after();
       uint32_t xr[128];
       tmem_ld32(tS + 0, xr + 0);
@@ -334,26 +384,43 @@ split_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
       #pragma unroll
       for (int c = 8; c < 128; c += 2) m4[(c >> 1) & 3] = fmax3(m4[(c >> 1) & 3], x[c], x[c + 1]);
       const float m_tile = fmaxf(fmax3(m4[0], m4[1], m4[2]), m4[3]) * sl2;
-      const bool need = m_tile > m_run + kRescaleThreshold;
+      const bool need = m_tile > m_run + SplitGeom<D, F8>::kRescaleThreshold;
       const bool warp_rescale = __any_sync(0xffffffffu, need) && j > 0;
       const float m_new = need ? m_tile : m_run;
       const float alpha = need ? fast_exp2(m_run - m_new) : 1.f;
       m_run = m_new;
       const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
-      const float2 sl2v = make_float2(sl2, sl2), negm = make_float2(-m_use, -m_use);
+      // e4m3 P is P * 2^kLog2PScale, the shift folded into the exponent; l carries
+      // the same factor, which cancels in O / l.
+      const float negm_s = -(m_use - SplitGeom<D, F8>::kLog2PScale);
+      const float2 sl2v = make_float2(sl2, sl2), negm = make_float2(negm_s, negm_s);
       float2 s4[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                       make_float2(0.f, 0.f)};
-      #pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        uint32_t pk[32];
+      if constexpr (F8) {
+        uint32_t pk[32];  // four keys per column
         #pragma unroll
         for (int i = 0; i < 32; ++i) {
-          const float2 y = fma2(make_float2(x[c * 64 + 2 * i], x[c * 64 + 2 * i + 1]), sl2v, negm);
-          const float2 p = make_float2(fast_exp2(y.x), fast_exp2(y.y));
-          s4[i & 3] = add2(s4[i & 3], p);
-          pk[i] = pack_bf16x2(p.x, p.y);
+          const float2 y0 = fma2(make_float2(x[4 * i], x[4 * i + 1]), sl2v, negm);
+          const float2 y1 = fma2(make_float2(x[4 * i + 2], x[4 * i + 3]), sl2v, negm);
+          const float2 p0 = make_float2(fast_exp2(y0.x), fast_exp2(y0.y));
+          const float2 p1 = make_float2(fast_exp2(y1.x), fast_exp2(y1.y));
+          s4[i & 3] = add2(s4[i & 3], add2(p0, p1));
+          pk[i] = pack_e4m3x4(p0.x, p0.y, p1.x, p1.y);
         }
-        tmem_st32(tS + c * 32, pk);
+        tmem_st32(tS, pk);
+      } else {
+        #pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          uint32_t pk[32];
+          #pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const float2 y = fma2(make_float2(x[c * 64 + 2 * i], x[c * 64 + 2 * i + 1]), sl2v, negm);
+            const float2 p = make_float2(fast_exp2(y.x), fast_exp2(y.y));
+            s4[i & 3] = add2(s4[i & 3], p);
+            pk[i] = pack_bf16x2(p.x, p.y);
+          }
+          tmem_st32(tS + c * 32, pk);
+        }
       }
       const float2 s2 = add2(add2(s4[0], s4[1]), add2(s4[2], s4[3]));
       l_run = l_run * alpha + (s2.x + s2.y);
@@ -384,9 +451,9 @@ split_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
                                                  LCATTN_ERR_DEVICE_TIMEOUT));
       tc_fence_after();
     }
-    if (ok && (have_o || n == 0)) {
+    if (ok && warp_live && (have_o || n == 0)) {
       const bool live = l_run > 0.f;
-      const float inv = live ? 1.f / l_run : 0.f;
+      const float inv = live ? a.o_scale / l_run : 0.f;
       // O in batches that fit the registers (all of it up to D = 128).
       constexpr int kBatch = D <= 128 ? D : 32;
       float4* dst = reinterpret_cast<float4*>(
@@ -411,7 +478,7 @@ split_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CU
       }
       if (s_pos < pr.Sq) {
         a.lse_part[(((int64_t)un.c * pr.B + un.b) * pr.Hq + h) * pr.Sq + s_pos] =
-            live ? (m_run + __log2f(l_run)) * 0.69314718055994531f : -INFINITY;
+            live ? (m_run - SplitGeom<D, F8>::kLog2PScale + __log2f(l_run)) * 0.69314718055994531f : -INFINITY;
       }
     }
   }
@@ -478,20 +545,20 @@ int split_heads_packed(int G) {
 
 namespace {
 
-template <int D>
+template <int D, bool F8 = false>
 cudaError_t launch_split_d(const CUtensorMap& tq_packed, const CUtensorMap& tk,
                            const CUtensorMap& tv, const SplitArgs& a, cudaStream_t st) {
   static bool attr_done = false;
-  const size_t smem = sizeof(SplitSmem<D>) + 1024;
+  const size_t smem = sizeof(SplitSmem<D, F8>) + 1024;
   if (!attr_done) {
     cudaError_t e =
-        cudaFuncSetAttribute(split_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        cudaFuncSetAttribute(split_kernel<D, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     attr_done = true;
   }
   const int64_t units = (int64_t)a.pr.B * a.pr.Hkv * (a.pr.G / a.Gp) * a.nQc * a.splits;
   if (units > 0x7fffffffLL) return cudaErrorInvalidValue;
-  split_kernel<D><<<(unsigned)units, kThreads, smem, st>>>(tq_packed, tk, tv, a);
+  split_kernel<D, F8><<<(unsigned)units, kThreads, smem, st>>>(tq_packed, tk, tv, a);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int64_t rows = (int64_t)a.pr.B * a.pr.Sq * a.pr.Hq;
@@ -508,6 +575,12 @@ cudaError_t launch_fwd_split(const CUtensorMap& tq_packed, const CUtensorMap& tk
   if (a.pr.D == 64) return launch_split_d<64>(tq_packed, tk, tv, a, st);
   if (a.pr.D == 256) return launch_split_d<256>(tq_packed, tk, tv, a, st);
   return launch_split_d<128>(tq_packed, tk, tv, a, st);
+}
+
+cudaError_t launch_fwd_split_e4m3(const CUtensorMap& tq_packed, const CUtensorMap& tk, const CUtensorMap& tvt,
+                                  const SplitArgs& a, cudaStream_t st) {
+  if (a.pr.D != 128) return cudaErrorInvalidValue;
+  return launch_split_d<128, true>(tq_packed, tk, tvt, a, st);
 }
 
 }  // namespace lcattn

@@ -77,6 +77,7 @@ struct SplitArgs {
   int Rq;                   // query positions per tile, Gp * Rq = 128
   int nQc;                  // query chunks, ceil(Sq / Rq)
   int splits;               // slices of each key-tile list
+  float o_scale = 1.f;      // factor of O / l (e4m3: the V factor)
   float* o_part;            // [splits][B][Sq][Hq][128] fp32, O / l of each slice
   float* lse_part;          // [splits][B][Hq][Sq]
   void* o;
@@ -86,6 +87,11 @@ struct SplitArgs {
 int split_heads_packed(int G);
 cudaError_t launch_fwd_split(const CUtensorMap& tq_packed, const CUtensorMap& tk,
                              const CUtensorMap& tv, const SplitArgs& a, cudaStream_t st);
+// The same with e4m3 Q (packed box of 128 bytes x Gp heads x Rq rows) and K,
+// and `tvt` mapping V^T [B][Hkv][128][Skp] e4m3; a.scale_log2 carries the Q and
+// K factors, a.o_scale the V factor.  D = 128.
+cudaError_t launch_fwd_split_e4m3(const CUtensorMap& tq_packed, const CUtensorMap& tk, const CUtensorMap& tvt,
+                                  const SplitArgs& a, cudaStream_t st);
 
 struct BwdArgs {
   ProblemDev pr;

@@ -249,6 +249,7 @@ class Workload:
     Sq: Optional[int] = None     # query length when it differs from the key length N
     forward_only: bool = False   # decode-style rows: the step is the forward alone
     fp8: bool = False            # e4m3 Q, K, V with per-tensor factors (forward only)
+    vt_cache: bool = False       # e4m3 V kept transposed, as a K/V cache would hold it: the step reads V^T
 
     @property
     def q_len(self) -> int:
@@ -269,6 +270,8 @@ def workload(name: str, seed: int = 0) -> Workload:
       captures of the 128K kernels at a size a multi-pass capture can hold.
     * ``dense_8k_fp8``: as ``dense_8k`` with e4m3 Q, K, V (per-tensor factors,
       :func:`qkv_fp8`), forward only.
+    * ``decode_32k_fp8``: as ``decode_32k`` with e4m3 Q, K, V, and V kept
+      transposed (an e4m3 K/V cache): the step is the forward on Q, K and V^T.
     * ``dense_8k_hd64``: as ``dense_8k`` with head dim 64 (the variant next to the
       pages' 128).
     * ``dense_8k_hd256``: B=1, N=8192, GQA 32:8, head dim 256, FULL and CAUSAL.
@@ -317,6 +320,9 @@ def workload(name: str, seed: int = 0) -> Workload:
     if name == "dense_8k_fp8":
         return Workload(name, 1, 8192, 64, 8, 128, [MaskSpec("FULL"), MaskSpec("CAUSAL")], forward_only=True,
                         fp8=True)
+    if name == "decode_32k_fp8":
+        return Workload(name, 8, 32768, 64, 8, 128, [MaskSpec("CAUSAL")], Sq=1, forward_only=True, fp8=True,
+                        vt_cache=True)
     if name == "dense_8k_hd64":
         return Workload(name, 1, 8192, 64, 8, 64, [MaskSpec("FULL"), MaskSpec("CAUSAL")])
     if name == "dense_8k_hd256":
@@ -334,5 +340,5 @@ def workload(name: str, seed: int = 0) -> Workload:
 
 
 WORKLOADS = ("causal_1k", "dense_8k", "docs_32k", "hetero_16k", "long_128k", "long_128k_8to1", "dynamic_32k",
-             "decode_32k", "dense_8k_fp8",
+             "decode_32k", "dense_8k_fp8", "decode_32k_fp8",
              "dense_8k_hd64", "dense_8k_hd256", "dense_8k_hd256_fwd")

@@ -147,3 +147,51 @@ def test_fp8_views_of_a_fused_qkv_buffer():
     O, L = fp8_ref.attention_fwd_fp8(x["q8"].numpy(), x["k8"].numpy(), x["v8"].numpy(), x["q_scale"],
                                      x["k_scale"], x["v_scale"], spec, 1.0 / math.sqrt(128))
     _check(o_view, lse_view, O, L)
+
+
+@pytest.mark.parametrize("B,Sq,Sk,Hq,Hkv,kind", [(2, 1, 3000, 16, 2, "CAUSAL"), (1, 40, 2500, 4, 4, "FULL"),
+                                                 (3, 16, 1100, 8, 1, "CAUSAL_SLIDING_WINDOW")])
+def test_fp8_split_kv_decode_rows(B, Sq, Sk, Hq, Hkv, kind):
+    """Short query sides take the e4m3 split-KV path (checked: its workspace is
+    non-zero): lcattn_fwd_fp8 and lcattn_fwd_fp8_vt on a V^T made once by
+    lcattn_fp8_transpose_v give the same bits, and match the oracle."""
+    spec = MaskSpec(kind, {"window": Sk // 3} if "WINDOW" in kind else {})
+    x = qkv_fp8(B, Sq, Hq, Hkv, 128, seed=23, Sk=Sk)
+    dev = {k: (t.cuda() if torch.is_tensor(t) else t) for k, t in x.items()}
+    mask = lc.DeviceMask(spec, Sq, Hq, B, Sk=Sk)
+    shape = lc.make_shape(dev["q8"], dev["k8"], dev["v8"])
+    assert lc.library().lcattn_fwd_fp8_vt_workspace_size(lc.ctypes.byref(shape), lc.ctypes.byref(mask.desc)) > 0
+    meta = lc.lcattn_mask_compile(shape, mask)
+    o1, l1 = lc.lcattn_fwd_fp8(dev["q8"], dev["k8"], dev["v8"], x["q_scale"], x["k_scale"], x["v_scale"], mask, meta)
+    vt = lc.lcattn_fp8_transpose_v(dev["v8"], dev["k8"], dev["q8"])
+    o2, l2 = lc.lcattn_fwd_fp8_vt(dev["q8"], dev["k8"], vt, dev["v8"], x["q_scale"], x["k_scale"], x["v_scale"],
+                                  mask, meta)
+    torch.cuda.synchronize()
+    assert lc.lcattn_read_status(meta) == 0
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    O, L = fp8_ref.attention_fwd_fp8(x["q8"].numpy(), x["k8"].numpy(), x["v8"].numpy(), x["q_scale"],
+                                     x["k_scale"], x["v_scale"], spec, 1.0 / math.sqrt(128))
+    _check(o1, l1, O, L)
+
+
+def test_fp8_vt_entry_regular_path_without_workspace():
+    """A square problem takes the persistent kernel: lcattn_fwd_fp8_vt needs no
+    workspace there, and its V^T input gives the bits of lcattn_fwd_fp8."""
+    B, N, Hq, Hkv = 1, 520, 4, 2
+    x = qkv_fp8(B, N, Hq, Hkv, 128, seed=29)
+    dev = {k: (t.cuda() if torch.is_tensor(t) else t) for k, t in x.items()}
+    spec = MaskSpec("CAUSAL_DOCUMENT", {"doc_lens": segment_lengths(N, 60, 300, 2)})
+    mask = lc.DeviceMask(spec, N, Hq, B)
+    shape = lc.make_shape(dev["q8"], dev["k8"], dev["v8"])
+    assert lc.library().lcattn_fwd_fp8_vt_workspace_size(lc.ctypes.byref(shape), lc.ctypes.byref(mask.desc)) == 0
+    meta = lc.lcattn_mask_compile(shape, mask)
+    o1, l1 = lc.lcattn_fwd_fp8(dev["q8"], dev["k8"], dev["v8"], x["q_scale"], x["k_scale"], x["v_scale"], mask, meta)
+    vt = lc.lcattn_fp8_transpose_v(dev["v8"], dev["k8"], dev["q8"])
+    o2, l2 = lc.lcattn_fwd_fp8_vt(dev["q8"], dev["k8"], vt, dev["v8"], x["q_scale"], x["k_scale"], x["v_scale"],
+                                  mask, meta)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    # V^T itself: key-contiguous rows, zero padding up to a multiple of 16 keys.
+    v = dev["v8"]
+    assert torch.equal(vt[:, :, :, :N], v.permute(0, 2, 3, 1))
+    assert (vt[:, :, :, N:] == 0).all()
