@@ -854,10 +854,8 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
         #pragma unroll
         for (int c4 = 0; c4 < 8; ++c4) {
           const float4 da = dv4[c4], db = dv4[8 + c4];
-          // P' (bf16 pairs -> fp32) times (dP - D), on column pairs.
-          auto unpack = [](uint32_t w) {
-            return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
-          };
+          // dP - D on column pairs (fp32), rounded to bf16 pairs, times the bf16
+          // P' pairs on the packed bf16 ALU: dS^T leaves in bf16 either way.
           const float2 ta0 = add2(make_float2(__uint_as_float(d0[4 * c4]), __uint_as_float(d0[4 * c4 + 1])),
                                   make_float2(da.x, da.y));
           const float2 ta1 = add2(make_float2(__uint_as_float(d0[4 * c4 + 2]), __uint_as_float(d0[4 * c4 + 3])),
@@ -866,13 +864,10 @@ dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUt
                                   make_float2(db.x, db.y));
           const float2 tb1 = add2(make_float2(__uint_as_float(d1[4 * c4 + 2]), __uint_as_float(d1[4 * c4 + 3])),
                                   make_float2(db.z, db.w));
-          const float2 za0 = mul2(unpack(pk[2 * c4]), ta0), za1 = mul2(unpack(pk[2 * c4 + 1]), ta1);
-          const float2 zb0 = mul2(unpack(pk[16 + 2 * c4]), tb0), zb1 = mul2(unpack(pk[16 + 2 * c4 + 1]), tb1);
-          const float sa[4] = {za0.x, za0.y, za1.x, za1.y}, sb[4] = {zb0.x, zb0.y, zb1.x, zb1.y};
-          dk[2 * c4] = pack_bf16x2(sa[0], sa[1]);
-          dk[2 * c4 + 1] = pack_bf16x2(sa[2], sa[3]);
-          dk[16 + 2 * c4] = pack_bf16x2(sb[0], sb[1]);
-          dk[16 + 2 * c4 + 1] = pack_bf16x2(sb[2], sb[3]);
+          dk[2 * c4] = mul_bf16x2(pk[2 * c4], pack_bf16x2(ta0.x, ta0.y));
+          dk[2 * c4 + 1] = mul_bf16x2(pk[2 * c4 + 1], pack_bf16x2(ta1.x, ta1.y));
+          dk[16 + 2 * c4] = mul_bf16x2(pk[16 + 2 * c4], pack_bf16x2(tb0.x, tb0.y));
+          dk[16 + 2 * c4 + 1] = mul_bf16x2(pk[16 + 2 * c4 + 1], pack_bf16x2(tb1.x, tb1.y));
         }
         tmem_st32(tP + c0, dk);
         if (kDq) {

@@ -380,16 +380,14 @@ dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUten
         tc_fence_before();
         mbar_arrive(&sm.dp_free);  // dP(j+1) may overwrite the dP columns now
         const float2 ndv = make_float2(nd, nd);
-        auto unpack = [](uint32_t w) {
-          return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
-        };
+        // dP - D on column pairs (fp32), rounded to bf16 pairs, times the bf16 P'
+        // pairs on the packed bf16 ALU (dS' leaves in bf16 either way).
         #pragma unroll
         for (int c2 = 0; c2 < 16; ++c2) {
           const float2 ta = add2(make_float2(__uint_as_float(d0[2 * c2]), __uint_as_float(d0[2 * c2 + 1])), ndv);
           const float2 tb = add2(make_float2(__uint_as_float(d1[2 * c2]), __uint_as_float(d1[2 * c2 + 1])), ndv);
-          const float2 za = mul2(unpack(pk[c2]), ta), zb = mul2(unpack(pk[16 + c2]), tb);
-          dsk[c2] = pack_bf16x2(za.x, za.y);
-          dsk[16 + c2] = pack_bf16x2(zb.x, zb.y);
+          dsk[c2] = mul_bf16x2(pk[c2], pack_bf16x2(ta.x, ta.y));
+          dsk[16 + c2] = mul_bf16x2(pk[16 + c2], pack_bf16x2(tb.x, tb.y));
         }
       }
       tmem_st32(tS + c0, dsk);  // columns [64x, 64x + 32) of this S buffer: only this warpgroup's
