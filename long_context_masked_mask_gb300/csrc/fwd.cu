@@ -99,7 +99,10 @@ struct FwdSmem {
   uint64_t drain;
   uint64_t stg_full[2];  // a slot's staging box is written (128 arrivals; one phase per epilogue)
   uint64_t stg_free[2];  // ... and read by its TMA stores (one phase per epilogue)
-  int items[kItemQ];           // item indices handed from the producer to the other roles
+  // Items handed from the producer to the other roles: (index, query tile, key
+  // tiles, -); the producer has read the tile metadata, so the others need no
+  // dependent global loads at an item's start.  Index -1 ends the sequence.
+  int4 items[kItemQ];
   uint64_t item_full[kItemQ];
   uint64_t item_empty[kItemQ];
   uint32_t tmem_base;
@@ -200,7 +203,7 @@ struct FwdItem {
 // in blocks of `hb` heads (whole GQA groups) of one batch entry, rank-major
 // within a block; the items in flight then cover a few heads' K/V, which stays
 // in L2 (with MHA every head has its own K/V, far more than L2 holds).
-__device__ __forceinline__ FwdItem fwd_item(const FwdArgs& a, int hpc, int hb, int idx) {
+__device__ __forceinline__ FwdItem fwd_item(const FwdArgs& a, int hpc, int hb, int idx, int* rank_out = nullptr) {
   FwdItem it;
   int rank;
   if (hpc == 1) {
@@ -221,8 +224,26 @@ __device__ __forceinline__ FwdItem fwd_item(const FwdArgs& a, int hpc, int hb, i
   }
   const int lh = a.meta.nH == 1 ? 0 : it.h0;
   const int64_t lbase = ((int64_t)it.b * a.meta.nH + lh) * a.meta.nQt;
+  if (rank_out) {  // placement only: the caller supplies qt and n
+    *rank_out = rank;
+    it.qt = 0; it.n = 0; it.list = nullptr;
+    return it;
+  }
   it.qt = __ldg(a.meta.fwd_ord + lbase + rank);
   it.n = __ldg(a.meta.fwd_cnt + lbase + it.qt);
+  it.list = a.meta.fwd_lst + (lbase + it.qt) * a.meta.nKt;
+  return it;
+}
+
+// The item of a queue entry (index, query tile, key tiles): placement by
+// arithmetic, no metadata loads.
+__device__ __forceinline__ FwdItem fwd_item_queued(const FwdArgs& a, int hpc, int hb, int4 q) {
+  int rank = 0;
+  FwdItem it = fwd_item(a, hpc, hb, q.x, &rank);
+  const int lh = a.meta.nH == 1 ? 0 : it.h0;
+  const int64_t lbase = ((int64_t)it.b * a.meta.nH + lh) * a.meta.nQt;
+  it.qt = q.y;
+  it.n = q.z;
   it.list = a.meta.fwd_lst + (lbase + it.qt) * a.meta.nKt;
   return it;
 }
@@ -337,7 +358,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
       return v < static_cast<unsigned long long>(total) ? static_cast<int>(v) : -1;
     };
     int published = 0;
-    auto publish = [&](int idx) -> bool {
+    auto publish = [&](int idx, int qt, int nk) -> bool {
       const int e = published % kItemQ;
       if (published >= kItemQ) {
         const bool okw = mbar_wait(&sm.item_empty[e], ((published / kItemQ) - 1) & 1, abort_flag,
@@ -345,7 +366,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
         if (!__all_sync(0xffffffffu, okw)) return false;
       }
       if (lane == 0) {
-        sm.items[e] = idx;
+        sm.items[e] = make_int4(idx, qt, nk, 0);
         mbar_arrive(&sm.item_full[e]);  // release: the index is visible to whoever sees the phase
       }
       __syncwarp();
@@ -394,22 +415,26 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
     };
     int prev_kt = -1, prev_b = 0, prev_g = 0;  // K ahead of V: the tile whose V is still to come
     int cur = fetch();
-    int cur_n = cur >= 0 ? fwd_item(a, hpc, hb, cur).n : 0;  // key tiles of item `cur`
+    FwdItem cur_it{};  // item `cur` (its metadata read once, here)
+    if (cur >= 0) cur_it = fwd_item(a, hpc, hb, cur);
+    int cur_n = cur >= 0 ? cur_it.n : 0;  // key tiles of item `cur`
     while (ok) {
       if (cur >= 0 && cur_n == 0) {  // an empty item: written here, never queued
-        zero_item(fwd_item(a, hpc, hb, cur));
+        zero_item(cur_it);
         cur = fetch();
-        cur_n = cur >= 0 ? fwd_item(a, hpc, hb, cur).n : 0;
+        if (cur >= 0) cur_it = fwd_item(a, hpc, hb, cur);
+        cur_n = cur >= 0 ? cur_it.n : 0;
         continue;
       }
-      if (!publish(cur)) { ok = false; break; }
+      if (!publish(cur, cur >= 0 ? cur_it.qt : 0, cur_n)) { ok = false; break; }
       if (cur < 0) break;
       const int nxt = fetch();
-      const FwdItem it = fwd_item(a, hpc, hb, cur);
+      const FwdItem it = cur_it;
       cur = nxt;
       if (nxt >= 0) {
         // Warm L2 with the next item's query rows while this item runs.
         const FwdItem nx = fwd_item(a, hpc, hb, nxt);
+        cur_it = nx;
         cur_n = nx.n;
         if (nx.n > 0)
           for (int s = 0; s < hpc; ++s)
@@ -575,11 +600,11 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
           ok = mbar_wait(&sm.item_full[e], (k / kItemQ) & 1, abort_flag, gstatus,
                          LCATTN_ERR_DEVICE_TIMEOUT);
           if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-          const int idx = sm.items[e];
+          const int4 iq = sm.items[e];
           __syncwarp();
           if (lane == 0) mbar_arrive(&sm.item_empty[e]);
-          if (idx < 0) break;
-          const int n = fwd_item(a, hpc, hb, idx).n;
+          if (iq.x < 0) break;
+          const int n = iq.z;
           if (n == 0) continue;
           const int qb = kQBufs == 2 ? (nq & 1) : 0;
           const int quse = kQBufs == 2 ? (nq >> 1) : nq;
@@ -619,11 +644,11 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
         ok = mbar_wait(&sm.item_full[e], (k / kItemQ) & 1, abort_flag, gstatus,
                        LCATTN_ERR_DEVICE_TIMEOUT);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-        const int idx = sm.items[e];
+        const int4 iq = sm.items[e];
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm.item_empty[e]);
-        if (idx < 0) break;
-        const int n = fwd_item(a, hpc, hb, idx).n;
+        if (iq.x < 0) break;
+        const int n = iq.z;
         if (n == 0) continue;
         for (int j = 0; j < n; ++j, ++T) {
           const int tk = 2 * T, tv = 2 * T - 1;
@@ -719,11 +744,11 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
         ok = mbar_wait(&sm.item_full[e], (k / kItemQ) & 1, abort_flag, gstatus,
                        LCATTN_ERR_DEVICE_TIMEOUT);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-        const int idx = sm.items[e];
+        const int4 iq = sm.items[e];
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm.item_empty[e]);
-        if (idx < 0) break;
-        const FwdItem it = fwd_item(a, hpc, hb, idx);
+        if (iq.x < 0) break;
+        const FwdItem it = fwd_item_queued(a, hpc, hb, iq);
         const int n = it.n, b = it.b;
         if (alt && n > 0) {
           const bool mine = static_cast<int>((pbits >> 2) & 1u) == s;
