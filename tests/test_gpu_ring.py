@@ -147,7 +147,7 @@ def test_shard_descriptor_bits():
 
 
 @pytest.mark.parametrize("kind", ["CAUSAL", "CAUSAL_DOCUMENT", "UNIFORM_BLOCK"])
-@pytest.mark.parametrize("world", [2, 3])
+@pytest.mark.parametrize("world", [2, 3, 8])
 def test_ring_zigzag_layout_matches_oracle(kind, world):
     """Zigzag shards (an early and a late chunk per device): every device
     computes two query chunks against the two K/V chunks it holds per round."""
@@ -157,5 +157,21 @@ def test_ring_zigzag_layout_matches_oracle(kind, world):
     dev = {k: t.cuda() for k, t in x.items()}
     mask = lc.DeviceMask(spec, N, Hq, B)
     out = ring.emulate(dev["q"], dev["k"], dev["v"], mask, world, d_o=dev["do"], layout="zigzag")
+    torch.cuda.synchronize()
+    _check(out, x, spec, D)
+
+
+@pytest.mark.parametrize("kind", ["FULL", "CAUSAL_DOCUMENT"])
+def test_ring_eight_devices_merge_error_stays_in_bounds(kind):
+    """Eight emulated devices: every query row merges eight partial results by
+    LSE (fp32 running O and LSE), and the merged O, LSE and gradients stay
+    within the single-device parity bars (the pages note that Ring P2P's
+    numeric error can accumulate over rounds)."""
+    B, N, Hq, Hkv, D = 1, 1000, 4, 2, 128
+    spec = _spec(kind, N, Hq, seed=4)
+    x = qkv(B, N, Hq, Hkv, D, seed=41)
+    dev = {k: t.cuda() for k, t in x.items()}
+    mask = lc.DeviceMask(spec, N, Hq, B)
+    out = ring.emulate(dev["q"], dev["k"], dev["v"], mask, 8, d_o=dev["do"])
     torch.cuda.synchronize()
     _check(out, x, spec, D)
