@@ -274,6 +274,48 @@ def test_persistent_forward_repeats_exactly():
         assert np.abs(lse[0, h, rows].double().cpu().numpy() - rl).max() <= LSE_MAXABS
 
 
+@pytest.mark.parametrize("case", ["mha_window", "block_sparse_empty_units", "gqa_hd64"])
+def test_backward_many_units(case):
+    """More dK/dV units than SMs (several waves of CTAs), at 2048 rows: every
+    gradient matches the oracle, and repeated calls give identical dK and dV
+    bits (each comes out of one unit, or a fixed-order sum of head shares).
+    The block-sparse case has key tiles that no query tile of a head reaches
+    (empty units, whose dK and dV rows are written as zeros); the head-dim-64
+    case splits units over head shares."""
+    D = 128
+    if case == "mha_window":
+        N, Hq, Hkv = 2048, 20, 20
+        spec = MaskSpec("CAUSAL_SLIDING_WINDOW", {"window": 700})
+    elif case == "block_sparse_empty_units":
+        N, Hq, Hkv = 2048, 16, 16
+        nb = N // 128
+        keep = block_keep(Hq, nb, nb, 0.08, seed=4, force_diagonal=False)
+        assert (~keep.any(axis=1)).any()  # some (head, key block) sees no query block
+        spec = MaskSpec("UNIFORM_BLOCK", {"block": 128, "keep": keep})
+    else:
+        N, Hq, Hkv, D = 2048, 32, 16, 64
+        spec = MaskSpec("CAUSAL")
+    assert (N // 128) * Hkv > 152  # more units than SMs, before any head-share split
+    x = qkv(1, N, Hq, Hkv, D, seed=21)
+    dev = {k: t.cuda() for k, t in x.items()}
+    out = lc.attention(dev["q"], dev["k"], dev["v"], spec, d_o=dev["do"])
+    meta = out["tile_meta"]
+    assert lc.lcattn_read_status(meta) == 0
+    f64 = {k: t.double().numpy() for k, t in x.items()}
+    dQ, dK, dV, O, LSE = oracle.attention_bwd(f64["q"], f64["k"], f64["v"], f64["do"], spec, 1.0 / math.sqrt(D))
+    for name, ref in (("dq", dQ), ("dk", dK), ("dv", dV)):
+        g = out[name].double().cpu().numpy()
+        assert np.isfinite(g).all(), name
+        assert relf(g, ref) <= G_RELF, (name, relf(g, ref))
+    first = (out["dk"].clone(), out["dv"].clone())
+    for _ in range(3):
+        dq, dk, dv = lc.lcattn_bwd(dev["q"], dev["k"], dev["v"], out["o"], dev["do"], out["lse"],
+                                   out["mask"], meta)
+        assert lc.lcattn_read_status(meta) == 0
+        assert torch.equal(dk, first[0]) and torch.equal(dv, first[1])
+        assert relf(dq.double().cpu().numpy(), dQ) <= G_RELF
+
+
 @pytest.mark.parametrize("case", ["block_sparse_gqa", "mha_many_items"])
 def test_forward_one_head_items_repeat(case):
     """Work items that carry one query head run S one tile ahead of PV with S
