@@ -71,11 +71,17 @@ template <int D, bool F8 = false> struct FwdGeom {
 constexpr int kItemQ = 4;           // depth of the work-item queue (producer -> other roles)
 constexpr int kHalfBytes = 16384;   // one 64-column TMA box of 128 rows
 constexpr int kThreads = 384;        // 3 warpgroups
-// Register split (launch: 384 threads x 168): softmax warpgroups 216 each,
-// producer/MMA warpgroup 72.  128 * (216 + 216 + 72) = 384 * 168.
-constexpr int kRegsSoftmax = 216;
-constexpr int kRegsOther = 72;
-static_assert(128 * (2 * kRegsSoftmax + kRegsOther) <= kThreads * 168, "register split");
+// Register split (launch: 384 threads x 168): softmax warpgroups 216 each and
+// producer/MMA warpgroup 72 for bf16 two-head items at head dim 128; 200 and
+// 104 for the other instances, whose producer/MMA loops spill at 72.  Same-box
+// A/B of 200 / 104 against 216 / 72: one-head items 3-4% faster, head dim 64
+// 1.3%, e4m3 0.5-1%; bf16 two-head items at head dim 128 1.4-1.9% slower.
+template <int D, int HPC, bool F8> struct FwdRegs {
+  static constexpr bool kWide = D == 128 && HPC == 2 && !F8;
+  static constexpr int kSoftmax = kWide ? 216 : 200;
+  static constexpr int kOther = kWide ? 72 : 104;
+  static_assert(128 * (2 * kSoftmax + kOther) <= kThreads * 168, "register split");
+};
 
 template <int D, bool F8 = false>
 struct FwdSmem {
@@ -322,7 +328,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
   const uint32_t tmem = sm.tmem_base;
   volatile int* abort_flag = &sm.abort_flag;
   if (warp >= 8) {
-    regs_dec<kRegsOther>();
+    regs_dec<FwdRegs<D, HPC, F8>::kOther>();
     if (warp == 8) {
     // ---------------------------------------------------------------- producer
     // The whole warp runs the loop (waits included); the elected lane issues.
@@ -701,7 +707,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
     }
     }
   } else {
-    regs_inc<kRegsSoftmax>();
+    regs_inc<FwdRegs<D, HPC, F8>::kSoftmax>();
     // ---------------------------------------------------------------- softmax
     const int s = warp >> 2;
     const int r = tid & 127;  // == 32 * (warp % 4) + lane: this thread's TMEM lane
