@@ -716,14 +716,20 @@ def run_gpu(args, rank, world, dist):
     value = whole_job_rate(world, leg.step_flops, ms)
     # The end-to-end leg follows the timed steps directly, so that both see the
     # GPU in the same state; the per-kernel breakdown (diagnostics) comes last.
+    # Clocks are sampled through the end-to-end leg as well: its steps can meet a
+    # GPU that has been power-capped for longer than the timed steps did.
+    e2e_sampler = ClockSampler(gpu_sel)
+    time.sleep(0.3)
     e2e_ms, h2d, d2h = leg.e2e(min(args.warmup, 3), args.e2e_steps, flush, stream)
+    e2e_clocks = e2e_sampler.stop()
     per_mask, kernels = leg.breakdown(args.breakdown_reps, flush, stream, pk)
     roof = leg.roofline(pk)
     e2e_t = max_over_ranks(statistics.mean(e2e_ms), dist, dev)
     e2e = {"value": whole_job_rate(world, leg.step_flops, e2e_t), "unit": UNIT, "ms_per_step": e2e_t,
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
            "copies": "pinned host buffers; dO and each mask's results move on a copy stream that "
-                     "overlaps compute; all copies inside the timed region"}
+                     "overlaps compute; all copies inside the timed region",
+           "ms_steps": [round(t, 3) for t in e2e_ms], "clocks": e2e_clocks}
     leg.check_status()
     select_roof = getattr(leg, "select_roof", None)
     launches = leg.launches_per_step * args.steps
