@@ -635,9 +635,10 @@ class Leg:
         h2d = sum(t.numel() * t.element_size() for t in host.values())
         d2h = sum(t.numel() * t.element_size() for o in outs for t in o.values())
         # Copies overlap compute the way a training loop would: dO goes up on a
-        # copy stream while the first forward runs, and each mask's results go down
-        # on it while the next mask computes.  Every byte still moves inside the
-        # timed region: e1 is recorded after the copy stream has been joined.
+        # copy stream while the first forward runs, each mask's O and LSE go down
+        # on it while its backward runs, and its gradients while the next mask
+        # computes.  Every byte still moves inside the timed region: e1 is
+        # recorded after the copy stream has been joined.
         copy_stream = torch.cuda.Stream(device=self.dev)
         ms = []
         for i in range(warmup + steps):
@@ -659,15 +660,19 @@ class Leg:
                     self.select(r, q_, k_)
                 lc.lcattn_mask_compile(self.shape, r["mask"], r["meta"])
                 self.fwd(r, q_, k_, v_)
+                copy_stream.wait_stream(stream)
+                with torch.cuda.stream(copy_stream):
+                    for n in ("o", "lse"):
+                        o[n].copy_(r[n], non_blocking=True)
                 if j == 0:
                     stream.wait_event(do_ready)
                 if not self.fwd_only:
                     lc.lcattn_bwd(q_, k_, v_, r["o"], do_, r["lse"], r["mask"], r["meta"],
                                   dq=r["dq"], dk=r["dk"], dv=r["dv"], workspace=self.ws)
-                copy_stream.wait_stream(stream)
-                with torch.cuda.stream(copy_stream):
-                    for n in o:
-                        o[n].copy_(r[n], non_blocking=True)
+                    copy_stream.wait_stream(stream)
+                    with torch.cuda.stream(copy_stream):
+                        for n in ("dq", "dk", "dv"):
+                            o[n].copy_(r[n], non_blocking=True)
             stream.wait_stream(copy_stream)
             e1.record(stream)
             torch.cuda.synchronize()
