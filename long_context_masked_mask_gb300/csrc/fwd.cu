@@ -71,15 +71,13 @@ template <int D, bool F8 = false> struct FwdGeom {
 constexpr int kItemQ = 4;           // depth of the work-item queue (producer -> other roles)
 constexpr int kHalfBytes = 16384;   // one 64-column TMA box of 128 rows
 constexpr int kThreads = 384;        // 3 warpgroups
-// Register split (launch: 384 threads x 168): softmax warpgroups 216 each and
-// producer/MMA warpgroup 72 for bf16 two-head items at head dim 128; 200 and
-// 104 for the other instances, whose producer/MMA loops spill at 72.  Same-box
-// A/B of 200 / 104 against 216 / 72: one-head items 3-4% faster, head dim 64
-// 1.3%, e4m3 0.5-1%; bf16 two-head items at head dim 128 1.4-1.9% slower.
+// Register split (launch: 384 threads x 168): softmax warpgroups 200 each,
+// producer/MMA warpgroup 104.  Same-box A/B against 216 / 72: one-head items
+// 3-4% faster, head dim 64 1.3%, e4m3 0.5-1%, and, with the MMA warp's slot
+// loop unrolled (which spilled at 72), bf16 two-head items 2.5-3.3%.
 template <int D, int HPC, bool F8> struct FwdRegs {
-  static constexpr bool kWide = D == 128 && HPC == 2 && !F8;
-  static constexpr int kSoftmax = kWide ? 216 : 200;
-  static constexpr int kOther = kWide ? 72 : 104;
+  static constexpr int kSoftmax = 200;
+  static constexpr int kOther = 104;
   static_assert(128 * (2 * kSoftmax + kOther) <= kThreads * 168, "register split");
 };
 
@@ -666,7 +664,7 @@ fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUte
           if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
           tc_fence_after();
           const uint64_t kb = sdesc_add(dk0, (tk % kStages) * kTileBytes);
-          #pragma unroll 1  // the MMA warp has 72 registers
+          #pragma unroll (D == 64 ? 1 : 2)  // rolled at head dim 64, whose MMA warp spills unrolled
           for (int s = 0; s < hpc; ++s) {
             if (T > 0 && !issue_pv(s, j == 0)) { ok = false; break; }
             if (j == 0) {
